@@ -1,0 +1,577 @@
+/*
+ * kv4_oracle.c — plain CPU oracle for the KV4-RL rollout decode hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark load it; the product path never does.
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math [-fopenmp] -shared -fPIC.
+ * Contraction is off so every float expression below rounds exactly as written;
+ * fused multiply-adds appear only where fmaf() is spelled out.
+ *
+ * Pages cited (title, then section):
+ *   [zh] "KV4-RL:用 INT4 KV 缓存量化为 RLVR 异步 Rollout 提速"
+ *   [ko] "INT4 KV 캐시로 비동기 RLVR 롤아웃을 1.8배 가속한다"
+ *
+ * What each step follows:
+ *   Hadamard rotation of post-RoPE keys and of the query, QH(HK)^T = QK^T
+ *       [zh] 前置知识 › 分组仿射 KV 量化; 核心方法; 方法步骤详情 step 2.
+ *   Group-affine quantizer x^ = Δc + m, one group per 128-dim token-head vector,
+ *   FP16 Δ and m computed online, 4 bits (main cache) or 8 bits (side cache)
+ *       [zh] 分组仿射 KV 量化; 方法步骤详情 steps 2-3; [ko] 전제와 한계.
+ *   INT8 query; integer QK with the scale and offset applied after the dot
+ *       [zh] 分组仿射 KV 量化 (scale/offset deferred past the dot product);
+ *       [ko] 전제와 한계; [zh] 方法步骤详情 step 4.
+ *   Integer PV over the INT4 region; protected path over sink + recent with
+ *   INT8 keys and BF16-dequantized values, FP32 accumulation
+ *       [ko] 전제와 한계; [zh] 核心方法, 方法步骤详情 steps 3-4.
+ *   Disjoint regions, each giving a local output and log-normaliser, merged by
+ *   an exact softmax (log-sum-exp) merge
+ *       [ko] 전제와 한계; [zh] 核心方法 (third difference).
+ *
+ * Readings where the pages leave a step open (each is listed in the design doc):
+ *   R1 V is not rotated; only K (post-RoPE) and q are.
+ *   R2 Δ and m use directed rounding: m = fp16_down(min x),
+ *      Δ = fp16_up(up((max x − m) / n)), so m ≤ min x and m + nΔ ≥ max x.
+ *      Codes are c = clamp(rint((x − m) · fl(1/Δ)), 0, n); Δ = 0 gives c = 0.
+ *   R3 The query is symmetric INT8 per q head: s_q = max|q'|/127,
+ *      q8 = rint(q' · fl(127/max|q'|)).
+ *   R4 Regions: protected = [0, min(s,L)) ∪ [max(s, L−w), L); INT4 = [s, L−w).
+ *   R5 Integer PV: per page ∩ INT4 region, p' = 2^(σ − M_page) with the exp2
+ *      below, w = p'·Δ^V, ŵ = min(rint(w · fl(255/max w)), 255) in 0..255,
+ *      acc_j = Σ ŵ c^V_j, page output s_w·acc_j + Σ p'·m^V with s_w = max w / 255.
+ *      A page whose max w is not above 2^-64 keeps only its offsets (ŵ = 0).
+ *   R6 Scores are log2-domain: σ = fl(fl(u · s_q) · C), u = fmaf(Δ, dot, fl(m · Σq8)),
+ *      C = fl(sm_scale · log2 e).
+ * Everything after the integer decisions (page outputs, region merges,
+ * the protected path, the final normalisation) is carried in double here.
+ */
+#include "kv4_oracle.h"
+
+#include <float.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                            */
+/* ------------------------------------------------------------------------ */
+
+double orc_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+/* Encode a double that is exactly an fp16 value (or ±inf). */
+static uint16_t f16_encode_exact(double v, int neg)
+{
+    uint16_t s = neg ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isinf(a)) return s | 0x7c00;
+    if (a == 0.0) return s;
+    if (a < ldexp(1.0, -14))                      /* subnormal: a = f * 2^-24 */
+        return s | (uint16_t)(a * ldexp(1.0, 24));
+    int e;
+    double m = frexp(a, &e);                      /* a = m * 2^e, m in [0.5, 1) */
+    int E = e - 1;                                /* a = (2m) * 2^E */
+    int frac = (int)(m * 2048.0) - 1024;          /* exact: a has ≤ 11 significant bits */
+    return s | (uint16_t)(((E + 15) << 10) | frac);
+}
+
+/*
+ * float -> fp16 in round-to-nearest-even, toward −inf or toward +inf.
+ * Written from the definition: pick the fp16 quantum of the binade, scale the
+ * value onto an integer grid (exact, the quantum is a power of two), round the
+ * grid coordinate with the requested rule, then scale back and handle overflow.
+ */
+uint16_t orc_f32_to_f16(float xf, int mode)
+{
+    double x = (double)xf;
+    int neg = signbit(xf) != 0;
+    if (isnan(x)) return (uint16_t)((neg ? 0x8000 : 0) | 0x7e00);
+    if (isinf(x)) return (uint16_t)((neg ? 0x8000 : 0) | 0x7c00);
+    if (x == 0.0) return (uint16_t)(neg ? 0x8000 : 0);
+    int e;
+    frexp(fabs(x), &e);
+    int E = e - 1;                    /* 2^E ≤ |x| < 2^(E+1) */
+    if (E < -14) E = -14;             /* below the normal range the quantum is 2^-24 */
+    double q = ldexp(1.0, E - 10);
+    double t = x / q;                 /* exact */
+    double r;
+    if (mode == ORC_RD)
+        r = floor(t);
+    else if (mode == ORC_RU)
+        r = ceil(t);
+    else
+        r = nearbyint(t);             /* default rounding mode: nearest, ties to even */
+    double v = r * q;
+    if (v > 65504.0) return (mode == ORC_RD) ? 0x7bff : 0x7c00;
+    if (v < -65504.0) return (mode == ORC_RU) ? 0xfbff : 0xfc00;
+    return f16_encode_exact(v, neg);
+}
+
+float orc_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+uint16_t orc_f32_to_bf16_rn(float x)
+{
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u)          /* NaN: keep sign, force quiet */
+        return (uint16_t)((u >> 16) | 0x40);
+    /* round the low 16 bits away, ties to the even upper half */
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * exp2 for the PV weights. Written from the textbook range reduction
+ * 2^x = 2^n · 2^f with n = rint(x), f = x − n in [−1/2, 1/2], and the Taylor
+ * series 2^f = Σ_k (f ln 2)^k / k!, truncated after k = 7 and evaluated by
+ * Horner's rule with fused multiply-adds. Coefficients are (ln 2)^k / k!
+ * computed in double and rounded once to float. Defined for x ≤ 0 (the only
+ * use); x < −125 returns 0 so every nonzero result is a normal float.
+ */
+static float exp2_coef[8];
+
+__attribute__((constructor)) static void exp2_init(void)
+{
+    double fact = 1.0, lnp = 1.0;
+    for (int k = 0; k < 8; k++) {
+        if (k > 0) { fact *= (double)k; lnp *= 0.69314718055994530942; }
+        exp2_coef[k] = (float)(lnp / fact);
+    }
+}
+
+float orc_exp2f(float x)
+{
+    if (!(x >= -125.0f)) return 0.0f;
+    float n = rintf(x);
+    float f = x - n;                                 /* exact */
+    float p = exp2_coef[7];
+    for (int k = 6; k >= 0; k--) p = fmaf(p, f, exp2_coef[k]);
+    return ldexpf(p, (int)n);
+}
+
+/* Directed float subtraction a − b rounded toward +inf: the round-to-nearest
+   result plus the exact error term (Knuth's TwoSum) decide the direction. */
+static float fsub_up(float a, float b)
+{
+    float nb = -b;
+    float s = a + nb;
+    float bb = s - a;
+    float err = (a - (s - bb)) + (nb - bb);
+    return (err > 0.0f) ? nextafterf(s, INFINITY) : s;
+}
+
+/* Directed float division a / n rounded toward +inf, for a ≥ 0 and n > 0:
+   the remainder a − q·n of the nearest quotient q is exact in one fmaf. */
+static float fdiv_up(float a, float n)
+{
+    float q = a / n;
+    float rem = fmaf(-q, n, a);
+    return (rem > 0.0f) ? nextafterf(q, INFINITY) : q;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* 128-point fast Walsh–Hadamard transform, normalised to H/√128 (orthonormal,
+   symmetric). Butterfly stages h = 1, 2, …, 64 in that order, then one scale.
+   [zh] 分组仿射 KV 量化; 方法步骤详情 step 2 (same rotation for K and q). */
+void orc_fwht128(const float *in, float *out)
+{
+    float x[ORC_D];
+    memcpy(x, in, sizeof x);
+    for (int h = 1; h < ORC_D; h <<= 1)
+        for (int i = 0; i < ORC_D; i++)
+            if ((i & h) == 0) {
+                float a = x[i], b = x[i + h];
+                x[i] = a + b;
+                x[i + h] = a - b;
+            }
+    const float scale = (float)(1.0 / sqrt(128.0));
+    for (int i = 0; i < ORC_D; i++) out[i] = x[i] * scale;
+}
+
+/* Group-affine quantizer x^ = Δc + m over one group of n values, levels = 2^b − 1.
+   [zh] 分组仿射 KV 量化; 方法步骤详情 step 2 (FP16 Δ and m computed online).
+   Rounding directions: reading R2 in the file header. */
+void orc_quant_affine(const float *x, int n, int levels,
+                      uint8_t *code, uint16_t *delta_h, uint16_t *min_h)
+{
+    float lo = x[0], hi = x[0];
+    for (int i = 1; i < n; i++) {
+        if (x[i] < lo) lo = x[i];
+        if (x[i] > hi) hi = x[i];
+    }
+    uint16_t mh = orc_f32_to_f16(lo, ORC_RD);
+    float m = (float)orc_f16_to_f64(mh);
+    float r = fsub_up(hi, m);
+    float d = fdiv_up(r, (float)levels);
+    uint16_t dh = orc_f32_to_f16(d, ORC_RU);
+    float delta = (float)orc_f16_to_f64(dh);
+    *delta_h = dh;
+    *min_h = mh;
+    if (delta == 0.0f) {
+        memset(code, 0, (size_t)n);
+        return;
+    }
+    float inv = 1.0f / delta;
+    for (int i = 0; i < n; i++) {
+        float t = (x[i] - m) * inv;
+        float c = rintf(t);
+        if (c < 0.0f) c = 0.0f;
+        if (c > (float)levels) c = (float)levels;
+        code[i] = (uint8_t)c;
+    }
+}
+
+/* Symmetric INT8 query, one scale per q head (reading R3).
+   [ko] 전제와 한계 (the rotated query is quantized to INT8 and serves both paths). */
+void orc_quant_query(const float *q_rot, int8_t *q8, float *q_scale, int32_t *q_sum)
+{
+    float a = 0.0f;
+    for (int i = 0; i < ORC_D; i++) {
+        float v = fabsf(q_rot[i]);
+        if (v > a) a = v;
+    }
+    int32_t sum = 0;
+    if (a == 0.0f) {
+        memset(q8, 0, ORC_D);
+        *q_scale = 0.0f;
+        *q_sum = 0;
+        return;
+    }
+    float inv = 127.0f / a;
+    for (int i = 0; i < ORC_D; i++) {
+        int v = (int)rintf(q_rot[i] * inv);
+        q8[i] = (int8_t)v;
+        sum += v;
+    }
+    *q_scale = a / 127.0f;
+    *q_sum = sum;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache state                                                               */
+/* ------------------------------------------------------------------------ */
+
+static size_t idx_main(const orc_cache *c, int slot, int pos, int head)
+{
+    return ((size_t)slot * c->max_len + pos) * c->num_heads + head;
+}
+
+static size_t idx_side(const orc_cache *c, int slot, int sidx, int head)
+{
+    return ((size_t)slot * (c->sink + c->window) + sidx) * c->num_heads + head;
+}
+
+static void load_bf16_row(const uint16_t *src, float *dst)
+{
+    for (int i = 0; i < ORC_D; i++) dst[i] = orc_bf16_to_f32(src[i]);
+}
+
+/* Write one token-head into both caches. */
+static void append_one(orc_cache *c, int slot, int pos, int head,
+                       const float *k_rot, const float *v)
+{
+    size_t mi = idx_main(c, slot, pos, head);
+    orc_quant_affine(k_rot, ORC_D, 15, c->k4_code + mi * ORC_D, c->k4_delta + mi, c->k4_min + mi);
+    orc_quant_affine(v, ORC_D, 15, c->v4_code + mi * ORC_D, c->v4_delta + mi, c->v4_min + mi);
+
+    /* Side buffer: an INT8 copy of a sink position and of the position in the
+       recent ring. [ko] 전제와 한계; [zh] 方法步骤详情 step 3. */
+    int s = c->sink, w = c->window;
+    int targets[2], nt = 0;
+    if (pos < s) targets[nt++] = pos;
+    if (w > 0) targets[nt++] = s + (pos % w);
+    for (int k = 0; k < nt; k++) {
+        size_t si = idx_side(c, slot, targets[k], head);
+        orc_quant_affine(k_rot, ORC_D, 255, c->k8_code + si * ORC_D, c->k8_delta + si, c->k8_min + si);
+        orc_quant_affine(v, ORC_D, 255, c->v8_code + si * ORC_D, c->v8_delta + si, c->v8_min + si);
+    }
+}
+
+/* Append T tokens at positions start … start+T−1, one token at a time in order
+   (sequential semantics: the ring ends up holding the last w positions). */
+int orc_append(orc_cache *c, int slot, int start, int T,
+               const uint16_t *k_bf16, const uint16_t *v_bf16)
+{
+    if (slot < 0 || slot >= c->num_slots || start < 0 || T < 0 || start + T > c->max_len)
+        return -1;
+    float kx[ORC_D], kr[ORC_D], vx[ORC_D];
+    for (int t = 0; t < T; t++) {
+        for (int h = 0; h < c->num_heads; h++) {
+            size_t off = ((size_t)t * c->num_heads + h) * ORC_D;
+            load_bf16_row(k_bf16 + off, kx);
+            load_bf16_row(v_bf16 + off, vx);
+            orc_fwht128(kx, kr);
+            append_one(c, slot, start + t, h, kr, vx);
+        }
+        c->length[slot] = start + t + 1;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention for one sequence                                         */
+/* ------------------------------------------------------------------------ */
+
+static float log2e_scale(float sm_scale)
+{
+    return (float)((double)sm_scale * 1.4426950408889634074);
+}
+
+/* σ from an integer dot, the code group's FP16 (Δ, m) and the query's (s_q, Σq8).
+   [zh] 分组仿射 KV 量化: the scale and offset are applied after the dot product. */
+static float score_from_dot(int32_t dot, uint16_t dh, uint16_t mh,
+                            float q_scale, int32_t q_sum, float C)
+{
+    float delta = (float)orc_f16_to_f64(dh);
+    float m = (float)orc_f16_to_f64(mh);
+    float u = fmaf(delta, (float)dot, m * (float)q_sum);
+    return (u * q_scale) * C;
+}
+
+static int32_t dot_s8_u8(const int8_t *a, const uint8_t *b)
+{
+    int32_t s = 0;
+    for (int i = 0; i < ORC_D; i++) s += (int32_t)a[i] * (int32_t)b[i];
+    return s;
+}
+
+/* One q head against one sequence. Returns output (normalised) and lse (natural log). */
+static void decode_head(const orc_cache *c, int slot, int L, int head,
+                        const int8_t *q8, float q_scale, int32_t q_sum, float C,
+                        int pv_mode, double *out, double *lse,
+                        int32_t *dbg_qk, float *dbg_sigma, uint8_t *dbg_w)
+{
+    const int s = c->sink, w = c->window, P = 16;
+    /* Regions, reading R4. */
+    int r4_lo = s, r4_hi = L - w;
+    if (r4_hi < r4_lo) r4_hi = r4_lo;                 /* empty */
+    int sink_hi = (s < L) ? s : L;
+    int ring_lo = (L - w > s) ? (L - w) : s;
+
+    /* ---- INT4 region: integer QK, page-local integer PV (reading R5) ---- */
+    double M4 = -INFINITY, l4 = 0.0;
+    double o4[ORC_D];
+    for (int j = 0; j < ORC_D; j++) o4[j] = 0.0;
+    if (r4_hi > r4_lo) {
+        int p_first = r4_lo / P, p_last = (r4_hi - 1) / P;
+        float sig_buf[16];
+        for (int pg = p_first; pg <= p_last; pg++) {
+            int t0 = pg * P, t1 = t0 + P;
+            if (t0 < r4_lo) t0 = r4_lo;
+            if (t1 > r4_hi) t1 = r4_hi;
+            int n = t1 - t0;
+            float Mp = -INFINITY;
+            for (int i = 0; i < n; i++) {
+                int t = t0 + i;
+                size_t mi = idx_main(c, slot, t, head);
+                int32_t dot = dot_s8_u8(q8, c->k4_code + mi * ORC_D);
+                float sg = score_from_dot(dot, c->k4_delta[mi], c->k4_min[mi], q_scale, q_sum, C);
+                sig_buf[i] = sg;
+                if (dbg_qk) dbg_qk[t] = dot;
+                if (dbg_sigma) dbg_sigma[t] = sg;
+                if (sg > Mp) Mp = sg;
+            }
+            float pp[16], wv[16];
+            float wmax = 0.0f;
+            double lp = 0.0, bias = 0.0;
+            for (int i = 0; i < n; i++) {
+                size_t mi = idx_main(c, slot, t0 + i, head);
+                pp[i] = orc_exp2f(sig_buf[i] - Mp);
+                float dv = (float)orc_f16_to_f64(c->v4_delta[mi]);
+                float mv = (float)orc_f16_to_f64(c->v4_min[mi]);
+                wv[i] = pp[i] * dv;
+                if (wv[i] > wmax) wmax = wv[i];
+                lp += (double)pp[i];
+                bias += (double)pp[i] * (double)mv;
+            }
+            double op[ORC_D];
+            if (pv_mode == ORC_PV_FLOAT) {
+                for (int j = 0; j < ORC_D; j++) op[j] = 0.0;
+                for (int i = 0; i < n; i++) {
+                    size_t mi = idx_main(c, slot, t0 + i, head);
+                    double dv = orc_f16_to_f64(c->v4_delta[mi]);
+                    double mv = orc_f16_to_f64(c->v4_min[mi]);
+                    const uint8_t *vc = c->v4_code + mi * ORC_D;
+                    for (int j = 0; j < ORC_D; j++) op[j] += (double)pp[i] * (dv * vc[j] + mv);
+                }
+            } else {
+                /* pages whose largest weight is below 2^-64 contribute their
+                   offsets only: their ŵ are 0 and s_w is 0 */
+                uint8_t wh[16];
+                int quantize = wmax > 0x1p-64f;
+                float iw = quantize ? 255.0f / wmax : 0.0f;
+                for (int i = 0; i < n; i++) {
+                    float r = rintf(wv[i] * iw);
+                    if (r > 255.0f) r = 255.0f;
+                    wh[i] = (uint8_t)r;
+                    if (dbg_w) dbg_w[t0 + i] = wh[i];
+                }
+                double sw = quantize ? (double)wmax / 255.0 : 0.0;
+                for (int j = 0; j < ORC_D; j++) {
+                    int32_t acc = 0;
+                    for (int i = 0; i < n; i++) {
+                        size_t mi = idx_main(c, slot, t0 + i, head);
+                        acc += (int32_t)wh[i] * (int32_t)c->v4_code[mi * ORC_D + j];
+                    }
+                    op[j] = sw * (double)acc + bias;
+                }
+            }
+            /* fold the page into the region total, relative to the running max */
+            double Mn = (Mp > M4) ? Mp : M4;
+            double a = (M4 == -INFINITY) ? 0.0 : exp2(M4 - Mn);
+            double b = exp2(Mp - Mn);
+            for (int j = 0; j < ORC_D; j++) o4[j] = o4[j] * a + op[j] * b;
+            l4 = l4 * a + lp * b;
+            M4 = Mn;
+        }
+    }
+
+    /* ---- protected region: INT8 side keys, BF16 values, plain sums ---- */
+    double Mp_ = -INFINITY, lp_ = 0.0;
+    double opr[ORC_D];
+    for (int j = 0; j < ORC_D; j++) opr[j] = 0.0;
+    int npos = 0;
+    int pos_list[512];
+    for (int t = 0; t < sink_hi; t++) pos_list[npos++] = t;
+    for (int t = ring_lo; t < L; t++) pos_list[npos++] = t;
+    float sig_p[512];
+    for (int k = 0; k < npos; k++) {
+        int t = pos_list[k];
+        int sidx = (t < s) ? t : s + (t % w);
+        size_t si = idx_side(c, slot, sidx, head);
+        int32_t dot = dot_s8_u8(q8, c->k8_code + si * ORC_D);
+        float sg = score_from_dot(dot, c->k8_delta[si], c->k8_min[si], q_scale, q_sum, C);
+        sig_p[k] = sg;
+        if (dbg_qk) dbg_qk[t] = dot;
+        if (dbg_sigma) dbg_sigma[t] = sg;
+        if (sg > Mp_) Mp_ = sg;
+    }
+    for (int k = 0; k < npos; k++) {
+        int t = pos_list[k];
+        int sidx = (t < s) ? t : s + (t % w);
+        size_t si = idx_side(c, slot, sidx, head);
+        double p = exp2((double)sig_p[k] - Mp_);
+        float dv = (float)orc_f16_to_f64(c->v8_delta[si]);
+        float mv = (float)orc_f16_to_f64(c->v8_min[si]);
+        const uint8_t *vc = c->v8_code + si * ORC_D;
+        for (int j = 0; j < ORC_D; j++) {
+            float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
+            opr[j] += p * (double)v;
+        }
+        lp_ += p;
+    }
+
+    /* ---- exact log-sum-exp merge of the two regions ---- */
+    double Ms = (M4 > Mp_) ? M4 : Mp_;
+    if (Ms == -INFINITY) {                          /* L == 0 */
+        for (int j = 0; j < ORC_D; j++) out[j] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double a4 = (M4 == -INFINITY) ? 0.0 : exp2(M4 - Ms);
+    double ap = (Mp_ == -INFINITY) ? 0.0 : exp2(Mp_ - Ms);
+    double den = a4 * l4 + ap * lp_;
+    for (int j = 0; j < ORC_D; j++) out[j] = (a4 * o4[j] + ap * opr[j]) / den;
+    *lse = (Ms + log2(den)) * 0.69314718055994530942;
+}
+
+int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf16,
+               float sm_scale, int pv_mode, double *out, double *lse, orc_debug *dbg)
+{
+    if (slot < 0 || slot >= c->num_slots || L < 0 || L > c->max_len || G <= 0)
+        return -1;
+    if (c->sink + c->window > 256) return -1;
+    const float C = log2e_scale(sm_scale);
+    const int HG = c->num_heads * G;
+    for (int hq = 0; hq < HG; hq++) {
+        float qx[ORC_D], qr[ORC_D];
+        int8_t q8[ORC_D];
+        float q_scale;
+        int32_t q_sum;
+        load_bf16_row(q_bf16 + (size_t)hq * ORC_D, qx);
+        orc_fwht128(qx, qr);
+        orc_quant_query(qr, q8, &q_scale, &q_sum);
+        if (dbg) {
+            if (dbg->q8) memcpy(dbg->q8 + (size_t)hq * ORC_D, q8, ORC_D);
+            if (dbg->q_scale) dbg->q_scale[hq] = q_scale;
+            if (dbg->q_sum) dbg->q_sum[hq] = q_sum;
+        }
+        decode_head(c, slot, L, hq / G, q8, q_scale, q_sum, C, pv_mode,
+                    out + (size_t)hq * ORC_D, lse + hq,
+                    dbg && dbg->qk ? dbg->qk + (size_t)hq * L : NULL,
+                    dbg && dbg->sigma ? dbg->sigma + (size_t)hq * L : NULL,
+                    dbg && dbg->w_hat ? dbg->w_hat + (size_t)hq * L : NULL);
+    }
+    return 0;
+}
+
+/* A batch of sequences, spread over host threads by sequence (CPU baseline). */
+int orc_decode_batch(const orc_cache *c, int B, const int32_t *slots, const int32_t *lens,
+                     int G, const uint16_t *q_bf16, float sm_scale, int pv_mode,
+                     double *out, double *lse, int num_threads)
+{
+    const int HG = c->num_heads * G;
+    int bad = 0;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#endif
+    for (int b = 0; b < B; b++) {
+        int rc = orc_decode(c, slots[b], lens[b], G, q_bf16 + (size_t)b * HG * ORC_D, sm_scale,
+                            pv_mode, out + (size_t)b * HG * ORC_D, lse + (size_t)b * HG, NULL);
+        bad |= (rc != 0);
+    }
+    (void)num_threads;
+    return bad ? -1 : 0;
+}
+
+/* Array forms of the scalar conversions, for the tests' bulk checks. */
+void orc_f32_to_f16_array(const float *x, uint16_t *out, int64_t n, int mode)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = orc_f32_to_f16(x[i], mode);
+}
+
+void orc_f32_to_bf16_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = orc_f32_to_bf16_rn(x[i]);
+}
+
+void orc_exp2f_array(const float *x, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = orc_exp2f(x[i]);
+}
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

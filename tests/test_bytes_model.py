@@ -1,0 +1,39 @@
+"""The byte model used for the roofline, pinned to the numbers the pages print."""
+import json
+import os
+
+from int8_hybrid_paged_gb300 import bytes_model as bm
+
+G = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_constants.json")))
+
+
+def test_dense_kv_bytes_match_the_printed_example():
+    e = G["kv_bytes_per_token_fp16"]
+    assert bm.kv_cache_bytes(e["layers"], e["kv_heads"], e["head_dim"], e["bytes_per_elem"],
+                             1, 1) == e["value"]
+    r = G["kv_bytes_per_request_32k_fp16"]
+    assert bm.kv_cache_bytes(32, 8, 128, 2, 1, r["seq"]) == r["value"]
+    m = G["kv_bytes_16_requests_32k_fp16"]
+    assert bm.kv_cache_bytes(32, 8, 128, 2, m["batch"], m["seq"]) == m["value"]
+
+
+def test_int4_token_head_bytes_follow_the_bit_budget():
+    bits = G["bits_per_element"]["value"]
+    # K and V, 128 elements each, at 4.25 bits
+    assert bm.INT4_TOKEN_HEAD_BYTES == 2 * 128 * bits / 8 == 136
+    assert bm.BF16_TOKEN_HEAD_BYTES == bm.kv_cache_bytes(1, 1, 128, 2, 1, 1) == 512
+    # INT8 side entry: 8-bit codes + the same FP16 pair
+    assert bm.SIDE_POSITION_HEAD_BYTES == 2 * (128 + 4) == 264
+
+
+def test_regions_and_decode_bytes():
+    s, w = G["sink_positions"]["value"], G["recent_positions"]["value"]
+    assert s + w == G["protected_budget"]["value"]
+    assert bm.regions(100, s, w) == (0, 100)
+    assert bm.regions(144, s, w) == (0, 144)
+    assert bm.regions(1000, s, w) == (856, 144)
+    # one sequence of 1000 positions, one KV head, one q head
+    n4, npr = 856, 144
+    pages = (1000 - 128 - 1) // 16 - 16 // 16 + 1
+    expect = n4 * 136 + npr * 264 + 4 * pages + 8 + 128 * 6
+    assert bm.decode_call_bytes([1000], 1, 1, s, w) == expect
