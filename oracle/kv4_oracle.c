@@ -31,7 +31,7 @@
  *
  * Readings where the pages leave a step open (each is listed in the design doc):
  *   R1 V is not rotated; only K (post-RoPE) and q are.
- *   R2 Δ and m use directed rounding: m = fp16_down(min x),
+ *   R2 Δ and m use directed rounding: m = fp16_down(min x) (a zero minimum as +0),
  *      Δ = fp16_up(up((max x − m) / n)), so m ≤ min x and m + nΔ ≥ max x.
  *      Codes are c = clamp(rint((x − m) · fl(1/Δ)), 0, n); Δ = 0 gives c = 0.
  *   R3 The query is symmetric INT8 per q head: s_q = max|q'|/127,
@@ -225,6 +225,7 @@ void orc_quant_affine(const float *x, int n, int levels,
         if (x[i] < lo) lo = x[i];
         if (x[i] > hi) hi = x[i];
     }
+    lo = lo + 0.0f;                       /* a zero minimum carries no sign: −0 becomes +0 */
     uint16_t mh = orc_f32_to_f16(lo, ORC_RD);
     float m = (float)orc_f16_to_f64(mh);
     float r = fsub_up(hi, m);
