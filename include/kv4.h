@@ -1,0 +1,195 @@
+/*
+ * kv4.h — C ABI of libkv4: the KV4-RL rollout decode hot path on GB300 (sm_103a).
+ *
+ * A paged INT4 KV cache holds every position; a fixed-size INT8 side buffer
+ * holds s sink positions and the w most recent positions of each sequence.
+ * Decode attention reads the two regions disjointly and merges them exactly.
+ *
+ * Pages cited (title, then section):
+ *   [zh] "KV4-RL:用 INT4 KV 缓存量化为 RLVR 异步 Rollout 提速"
+ *        (paper.rainbus.top/paper/2610.14448)
+ *   [ko] "INT4 KV 캐시로 비동기 RLVR 롤아웃을 1.8배 가속한다" (onedev.kr/papers/984)
+ *
+ * Conventions for every call
+ *   - Pointers named *_dev are device pointers; the caller owns them. The cache
+ *     owns its pools and its decode workspace.
+ *   - Calls are asynchronous on the caller's CUDA stream (`stream`, a
+ *     cudaStream_t passed as void*; NULL = legacy default stream). Host-side
+ *     validation happens before anything is enqueued; a call that returns an
+ *     error has enqueued nothing.
+ *   - Index errors that only the device can see (a slot, page or length out of
+ *     range inside a device array) never fault: the kernel skips the access and
+ *     records the first such error in a device error word, read with
+ *     kv4_get_device_error(). No call traps, aborts or throws across the ABI.
+ *   - head_dim is 128 and page_size is 16; other values return KV4_ERR_UNSUPPORTED.
+ */
+#ifndef KV4_H
+#define KV4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct kv4_cache kv4_cache;
+
+typedef enum {
+    KV4_OK = 0,
+    KV4_ERR_INVALID_ARG = -1,   /* null pointer, negative size, inconsistent sizes */
+    KV4_ERR_UNSUPPORTED = -2,   /* head_dim != 128, page_size != 16, s + w > 256, group size */
+    KV4_ERR_OUT_OF_MEMORY = -3, /* a pool or workspace allocation failed at create */
+    KV4_ERR_CUDA = -4,          /* a CUDA runtime call failed; the cache stays usable if it can */
+    KV4_ERR_OUT_OF_RANGE = -5,  /* batch, q heads or tokens above the cache's configured limits */
+    KV4_ERR_DEVICE_FAULT = -6   /* reported by kv4_get_device_error: see kv4_device_error */
+} kv4_status;
+
+/* Codes stored in the device error word (first error wins; 0 = none). */
+typedef enum {
+    KV4_DEVERR_NONE = 0,
+    KV4_DEVERR_BAD_SLOT = 1,       /* slot id outside [0, max_slots) */
+    KV4_DEVERR_BAD_PAGE = 2,       /* block-table entry outside [0, num_pages) */
+    KV4_DEVERR_BAD_POSITION = 3,   /* position beyond block_table_stride pages, or negative */
+    KV4_DEVERR_LEN_MISMATCH = 4,   /* decode context_len differs from the slot's appended length */
+    KV4_DEVERR_WAIT_TIMEOUT = 5,   /* a shared-memory staging wait gave up (no data arrived) */
+    KV4_DEVERR_BAD_TOKENS = 6      /* cu_tokens not non-decreasing or not ending at total_tokens */
+} kv4_device_error;
+
+typedef struct {
+    int32_t num_kv_heads;    /* H_kv >= 1 */
+    int32_t head_dim;        /* must be 128 (one quantization group per token-head, [zh] 分组仿射 KV 量化) */
+    int32_t page_size;       /* must be 16 */
+    int32_t sink;            /* s >= 0: INT8-protected sink positions (16 in [zh] 核心方法) */
+    int32_t window;          /* w >= 0: INT8-protected recent positions (128 in [zh] 核心方法); s + w <= 256 */
+    int64_t num_pages;       /* physical pages in the INT4 pool (each holds 16 positions of every KV head) */
+    int32_t max_slots;       /* sequences that own a side buffer (slot ids are 0 .. max_slots-1) */
+    int32_t max_batch;       /* largest batch of one decode call */
+    int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4, 8}) */
+    int32_t max_work_items;  /* split-K partials kept by the decode workspace; 0 = a default that
+                                fits max_batch (at least 3 * max_batch * H_kv) */
+} kv4_cache_config;
+
+/*
+ * Memory layout (all blocks 16-byte aligned; pools zeroed at create).
+ *
+ * INT4 page pool: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES = 2176 bytes;
+ * the block of (page p, KV head h) starts at (p * H_kv + h) * 2176. Inside it,
+ * for the 16 token slots t of the page:
+ *   [0,    1024)  K codes, row t = 64 bytes; byte j = c[2j] | c[2j+1] << 4 (rotated K)
+ *   [1024, 2048)  V codes, 64 dim-pair rows of 16 bytes; byte (j, t) = c_t[2j] | c_t[2j+1] << 4
+ *   [2048, 2112)  K metadata, t -> {fp16 delta, fp16 min} (4 bytes)
+ *   [2112, 2176)  V metadata, same form
+ * Side pool: max_slots * H_kv blocks of side_block_bytes = align16((s+w) * 264);
+ * block (slot, h) at (slot * H_kv + h) * side_block_bytes. With S = s + w and
+ * side index i (i = p for a sink position p < s, i = s + p mod w for a ring position):
+ *   [0,        S*128)  INT8-grid K codes (u8, rotated K), row i = 128 bytes
+ *   [S*128,    S*256)  INT8-grid V codes (u8), row i
+ *   [S*256,    S*260)  K metadata {fp16 delta, fp16 min} per i
+ *   [S*260,    S*264)  V metadata per i
+ * Lengths: int32 per slot, the slot's length after its last append.
+ */
+#define KV4_HEAD_DIM 128
+#define KV4_PAGE_SIZE 16
+#define KV4_PAGE_BLOCK_BYTES 2176
+
+typedef struct {
+    void   *page_pool_dev;   size_t page_pool_bytes;
+    void   *side_pool_dev;   size_t side_pool_bytes;   size_t side_block_bytes;
+    int32_t *seq_len_dev;    /* [max_slots] */
+    int32_t num_sms;         /* SMs of the device the cache lives on */
+    int32_t decode_grid;     /* persistent CTAs launched by decode */
+    int32_t device;
+} kv4_cache_info;
+
+/* Allocate the pools and the decode workspace on the current device (cudaMalloc),
+ * zero them, size the persistent decode grid. *out receives the handle.
+ * Errors: KV4_ERR_INVALID_ARG, KV4_ERR_UNSUPPORTED, KV4_ERR_OUT_OF_MEMORY, KV4_ERR_CUDA. */
+kv4_status kv4_cache_create(const kv4_cache_config *config, kv4_cache **out);
+
+/* Free everything the cache owns (synchronises the device first). NULL is a no-op. */
+kv4_status kv4_cache_free(kv4_cache *cache);
+
+/* Pointers and sizes of the cache's pools (for inspection and tests). */
+kv4_status kv4_cache_get_info(const kv4_cache *cache, kv4_cache_info *info);
+
+/*
+ * kv4_append — quantize and store new tokens of n_seqs sequences.
+ * [zh] 方法步骤详情 steps 2-3, 前置知识 › 分组仿射 KV 量化; [ko] 전제와 한계.
+ * For each token-head: rotate K (post-RoPE, supplied by the caller) with the
+ * orthonormal 128-point Hadamard transform H/sqrt(128); quantize rotated K and
+ * (unrotated) V to 4-bit affine codes with fp16 delta = up-rounded step and
+ * fp16 min = down-rounded minimum; write them to page block_table[i][pos/16],
+ * slot pos%16. A position p < s also gets an 8-bit copy in sink row p; a
+ * position p >= L_new - w (L_new = start_pos[i] + its token count) gets an
+ * 8-bit copy in ring row s + p mod w. The slot's length becomes L_new.
+ *   k_bf16_dev, v_bf16_dev : [total_tokens][H_kv][128] bf16, tokens of sequence i
+ *                            at rows cu_tokens[i] .. cu_tokens[i+1]-1
+ *   cu_tokens_dev          : [n_seqs+1] int32, non-decreasing, cu[0] = 0, cu[n] = total_tokens
+ *   slot_ids_dev           : [n_seqs] int32 side-buffer slot of each sequence (distinct)
+ *   start_pos_dev          : [n_seqs] int32 position of each sequence's first new token
+ *   block_table_dev        : [n_seqs][block_table_stride] int32 physical page per 16 positions
+ * Sequences must not repeat a slot within one call. Appends of one slot must be
+ * issued in position order on one stream (a later call sees earlier writes).
+ */
+kv4_status kv4_append(kv4_cache *cache, const void *k_bf16_dev, const void *v_bf16_dev,
+                      const int32_t *cu_tokens_dev, const int32_t *slot_ids_dev,
+                      const int32_t *start_pos_dev, const int32_t *block_table_dev,
+                      int block_table_stride, int n_seqs, int total_tokens, void *stream);
+
+/*
+ * kv4_decode_attention — one decode step of attention for a batch of sequences.
+ * [ko] 전제와 한계; [zh] 核心方法, 方法步骤详情 step 4.
+ * Per q head (q head hq uses KV head hq / G, G = num_q_heads / H_kv):
+ *   q' = Hadamard(q); q8 = rint(q' * 127/max|q'|) with s_q = max|q'|/127.
+ *   INT4 region [s, L-w): integer dot q8 . c, score scale/offset applied after
+ *     the dot; per page, u8 weights w^ = rint(255 * p'Delta_V / max) from
+ *     p' = 2^(sigma - page max), integer PV sum w^ * c_V, rescaled in FP32.
+ *   Protected region [0, min(s,L)) U [max(s, L-w), L): the same q8 against INT8
+ *     side keys; side values dequantized to bf16; PV accumulated in FP32.
+ *   The regions' outputs and log-normalizers are merged exactly (log-sum-exp),
+ *   split-K partials over pages likewise.
+ *   q_bf16_dev       : [batch][num_q_heads][128] bf16 (post-RoPE, unrotated)
+ *   slot_ids_dev     : [batch] int32
+ *   context_lens_dev : [batch] int32 L_b, including the token appended this step;
+ *                      must equal the slot's appended length
+ *   block_table_dev  : [batch][block_table_stride] int32
+ *   sm_scale         : softmax scale (1/sqrt(128) for standard attention)
+ *   out_dev          : [batch][num_q_heads][128] fp32, normalized output
+ *   lse_dev          : [batch][num_q_heads] fp32 natural-log normalizer, or NULL
+ * L_b = 0 gives a zero output and lse = -inf. Uses the cache's workspace, so
+ * decode calls on one cache must not overlap (issue them on one stream).
+ */
+kv4_status kv4_decode_attention(kv4_cache *cache, const void *q_bf16_dev, int num_q_heads,
+                                const int32_t *slot_ids_dev, const int32_t *context_lens_dev,
+                                const int32_t *block_table_dev, int block_table_stride, int batch,
+                                float sm_scale, float *out_dev, float *lse_dev, void *stream);
+
+/*
+ * kv4_decode_attention_debug — the same kernels, also writing their integer
+ * intermediates (any pointer may be NULL):
+ *   q8_dev     : [batch][num_q_heads][128] int8 quantized rotated query
+ *   q_scale_dev: [batch][num_q_heads] fp32 s_q
+ *   qk_dev     : [batch][num_q_heads][debug_stride] int32 QK accumulator per position
+ *                (INT4 codes in the INT4 region, INT8 side codes in the protected region)
+ *   w_hat_dev  : [batch][num_q_heads][debug_stride] u8 PV weight per INT4-region position
+ * Positions >= debug_stride are not written. For tests; slower than the plain call.
+ */
+kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, int num_q_heads,
+                                      const int32_t *slot_ids_dev, const int32_t *context_lens_dev,
+                                      const int32_t *block_table_dev, int block_table_stride,
+                                      int batch, float sm_scale, float *out_dev, float *lse_dev,
+                                      int8_t *q8_dev, float *q_scale_dev, int32_t *qk_dev,
+                                      uint8_t *w_hat_dev, int debug_stride, void *stream);
+
+/* Read (synchronously: waits for the device) and optionally clear the device
+ * error word. *code receives a kv4_device_error value. Returns KV4_OK. */
+kv4_status kv4_get_device_error(kv4_cache *cache, int32_t *code, int clear);
+
+/* Static description of a status code. */
+const char *kv4_status_string(kv4_status status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KV4_H */

@@ -1,0 +1,289 @@
+// api.cpp — the C ABI of libkv4 (declared in include/kv4.h): argument
+// validation, pool ownership, workspace sizing and kernel launches.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "kv4_internal.h"
+
+struct kv4_cache {
+    kv4_cache_config cfg;
+    int device = 0;
+    int num_sms = 0;
+    int grid[5] = {0, 0, 0, 0, 0};        // persistent decode CTAs per group size (index G)
+    uint8_t* pages = nullptr;
+    size_t pages_bytes = 0;
+    uint8_t* side = nullptr;
+    size_t side_bytes = 0;
+    size_t side_block = 0;
+    int32_t* seq_len = nullptr;
+    int32_t* err = nullptr;
+    kv4::PlanHeader* plan = nullptr;
+    int32_t* item_start = nullptr;
+    float* part_o = nullptr;
+    float2* part_ml = nullptr;
+    int32_t max_items = 0;
+    int32_t max_group = 0;
+};
+
+namespace {
+
+constexpr int kItemsPerCta = 16;   // target split-K items per persistent CTA
+
+bool group_supported(int g) { return g == 1 || g == 2 || g == 4; }
+
+void release(kv4_cache* c)
+{
+    cudaFree(c->pages);
+    cudaFree(c->side);
+    cudaFree(c->seq_len);
+    cudaFree(c->err);
+    cudaFree(c->plan);
+    cudaFree(c->item_start);
+    cudaFree(c->part_o);
+    cudaFree(c->part_ml);
+}
+
+template <typename T>
+bool alloc_zero(T** p, size_t bytes)
+{
+    if (bytes == 0) bytes = 16;
+    if (cudaMalloc(reinterpret_cast<void**>(p), bytes) != cudaSuccess) {
+        *p = nullptr;
+        return false;
+    }
+    return cudaMemset(*p, 0, bytes) == cudaSuccess;
+}
+
+kv4_status check_launch(cudaError_t e)
+{
+    return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kv4_status_string(kv4_status s)
+{
+    switch (s) {
+    case KV4_OK: return "ok";
+    case KV4_ERR_INVALID_ARG: return "invalid argument";
+    case KV4_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KV4_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case KV4_ERR_CUDA: return "CUDA runtime error";
+    case KV4_ERR_OUT_OF_RANGE: return "size above the cache's configured limits";
+    case KV4_ERR_DEVICE_FAULT: return "device-side index error (see kv4_get_device_error)";
+    }
+    return "unknown status";
+}
+
+kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
+{
+    if (!cfg || !out) return KV4_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (cfg->num_kv_heads < 1 || cfg->sink < 0 || cfg->window < 0 || cfg->num_pages < 1 ||
+        cfg->max_slots < 1 || cfg->max_batch < 1 || cfg->max_q_heads < 1 || cfg->max_work_items < 0)
+        return KV4_ERR_INVALID_ARG;
+    if (cfg->head_dim != KV4_HEAD_DIM || cfg->page_size != KV4_PAGE_SIZE) return KV4_ERR_UNSUPPORTED;
+    if (cfg->sink + cfg->window > kv4::kMaxProtected) return KV4_ERR_UNSUPPORTED;
+    if (cfg->max_q_heads % cfg->num_kv_heads != 0) return KV4_ERR_INVALID_ARG;
+    const int gmax = cfg->max_q_heads / cfg->num_kv_heads;
+    if (gmax > 4) return KV4_ERR_UNSUPPORTED;
+    if ((int64_t)cfg->num_pages * cfg->num_kv_heads > (int64_t)INT32_MAX * 8) return KV4_ERR_UNSUPPORTED;
+    if (cfg->num_pages > INT32_MAX) return KV4_ERR_UNSUPPORTED;
+
+    kv4_cache* c = new (std::nothrow) kv4_cache();
+    if (!c) return KV4_ERR_OUT_OF_MEMORY;
+    c->cfg = *cfg;
+    c->max_group = gmax;
+    if (cudaGetDevice(&c->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+        delete c;
+        return KV4_ERR_CUDA;
+    }
+    for (int g = 1; g <= 4; g <<= 1) {
+        int per_sm = 0;
+        if (kv4::decode_ctas_per_sm(g, &per_sm) != cudaSuccess || per_sm < 1) per_sm = 1;
+        c->grid[g] = c->num_sms * per_sm;
+    }
+    const int H = cfg->num_kv_heads;
+    const int S = cfg->sink + cfg->window;
+    c->side_block = ((size_t)S * 264 + 15) / 16 * 16;
+    c->pages_bytes = (size_t)cfg->num_pages * H * kv4::kPageBlock;
+    c->side_bytes = (size_t)cfg->max_slots * H * c->side_block;
+    int64_t items = cfg->max_work_items;
+    if (items == 0)
+        items = 2LL * cfg->max_batch * H + (int64_t)kItemsPerCta * 2 * c->grid[4];
+    if (items < 3LL * cfg->max_batch * H) items = 3LL * cfg->max_batch * H;
+    if (items > INT32_MAX / 2) {
+        delete c;
+        return KV4_ERR_UNSUPPORTED;
+    }
+    c->max_items = (int32_t)items;
+    bool ok = alloc_zero(&c->pages, c->pages_bytes) && alloc_zero(&c->side, c->side_bytes) &&
+              alloc_zero(&c->seq_len, sizeof(int32_t) * cfg->max_slots) &&
+              alloc_zero(&c->err, sizeof(int32_t)) && alloc_zero(&c->plan, sizeof(kv4::PlanHeader)) &&
+              alloc_zero(&c->item_start, sizeof(int32_t) * ((size_t)cfg->max_batch + 1)) &&
+              alloc_zero(&c->part_o, sizeof(float) * (size_t)items * gmax * kv4::kHeadDim) &&
+              alloc_zero(&c->part_ml, sizeof(float2) * (size_t)items * gmax);
+    if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
+        release(c);
+        delete c;
+        cudaGetLastError();
+        return KV4_ERR_OUT_OF_MEMORY;
+    }
+    *out = c;
+    return KV4_OK;
+}
+
+kv4_status kv4_cache_free(kv4_cache* c)
+{
+    if (!c) return KV4_OK;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(c->device);
+    cudaDeviceSynchronize();
+    release(c);
+    cudaSetDevice(prev);
+    delete c;
+    return KV4_OK;
+}
+
+kv4_status kv4_cache_get_info(const kv4_cache* c, kv4_cache_info* info)
+{
+    if (!c || !info) return KV4_ERR_INVALID_ARG;
+    info->page_pool_dev = c->pages;
+    info->page_pool_bytes = c->pages_bytes;
+    info->side_pool_dev = c->side;
+    info->side_pool_bytes = c->side_bytes;
+    info->side_block_bytes = c->side_block;
+    info->seq_len_dev = c->seq_len;
+    info->num_sms = c->num_sms;
+    info->decode_grid = c->grid[4];
+    info->device = c->device;
+    return KV4_OK;
+}
+
+kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t* cu_tokens,
+                      const int32_t* slot_ids, const int32_t* start_pos, const int32_t* block_table,
+                      int stride, int n_seqs, int total_tokens, void* stream)
+{
+    if (!c || n_seqs < 0 || total_tokens < 0 || stride < 0) return KV4_ERR_INVALID_ARG;
+    if (n_seqs == 0 || total_tokens == 0) return KV4_OK;
+    if (!k || !v || !cu_tokens || !slot_ids || !start_pos || !block_table || stride < 1)
+        return KV4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 7) return KV4_ERR_INVALID_ARG;
+    if ((int64_t)total_tokens * c->cfg.num_kv_heads > (int64_t)INT32_MAX * 8) return KV4_ERR_OUT_OF_RANGE;
+    kv4::AppendArgs a{};
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.cu_tokens = cu_tokens;
+    a.slot_ids = slot_ids;
+    a.start_pos = start_pos;
+    a.block_table = block_table;
+    a.stride = stride;
+    a.n_seqs = n_seqs;
+    a.total_tokens = total_tokens;
+    a.num_heads = c->cfg.num_kv_heads;
+    a.sink = c->cfg.sink;
+    a.window = c->cfg.window;
+    a.max_slots = c->cfg.max_slots;
+    a.num_pages = c->cfg.num_pages;
+    a.pages = c->pages;
+    a.side = c->side;
+    a.side_block_bytes = (int64_t)c->side_block;
+    a.seq_len = c->seq_len;
+    a.err = c->err;
+    return check_launch(kv4::launch_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
+                                const int32_t* slot_ids, const int32_t* context_lens,
+                                const int32_t* block_table, int stride, int batch, float sm_scale,
+                                float* out, float* lse, int8_t* dq8, float* dqs, int32_t* dqk,
+                                uint8_t* dw, int dbg_stride, void* stream)
+{
+    if (!c || batch < 0 || num_q_heads < 1 || stride < 0) return KV4_ERR_INVALID_ARG;
+    if (batch == 0) return KV4_OK;
+    if (!q || !slot_ids || !context_lens || !block_table || !out || stride < 1) return KV4_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale)) return KV4_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(q) & 7 || reinterpret_cast<uintptr_t>(out) & 15)
+        return KV4_ERR_INVALID_ARG;
+    const int H = c->cfg.num_kv_heads;
+    if (num_q_heads % H != 0) return KV4_ERR_INVALID_ARG;
+    const int G = num_q_heads / H;
+    if (!group_supported(G)) return KV4_ERR_UNSUPPORTED;
+    if (batch > c->cfg.max_batch || num_q_heads > c->cfg.max_q_heads) return KV4_ERR_OUT_OF_RANGE;
+    if ((dqk || dw) && dbg_stride < 1) return KV4_ERR_INVALID_ARG;
+    kv4::DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.slot_ids = slot_ids;
+    a.context_lens = context_lens;
+    a.block_table = block_table;
+    a.stride = stride;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_heads = H;
+    a.group = G;
+    a.sink = c->cfg.sink;
+    a.window = c->cfg.window;
+    a.max_slots = c->cfg.max_slots;
+    a.num_pages = c->cfg.num_pages;
+    a.log2_scale = (float)((double)sm_scale * 1.4426950408889634074);
+    a.pages = c->pages;
+    a.side = c->side;
+    a.side_block_bytes = (int64_t)c->side_block;
+    a.seq_len = c->seq_len;
+    a.err = c->err;
+    a.plan = c->plan;
+    a.item_start = c->item_start;
+    a.part_o = c->part_o;
+    a.part_ml = c->part_ml;
+    // partial buffers are laid out for this call's G: [items][G][128]
+    a.max_items = (int32_t)std::min<int64_t>(c->max_items, (int64_t)c->max_items * c->max_group / G);
+    a.target_items = kItemsPerCta * c->grid[G];
+    a.out = out;
+    a.lse = lse;
+    a.dbg_q8 = dq8;
+    a.dbg_qscale = dqs;
+    a.dbg_qk = dqk;
+    a.dbg_w = dw;
+    a.dbg_stride = dbg_stride;
+    return check_launch(kv4::launch_decode(a, c->grid[G], static_cast<cudaStream_t>(stream)));
+}
+
+kv4_status kv4_decode_attention(kv4_cache* c, const void* q, int num_q_heads, const int32_t* slot_ids,
+                                const int32_t* context_lens, const int32_t* block_table, int stride,
+                                int batch, float sm_scale, float* out, float* lse, void* stream)
+{
+    return decode_common(c, q, num_q_heads, slot_ids, context_lens, block_table, stride, batch,
+                         sm_scale, out, lse, nullptr, nullptr, nullptr, nullptr, 0, stream);
+}
+
+kv4_status kv4_decode_attention_debug(kv4_cache* c, const void* q, int num_q_heads,
+                                      const int32_t* slot_ids, const int32_t* context_lens,
+                                      const int32_t* block_table, int stride, int batch,
+                                      float sm_scale, float* out, float* lse, int8_t* q8,
+                                      float* q_scale, int32_t* qk, uint8_t* w_hat, int debug_stride,
+                                      void* stream)
+{
+    return decode_common(c, q, num_q_heads, slot_ids, context_lens, block_table, stride, batch,
+                         sm_scale, out, lse, q8, q_scale, qk, w_hat, debug_stride, stream);
+}
+
+kv4_status kv4_get_device_error(kv4_cache* c, int32_t* code, int clear)
+{
+    if (!c || !code) return KV4_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return KV4_ERR_CUDA;
+    if (cudaMemcpy(code, c->err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KV4_ERR_CUDA;
+    if (clear && cudaMemset(c->err, 0, sizeof(int32_t)) != cudaSuccess) return KV4_ERR_CUDA;
+    return KV4_OK;
+}
+
+}  // extern "C"

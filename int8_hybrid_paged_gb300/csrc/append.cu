@@ -1,0 +1,123 @@
+// append.cu — kv4_append: Hadamard-rotate K, quantize K and V to 4-bit affine
+// codes, pack them into the page of each position, and write the 8-bit side
+// copies of sink and recent positions.
+//
+// Pages cited (title, then section):
+//   [zh] "KV4-RL:用 INT4 KV 缓存量化为 RLVR 异步 Rollout 提速" — 方法步骤详情 steps 2-3,
+//        前置知识 › 分组仿射 KV 量化
+//   [ko] "INT4 KV 캐시로 비동기 RLVR 롤아웃을 1.8배 가속한다" — 전제와 한계
+//
+// One warp per (token, KV head): lane l holds dims 4l..4l+3 of K and V (one
+// 8-byte load each, 256 contiguous bytes per warp), the rotation and both
+// min/max reductions run in registers and shuffles, and the warp writes the
+// token's 64-byte K code row in one coalesced store.
+#include "device_common.cuh"
+#include "kv4_internal.h"
+
+namespace kv4 {
+
+__global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (gw >= (int64_t)a.total_tokens * a.num_heads) return;   // whole warp leaves together
+    const int tok = (int)(gw / a.num_heads);
+    const int h = (int)(gw - (int64_t)tok * a.num_heads);
+
+    // sequence i of this token: the largest i with cu[i] <= tok (cu[n] = total > tok)
+    int lo = 0, hi = a.n_seqs;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(&a.cu_tokens[mid]) <= tok) lo = mid; else hi = mid;
+    }
+    const int i = lo;
+    const int c0 = __ldg(&a.cu_tokens[i]);
+    const int c1 = __ldg(&a.cu_tokens[i + 1]);
+    if (tok < c0 || tok >= c1) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_TOKENS);
+        return;
+    }
+    const int slot = __ldg(&a.slot_ids[i]);
+    const int start = __ldg(&a.start_pos[i]);
+    const int pos = start + (tok - c0);
+    const int new_len = start + (c1 - c0);
+    if (slot < 0 || slot >= a.max_slots) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_SLOT);
+        return;
+    }
+    if (start < 0 || pos / kPage >= a.stride) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_POSITION);
+        return;
+    }
+    const int page = __ldg(&a.block_table[(int64_t)i * a.stride + pos / kPage]);
+    if (page < 0 || (int64_t)page >= a.num_pages) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_PAGE);
+        return;
+    }
+
+    float kx[4], vx[4];
+    const int64_t row = ((int64_t)tok * a.num_heads + h) * kHeadDim + 4 * lane;
+    load_bf16x4(a.k + row, kx);
+    load_bf16x4(a.v + row, vx);
+    warp_fwht128(kx, lane);                 // keys are stored in the rotated basis; V is not rotated
+
+    uint32_t kc[4], vc[4];
+    __half kd, km, vd, vm;
+    warp_quant<15>(kx, kc, kd, km);
+    warp_quant<15>(vx, vc, vd, vm);
+
+    uint8_t* blk = a.pages + ((int64_t)page * a.num_heads + h) * kPageBlock;
+    const int ts = pos % kPage;
+    // K row ts: byte j = c[2j] | c[2j+1] << 4; this lane owns bytes 2l and 2l+1
+    const uint16_t kb = (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
+    *reinterpret_cast<uint16_t*>(blk + kKCodeOff + ts * 64 + 2 * lane) = kb;
+    // V dim-pair rows 2l and 2l+1, column ts
+    blk[kVCodeOff + (2 * lane) * 16 + ts] = (uint8_t)(vc[0] | (vc[1] << 4));
+    blk[kVCodeOff + (2 * lane + 1) * 16 + ts] = (uint8_t)(vc[2] | (vc[3] << 4));
+    if (lane == 0) {
+        *reinterpret_cast<__half2*>(blk + kKMetaOff + ts * 4) = __halves2half2(kd, km);
+        *reinterpret_cast<__half2*>(blk + kVMetaOff + ts * 4) = __halves2half2(vd, vm);
+    }
+
+    // INT8 side copies: sink row pos (pos < s), ring row s + pos mod w for the last
+    // w positions of this append. Earlier positions of a long chunk would map to the
+    // same ring rows and be overwritten anyway; skipping them avoids the race.
+    const int s = a.sink, w = a.window;
+    const bool to_sink = pos < s;
+    const bool to_ring = (w > 0) && (pos >= new_len - w);
+    if (to_sink || to_ring) {
+        uint32_t k8[4], v8[4];
+        __half k8d, k8m, v8d, v8m;
+        warp_quant<255>(kx, k8, k8d, k8m);
+        warp_quant<255>(vx, v8, v8d, v8m);
+        const int S = s + w;
+        uint8_t* sb = a.side + ((int64_t)slot * a.num_heads + h) * a.side_block_bytes;
+        const uint32_t kw = k8[0] | (k8[1] << 8) | (k8[2] << 16) | (k8[3] << 24);
+        const uint32_t vw = v8[0] | (v8[1] << 8) | (v8[2] << 16) | (v8[3] << 24);
+        int idx[2];
+        int n = 0;
+        if (to_sink) idx[n++] = pos;
+        if (to_ring) idx[n++] = s + pos % w;
+        for (int k = 0; k < n; ++k) {
+            const int r = idx[k];
+            *reinterpret_cast<uint32_t*>(sb + r * 128 + 4 * lane) = kw;
+            *reinterpret_cast<uint32_t*>(sb + S * 128 + r * 128 + 4 * lane) = vw;
+            if (lane == 0) {
+                *reinterpret_cast<__half2*>(sb + S * 256 + r * 4) = __halves2half2(k8d, k8m);
+                *reinterpret_cast<__half2*>(sb + S * 260 + r * 4) = __halves2half2(v8d, v8m);
+            }
+        }
+    }
+    if (lane == 0 && h == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream)
+{
+    const int64_t warps = (int64_t)a.total_tokens * a.num_heads;
+    if (warps == 0) return cudaSuccess;
+    const int64_t blocks = (warps + 7) / 8;
+    kv4_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kv4

@@ -1,0 +1,249 @@
+// device_common.cuh — device helpers shared by the append and decode kernels.
+//
+// Pages cited (title, then section):
+//   [zh] "KV4-RL:用 INT4 KV 缓存量化为 RLVR 异步 Rollout 提速"
+//   [ko] "INT4 KV 캐시로 비동기 RLVR 롤아웃을 1.8배 가속한다"
+//
+// Every float operation that feeds an integer decision (a code, an INT8 query
+// value, a u8 PV weight) is spelled with an explicit-rounding intrinsic, so the
+// compiler cannot contract or reorder it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace kv4 {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------- errors
+__device__ __forceinline__ void report_error(int32_t* err, int32_t code)
+{
+    if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- bf16 loads
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 4 consecutive bf16 values (8 bytes, 8-byte aligned) -> float.
+__device__ __forceinline__ void load_bf16x4(const uint16_t* p, float (&x)[4])
+{
+    uint2 r = __ldg(reinterpret_cast<const uint2*>(p));
+    x[0] = bf16_lo(r.x);
+    x[1] = bf16_hi(r.x);
+    x[2] = bf16_lo(r.y);
+    x[3] = bf16_hi(r.y);
+}
+
+// ---------------------------------------------------------------- warp reductions
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, m));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_int(int v)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
+    return v;
+}
+
+// ---------------------------------------------------------------- Hadamard rotation
+// Orthonormal 128-point Walsh–Hadamard transform (H/√128) over one warp; lane l
+// holds dims 4l..4l+3. Stages h = 1, 2 run inside the lane, h = 4 … 64 pair lane
+// l with lane l ^ (h/4). Within a stage each pair (i, i+h) becomes
+// (x_i + x_{i+h}, x_i − x_{i+h}); the stage order is fixed, so the rounded result
+// does not depend on how the pairs are spread over lanes.
+// [zh] 前置知识 › 分组仿射 KV 量化 (QH(HK)^T = QK^T); 方法步骤详情 step 2.
+__device__ __forceinline__ void warp_fwht128(float (&x)[4], int lane)
+{
+    float a0 = __fadd_rn(x[0], x[1]), a1 = __fsub_rn(x[0], x[1]);
+    float a2 = __fadd_rn(x[2], x[3]), a3 = __fsub_rn(x[2], x[3]);
+    x[0] = __fadd_rn(a0, a2);
+    x[2] = __fsub_rn(a0, a2);
+    x[1] = __fadd_rn(a1, a3);
+    x[3] = __fsub_rn(a1, a3);
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float y = __shfl_xor_sync(kFull, x[i], m);
+            x[i] = upper ? __fsub_rn(y, x[i]) : __fadd_rn(x[i], y);
+        }
+    }
+    const float inv_sqrt128 = 0x1.6a09e6p-4f;   // nearest float to 1/√128
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = __fmul_rn(x[i], inv_sqrt128);
+}
+
+// ---------------------------------------------------------------- affine quantizer
+// One group = the warp's 128 values. x^ = Δc + m with fp16 Δ, m:
+// m = fp16 rounded down from min x (a zero minimum is taken as +0),
+// Δ = fp16 rounded up from (max x − m)/LEVELS, itself rounded up in float,
+// c = clamp(rint((x − m) · fl(1/Δ)), 0, LEVELS); Δ = 0 gives c = 0.
+// [zh] 前置知识 › 分组仿射 KV 量化; 方法步骤详情 step 2 (fp16 Δ, m computed online).
+template <int LEVELS>
+__device__ __forceinline__ void warp_quant(const float (&x)[4], uint32_t (&c)[4],
+                                           __half& delta_h, __half& min_h)
+{
+    float lo = warp_min(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
+    float hi = warp_max(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+    lo = __fadd_rn(lo, 0.0f);
+    min_h = __float2half_rd(lo);
+    const float m = __half2float(min_h);
+    const float r = __fadd_ru(hi, -m);
+    const float d = __fdiv_ru(r, (float)LEVELS);
+    delta_h = __float2half_ru(d);
+    const float delta = __half2float(delta_h);
+    if (delta == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[i] = 0;
+        return;
+    }
+    const float inv = __fdiv_rn(1.0f, delta);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        int v = __float2int_rn(__fmul_rn(__fsub_rn(x[i], m), inv));
+        v = v < 0 ? 0 : (v > LEVELS ? LEVELS : v);
+        c[i] = (uint32_t)v;
+    }
+}
+
+// ---------------------------------------------------------------- exp2
+// exp2 for the page-local PV weights, identical on every device and on the host
+// oracle: 2^x = 2^n · 2^f, n = rint(x), f = x − n ∈ [−½, ½], 2^f by the Taylor
+// series Σ (f ln2)^k / k! up to k = 7 in Horner form with fused multiply-adds.
+// Coefficients: (ln 2)^k / k! rounded to float. Used for x ≤ 0; x < −125 gives 0,
+// so every nonzero result is a normal float and the 2^n scaling is exact.
+__device__ __forceinline__ float exp2_poly(float x)
+{
+    if (!(x >= -125.0f)) return 0.0f;
+    const int n = __float2int_rn(x);
+    const float f = __fsub_rn(x, (float)n);
+    float p = 0x1.ffcbfcp-17f;
+    p = __fmaf_rn(p, f, 0x1.430912p-13f);
+    p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
+    p = __fmaf_rn(p, f, 0x1.3b2ab6p-7f);
+    p = __fmaf_rn(p, f, 0x1.c6b08ep-5f);
+    p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
+    p = __fmaf_rn(p, f, 0x1.62e430p-1f);
+    p = __fmaf_rn(p, f, 1.0f);
+    return __int_as_float(__float_as_int(p) + (n << 23));
+}
+
+// Fast exp2 (hardware approximation) for rescaling factors that decide no integer.
+__device__ __forceinline__ float exp2_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------- integer dots
+// Σ_k a_k·b_k over four byte lanes: a signed (INT8 query), b unsigned (codes).
+__device__ __forceinline__ int dp4a_su(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// both unsigned (u8 PV weights against codes)
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c)
+{
+    uint32_t d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return (int)d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// ---------------------------------------------------------------- bulk copies + mbarrier
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size multiple of 16),
+// completion counted on `bar`. Plain (non-multicast) form.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`, giving up after ~2 s. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
+}  // namespace kv4

@@ -1,0 +1,250 @@
+"""Python binding of libkv4 (include/kv4.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls. Tensors are
+torch CUDA tensors; their device pointers and the current torch stream are
+passed through unchanged. The compute happens in libkv4's kernels; there is no
+fallback: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkv4.so")
+
+KV4_OK = 0
+STATUS = {0: "KV4_OK", -1: "KV4_ERR_INVALID_ARG", -2: "KV4_ERR_UNSUPPORTED",
+          -3: "KV4_ERR_OUT_OF_MEMORY", -4: "KV4_ERR_CUDA", -5: "KV4_ERR_OUT_OF_RANGE",
+          -6: "KV4_ERR_DEVICE_FAULT"}
+DEVICE_ERRORS = {0: "none", 1: "bad slot", 2: "bad page", 3: "bad position",
+                 4: "context length mismatch", 5: "staging wait timeout", 6: "bad token layout"}
+PAGE_BLOCK_BYTES = 2176
+HEAD_DIM = 128
+PAGE_SIZE = 16
+
+EXPORTED = ("kv4_cache_create", "kv4_cache_free", "kv4_cache_get_info", "kv4_append",
+            "kv4_decode_attention", "kv4_decode_attention_debug", "kv4_get_device_error",
+            "kv4_status_string")
+
+
+class KV4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({_status_text(status)})")
+
+
+class kv4_cache_config(C.Structure):
+    _fields_ = [("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("page_size", C.c_int32),
+                ("sink", C.c_int32), ("window", C.c_int32), ("num_pages", C.c_int64),
+                ("max_slots", C.c_int32), ("max_batch", C.c_int32), ("max_q_heads", C.c_int32),
+                ("max_work_items", C.c_int32)]
+
+
+class kv4_cache_info(C.Structure):
+    _fields_ = [("page_pool_dev", C.c_void_p), ("page_pool_bytes", C.c_size_t),
+                ("side_pool_dev", C.c_void_p), ("side_pool_bytes", C.c_size_t),
+                ("side_block_bytes", C.c_size_t), ("seq_len_dev", C.c_void_p),
+                ("num_sms", C.c_int32), ("decode_grid", C.c_int32), ("device", C.c_int32)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libkv4. Raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libkv4 is not built ({path} missing); run "
+                           "`python -m int8_hybrid_paged_gb300.build` first")
+    lib = C.CDLL(path)
+    P, I, F = C.c_void_p, C.c_int, C.c_float
+    lib.kv4_status_string.argtypes = [I]
+    lib.kv4_status_string.restype = C.c_char_p
+    lib.kv4_cache_create.argtypes = [C.POINTER(kv4_cache_config), C.POINTER(P)]
+    lib.kv4_cache_free.argtypes = [P]
+    lib.kv4_cache_get_info.argtypes = [P, C.POINTER(kv4_cache_info)]
+    lib.kv4_append.argtypes = [P, P, P, P, P, P, P, I, I, I, P]
+    lib.kv4_decode_attention.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P]
+    lib.kv4_decode_attention_debug.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P, P, P, P, I, P]
+    lib.kv4_get_device_error.argtypes = [P, C.POINTER(C.c_int32), I]
+    for name in EXPORTED:
+        getattr(lib, name).restype = C.c_int if name != "kv4_status_string" else C.c_char_p
+    _lib = lib
+    return lib
+
+
+def _status_text(status: int) -> str:
+    try:
+        return load().kv4_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - only for message text
+        return "?"
+
+
+def _check(status: int, where: str):
+    if status != KV4_OK:
+        raise KV4Error(status, where)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+# --------------------------------------------------------------------------- entry points
+
+def kv4_status_string(status: int) -> str:
+    return load().kv4_status_string(status).decode()
+
+
+def kv4_cache_create(num_kv_heads, num_pages, max_slots, max_batch, max_q_heads, sink=16,
+                     window=128, head_dim=HEAD_DIM, page_size=PAGE_SIZE, max_work_items=0):
+    cfg = kv4_cache_config(num_kv_heads, head_dim, page_size, sink, window, num_pages, max_slots,
+                           max_batch, max_q_heads, max_work_items)
+    h = C.c_void_p()
+    _check(load().kv4_cache_create(C.byref(cfg), C.byref(h)), "kv4_cache_create")
+    return h
+
+
+def kv4_cache_free(handle):
+    _check(load().kv4_cache_free(handle), "kv4_cache_free")
+
+
+def kv4_cache_get_info(handle) -> kv4_cache_info:
+    info = kv4_cache_info()
+    _check(load().kv4_cache_get_info(handle, C.byref(info)), "kv4_cache_get_info")
+    return info
+
+
+def kv4_append(handle, k, v, cu_tokens, slot_ids, start_pos, block_table, stream=None):
+    """k, v: bf16 [T][H_kv][128]; cu_tokens int32 [n+1]; slot_ids, start_pos int32 [n];
+    block_table int32 [n][stride]."""
+    n = slot_ids.numel()
+    _check(load().kv4_append(handle, _ptr(k, torch.bfloat16, "k"), _ptr(v, torch.bfloat16, "v"),
+                             _ptr(cu_tokens, torch.int32, "cu_tokens"),
+                             _ptr(slot_ids, torch.int32, "slot_ids"),
+                             _ptr(start_pos, torch.int32, "start_pos"),
+                             _ptr(block_table, torch.int32, "block_table"),
+                             block_table.shape[-1], n, k.shape[0], _stream(stream)), "kv4_append")
+
+
+def kv4_decode_attention(handle, q, slot_ids, context_lens, block_table, out, lse=None,
+                         sm_scale=None, stream=None):
+    """q: bf16 [B][H_q][128]; out: fp32 [B][H_q][128]; lse: fp32 [B][H_q] or None."""
+    B, Hq = q.shape[0], q.shape[1]
+    scale = float(HEAD_DIM ** -0.5 if sm_scale is None else sm_scale)
+    _check(load().kv4_decode_attention(handle, _ptr(q, torch.bfloat16, "q"), Hq,
+                                       _ptr(slot_ids, torch.int32, "slot_ids"),
+                                       _ptr(context_lens, torch.int32, "context_lens"),
+                                       _ptr(block_table, torch.int32, "block_table"),
+                                       block_table.shape[-1], B, scale,
+                                       _ptr(out, torch.float32, "out"),
+                                       _ptr(lse, torch.float32, "lse"), _stream(stream)),
+           "kv4_decode_attention")
+
+
+def kv4_decode_attention_debug(handle, q, slot_ids, context_lens, block_table, out, lse=None,
+                               q8=None, q_scale=None, qk=None, w_hat=None, sm_scale=None,
+                               stream=None):
+    B, Hq = q.shape[0], q.shape[1]
+    scale = float(HEAD_DIM ** -0.5 if sm_scale is None else sm_scale)
+    dstride = qk.shape[-1] if qk is not None else (w_hat.shape[-1] if w_hat is not None else 0)
+    _check(load().kv4_decode_attention_debug(
+        handle, _ptr(q, torch.bfloat16, "q"), Hq, _ptr(slot_ids, torch.int32, "slot_ids"),
+        _ptr(context_lens, torch.int32, "context_lens"),
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[-1], B, scale,
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(q8, torch.int8, "q8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(qk, torch.int32, "qk"), _ptr(w_hat, torch.uint8, "w_hat"), dstride,
+        _stream(stream)), "kv4_decode_attention_debug")
+
+
+def kv4_get_device_error(handle, clear=True) -> int:
+    code = C.c_int32(0)
+    _check(load().kv4_get_device_error(handle, C.byref(code), 1 if clear else 0),
+           "kv4_get_device_error")
+    return int(code.value)
+
+
+# --------------------------------------------------------------------------- convenience
+
+class KV4Cache:
+    """Owning wrapper: creates the cache on construction, frees it on close()."""
+
+    def __init__(self, num_kv_heads, num_pages, max_slots, max_batch, max_q_heads, sink=16,
+                 window=128, max_work_items=0):
+        self.num_kv_heads, self.sink, self.window = num_kv_heads, sink, window
+        self.num_pages, self.max_slots = num_pages, max_slots
+        self.handle = kv4_cache_create(num_kv_heads, num_pages, max_slots, max_batch, max_q_heads,
+                                       sink, window, max_work_items=max_work_items)
+
+    def close(self):
+        if self.handle is not None:
+            kv4_cache_free(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+    def info(self):
+        return kv4_cache_get_info(self.handle)
+
+    def append(self, k, v, cu_tokens, slot_ids, start_pos, block_table, stream=None):
+        kv4_append(self.handle, k, v, cu_tokens, slot_ids, start_pos, block_table, stream)
+
+    def decode(self, q, slot_ids, context_lens, block_table, out=None, lse=None, sm_scale=None,
+               stream=None):
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        kv4_decode_attention(self.handle, q, slot_ids, context_lens, block_table, out, lse,
+                             sm_scale, stream)
+        return out
+
+    def device_error(self, clear=True):
+        return kv4_get_device_error(self.handle, clear)
+
+    def raw_pools(self):
+        """Host copies of the page pool (uint8), the side pool (uint8) and the slot
+        lengths (int32), read through views of the cache's device memory."""
+        info = self.info()
+        dev = torch.device("cuda", info.device)
+
+        def view(ptr, nbytes, typestr, itemsize):
+            class _Mem:
+                __cuda_array_interface__ = {"shape": (nbytes // itemsize,), "typestr": typestr,
+                                            "data": (ptr, True), "version": 3}
+            return torch.as_tensor(_Mem(), device=dev)
+
+        torch.cuda.synchronize(dev)
+        pages = view(info.page_pool_dev, info.page_pool_bytes, "|u1", 1).cpu().numpy()
+        side = view(info.side_pool_dev, info.side_pool_bytes, "|u1", 1).cpu().numpy()
+        lens = view(info.seq_len_dev, 4 * self.max_slots, "<i4", 4).cpu().numpy()
+        return pages, side, int(info.side_block_bytes), lens

@@ -1,0 +1,119 @@
+"""Test helpers: read libkv4's documented page/side layout back into the oracle's
+logical form, and set up matching GPU and oracle caches from the seeded inputs."""
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from int8_hybrid_paged_gb300 import inputs
+from int8_hybrid_paged_gb300.kv4 import KV4Cache
+
+D = 128
+P = 16
+BLOCK = 2176
+
+
+def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
+    """K/V INT4 codes and metadata of positions (page_ids[i], slots_in_page[i]) of head h,
+    following the page-block layout declared in include/kv4.h."""
+    n = len(page_ids)
+    base = (np.asarray(page_ids, np.int64) * H + h) * BLOCK
+    ts = np.asarray(slots_in_page, np.int64)
+    krow = pages[(base + ts * 64)[:, None] + np.arange(64)[None, :]]
+    k = np.empty((n, D), np.uint8)
+    k[:, 0::2] = krow & 15
+    k[:, 1::2] = krow >> 4
+    vbytes = pages[(base + 1024 + ts)[:, None] + (np.arange(64) * 16)[None, :]]
+    v = np.empty((n, D), np.uint8)
+    v[:, 0::2] = vbytes & 15
+    v[:, 1::2] = vbytes >> 4
+    km = pages[(base + 2048 + ts * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    vm = pages[(base + 2112 + ts * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    return k, v, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
+
+
+def unpack_side(side, side_block, H, S, slot, h):
+    blk = side[(slot * H + h) * side_block:(slot * H + h) * side_block + S * 264]
+    k8 = blk[:S * 128].reshape(S, 128)
+    v8 = blk[S * 128:S * 256].reshape(S, 128)
+    km = blk[S * 256:S * 260].copy().view(np.uint16).reshape(S, 2)
+    vm = blk[S * 260:S * 264].copy().view(np.uint16).reshape(S, 2)
+    return k8, v8, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
+
+
+class Setup:
+    """A GPU cache and (for the sampled sequences) oracle caches over the same inputs."""
+
+    def __init__(self, H, G, s, w, lens, seed=0, spare_pages=7, kv_device="cpu",
+                 chunks=None, max_work_items=0):
+        self.H, self.G, self.s, self.w = H, G, s, w
+        self.lens = [int(L) for L in lens]
+        self.B = len(lens)
+        self.seed = seed
+        need = sum((L + P - 1) // P for L in self.lens)
+        self.num_pages = need + spare_pages
+        self.bt = inputs.block_tables(self.lens, P, self.num_pages, seed)
+        self.cache = KV4Cache(H, self.num_pages, max_slots=self.B + 1, max_batch=self.B,
+                              max_q_heads=H * G, sink=s, window=w, max_work_items=max_work_items)
+        self.kv = []
+        for b, L in enumerate(self.lens):
+            k, v = inputs.sequence_kv(b, L, H, seed, device=kv_device)
+            self.kv.append((k, v))
+        self.bt_dev = torch.from_numpy(self.bt).cuda()
+        self._append(chunks)
+
+    def _append(self, chunks):
+        """chunks: list of position cut points applied to every sequence; default one call."""
+        cuts = sorted(set([0] + list(chunks or []) + [max(self.lens)]))
+        for lo, hi in zip(cuts[:-1], cuts[1:]):
+            ks, vs, cu, slots, starts, rows = [], [], [0], [], [], []
+            for b, L in enumerate(self.lens):
+                a, z = min(lo, L), min(hi, L)
+                if z <= a:
+                    continue
+                ks.append(self.kv[b][0][a:z])
+                vs.append(self.kv[b][1][a:z])
+                cu.append(cu[-1] + z - a)
+                slots.append(b)
+                starts.append(a)
+                rows.append(b)
+            if not slots:
+                continue
+            k = torch.cat(ks).cuda().contiguous()
+            v = torch.cat(vs).cuda().contiguous()
+            self.cache.append(k, v, torch.tensor(cu, dtype=torch.int32).cuda(),
+                              torch.tensor(slots, dtype=torch.int32).cuda(),
+                              torch.tensor(starts, dtype=torch.int32).cuda(),
+                              self.bt_dev[rows].contiguous())
+
+    def oracle_for(self, b):
+        oc = oracle.OracleCache(self.H, self.s, self.w, self.lens[b], num_slots=1)
+        k, v = self.kv[b]
+        oc.append(0, 0, inputs.bf16_bits(k), inputs.bf16_bits(v))
+        return oc
+
+    def decode(self, q, debug_stride=0, lens=None):
+        lens = self.lens if lens is None else lens
+        B, Hq = q.shape[0], q.shape[1]
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        slots = torch.arange(B, dtype=torch.int32, device="cuda")
+        cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        if debug_stride:
+            from int8_hybrid_paged_gb300.kv4 import kv4_decode_attention_debug
+            q8 = torch.zeros((B, Hq, D), dtype=torch.int8, device="cuda")
+            qs = torch.zeros((B, Hq), dtype=torch.float32, device="cuda")
+            qk = torch.full((B, Hq, debug_stride), -(2 ** 31), dtype=torch.int32, device="cuda")
+            wh = torch.zeros((B, Hq, debug_stride), dtype=torch.uint8, device="cuda")
+            kv4_decode_attention_debug(self.cache.handle, q, slots, cl, self.bt_dev, out, lse,
+                                       q8, qs, qk, wh, sm_scale=1 / math.sqrt(D))
+            torch.cuda.synchronize()
+            return out, lse, dict(q8=q8.cpu().numpy(), q_scale=qs.cpu().numpy(),
+                                  qk=qk.cpu().numpy(), w_hat=wh.cpu().numpy())
+        self.cache.decode(q, slots, cl, self.bt_dev, out, lse, sm_scale=1 / math.sqrt(D))
+        torch.cuda.synchronize()
+        return out, lse, None
+
+    def close(self):
+        self.cache.close()
