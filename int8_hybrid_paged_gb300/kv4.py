@@ -240,7 +240,7 @@ class KV4Cache:
         def view(ptr, nbytes, typestr, itemsize):
             class _Mem:
                 __cuda_array_interface__ = {"shape": (nbytes // itemsize,), "typestr": typestr,
-                                            "data": (ptr, True), "version": 3}
+                                            "data": (ptr, False), "version": 3}
             return torch.as_tensor(_Mem(), device=dev)
 
         torch.cuda.synchronize(dev)
