@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Decode-attention throughput of the KV4 hot path (libkv4) on GB300.
+
+One step = one kv4_decode_attention call (plan + split-K attention + merge)
+over the whole batch of the workload, with the paged INT4 cache and INT8 side
+buffers already filled by one prefill kv4_append. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kv4|reference]
+                  [--workload qwen3-8b|qwen3-4b|long-tail]
+
+--impl reference times the CPU oracle (the method's plain definition) on the
+host cores on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs its own batch (weak scaling, no collective
+in the data path); the timing barrier and the max-over-ranks use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from int8_hybrid_paged_gb300 import bytes_model, inputs  # noqa: E402
+
+METRIC = "decode-attn context tokens/s and achieved HBM GB/s (% GB300 peak), 1 GPU"
+UNIT = "context tokens/s"
+DTYPE = "s8 x u4/u8 -> s32 dots, fp32 softmax/accumulate"
+L2_BYTES = 129 * 2 ** 20
+SPLIT_SOURCES = ["int8_hybrid_paged_gb300/csrc/decode.cu",
+                 "int8_hybrid_paged_gb300/csrc/device_common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["kv4", "reference"], default="kv4")
+    ap.add_argument("--workload", default="qwen3-8b", choices=["qwen3-8b", "qwen3-4b", "long-tail"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- environment
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (torch.cuda.is_available() and args.impl == "kv4") else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max_sum(world, t_max, v_sum, device):
+    if world == 1:
+        return t_max, v_sum
+    import torch.distributed as dist
+    a = torch.tensor([t_max], dtype=torch.float64, device=device)
+    b = torch.tensor([v_sum], dtype=torch.float64, device=device)
+    dist.all_reduce(a, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(a.item()), float(b.item())
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.25)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+def split_kernel_traffic():
+    """dram bytes per launch of the split kernel from the committed ncu summary, if the
+    kernel sources are unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256()
+    for f in SPLIT_SOURCES:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    if d.get("source_sha256") != h.hexdigest():
+        return None
+    return d
+
+
+# --------------------------------------------------------------------------- workload
+
+def build_workload(wl, seed, device, sample_seqs=0):
+    """Fill a cache with the workload's sequences (one prefill append). Host copies
+    (bf16 bits) of the first `sample_seqs` sequences' K/V are kept for the CPU
+    baseline; the device K/V are freed once appended."""
+    from int8_hybrid_paged_gb300.kv4 import KV4Cache
+
+    lens = list(wl.context_lens)
+    B, H, Hq = wl.batch, wl.num_kv_heads, wl.num_q_heads
+    need = sum((L + 15) // 16 for L in lens)
+    num_pages = need + max(64, need // 100)
+    bt = inputs.block_tables(lens, 16, num_pages, seed)
+    cache = KV4Cache(H, num_pages, max_slots=B, max_batch=B, max_q_heads=Hq, sink=wl.sink,
+                     window=wl.window)
+    total = sum(lens)
+    k, v = inputs.kv_tokens(total, H, seed * 1_000_003 + 17, device=device)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    bt_dev = torch.from_numpy(bt).to(device)
+    cache.append(k, v, torch.from_numpy(cu).to(device), slots,
+                 torch.zeros(B, dtype=torch.int32, device=device), bt_dev)
+    host_kv = [(inputs.bf16_bits(k[cu[b]:cu[b + 1]]), inputs.bf16_bits(v[cu[b]:cu[b + 1]]))
+               for b in range(min(sample_seqs, B))]
+    del k, v
+    q = inputs.queries(B, Hq, seed, device=device)
+    cl = torch.tensor(lens, dtype=torch.int32, device=device)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    err = cache.device_error()
+    if err:
+        raise RuntimeError(f"device error {err} while filling the cache")
+    return dict(cache=cache, host_kv=host_kv, cu=cu, bt=bt, bt_dev=bt_dev, q=q, cl=cl,
+                slots=slots, lens=lens, num_pages=num_pages)
+
+
+def oracle_sample(wl, st, cpu_seconds, threads):
+    """Time the CPU oracle's decode over a bounded sample of the workload's sequences
+    (the same inputs as the GPU run). Returns the cpu_baseline dict."""
+    import oracle
+
+    lens = st["lens"]
+    pick = list(range(len(st["host_kv"])))
+    H, G = wl.num_kv_heads, wl.group
+    maxL = max(lens[b] for b in pick)
+    oc = oracle.OracleCache(H, wl.sink, wl.window, maxL, num_slots=len(pick))
+    for i, b in enumerate(pick):
+        oc.append(i, 0, st["host_kv"][b][0], st["host_kv"][b][1])
+    qb = inputs.bf16_bits(st["q"][pick])
+    slots = np.arange(len(pick), dtype=np.int32)
+    sl = np.array([lens[b] for b in pick], np.int32)
+    used = min(threads, len(pick) * wl.num_q_heads)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oc.decode_batch(slots, sl, G, qb, 1 / math.sqrt(128), threads=used)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= cpu_seconds:
+            break
+    return {"value": float(sl.sum()) * reps / el, "unit": UNIT, "cores": used,
+            "kind": "oracle",
+            "sample": f"first {len(pick)} of {len(lens)} sequences ({int(sl.sum())} context "
+                      f"tokens, {wl.num_q_heads} q heads) x {reps} repetitions in {el:.1f} s, "
+                      f"OpenMP over (sequence, q head); host CPU: {cpu_model()}"}
+
+
+# --------------------------------------------------------------------------- arms
+
+def run_kv4(args, rank, world, local):
+    from int8_hybrid_paged_gb300 import build as kbuild
+    from int8_hybrid_paged_gb300 import kv4
+
+    kbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = inputs.workload(args.workload)
+    seed = wl.seed + rank
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    st = build_workload(wl, seed, dev, sample_seqs=8 if want_cpu else 0)
+    cache = st["cache"]
+    B, Hq, H = wl.batch, wl.num_q_heads, wl.num_kv_heads
+    lens = st["lens"]
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    layers = wl.layers
+
+    def step():
+        for _ in range(layers):
+            kv4.kv4_decode_attention(cache.handle, st["q"], st["slots"], st["cl"], st["bt_dev"],
+                                     out, lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if cache.device_error():
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    kv4.kv4_profile_start(cache.handle, args.steps * layers)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    prof = kv4.kv4_profile_stop(cache.handle)
+    clk = clocks.stop()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    if cache.device_error():
+        raise RuntimeError("device error during the timed region")
+
+    tokens_step = float(sum(lens)) * layers
+    t_max, tok_sum = reduce_max_sum(world, ms, tokens_step * args.steps, dev)
+    value = tok_sum / (t_max * 1e-3)
+
+    call_bytes = bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
+    split_bytes = call_bytes - B * Hq * (128 * 4 + 4)        # outputs are written by the merge
+    split_ms = prof["split_ms"] / max(1, prof["calls"])
+    peak, peak_src = measured_peaks()
+    achieved = split_bytes / (split_ms * 1e-3) / 1e9
+    traffic = split_kernel_traffic()
+    step_gbs = call_bytes * layers / (ms / args.steps * 1e-3) / 1e9
+
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+        "data": "synthetic (seeded bf16 N(0,1) K/V/q, 4 K outlier channels x20, lognormal lengths)",
+        "config": {"workload": wl.name, "batch": B, "q_heads": Hq, "kv_heads": H,
+                   "head_dim": 128, "page_size": 16, "sink": wl.sink, "window": wl.window,
+                   "layers": layers, "context_tokens_per_step": int(tokens_step),
+                   "max_context": max(lens), "pool_pages": st["num_pages"],
+                   "l2": f"inputs larger than L2: {call_bytes / 1e9:.2f} GB read per call "
+                         f"vs {L2_BYTES / 2**20:.0f} MiB L2, no flush",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "achieved_hbm_gbs": step_gbs,
+        "pct_hbm_peak": 100.0 * step_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": "kv4_decode_split_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": split_bytes,
+                     "avg_launch_ms": split_ms,
+                     "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
+                     "plan_ms": prof["plan_ms"] / max(1, prof["calls"]),
+                     "merge_ms": prof["merge_ms"] / max(1, prof["calls"])},
+        "gpu_launches": 3 * args.steps * layers,
+        "clocks": clk,
+    }
+
+    # ---- end to end through the public API from pinned host buffers
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(st, wl, args, dev, world)
+
+    # ---- CPU oracle baseline (rank 0, one GPU)
+    if want_cpu:
+        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores())
+    cache.close()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+def run_e2e(st, wl, args, dev, world):
+    from int8_hybrid_paged_gb300 import kv4
+
+    cache = st["cache"]
+    B, Hq = wl.batch, wl.num_q_heads
+    q_h = st["q"].cpu().pin_memory()
+    cl_h = st["cl"].cpu().pin_memory()
+    sl_h = st["slots"].cpu().pin_memory()
+    bt_h = st["bt_dev"].cpu().pin_memory()
+    out_h = torch.empty((B, Hq, 128), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(st["q"])
+    cl_d = torch.empty_like(st["cl"])
+    sl_d = torch.empty_like(st["slots"])
+    bt_d = torch.empty_like(st["bt_dev"])
+    out_d = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(1, min(args.steps, 500))
+
+    def step():
+        q_d.copy_(q_h, non_blocking=True)
+        cl_d.copy_(cl_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        for _ in range(wl.layers):
+            kv4.kv4_decode_attention(cache.handle, q_d, sl_d, cl_d, bt_d, out_d, None,
+                                     stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(min(args.warmup, 5) + 1):
+        step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    el = time.perf_counter() - t0
+    t_max, tok = reduce_max_sum(world, el, float(sum(st["lens"])) * wl.layers * n, dev)
+    h2d = q_h.numel() * 2 + cl_h.numel() * 4 + sl_h.numel() * 4 + bt_h.numel() * 4
+    d2h = out_h.numel() * 4
+    return {"value": tok / t_max, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": n,
+            "how": "pinned host q, context_lens, slot_ids, block_table copied in and the fp32 "
+                   "output copied out every step, host-synchronised, wall clock"}
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle on the host cores, each step a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.load()
+    wl = inputs.workload(args.workload)
+    lens = list(wl.context_lens)
+    H, G, Hq = wl.num_kv_heads, wl.group, wl.num_q_heads
+    threads = host_cores()
+    # budget per step so that warm-up + steps stay near two minutes
+    per_step_s = min(2.0, 120.0 / max(1, args.steps + args.warmup))
+    # calibrate on the first sequence, then size the per-step sample
+    kv = {}
+
+    def seq(b):
+        if b not in kv:
+            k, v = inputs.sequence_kv(b, lens[b], H, wl.seed)
+            kv[b] = (inputs.bf16_bits(k), inputs.bf16_bits(v))
+        return kv[b]
+
+    qb = inputs.bf16_bits(inputs.queries(wl.batch, Hq, wl.seed))
+
+    def make(nseq):
+        oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq)
+        for i in range(nseq):
+            oc.append(i, 0, *seq(i))
+        return oc
+
+    oc = make(1)
+    t0 = time.perf_counter()
+    oc.decode_batch(np.zeros(1, np.int32), np.array(lens[:1], np.int32), G, qb[:1],
+                    1 / math.sqrt(128), threads=threads)
+    t1 = max(1e-4, time.perf_counter() - t0)
+    nseq = int(max(1, min(wl.batch, 64, per_step_s / t1)))
+    oc = make(nseq)
+    slots = np.arange(nseq, dtype=np.int32)
+    sl = np.array(lens[:nseq], np.int32)
+
+    def step():
+        oc.decode_batch(slots, sl, G, qb[:nseq], 1 / math.sqrt(128), threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = float(sl.sum()) * args.steps / el
+    sample = (f"{nseq} of {len(lens)} sequences per step ({int(sl.sum())} context tokens, "
+              f"{Hq} q heads), OpenMP over sequences, host CPU: {cpu_model()}")
+    res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "fp32/fp64 (CPU oracle)", "data": "synthetic",
+           "config": {"workload": wl.name, "batch": wl.batch, "q_heads": Hq, "kv_heads": H},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_kv4(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -65,7 +65,7 @@ typedef struct {
     int64_t num_pages;       /* physical pages in the INT4 pool (each holds 16 positions of every KV head) */
     int32_t max_slots;       /* sequences that own a side buffer (slot ids are 0 .. max_slots-1) */
     int32_t max_batch;       /* largest batch of one decode call */
-    int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4, 8}) */
+    int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
     int32_t max_work_items;  /* split-K partials kept by the decode workspace; 0 = a default that
                                 fits max_batch (at least 3 * max_batch * H_kv) */
 } kv4_cache_config;
@@ -181,6 +181,22 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
                                       int batch, float sm_scale, float *out_dev, float *lse_dev,
                                       int8_t *q8_dev, float *q_scale_dev, int32_t *qk_dev,
                                       uint8_t *w_hat_dev, int debug_stride, void *stream);
+
+/* Per-kernel device time of decode calls, from CUDA events recorded around each
+ * of the three decode launches on the caller's stream while profiling is on. */
+typedef struct {
+    int32_t calls;       /* decode calls recorded */
+    float plan_ms;       /* summed device time of the plan kernel */
+    float split_ms;      /* summed device time of the split-K attention kernel */
+    float merge_ms;      /* summed device time of the merge kernel */
+} kv4_profile;
+
+/* Start recording events around the next max_calls decode calls of this cache
+ * (creates 4 * max_calls CUDA events; no device memory). */
+kv4_status kv4_profile_start(kv4_cache *cache, int max_calls);
+
+/* Stop recording, wait for the recorded events and return the summed times. */
+kv4_status kv4_profile_stop(kv4_cache *cache, kv4_profile *out);
 
 /* Read (synchronously: waits for the device) and optionally clear the device
  * error word. *code receives a kv4_device_error value. Returns KV4_OK. */

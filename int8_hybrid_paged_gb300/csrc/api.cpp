@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "kv4_internal.h"
 
@@ -28,6 +29,11 @@ struct kv4_cache {
     float2* part_ml = nullptr;
     int32_t max_items = 0;
     int32_t max_group = 0;
+    // profiling: 4 events per recorded decode call
+    std::vector<cudaEvent_t> events;
+    int prof_capacity = 0;
+    int prof_calls = 0;
+    bool profiling = false;
 };
 
 namespace {
@@ -36,8 +42,18 @@ constexpr int kItemsPerCta = 16;   // target split-K items per persistent CTA
 
 bool group_supported(int g) { return g == 1 || g == 2 || g == 4; }
 
+void drop_events(kv4_cache* c)
+{
+    for (cudaEvent_t e : c->events) cudaEventDestroy(e);
+    c->events.clear();
+    c->prof_capacity = 0;
+    c->prof_calls = 0;
+    c->profiling = false;
+}
+
 void release(kv4_cache* c)
 {
+    drop_events(c);
     cudaFree(c->pages);
     cudaFree(c->side);
     cudaFree(c->seq_len);
@@ -254,7 +270,9 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.dbg_qk = dqk;
     a.dbg_w = dw;
     a.dbg_stride = dbg_stride;
-    return check_launch(kv4::launch_decode(a, c->grid[G], static_cast<cudaStream_t>(stream)));
+    cudaEvent_t* ev = nullptr;
+    if (c->profiling && c->prof_calls < c->prof_capacity) ev = &c->events[4 * c->prof_calls++];
+    return check_launch(kv4::launch_decode(a, c->grid[G], static_cast<cudaStream_t>(stream), ev));
 }
 
 kv4_status kv4_decode_attention(kv4_cache* c, const void* q, int num_q_heads, const int32_t* slot_ids,
@@ -274,6 +292,44 @@ kv4_status kv4_decode_attention_debug(kv4_cache* c, const void* q, int num_q_hea
 {
     return decode_common(c, q, num_q_heads, slot_ids, context_lens, block_table, stride, batch,
                          sm_scale, out, lse, q8, q_scale, qk, w_hat, debug_stride, stream);
+}
+
+kv4_status kv4_profile_start(kv4_cache* c, int max_calls)
+{
+    if (!c || max_calls < 1) return KV4_ERR_INVALID_ARG;
+    drop_events(c);
+    c->events.resize((size_t)4 * max_calls, nullptr);
+    for (auto& e : c->events)
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            e = nullptr;
+            drop_events(c);
+            return KV4_ERR_CUDA;
+        }
+    c->prof_capacity = max_calls;
+    c->prof_calls = 0;
+    c->profiling = true;
+    return KV4_OK;
+}
+
+kv4_status kv4_profile_stop(kv4_cache* c, kv4_profile* out)
+{
+    if (!c || !out) return KV4_ERR_INVALID_ARG;
+    *out = kv4_profile{0, 0.f, 0.f, 0.f};
+    if (!c->profiling) return KV4_OK;
+    kv4_status st = KV4_OK;
+    for (int i = 0; i < c->prof_calls; ++i) {
+        cudaEvent_t* e = &c->events[4 * i];
+        float t[3] = {0.f, 0.f, 0.f};
+        if (cudaEventSynchronize(e[3]) != cudaSuccess) { st = KV4_ERR_CUDA; break; }
+        for (int k = 0; k < 3; ++k)
+            if (cudaEventElapsedTime(&t[k], e[k], e[k + 1]) != cudaSuccess) st = KV4_ERR_CUDA;
+        out->plan_ms += t[0];
+        out->split_ms += t[1];
+        out->merge_ms += t[2];
+        out->calls += 1;
+    }
+    drop_events(c);
+    return st;
 }
 
 kv4_status kv4_get_device_error(kv4_cache* c, int32_t* code, int clear)

@@ -689,22 +689,26 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 
 // ---------------------------------------------------------------- launchers
 template <int G, bool DEBUG>
-static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream)
+static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
+    if (ev) cudaEventRecord(ev[0], stream);
     kv4_decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+    if (ev) cudaEventRecord(ev[1], stream);
     kv4_decode_split_kernel<G, DEBUG><<<grid, kDecodeThreads, sizeof(SplitSmem), stream>>>(a);
+    if (ev) cudaEventRecord(ev[2], stream);
     const int warps = a.batch * a.num_q_heads;
     kv4_decode_merge_kernel<G><<<(warps + 3) / 4, 128, 0, stream>>>(a);
+    if (ev) cudaEventRecord(ev[3], stream);
     return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream)
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     const bool dbg = a.dbg_q8 || a.dbg_qscale || a.dbg_qk || a.dbg_w;
     switch (a.group) {
-    case 1: return dbg ? launch_g<1, true>(a, grid, stream) : launch_g<1, false>(a, grid, stream);
-    case 2: return dbg ? launch_g<2, true>(a, grid, stream) : launch_g<2, false>(a, grid, stream);
-    case 4: return dbg ? launch_g<4, true>(a, grid, stream) : launch_g<4, false>(a, grid, stream);
+    case 1: return dbg ? launch_g<1, true>(a, grid, stream, ev) : launch_g<1, false>(a, grid, stream, ev);
+    case 2: return dbg ? launch_g<2, true>(a, grid, stream, ev) : launch_g<2, false>(a, grid, stream, ev);
+    case 4: return dbg ? launch_g<4, true>(a, grid, stream, ev) : launch_g<4, false>(a, grid, stream, ev);
     default: return cudaErrorInvalidValue;
     }
 }

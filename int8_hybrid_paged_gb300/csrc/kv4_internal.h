@@ -88,7 +88,8 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream);
+// ev: null, or 4 events recorded before plan, between plan/split, split/merge, after merge.
+cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev);
 // Persistent decode CTAs that fit on one SM (occupancy of the split kernel).
 cudaError_t decode_ctas_per_sm(int group, int* ctas);
 

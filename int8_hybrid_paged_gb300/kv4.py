@@ -27,7 +27,7 @@ PAGE_SIZE = 16
 
 EXPORTED = ("kv4_cache_create", "kv4_cache_free", "kv4_cache_get_info", "kv4_append",
             "kv4_decode_attention", "kv4_decode_attention_debug", "kv4_get_device_error",
-            "kv4_status_string")
+            "kv4_status_string", "kv4_profile_start", "kv4_profile_stop")
 
 
 class KV4Error(RuntimeError):
@@ -48,6 +48,11 @@ class kv4_cache_info(C.Structure):
                 ("side_pool_dev", C.c_void_p), ("side_pool_bytes", C.c_size_t),
                 ("side_block_bytes", C.c_size_t), ("seq_len_dev", C.c_void_p),
                 ("num_sms", C.c_int32), ("decode_grid", C.c_int32), ("device", C.c_int32)]
+
+
+class kv4_profile(C.Structure):
+    _fields_ = [("calls", C.c_int32), ("plan_ms", C.c_float), ("split_ms", C.c_float),
+                ("merge_ms", C.c_float)]
 
 
 _lib = None
@@ -72,6 +77,8 @@ def load(path: str = LIB_PATH):
     lib.kv4_decode_attention.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P]
     lib.kv4_decode_attention_debug.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P, P, P, P, I, P]
     lib.kv4_get_device_error.argtypes = [P, C.POINTER(C.c_int32), I]
+    lib.kv4_profile_start.argtypes = [P, I]
+    lib.kv4_profile_stop.argtypes = [P, C.POINTER(kv4_profile)]
     for name in EXPORTED:
         getattr(lib, name).restype = C.c_int if name != "kv4_status_string" else C.c_char_p
     _lib = lib
@@ -183,6 +190,17 @@ def kv4_get_device_error(handle, clear=True) -> int:
     _check(load().kv4_get_device_error(handle, C.byref(code), 1 if clear else 0),
            "kv4_get_device_error")
     return int(code.value)
+
+
+def kv4_profile_start(handle, max_calls):
+    _check(load().kv4_profile_start(handle, int(max_calls)), "kv4_profile_start")
+
+
+def kv4_profile_stop(handle) -> dict:
+    prof = kv4_profile()
+    _check(load().kv4_profile_stop(handle, C.byref(prof)), "kv4_profile_stop")
+    return dict(calls=prof.calls, plan_ms=prof.plan_ms, split_ms=prof.split_ms,
+                merge_ms=prof.merge_ms)
 
 
 # --------------------------------------------------------------------------- convenience

@@ -532,24 +532,44 @@ int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf1
     return 0;
 }
 
-/* A batch of sequences, spread over host threads by sequence (CPU baseline). */
+/* One q head of one sequence (the unit the batch entry spreads over threads). */
+static int decode_one_head(const orc_cache *c, int slot, int L, int G, int hq,
+                           const uint16_t *q_row, float C, int pv_mode, double *out, double *lse)
+{
+    float qx[ORC_D], qr[ORC_D];
+    int8_t q8[ORC_D];
+    float q_scale;
+    int32_t q_sum;
+    load_bf16_row(q_row, qx);
+    orc_fwht128(qx, qr);
+    orc_quant_query(qr, q8, &q_scale, &q_sum);
+    decode_head(c, slot, L, hq / G, q8, q_scale, q_sum, C, pv_mode, out, lse, NULL, NULL, NULL);
+    return 0;
+}
+
+/* A batch of sequences, spread over host threads by (sequence, q head) (CPU baseline). */
 int orc_decode_batch(const orc_cache *c, int B, const int32_t *slots, const int32_t *lens,
                      int G, const uint16_t *q_bf16, float sm_scale, int pv_mode,
                      double *out, double *lse, int num_threads)
 {
     const int HG = c->num_heads * G;
-    int bad = 0;
+    const float C = log2e_scale(sm_scale);
+    for (int b = 0; b < B; b++)
+        if (slots[b] < 0 || slots[b] >= c->num_slots || lens[b] < 0 || lens[b] > c->max_len)
+            return -1;
+    if (G <= 0 || c->sink + c->window > 256) return -1;
+    const long n = (long)B * HG;
 #ifdef _OPENMP
     if (num_threads > 0) omp_set_num_threads(num_threads);
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+#pragma omp parallel for schedule(dynamic, 1)
 #endif
-    for (int b = 0; b < B; b++) {
-        int rc = orc_decode(c, slots[b], lens[b], G, q_bf16 + (size_t)b * HG * ORC_D, sm_scale,
-                            pv_mode, out + (size_t)b * HG * ORC_D, lse + (size_t)b * HG, NULL);
-        bad |= (rc != 0);
+    for (long i = 0; i < n; i++) {
+        int b = (int)(i / HG), hq = (int)(i % HG);
+        decode_one_head(c, slots[b], lens[b], G, hq, q_bf16 + ((size_t)b * HG + hq) * ORC_D, C,
+                        pv_mode, out + ((size_t)b * HG + hq) * ORC_D, lse + (size_t)b * HG + hq);
     }
     (void)num_threads;
-    return bad ? -1 : 0;
+    return 0;
 }
 
 /* Array forms of the scalar conversions, for the tests' bulk checks. */

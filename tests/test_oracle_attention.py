@@ -278,3 +278,14 @@ def test_empty_context():
     q = inputs.bf16_bits(inputs.queries(1, 2, seed=1))[0]
     out, lse, _ = c.decode(0, 0, 2, q, 0.1)
     assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_batch_entry_equals_per_sequence_calls():
+    H, G, lens = 2, 4, [300, 77, 1000, 1]
+    c, _ = make_cache(H, 16, 128, lens)
+    q = inputs.bf16_bits(inputs.queries(len(lens), H * G, seed=8))
+    o, l = c.decode_batch(np.arange(len(lens)), np.array(lens), G, q, 1 / math.sqrt(D), threads=3)
+    for b, L in enumerate(lens):
+        o1, l1, _ = c.decode(b, L, G, q[b], 1 / math.sqrt(D))
+        np.testing.assert_array_equal(o1, o[b])
+        np.testing.assert_array_equal(l1, l[b])
