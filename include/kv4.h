@@ -182,6 +182,39 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
                                       int8_t *q8_dev, float *q_scale_dev, int32_t *qk_dev,
                                       uint8_t *w_hat_dev, int debug_stride, void *stream);
 
+/*
+ * kv4_decode_attention_noalloc — the same decode attention for callers that
+ * cannot allocate device memory: for example code that runs inside a host
+ * framework whose allocator has already reserved the whole GPU for its own
+ * arena, or a plugin that is handed device buffers but has no right to call
+ * cudaMalloc itself. The paper has no counterpart of this entry point.
+ * It reads the pools through plain pointers laid out as described above (the
+ * caller may own them, or take them from kv4_cache_get_info), and it keeps its
+ * split-K scratch in a 16 MiB array that libkv4 reserves statically on every
+ * GPU that loads it, until the process exits. The call itself allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ *   config          : the cache geometry the pools were built with
+ *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
+ *   other arguments : as kv4_decode_attention
+ * Limits: batch <= 4096 and 3 * batch * H_kv <= 16 MiB / (G * 520 bytes) (for G = 4 and
+ * H_kv = 8 that is batch <= 335); larger calls return KV4_ERR_OUT_OF_RANGE before
+ * anything is enqueued. The first call on each device looks up the scratch
+ * array's device address with that device current; make that first call before
+ * any stream capture. Every call on a device shares the one array and leaves
+ * its contents behind (each call rewrites what it reads, including the work
+ * counter that must start at zero), so calls whose kernels overlap on the GPU
+ * race: issue them on one stream. Device-side index errors are skipped without
+ * a report (there is no cache error word here).
+ */
+kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
+                                        const void *page_pool_dev, const void *side_pool_dev,
+                                        const int32_t *seq_len_dev, const void *q_bf16_dev,
+                                        int num_q_heads, const int32_t *slot_ids_dev,
+                                        const int32_t *context_lens_dev,
+                                        const int32_t *block_table_dev, int block_table_stride,
+                                        int batch, float sm_scale, float *out_dev, float *lse_dev,
+                                        void *stream);
+
 /* Per-kernel device time of decode calls, from CUDA events recorded around each
  * of the three decode launches on the caller's stream while profiling is on. */
 typedef struct {

@@ -18,6 +18,8 @@
 //   merge  (warp per q head) exact log-sum-exp merge of the item partials.
 #include <float.h>
 
+#include <mutex>
+
 #include "device_common.cuh"
 #include "kv4_internal.h"
 
@@ -725,3 +727,135 @@ cudaError_t decode_ctas_per_sm(int group, int* ctas)
 }
 
 }  // namespace kv4
+
+// ---------------------------------------------------------------- decode without allocation
+// A variant of kv4_decode_attention for callers that cannot make device
+// allocations: its split-K scratch (plan header, item offsets, partial outputs)
+// lives in the file-scope array below instead of a cache-owned workspace, and it
+// reads caller-provided pools, so nothing is allocated by anyone for the call.
+// The array is reserved on every GPU that loads this library, until the process
+// exits. In host code its name is only a host-side stand-in; the kernels get its
+// device address, looked up once per device with that device current.
+namespace kv4 {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
+constexpr int kNoAllocMaxBatch = 4096;
+constexpr size_t kNoAllocHeaderBytes = 256;
+constexpr size_t kNoAllocStartBytes = ((size_t)(kNoAllocMaxBatch + 1) * 4 + 255) / 256 * 256;
+
+static __device__ __align__(256) unsigned char g_kv4_noalloc_scratch[kNoAllocScratchBytes];
+
+}  // namespace kv4
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDevice {
+    std::once_flag once;
+    unsigned char* scratch = nullptr;   // device address of g_kv4_noalloc_scratch
+    cudaError_t status = cudaSuccess;
+    int grid[5] = {0, 0, 0, 0, 0};
+};
+
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Set-up on the current device, once: resolve the scratch array's device address
+// and size the persistent grid. Allocates nothing.
+NoAllocDevice* noalloc_device(int dev)
+{
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
+    NoAllocDevice* d = &g_noalloc_dev[dev];
+    std::call_once(d->once, [d, dev]() {
+        void* p = nullptr;
+        d->status = cudaGetSymbolAddress(&p, kv4::g_kv4_noalloc_scratch);
+        if (d->status != cudaSuccess) return;
+        d->scratch = static_cast<unsigned char*>(p);
+        int sms = 0;
+        d->status = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (d->status != cudaSuccess) return;
+        for (int g = 1; g <= 4; g <<= 1) {
+            int per_sm = 0;
+            if (kv4::decode_ctas_per_sm(g, &per_sm) != cudaSuccess || per_sm < 1) per_sm = 1;
+            d->grid[g] = sms * per_sm;
+        }
+    });
+    return d;
+}
+
+}  // namespace
+
+extern "C" kv4_status kv4_decode_attention_noalloc(
+    const kv4_cache_config* cfg, const void* page_pool_dev, const void* side_pool_dev,
+    const int32_t* seq_len_dev, const void* q_bf16_dev, int num_q_heads,
+    const int32_t* slot_ids_dev, const int32_t* context_lens_dev, const int32_t* block_table_dev,
+    int block_table_stride, int batch, float sm_scale, float* out_dev, float* lse_dev, void* stream)
+{
+    using namespace kv4;
+    if (!cfg || batch < 0 || num_q_heads < 1 || block_table_stride < 0) return KV4_ERR_INVALID_ARG;
+    if (cfg->head_dim != KV4_HEAD_DIM || cfg->page_size != KV4_PAGE_SIZE) return KV4_ERR_UNSUPPORTED;
+    if (cfg->num_kv_heads < 1 || cfg->sink < 0 || cfg->window < 0 || cfg->num_pages < 1 ||
+        cfg->max_slots < 1)
+        return KV4_ERR_INVALID_ARG;
+    if (cfg->sink + cfg->window > kMaxProtected || cfg->num_pages > INT32_MAX) return KV4_ERR_UNSUPPORTED;
+    if (batch == 0) return KV4_OK;
+    if (!page_pool_dev || !side_pool_dev || !seq_len_dev || !q_bf16_dev || !slot_ids_dev ||
+        !context_lens_dev || !block_table_dev || !out_dev || block_table_stride < 1)
+        return KV4_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale) || sm_scale == INFINITY || sm_scale == -INFINITY) return KV4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q_bf16_dev) & 7) || (reinterpret_cast<uintptr_t>(out_dev) & 15) ||
+        (reinterpret_cast<uintptr_t>(page_pool_dev) & 15) || (reinterpret_cast<uintptr_t>(side_pool_dev) & 15))
+        return KV4_ERR_INVALID_ARG;
+    const int H = cfg->num_kv_heads;
+    if (num_q_heads % H != 0) return KV4_ERR_INVALID_ARG;
+    const int G = num_q_heads / H;
+    if (G != 1 && G != 2 && G != 4) return KV4_ERR_UNSUPPORTED;
+    // sizes beyond the scratch array are refused: at most 4096 sequences, and room for
+    // at least 3 * batch * H_kv partials of G heads
+    if (batch > kNoAllocMaxBatch) return KV4_ERR_OUT_OF_RANGE;
+    const size_t per_item = (size_t)G * (kHeadDim * sizeof(float) + sizeof(float2));
+    const size_t avail = kNoAllocScratchBytes - kNoAllocHeaderBytes - kNoAllocStartBytes - 256;
+    const size_t items_cap = avail / per_item;
+    if ((size_t)3 * batch * H > items_cap) return KV4_ERR_OUT_OF_RANGE;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KV4_ERR_CUDA;
+    NoAllocDevice* d = noalloc_device(dev);
+    if (!d) return KV4_ERR_UNSUPPORTED;
+    if (d->status != cudaSuccess || !d->scratch) return KV4_ERR_CUDA;
+
+    unsigned char* base = d->scratch;
+    const size_t ml_off = kNoAllocHeaderBytes + kNoAllocStartBytes;
+    const size_t o_off = ml_off + (items_cap * G * sizeof(float2) + 255) / 256 * 256;
+
+    DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(q_bf16_dev);
+    a.slot_ids = slot_ids_dev;
+    a.context_lens = context_lens_dev;
+    a.block_table = block_table_dev;
+    a.stride = block_table_stride;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.num_heads = H;
+    a.group = G;
+    a.sink = cfg->sink;
+    a.window = cfg->window;
+    a.max_slots = cfg->max_slots;
+    a.num_pages = cfg->num_pages;
+    a.log2_scale = (float)((double)sm_scale * 1.4426950408889634074);
+    a.pages = static_cast<const uint8_t*>(page_pool_dev);
+    a.side = static_cast<const uint8_t*>(side_pool_dev);
+    a.side_block_bytes = (int64_t)(((size_t)(cfg->sink + cfg->window) * 264 + 15) / 16 * 16);
+    a.seq_len = seq_len_dev;
+    a.err = nullptr;                      // no error word: device index errors are skipped silently
+    a.plan = reinterpret_cast<PlanHeader*>(base);
+    a.item_start = reinterpret_cast<int32_t*>(base + kNoAllocHeaderBytes);
+    a.part_ml = reinterpret_cast<float2*>(base + ml_off);
+    a.part_o = reinterpret_cast<float*>(base + o_off);
+    a.max_items = (int32_t)items_cap;
+    a.target_items = 16 * d->grid[G];
+    a.out = out_dev;
+    a.lse = lse_dev;
+    const cudaError_t e = launch_decode(a, d->grid[G], static_cast<cudaStream_t>(stream), nullptr);
+    return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
+}

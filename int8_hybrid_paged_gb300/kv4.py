@@ -27,7 +27,8 @@ PAGE_SIZE = 16
 
 EXPORTED = ("kv4_cache_create", "kv4_cache_free", "kv4_cache_get_info", "kv4_append",
             "kv4_decode_attention", "kv4_decode_attention_debug", "kv4_get_device_error",
-            "kv4_status_string", "kv4_profile_start", "kv4_profile_stop")
+            "kv4_status_string", "kv4_profile_start", "kv4_profile_stop",
+            "kv4_decode_attention_noalloc")
 
 
 class KV4Error(RuntimeError):
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
     lib.kv4_decode_attention_debug.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P, P, P, P, I, P]
     lib.kv4_get_device_error.argtypes = [P, C.POINTER(C.c_int32), I]
     lib.kv4_profile_start.argtypes = [P, I]
+    lib.kv4_decode_attention_noalloc.argtypes = [C.POINTER(kv4_cache_config), P, P, P, P, I, P,
+                                                 P, P, I, I, F, P, P, P]
     lib.kv4_profile_stop.argtypes = [P, C.POINTER(kv4_profile)]
     for name in EXPORTED:
         getattr(lib, name).restype = C.c_int if name != "kv4_status_string" else C.c_char_p
@@ -190,6 +193,22 @@ def kv4_get_device_error(handle, clear=True) -> int:
     _check(load().kv4_get_device_error(handle, C.byref(code), 1 if clear else 0),
            "kv4_get_device_error")
     return int(code.value)
+
+
+def kv4_decode_attention_noalloc(config, page_pool_dev, side_pool_dev, seq_len_dev, q, slot_ids,
+                                 context_lens, block_table, out, lse=None, sm_scale=None,
+                                 stream=None):
+    """Decode attention that allocates nothing (scratch in libkv4's static device array).
+    config: kv4_cache_config; the pool arguments are device addresses (ints)."""
+    B, Hq = q.shape[0], q.shape[1]
+    scale = float(HEAD_DIM ** -0.5 if sm_scale is None else sm_scale)
+    _check(load().kv4_decode_attention_noalloc(
+        C.byref(config), C.c_void_p(page_pool_dev), C.c_void_p(side_pool_dev),
+        C.c_void_p(seq_len_dev), _ptr(q, torch.bfloat16, "q"), Hq,
+        _ptr(slot_ids, torch.int32, "slot_ids"), _ptr(context_lens, torch.int32, "context_lens"),
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[-1], B, scale,
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)),
+        "kv4_decode_attention_noalloc")
 
 
 def kv4_profile_start(handle, max_calls):
