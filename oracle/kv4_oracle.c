@@ -38,9 +38,11 @@
  *      q8 = rint(q' · fl(127/max|q'|)).
  *   R4 Regions: protected = [0, min(s,L)) ∪ [max(s, L−w), L); INT4 = [s, L−w).
  *   R5 Integer PV: per page ∩ INT4 region, p' = 2^(σ − M_page) with the exp2
- *      below, w = p'·Δ^V, ŵ = min(rint(w · fl(255/max w)), 255) in 0..255,
- *      acc_j = Σ ŵ c^V_j, page output s_w·acc_j + Σ p'·m^V with s_w = max w / 255.
- *      A page whose max w is not above 2^-64 keeps only its offsets (ŵ = 0).
+ *      below, w = p'·Δ^V, and u8 weights with one power-of-two scale per page:
+ *      e = floor(log2(max w)), ŵ = min(rint(w · 2^(7−e)), 255) in 0..255 (the
+ *      largest weight lands in 128..255), acc_j = Σ ŵ c^V_j, page output
+ *      s_w·acc_j + Σ p'·m^V with s_w = 2^(e−7). A page whose max w is not above
+ *      2^-64 keeps only its offsets (ŵ = 0).
  *   R6 Scores are log2-domain: σ = fl(fl(u · s_q) · C), u = fmaf(Δ, dot, fl(m · Σq8)),
  *      C = fl(sm_scale · log2 e).
  * Everything after the integer decisions (page outputs, region merges,
@@ -422,18 +424,20 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                     for (int j = 0; j < ORC_D; j++) op[j] += (double)pp[i] * (dv * vc[j] + mv);
                 }
             } else {
-                /* pages whose largest weight is below 2^-64 contribute their
-                   offsets only: their ŵ are 0 and s_w is 0 */
+                /* u8 weights sharing the page's power-of-two scale; pages whose
+                   largest weight is below 2^-64 contribute their offsets only */
                 uint8_t wh[16];
                 int quantize = wmax > 0x1p-64f;
-                float iw = quantize ? 255.0f / wmax : 0.0f;
+                int e = 0;
+                if (quantize) frexpf(wmax, &e);      /* wmax = f·2^e, f in [0.5, 1) */
+                e -= 1;                              /* floor(log2(wmax)) */
                 for (int i = 0; i < n; i++) {
-                    float r = rintf(wv[i] * iw);
+                    float r = quantize ? rintf(ldexpf(wv[i], 7 - e)) : 0.0f;
                     if (r > 255.0f) r = 255.0f;
                     wh[i] = (uint8_t)r;
                     if (dbg_w) dbg_w[t0 + i] = wh[i];
                 }
-                double sw = quantize ? (double)wmax / 255.0 : 0.0;
+                double sw = quantize ? ldexp(1.0, e - 7) : 0.0;
                 for (int j = 0; j < ORC_D; j++) {
                     int32_t acc = 0;
                     for (int i = 0; i < n; i++) {

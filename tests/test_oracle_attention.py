@@ -164,7 +164,9 @@ def test_float_pv_equals_single_softmax(H, s, w, lens, G):
 @pytest.mark.parametrize("H,s,w,lens,G", CASES)
 def test_integer_pv_within_weight_rounding_bound(H, s, w, lens, G):
     """Integer PV differs from float PV only through ŵ: per page
-    |ŵ·s_w − p'Δ^V| ≤ s_w/2, so each output element moves by at most
+    |ŵ·s_w − p'Δ^V| ≤ s_w/2 with s_w = 2^(floor(log2 max w) − 7) (a weight that
+    rounds to 256 is held at 255, at most s_w/2 further when it is within 1 of the
+    top), so each output element moves by at most
     Σ_pages 2^(M_page−M*) (s_w/2) Σ_t c^V_tj / den (checked with 1% slack)."""
     sm = 1 / math.sqrt(D)
     c, _ = make_cache(H, s, w, lens)
@@ -184,13 +186,17 @@ def test_integer_pv_within_weight_rounding_bound(H, s, w, lens, G):
                 ts = [t for t in r4 if t // 16 == pg]
                 Mp = sig[ts].max()
                 wts = np.exp2(sig[ts] - Mp) * f16v(c.v4_delta[b, ts, h])
-                sw = wts.max() / 255
-                csum = c.v4_code[b, ts, h].astype(np.float64).sum(axis=0)
+                sw = 2.0 ** (np.floor(np.log2(wts.max())) - 7) if wts.max() > 0 else 0.0
+                codes = c.v4_code[b, ts, h].astype(np.float64)
+                csum = codes.sum(axis=0)
+                held = (wts / sw >= 255.5) if sw > 0 else np.zeros(len(ts), bool)
+                csum = csum + codes[held].sum(axis=0)          # held at 255: one more s_w/2
                 bound += 2.0 ** (Mp - Ms) * (sw / 2) * csum
             bound = bound / den * 1.01 + 1e-9
             assert np.all(np.abs(o_int[hq] - o_flt[hq]) <= bound)
-            if r4:
-                assert dbg["w_hat"][hq, r4].max() == 255      # each page's largest weight
+            for pg in sorted({t // 16 for t in r4}):
+                ts = [t for t in r4 if t // 16 == pg]
+                assert 128 <= dbg["w_hat"][hq, ts].max() <= 255    # each page's largest weight
 
 
 def test_close_to_exact_attention_on_unquantized_inputs():
