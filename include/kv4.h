@@ -66,8 +66,8 @@ typedef struct {
     int32_t max_slots;       /* sequences that own a side buffer (slot ids are 0 .. max_slots-1) */
     int32_t max_batch;       /* largest batch of one decode call */
     int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
-    int32_t max_work_items;  /* split-K partials kept by the decode workspace; 0 = a default that
-                                fits max_batch (at least 3 * max_batch * H_kv) */
+    int32_t max_work_items;  /* ignored (kept for layout stability): the decode workspace is sized
+                                from max_batch, max_q_heads and the device's SM count */
 } kv4_cache_config;
 
 /*
@@ -77,16 +77,21 @@ typedef struct {
  * the block of (page p, KV head h) starts at (p * H_kv + h) * 2176. Inside it,
  * for the 16 token slots t of the page:
  *   [0,    1024)  K codes, row t = 64 bytes; byte j = c[2j] | c[2j+1] << 4 (rotated K)
- *   [1024, 2048)  V codes, 64 dim-pair rows of 16 bytes; byte (j, t) = c_t[2j] | c_t[2j+1] << 4
+ *   [1024, 2048)  V codes: one byte per (dim pair j, token t) = c_t[2j] | c_t[2j+1] << 4, at
+ *                 offset 4*(8*(4*(j%8) + (t%8)/2) + j/8) + (2*(t%2) + t/8) (32 groups of
+ *                 eight 32-bit words; each word holds one dim pair of tokens
+ *                 2u, 2u+8, 2u+1, 2u+9 with u = (t%8)/2, one tensor-core fragment)
  *   [2048, 2112)  K metadata, t -> {fp16 delta, fp16 min} (4 bytes)
  *   [2112, 2176)  V metadata, same form
- * Side pool: max_slots * H_kv blocks of side_block_bytes = align16((s+w) * 264);
- * block (slot, h) at (slot * H_kv + h) * side_block_bytes. With S = s + w and
- * side index i (i = p for a sink position p < s, i = s + p mod w for a ring position):
- *   [0,        S*128)  INT8-grid K codes (u8, rotated K), row i = 128 bytes
- *   [S*128,    S*256)  INT8-grid V codes (u8), row i
- *   [S*256,    S*260)  K metadata {fp16 delta, fp16 min} per i
- *   [S*260,    S*264)  V metadata per i
+ * Side pool: max_slots * H_kv blocks of side_block_bytes = ceil((s+w)/16) * 4352;
+ * block (slot, h) at (slot * H_kv + h) * side_block_bytes. Side row i (i = p for a
+ * sink position p < s, i = s + p mod w for a ring position) is row i%16 of group
+ * i/16; group g starts at g * 4352 and holds, like two pages:
+ *   [0,    2048)  INT8-grid K codes (u8, rotated K) of its 16 rows, 128 bytes each
+ *   [2048, 2112)  K metadata {fp16 delta, fp16 min} per row
+ *   [2112, 2176)  V metadata per row
+ *   [2176, 4224)  INT8-grid V codes (u8) of its 16 rows
+ *   [4224, 4352)  unused
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128
@@ -95,7 +100,7 @@ typedef struct {
 
 typedef struct {
     void   *page_pool_dev;   size_t page_pool_bytes;
-    void   *side_pool_dev;   size_t side_pool_bytes;   size_t side_block_bytes;
+    void   *side_pool_dev;   size_t side_pool_bytes;   size_t side_block_bytes;   /* per (slot, head) */
     int32_t *seq_len_dev;    /* [max_slots] */
     int32_t num_sms;         /* SMs of the device the cache lives on */
     int32_t decode_grid;     /* persistent CTAs launched by decode */
@@ -196,9 +201,10 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  *   config          : the cache geometry the pools were built with
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
  *   other arguments : as kv4_decode_attention
- * Limits: batch <= 4096 and 3 * batch * H_kv <= 16 MiB / (G * 520 bytes) (for G = 4 and
- * H_kv = 8 that is batch <= 335); larger calls return KV4_ERR_OUT_OF_RANGE before
- * anything is enqueued. The first call on each device looks up the scratch
+ * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 144 bytes
+ * per q head plus G * 520 bytes for each of 2 * batch * H_kv + 4 * (persistent CTAs)
+ * partials (on a 152-SM GB300 with H_q = 32, H_kv = 8 that is batch <= 309); larger
+ * calls return KV4_ERR_OUT_OF_RANGE before anything is enqueued. The first call on each device looks up the scratch
  * array's device address with that device current; make that first call before
  * any stream capture. Every call on a device shares the one array and leaves
  * its contents behind (each call rewrites what it reads, including the work

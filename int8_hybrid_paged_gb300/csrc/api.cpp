@@ -23,11 +23,8 @@ struct kv4_cache {
     size_t side_block = 0;
     int32_t* seq_len = nullptr;
     int32_t* err = nullptr;
-    kv4::PlanHeader* plan = nullptr;
-    int32_t* item_start = nullptr;
-    float* part_o = nullptr;
-    float2* part_ml = nullptr;
-    int32_t max_items = 0;
+    unsigned char* ws = nullptr;           // decode workspace (layout: decode_workspace_bytes)
+    size_t ws_bytes = 0;
     int32_t max_group = 0;
     // profiling: 4 events per recorded decode call
     std::vector<cudaEvent_t> events;
@@ -37,8 +34,6 @@ struct kv4_cache {
 };
 
 namespace {
-
-constexpr int kItemsPerCta = 16;   // target split-K items per persistent CTA
 
 bool group_supported(int g) { return g == 1 || g == 2 || g == 4; }
 
@@ -58,10 +53,7 @@ void release(kv4_cache* c)
     cudaFree(c->side);
     cudaFree(c->seq_len);
     cudaFree(c->err);
-    cudaFree(c->plan);
-    cudaFree(c->item_start);
-    cudaFree(c->part_o);
-    cudaFree(c->part_ml);
+    cudaFree(c->ws);
 }
 
 template <typename T>
@@ -129,24 +121,16 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
     }
     const int H = cfg->num_kv_heads;
     const int S = cfg->sink + cfg->window;
-    c->side_block = ((size_t)S * 264 + 15) / 16 * 16;
+    c->side_block = (size_t)((S + 15) / 16) * kv4::kSideGroupBytes;
     c->pages_bytes = (size_t)cfg->num_pages * H * kv4::kPageBlock;
     c->side_bytes = (size_t)cfg->max_slots * H * c->side_block;
-    int64_t items = cfg->max_work_items;
-    if (items == 0)
-        items = 2LL * cfg->max_batch * H + (int64_t)kItemsPerCta * 2 * c->grid[4];
-    if (items < 3LL * cfg->max_batch * H) items = 3LL * cfg->max_batch * H;
-    if (items > INT32_MAX / 2) {
-        delete c;
-        return KV4_ERR_UNSUPPORTED;
-    }
-    c->max_items = (int32_t)items;
+    int grid_max = 0;
+    for (int g = 1; g <= 4; g <<= 1) grid_max = std::max(grid_max, c->grid[g]);
+    c->ws_bytes = kv4::decode_workspace_bytes(cfg->max_batch, cfg->max_q_heads, H, gmax, grid_max,
+                                              nullptr, nullptr);
     bool ok = alloc_zero(&c->pages, c->pages_bytes) && alloc_zero(&c->side, c->side_bytes) &&
               alloc_zero(&c->seq_len, sizeof(int32_t) * cfg->max_slots) &&
-              alloc_zero(&c->err, sizeof(int32_t)) && alloc_zero(&c->plan, sizeof(kv4::PlanHeader)) &&
-              alloc_zero(&c->item_start, sizeof(int32_t) * ((size_t)cfg->max_batch + 1)) &&
-              alloc_zero(&c->part_o, sizeof(float) * (size_t)items * gmax * kv4::kHeadDim) &&
-              alloc_zero(&c->part_ml, sizeof(float2) * (size_t)items * gmax);
+              alloc_zero(&c->err, sizeof(int32_t)) && alloc_zero(&c->ws, c->ws_bytes);
     if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
         release(c);
         delete c;
@@ -256,13 +240,15 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.side_block_bytes = (int64_t)c->side_block;
     a.seq_len = c->seq_len;
     a.err = c->err;
-    a.plan = c->plan;
-    a.item_start = c->item_start;
-    a.part_o = c->part_o;
-    a.part_ml = c->part_ml;
-    // partial buffers are laid out for this call's G: [items][G][128]
-    a.max_items = (int32_t)std::min<int64_t>(c->max_items, (int64_t)c->max_items * c->max_group / G);
-    a.target_items = kItemsPerCta * c->grid[G];
+    kv4::DecodeWorkspace ws{};
+    kv4::decode_workspace_bytes(batch, num_q_heads, H, G, c->grid[G], &ws, c->ws);
+    a.plan = ws.plan;
+    a.cost_start = ws.cost_start;
+    a.seg_start = ws.seg_start;
+    a.qinfo = ws.qinfo;
+    a.part_o = ws.part_o;
+    a.part_ml = ws.part_ml;
+    a.num_warps = c->grid[G] * (kv4::kDecodeThreads / 32);
     a.out = out;
     a.lse = lse;
     a.dbg_q8 = dq8;

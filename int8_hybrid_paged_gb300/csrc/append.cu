@@ -16,6 +16,17 @@
 
 namespace kv4 {
 
+// Byte of (dim pair j, token t) inside a page's V code block. The block is 32 lanes x
+// 8 words: word (l, m) holds pair j = 8m + (l >> 2) for tokens 2(l&3), 2(l&3)+8,
+// 2(l&3)+1, 2(l&3)+9 (bytes 0..3), so one lane's eight words are one tensor-core
+// fragment per 16-dim tile and sit in 32 contiguous bytes.
+__device__ __forceinline__ int v_byte_offset(int j, int t)
+{
+    const int tq = (t & 7) >> 1;
+    const int byte = ((t & 1) << 1) | (t >> 3);
+    return ((((j & 7) << 2) + tq) * 8 + (j >> 3)) * 4 + byte;
+}
+
 __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
 {
     const int lane = threadIdx.x & 31;
@@ -71,9 +82,9 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
     // K row ts: byte j = c[2j] | c[2j+1] << 4; this lane owns bytes 2l and 2l+1
     const uint16_t kb = (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
     *reinterpret_cast<uint16_t*>(blk + kKCodeOff + ts * 64 + 2 * lane) = kb;
-    // V dim-pair rows 2l and 2l+1, column ts
-    blk[kVCodeOff + (2 * lane) * 16 + ts] = (uint8_t)(vc[0] | (vc[1] << 4));
-    blk[kVCodeOff + (2 * lane + 1) * 16 + ts] = (uint8_t)(vc[2] | (vc[3] << 4));
+    // V dim pairs 2l and 2l+1 of token ts, at their places in the tile-interleaved layout
+    blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
     if (lane == 0) {
         *reinterpret_cast<__half2*>(blk + kKMetaOff + ts * 4) = __halves2half2(kd, km);
         *reinterpret_cast<__half2*>(blk + kVMetaOff + ts * 4) = __halves2half2(vd, vm);
@@ -90,7 +101,6 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
         __half k8d, k8m, v8d, v8m;
         warp_quant<255>(kx, k8, k8d, k8m);
         warp_quant<255>(vx, v8, v8d, v8m);
-        const int S = s + w;
         uint8_t* sb = a.side + ((int64_t)slot * a.num_heads + h) * a.side_block_bytes;
         const uint32_t kw = k8[0] | (k8[1] << 8) | (k8[2] << 16) | (k8[3] << 24);
         const uint32_t vw = v8[0] | (v8[1] << 8) | (v8[2] << 16) | (v8[3] << 24);
@@ -99,12 +109,14 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
         if (to_sink) idx[n++] = pos;
         if (to_ring) idx[n++] = s + pos % w;
         for (int k = 0; k < n; ++k) {
-            const int r = idx[k];
-            *reinterpret_cast<uint32_t*>(sb + r * 128 + 4 * lane) = kw;
-            *reinterpret_cast<uint32_t*>(sb + S * 128 + r * 128 + 4 * lane) = vw;
+            // side row r lives in group r/16: [K rows | K meta | V meta] then [V rows | pad]
+            uint8_t* g = sb + (idx[k] >> 4) * (2 * kPageBlock);
+            const int rr = idx[k] & 15;
+            *reinterpret_cast<uint32_t*>(g + kSideKCodeOff + rr * 128 + 4 * lane) = kw;
+            *reinterpret_cast<uint32_t*>(g + kSideVCodeOff + rr * 128 + 4 * lane) = vw;
             if (lane == 0) {
-                *reinterpret_cast<__half2*>(sb + S * 256 + r * 4) = __halves2half2(k8d, k8m);
-                *reinterpret_cast<__half2*>(sb + S * 260 + r * 4) = __halves2half2(v8d, v8m);
+                *reinterpret_cast<__half2*>(g + kSideKMetaOff + rr * 4) = __halves2half2(k8d, k8m);
+                *reinterpret_cast<__half2*>(g + kSideVMetaOff + rr * 4) = __halves2half2(v8d, v8m);
             }
         }
     }

@@ -1,4 +1,4 @@
-// decode.cu — kv4_decode_attention: plan, split-K-over-pages attention, exact merge.
+// decode.cu — kv4_decode_attention: prep, stream-K split attention, exact merge.
 //
 // Pages cited (title, then section):
 //   [zh] "KV4-RL:用 INT4 KV 缓存量化为 RLVR 异步 Rollout 提速" — 核心方法 (regions read in
@@ -9,13 +9,22 @@
 //        accumulation; disjoint regions merged by their log-normalizers)
 //
 // Three launches on the caller's stream:
-//   plan   (1 CTA)   per sequence: INT4 pages, chunk size, work-item prefix sums.
-//   split  (persistent, SMs × resident CTAs) each CTA takes work items from an
-//          atomic ticket: an item is (sequence b, KV head h, chunk of INT4 pages)
-//          or (b, h, protected region). Pages are staged into shared memory with
-//          1-D bulk copies on per-warp mbarrier rings; each warp streams its own
-//          pages, so no CTA-wide barrier sits inside the page loop.
-//   merge  (warp per q head) exact log-sum-exp merge of the item partials.
+//   prep   block 0 plans the call: every (sequence b, KV head h) is a run of
+//          "stage items" — its INT4 pages (one 2176-byte block each) followed by
+//          its protected unit (the side-buffer groups, two page-sized blocks per 16
+//          rows) — and the runs are laid end to end in one cost line. Every warp of
+//          the split grid gets an equal span of that line. The other blocks rotate
+//          and quantize every q head once (INT8 query, its scale, sum and widening
+//          offsets).
+//   split  persistent; each warp walks its span alone: a producer (lane 0 issues,
+//          all lanes track) keeps a 6-deep ring of 1-D bulk copies (global ->
+//          shared, mbarrier-completed) running across run boundaries, and the
+//          consumer turns INT4 pages into integer QK / integer PV on the tensor
+//          cores and protected groups into INT8 QK / FP32 PV. Each run piece ends
+//          in one partial (output relative to its max, max, normalizer).
+//   merge  warp per q head: exact log-sum-exp merge of that head's partials.
+// No ticket, search or block-wide barrier sits on the data path, and the spans
+// are balanced to one run piece, whatever the length mix.
 #include <float.h>
 
 #include <mutex>
@@ -27,20 +36,24 @@ namespace kv4 {
 
 constexpr int kWarps = kDecodeThreads / 32;
 constexpr int kMaxG = 4;
-constexpr int kMinChunkPages = 16;
+
+// Per-warp query state of the current (b, h): INT8 rotated query of its G heads,
+// s_q, Σq8 and the QK widening offsets of each dim half.
+struct __align__(16) WarpQ {
+    int8_t q8[kMaxG][kHeadDim];
+    float scale[kMaxG];
+    float qsum[kMaxG];
+    float corr[kMaxG][2];
+};
 
 struct __align__(128) SplitSmem {
-    uint8_t stage[kWarps][kStages][kPageBlock];   // page staging, per warp
-    int8_t q8[kMaxG][kHeadDim];                   // INT8 rotated query of the item's heads
-    float qscale[kMaxG];
-    int32_t qsum[kMaxG];
-    uint8_t wbuf[kWarps][kMaxG][16];              // u8 PV weights of the page in flight
-    float pbuf[kWarps][kMaxG][16];                // protected-path weights of a position group
-    float wM[kWarps][kMaxG];                      // per-warp running max (log2)
-    float wL[kWarps][kMaxG];                      // per-warp normalizer
+    uint8_t stage[kWarps][kStages][kPageBlock];   // staging ring of each warp
+    WarpQ wq[kWarps];
+    union {
+        __half wsm[2][kMaxG][16];                 // u8 PV weights (as fp16) of a page pair
+        float pbuf[kMaxG][16];                    // protected weights of a 16-row group
+    } xb[kWarps];
     uint64_t bar[kWarps][kStages];
-    int32_t item;
-    int32_t abort;
 };
 
 __device__ __forceinline__ int int4_pages(int L, int s, int w)
@@ -49,283 +62,423 @@ __device__ __forceinline__ int int4_pages(int L, int s, int w)
     return (L - w > s) ? ((L - w - 1) / kPage - s / kPage + 1) : 0;
 }
 
-// ---------------------------------------------------------------- plan
-// Chunk size C (pages per item) aims at about `target_items` items in total and is
-// raised if the workspace could not hold the items otherwise:
-// items ≤ H·(T/C + 2B) ≤ max_items  ⇐  C ≥ H·T / (max_items − 2·H·B).
-__global__ void __launch_bounds__(1024) kv4_decode_plan_kernel(DecodeArgs a)
+// Stage items of a protected unit: two page-sized blocks per 16-row side group,
+// or one empty item when there is no side buffer (so every (b, h) has a unit).
+__device__ __forceinline__ int prot_items(int S) { return S > 0 ? 2 * ((S + 15) >> 4) : 1; }
+
+// Number of warp-span pieces of the INT4 pages [base, base + n) of the cost line.
+__device__ __forceinline__ int n_pieces(int base, int n, int span)
 {
-    __shared__ long long s_red[32];
-    __shared__ int s_scan[32];
-    __shared__ int s_chunk;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = a.batch, H = a.num_heads;
-    const int per = (B + 1023) / 1024;
-    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    return n > 0 ? (base + n - 1) / span - base / span + 1 : 0;
+}
 
-    long long T = 0;
-    for (int b = b0; b < b1; ++b) T += int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) T += __shfl_xor_sync(kFull, T, m);
-    if (lane == 0) s_red[warp] = T;
-    __syncthreads();
-    if (tid == 0) {
-        long long tot = 0;
-        for (int k = 0; k < 32; ++k) tot += s_red[k];
-        long long need = tot * H;
-        long long C = (need + a.target_items - 1) / max(1, a.target_items);
-        if (C < kMinChunkPages) C = kMinChunkPages;
-        const long long room = (long long)a.max_items - 2LL * H * B;
-        if (room > 0) {
-            long long Cmin = (need + room - 1) / room;
-            if (C < Cmin) C = Cmin;
-        }
-        if (C > (1 << 30)) C = 1 << 30;
-        s_chunk = (int)C;
-    }
-    __syncthreads();
-    const int C = s_chunk;
-
-    int local = 0;
-    for (int b = b0; b < b1; ++b) {
-        const int n = int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
-        local += H * ((n + C - 1) / C + 1);
-    }
-    // block-wide exclusive scan of the per-thread counts
-    int incl = local;
+// Block-wide exclusive scan over 1024 threads; returns the thread's offset and the total.
+__device__ __forceinline__ int block_scan(int v, int* s_scan, int& total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-        const int v = __shfl_up_sync(kFull, incl, m);
-        if (lane >= m) incl += v;
+        const int u = __shfl_up_sync(kFull, incl, m);
+        if (lane >= m) incl += u;
     }
     if (lane == 31) s_scan[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int v = s_scan[lane];
-        int x = v;
+        const int x0 = s_scan[lane];
+        int x = x0;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
             const int u = __shfl_up_sync(kFull, x, m);
             if (lane >= m) x += u;
         }
-        s_scan[lane] = x - v;   // exclusive offset of each warp
+        s_scan[lane] = x - x0;
+        if (lane == 31) s_scan[32] = x;
     }
     __syncthreads();
-    int off = s_scan[warp] + incl - local;
-    for (int b = b0; b < b1; ++b) {
-        a.item_start[b] = off;
-        const int n = int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
-        off += H * ((n + C - 1) / C + 1);
-    }
-    if (tid == 1023) {
-        a.item_start[B] = off;        // thread 1023 owns the last range (possibly empty)
-        a.plan->chunk_pages = C;
-        a.plan->total_items = off;
-        a.plan->counter = 0;
-    }
+    const int off = s_scan[warp] + incl - v;
+    total = s_scan[32];
+    __syncthreads();
+    return off;
 }
 
-// ---------------------------------------------------------------- split: helpers
+// ---------------------------------------------------------------- prep
+__global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (blockIdx.x == 0) {
+        // ---- plan: cost line, spans, piece counts
+        __shared__ int s_scan[33];
+        const int B = a.batch, H = a.num_heads, s = a.sink, w = a.window;
+        const int cp = prot_items(s + w);
+        const int per = (B + 1023) / 1024;
+        const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+        int cost = 0;
+        for (int b = b0; b < b1; ++b) cost += H * (int4_pages(max(0, a.context_lens[b]), s, w) + cp);
+        int total = 0;
+        int off = block_scan(cost, s_scan, total);
+        const int span = max(1, (total + a.num_warps - 1) / a.num_warps);
+        int segs = 0;
+        for (int b = b0; b < b1; ++b) {
+            a.cost_start[b] = off;
+            const int n = int4_pages(max(0, a.context_lens[b]), s, w);
+            for (int h = 0; h < H; ++h) segs += n_pieces(off + h * (n + cp), n, span);
+            off += H * (n + cp);
+        }
+        int nseg = 0;
+        int soff = block_scan(segs, s_scan, nseg);
+        const int base = B * H;                        // protected partials come first
+        for (int b = b0; b < b1; ++b) {
+            a.seg_start[b] = base + soff;
+            const int n = int4_pages(max(0, a.context_lens[b]), s, w);
+            const int cs = a.cost_start[b];
+            for (int h = 0; h < H; ++h) soff += n_pieces(cs + h * (n + cp), n, span);
+        }
+        if (tid == 1023) {
+            a.cost_start[B] = total;
+            a.seg_start[B] = base + nseg;
+            a.plan->total_cost = total;
+            a.plan->span = span;
+            a.plan->total_items = base + nseg;
+        }
+        return;
+    }
+    // ---- query: rotate and quantize one q head per warp
+    const int gw = (blockIdx.x - 1) * 32 + warp;
+    if (gw >= a.batch * a.num_q_heads) return;
+    float x[4];
+    load_bf16x4(a.q + (int64_t)gw * kHeadDim + 4 * lane, x);
+    warp_fwht128(x, lane);
+    const float amax =
+        warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+    int q[4] = {0, 0, 0, 0};
+    float sq = 0.f;
+    if (amax > 0.f) {
+        const float inv = __fdiv_rn(127.0f, amax);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __float2int_rn(__fmul_rn(x[i], inv));
+        sq = __fdiv_rn(amax, 127.0f);
+    }
+    const int qsum = warp_sum_int(q[0] + q[1] + q[2] + q[3]);
+    // widening offsets of each dim half for the tensor-core QK: 1024·Σ q_even + 64·Σ q_odd
+    int se = q[0] + q[2], so = q[1] + q[3];
+#pragma unroll
+    for (int m = 1; m < 16; m <<= 1) {
+        se += __shfl_xor_sync(kFull, se, m);
+        so += __shfl_xor_sync(kFull, so, m);
+    }
+    const float corr = 1024.f * (float)se + 64.f * (float)so;
+    const float corr_hi = __shfl_sync(kFull, corr, 16);
+    const uint32_t packed = (uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
+                            ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24);
+    uint8_t* rec = a.qinfo + (int64_t)gw * kQInfoBytes;
+    *reinterpret_cast<uint32_t*>(rec + 4 * lane) = packed;
+    if (lane == 0)
+        *reinterpret_cast<float4*>(rec + kHeadDim) = make_float4(sq, (float)qsum, corr, corr_hi);
+    if (a.dbg_q8) *reinterpret_cast<uint32_t*>(a.dbg_q8 + (int64_t)gw * kHeadDim + 4 * lane) = packed;
+    if (a.dbg_qscale && lane == 0) a.dbg_qscale[gw] = sq;
+}
 
-// Per-warp running state of one item: o is relative to 2^M, l likewise.
-template <int G>
-struct WarpState {
-    float o[G][4];      // dims 4·lane .. 4·lane+3 of each head
-    float M[G];         // running max (log2 domain), uniform over the warp
-    float l[G];         // this lane's share of the normalizer
-    float bias[G];      // this lane's share of Σ p'·m^V (INT4 path)
+// ---------------------------------------------------------------- tensor-core integer dots
+// A 4-bit code c is widened to the fp16 value 1024 + c (low nibble) or 1024 + 16c
+// (high nibble) by one AND/OR of its 32-bit word; the INT8 query enters as fp16 q
+// (even dims, low nibbles) or q/16 (odd dims), all exactly representable. Every
+// product is exact, every partial sum an integer below 2^23, and the accumulator
+// is seeded with minus the widening offset (1024·Σq_even + 64·Σq_odd for QK,
+// 1024·Σŵ for PV), so the fp32 result is the exact integer dot.
+// QK: m16n8k16, rows = the 16 tokens of a page, 8 columns = 4 heads x 2 halves of
+// the 128 dims. PV: rows = 16 dims, k = the 16 tokens of one page, 8 columns =
+// 2 pages x 4 heads (pages are taken in pairs). No column is padding.
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1, float c0, float c1,
+                                        float c2, float c3)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2),
+          "f"(c3));
+}
+
+// nibbles 0 and 4 of w as fp16 (1024 + n0, 1024 + n4)
+__device__ __forceinline__ uint32_t wide_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+// nibbles 1 and 5 of w as fp16 (1024 + 16 n1, 1024 + 16 n5)
+__device__ __forceinline__ uint32_t wide_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
+
+__device__ __forceinline__ uint32_t half2_bits(__half lo, __half hi)
+{
+    __half2 v = __halves2half2(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// ---------------------------------------------------------------- span walker
+// Walks the stage items of one warp's span [lo, hi) of the cost line: for each
+// (b, h) touched, the INT4 pages of the span's overlap, then the protected unit
+// if its first item lies in the span (its owner takes all of it).
+struct Walk {
+    int lo, hi;
+    int b, h;
+    int L, n, cbh, csb, slot;   // of the current b
+    int k;                      // current item of (b, h): k < n INT4 page, else protected item
+    int a1;                     // end of the span's INT4 pages of (b, h)
+    bool own;                   // this span owns (b, h)'s protected unit
+    bool done;
 };
 
-template <int G>
-__device__ __forceinline__ void state_init(WarpState<G>& st)
+__device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b, int cp)
 {
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        st.M[g] = -INFINITY;
-        st.l[g] = 0.f;
-        st.bias[g] = 0.f;
-#pragma unroll
-        for (int d = 0; d < 4; ++d) st.o[g][d] = 0.f;
+    W.b = b;
+    W.L = max(0, __ldg(&a.context_lens[b]));
+    W.n = int4_pages(W.L, a.sink, a.window);
+    W.cbh = W.n + cp;
+    W.csb = __ldg(&a.cost_start[b]);
+    W.slot = __ldg(&a.slot_ids[b]);
+}
+
+// Position the walker at the first item of (b, h) inside the span; false if none.
+__device__ __forceinline__ bool walk_enter(Walk& W)
+{
+    const int base = W.csb + W.h * W.cbh;
+    const int a0 = max(W.lo, base) - base;
+    W.a1 = min(W.hi, base + W.n) - base;
+    const int pstart = base + W.n;
+    W.own = pstart >= W.lo && pstart < W.hi;
+    if (a0 < W.a1) { W.k = a0; return true; }
+    if (W.own) { W.k = W.n; return true; }
+    return false;
+}
+
+__device__ __forceinline__ void walk_next_bh(Walk& W, const DecodeArgs& a, int cp)
+{
+    for (;;) {
+        if (++W.h == a.num_heads) {
+            if (W.b + 1 >= a.batch) { W.done = true; return; }
+            walk_load_b(W, a, W.b + 1, cp);
+            W.h = 0;
+        }
+        if (W.csb + W.h * W.cbh >= W.hi) { W.done = true; return; }
+        if (walk_enter(W)) return;
     }
 }
 
-// Heads scored by a lane: with G ≥ 2 the two lanes of a token pair split the
-// heads (half 0 takes the first G/2); with G = 1 both score head 0.
+__device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, int hi, int cp)
+{
+    W.lo = lo;
+    W.hi = hi;
+    W.done = lo >= hi;
+    if (W.done) return;
+    int l = 0, r = a.batch;                          // largest b with cost_start[b] <= lo
+    while (r - l > 1) {
+        const int m = (l + r) >> 1;
+        if (__ldg(&a.cost_start[m]) <= lo) l = m; else r = m;
+    }
+    walk_load_b(W, a, l, cp);
+    W.h = min(a.num_heads - 1, (lo - W.csb) / W.cbh);
+    if (!walk_enter(W)) walk_next_bh(W, a, cp);
+}
+
+// one item forward
+__device__ __forceinline__ void walk_step(Walk& W, const DecodeArgs& a, int cp)
+{
+    if (W.k < W.n) {
+        if (++W.k < W.a1) return;
+        if (W.own) { W.k = W.n; return; }
+        walk_next_bh(W, a, cp);
+        return;
+    }
+    if (++W.k < W.n + cp) return;
+    walk_next_bh(W, a, cp);
+}
+
+// ---------------------------------------------------------------- INT4 page pair
+// Lane (g', t') = (lane >> 2, lane & 3) scores token g' + 8·(t' >> 1) of each page for
+// heads hA = 2(t' & 1), hA + 1, and accumulates output dims 16m + 2g' + {0, 1}
+// (m = 0..7) of those heads from page t' >> 1 of each pair.
+struct Int4State {
+    float o[8][2][2];
+    float M[2], l[2], bias[2];
+};
+
+template <int G, bool DEBUG>
+__device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, Int4State& st,
+                                          const uint32_t (&qb)[8][2], const float (&cq)[2],
+                                          const float (&sq)[2], const float (&qsf)[2],
+                                          const uint8_t* pg0, const uint8_t* pg1, bool two,
+                                          int lp0, int r4_hi, int b, int h, int warp, int lane)
+{
+    const int gq = lane >> 2, tq = lane & 3;
+    const int half = tq >> 1;
+    const int hd[2] = {2 * (tq & 1), 2 * (tq & 1) + 1};
+    const bool ok[2] = {hd[0] < G, hd[1] < G};
+    const unsigned hmask = (lane & 1) ? 0xAAAAAAAAu : 0x55555555u;
+    const int r4_lo = a.sink;
+    const int tok = gq + 8 * half;
+
+    // ---- integer QK of both pages
+    float sig[2][2], Mp[2][2], vdl[2], vmn[2];
+    bool val[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int pos = (lp0 + p) * kPage + tok;
+        val[p] = (p == 0 || two) && pos >= r4_lo && pos < r4_hi;
+        sig[p][0] = sig[p][1] = -INFINITY;
+        vdl[p] = vmn[p] = 0.f;
+        if (p == 0 || two) {
+            const uint8_t* pg = p ? pg1 : pg0;
+            const uint4 k0 = *reinterpret_cast<const uint4*>(pg + kKCodeOff + gq * 64 + 16 * tq);
+            const uint4 k1 = *reinterpret_cast<const uint4*>(pg + kKCodeOff + (gq + 8) * 64 + 16 * tq);
+            const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
+            const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+            float d[4] = {cq[0], cq[1], cq[0], cq[1]};
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                mma_f16(d, wide_lo(w0[ii]), wide_lo(w1[ii]), wide_hi(w0[ii]), wide_hi(w1[ii]),
+                        qb[2 * ii][0], qb[2 * ii][1], d[0], d[1], d[2], d[3]);
+                const uint32_t s0 = w0[ii] >> 8, s1 = w1[ii] >> 8;
+                mma_f16(d, wide_lo(s0), wide_lo(s1), wide_hi(s0), wide_hi(s1), qb[2 * ii + 1][0],
+                        qb[2 * ii + 1][1], d[0], d[1], d[2], d[3]);
+            }
+            // the two dim halves of each (token, head) sit in lanes t' and t' ^ 2
+            const bool lo = half == 0;
+            const float r0 = __shfl_xor_sync(kFull, lo ? d[2] : d[0], 2);
+            const float r1 = __shfl_xor_sync(kFull, lo ? d[3] : d[1], 2);
+            const float dot[2] = {(lo ? d[0] : d[2]) + r0, (lo ? d[1] : d[3]) + r1};
+            const __half2 km = *reinterpret_cast<const __half2*>(pg + kKMetaOff + tok * 4);
+            const __half2 vm = *reinterpret_cast<const __half2*>(pg + kVMetaOff + tok * 4);
+            const float kd = __low2float(km), kmin = __high2float(km);
+            vdl[p] = __low2float(vm);
+            vmn[p] = __high2float(vm);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float u = __fmaf_rn(kd, dot[j], __fmul_rn(kmin, qsf[j]));
+                if (val[p] && ok[j]) sig[p][j] = __fmul_rn(__fmul_rn(u, sq[j]), a.log2_scale);
+                if (DEBUG && val[p] && ok[j] && a.dbg_qk && pos < a.dbg_stride)
+                    a.dbg_qk[((int64_t)b * a.num_q_heads + h * G + hd[j]) * a.dbg_stride + pos] =
+                        (int)dot[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float m = sig[p][j];
+#pragma unroll
+            for (int msk = 2; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
+            Mp[p][j] = m;
+        }
+    }
+
+    // ---- running max and rescale factors
+    float alpha[2], beta[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float Mn = fmaxf(st.M[j], fmaxf(Mp[0][j], Mp[1][j]));
+        const bool none = (Mn == -INFINITY);
+        alpha[j] = none ? 1.f : (st.M[j] == -INFINITY ? 0.f : exp2_fast(st.M[j] - Mn));
+        beta[0][j] = (Mp[0][j] == -INFINITY) ? 0.f : exp2_fast(Mp[0][j] - Mn);
+        beta[1][j] = (Mp[1][j] == -INFINITY) ? 0.f : exp2_fast(Mp[1][j] - Mn);
+        st.M[j] = Mn;
+    }
+
+    // ---- page-local weights, u8 with one power-of-two scale per (page, head)
+    float Wsum[2][2], swp[2][2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const bool v = val[p] && ok[j];
+            const float pp = v ? exp2_poly(__fsub_rn(sig[p][j], Mp[p][j])) : 0.f;
+            const float wv = v ? __fmul_rn(pp, vdl[p]) : 0.f;
+            const float wmax = __uint_as_float(__reduce_max_sync(hmask, __float_as_uint(wv)));
+            int wh = 0;
+            float sw = 0.f;
+            if (wmax > 0x1p-64f) {
+                const int e = (int)(__float_as_uint(wmax) >> 23) - 127;   // floor(log2 wmax)
+                const float up = __uint_as_float((uint32_t)(134 - e) << 23);   // 2^(7-e)
+                wh = min(__float2int_rn(__fmul_rn(wv, up)), 255);
+                sw = __uint_as_float((uint32_t)(120 + e) << 23);              // 2^(e-7)
+            }
+            Wsum[p][j] = (float)__reduce_add_sync(hmask, (unsigned)wh);
+            swp[p][j] = sw;
+            sm.xb[warp].wsm[p][hd[j]][tok] = __int2half_rn(wh);
+            if (DEBUG && v && a.dbg_w) {
+                const int pos = (lp0 + p) * kPage + tok;
+                if (pos < a.dbg_stride)
+                    a.dbg_w[((int64_t)b * a.num_q_heads + h * G + hd[j]) * a.dbg_stride + pos] =
+                        (uint8_t)wh;
+            }
+            st.l[j] = (p == 0 ? st.l[j] * alpha[j] : st.l[j]) + beta[p][j] * pp;
+            st.bias[j] = (p == 0 ? st.bias[j] * alpha[j] : st.bias[j]) +
+                         beta[p][j] * (v ? pp * vmn[p] : 0.f);
+        }
+    }
+    if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+        for (int m = 0; m < 8; ++m)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                st.o[m][r][0] *= alpha[0];
+                st.o[m][r][1] *= alpha[1];
+            }
+    }
+    __syncwarp();
+
+    // ---- integer PV of both pages
+    const int pc = gq >> 2, hc = gq & 3;
+    const uint32_t wb0 = lds32(&sm.xb[warp].wsm[pc][hc][2 * tq]);
+    const uint32_t wb1 = lds32(&sm.xb[warp].wsm[pc][hc][2 * tq + 8]);
+    const uint32_t bA0 = pc == 0 ? wb0 : 0u, bA1 = pc == 0 ? wb1 : 0u;
+    const uint32_t bB0 = pc == 1 ? wb0 : 0u, bB1 = pc == 1 ? wb1 : 0u;
+    const uint4 va0 = *reinterpret_cast<const uint4*>(pg0 + kVCodeOff + lane * 32);
+    const uint4 va1 = *reinterpret_cast<const uint4*>(pg0 + kVCodeOff + lane * 32 + 16);
+    uint4 vb0 = make_uint4(0, 0, 0, 0), vb1 = make_uint4(0, 0, 0, 0);
+    if (two) {
+        vb0 = *reinterpret_cast<const uint4*>(pg1 + kVCodeOff + lane * 32);
+        vb1 = *reinterpret_cast<const uint4*>(pg1 + kVCodeOff + lane * 32 + 16);
+    }
+    const uint32_t vA[8] = {va0.x, va0.y, va0.z, va0.w, va1.x, va1.y, va1.z, va1.w};
+    const uint32_t vB[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
+    // this lane's output columns belong to page `half` of the pair
+    const float W0 = half ? Wsum[1][0] : Wsum[0][0], W1 = half ? Wsum[1][1] : Wsum[0][1];
+    const float ci0 = -1024.f * W0, ci1 = -1024.f * W1;
+    const float k0 = half ? beta[1][0] * swp[1][0] : beta[0][0] * swp[0][0];
+    const float k1 = half ? beta[1][1] * swp[1][1] : beta[0][1] * swp[0][1];
+    const float k0h = k0 * 0.0625f, k1h = k1 * 0.0625f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        float c[4];
+        const uint32_t sa = vA[m] >> 8, sb = vB[m] >> 8;
+        mma_f16(c, wide_lo(vA[m]), wide_hi(vA[m]), wide_lo(sa), wide_hi(sa), bA0, bA1, ci0, ci1, ci0,
+                ci1);
+        mma_f16(c, wide_lo(vB[m]), wide_hi(vB[m]), wide_lo(sb), wide_hi(sb), bB0, bB1, c[0], c[1],
+                c[2], c[3]);
+        st.o[m][0][0] = fmaf(k0, c[0], st.o[m][0][0]);
+        st.o[m][0][1] = fmaf(k1, c[1], st.o[m][0][1]);
+        st.o[m][1][0] = fmaf(k0h, c[2], st.o[m][1][0]);
+        st.o[m][1][1] = fmaf(k1h, c[3], st.o[m][1][1]);
+    }
+    __syncwarp();
+}
+
+// ---------------------------------------------------------------- protected 16-row group
+// The side group's K block (codes, K meta, V meta) and V block sit in two stages.
+// QK: lane pair (t, half) dots row t over 64 dims with dp4a against the INT8
+// query (natural dim order); PV: lane l accumulates dims 4l..4l+3 of every head
+// from bf16-dequantized 8-bit values in FP32, with weights 2^(σ − running max).
+template <int G>
+struct ProtState {
+    float o[G][4];
+    float M[G];
+    float l[G];        // this lane's share of the normalizer
+};
+
 template <int G>
 struct HeadSplit {
     static constexpr int GL = (G >= 2) ? G / 2 : 1;
     __device__ static int head(int half, int j) { return (G >= 2) ? half * GL + j : 0; }
-    // does the lane own head gg's normalizer contribution?
     __device__ static bool owns(int half, int gg) { return (G >= 2) ? (gg / GL == half) : (half == 0); }
 };
-
-// Exchange per-lane values of the lane's own heads so every lane knows all G.
-template <int G>
-__device__ __forceinline__ void share_heads(const float (&mine)[HeadSplit<G>::GL], int half,
-                                            float (&all)[G])
-{
-    constexpr int GL = HeadSplit<G>::GL;
-    float other[GL];
-#pragma unroll
-    for (int j = 0; j < GL; ++j) other[j] = __shfl_xor_sync(kFull, mine[j], 1);
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-        if (G >= 2) {
-            const int jj = gg % GL, hh = gg / GL;
-            all[gg] = (hh == half) ? mine[jj] : other[jj];
-        } else {
-            all[gg] = mine[0];
-        }
-    }
-}
-
-// max over the 16 token lanes of the same half (lane bits 1..4)
-__device__ __forceinline__ float token_max(float v)
-{
-#pragma unroll
-    for (int m = 2; m < 32; m <<= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, m));
-    return v;
-}
-
-template <int G>
-__device__ __forceinline__ int pick(const int (&v)[G], int g)
-{
-    int r = v[0];
-#pragma unroll
-    for (int gg = 1; gg < G; ++gg)
-        if (gg == g) r = v[gg];
-    return r;
-}
-
-// ---------------------------------------------------------------- split: INT4 page
-// One staged page (16 positions) against the item's G query heads.
-// QK: lane pair (t, half) covers token t; each lane dots 64 dims (8 words of 8
-// codes) against the matching query bytes with dp4a, the pair sums by shuffle.
-// PV: lane l owns dims 4l..4l+3; the u8 weights of all 16 tokens are broadcast
-// from shared memory and dotted with 4-token code words.
-template <int G, bool DEBUG>
-__device__ __forceinline__ void int4_page(const DecodeArgs& a, SplitSmem& sm, WarpState<G>& st,
-                                          const uint8_t* pg, int lp, int r4_lo, int r4_hi,
-                                          const uint32_t (&qlo)[G][8], const uint32_t (&qhi)[G][8],
-                                          const float (&qs)[G], const float (&qsumf)[G],
-                                          int b, int h, int warp, int lane)
-{
-    using HS = HeadSplit<G>;
-    constexpr int GL = HS::GL;
-    const int t = lane >> 1, half = lane & 1;
-
-    // ---- integer QK
-    const uint4 ka = *reinterpret_cast<const uint4*>(pg + kKCodeOff + t * 64 + half * 32);
-    const uint4 kb = *reinterpret_cast<const uint4*>(pg + kKCodeOff + t * 64 + half * 32 + 16);
-    const uint32_t kw[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
-    int dot[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) dot[g] = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t lo = kw[i] & 0x0F0F0F0Fu;
-        const uint32_t hi = (kw[i] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            dot[g] = dp4a_su(qlo[g][i], lo, dot[g]);
-            dot[g] = dp4a_su(qhi[g][i], hi, dot[g]);
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) dot[g] += __shfl_xor_sync(kFull, dot[g], 1);
-
-    const int pos = lp * kPage + t;
-    const bool valid = pos >= r4_lo && pos < r4_hi;
-    const __half2 kmeta = *reinterpret_cast<const __half2*>(pg + kKMetaOff + t * 4);
-    const __half2 vmeta = *reinterpret_cast<const __half2*>(pg + kVMetaOff + t * 4);
-    const float kd = __low2float(kmeta), kmin = __high2float(kmeta);
-    const float vd = __low2float(vmeta), vmin = __high2float(vmeta);
-
-    // ---- scores, page max, page-local weights, u8 quantization (lane's own heads)
-    float pmax[GL], wmx[GL], pp[GL];
-#pragma unroll
-    for (int j = 0; j < GL; ++j) {
-        const int g = HS::head(half, j);
-        const int d = pick<G>(dot, g);
-        float sqg = qs[0], qsg = qsumf[0];
-#pragma unroll
-        for (int gg = 1; gg < G; ++gg)
-            if (gg == g) { sqg = qs[gg]; qsg = qsumf[gg]; }
-        const float u = __fmaf_rn(kd, (float)d, __fmul_rn(kmin, qsg));
-        const float sig = valid ? __fmul_rn(__fmul_rn(u, sqg), a.log2_scale) : -INFINITY;
-        const float Mp = token_max(sig);
-        const float p = valid ? exp2_poly(__fsub_rn(sig, Mp)) : 0.f;
-        const float wv = valid ? __fmul_rn(p, vd) : 0.f;
-        const float wmax = token_max(wv);
-        const bool qz = wmax > 0x1p-64f;
-        const float iw = qz ? __fdiv_rn(255.f, wmax) : 0.f;
-        int wh = 0;
-        if (valid && qz) wh = min(__float2int_rn(__fmul_rn(wv, iw)), 255);
-        if (G >= 2 || half == 0) sm.wbuf[warp][g][t] = (uint8_t)wh;
-        if (DEBUG && valid && pos < a.dbg_stride && (G >= 2 || half == 0)) {
-            const int64_t o = ((int64_t)b * a.num_q_heads + h * G + g) * a.dbg_stride + pos;
-            if (a.dbg_qk) a.dbg_qk[o] = d;
-            if (a.dbg_w) a.dbg_w[o] = (uint8_t)wh;
-        }
-        pmax[j] = Mp;
-        wmx[j] = qz ? __fmul_rn(wmax, 1.0f / 255.0f) : 0.f;
-        pp[j] = p;
-    }
-    float Mall[G], swall[G];
-    share_heads<G>(pmax, half, Mall);
-    share_heads<G>(wmx, half, swall);
-
-    // ---- rescale factors; normalizer and offset-term shares of this lane
-    float alpha[G], scale[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float Mn = fmaxf(st.M[g], Mall[g]);
-        const bool none = (Mn == -INFINITY);            // no valid position yet
-        alpha[g] = none ? 1.f : exp2_fast(st.M[g] - Mn);
-        const float beta = none ? 0.f : exp2_fast(Mall[g] - Mn);
-        scale[g] = beta * swall[g];
-        st.M[g] = Mn;
-        float contrib = 0.f;
-        if (HS::owns(half, g)) contrib = pp[(G >= 2) ? g % GL : 0];
-        st.l[g] = st.l[g] * alpha[g] + beta * contrib;
-        st.bias[g] = st.bias[g] * alpha[g] + beta * (valid ? contrib * vmin : 0.f);
-    }
-    __syncwarp();
-
-    // ---- integer PV
-    uint32_t W[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const uint4 wq = *reinterpret_cast<const uint4*>(&sm.wbuf[warp][g][0]);
-        W[g][0] = wq.x; W[g][1] = wq.y; W[g][2] = wq.z; W[g][3] = wq.w;
-    }
-    const uint4 va = *reinterpret_cast<const uint4*>(pg + kVCodeOff + lane * 32);
-    const uint4 vb = *reinterpret_cast<const uint4*>(pg + kVCodeOff + lane * 32 + 16);
-    const uint32_t v0[4] = {va.x, va.y, va.z, va.w};   // dim pair 2l, token quads 0..3
-    const uint32_t v1[4] = {vb.x, vb.y, vb.z, vb.w};   // dim pair 2l+1
-    int acc[G][4];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int d = 0; d < 4; ++d) acc[g][d] = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t lo0 = v0[k] & 0x0F0F0F0Fu, hi0 = (v0[k] >> 4) & 0x0F0F0F0Fu;
-        const uint32_t lo1 = v1[k] & 0x0F0F0F0Fu, hi1 = (v1[k] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            acc[g][0] = dp4a_uu(lo0, W[g][k], acc[g][0]);
-            acc[g][1] = dp4a_uu(hi0, W[g][k], acc[g][1]);
-            acc[g][2] = dp4a_uu(lo1, W[g][k], acc[g][2]);
-            acc[g][3] = dp4a_uu(hi1, W[g][k], acc[g][3]);
-        }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int d = 0; d < 4; ++d) st.o[g][d] = fmaf(scale[g], (float)acc[g][d], st.o[g][d] * alpha[g]);
-    __syncwarp();
-}
 
 template <int G>
 __device__ __forceinline__ float pickf(const float (&v)[G], int g)
@@ -337,75 +490,82 @@ __device__ __forceinline__ float pickf(const float (&v)[G], int g)
     return r;
 }
 
-// ---------------------------------------------------------------- split: protected group
-// 16 protected positions (group `grp`) against the item's G heads. The same INT8
-// query meets the 8-bit side keys (natural dim order, query bytes broadcast from
-// shared memory); side values are dequantized to bf16 and accumulated in FP32.
+// Position held by side row rr at context length L, or -1 if the row is not in
+// the protected set [0, min(s, L)) ∪ [max(s, L - w), L).
+__device__ __forceinline__ int side_row_position(int rr, int s, int w, int L)
+{
+    if (rr < s) return rr < L ? rr : -1;
+    if (rr >= s + w || L <= 0) return -1;
+    const int k = rr - s;
+    const int d = ((L - 1 - k) % w + w) % w;        // the latest position p < L with p mod w = k
+    const int p = L - 1 - d;
+    return p >= s ? p : -1;
+}
+
 template <int G, bool DEBUG>
-__device__ __forceinline__ void protected_group(const DecodeArgs& a, SplitSmem& sm,
-                                                WarpState<G>& st, const uint8_t* sb, int S,
-                                                int grp, int npos, int n_sink, int ring_lo,
-                                                const float (&qs)[G], const float (&qsumf)[G],
-                                                int b, int h, int warp, int lane)
+__device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, ProtState<G>& st,
+                                           const uint8_t* pk, const uint8_t* pv, int grp, int L,
+                                           int b, int h, int warp, int lane)
 {
     using HS = HeadSplit<G>;
     constexpr int GL = HS::GL;
     const int t = lane >> 1, half = lane & 1;
     const int s = a.sink, w = a.window;
-    const int k = grp * 16 + t;
-    const bool valid = k < npos;
-    int tpos = 0, sidx = 0;
-    if (valid) {
-        tpos = (k < n_sink) ? k : ring_lo + (k - n_sink);
-        sidx = (tpos < s) ? tpos : s + tpos % w;
-    }
+    const int pos = side_row_position(grp * 16 + t, s, w, L);
+    const bool valid = pos >= 0;
+    const WarpQ& wq = sm.wq[warp];
+
     int dot[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) dot[g] = 0;
-    if (valid) {
-        const uint4* kr = reinterpret_cast<const uint4*>(sb + sidx * 128 + half * 64);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const uint4 c4 = __ldg(kr + q4);
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const uint4 c4 = *reinterpret_cast<const uint4*>(pk + kSideKCodeOff + t * 128 + half * 64 + q4 * 16);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const uint4 qv = *reinterpret_cast<const uint4*>(&sm.q8[g][half * 64 + q4 * 16]);
-                dot[g] = dp4a_su(qv.x, c4.x, dot[g]);
-                dot[g] = dp4a_su(qv.y, c4.y, dot[g]);
-                dot[g] = dp4a_su(qv.z, c4.z, dot[g]);
-                dot[g] = dp4a_su(qv.w, c4.w, dot[g]);
-            }
+        for (int g = 0; g < G; ++g) {
+            const uint4 qv = *reinterpret_cast<const uint4*>(&wq.q8[g][half * 64 + q4 * 16]);
+            dot[g] = dp4a_su(qv.x, c4.x, dot[g]);
+            dot[g] = dp4a_su(qv.y, c4.y, dot[g]);
+            dot[g] = dp4a_su(qv.z, c4.z, dot[g]);
+            dot[g] = dp4a_su(qv.w, c4.w, dot[g]);
         }
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) dot[g] += __shfl_xor_sync(kFull, dot[g], 1);
+    const __half2 km = *reinterpret_cast<const __half2*>(pk + kSideKMetaOff + t * 4);
+    const float kd = __low2float(km), kmin = __high2float(km);
 
-    float kd = 0.f, kmin = 0.f;
-    if (valid) {
-        const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(sb + S * 256 + sidx * 4));
-        const __half2 km = *reinterpret_cast<const __half2*>(&mw);
-        kd = __low2float(km);
-        kmin = __high2float(km);
-    }
     float sig[GL], gmax[GL];
 #pragma unroll
     for (int j = 0; j < GL; ++j) {
         const int g = HS::head(half, j);
-        const int d = pick<G>(dot, g);
-        const float sqg = pickf<G>(qs, g), qsg = pickf<G>(qsumf, g);
-        const float u = __fmaf_rn(kd, (float)d, __fmul_rn(kmin, qsg));
-        sig[j] = valid ? __fmul_rn(__fmul_rn(u, sqg), a.log2_scale) : -INFINITY;
-        gmax[j] = token_max(sig[j]);
-        if (DEBUG && valid && a.dbg_qk && tpos < a.dbg_stride && (G >= 2 || half == 0))
-            a.dbg_qk[((int64_t)b * a.num_q_heads + h * G + g) * a.dbg_stride + tpos] = d;
+        int d = dot[0];
+#pragma unroll
+        for (int gg = 1; gg < G; ++gg)
+            if (gg == g) d = dot[gg];
+        const float u = __fmaf_rn(kd, (float)d, __fmul_rn(kmin, wq.qsum[g]));
+        sig[j] = valid ? __fmul_rn(__fmul_rn(u, wq.scale[g]), a.log2_scale) : -INFINITY;
+        float m = sig[j];
+#pragma unroll
+        for (int msk = 2; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
+        gmax[j] = m;
+        if (DEBUG && valid && a.dbg_qk && pos < a.dbg_stride && (G >= 2 || half == 0))
+            a.dbg_qk[((int64_t)b * a.num_q_heads + h * G + g) * a.dbg_stride + pos] = d;
     }
     float Mall[G];
-    share_heads<G>(gmax, half, Mall);
+    {
+        float other[GL];
+#pragma unroll
+        for (int j = 0; j < GL; ++j) other[j] = __shfl_xor_sync(kFull, gmax[j], 1);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg)
+            Mall[gg] = (G >= 2) ? ((gg / GL == half) ? gmax[gg % GL] : other[gg % GL]) : gmax[0];
+    }
     float alpha[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const float Mn = fmaxf(st.M[g], Mall[g]);
-        alpha[g] = (Mn == -INFINITY) ? 1.f : exp2_fast(st.M[g] - Mn);
+        alpha[g] = (Mn == -INFINITY) ? 1.f : (st.M[g] == -INFINITY ? 0.f : exp2_fast(st.M[g] - Mn));
         st.M[g] = Mn;
     }
     float p[GL];
@@ -413,7 +573,7 @@ __device__ __forceinline__ void protected_group(const DecodeArgs& a, SplitSmem& 
     for (int j = 0; j < GL; ++j) {
         const int g = HS::head(half, j);
         p[j] = valid ? exp2_poly(__fsub_rn(sig[j], pickf<G>(st.M, g))) : 0.f;
-        if (G >= 2 || half == 0) sm.pbuf[warp][g][t] = p[j];
+        if (G >= 2 || half == 0) sm.xb[warp].pbuf[g][t] = p[j];
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -423,14 +583,10 @@ __device__ __forceinline__ void protected_group(const DecodeArgs& a, SplitSmem& 
         for (int d = 0; d < 4; ++d) st.o[g][d] *= alpha[g];
     }
     __syncwarp();
-    const int n_here = min(16, npos - grp * 16);
-    for (int tt = 0; tt < n_here; ++tt) {
-        const int kk = grp * 16 + tt;
-        const int tp = (kk < n_sink) ? kk : ring_lo + (kk - n_sink);
-        const int si = (tp < s) ? tp : s + tp % w;
-        const uint32_t vcw = __ldg(reinterpret_cast<const uint32_t*>(sb + S * 128 + si * 128 + 4 * lane));
-        const uint32_t mw = __ldg(reinterpret_cast<const uint32_t*>(sb + S * 260 + si * 4));
-        const __half2 vm = *reinterpret_cast<const __half2*>(&mw);
+    for (int tt = 0; tt < 16; ++tt) {
+        if (side_row_position(grp * 16 + tt, s, w, L) < 0) continue;     // uniform
+        const uint32_t vcw = lds32(pv + (kSideVCodeOff - kPageBlock) + tt * 128 + 4 * lane);
+        const __half2 vm = *reinterpret_cast<const __half2*>(pk + kSideVMetaOff + tt * 4);
         const float vd = __low2float(vm), vmin = __high2float(vm);
         float v[4];
 #pragma unroll
@@ -439,7 +595,7 @@ __device__ __forceinline__ void protected_group(const DecodeArgs& a, SplitSmem& 
                 __float2bfloat16_rn(__fmaf_rn(vd, (float)((vcw >> (8 * m)) & 255u), vmin)));
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            const float pw = sm.pbuf[warp][g][tt];
+            const float pw = sm.xb[warp].pbuf[g][tt];
 #pragma unroll
             for (int m = 0; m < 4; ++m) st.o[g][m] = fmaf(pw, v[m], st.o[g][m]);
         }
@@ -447,210 +603,256 @@ __device__ __forceinline__ void protected_group(const DecodeArgs& a, SplitSmem& 
     __syncwarp();
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // ---------------------------------------------------------------- split kernel
 template <int G, bool DEBUG>
-__global__ void __launch_bounds__(kDecodeThreads) kv4_decode_split_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int H = a.num_heads, s = a.sink, w = a.window;
-
     if (tid == 0) {
         for (int ww = 0; ww < kWarps; ++ww)
             for (int k = 0; k < kStages; ++k) mbar_init(&sm.bar[ww][k], 1);
         fence_mbar_init();
-        sm.abort = 0;
     }
     __syncthreads();
-    uint32_t phase = 0;                    // bit k: parity awaited next on this warp's stage k
-    const int total = a.plan->total_items;
-    const int C = a.plan->chunk_pages;
 
-    for (;;) {
-        if (tid == 0) sm.item = atomicAdd(&a.plan->counter, 1);
-        __syncthreads();
-        const int item = sm.item;
-        if (item >= total || sm.abort) break;
+    const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
+    const int cp = prot_items(S), nb = (S + 15) >> 4;
+    const int total = a.plan->total_cost, span = a.plan->span;
+    const int wg = blockIdx.x * kWarps + warp;
+    const int lo = min(total, wg * span), hi = min(total, lo + span);
+    const int p_first = s / kPage;
 
-        // ---- which sequence, head and chunk
-        int lo = 0, hi = a.batch;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(&a.item_start[mid]) <= item) lo = mid; else hi = mid;
-        }
-        const int b = lo;
-        const int i0 = __ldg(&a.item_start[b]), i1 = __ldg(&a.item_start[b + 1]);
-        const int per_head = (i1 - i0) / H;
-        const int r = item - i0;
-        const int h = r / per_head, c = r - h * per_head;
-        const bool prot = (c == per_head - 1);
-        const int L = max(0, __ldg(&a.context_lens[b]));
-        const int slot = __ldg(&a.slot_ids[b]);
-        const bool slot_ok = slot >= 0 && slot < a.max_slots;
+    Walk P, Cw;
+    walk_init(P, a, lo, hi, cp);
+    Cw = P;
+    uint32_t phase = 0;                     // bit k: parity awaited next on stage k
+    int prod = 0, cons = 0;
+    int win_b = -1, win_lp = 0, win = 0;    // block-table window: entry lp = win_lp + lane
+    bool aborted = false;
 
-        // ---- rotate and quantize the item's G query heads (one warp per head)
-        if (warp < G) {
-            const int hq = h * G + warp;
-            float x[4];
-            load_bf16x4(a.q + ((int64_t)b * a.num_q_heads + hq) * kHeadDim + 4 * lane, x);
-            warp_fwht128(x, lane);
-            const float amax =
-                warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
-            int q[4] = {0, 0, 0, 0};
-            float sq = 0.f;
-            if (amax > 0.f) {
-                const float inv = __fdiv_rn(127.0f, amax);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) q[i] = __float2int_rn(__fmul_rn(x[i], inv));
-                sq = __fdiv_rn(amax, 127.0f);
-            }
-            const int qsum = warp_sum_int(q[0] + q[1] + q[2] + q[3]);
-            const uint32_t packed = (uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
-                                    ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24);
-            *reinterpret_cast<uint32_t*>(&sm.q8[warp][4 * lane]) = packed;
-            if (lane == 0) {
-                sm.qscale[warp] = sq;
-                sm.qsum[warp] = qsum;
-            }
-            if (DEBUG && prot) {
-                const int64_t o = ((int64_t)b * a.num_q_heads + hq);
-                if (a.dbg_q8) *reinterpret_cast<uint32_t*>(a.dbg_q8 + o * kHeadDim + 4 * lane) = packed;
-                if (a.dbg_qscale && lane == 0) a.dbg_qscale[o] = sq;
-            }
-        }
-        __syncthreads();
-
-        WarpState<G> st;
-        state_init<G>(st);
-        float qs[G], qsumf[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            qs[g] = sm.qscale[g];
-            qsumf[g] = (float)sm.qsum[g];
-        }
-
-        if (!prot) {
-            // ---- INT4 region [s, L - w): pages cp0 .. cp1-1, warp w takes every 4th
-            const int r4_lo = s, r4_hi = L - w;
-            const int cp0 = s / kPage + c * C;
-            const int cp1 = min(cp0 + C, (r4_hi - 1) / kPage + 1);
-            const int np = max(0, cp1 - cp0);
-            const int nl = (np > warp) ? (np - warp + kWarps - 1) / kWarps : 0;
-            uint32_t qlo[G][8], qhi[G][8];
-            {
-                const int half = lane & 1;
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int base = 64 * half + 8 * i;
-                        const uint32_t A = *reinterpret_cast<const uint32_t*>(&sm.q8[g][base]);
-                        const uint32_t B = *reinterpret_cast<const uint32_t*>(&sm.q8[g][base + 4]);
-                        qlo[g][i] = prmt(A, B, 0x6420);   // dims base+0, +2, +4, +6 (low nibbles)
-                        qhi[g][i] = prmt(A, B, 0x7531);   // dims base+1, +3, +5, +7 (high nibbles)
-                    }
-            }
-            const int64_t bt_row = (int64_t)b * a.stride;
-            const uint8_t* head_base = a.pages + (int64_t)h * kPageBlock;
-            const int64_t page_stride = (int64_t)H * kPageBlock;
-            auto issue = [&](int stg, int j) {
-                const int lp = cp0 + warp + kWarps * j;
-                int page = 0;
-                if (lp < a.stride) page = __ldg(&a.block_table[bt_row + lp]);
-                else report_error(a.err, KV4_DEVERR_BAD_POSITION);
-                if (page < 0 || (int64_t)page >= a.num_pages) {
-                    report_error(a.err, KV4_DEVERR_BAD_PAGE);
-                    page = 0;
+    // keep the ring kStages items ahead of the consumer
+    auto produce = [&]() {
+        while (!P.done && prod < cons + kStages) {
+            const int stg = prod % kStages;
+            uint64_t* bar = &sm.bar[warp][stg];
+            if (P.k < P.n) {
+                const int lp = p_first + P.k;
+                if (P.b != win_b || lp < win_lp || lp >= win_lp + 32) {
+                    win_b = P.b;
+                    win_lp = lp;
+                    const int e = lp + lane;
+                    win = (e < a.stride) ? __ldg(&a.block_table[(int64_t)P.b * a.stride + e]) : -1;
                 }
-                fence_proxy_async();
-                mbar_expect_tx(&sm.bar[warp][stg], kPageBlock);
-                bulk_g2s(sm.stage[warp][stg], head_base + (int64_t)page * page_stride, kPageBlock,
-                         &sm.bar[warp][stg]);
-            };
-            if (lane == 0)
-                for (int k = 0; k < kStages && k < nl; ++k) issue(k, k);
+                int page = __shfl_sync(kFull, win, lp - win_lp);
+                if (lane == 0) {
+                    if (lp >= a.stride) report_error(a.err, KV4_DEVERR_BAD_POSITION);
+                    else if (page < 0 || (int64_t)page >= a.num_pages) report_error(a.err, KV4_DEVERR_BAD_PAGE);
+                    if (lp >= a.stride || page < 0 || (int64_t)page >= a.num_pages) page = 0;
+                    fence_proxy_async();
+                    mbar_expect_tx(bar, kPageBlock);
+                    bulk_g2s(sm.stage[warp][stg], a.pages + ((int64_t)page * H + P.h) * kPageBlock,
+                             kPageBlock, bar);
+                }
+            } else if (S > 0) {
+                if (lane == 0) {
+                    const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
+                    fence_proxy_async();
+                    mbar_expect_tx(bar, kPageBlock);
+                    bulk_g2s(sm.stage[warp][stg],
+                             a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes +
+                                 (int64_t)(P.k - P.n) * kPageBlock,
+                             kPageBlock, bar);
+                }
+            } else if (lane == 0) {
+                mbar_arrive(bar);           // empty protected item: no side buffer
+            }
+            ++prod;
+            walk_step(P, a, cp);
+        }
+    };
+    auto wait_stage = [&](int stg) {
+        const bool okw = aborted || mbar_wait_bounded(&sm.bar[warp][stg], (phase >> stg) & 1u);
+        phase ^= 1u << stg;
+        if (!okw) {
+            if (lane == 0) report_error(a.err, KV4_DEVERR_WAIT_TIMEOUT);
+            aborted = true;
+        }
+    };
+
+    produce();
+    int q_b = -1, q_h = -1;
+    const int gq = lane >> 2, tq = lane & 3, half = tq >> 1;
+    while (!Cw.done && !aborted) {
+        const int b = Cw.b, h = Cw.h;
+        // ---- query state of (b, h) into this warp's shared memory
+        if (b != q_b || h != q_h) {
             __syncwarp();
-            for (int j = 0; j < nl; ++j) {
-                const int stg = j % kStages;
-                const bool ok = mbar_wait_bounded(&sm.bar[warp][stg], (phase >> stg) & 1u);
-                phase ^= 1u << stg;
-                if (!ok && lane == 0) {
-                    report_error(a.err, KV4_DEVERR_WAIT_TIMEOUT);
-                    sm.abort = 1;
+            const uint8_t* rec = a.qinfo + ((int64_t)b * a.num_q_heads + h * G) * kQInfoBytes;
+            if (lane < G * 8) {
+                const int g = lane >> 3, part = lane & 7;
+                *reinterpret_cast<uint4*>(&sm.wq[warp].q8[g][part * 16]) =
+                    __ldg(reinterpret_cast<const uint4*>(rec + g * kQInfoBytes + part * 16));
+            }
+            if (lane < G) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(rec + lane * kQInfoBytes + kHeadDim));
+                sm.wq[warp].scale[lane] = f.x;
+                sm.wq[warp].qsum[lane] = f.y;
+                sm.wq[warp].corr[lane][0] = f.z;
+                sm.wq[warp].corr[lane][1] = f.w;
+            }
+            __syncwarp();
+            q_b = b;
+            q_h = h;
+        }
+
+        if (Cw.k < Cw.n) {
+            // ---- INT4 run: pages first .. last-1 of (b, h)
+            const int first = Cw.k, last = Cw.a1;
+            const WarpQ& wq = sm.wq[warp];
+            uint32_t qb[8][2];
+            {
+                // column g' = head g'&3 over dim half g'>>2; k rows 2t', 2t'+1, 2t'+8, 2t'+9
+                // come from code lane t', whose dims lie in half t'>>1
+                const int bh = gq & 3;
+                const bool bok = (half == (gq >> 2)) && (bh < G);
+#pragma unroll
+                for (int st = 0; st < 8; ++st) {
+                    const int base = 32 * tq + 8 * (st >> 1) + ((st & 1) ? 2 : 0);
+                    if (bok) {
+                        const int8_t* qq = wq.q8[bh];
+                        qb[st][0] = half2_bits(__int2half_rn(qq[base]), __int2half_rn(qq[base + 4]));
+                        qb[st][1] = half2_bits(__float2half_rn(0.0625f * (float)qq[base + 1]),
+                                               __float2half_rn(0.0625f * (float)qq[base + 5]));
+                    } else {
+                        qb[st][0] = 0u;
+                        qb[st][1] = 0u;
+                    }
                 }
-                int4_page<G, DEBUG>(a, sm, st, sm.stage[warp][stg], cp0 + warp + kWarps * j, r4_lo,
-                                    r4_hi, qlo, qhi, qs, qsumf, b, h, warp, lane);
-                if (lane == 0 && j + kStages < nl) issue(stg, j + kStages);
-                __syncwarp();
             }
+            float cq[2], sq[2], qsf[2];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int hh = 2 * (tq & 1) + j;
+                const bool okh = hh < G;
+                cq[j] = okh ? -wq.corr[hh][half] : 0.f;
+                sq[j] = okh ? wq.scale[hh] : 0.f;
+                qsf[j] = okh ? wq.qsum[hh] : 0.f;
+            }
+            Int4State st;
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) st.o[m][r][0] = st.o[m][r][1] = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                st.M[j] = -INFINITY;
+                st.l[j] = 0.f;
+                st.bias[j] = 0.f;
+            }
+            const int r4_hi = Cw.L - w;
+            for (int j = first; j < last; j += 2) {
+                const bool two = j + 1 < last;
+                const int s0 = cons % kStages, s1 = (cons + 1) % kStages;
+                wait_stage(s0);
+                if (two) wait_stage(s1);
+                int4_pair<G, DEBUG>(a, sm, st, qb, cq, sq, qsf, sm.stage[warp][s0], sm.stage[warp][s1],
+                                    two, p_first + j, r4_hi, b, h, warp, lane);
+                cons += two ? 2 : 1;
+                produce();
+            }
+            // ---- partial of this piece: normalizer and offset terms over the 16 lanes of
+            // a head pair, output halves (pages of a pair) over lanes t' and t' ^ 2
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+#pragma unroll
+                for (int msk = 2; msk < 32; msk <<= 1) {
+                    st.l[j] += __shfl_xor_sync(kFull, st.l[j], msk);
+                    st.bias[j] += __shfl_xor_sync(kFull, st.bias[j], msk);
+                }
+#pragma unroll
+            for (int m = 0; m < 8; ++m)
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        st.o[m][r][j] += __shfl_xor_sync(kFull, st.o[m][r][j], 2);
+                        st.o[m][r][j] += st.bias[j];
+                    }
+            const int base = Cw.csb + h * Cw.cbh;
+            int idx = __ldg(&a.seg_start[b]) + (wg - base / span);
+            for (int hh = 0; hh < h; ++hh) idx += n_pieces(Cw.csb + hh * Cw.cbh, Cw.n, span);
+            if (tq < 2) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int hd = 2 * (tq & 1) + j;
+                    if (hd >= G) continue;
+                    float* po = a.part_o + ((int64_t)idx * G + hd) * kHeadDim;
+#pragma unroll
+                    for (int m = 0; m < 8; ++m)
+                        *reinterpret_cast<float2*>(po + 16 * m + 2 * gq) =
+                            make_float2(st.o[m][0][j], st.o[m][1][j]);
+                    if (gq == 0) a.part_ml[(int64_t)idx * G + hd] = make_float2(st.M[j], st.l[j]);
+                }
+            }
+            if (Cw.own) Cw.k = Cw.n;
+            else walk_next_bh(Cw, a, cp);
         } else {
-            // ---- protected region [0, min(s, L)) ∪ [max(s, L - w), L) from the side buffer
-            if (tid == 0) {
+            // ---- protected unit of (b, h), owned by this span
+            ProtState<G> st;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                st.M[g] = -INFINITY;
+                st.l[g] = 0.f;
+#pragma unroll
+                for (int d = 0; d < 4; ++d) st.o[g][d] = 0.f;
+            }
+            const bool slot_ok = Cw.slot >= 0 && Cw.slot < a.max_slots;
+            const int L = slot_ok ? Cw.L : 0;
+            if (lane == 0) {
                 if (!slot_ok) report_error(a.err, KV4_DEVERR_BAD_SLOT);
-                else if (L != __ldg(&a.seq_len[slot])) report_error(a.err, KV4_DEVERR_LEN_MISMATCH);
+                else if (Cw.L != __ldg(&a.seq_len[Cw.slot])) report_error(a.err, KV4_DEVERR_LEN_MISMATCH);
             }
-            const int n_sink = slot_ok ? min(s, L) : 0;
-            const int ring_lo = max(s, L - w);
-            const int n_ring = slot_ok ? max(0, L - ring_lo) : 0;
-            const int npos = n_sink + n_ring;
-            const int S = s + w;
-            const uint8_t* sb = a.side + ((int64_t)(slot_ok ? slot : 0) * H + h) * a.side_block_bytes;
-            for (int grp = warp; grp * 16 < npos; grp += kWarps)
-                protected_group<G, DEBUG>(a, sm, st, sb, S, grp, npos, n_sink, ring_lo, qs, qsumf, b,
-                                          h, warp, lane);
-        }
-
-        // ---- warp totals -> shared memory (own stage 0 is idle now)
-        float ltot[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float l = st.l[g], bb = st.bias[g];
-#pragma unroll
-            for (int m = 16; m > 0; m >>= 1) {
-                l += __shfl_xor_sync(kFull, l, m);
-                bb += __shfl_xor_sync(kFull, bb, m);
+            if (S > 0) {
+                for (int grp = 0; grp < nb; ++grp) {
+                    const int s0 = cons % kStages, s1 = (cons + 1) % kStages;
+                    wait_stage(s0);
+                    wait_stage(s1);
+                    prot_group<G, DEBUG>(a, sm, st, sm.stage[warp][s0], sm.stage[warp][s1], grp, L, b,
+                                         h, warp, lane);
+                    cons += 2;
+                    produce();
+                }
+            } else {
+                wait_stage(cons % kStages);
+                cons += 1;
+                produce();
             }
-            ltot[g] = l;
+            float* po = a.part_o + ((int64_t)(b * H + h) * G) * kHeadDim;
 #pragma unroll
-            for (int d = 0; d < 4; ++d) st.o[g][d] += bb;
-        }
-        float* red = reinterpret_cast<float*>(sm.stage[warp][0]);
+            for (int g = 0; g < G; ++g) {
+                float l = st.l[g];
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-            *reinterpret_cast<float4*>(&red[g * kHeadDim + 4 * lane]) =
-                make_float4(st.o[g][0], st.o[g][1], st.o[g][2], st.o[g][3]);
-        if (lane < G) {
-            sm.wM[warp][lane] = pickf<G>(st.M, lane);
-            sm.wL[warp][lane] = pickf<G>(ltot, lane);
-        }
-        __syncthreads();
-
-        // ---- combine the warps (thread = dim) and write the item's partial
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            float Mx = -INFINITY;
-#pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) Mx = fmaxf(Mx, sm.wM[ww][g]);
-            float acc = 0.f, lsum = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) {
-                const float Mw = sm.wM[ww][g];
-                if (Mw == -INFINITY) continue;
-                const float f = exp2_fast(Mw - Mx);
-                acc = fmaf(f, reinterpret_cast<const float*>(sm.stage[ww][0])[g * kHeadDim + tid], acc);
-                lsum = fmaf(f, sm.wL[ww][g], lsum);
+                for (int msk = 16; msk > 0; msk >>= 1) l += __shfl_xor_sync(kFull, l, msk);
+                *reinterpret_cast<float4*>(po + g * kHeadDim + 4 * lane) =
+                    make_float4(st.o[g][0], st.o[g][1], st.o[g][2], st.o[g][3]);
+                if (lane == 0) a.part_ml[(int64_t)(b * H + h) * G + g] = make_float2(st.M[g], l);
             }
-            a.part_o[((int64_t)item * G + g) * kHeadDim + tid] = acc;
-            if (tid == 0) a.part_ml[(int64_t)item * G + g] = make_float2(Mx, lsum);
+            walk_next_bh(Cw, a, cp);
         }
-        __syncthreads();
     }
 }
 
 // ---------------------------------------------------------------- merge
-// Exact log-sum-exp merge of a q head's partials: M* = max M_i,
-// O = Σ 2^(M_i − M*) o_i / Σ 2^(M_i − M*) l_i, lse = (M* + log2 den) · ln 2.
+// Exact log-sum-exp merge of a q head's partials (its protected unit and the span
+// pieces of its INT4 pages): M* = max M_i, O = Σ 2^(M_i − M*) o_i / Σ 2^(M_i − M*) l_i,
+// lse = (M* + log2 den) · ln 2.
 template <int G>
 __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 {
@@ -659,22 +861,27 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
     if (gw >= a.batch * a.num_q_heads) return;
     const int b = gw / a.num_q_heads, hq = gw - b * a.num_q_heads;
     const int h = hq / G, g = hq - h * G;
-    const int i0 = a.item_start[b], i1 = a.item_start[b + 1];
-    const int per_head = (i1 - i0) / a.num_heads;
-    const int first = i0 + h * per_head;
+    const int H = a.num_heads, cp = prot_items(a.sink + a.window), span = a.plan->span;
+    const int n = int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
+    const int cbh = n + cp, csb = a.cost_start[b];
+    int first = a.seg_start[b];
+    for (int hh = 0; hh < h; ++hh) first += n_pieces(csb + hh * cbh, n, span);
+    const int cnt = n_pieces(csb + h * cbh, n, span);
+    auto item = [&](int k) { return k == 0 ? b * H + h : first + k - 1; };
     float Mx = -INFINITY;
-    for (int k = lane; k < per_head; k += 32) Mx = fmaxf(Mx, a.part_ml[(int64_t)(first + k) * G + g].x);
+    for (int k = lane; k <= cnt; k += 32) Mx = fmaxf(Mx, a.part_ml[(int64_t)item(k) * G + g].x);
     Mx = warp_max(Mx);
     float den = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     if (Mx != -INFINITY) {
-        for (int k = 0; k < per_head; ++k) {
-            const float2 ml = a.part_ml[(int64_t)(first + k) * G + g];
+        for (int k = 0; k <= cnt; ++k) {
+            const int it = item(k);
+            const float2 ml = a.part_ml[(int64_t)it * G + g];
             if (ml.x == -INFINITY) continue;
             const float f = exp2f(ml.x - Mx);
             den = fmaf(f, ml.y, den);
             const float4 v = *reinterpret_cast<const float4*>(
-                &a.part_o[((int64_t)(first + k) * G + g) * kHeadDim + 4 * lane]);
+                &a.part_o[((int64_t)it * G + g) * kHeadDim + 4 * lane]);
             o.x = fmaf(f, v.x, o.x);
             o.y = fmaf(f, v.y, o.y);
             o.z = fmaf(f, v.z, o.z);
@@ -694,7 +901,8 @@ template <int G, bool DEBUG>
 static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     if (ev) cudaEventRecord(ev[0], stream);
-    kv4_decode_plan_kernel<<<1, 1024, 0, stream>>>(a);
+    const int prep_blocks = 1 + (a.batch * a.num_q_heads + 31) / 32;
+    kv4_decode_prep_kernel<<<prep_blocks, 1024, 0, stream>>>(a);
     if (ev) cudaEventRecord(ev[1], stream);
     kv4_decode_split_kernel<G, DEBUG><<<grid, kDecodeThreads, sizeof(SplitSmem), stream>>>(a);
     if (ev) cudaEventRecord(ev[2], stream);
@@ -715,33 +923,70 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cu
     }
 }
 
+// Opt every split-kernel instantiation in to its dynamic shared memory (above the
+// 48 KB default) on the current device, then report resident CTAs per SM.
+template <int G>
+static cudaError_t split_setup(int* ctas)
+{
+    const int smem = (int)sizeof(SplitSmem);
+    cudaError_t e = cudaFuncSetAttribute(kv4_decode_split_kernel<G, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kv4_decode_split_kernel<G, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false>,
+                                                         kDecodeThreads, smem);
+}
+
 cudaError_t decode_ctas_per_sm(int group, int* ctas)
 {
-    const size_t smem = sizeof(SplitSmem);
     switch (group) {
-    case 1: return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<1, false>, kDecodeThreads, smem);
-    case 2: return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<2, false>, kDecodeThreads, smem);
-    case 4: return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<4, false>, kDecodeThreads, smem);
+    case 1: return split_setup<1>(ctas);
+    case 2: return split_setup<2>(ctas);
+    case 4: return split_setup<4>(ctas);
     default: return cudaErrorInvalidValue;
     }
+}
+
+size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int group, int grid,
+                              DecodeWorkspace* ws, unsigned char* base)
+{
+    // plan header | cost_start[B+1] | seg_start[B+1] | query records | partial (M, l) | partial o
+    auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t items = (size_t)2 * batch * num_kv_heads + (size_t)grid * kWarps;
+    size_t off = 0;
+    const size_t o_plan = off;  off = up(off + sizeof(PlanHeader));
+    const size_t o_cost = off;  off = up(off + sizeof(int32_t) * (batch + 1));
+    const size_t o_seg = off;   off = up(off + sizeof(int32_t) * (batch + 1));
+    const size_t o_q = off;     off = up(off + (size_t)kQInfoBytes * batch * num_q_heads);
+    const size_t o_ml = off;    off = up(off + sizeof(float2) * items * group);
+    const size_t o_o = off;     off = up(off + sizeof(float) * items * group * kHeadDim);
+    if (ws && base) {
+        ws->plan = reinterpret_cast<PlanHeader*>(base + o_plan);
+        ws->cost_start = reinterpret_cast<int32_t*>(base + o_cost);
+        ws->seg_start = reinterpret_cast<int32_t*>(base + o_seg);
+        ws->qinfo = base + o_q;
+        ws->part_ml = reinterpret_cast<float2*>(base + o_ml);
+        ws->part_o = reinterpret_cast<float*>(base + o_o);
+    }
+    return off;
 }
 
 }  // namespace kv4
 
 // ---------------------------------------------------------------- decode without allocation
 // A variant of kv4_decode_attention for callers that cannot make device
-// allocations: its split-K scratch (plan header, item offsets, partial outputs)
-// lives in the file-scope array below instead of a cache-owned workspace, and it
-// reads caller-provided pools, so nothing is allocated by anyone for the call.
-// The array is reserved on every GPU that loads this library, until the process
+// allocations: its workspace (plan, query records, partial outputs) lives in the
+// file-scope array below instead of a cache-owned buffer, and it reads
+// caller-provided pools, so nothing is allocated by anyone for the call. The
+// array is reserved on every GPU that loads this library, until the process
 // exits. In host code its name is only a host-side stand-in; the kernels get its
 // device address, looked up once per device with that device current.
 namespace kv4 {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
 constexpr int kNoAllocMaxBatch = 4096;
-constexpr size_t kNoAllocHeaderBytes = 256;
-constexpr size_t kNoAllocStartBytes = ((size_t)(kNoAllocMaxBatch + 1) * 4 + 255) / 256 * 256;
 
 static __device__ __align__(256) unsigned char g_kv4_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -810,24 +1055,20 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     if (num_q_heads % H != 0) return KV4_ERR_INVALID_ARG;
     const int G = num_q_heads / H;
     if (G != 1 && G != 2 && G != 4) return KV4_ERR_UNSUPPORTED;
-    // sizes beyond the scratch array are refused: at most 4096 sequences, and room for
-    // at least 3 * batch * H_kv partials of G heads
     if (batch > kNoAllocMaxBatch) return KV4_ERR_OUT_OF_RANGE;
-    const size_t per_item = (size_t)G * (kHeadDim * sizeof(float) + sizeof(float2));
-    const size_t avail = kNoAllocScratchBytes - kNoAllocHeaderBytes - kNoAllocStartBytes - 256;
-    const size_t items_cap = avail / per_item;
-    if ((size_t)3 * batch * H > items_cap) return KV4_ERR_OUT_OF_RANGE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return KV4_ERR_CUDA;
     NoAllocDevice* d = noalloc_device(dev);
     if (!d) return KV4_ERR_UNSUPPORTED;
     if (d->status != cudaSuccess || !d->scratch) return KV4_ERR_CUDA;
+    // a call whose workspace would not fit in the array is refused before anything runs
+    if (decode_workspace_bytes(batch, num_q_heads, H, G, d->grid[G], nullptr, nullptr) >
+        kNoAllocScratchBytes)
+        return KV4_ERR_OUT_OF_RANGE;
 
-    unsigned char* base = d->scratch;
-    const size_t ml_off = kNoAllocHeaderBytes + kNoAllocStartBytes;
-    const size_t o_off = ml_off + (items_cap * G * sizeof(float2) + 255) / 256 * 256;
-
+    DecodeWorkspace ws{};
+    decode_workspace_bytes(batch, num_q_heads, H, G, d->grid[G], &ws, d->scratch);
     DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q_bf16_dev);
     a.slot_ids = slot_ids_dev;
@@ -845,15 +1086,16 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.log2_scale = (float)((double)sm_scale * 1.4426950408889634074);
     a.pages = static_cast<const uint8_t*>(page_pool_dev);
     a.side = static_cast<const uint8_t*>(side_pool_dev);
-    a.side_block_bytes = (int64_t)(((size_t)(cfg->sink + cfg->window) * 264 + 15) / 16 * 16);
+    a.side_block_bytes = (int64_t)((cfg->sink + cfg->window + 15) / 16) * kSideGroupBytes;
     a.seq_len = seq_len_dev;
     a.err = nullptr;                      // no error word: device index errors are skipped silently
-    a.plan = reinterpret_cast<PlanHeader*>(base);
-    a.item_start = reinterpret_cast<int32_t*>(base + kNoAllocHeaderBytes);
-    a.part_ml = reinterpret_cast<float2*>(base + ml_off);
-    a.part_o = reinterpret_cast<float*>(base + o_off);
-    a.max_items = (int32_t)items_cap;
-    a.target_items = 16 * d->grid[G];
+    a.plan = ws.plan;
+    a.cost_start = ws.cost_start;
+    a.seg_start = ws.seg_start;
+    a.qinfo = ws.qinfo;
+    a.part_o = ws.part_o;
+    a.part_ml = ws.part_ml;
+    a.num_warps = d->grid[G] * (kDecodeThreads / 32);
     a.out = out_dev;
     a.lse = lse_dev;
     const cudaError_t e = launch_decode(a, d->grid[G], static_cast<cudaStream_t>(stream), nullptr);

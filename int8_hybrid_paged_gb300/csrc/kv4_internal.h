@@ -18,15 +18,34 @@ constexpr int kVCodeOff = 1024;          // [64 dim pairs][16 tok]
 constexpr int kKMetaOff = 2048;          // [16 tok] {fp16 delta, fp16 min}
 constexpr int kVMetaOff = 2112;
 constexpr int kMaxProtected = 256;       // s + w limit
+// Side buffer of one (slot, KV head): ceil((s+w)/16) groups of 16 rows, each two
+// page-sized blocks: [K codes 16x128 | K meta 16x4 | V meta 16x4] [V codes 16x128 | pad]
+constexpr int kSideGroupBytes = 2 * kPageBlock;
+constexpr int kSideKCodeOff = 0;
+constexpr int kSideKMetaOff = 2048;
+constexpr int kSideVMetaOff = 2112;
+constexpr int kSideVCodeOff = kPageBlock;
 constexpr int kDecodeThreads = 128;      // 4 warps per decode CTA
-constexpr int kStages = 4;               // page stages per warp
+constexpr int kStages = 6;               // page stages per warp (three page pairs)
 
-// Device-resident decode plan, written by the plan kernel, read by split/merge.
+// Device-resident decode plan, written by the prep kernel, read by split and merge.
 struct PlanHeader {
-    int32_t chunk_pages;   // INT4 pages per split work item
-    int32_t total_items;   // work items of this call
-    int32_t counter;       // dynamic work-fetch ticket
+    int32_t total_cost;    // stage items on the cost line
+    int32_t span;          // cost per warp span
+    int32_t total_items;   // partials of this call (protected units first, then span pieces)
     int32_t pad;
+};
+
+constexpr int kQInfoBytes = 144;   // per q head: 128 INT8 query bytes + {s_q, Σq8, offsets x2}
+
+// Pointers into a decode workspace (cache-owned or the static no-allocation array).
+struct DecodeWorkspace {
+    PlanHeader* plan;
+    int32_t* cost_start;   // [B+1]
+    int32_t* seg_start;    // [B+1]
+    uint8_t* qinfo;        // [B*Hq][144]
+    float2* part_ml;       // [items][G] {max (log2), normalizer}
+    float* part_o;         // [items][G][128]
 };
 
 struct AppendArgs {
@@ -71,11 +90,12 @@ struct DecodeArgs {
     int32_t* err;
     // workspace
     PlanHeader* plan;
-    int32_t* item_start;          // [B+1]
-    float* part_o;                // [max_items][G][128]
-    float2* part_ml;              // [max_items][G] {max (log2), sum}
-    int32_t max_items;
-    int32_t target_items;
+    int32_t* cost_start;
+    int32_t* seg_start;
+    uint8_t* qinfo;
+    float* part_o;
+    float2* part_ml;
+    int32_t num_warps;            // warps of the persistent split grid
     // outputs
     float* out;                   // [B][Hq][128]
     float* lse;                   // [B][Hq] or null
@@ -90,7 +110,11 @@ struct DecodeArgs {
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 // ev: null, or 4 events recorded before plan, between plan/split, split/merge, after merge.
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev);
-// Persistent decode CTAs that fit on one SM (occupancy of the split kernel).
+// Persistent decode CTAs that fit on one SM (occupancy of the split kernel); also
+// opts the kernel in to its shared memory on the current device.
 cudaError_t decode_ctas_per_sm(int group, int* ctas);
+// Bytes of a decode workspace for these sizes; with ws and base, also lays it out at base.
+size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int group, int grid,
+                              DecodeWorkspace* ws, unsigned char* base);
 
 }  // namespace kv4

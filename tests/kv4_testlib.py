@@ -24,7 +24,10 @@ def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
     k = np.empty((n, D), np.uint8)
     k[:, 0::2] = krow & 15
     k[:, 1::2] = krow >> 4
-    vbytes = pages[(base + 1024 + ts)[:, None] + (np.arange(64) * 16)[None, :]]
+    j = np.arange(64)[None, :]
+    t = ts[:, None]
+    voff = 4 * (8 * (4 * (j % 8) + (t % 8) // 2) + j // 8) + (2 * (t % 2) + t // 8)
+    vbytes = pages[base[:, None] + 1024 + voff]
     v = np.empty((n, D), np.uint8)
     v[:, 0::2] = vbytes & 15
     v[:, 1::2] = vbytes >> 4
@@ -34,11 +37,16 @@ def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
 
 
 def unpack_side(side, side_block, H, S, slot, h):
-    blk = side[(slot * H + h) * side_block:(slot * H + h) * side_block + S * 264]
-    k8 = blk[:S * 128].reshape(S, 128)
-    v8 = blk[S * 128:S * 256].reshape(S, 128)
-    km = blk[S * 256:S * 260].copy().view(np.uint16).reshape(S, 2)
-    vm = blk[S * 260:S * 264].copy().view(np.uint16).reshape(S, 2)
+    """INT8 side rows 0..S-1 of (slot, head h): 16-row groups of two 2176-byte blocks
+    ([K codes | K meta | V meta] [V codes | pad]), as declared in include/kv4.h."""
+    blk = side[(slot * H + h) * side_block:(slot * H + h + 1) * side_block]
+    r = np.arange(S)
+    g = (r // 16) * 4352
+    rr = r % 16
+    k8 = blk[(g + rr * 128)[:, None] + np.arange(128)[None, :]]
+    v8 = blk[(g + 2176 + rr * 128)[:, None] + np.arange(128)[None, :]]
+    km = blk[(g + 2048 + rr * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    vm = blk[(g + 2112 + rr * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
     return k8, v8, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
 
 

@@ -93,7 +93,7 @@ def test_noalloc_refuses_batches_beyond_its_scratch():
     st = Setup(8, 4, 16, 128, [40], seed=22)
     try:
         info = st.cache.info()
-        B = 400                                  # 3 * 400 * 8 partials do not fit in 16 MiB
+        B = 600                                  # the workspace of 600 x 32 heads exceeds 16 MiB
         q = torch.zeros((B, 32, 128), dtype=torch.bfloat16, device="cuda")
         out = torch.zeros((B, 32, 128), dtype=torch.float32, device="cuda")
         z = torch.zeros(B, dtype=torch.int32, device="cuda")
