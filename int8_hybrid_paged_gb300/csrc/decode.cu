@@ -294,132 +294,149 @@ __device__ __forceinline__ void walk_step(Walk& W, const DecodeArgs& a, int cp)
 }
 
 // ---------------------------------------------------------------- INT4 page pair
-// Lane (g', t') = (lane >> 2, lane & 3) scores token g' + 8·(t' >> 1) of each page for
-// heads hA = 2(t' & 1), hA + 1, and accumulates output dims 16m + 2g' + {0, 1}
-// (m = 0..7) of those heads from page t' >> 1 of each pair.
+// Lane (g', t') = (lane >> 2, lane & 3) scores tokens g' and g' + 8 of each page for
+// head 2(t' & 1) + (t' >> 1), and accumulates output dims 16m + 2g' + {0, 1}
+// (m = 0..7) of heads 2(t' & 1), 2(t' & 1) + 1 from page t' >> 1 of each pair.
 struct Int4State {
     float o[8][2][2];
-    float M[2], l[2], bias[2];
+    float M, l, bias;    // running max, normalizer and offset-term shares of the scored head
 };
 
 template <int G, bool DEBUG>
 __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, Int4State& st,
-                                          const uint32_t (&qb)[8][2], const float (&cq)[2],
-                                          const float (&sq)[2], const float (&qsf)[2],
-                                          const uint8_t* pg0, const uint8_t* pg1, bool two,
+                                          const uint32_t (&qb)[8][2], const float (&cq)[2], float sqh,
+                                          float qsh, const uint8_t* pg0, const uint8_t* pg1, bool two,
                                           int lp0, int r4_hi, int b, int h, int warp, int lane)
 {
     const int gq = lane >> 2, tq = lane & 3;
     const int half = tq >> 1;
-    const int hd[2] = {2 * (tq & 1), 2 * (tq & 1) + 1};
-    const bool ok[2] = {hd[0] < G, hd[1] < G};
-    const unsigned hmask = (lane & 1) ? 0xAAAAAAAAu : 0x55555555u;
+    const bool lo = half == 0;
+    const int hs = 2 * (tq & 1) + half;            // head scored by this lane
+    const bool okS = hs < G;
     const int r4_lo = a.sink;
-    const int tok = gq + 8 * half;
 
-    // ---- integer QK of both pages
-    float sig[2][2], Mp[2][2], vdl[2], vmn[2];
-    bool val[2];
+    // ---- integer QK of both pages; this lane keeps tokens gq, gq + 8 of head hs
+    float2 sig[2], vdl[2], vmn[2];
+    float Mp[2];
+    bool v0[2], v1[2];
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const int pos = (lp0 + p) * kPage + tok;
-        val[p] = (p == 0 || two) && pos >= r4_lo && pos < r4_hi;
-        sig[p][0] = sig[p][1] = -INFINITY;
-        vdl[p] = vmn[p] = 0.f;
+        const int pos0 = (lp0 + p) * kPage + gq;
+        const bool live = (p == 0 || two) && okS;
+        v0[p] = live && pos0 >= r4_lo && pos0 < r4_hi;
+        v1[p] = live && pos0 + 8 >= r4_lo && pos0 + 8 < r4_hi;
+        sig[p] = make_float2(-INFINITY, -INFINITY);
+        vdl[p] = vmn[p] = make_float2(0.f, 0.f);
         if (p == 0 || two) {
             const uint8_t* pg = p ? pg1 : pg0;
             const uint4 k0 = *reinterpret_cast<const uint4*>(pg + kKCodeOff + gq * 64 + 16 * tq);
             const uint4 k1 = *reinterpret_cast<const uint4*>(pg + kKCodeOff + (gq + 8) * 64 + 16 * tq);
             const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
             const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
-            float d[4] = {cq[0], cq[1], cq[0], cq[1]};
+            float d[4];
+            mma_f16(d, wide_lo(w0[0]), wide_lo(w1[0]), wide_hi(w0[0]), wide_hi(w1[0]), qb[0][0],
+                    qb[0][1], cq[0], cq[1], cq[0], cq[1]);
 #pragma unroll
             for (int ii = 0; ii < 4; ++ii) {
-                mma_f16(d, wide_lo(w0[ii]), wide_lo(w1[ii]), wide_hi(w0[ii]), wide_hi(w1[ii]),
-                        qb[2 * ii][0], qb[2 * ii][1], d[0], d[1], d[2], d[3]);
+                if (ii > 0)
+                    mma_f16(d, wide_lo(w0[ii]), wide_lo(w1[ii]), wide_hi(w0[ii]), wide_hi(w1[ii]),
+                            qb[2 * ii][0], qb[2 * ii][1], d[0], d[1], d[2], d[3]);
                 const uint32_t s0 = w0[ii] >> 8, s1 = w1[ii] >> 8;
                 mma_f16(d, wide_lo(s0), wide_lo(s1), wide_hi(s0), wide_hi(s1), qb[2 * ii + 1][0],
                         qb[2 * ii + 1][1], d[0], d[1], d[2], d[3]);
             }
-            // the two dim halves of each (token, head) sit in lanes t' and t' ^ 2
-            const bool lo = half == 0;
-            const float r0 = __shfl_xor_sync(kFull, lo ? d[2] : d[0], 2);
-            const float r1 = __shfl_xor_sync(kFull, lo ? d[3] : d[1], 2);
-            const float dot[2] = {(lo ? d[0] : d[2]) + r0, (lo ? d[1] : d[3]) + r1};
-            const __half2 km = *reinterpret_cast<const __half2*>(pg + kKMetaOff + tok * 4);
-            const __half2 vm = *reinterpret_cast<const __half2*>(pg + kVMetaOff + tok * 4);
-            const float kd = __low2float(km), kmin = __high2float(km);
-            vdl[p] = __low2float(vm);
-            vmn[p] = __high2float(vm);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const float u = __fmaf_rn(kd, dot[j], __fmul_rn(kmin, qsf[j]));
-                if (val[p] && ok[j]) sig[p][j] = __fmul_rn(__fmul_rn(u, sq[j]), a.log2_scale);
-                if (DEBUG && val[p] && ok[j] && a.dbg_qk && pos < a.dbg_stride)
-                    a.dbg_qk[((int64_t)b * a.num_q_heads + h * G + hd[j]) * a.dbg_stride + pos] =
-                        (int)dot[j];
+            // lanes t' and t' ^ 2 hold the two dim halves of heads 2(t'&1), 2(t'&1)+1:
+            // the low lane keeps the first head, the high lane the second
+            const float r0 = __shfl_xor_sync(kFull, lo ? d[1] : d[0], 2);
+            const float r1 = __shfl_xor_sync(kFull, lo ? d[3] : d[2], 2);
+            const float2 dot = make_float2((lo ? d[0] : d[1]) + r0, (lo ? d[2] : d[3]) + r1);
+            const __half2 km0 = *reinterpret_cast<const __half2*>(pg + kKMetaOff + gq * 4);
+            const __half2 km1 = *reinterpret_cast<const __half2*>(pg + kKMetaOff + (gq + 8) * 4);
+            const __half2 vm0 = *reinterpret_cast<const __half2*>(pg + kVMetaOff + gq * 4);
+            const __half2 vm1 = *reinterpret_cast<const __half2*>(pg + kVMetaOff + (gq + 8) * 4);
+            vdl[p] = make_float2(__low2float(vm0), __low2float(vm1));
+            vmn[p] = make_float2(__high2float(vm0), __high2float(vm1));
+            const float2 kd = make_float2(__low2float(km0), __low2float(km1));
+            const float2 kmin = make_float2(__high2float(km0), __high2float(km1));
+            const float2 u = __ffma2_rn(kd, dot, __fmul2_rn(kmin, make_float2(qsh, qsh)));
+            const float2 sg =
+                __fmul2_rn(__fmul2_rn(u, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
+            sig[p] = make_float2(v0[p] ? sg.x : -INFINITY, v1[p] ? sg.y : -INFINITY);
+            if (DEBUG && a.dbg_qk) {
+                const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
+                if (v0[p] && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = (int)dot.x;
+                if (v1[p] && pos0 + 8 < a.dbg_stride) a.dbg_qk[row + pos0 + 8] = (int)dot.y;
             }
         }
+        float m = fmaxf(sig[p].x, sig[p].y);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float m = sig[p][j];
-#pragma unroll
-            for (int msk = 2; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
-            Mp[p][j] = m;
-        }
+        for (int msk = 4; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
+        Mp[p] = m;
     }
 
-    // ---- running max and rescale factors
-    float alpha[2], beta[2][2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const float Mn = fmaxf(st.M[j], fmaxf(Mp[0][j], Mp[1][j]));
-        const bool none = (Mn == -INFINITY);
-        alpha[j] = none ? 1.f : (st.M[j] == -INFINITY ? 0.f : exp2_fast(st.M[j] - Mn));
-        beta[0][j] = (Mp[0][j] == -INFINITY) ? 0.f : exp2_fast(Mp[0][j] - Mn);
-        beta[1][j] = (Mp[1][j] == -INFINITY) ? 0.f : exp2_fast(Mp[1][j] - Mn);
-        st.M[j] = Mn;
-    }
+    // ---- running max of head hs and rescale factors
+    const float Mn = fmaxf(st.M, fmaxf(Mp[0], Mp[1]));
+    const bool none = (Mn == -INFINITY);
+    const float alpha = none ? 1.f : (st.M == -INFINITY ? 0.f : exp2_fast(st.M - Mn));
+    const float beta0 = (Mp[0] == -INFINITY) ? 0.f : exp2_fast(Mp[0] - Mn);
+    const float beta1 = (Mp[1] == -INFINITY) ? 0.f : exp2_fast(Mp[1] - Mn);
+    st.M = Mn;
 
     // ---- page-local weights, u8 with one power-of-two scale per (page, head)
-    float Wsum[2][2], swp[2][2];
+    float ksc[2], wsumf[2];
+    float lsum = 0.f, bsum = 0.f;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
+        const float2 pp2 = exp2_poly2(__fadd2_rn(sig[p], make_float2(-Mp[p], -Mp[p])));
+        const float2 pp = make_float2(v0[p] ? pp2.x : 0.f, v1[p] ? pp2.y : 0.f);
+        const float2 wv = __fmul2_rn(pp, vdl[p]);
+        float wmax = fmaxf(wv.x, wv.y);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const bool v = val[p] && ok[j];
-            const float pp = v ? exp2_poly(__fsub_rn(sig[p][j], Mp[p][j])) : 0.f;
-            const float wv = v ? __fmul_rn(pp, vdl[p]) : 0.f;
-            const float wmax = __uint_as_float(__reduce_max_sync(hmask, __float_as_uint(wv)));
-            int wh = 0;
-            float sw = 0.f;
-            if (wmax > 0x1p-64f) {
-                const int e = (int)(__float_as_uint(wmax) >> 23) - 127;   // floor(log2 wmax)
-                const float up = __uint_as_float((uint32_t)(134 - e) << 23);   // 2^(7-e)
-                wh = min(__float2int_rn(__fmul_rn(wv, up)), 255);
-                sw = __uint_as_float((uint32_t)(120 + e) << 23);              // 2^(e-7)
-            }
-            Wsum[p][j] = (float)__reduce_add_sync(hmask, (unsigned)wh);
-            swp[p][j] = sw;
-            sm.xb[warp].wsm[p][hd[j]][tok] = __int2half_rn(wh);
-            if (DEBUG && v && a.dbg_w) {
-                const int pos = (lp0 + p) * kPage + tok;
-                if (pos < a.dbg_stride)
-                    a.dbg_w[((int64_t)b * a.num_q_heads + h * G + hd[j]) * a.dbg_stride + pos] =
-                        (uint8_t)wh;
-            }
-            st.l[j] = (p == 0 ? st.l[j] * alpha[j] : st.l[j]) + beta[p][j] * pp;
-            st.bias[j] = (p == 0 ? st.bias[j] * alpha[j] : st.bias[j]) +
-                         beta[p][j] * (v ? pp * vmn[p] : 0.f);
+        for (int msk = 4; msk < 32; msk <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(kFull, wmax, msk));
+        const bool qz = wmax > 0x1p-64f;
+        const int e = (int)(__float_as_uint(wmax) >> 23) - 127;         // floor(log2 wmax)
+        const float up = __uint_as_float((uint32_t)(134 - e) << 23);     // 2^(7-e)
+        const float2 sc = __fmul2_rn(wv, make_float2(up, up));
+        const int wh0 = qz ? min(__float2int_rn(sc.x), 255) : 0;
+        const int wh1 = qz ? min(__float2int_rn(sc.y), 255) : 0;
+        int ws = wh0 + wh1;
+#pragma unroll
+        for (int msk = 4; msk < 32; msk <<= 1) ws += __shfl_xor_sync(kFull, ws, msk);
+        const float beta = p ? beta1 : beta0;
+        ksc[p] = qz ? beta * __uint_as_float((uint32_t)(120 + e) << 23) : 0.f;   // β·2^(e-7)
+        wsumf[p] = (float)ws;
+        sm.xb[warp].wsm[p][hs][gq] = __int2half_rn(wh0);
+        sm.xb[warp].wsm[p][hs][gq + 8] = __int2half_rn(wh1);
+        if (DEBUG && a.dbg_w) {
+            const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
+            const int pos0 = (lp0 + p) * kPage + gq;
+            if (v0[p] && pos0 < a.dbg_stride) a.dbg_w[row + pos0] = (uint8_t)wh0;
+            if (v1[p] && pos0 + 8 < a.dbg_stride) a.dbg_w[row + pos0 + 8] = (uint8_t)wh1;
         }
+        lsum = fmaf(beta, pp.x + pp.y, lsum);
+        bsum = fmaf(beta, fmaf(pp.x, vmn[p].x, pp.y * vmn[p].y), bsum);
     }
-    if (__any_sync(kFull, alpha[0] != 1.f || alpha[1] != 1.f)) {
+    st.l = fmaf(st.l, alpha, lsum);
+    st.bias = fmaf(st.bias, alpha, bsum);
+
+    // ---- hand the per-(page, head) factors to the lanes whose PV columns need them:
+    // columns of lane (g', t') are page t'>>1, heads 2(t'&1) and 2(t'&1)+1, scored by
+    // lanes t'&1 and (t'&1)+2 of the same g'
+    const int srcA = (lane & ~3) | (tq & 1), srcB = srcA | 2;
+    const float kA0 = __shfl_sync(kFull, ksc[0], srcA), kA1 = __shfl_sync(kFull, ksc[1], srcA);
+    const float kB0 = __shfl_sync(kFull, ksc[0], srcB), kB1 = __shfl_sync(kFull, ksc[1], srcB);
+    const float WA0 = __shfl_sync(kFull, wsumf[0], srcA), WA1 = __shfl_sync(kFull, wsumf[1], srcA);
+    const float WB0 = __shfl_sync(kFull, wsumf[0], srcB), WB1 = __shfl_sync(kFull, wsumf[1], srcB);
+    const float kA = half ? kA1 : kA0, kB = half ? kB1 : kB0;
+    const float WA = half ? WA1 : WA0, WB = half ? WB1 : WB0;
+    if (__any_sync(kFull, alpha != 1.f)) {
+        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcB);
 #pragma unroll
         for (int m = 0; m < 8; ++m)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                st.o[m][r][0] *= alpha[0];
-                st.o[m][r][1] *= alpha[1];
+                st.o[m][r][0] *= aA;
+                st.o[m][r][1] *= aB;
             }
     }
     __syncwarp();
@@ -439,12 +456,8 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     }
     const uint32_t vA[8] = {va0.x, va0.y, va0.z, va0.w, va1.x, va1.y, va1.z, va1.w};
     const uint32_t vB[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
-    // this lane's output columns belong to page `half` of the pair
-    const float W0 = half ? Wsum[1][0] : Wsum[0][0], W1 = half ? Wsum[1][1] : Wsum[0][1];
-    const float ci0 = -1024.f * W0, ci1 = -1024.f * W1;
-    const float k0 = half ? beta[1][0] * swp[1][0] : beta[0][0] * swp[0][0];
-    const float k1 = half ? beta[1][1] * swp[1][1] : beta[0][1] * swp[0][1];
-    const float k0h = k0 * 0.0625f, k1h = k1 * 0.0625f;
+    const float ci0 = -1024.f * WA, ci1 = -1024.f * WB;
+    const float kAh = kA * 0.0625f, kBh = kB * 0.0625f;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
         float c[4];
@@ -453,10 +466,10 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
                 ci1);
         mma_f16(c, wide_lo(vB[m]), wide_hi(vB[m]), wide_lo(sb), wide_hi(sb), bB0, bB1, c[0], c[1],
                 c[2], c[3]);
-        st.o[m][0][0] = fmaf(k0, c[0], st.o[m][0][0]);
-        st.o[m][0][1] = fmaf(k1, c[1], st.o[m][0][1]);
-        st.o[m][1][0] = fmaf(k0h, c[2], st.o[m][1][0]);
-        st.o[m][1][1] = fmaf(k1h, c[3], st.o[m][1][1]);
+        st.o[m][0][0] = fmaf(kA, c[0], st.o[m][0][0]);
+        st.o[m][0][1] = fmaf(kB, c[1], st.o[m][0][1]);
+        st.o[m][1][0] = fmaf(kAh, c[2], st.o[m][1][0]);
+        st.o[m][1][1] = fmaf(kBh, c[3], st.o[m][1][1]);
     }
     __syncwarp();
 }
@@ -513,6 +526,7 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     const int s = a.sink, w = a.window;
     const int pos = side_row_position(grp * 16 + t, s, w, L);
     const bool valid = pos >= 0;
+    const unsigned vmask = __ballot_sync(kFull, valid);   // row r valid <=> bit 2r
     const WarpQ& wq = sm.wq[warp];
 
     int dot[G];
@@ -584,7 +598,7 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     }
     __syncwarp();
     for (int tt = 0; tt < 16; ++tt) {
-        if (side_row_position(grp * 16 + tt, s, w, L) < 0) continue;     // uniform
+        if (!((vmask >> (2 * tt)) & 1u)) continue;                        // uniform
         const uint32_t vcw = lds32(pv + (kSideVCodeOff - kPageBlock) + tt * 128 + 4 * lane);
         const __half2 vm = *reinterpret_cast<const __half2*>(pk + kSideVMetaOff + tt * 4);
         const float vd = __low2float(vm), vmin = __high2float(vm);
@@ -633,48 +647,79 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
     walk_init(P, a, lo, hi, cp);
     Cw = P;
     uint32_t phase = 0;                     // bit k: parity awaited next on stage k
-    int prod = 0, cons = 0;
-    int win_b = -1, win_lp = 0, win = 0;    // block-table window: entry lp = win_lp + lane
+    int prod = 0, cons = 0;                 // items issued / consumed
+    int pst = 0, cst = 0;                   // stage of the next item to issue / consume
     bool aborted = false;
 
-    // keep the ring kStages items ahead of the consumer
+    // Producer: walks its own copy of the span run by run; within a run the items
+    // are consecutive pages (block-table window of 32 entries, one load per lane)
+    // or consecutive side blocks. All lanes track it; lane 0 issues.
+    int r_kind = -1;                        // 0 INT4 pages, 1 side blocks, 2 empty item; -1 none
+    int r_i = 0, r_end = 0, r_lp0 = 0, win_lo = 0, win = 0;
+    const uint8_t* r_src = nullptr;
+    auto next_run = [&]() -> bool {
+        if (r_kind >= 0) {                  // leave the run that just ended
+            if (r_kind == 0 && P.own) P.k = P.n;
+            else walk_next_bh(P, a, cp);
+        }
+        if (P.done) { r_kind = -1; return false; }
+        if (P.k < P.n) {
+            r_kind = 0;
+            r_i = P.k;
+            r_end = P.a1;
+            r_lp0 = p_first;
+            r_src = a.pages + (int64_t)P.h * kPageBlock;
+            win_lo = -64;                   // force a window load
+        } else {
+            r_kind = S > 0 ? 1 : 2;
+            r_i = 0;
+            r_end = cp;
+            const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
+            r_src = a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes;
+        }
+        return true;
+    };
     auto produce = [&]() {
-        while (!P.done && prod < cons + kStages) {
-            const int stg = prod % kStages;
-            uint64_t* bar = &sm.bar[warp][stg];
-            if (P.k < P.n) {
-                const int lp = p_first + P.k;
-                if (P.b != win_b || lp < win_lp || lp >= win_lp + 32) {
-                    win_b = P.b;
-                    win_lp = lp;
+        bool fenced = false;
+        while (prod < cons + kStages) {
+            if (r_kind < 0 || r_i >= r_end) {
+                if (!next_run()) break;
+            }
+            if (!fenced) {
+                if (lane == 0) fence_proxy_async();
+                fenced = true;
+            }
+            uint64_t* bar = &sm.bar[warp][pst];
+            if (r_kind == 0) {
+                const int lp = r_lp0 + r_i;
+                if (lp - win_lo >= 32 || lp < win_lo) {
+                    win_lo = lp;
                     const int e = lp + lane;
-                    win = (e < a.stride) ? __ldg(&a.block_table[(int64_t)P.b * a.stride + e]) : -1;
+                    int pg = -1;
+                    if (e < a.stride) pg = __ldg(&a.block_table[(int64_t)P.b * a.stride + e]);
+                    // entries past the sequence's pages are never issued; report the rest
+                    if (e < r_lp0 + r_end && (e >= a.stride || pg < 0 || (int64_t)pg >= a.num_pages)) {
+                        report_error(a.err, e >= a.stride ? KV4_DEVERR_BAD_POSITION : KV4_DEVERR_BAD_PAGE);
+                        pg = 0;
+                    }
+                    win = pg;
                 }
-                int page = __shfl_sync(kFull, win, lp - win_lp);
+                const int page = __shfl_sync(kFull, win, lp - win_lo);
                 if (lane == 0) {
-                    if (lp >= a.stride) report_error(a.err, KV4_DEVERR_BAD_POSITION);
-                    else if (page < 0 || (int64_t)page >= a.num_pages) report_error(a.err, KV4_DEVERR_BAD_PAGE);
-                    if (lp >= a.stride || page < 0 || (int64_t)page >= a.num_pages) page = 0;
-                    fence_proxy_async();
                     mbar_expect_tx(bar, kPageBlock);
-                    bulk_g2s(sm.stage[warp][stg], a.pages + ((int64_t)page * H + P.h) * kPageBlock,
-                             kPageBlock, bar);
+                    bulk_g2s(sm.stage[warp][pst], r_src + (int64_t)page * H * kPageBlock, kPageBlock, bar);
                 }
-            } else if (S > 0) {
+            } else if (r_kind == 1) {
                 if (lane == 0) {
-                    const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
-                    fence_proxy_async();
                     mbar_expect_tx(bar, kPageBlock);
-                    bulk_g2s(sm.stage[warp][stg],
-                             a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes +
-                                 (int64_t)(P.k - P.n) * kPageBlock,
-                             kPageBlock, bar);
+                    bulk_g2s(sm.stage[warp][pst], r_src + (int64_t)r_i * kPageBlock, kPageBlock, bar);
                 }
             } else if (lane == 0) {
                 mbar_arrive(bar);           // empty protected item: no side buffer
             }
+            ++r_i;
             ++prod;
-            walk_step(P, a, cp);
+            if (++pst == kStages) pst = 0;
         }
     };
     auto wait_stage = [&](int stg) {
@@ -685,6 +730,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             aborted = true;
         }
     };
+    auto next_stage = [](int x) { return x + 1 == kStages ? 0 : x + 1; };
 
     produce();
     int q_b = -1, q_h = -1;
@@ -736,55 +782,53 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     }
                 }
             }
-            float cq[2], sq[2], qsf[2];
+            float cq[2];
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int hh = 2 * (tq & 1) + j;
-                const bool okh = hh < G;
-                cq[j] = okh ? -wq.corr[hh][half] : 0.f;
-                sq[j] = okh ? wq.scale[hh] : 0.f;
-                qsf[j] = okh ? wq.qsum[hh] : 0.f;
+                cq[j] = hh < G ? -wq.corr[hh][half] : 0.f;
             }
+            const int hs = 2 * (tq & 1) + half;
+            const float sqh = hs < G ? wq.scale[hs] : 0.f;
+            const float qsh = hs < G ? wq.qsum[hs] : 0.f;
             Int4State st;
 #pragma unroll
             for (int m = 0; m < 8; ++m)
 #pragma unroll
                 for (int r = 0; r < 2; ++r) st.o[m][r][0] = st.o[m][r][1] = 0.f;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                st.M[j] = -INFINITY;
-                st.l[j] = 0.f;
-                st.bias[j] = 0.f;
-            }
+            st.M = -INFINITY;
+            st.l = 0.f;
+            st.bias = 0.f;
             const int r4_hi = Cw.L - w;
             for (int j = first; j < last; j += 2) {
                 const bool two = j + 1 < last;
-                const int s0 = cons % kStages, s1 = (cons + 1) % kStages;
+                const int s0 = cst, s1 = next_stage(cst);
                 wait_stage(s0);
                 if (two) wait_stage(s1);
-                int4_pair<G, DEBUG>(a, sm, st, qb, cq, sq, qsf, sm.stage[warp][s0], sm.stage[warp][s1],
-                                    two, p_first + j, r4_hi, b, h, warp, lane);
+                int4_pair<G, DEBUG>(a, sm, st, qb, cq, sqh, qsh, sm.stage[warp][s0],
+                                    sm.stage[warp][s1], two, p_first + j, r4_hi, b, h, warp, lane);
                 cons += two ? 2 : 1;
+                cst = two ? next_stage(s1) : s1;
                 produce();
             }
-            // ---- partial of this piece: normalizer and offset terms over the 16 lanes of
-            // a head pair, output halves (pages of a pair) over lanes t' and t' ^ 2
+            // ---- partial of this piece: normalizer and offset terms over the 8 lanes that
+            // scored a head, handed to the PV lanes; output halves (pages of a pair) over
+            // lanes t' and t' ^ 2
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
-#pragma unroll
-                for (int msk = 2; msk < 32; msk <<= 1) {
-                    st.l[j] += __shfl_xor_sync(kFull, st.l[j], msk);
-                    st.bias[j] += __shfl_xor_sync(kFull, st.bias[j], msk);
-                }
+            for (int msk = 4; msk < 32; msk <<= 1) {
+                st.l += __shfl_xor_sync(kFull, st.l, msk);
+                st.bias += __shfl_xor_sync(kFull, st.bias, msk);
+            }
+            const int srcA = (lane & ~3) | (tq & 1);
+            const float biasA = __shfl_sync(kFull, st.bias, srcA);
+            const float biasB = __shfl_sync(kFull, st.bias, srcA | 2);
 #pragma unroll
             for (int m = 0; m < 8; ++m)
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        st.o[m][r][j] += __shfl_xor_sync(kFull, st.o[m][r][j], 2);
-                        st.o[m][r][j] += st.bias[j];
-                    }
+                for (int r = 0; r < 2; ++r) {
+                    st.o[m][r][0] += __shfl_xor_sync(kFull, st.o[m][r][0], 2) + biasA;
+                    st.o[m][r][1] += __shfl_xor_sync(kFull, st.o[m][r][1], 2) + biasB;
+                }
             const int base = Cw.csb + h * Cw.cbh;
             int idx = __ldg(&a.seg_start[b]) + (wg - base / span);
             for (int hh = 0; hh < h; ++hh) idx += n_pieces(Cw.csb + hh * Cw.cbh, Cw.n, span);
@@ -798,9 +842,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     for (int m = 0; m < 8; ++m)
                         *reinterpret_cast<float2*>(po + 16 * m + 2 * gq) =
                             make_float2(st.o[m][0][j], st.o[m][1][j]);
-                    if (gq == 0) a.part_ml[(int64_t)idx * G + hd] = make_float2(st.M[j], st.l[j]);
                 }
             }
+            if (gq == 0 && hs < G) a.part_ml[(int64_t)idx * G + hs] = make_float2(st.M, st.l);
             if (Cw.own) Cw.k = Cw.n;
             else walk_next_bh(Cw, a, cp);
         } else {
@@ -821,17 +865,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             }
             if (S > 0) {
                 for (int grp = 0; grp < nb; ++grp) {
-                    const int s0 = cons % kStages, s1 = (cons + 1) % kStages;
+                    const int s0 = cst, s1 = next_stage(cst);
                     wait_stage(s0);
                     wait_stage(s1);
                     prot_group<G, DEBUG>(a, sm, st, sm.stage[warp][s0], sm.stage[warp][s1], grp, L, b,
                                          h, warp, lane);
                     cons += 2;
+                    cst = next_stage(s1);
                     produce();
                 }
             } else {
-                wait_stage(cons % kStages);
+                wait_stage(cst);
                 cons += 1;
+                cst = next_stage(cst);
                 produce();
             }
             float* po = a.part_o + ((int64_t)(b * H + h) * G) * kHeadDim;

@@ -148,6 +148,28 @@ __device__ __forceinline__ float exp2_poly(float x)
     return __int_as_float(__float_as_int(p) + (n << 23));
 }
 
+// The same exp2 on two values with packed fp32 arithmetic; bit-identical to
+// exp2_poly (rint(x) is taken as (x + 1.5·2^23) − 1.5·2^23, exact for |x| < 2^22).
+__device__ __forceinline__ float2 exp2_poly2(float2 x)
+{
+    const float kMagic = 12582912.0f;
+    const float2 xm = __fadd2_rn(x, make_float2(kMagic, kMagic));
+    const float2 n = __fadd2_rn(xm, make_float2(-kMagic, -kMagic));
+    const float2 f = __ffma2_rn(n, make_float2(-1.0f, -1.0f), x);
+    float2 p = make_float2(0x1.ffcbfcp-17f, 0x1.ffcbfcp-17f);
+    p = __ffma2_rn(p, f, make_float2(0x1.430912p-13f, 0x1.430912p-13f));
+    p = __ffma2_rn(p, f, make_float2(0x1.5d87fep-10f, 0x1.5d87fep-10f));
+    p = __ffma2_rn(p, f, make_float2(0x1.3b2ab6p-7f, 0x1.3b2ab6p-7f));
+    p = __ffma2_rn(p, f, make_float2(0x1.c6b08ep-5f, 0x1.c6b08ep-5f));
+    p = __ffma2_rn(p, f, make_float2(0x1.ebfbe0p-3f, 0x1.ebfbe0p-3f));
+    p = __ffma2_rn(p, f, make_float2(0x1.62e430p-1f, 0x1.62e430p-1f));
+    p = __ffma2_rn(p, f, make_float2(1.0f, 1.0f));
+    const int n0 = __float_as_int(xm.x) - __float_as_int(kMagic);
+    const int n1 = __float_as_int(xm.y) - __float_as_int(kMagic);
+    return make_float2(x.x >= -125.0f ? __int_as_float(__float_as_int(p.x) + (n0 << 23)) : 0.0f,
+                       x.y >= -125.0f ? __int_as_float(__float_as_int(p.y) + (n1 << 23)) : 0.0f);
+}
+
 // Fast exp2 (hardware approximation) for rescaling factors that decide no integer.
 __device__ __forceinline__ float exp2_fast(float x)
 {
