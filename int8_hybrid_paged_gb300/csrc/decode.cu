@@ -201,10 +201,23 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
           "f"(c3));
 }
 
+// (a & b) | c in one LOP3 (lookup table 0xEA), all three operands in registers.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 // nibbles 0 and 4 of w as fp16 (1024 + n0, 1024 + n4)
-__device__ __forceinline__ uint32_t wide_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t wide_lo(uint32_t w)
+{
+    return and_or(w, 0x000F000Fu, 0x64006400u);
+}
 // nibbles 1 and 5 of w as fp16 (1024 + 16 n1, 1024 + 16 n5)
-__device__ __forceinline__ uint32_t wide_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
+__device__ __forceinline__ uint32_t wide_hi(uint32_t w)
+{
+    return and_or(w, 0x00F000F0u, 0x64006400u);
+}
 
 __device__ __forceinline__ uint32_t half2_bits(__half lo, __half hi)
 {
