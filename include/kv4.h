@@ -78,11 +78,12 @@ typedef struct {
  * for the 16 token slots t of the page:
  *   [0,    1024)  K codes, row t = 64 bytes; byte j = c[2j] | c[2j+1] << 4 (rotated K)
  *   [1024, 2048)  V codes: one byte per (dim pair j, token t) = c_t[2j] | c_t[2j+1] << 4, at
- *                 offset 4*(8*(4*(j%8) + (t%8)/2) + j/8) + (2*(t%2) + t/8) (32 groups of
- *                 eight 32-bit words; each word holds one dim pair of tokens
- *                 2u, 2u+8, 2u+1, 2u+9 with u = (t%8)/2, one tensor-core fragment)
- *   [2048, 2112)  K metadata, t -> {fp16 delta, fp16 min} (4 bytes)
- *   [2112, 2176)  V metadata, same form
+ *                 offset 4*(8*(4*(j%8) + t%4) + j/8) + t/4 (32 groups of eight 32-bit
+ *                 words; each word holds one dim pair of tokens u, u+4, u+8, u+12 with
+ *                 u = t%4, one tensor-core fragment)
+ *   [2048, 2176)  K and V metadata, {fp16 delta, fp16 min} (4 bytes) per token: 8 rows
+ *                 of 16 bytes, row r = [K of token r | K of token r+8 | V of token r |
+ *                 V of token r+8], so one 16-byte load brings both tokens a lane scores
  * Side pool: max_slots * H_kv blocks of side_block_bytes = ceil((s+w)/16) * 4352;
  * block (slot, h) at (slot * H_kv + h) * side_block_bytes. Side row i (i = p for a
  * sink position p < s, i = s + p mod w for a ring position) is row i%16 of group

@@ -17,14 +17,12 @@
 namespace kv4 {
 
 // Byte of (dim pair j, token t) inside a page's V code block. The block is 32 lanes x
-// 8 words: word (l, m) holds pair j = 8m + (l >> 2) for tokens 2(l&3), 2(l&3)+8,
-// 2(l&3)+1, 2(l&3)+9 (bytes 0..3), so one lane's eight words are one tensor-core
-// fragment per 16-dim tile and sit in 32 contiguous bytes.
+// 8 words: word (l, m) holds pair j = 8m + (l >> 2) for tokens u, u+4, u+8, u+12 with
+// u = l & 3 (bytes 0..3), so one lane's eight words are one tensor-core fragment per
+// 16-dim tile and sit in 32 contiguous bytes.
 __device__ __forceinline__ int v_byte_offset(int j, int t)
 {
-    const int tq = (t & 7) >> 1;
-    const int byte = ((t & 1) << 1) | (t >> 3);
-    return ((((j & 7) << 2) + tq) * 8 + (j >> 3)) * 4 + byte;
+    return ((((j & 7) << 2) + (t & 3)) * 8 + (j >> 3)) * 4 + (t >> 2);
 }
 
 __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
@@ -86,8 +84,10 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
     blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
     blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
     if (lane == 0) {
-        *reinterpret_cast<__half2*>(blk + kKMetaOff + ts * 4) = __halves2half2(kd, km);
-        *reinterpret_cast<__half2*>(blk + kVMetaOff + ts * 4) = __halves2half2(vd, vm);
+        // metadata row ts % 8: [K ts, K ts+8, V ts, V ts+8] for ts < 8, the same row for ts >= 8
+        uint8_t* mrow = blk + kMetaOff + 16 * (ts & 7) + 4 * (ts >> 3);
+        *reinterpret_cast<__half2*>(mrow) = __halves2half2(kd, km);
+        *reinterpret_cast<__half2*>(mrow + 8) = __halves2half2(vd, vm);
     }
 
     // INT8 side copies: sink row pos (pos < s), ring row s + pos mod w for the last

@@ -46,13 +46,34 @@ struct __align__(16) WarpQ {
     float corr[kMaxG][2];
 };
 
+// Span walker state (one per producer and consumer of a warp): the current (b, h) of
+// the span and the item reached in it.
+struct Walk {
+    int lo, hi;
+    int b, h;
+    int L, n, cbh, csb, slot;   // of the current b
+    int k;                      // current item of (b, h): k < n INT4 page, else protected item
+    int a1;                     // end of the span's INT4 pages of (b, h)
+    int own;                    // this span owns (b, h)'s protected unit
+    int done;
+};
+
+// PV operands of an INT4 page pair: the u8 weights (as fp16) in the B-fragment order of
+// each page's MMA (columns 4p..4p+3 of page p; the rest stay zero) and the page scales.
+struct PairSmem {
+    uint32_t wfrag[2][8][8];
+    float ksc[2][kMaxG];
+};
+
 struct __align__(128) SplitSmem {
     uint8_t stage[kWarps][kStages][kPageBlock];   // staging ring of each warp
     WarpQ wq[kWarps];
+    uint4 qfrag[kWarps][4][32];                   // QK B fragments: [k step pair][lane]
     union {
-        __half wsm[2][kMaxG][16];                 // u8 PV weights (as fp16) of a page pair
+        PairSmem pair;                            // INT4 runs
         float pbuf[kMaxG][16];                    // protected weights of a 16-row group
     } xb[kWarps];
+    Walk walk[kWarps][2];                         // producer, consumer
     uint64_t bar[kWarps][kStages];
 };
 
@@ -225,21 +246,15 @@ __device__ __forceinline__ uint32_t half2_bits(__half lo, __half hi)
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ uint32_t half2_u32(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __half2 u32_half2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
 __device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
 // ---------------------------------------------------------------- span walker
 // Walks the stage items of one warp's span [lo, hi) of the cost line: for each
 // (b, h) touched, the INT4 pages of the span's overlap, then the protected unit
 // if its first item lies in the span (its owner takes all of it).
-struct Walk {
-    int lo, hi;
-    int b, h;
-    int L, n, cbh, csb, slot;   // of the current b
-    int k;                      // current item of (b, h): k < n INT4 page, else protected item
-    int a1;                     // end of the span's INT4 pages of (b, h)
-    bool own;                   // this span owns (b, h)'s protected unit
-    bool done;
-};
 
 __device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b, int cp)
 {
@@ -308,78 +323,106 @@ __device__ __forceinline__ void walk_step(Walk& W, const DecodeArgs& a, int cp)
 
 // ---------------------------------------------------------------- INT4 page pair
 // Lane (g', t') = (lane >> 2, lane & 3) scores tokens g' and g' + 8 of each page for
-// head 2(t' & 1) + (t' >> 1), and accumulates output dims 16m + 2g' + {0, 1}
+// head hs = 2(t' & 1) + (t' >> 1), and accumulates output dims 16m + 2g' + {0, 1}
 // (m = 0..7) of heads 2(t' & 1), 2(t' & 1) + 1 from page t' >> 1 of each pair.
+//
+// QK columns: column n of the B operand is head n (n < 4) or n ^ 5 (n >= 4) over the
+// dim half n & 1, so lane t' < 2 holds (head hs, half 0 | head hs + 1, half 1) and its
+// partner t' + 2 holds (head hs + 1, half 0 | head hs, half 1): each lane keeps its
+// first column and adds its partner's second, with no select on either side.
+//
+// PV columns: n = 4 page + head. The u8 weights go to shared memory as packed half2
+// words (token g', token g' + 8) in the B-fragment order of each page's MMA; the
+// columns of the other page stay zero, so each MMA takes its operand with one load.
 struct Int4State {
     float o[8][2][2];
-    float M, l, bias;    // running max, normalizer and offset-term shares of the scored head
+    float M, l, bias;    // running max, normalizer and offset-term share of the scored head
+    float wacc;          // Σ over pages of (page scale) x Σ u8 weights, for the widening offset
 };
 
-template <int G, bool DEBUG>
+__device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
+__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// position of word w (tokens w, w + 8) inside a column's 8 B-fragment words:
+// a lane reads words t' and t' + 4 with one 8-byte load
+__device__ __forceinline__ int wfrag_pos(int w) { return 2 * (w & 3) + (w >> 2); }
+
+template <int G, bool DEBUG, bool EDGE>
 __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, Int4State& st,
-                                          const uint32_t (&qb)[8][2], const float (&cq)[2], float sqh,
-                                          float qsh, const uint8_t* pg0, const uint8_t* pg1, bool two,
-                                          int lp0, int r4_hi, int b, int h, int warp, int lane)
+                                          const uint4* __restrict__ qf, float cq0, float cq1,
+                                          float sqh, float qsh, const uint8_t* pg0,
+                                          const uint8_t* pg1, bool two, int lp0, int r4_hi, int b,
+                                          int h, int warp, int lane)
 {
     const int gq = lane >> 2, tq = lane & 3;
     const int half = tq >> 1;
-    const bool lo = half == 0;
     const int hs = 2 * (tq & 1) + half;            // head scored by this lane
-    const bool okS = hs < G;
-    const int r4_lo = a.sink;
+    const uint8_t* pgs[2] = {pg0, pg1};
+    PairSmem& ps = sm.xb[warp].pair;
 
-    // ---- integer QK of both pages; this lane keeps tokens gq, gq + 8 of head hs
-    float2 sig[2], vdl[2], vmn[2];
-    float Mp[2];
-    bool v0[2], v1[2];
+    // ---- integer QK of both pages (two independent MMA chains)
+    uint4 kr0[2], kr1[2], mt[2];
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const int pos0 = (lp0 + p) * kPage + gq;
-        const bool live = (p == 0 || two) && okS;
-        v0[p] = live && pos0 >= r4_lo && pos0 < r4_hi;
-        v1[p] = live && pos0 + 8 >= r4_lo && pos0 + 8 < r4_hi;
-        sig[p] = make_float2(-INFINITY, -INFINITY);
-        vdl[p] = vmn[p] = make_float2(0.f, 0.f);
-        if (p == 0 || two) {
-            const uint8_t* pg = p ? pg1 : pg0;
-            const uint4 k0 = *reinterpret_cast<const uint4*>(pg + kKCodeOff + gq * 64 + 16 * tq);
-            const uint4 k1 = *reinterpret_cast<const uint4*>(pg + kKCodeOff + (gq + 8) * 64 + 16 * tq);
-            const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
-            const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
-            float d[4];
-            mma_f16(d, wide_lo(w0[0]), wide_lo(w1[0]), wide_hi(w0[0]), wide_hi(w1[0]), qb[0][0],
-                    qb[0][1], cq[0], cq[1], cq[0], cq[1]);
+        kr0[p] = lds128(pgs[p] + kKCodeOff + gq * 64 + 16 * tq);
+        kr1[p] = lds128(pgs[p] + kKCodeOff + (gq + 8) * 64 + 16 * tq);
+        mt[p] = lds128(pgs[p] + kMetaOff + 16 * gq);
+    }
+    float d[2][4];
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                if (ii > 0)
-                    mma_f16(d, wide_lo(w0[ii]), wide_lo(w1[ii]), wide_hi(w0[ii]), wide_hi(w1[ii]),
-                            qb[2 * ii][0], qb[2 * ii][1], d[0], d[1], d[2], d[3]);
-                const uint32_t s0 = w0[ii] >> 8, s1 = w1[ii] >> 8;
-                mma_f16(d, wide_lo(s0), wide_lo(s1), wide_hi(s0), wide_hi(s1), qb[2 * ii + 1][0],
-                        qb[2 * ii + 1][1], d[0], d[1], d[2], d[3]);
-            }
-            // lanes t' and t' ^ 2 hold the two dim halves of heads 2(t'&1), 2(t'&1)+1:
-            // the low lane keeps the first head, the high lane the second
-            const float r0 = __shfl_xor_sync(kFull, lo ? d[1] : d[0], 2);
-            const float r1 = __shfl_xor_sync(kFull, lo ? d[3] : d[2], 2);
-            const float2 dot = make_float2((lo ? d[0] : d[1]) + r0, (lo ? d[2] : d[3]) + r1);
-            const __half2 km0 = *reinterpret_cast<const __half2*>(pg + kKMetaOff + gq * 4);
-            const __half2 km1 = *reinterpret_cast<const __half2*>(pg + kKMetaOff + (gq + 8) * 4);
-            const __half2 vm0 = *reinterpret_cast<const __half2*>(pg + kVMetaOff + gq * 4);
-            const __half2 vm1 = *reinterpret_cast<const __half2*>(pg + kVMetaOff + (gq + 8) * 4);
-            vdl[p] = make_float2(__low2float(vm0), __low2float(vm1));
-            vmn[p] = make_float2(__high2float(vm0), __high2float(vm1));
-            const float2 kd = make_float2(__low2float(km0), __low2float(km1));
-            const float2 kmin = make_float2(__high2float(km0), __high2float(km1));
-            const float2 u = __ffma2_rn(kd, dot, __fmul2_rn(kmin, make_float2(qsh, qsh)));
-            const float2 sg =
-                __fmul2_rn(__fmul2_rn(u, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
+    for (int p = 0; p < 2; ++p) {
+        d[p][0] = cq0;
+        d[p][1] = cq1;
+        d[p][2] = cq0;
+        d[p][3] = cq1;
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+        const uint4 qv = qf[32 * ii];                // B fragments of k steps 2ii, 2ii + 1
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const uint32_t w0 = ii == 0 ? kr0[p].x : ii == 1 ? kr0[p].y : ii == 2 ? kr0[p].z : kr0[p].w;
+            const uint32_t w1 = ii == 0 ? kr1[p].x : ii == 1 ? kr1[p].y : ii == 2 ? kr1[p].z : kr1[p].w;
+            mma_f16(d[p], wide_lo(w0), wide_lo(w1), wide_hi(w0), wide_hi(w1), qv.x, qv.y, d[p][0],
+                    d[p][1], d[p][2], d[p][3]);
+            const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
+            mma_f16(d[p], wide_lo(s0), wide_lo(s1), wide_hi(s0), wide_hi(s1), qv.z, qv.w, d[p][0],
+                    d[p][1], d[p][2], d[p][3]);
+        }
+    }
+
+    // ---- scores of head hs, tokens gq and gq + 8 of each page
+    float2 sig[2], vdl[2], vmn[2];
+    bool v0[2], v1[2];
+    float Mp[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const float r0 = __shfl_xor_sync(kFull, d[p][1], 2);
+        const float r1 = __shfl_xor_sync(kFull, d[p][3], 2);
+        const float2 dot = __fadd2_rn(make_float2(d[p][0], d[p][2]), make_float2(r0, r1));
+        const __half2 km0 = u32_half2(mt[p].x), km1 = u32_half2(mt[p].y);
+        const __half2 vm0 = u32_half2(mt[p].z), vm1 = u32_half2(mt[p].w);
+        vdl[p] = make_float2(__low2float(vm0), __low2float(vm1));
+        vmn[p] = make_float2(__high2float(vm0), __high2float(vm1));
+        const float2 kd = make_float2(__low2float(km0), __low2float(km1));
+        const float2 kmin = make_float2(__high2float(km0), __high2float(km1));
+        const float2 u = __ffma2_rn(kd, dot, __fmul2_rn(kmin, make_float2(qsh, qsh)));
+        const float2 sg =
+            __fmul2_rn(__fmul2_rn(u, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
+        const int pos0 = (lp0 + p) * kPage + gq;
+        if (EDGE) {
+            const bool live = p == 0 || two;
+            v0[p] = live && pos0 >= a.sink && pos0 < r4_hi;
+            v1[p] = live && pos0 + 8 >= a.sink && pos0 + 8 < r4_hi;
             sig[p] = make_float2(v0[p] ? sg.x : -INFINITY, v1[p] ? sg.y : -INFINITY);
-            if (DEBUG && a.dbg_qk) {
-                const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
-                if (v0[p] && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = (int)dot.x;
-                if (v1[p] && pos0 + 8 < a.dbg_stride) a.dbg_qk[row + pos0 + 8] = (int)dot.y;
-            }
+        } else {
+            v0[p] = v1[p] = true;
+            sig[p] = sg;
+        }
+        if (DEBUG && a.dbg_qk && hs < G) {
+            const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
+            if (v0[p] && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = (int)dot.x;
+            if (v1[p] && pos0 + 8 < a.dbg_stride) a.dbg_qk[row + pos0 + 8] = (int)dot.y;
         }
         float m = fmaxf(sig[p].x, sig[p].y);
 #pragma unroll
@@ -389,61 +432,63 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
 
     // ---- running max of head hs and rescale factors
     const float Mn = fmaxf(st.M, fmaxf(Mp[0], Mp[1]));
-    const bool none = (Mn == -INFINITY);
-    const float alpha = none ? 1.f : (st.M == -INFINITY ? 0.f : exp2_fast(st.M - Mn));
-    const float beta0 = (Mp[0] == -INFINITY) ? 0.f : exp2_fast(Mp[0] - Mn);
-    const float beta1 = (Mp[1] == -INFINITY) ? 0.f : exp2_fast(Mp[1] - Mn);
+    float alpha, beta[2];
+    if (EDGE) {
+        const bool none = (Mn == -INFINITY);
+        alpha = none ? 1.f : exp2_fast(st.M - Mn);
+        beta[0] = none ? 0.f : exp2_fast(Mp[0] - Mn);
+        beta[1] = none ? 0.f : exp2_fast(Mp[1] - Mn);
+    } else {
+        alpha = exp2_fast(st.M - Mn);              // st.M = -inf gives 0
+        beta[0] = exp2_fast(Mp[0] - Mn);
+        beta[1] = exp2_fast(Mp[1] - Mn);
+    }
     st.M = Mn;
 
     // ---- page-local weights, u8 with one power-of-two scale per (page, head)
-    float ksc[2], wsumf[2];
-    float lsum = 0.f, bsum = 0.f;
+    float ksc[2];
+    float2 lb = make_float2(0.f, 0.f);             // (Σ β p, Σ β p · V min)
+    float wsum = 0.f;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const float2 pp2 = exp2_poly2(__fadd2_rn(sig[p], make_float2(-Mp[p], -Mp[p])));
-        const float2 pp = make_float2(v0[p] ? pp2.x : 0.f, v1[p] ? pp2.y : 0.f);
+        // masked tokens give -inf - Mp (or NaN for an empty page): exp2_poly2 returns 0
+        const float2 pp = exp2_poly2(__fadd2_rn(sig[p], make_float2(-Mp[p], -Mp[p])));
         const float2 wv = __fmul2_rn(pp, vdl[p]);
         float wmax = fmaxf(wv.x, wv.y);
 #pragma unroll
         for (int msk = 4; msk < 32; msk <<= 1) wmax = fmaxf(wmax, __shfl_xor_sync(kFull, wmax, msk));
         const bool qz = wmax > 0x1p-64f;
-        const int e = (int)(__float_as_uint(wmax) >> 23) - 127;         // floor(log2 wmax)
-        const float up = __uint_as_float((uint32_t)(134 - e) << 23);     // 2^(7-e)
+        const uint32_t eb = __float_as_uint(wmax) & 0x7f800000u;       // 2^floor(log2 wmax)
+        const float up = __uint_as_float(0x82800000u - eb);              // 2^(7-e)
+        // rint by the 1.5·2^23 shift (round half to even), then the u8 ceiling
         const float2 sc = __fmul2_rn(wv, make_float2(up, up));
-        const int wh0 = qz ? min(__float2int_rn(sc.x), 255) : 0;
-        const int wh1 = qz ? min(__float2int_rn(sc.y), 255) : 0;
-        int ws = wh0 + wh1;
-#pragma unroll
-        for (int msk = 4; msk < 32; msk <<= 1) ws += __shfl_xor_sync(kFull, ws, msk);
-        const float beta = p ? beta1 : beta0;
-        ksc[p] = qz ? beta * __uint_as_float((uint32_t)(120 + e) << 23) : 0.f;   // β·2^(e-7)
-        wsumf[p] = (float)ws;
-        sm.xb[warp].wsm[p][hs][gq] = __int2half_rn(wh0);
-        sm.xb[warp].wsm[p][hs][gq + 8] = __int2half_rn(wh1);
-        if (DEBUG && a.dbg_w) {
+        const float2 rr = __fadd2_rn(__fadd2_rn(sc, make_float2(12582912.f, 12582912.f)),
+                                     make_float2(-12582912.f, -12582912.f));
+        const float wh0 = fminf(rr.x, 255.f), wh1 = fminf(rr.y, 255.f);
+        const uint32_t wpk = qz ? half2_u32(__floats2half2_rn(wh0, wh1)) : 0u;
+        ps.wfrag[p][4 * p + hs][wfrag_pos(gq)] = wpk;
+        ksc[p] = qz ? beta[p] * __uint_as_float(eb - 0x03800000u) : 0.f;   // β·2^(e-7)
+        wsum = fmaf(ksc[p], wh0 + wh1, wsum);
+        if (DEBUG && a.dbg_w && hs < G) {
             const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
             const int pos0 = (lp0 + p) * kPage + gq;
-            if (v0[p] && pos0 < a.dbg_stride) a.dbg_w[row + pos0] = (uint8_t)wh0;
-            if (v1[p] && pos0 + 8 < a.dbg_stride) a.dbg_w[row + pos0 + 8] = (uint8_t)wh1;
+            if (v0[p] && pos0 < a.dbg_stride) a.dbg_w[row + pos0] = qz ? (uint8_t)wh0 : 0;
+            if (v1[p] && pos0 + 8 < a.dbg_stride) a.dbg_w[row + pos0 + 8] = qz ? (uint8_t)wh1 : 0;
         }
-        lsum = fmaf(beta, pp.x + pp.y, lsum);
-        bsum = fmaf(beta, fmaf(pp.x, vmn[p].x, pp.y * vmn[p].y), bsum);
+        const float2 bb = make_float2(beta[p], beta[p]);
+        lb = __ffma2_rn(bb, make_float2(pp.x + pp.y, fmaf(pp.x, vmn[p].x, pp.y * vmn[p].y)), lb);
     }
-    st.l = fmaf(st.l, alpha, lsum);
-    st.bias = fmaf(st.bias, alpha, bsum);
-
-    // ---- hand the per-(page, head) factors to the lanes whose PV columns need them:
-    // columns of lane (g', t') are page t'>>1, heads 2(t'&1) and 2(t'&1)+1, scored by
-    // lanes t'&1 and (t'&1)+2 of the same g'
-    const int srcA = (lane & ~3) | (tq & 1), srcB = srcA | 2;
-    const float kA0 = __shfl_sync(kFull, ksc[0], srcA), kA1 = __shfl_sync(kFull, ksc[1], srcA);
-    const float kB0 = __shfl_sync(kFull, ksc[0], srcB), kB1 = __shfl_sync(kFull, ksc[1], srcB);
-    const float WA0 = __shfl_sync(kFull, wsumf[0], srcA), WA1 = __shfl_sync(kFull, wsumf[1], srcA);
-    const float WB0 = __shfl_sync(kFull, wsumf[0], srcB), WB1 = __shfl_sync(kFull, wsumf[1], srcB);
-    const float kA = half ? kA1 : kA0, kB = half ? kB1 : kB0;
-    const float WA = half ? WA1 : WA0, WB = half ? WB1 : WB0;
+    st.l = fmaf(st.l, alpha, lb.x);
+    st.bias = fmaf(st.bias, alpha, lb.y);
+    st.wacc = fmaf(st.wacc, alpha, wsum);
+    if (gq == 0) {
+        ps.ksc[0][hs] = ksc[0];
+        ps.ksc[1][hs] = ksc[1];
+    }
+    // rescale of the output accumulators when a head's max moved
     if (__any_sync(kFull, alpha != 1.f)) {
-        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcB);
+        const int srcA = (lane & ~3) | (tq & 1);
+        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
 #pragma unroll
         for (int m = 0; m < 8; ++m)
 #pragma unroll
@@ -454,30 +499,25 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     }
     __syncwarp();
 
-    // ---- integer PV of both pages
-    const int pc = gq >> 2, hc = gq & 3;
-    const uint32_t wb0 = lds32(&sm.xb[warp].wsm[pc][hc][2 * tq]);
-    const uint32_t wb1 = lds32(&sm.xb[warp].wsm[pc][hc][2 * tq + 8]);
-    const uint32_t bA0 = pc == 0 ? wb0 : 0u, bA1 = pc == 0 ? wb1 : 0u;
-    const uint32_t bB0 = pc == 1 ? wb0 : 0u, bB1 = pc == 1 ? wb1 : 0u;
-    const uint4 va0 = *reinterpret_cast<const uint4*>(pg0 + kVCodeOff + lane * 32);
-    const uint4 va1 = *reinterpret_cast<const uint4*>(pg0 + kVCodeOff + lane * 32 + 16);
-    uint4 vb0 = make_uint4(0, 0, 0, 0), vb1 = make_uint4(0, 0, 0, 0);
-    if (two) {
-        vb0 = *reinterpret_cast<const uint4*>(pg1 + kVCodeOff + lane * 32);
-        vb1 = *reinterpret_cast<const uint4*>(pg1 + kVCodeOff + lane * 32 + 16);
-    }
+    // ---- integer PV of both pages; the widening offsets are removed at the flush
+    const float2 kk = *reinterpret_cast<const float2*>(&ps.ksc[half][2 * (tq & 1)]);
+    const uint2 bw0 = lds64(&ps.wfrag[0][gq][2 * tq]);
+    const uint2 bw1 = lds64(&ps.wfrag[1][gq][2 * tq]);
+    const uint4 va0 = lds128(pg0 + kVCodeOff + lane * 32);
+    const uint4 va1 = lds128(pg0 + kVCodeOff + lane * 32 + 16);
+    const uint4 vb0 = lds128(pg1 + kVCodeOff + lane * 32);
+    const uint4 vb1 = lds128(pg1 + kVCodeOff + lane * 32 + 16);
     const uint32_t vA[8] = {va0.x, va0.y, va0.z, va0.w, va1.x, va1.y, va1.z, va1.w};
     const uint32_t vB[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
-    const float ci0 = -1024.f * WA, ci1 = -1024.f * WB;
+    const float kA = kk.x, kB = kk.y;
     const float kAh = kA * 0.0625f, kBh = kB * 0.0625f;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
         float c[4];
         const uint32_t sa = vA[m] >> 8, sb = vB[m] >> 8;
-        mma_f16(c, wide_lo(vA[m]), wide_hi(vA[m]), wide_lo(sa), wide_hi(sa), bA0, bA1, ci0, ci1, ci0,
-                ci1);
-        mma_f16(c, wide_lo(vB[m]), wide_hi(vB[m]), wide_lo(sb), wide_hi(sb), bB0, bB1, c[0], c[1],
+        mma_f16(c, wide_lo(vA[m]), wide_hi(vA[m]), wide_lo(sa), wide_hi(sa), bw0.x, bw0.y, 0.f, 0.f,
+                0.f, 0.f);
+        mma_f16(c, wide_lo(vB[m]), wide_hi(vB[m]), wide_lo(sb), wide_hi(sb), bw1.x, bw1.y, c[0], c[1],
                 c[2], c[3]);
         st.o[m][0][0] = fmaf(kA, c[0], st.o[m][0][0]);
         st.o[m][0][1] = fmaf(kB, c[1], st.o[m][0][1]);
@@ -487,11 +527,6 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     __syncwarp();
 }
 
-// ---------------------------------------------------------------- protected 16-row group
-// The side group's K block (codes, K meta, V meta) and V block sit in two stages.
-// QK: lane pair (t, half) dots row t over 64 dims with dp4a against the INT8
-// query (natural dim order); PV: lane l accumulates dims 4l..4l+3 of every head
-// from bf16-dequantized 8-bit values in FP32, with weights 2^(σ − running max).
 template <int G>
 struct ProtState {
     float o[G][4];
@@ -636,6 +671,23 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 }
 
 // ---------------------------------------------------------------- split kernel
+// The two walkers of a warp (producer, consumer) live in shared memory and are
+// read and written only where a run begins or ends, so the page loop keeps
+// nothing of them in registers.
+__device__ __forceinline__ Walk walk_load(const volatile Walk& s)
+{
+    Walk w;
+    w.lo = s.lo; w.hi = s.hi; w.b = s.b; w.h = s.h; w.L = s.L; w.n = s.n; w.cbh = s.cbh;
+    w.csb = s.csb; w.slot = s.slot; w.k = s.k; w.a1 = s.a1; w.own = s.own; w.done = s.done;
+    return w;
+}
+
+__device__ __forceinline__ void walk_store(volatile Walk& d, const Walk& w)
+{
+    d.lo = w.lo; d.hi = w.hi; d.b = w.b; d.h = w.h; d.L = w.L; d.n = w.n; d.cbh = w.cbh;
+    d.csb = w.csb; d.slot = w.slot; d.k = w.k; d.a1 = w.a1; d.own = w.own; d.done = w.done;
+}
+
 template <int G, bool DEBUG>
 __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(DecodeArgs a)
 {
@@ -651,46 +703,62 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
 
     const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
     const int cp = prot_items(S), nb = (S + 15) >> 4;
-    const int total = a.plan->total_cost, span = a.plan->span;
+    const int span = a.plan->span;
     const int wg = blockIdx.x * kWarps + warp;
-    const int lo = min(total, wg * span), hi = min(total, lo + span);
+    volatile Walk& Psm = sm.walk[warp][0];
+    volatile Walk& Csm = sm.walk[warp][1];
+    {
+        const int total = a.plan->total_cost;
+        const int lo = min(total, wg * span), hi = min(total, lo + span);
+        Walk W;
+        walk_init(W, a, lo, hi, cp);
+        if (lane == 0) {
+            walk_store(Psm, W);
+            walk_store(Csm, W);
+        }
+        __syncwarp();
+    }
     const int p_first = s / kPage;
-
-    Walk P, Cw;
-    walk_init(P, a, lo, hi, cp);
-    Cw = P;
     uint32_t phase = 0;                     // bit k: parity awaited next on stage k
     int prod = 0, cons = 0;                 // items issued / consumed
     int pst = 0, cst = 0;                   // stage of the next item to issue / consume
     bool aborted = false;
 
-    // Producer: walks its own copy of the span run by run; within a run the items
-    // are consecutive pages (block-table window of 32 entries, one load per lane)
-    // or consecutive side blocks. All lanes track it; lane 0 issues.
+    // Producer: walks the span run by run; within a run the items are consecutive
+    // pages (block-table window of 32 entries, one load per lane) or consecutive
+    // side blocks. All lanes track it; lane 0 issues.
     int r_kind = -1;                        // 0 INT4 pages, 1 side blocks, 2 empty item; -1 none
-    int r_i = 0, r_end = 0, r_lp0 = 0, win_lo = 0, win = 0;
+    int r_i = 0, r_end = 0, win_lo = 0, win = 0, r_b = 0;
     const uint8_t* r_src = nullptr;
     auto next_run = [&]() -> bool {
+        Walk P = walk_load(Psm);
         if (r_kind >= 0) {                  // leave the run that just ended
             if (r_kind == 0 && P.own) P.k = P.n;
             else walk_next_bh(P, a, cp);
         }
-        if (P.done) { r_kind = -1; return false; }
-        if (P.k < P.n) {
-            r_kind = 0;
-            r_i = P.k;
-            r_end = P.a1;
-            r_lp0 = p_first;
-            r_src = a.pages + (int64_t)P.h * kPageBlock;
-            win_lo = -64;                   // force a window load
+        bool more = !P.done;
+        if (more) {
+            if (P.k < P.n) {
+                r_kind = 0;
+                r_i = P.k;
+                r_end = P.a1;
+                r_b = P.b;
+                r_src = a.pages + (int64_t)P.h * kPageBlock;
+                win_lo = -64;               // force a window load
+            } else {
+                r_kind = S > 0 ? 1 : 2;
+                r_i = 0;
+                r_end = cp;
+                const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
+                r_src = a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes;
+            }
         } else {
-            r_kind = S > 0 ? 1 : 2;
-            r_i = 0;
-            r_end = cp;
-            const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
-            r_src = a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes;
+            r_kind = -1;
         }
-        return true;
+        __syncwarp();
+        if (lane == 0) walk_store(Psm, P);
+        __syncwarp();
+        return more;
     };
     auto produce = [&]() {
         bool fenced = false;
@@ -704,14 +772,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             }
             uint64_t* bar = &sm.bar[warp][pst];
             if (r_kind == 0) {
-                const int lp = r_lp0 + r_i;
+                const int lp = p_first + r_i;
                 if (lp - win_lo >= 32 || lp < win_lo) {
                     win_lo = lp;
                     const int e = lp + lane;
                     int pg = -1;
-                    if (e < a.stride) pg = __ldg(&a.block_table[(int64_t)P.b * a.stride + e]);
+                    if (e < a.stride) pg = __ldg(&a.block_table[(int64_t)r_b * a.stride + e]);
                     // entries past the sequence's pages are never issued; report the rest
-                    if (e < r_lp0 + r_end && (e >= a.stride || pg < 0 || (int64_t)pg >= a.num_pages)) {
+                    if (e < p_first + r_end && (e >= a.stride || pg < 0 || (int64_t)pg >= a.num_pages)) {
                         report_error(a.err, e >= a.stride ? KV4_DEVERR_BAD_POSITION : KV4_DEVERR_BAD_PAGE);
                         pg = 0;
                     }
@@ -748,8 +816,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
     produce();
     int q_b = -1, q_h = -1;
     const int gq = lane >> 2, tq = lane & 3, half = tq >> 1;
-    while (!Cw.done && !aborted) {
-        const int b = Cw.b, h = Cw.h;
+    while (!aborted) {
+        int b, h, k, n, a1, L, slot;
+        {
+            const Walk C = walk_load(Csm);
+            if (C.done) break;
+            b = C.b; h = C.h; k = C.k; n = C.n; a1 = C.a1; L = C.L; slot = C.slot;
+        }
         // ---- query state of (b, h) into this warp's shared memory
         if (b != q_b || h != q_h) {
             __syncwarp();
@@ -771,37 +844,35 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             q_h = h;
         }
 
-        if (Cw.k < Cw.n) {
-            // ---- INT4 run: pages first .. last-1 of (b, h)
-            const int first = Cw.k, last = Cw.a1;
+        if (k < n) {
+            // ---- INT4 run: pages k .. a1-1 of (b, h)
             const WarpQ& wq = sm.wq[warp];
-            uint32_t qb[8][2];
             {
-                // column g' = head g'&3 over dim half g'>>2; k rows 2t', 2t'+1, 2t'+8, 2t'+9
-                // come from code lane t', whose dims lie in half t'>>1
-                const int bh = gq & 3;
-                const bool bok = (half == (gq >> 2)) && (bh < G);
+                // B column g' = head(g') over dim half g' & 1, head(n) = n < 4 ? n : n ^ 5;
+                // k rows 2t', 2t'+1, 2t'+8, 2t'+9 come from code lane t', whose dims lie in
+                // half t' >> 1. Lane (g', t') keeps the fragments of its column in qfrag.
+                const int bh = gq < 4 ? gq : (gq ^ 5);
+                const bool bok = (half == (gq & 1)) && (bh < G);
+                const int8_t* qq = wq.q8[bok ? bh : 0];
 #pragma unroll
-                for (int st = 0; st < 8; ++st) {
-                    const int base = 32 * tq + 8 * (st >> 1) + ((st & 1) ? 2 : 0);
-                    if (bok) {
-                        const int8_t* qq = wq.q8[bh];
-                        qb[st][0] = half2_bits(__int2half_rn(qq[base]), __int2half_rn(qq[base + 4]));
-                        qb[st][1] = half2_bits(__float2half_rn(0.0625f * (float)qq[base + 1]),
-                                               __float2half_rn(0.0625f * (float)qq[base + 5]));
-                    } else {
-                        qb[st][0] = 0u;
-                        qb[st][1] = 0u;
+                for (int ii = 0; ii < 4; ++ii) {
+                    uint32_t f[4];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int base = 32 * tq + 8 * ii + 2 * e;
+                        f[2 * e] = bok ? half2_bits(__int2half_rn(qq[base]), __int2half_rn(qq[base + 4])) : 0u;
+                        f[2 * e + 1] = bok ? half2_bits(__float2half_rn(0.0625f * (float)qq[base + 1]),
+                                                        __float2half_rn(0.0625f * (float)qq[base + 5]))
+                                           : 0u;
                     }
+                    sm.qfrag[warp][ii][lane] = make_uint4(f[0], f[1], f[2], f[3]);
                 }
             }
-            float cq[2];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int hh = 2 * (tq & 1) + j;
-                cq[j] = hh < G ? -wq.corr[hh][half] : 0.f;
-            }
             const int hs = 2 * (tq & 1) + half;
+            // accumulator seeds: minus the widening offsets of (head hs, half 0) and
+            // (head hs ^ 1, half 1), the two columns this lane's C fragment covers
+            const float cq0 = hs < G ? -wq.corr[hs][0] : 0.f;
+            const float cq1 = (hs ^ 1) < G ? -wq.corr[hs ^ 1][1] : 0.f;
             const float sqh = hs < G ? wq.scale[hs] : 0.f;
             const float qsh = hs < G ? wq.qsum[hs] : 0.f;
             Int4State st;
@@ -812,39 +883,61 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             st.M = -INFINITY;
             st.l = 0.f;
             st.bias = 0.f;
-            const int r4_hi = Cw.L - w;
-            for (int j = first; j < last; j += 2) {
-                const bool two = j + 1 < last;
+            st.wacc = 0.f;
+            const uint4* qf = &sm.qfrag[warp][0][lane];
+            // the weight tiles' other-page columns must read zero (the protected path
+            // shares this memory)
+            reinterpret_cast<uint4*>(&sm.xb[warp].pair.wfrag[0][0][0])[lane] = make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+            const int r4_hi = L - w;
+            for (int j = k; j < a1; j += 2) {
+                const bool two = j + 1 < a1;
                 const int s0 = cst, s1 = next_stage(cst);
                 wait_stage(s0);
                 if (two) wait_stage(s1);
-                int4_pair<G, DEBUG>(a, sm, st, qb, cq, sqh, qsh, sm.stage[warp][s0],
-                                    sm.stage[warp][s1], two, p_first + j, r4_hi, b, h, warp, lane);
+                const int lp0 = p_first + j;
+                const uint8_t* pg0 = sm.stage[warp][s0];
+                const uint8_t* pg1 = two ? sm.stage[warp][s1] : pg0;
+                // interior pairs: both pages whole and inside [s, L - w)
+                if (two && lp0 * kPage >= s && (lp0 + 2) * kPage <= r4_hi)
+                    int4_pair<G, DEBUG, false>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, true,
+                                               lp0, r4_hi, b, h, warp, lane);
+                else
+                    int4_pair<G, DEBUG, true>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, two,
+                                              lp0, r4_hi, b, h, warp, lane);
                 cons += two ? 2 : 1;
                 cst = two ? next_stage(s1) : s1;
                 produce();
             }
-            // ---- partial of this piece: normalizer and offset terms over the 8 lanes that
-            // scored a head, handed to the PV lanes; output halves (pages of a pair) over
-            // lanes t' and t' ^ 2
+            // ---- partial of this piece: normalizer, offset terms and weight sums over the
+            // 8 lanes that scored a head, handed to the PV lanes; output halves (pages of a
+            // pair) over lanes t' and t' ^ 2
 #pragma unroll
             for (int msk = 4; msk < 32; msk <<= 1) {
                 st.l += __shfl_xor_sync(kFull, st.l, msk);
                 st.bias += __shfl_xor_sync(kFull, st.bias, msk);
+                st.wacc += __shfl_xor_sync(kFull, st.wacc, msk);
             }
             const int srcA = (lane & ~3) | (tq & 1);
             const float biasA = __shfl_sync(kFull, st.bias, srcA);
             const float biasB = __shfl_sync(kFull, st.bias, srcA | 2);
+            const float waccA = __shfl_sync(kFull, st.wacc, srcA);
+            const float waccB = __shfl_sync(kFull, st.wacc, srcA | 2);
+            // rows r = 0 carry low-nibble dims (code + 1024), rows r = 1 high-nibble dims
+            // ((16 code + 1024) / 16): remove 1024 resp. 64 times the scaled weight sums
+            const float offA0 = biasA - 1024.f * waccA, offA1 = biasA - 64.f * waccA;
+            const float offB0 = biasB - 1024.f * waccB, offB1 = biasB - 64.f * waccB;
 #pragma unroll
-            for (int m = 0; m < 8; ++m)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    st.o[m][r][0] += __shfl_xor_sync(kFull, st.o[m][r][0], 2) + biasA;
-                    st.o[m][r][1] += __shfl_xor_sync(kFull, st.o[m][r][1], 2) + biasB;
-                }
-            const int base = Cw.csb + h * Cw.cbh;
+            for (int m = 0; m < 8; ++m) {
+                st.o[m][0][0] += __shfl_xor_sync(kFull, st.o[m][0][0], 2) + offA0;
+                st.o[m][0][1] += __shfl_xor_sync(kFull, st.o[m][0][1], 2) + offB0;
+                st.o[m][1][0] += __shfl_xor_sync(kFull, st.o[m][1][0], 2) + offA1;
+                st.o[m][1][1] += __shfl_xor_sync(kFull, st.o[m][1][1], 2) + offB1;
+            }
+            Walk C = walk_load(Csm);
+            const int base = C.csb + h * C.cbh;
             int idx = __ldg(&a.seg_start[b]) + (wg - base / span);
-            for (int hh = 0; hh < h; ++hh) idx += n_pieces(Cw.csb + hh * Cw.cbh, Cw.n, span);
+            for (int hh = 0; hh < h; ++hh) idx += n_pieces(C.csb + hh * C.cbh, C.n, span);
             if (tq < 2) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -858,8 +951,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                 }
             }
             if (gq == 0 && hs < G) a.part_ml[(int64_t)idx * G + hs] = make_float2(st.M, st.l);
-            if (Cw.own) Cw.k = Cw.n;
-            else walk_next_bh(Cw, a, cp);
+            if (C.own) C.k = C.n;
+            else walk_next_bh(C, a, cp);
+            __syncwarp();
+            if (lane == 0) walk_store(Csm, C);
+            __syncwarp();
         } else {
             // ---- protected unit of (b, h), owned by this span
             ProtState<G> st;
@@ -870,18 +966,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
 #pragma unroll
                 for (int d = 0; d < 4; ++d) st.o[g][d] = 0.f;
             }
-            const bool slot_ok = Cw.slot >= 0 && Cw.slot < a.max_slots;
-            const int L = slot_ok ? Cw.L : 0;
+            const bool slot_ok = slot >= 0 && slot < a.max_slots;
+            const int Lp = slot_ok ? L : 0;
             if (lane == 0) {
                 if (!slot_ok) report_error(a.err, KV4_DEVERR_BAD_SLOT);
-                else if (Cw.L != __ldg(&a.seq_len[Cw.slot])) report_error(a.err, KV4_DEVERR_LEN_MISMATCH);
+                else if (L != __ldg(&a.seq_len[slot])) report_error(a.err, KV4_DEVERR_LEN_MISMATCH);
             }
             if (S > 0) {
                 for (int grp = 0; grp < nb; ++grp) {
                     const int s0 = cst, s1 = next_stage(cst);
                     wait_stage(s0);
                     wait_stage(s1);
-                    prot_group<G, DEBUG>(a, sm, st, sm.stage[warp][s0], sm.stage[warp][s1], grp, L, b,
+                    prot_group<G, DEBUG>(a, sm, st, sm.stage[warp][s0], sm.stage[warp][s1], grp, Lp, b,
                                          h, warp, lane);
                     cons += 2;
                     cst = next_stage(s1);
@@ -903,15 +999,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     make_float4(st.o[g][0], st.o[g][1], st.o[g][2], st.o[g][3]);
                 if (lane == 0) a.part_ml[(int64_t)(b * H + h) * G + g] = make_float2(st.M[g], l);
             }
-            walk_next_bh(Cw, a, cp);
+            Walk C = walk_load(Csm);
+            walk_next_bh(C, a, cp);
+            __syncwarp();
+            if (lane == 0) walk_store(Csm, C);
+            __syncwarp();
         }
     }
 }
 
-// ---------------------------------------------------------------- merge
-// Exact log-sum-exp merge of a q head's partials (its protected unit and the span
-// pieces of its INT4 pages): M* = max M_i, O = Σ 2^(M_i − M*) o_i / Σ 2^(M_i − M*) l_i,
-// lse = (M* + log2 den) · ln 2.
 template <int G>
 __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 {

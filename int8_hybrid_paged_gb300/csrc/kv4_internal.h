@@ -14,9 +14,8 @@ constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
 constexpr int kPageBlock = 2176;         // bytes per (page, KV head)
 constexpr int kKCodeOff = 0;             // [16 tok][64 B]
-constexpr int kVCodeOff = 1024;          // [64 dim pairs][16 tok]
-constexpr int kKMetaOff = 2048;          // [16 tok] {fp16 delta, fp16 min}
-constexpr int kVMetaOff = 2112;
+constexpr int kVCodeOff = 1024;          // [64 dim pairs][16 tok], fragment order
+constexpr int kMetaOff = 2048;           // [8][K t, K t+8, V t, V t+8] {fp16 delta, fp16 min}
 constexpr int kMaxProtected = 256;       // s + w limit
 // Side buffer of one (slot, KV head): ceil((s+w)/16) groups of 16 rows, each two
 // page-sized blocks: [K codes 16x128 | K meta 16x4 | V meta 16x4] [V codes 16x128 | pad]
@@ -26,7 +25,7 @@ constexpr int kSideKMetaOff = 2048;
 constexpr int kSideVMetaOff = 2112;
 constexpr int kSideVCodeOff = kPageBlock;
 constexpr int kDecodeThreads = 128;      // 4 warps per decode CTA
-constexpr int kStages = 6;               // page stages per warp (three page pairs)
+constexpr int kStages = 5;               // page stages per warp
 
 // Device-resident decode plan, written by the prep kernel, read by split and merge.
 struct PlanHeader {

@@ -26,13 +26,14 @@ def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
     k[:, 1::2] = krow >> 4
     j = np.arange(64)[None, :]
     t = ts[:, None]
-    voff = 4 * (8 * (4 * (j % 8) + (t % 8) // 2) + j // 8) + (2 * (t % 2) + t // 8)
+    voff = 4 * (8 * (4 * (j % 8) + t % 4) + j // 8) + t // 4
     vbytes = pages[base[:, None] + 1024 + voff]
     v = np.empty((n, D), np.uint8)
     v[:, 0::2] = vbytes & 15
     v[:, 1::2] = vbytes >> 4
-    km = pages[(base + 2048 + ts * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
-    vm = pages[(base + 2112 + ts * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    mrow = base + 2048 + 16 * (ts % 8) + 4 * (ts // 8)
+    km = pages[mrow[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    vm = pages[(mrow + 8)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
     return k, v, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
 
 
