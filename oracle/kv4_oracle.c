@@ -45,6 +45,11 @@
  *      2^-64 keeps only its offsets (ŵ = 0).
  *   R6 Scores are log2-domain: σ = fl(fl(u · s_q) · C), u = fmaf(Δ, dot, fl(m · Σq8)),
  *      C = fl(sm_scale · log2 e).
+ *   R7 Protected PV ("BF16 PV, FP32 accumulation"): the side rows are taken in
+ *      groups of 16 in side-row order (sink rows, then ring slots) under a running
+ *      max M; p = exp2(σ − M) with the exp2 below; the product uses p and
+ *      v = bf16(fmaf(Δ8, c, m8)) both rounded to BF16 and sums in FP32; the
+ *      normaliser sums the unrounded p. Float mode keeps p unrounded.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -364,6 +369,20 @@ static int32_t dot_s8_u8(const int8_t *a, const uint8_t *b)
     return s;
 }
 
+/* Position held by side row i (R4, R7): sink row i < s holds position i when
+   i < L; ring row s + k holds the latest position p < L with p mod w == k, which
+   is protected when p >= max(s, L - w). -1 when the row holds no protected
+   position. */
+static int side_row_position(int i, int s, int w, int L)
+{
+    if (i < s) return (i < L) ? i : -1;
+    const int k = i - s;
+    if (L - 1 < k) return -1;
+    const int p = k + w * ((L - 1 - k) / w);
+    const int lo = (L - w > s) ? L - w : s;
+    return (p >= lo) ? p : -1;
+}
+
 /* One q head against one sequence. Returns output (normalised) and lse (natural log). */
 static void decode_head(const orc_cache *c, int slot, int L, int head,
                         const int8_t *q8, float q_scale, int32_t q_sum, float C,
@@ -374,8 +393,6 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
     /* Regions, reading R4. */
     int r4_lo = s, r4_hi = L - w;
     if (r4_hi < r4_lo) r4_hi = r4_lo;                 /* empty */
-    int sink_hi = (s < L) ? s : L;
-    int ring_lo = (L - w > s) ? (L - w) : s;
 
     /* ---- INT4 region: integer QK, page-local integer PV (reading R5) ---- */
     double M4 = -INFINITY, l4 = 0.0;
@@ -457,40 +474,54 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         }
     }
 
-    /* ---- protected region: INT8 side keys, BF16 values, plain sums ---- */
-    double Mp_ = -INFINITY, lp_ = 0.0;
+    /* ---- protected region (R7): INT8 side keys and BF16 values, side rows in
+       groups of 16 in side-row order under a running max; the product takes p
+       rounded to BF16 (integer mode) or unrounded (float mode); the normaliser
+       sums the unrounded p ---- */
+    float Mr = -INFINITY;
+    double lp_ = 0.0;
     double opr[ORC_D];
     for (int j = 0; j < ORC_D; j++) opr[j] = 0.0;
-    int npos = 0;
-    int pos_list[512];
-    for (int t = 0; t < sink_hi; t++) pos_list[npos++] = t;
-    for (int t = ring_lo; t < L; t++) pos_list[npos++] = t;
-    float sig_p[512];
-    for (int k = 0; k < npos; k++) {
-        int t = pos_list[k];
-        int sidx = (t < s) ? t : s + (t % w);
-        size_t si = idx_side(c, slot, sidx, head);
-        int32_t dot = dot_s8_u8(q8, c->k8_code + si * ORC_D);
-        float sg = score_from_dot(dot, c->k8_delta[si], c->k8_min[si], q_scale, q_sum, C);
-        sig_p[k] = sg;
-        if (dbg_qk) dbg_qk[t] = dot;
-        if (dbg_sigma) dbg_sigma[t] = sg;
-        if (sg > Mp_) Mp_ = sg;
-    }
-    for (int k = 0; k < npos; k++) {
-        int t = pos_list[k];
-        int sidx = (t < s) ? t : s + (t % w);
-        size_t si = idx_side(c, slot, sidx, head);
-        double p = exp2((double)sig_p[k] - Mp_);
-        float dv = (float)orc_f16_to_f64(c->v8_delta[si]);
-        float mv = (float)orc_f16_to_f64(c->v8_min[si]);
-        const uint8_t *vc = c->v8_code + si * ORC_D;
-        for (int j = 0; j < ORC_D; j++) {
-            float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
-            opr[j] += p * (double)v;
+    const int S = s + w;
+    for (int g0 = 0; g0 < S; g0 += 16) {
+        const int n = (S - g0 < 16) ? S - g0 : 16;
+        int pos[16];
+        float sg[16];
+        float Mg = -INFINITY;
+        for (int i = 0; i < n; i++) {
+            pos[i] = side_row_position(g0 + i, s, w, L);
+            if (pos[i] < 0) continue;
+            size_t si = idx_side(c, slot, g0 + i, head);
+            int32_t dot = dot_s8_u8(q8, c->k8_code + si * ORC_D);
+            sg[i] = score_from_dot(dot, c->k8_delta[si], c->k8_min[si], q_scale, q_sum, C);
+            if (dbg_qk) dbg_qk[pos[i]] = dot;
+            if (dbg_sigma) dbg_sigma[pos[i]] = sg[i];
+            if (sg[i] > Mg) Mg = sg[i];
         }
-        lp_ += p;
+        if (Mg == -INFINITY) continue;               /* no protected row in this group */
+        const float Mn = (Mg > Mr) ? Mg : Mr;
+        const double a = (Mr == -INFINITY) ? 0.0 : exp2((double)Mr - (double)Mn);
+        for (int j = 0; j < ORC_D; j++) opr[j] *= a;
+        lp_ *= a;
+        for (int i = 0; i < n; i++) {
+            if (pos[i] < 0) continue;
+            size_t si = idx_side(c, slot, g0 + i, head);
+            const float p = orc_exp2f(sg[i] - Mn);
+            const double pw = (pv_mode == ORC_PV_FLOAT)
+                                  ? (double)p
+                                  : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
+            float dv = (float)orc_f16_to_f64(c->v8_delta[si]);
+            float mv = (float)orc_f16_to_f64(c->v8_min[si]);
+            const uint8_t *vc = c->v8_code + si * ORC_D;
+            for (int j = 0; j < ORC_D; j++) {
+                float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
+                opr[j] += pw * (double)v;
+            }
+            lp_ += (double)p;
+        }
+        Mr = Mn;
     }
+    const double Mp_ = (double)Mr;
 
     /* ---- exact log-sum-exp merge of the two regions ---- */
     double Ms = (M4 > Mp_) ? M4 : Mp_;

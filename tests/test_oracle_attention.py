@@ -163,11 +163,13 @@ def test_float_pv_equals_single_softmax(H, s, w, lens, G):
 
 @pytest.mark.parametrize("H,s,w,lens,G", CASES)
 def test_integer_pv_within_weight_rounding_bound(H, s, w, lens, G):
-    """Integer PV differs from float PV only through ŵ: per page
-    |ŵ·s_w − p'Δ^V| ≤ s_w/2 with s_w = 2^(floor(log2 max w) − 7) (a weight that
-    rounds to 256 is held at 255, at most s_w/2 further when it is within 1 of the
-    top), so each output element moves by at most
-    Σ_pages 2^(M_page−M*) (s_w/2) Σ_t c^V_tj / den (checked with 1% slack)."""
+    """Integer PV differs from float PV only through ŵ and the BF16 rounding of the
+    protected p. Per page |ŵ·s_w − p'Δ^V| ≤ s_w/2 with s_w = 2^(floor(log2 max w) − 7)
+    (a weight that rounds to 256 is held at 255, at most s_w/2 further when it is
+    within 1 of the top), so each output element moves by at most
+    Σ_pages 2^(M_page−M*) (s_w/2) Σ_t c^V_tj / den; a protected p rounded to BF16
+    (8 significant bits) moves by at most 2^-8 of itself, so each protected position
+    adds at most 2^-8 2^(σ_t−M*) |v_tj| / den (all checked with 1% slack)."""
     sm = 1 / math.sqrt(D)
     c, _ = make_cache(H, s, w, lens)
     q = inputs.bf16_bits(inputs.queries(len(lens), H * G, seed=6))
@@ -192,6 +194,12 @@ def test_integer_pv_within_weight_rounding_bound(H, s, w, lens, G):
                 held = (wts / sw >= 255.5) if sw > 0 else np.zeros(len(ts), bool)
                 csum = csum + codes[held].sum(axis=0)          # held at 255: one more s_w/2
                 bound += 2.0 ** (Mp - Ms) * (sw / 2) * csum
+            _, prot = regions(L, s, w)
+            for t_ in prot:
+                i = side_index(t_, s, w)
+                v32 = (f16v(c.v8_delta[b, i, h]) * c.v8_code[b, i, h].astype(np.float64)
+                       + f16v(c.v8_min[b, i, h])).astype(np.float32)
+                bound += 2.0 ** -8 * 2.0 ** (sig[t_] - Ms) * np.abs(bf16_round(v32))
             bound = bound / den * 1.01 + 1e-9
             assert np.all(np.abs(o_int[hq] - o_flt[hq]) <= bound)
             for pg in sorted({t // 16 for t in r4}):
