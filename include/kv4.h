@@ -86,13 +86,16 @@ typedef struct {
  *                 V of token r+8], so one 16-byte load brings both tokens a lane scores
  * Side pool: max_slots * H_kv blocks of side_block_bytes = ceil((s+w)/16) * 4352;
  * block (slot, h) at (slot * H_kv + h) * side_block_bytes. Side row i (i = p for a
- * sink position p < s, i = s + p mod w for a ring position) is row i%16 of group
- * i/16; group g starts at g * 4352 and holds, like two pages:
- *   [0,    2048)  INT8-grid K codes (u8, rotated K) of its 16 rows, 128 bytes each
- *   [2048, 2112)  K metadata {fp16 delta, fp16 min} per row
- *   [2112, 2176)  V metadata per row
- *   [2176, 4224)  INT8-grid V codes (u8) of its 16 rows
- *   [4224, 4352)  unused
+ * sink position p < s, i = s + p mod w for a ring position) is row r = i%16 of group
+ * i/16; group g starts at g * 4352 and holds two 2176-byte blocks. For dim d write
+ * u = d%32, e = (u%8/2)%2, b = 2*(u%2) + (u%8)/4 and word W = 2*(u/8) + e; a code
+ * byte (u8, INT8 grid) sits at:
+ *   K block [0, 2176):    1024*(W/4) + 64*r + 16*(d/32) + 4*(W%4) + b   (rotated K)
+ *                         K metadata {fp16 delta, fp16 min} of row r at 2048 + 8*(r%8) + 4*(r/8)
+ *   V block [2176, 4352): with n = 4*(d%8) + r%4, W' = 2*(d/16) + (d/8)%2 and
+ *                         b' = (r/8)%2 + 2*((r/4)%2): 2176 + 16*(32*(W'/4) + n) + 4*(W'%4) + b'
+ *                         V metadata of row r at 2176 + 2048 + 16*(r%4) + 4*b'
+ * so each lane of a warp reads its tensor-core fragments with 16-byte loads.
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128

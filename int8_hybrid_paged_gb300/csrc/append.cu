@@ -25,6 +25,29 @@ __device__ __forceinline__ int v_byte_offset(int j, int t)
     return ((((j & 7) << 2) + (t & 3)) * 8 + (j >> 3)) * 4 + (t >> 2);
 }
 
+// Side K code byte of (row r, dim d): the QK A fragments of the protected path take,
+// per 32-dim chunk t = d / 32, eight words [u, u+4, u+1, u+5] (u = 8 i + 2 e) in two
+// planes, so one byte permute widens two codes of one fragment register.
+__device__ __forceinline__ int side_k_offset(int r, int d)
+{
+    const int u = d & 31, r8 = u & 7;
+    const int word = 2 * (u >> 3) + ((r8 >> 1) & 1);
+    const int byte = ((r8 & 1) << 1) | (r8 >> 2);
+    return 1024 * (word >> 2) + 64 * r + 16 * (d >> 5) + 4 * (word & 3) + byte;
+}
+
+// Byte of side row r inside a V fragment word (rows t, t+8, t+4, t+12 with t = r % 4).
+__device__ __forceinline__ int side_v_byte(int r) { return ((r >> 3) & 1) | (((r >> 2) & 1) << 1); }
+
+// Side V code byte of (row r, dim d): lane n = 4 (d % 8) + r % 4 of the PV A fragments,
+// word 2 (d / 16) + (d / 8) % 2 of its sixteen, stored as four 512-byte planes.
+__device__ __forceinline__ int side_v_offset(int r, int d)
+{
+    const int n = 4 * (d & 7) + (r & 3);
+    const int word = 2 * (d >> 4) + ((d >> 3) & 1);
+    return 16 * (32 * (word >> 2) + n) + 4 * (word & 3) + side_v_byte(r);
+}
+
 __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
 {
     const int lane = threadIdx.x & 31;
@@ -102,21 +125,23 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
         warp_quant<255>(kx, k8, k8d, k8m);
         warp_quant<255>(vx, v8, v8d, v8m);
         uint8_t* sb = a.side + ((int64_t)slot * a.num_heads + h) * a.side_block_bytes;
-        const uint32_t kw = k8[0] | (k8[1] << 8) | (k8[2] << 16) | (k8[3] << 24);
-        const uint32_t vw = v8[0] | (v8[1] << 8) | (v8[2] << 16) | (v8[3] << 24);
         int idx[2];
         int n = 0;
         if (to_sink) idx[n++] = pos;
         if (to_ring) idx[n++] = s + pos % w;
         for (int k = 0; k < n; ++k) {
-            // side row r lives in group r/16: [K rows | K meta | V meta] then [V rows | pad]
-            uint8_t* g = sb + (idx[k] >> 4) * (2 * kPageBlock);
+            uint8_t* g = sb + (idx[k] >> 4) * kSideGroupBytes;
             const int rr = idx[k] & 15;
-            *reinterpret_cast<uint32_t*>(g + kSideKCodeOff + rr * 128 + 4 * lane) = kw;
-            *reinterpret_cast<uint32_t*>(g + kSideVCodeOff + rr * 128 + 4 * lane) = vw;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                g[kSideKCodeOff + side_k_offset(rr, 4 * lane + i)] = (uint8_t)k8[i];
+                g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
+            }
             if (lane == 0) {
-                *reinterpret_cast<__half2*>(g + kSideKMetaOff + rr * 4) = __halves2half2(k8d, k8m);
-                *reinterpret_cast<__half2*>(g + kSideVMetaOff + rr * 4) = __halves2half2(v8d, v8m);
+                *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
+                    __halves2half2(k8d, k8m);
+                *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
+                    __halves2half2(v8d, v8m);
             }
         }
     }

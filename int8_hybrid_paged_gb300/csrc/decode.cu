@@ -43,7 +43,8 @@ struct __align__(16) WarpQ {
     int8_t q8[kMaxG][kHeadDim];
     float scale[kMaxG];
     float qsum[kMaxG];
-    float corr[kMaxG][2];
+    float corr[kMaxG][2];     // INT4 widening offsets per dim half
+    float corr8[kMaxG][2];    // INT8 (side) widening offsets per dim half
 };
 
 // Span walker state (one per producer and consumer of a warp): the current (b, h) of
@@ -70,8 +71,7 @@ struct __align__(128) SplitSmem {
     WarpQ wq[kWarps];
     uint4 qfrag[kWarps][4][32];                   // QK B fragments: [k step pair][lane]
     union {
-        PairSmem pair;                            // INT4 runs
-        float pbuf[kMaxG][16];                    // protected weights of a 16-row group
+        PairSmem pair;                            // PV B operands of a page pair / side group
     } xb[kWarps];
     Walk walk[kWarps][2];                         // producer, consumer
     uint64_t bar[kWarps][kStages];
@@ -190,12 +190,17 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
     }
     const float corr = 1024.f * (float)se + 64.f * (float)so;
     const float corr_hi = __shfl_sync(kFull, corr, 16);
+    // INT8 side codes widen to 1024 + c in either slot: 1024·Σ q per dim half
+    const float corr8 = 1024.f * (float)(se + so);
+    const float corr8_hi = __shfl_sync(kFull, corr8, 16);
     const uint32_t packed = (uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
                             ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24);
     uint8_t* rec = a.qinfo + (int64_t)gw * kQInfoBytes;
     *reinterpret_cast<uint32_t*>(rec + 4 * lane) = packed;
-    if (lane == 0)
+    if (lane == 0) {
         *reinterpret_cast<float4*>(rec + kHeadDim) = make_float4(sq, (float)qsum, corr, corr_hi);
+        *reinterpret_cast<float4*>(rec + kHeadDim + 16) = make_float4(corr8, corr8_hi, 0.f, 0.f);
+    }
     if (a.dbg_q8) *reinterpret_cast<uint32_t*>(a.dbg_q8 + (int64_t)gw * kHeadDim + 4 * lane) = packed;
     if (a.dbg_qscale && lane == 0) a.dbg_qscale[gw] = sq;
 }
@@ -527,28 +532,56 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     __syncwarp();
 }
 
-template <int G>
+// ---------------------------------------------------------------- protected group
+// One 16-row side group on the tensor cores, lane roles as on an INT4 page.
+// QK: an INT8 code widens to 1024 + c in a low slot and to 16384 + 16c in a high
+// slot (whose query entry is q/16), one byte permute per two codes, so the query
+// B fragments of the INT4 path serve unchanged and every slot carries 1024 q.
+// PV: values dequantized to BF16 (A; rows = dims), weights p rounded to BF16 (B;
+// columns = heads, k order t, t+8, t+4, t+12 so a scoring lane's pair of rows is
+// one B word), FP32 accumulation straight into the running output.
 struct ProtState {
-    float o[G][4];
-    float M[G];
-    float l[G];        // this lane's share of the normalizer
+    float o[8][4];     // lanes t' < 2: dims 16m + g' (+8) of heads 2t', 2t' + 1
+    float M, l;        // running max and normalizer share of head hs
 };
 
-template <int G>
-struct HeadSplit {
-    static constexpr int GL = (G >= 2) ? G / 2 : 1;
-    __device__ static int head(int half, int j) { return (G >= 2) ? half * GL + j : 0; }
-    __device__ static bool owns(int half, int gg) { return (G >= 2) ? (gg / GL == half) : (half == 0); }
-};
-
-template <int G>
-__device__ __forceinline__ float pickf(const float (&v)[G], int g)
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1, float c0, float c1,
+                                         float c2, float c3)
 {
-    float r = v[0];
-#pragma unroll
-    for (int gg = 1; gg < G; ++gg)
-        if (gg == g) r = v[gg];
-    return r;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
+}
+
+// INT8 codes of bytes 0, 1 as fp16 1024 + c; of bytes 2, 3 as fp16 16384 + 16c
+__device__ __forceinline__ uint32_t w8_lo(uint32_t w) { return prmt(w, 0x64646464u, 0x4140u); }
+__device__ __forceinline__ uint32_t w8_hi(uint32_t w) { return prmt(w, 0x74747474u, 0x4342u); }
+
+__device__ __forceinline__ uint32_t bf16x2_u32(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Four side V codes of one dim (rows t, t+8, t+4, t+12) to two BF16 pairs
+// bf16(fmaf(Δ, c, m)) with each row's metadata.
+__device__ __forceinline__ void dequant_word(uint32_t w, float2 dA, float2 mA, float2 dB, float2 mB,
+                                             uint32_t& lo, uint32_t& hi)
+{
+    const float k = 8388608.0f;                      // 2^23: float bits 0x4b0000cc = 2^23 + c
+    const float x0 = __uint_as_float(prmt(w, 0x4b000000u, 0x7440u));
+    const float x1 = __uint_as_float(prmt(w, 0x4b000000u, 0x7441u));
+    const float x2 = __uint_as_float(prmt(w, 0x4b000000u, 0x7442u));
+    const float x3 = __uint_as_float(prmt(w, 0x4b000000u, 0x7443u));
+    const float2 c01 = __fadd2_rn(make_float2(x0, x1), make_float2(-k, -k));
+    const float2 c23 = __fadd2_rn(make_float2(x2, x3), make_float2(-k, -k));
+    const float2 v01 = __ffma2_rn(dA, c01, mA);
+    const float2 v23 = __ffma2_rn(dB, c23, mB);
+    lo = bf16x2_u32(v01.x, v01.y);
+    hi = bf16x2_u32(v23.x, v23.y);
 }
 
 // Position held by side row rr at context length L, or -1 if the row is not in
@@ -564,103 +597,97 @@ __device__ __forceinline__ int side_row_position(int rr, int s, int w, int L)
 }
 
 template <int G, bool DEBUG>
-__device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, ProtState<G>& st,
-                                           const uint8_t* pk, const uint8_t* pv, int grp, int L,
-                                           int b, int h, int warp, int lane)
+__device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, ProtState& st,
+                                           const uint4* __restrict__ qf, float cq0, float cq1,
+                                           float sqh, float qsh, const uint8_t* pk,
+                                           const uint8_t* pv, int grp, int L, int b, int h,
+                                           int warp, int lane)
 {
-    using HS = HeadSplit<G>;
-    constexpr int GL = HS::GL;
-    const int t = lane >> 1, half = lane & 1;
-    const int s = a.sink, w = a.window;
-    const int pos = side_row_position(grp * 16 + t, s, w, L);
-    const bool valid = pos >= 0;
-    const unsigned vmask = __ballot_sync(kFull, valid);   // row r valid <=> bit 2r
-    const WarpQ& wq = sm.wq[warp];
+    const int gq = lane >> 2, tq = lane & 3, half = tq >> 1;
+    const int hs = 2 * (tq & 1) + half;
+    PairSmem& ps = sm.xb[warp].pair;
 
-    int dot[G];
+    // ---- INT8 QK of rows gq, gq + 8 (two planes of four words per row and lane)
+    const uint4 k00 = lds128(pk + kSideKCodeOff + 64 * gq + 16 * tq);
+    const uint4 k01 = lds128(pk + kSideKCodeOff + 1024 + 64 * gq + 16 * tq);
+    const uint4 k10 = lds128(pk + kSideKCodeOff + 64 * (gq + 8) + 16 * tq);
+    const uint4 k11 = lds128(pk + kSideKCodeOff + 1024 + 64 * (gq + 8) + 16 * tq);
+    const uint32_t wa[8] = {k00.x, k00.y, k00.z, k00.w, k01.x, k01.y, k01.z, k01.w};
+    const uint32_t wb[8] = {k10.x, k10.y, k10.z, k10.w, k11.x, k11.y, k11.z, k11.w};
+    float d[4] = {cq0, cq1, cq0, cq1};
 #pragma unroll
-    for (int g = 0; g < G; ++g) dot[g] = 0;
+    for (int ii = 0; ii < 4; ++ii) {
+        const uint4 qv = qf[32 * ii];
+        mma_f16(d, w8_lo(wa[2 * ii]), w8_lo(wb[2 * ii]), w8_hi(wa[2 * ii]), w8_hi(wb[2 * ii]), qv.x,
+                qv.y, d[0], d[1], d[2], d[3]);
+        mma_f16(d, w8_lo(wa[2 * ii + 1]), w8_lo(wb[2 * ii + 1]), w8_hi(wa[2 * ii + 1]),
+                w8_hi(wb[2 * ii + 1]), qv.z, qv.w, d[0], d[1], d[2], d[3]);
+    }
+    const float r0 = __shfl_xor_sync(kFull, d[1], 2);
+    const float r1 = __shfl_xor_sync(kFull, d[3], 2);
+    const float2 dot = __fadd2_rn(make_float2(d[0], d[2]), make_float2(r0, r1));
+    const uint2 kmw = lds64(pk + kSideKMetaOff + 8 * gq);
+    const __half2 km0 = u32_half2(kmw.x), km1 = u32_half2(kmw.y);
+    const float2 kd = make_float2(__low2float(km0), __low2float(km1));
+    const float2 kmin = make_float2(__high2float(km0), __high2float(km1));
+    const float2 u = __ffma2_rn(kd, dot, __fmul2_rn(kmin, make_float2(qsh, qsh)));
+    const float2 sg =
+        __fmul2_rn(__fmul2_rn(u, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
+    const int pos0 = side_row_position(16 * grp + gq, a.sink, a.window, L);
+    const int pos1 = side_row_position(16 * grp + gq + 8, a.sink, a.window, L);
+    const float2 sig = make_float2(pos0 >= 0 ? sg.x : -INFINITY, pos1 >= 0 ? sg.y : -INFINITY);
+    if (DEBUG && a.dbg_qk && hs < G) {
+        const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
+        if (pos0 >= 0 && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = (int)dot.x;
+        if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_qk[row + pos1] = (int)dot.y;
+    }
+
+    // ---- running max of head hs; weights relative to it, rounded to BF16 for PV
+    float m = fmaxf(sig.x, sig.y);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-        const uint4 c4 = *reinterpret_cast<const uint4*>(pk + kSideKCodeOff + t * 128 + half * 64 + q4 * 16);
+    for (int msk = 4; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
+    const float Mn = fmaxf(st.M, m);
+    const float alpha = (Mn == -INFINITY) ? 1.f : exp2_fast(st.M - Mn);
+    st.M = Mn;
+    // masked rows give -inf - Mn (NaN while nothing is valid yet): exp2_poly2 returns 0
+    const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(-Mn, -Mn)));
+    st.l = fmaf(st.l, alpha, pp.x + pp.y);
+    ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
+    if (__any_sync(kFull, alpha != 1.f)) {
+        const int srcA = (lane & ~3) | (tq & 1);
+        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const uint4 qv = *reinterpret_cast<const uint4*>(&wq.q8[g][half * 64 + q4 * 16]);
-            dot[g] = dp4a_su(qv.x, c4.x, dot[g]);
-            dot[g] = dp4a_su(qv.y, c4.y, dot[g]);
-            dot[g] = dp4a_su(qv.z, c4.z, dot[g]);
-            dot[g] = dp4a_su(qv.w, c4.w, dot[g]);
+        for (int mm = 0; mm < 8; ++mm) {
+            st.o[mm][0] *= aA;
+            st.o[mm][1] *= aB;
+            st.o[mm][2] *= aA;
+            st.o[mm][3] *= aB;
         }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) dot[g] += __shfl_xor_sync(kFull, dot[g], 1);
-    const __half2 km = *reinterpret_cast<const __half2*>(pk + kSideKMetaOff + t * 4);
-    const float kd = __low2float(km), kmin = __high2float(km);
-
-    float sig[GL], gmax[GL];
-#pragma unroll
-    for (int j = 0; j < GL; ++j) {
-        const int g = HS::head(half, j);
-        int d = dot[0];
-#pragma unroll
-        for (int gg = 1; gg < G; ++gg)
-            if (gg == g) d = dot[gg];
-        const float u = __fmaf_rn(kd, (float)d, __fmul_rn(kmin, wq.qsum[g]));
-        sig[j] = valid ? __fmul_rn(__fmul_rn(u, wq.scale[g]), a.log2_scale) : -INFINITY;
-        float m = sig[j];
-#pragma unroll
-        for (int msk = 2; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
-        gmax[j] = m;
-        if (DEBUG && valid && a.dbg_qk && pos < a.dbg_stride && (G >= 2 || half == 0))
-            a.dbg_qk[((int64_t)b * a.num_q_heads + h * G + g) * a.dbg_stride + pos] = d;
-    }
-    float Mall[G];
-    {
-        float other[GL];
-#pragma unroll
-        for (int j = 0; j < GL; ++j) other[j] = __shfl_xor_sync(kFull, gmax[j], 1);
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg)
-            Mall[gg] = (G >= 2) ? ((gg / GL == half) ? gmax[gg % GL] : other[gg % GL]) : gmax[0];
-    }
-    float alpha[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float Mn = fmaxf(st.M[g], Mall[g]);
-        alpha[g] = (Mn == -INFINITY) ? 1.f : (st.M[g] == -INFINITY ? 0.f : exp2_fast(st.M[g] - Mn));
-        st.M[g] = Mn;
-    }
-    float p[GL];
-#pragma unroll
-    for (int j = 0; j < GL; ++j) {
-        const int g = HS::head(half, j);
-        p[j] = valid ? exp2_poly(__fsub_rn(sig[j], pickf<G>(st.M, g))) : 0.f;
-        if (G >= 2 || half == 0) sm.xb[warp].pbuf[g][t] = p[j];
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float contrib = HS::owns(half, g) ? p[(G >= 2) ? g % GL : 0] : 0.f;
-        st.l[g] = st.l[g] * alpha[g] + contrib;
-#pragma unroll
-        for (int d = 0; d < 4; ++d) st.o[g][d] *= alpha[g];
     }
     __syncwarp();
-    for (int tt = 0; tt < 16; ++tt) {
-        if (!((vmask >> (2 * tt)) & 1u)) continue;                        // uniform
-        const uint32_t vcw = lds32(pv + (kSideVCodeOff - kPageBlock) + tt * 128 + 4 * lane);
-        const __half2 vm = *reinterpret_cast<const __half2*>(pk + kSideVMetaOff + tt * 4);
-        const float vd = __low2float(vm), vmin = __high2float(vm);
-        float v[4];
+
+    // ---- BF16 PV, FP32 accumulation into the running output
+    const uint2 bw = lds64(&ps.wfrag[0][gq][2 * tq]);
+    const uint4 vmw = lds128(pv + (kSideVMetaOff - kPageBlock) + 16 * tq);
+    const __half2 vt0 = u32_half2(vmw.x), vt8 = u32_half2(vmw.y);
+    const __half2 vt4 = u32_half2(vmw.z), vt12 = u32_half2(vmw.w);
+    const float2 dA = make_float2(__low2float(vt0), __low2float(vt8));
+    const float2 mA = make_float2(__high2float(vt0), __high2float(vt8));
+    const float2 dB = make_float2(__low2float(vt4), __low2float(vt12));
+    const float2 mB = make_float2(__high2float(vt4), __high2float(vt12));
+    uint4 vq[4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-            v[m] = __bfloat162float(
-                __float2bfloat16_rn(__fmaf_rn(vd, (float)((vcw >> (8 * m)) & 255u), vmin)));
+    for (int i = 0; i < 4; ++i) vq[i] = lds128(pv + (kSideVCodeOff - kPageBlock) + 16 * (32 * i + lane));
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float pw = sm.xb[warp].pbuf[g][tt];
-#pragma unroll
-            for (int m = 0; m < 4; ++m) st.o[g][m] = fmaf(pw, v[m], st.o[g][m]);
-        }
+    for (int mm = 0; mm < 8; ++mm) {
+        const uint4 q4 = vq[mm >> 1];
+        const uint32_t w0 = (mm & 1) ? q4.z : q4.x;      // dim 16 mm + gq
+        const uint32_t w1 = (mm & 1) ? q4.w : q4.y;      // dim 16 mm + gq + 8
+        uint32_t a0, a1, a2, a3;
+        dequant_word(w0, dA, mA, dB, mB, a0, a2);
+        dequant_word(w1, dA, mA, dB, mB, a1, a3);
+        mma_bf16(st.o[mm], a0, a1, a2, a3, bw.x, bw.y, st.o[mm][0], st.o[mm][1], st.o[mm][2],
+                 st.o[mm][3]);
     }
     __syncwarp();
 }
@@ -834,26 +861,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             }
             if (lane < G) {
                 const float4 f = __ldg(reinterpret_cast<const float4*>(rec + lane * kQInfoBytes + kHeadDim));
+                const float4 f8 =
+                    __ldg(reinterpret_cast<const float4*>(rec + lane * kQInfoBytes + kHeadDim + 16));
                 sm.wq[warp].scale[lane] = f.x;
                 sm.wq[warp].qsum[lane] = f.y;
                 sm.wq[warp].corr[lane][0] = f.z;
                 sm.wq[warp].corr[lane][1] = f.w;
+                sm.wq[warp].corr8[lane][0] = f8.x;
+                sm.wq[warp].corr8[lane][1] = f8.y;
             }
             __syncwarp();
-            q_b = b;
-            q_h = h;
-        }
-
-        if (k < n) {
-            // ---- INT4 run: pages k .. a1-1 of (b, h)
-            const WarpQ& wq = sm.wq[warp];
             {
-                // B column g' = head(g') over dim half g' & 1, head(n) = n < 4 ? n : n ^ 5;
-                // k rows 2t', 2t'+1, 2t'+8, 2t'+9 come from code lane t', whose dims lie in
-                // half t' >> 1. Lane (g', t') keeps the fragments of its column in qfrag.
+                // QK B fragments. Column g' = head(g') over dim half g' & 1 with
+                // head(n) = n < 4 ? n : n ^ 5; k rows 2t', 2t'+1, 2t'+8, 2t'+9 come from code
+                // lane t', whose dims lie in half t' >> 1. Lane (g', t') keeps its column's
+                // fragments; the high slots hold q/16.
                 const int bh = gq < 4 ? gq : (gq ^ 5);
                 const bool bok = (half == (gq & 1)) && (bh < G);
-                const int8_t* qq = wq.q8[bok ? bh : 0];
+                const int8_t* qq = sm.wq[warp].q8[bok ? bh : 0];
 #pragma unroll
                 for (int ii = 0; ii < 4; ++ii) {
                     uint32_t f[4];
@@ -868,13 +893,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     sm.qfrag[warp][ii][lane] = make_uint4(f[0], f[1], f[2], f[3]);
                 }
             }
-            const int hs = 2 * (tq & 1) + half;
+            __syncwarp();
+            q_b = b;
+            q_h = h;
+        }
+        const WarpQ& wq = sm.wq[warp];
+        const int hs = 2 * (tq & 1) + half;
+        const float sqh = hs < G ? wq.scale[hs] : 0.f;
+        const float qsh = hs < G ? wq.qsum[hs] : 0.f;
+        const uint4* qf = &sm.qfrag[warp][0][lane];
+        // the weight tiles' unused columns must read zero; the other run kind shares them
+        reinterpret_cast<uint4*>(&sm.xb[warp].pair.wfrag[0][0][0])[lane] = make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+
+        if (k < n) {
+            // ---- INT4 run: pages k .. a1-1 of (b, h)
             // accumulator seeds: minus the widening offsets of (head hs, half 0) and
             // (head hs ^ 1, half 1), the two columns this lane's C fragment covers
             const float cq0 = hs < G ? -wq.corr[hs][0] : 0.f;
             const float cq1 = (hs ^ 1) < G ? -wq.corr[hs ^ 1][1] : 0.f;
-            const float sqh = hs < G ? wq.scale[hs] : 0.f;
-            const float qsh = hs < G ? wq.qsum[hs] : 0.f;
             Int4State st;
 #pragma unroll
             for (int m = 0; m < 8; ++m)
@@ -884,11 +921,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             st.l = 0.f;
             st.bias = 0.f;
             st.wacc = 0.f;
-            const uint4* qf = &sm.qfrag[warp][0][lane];
-            // the weight tiles' other-page columns must read zero (the protected path
-            // shares this memory)
-            reinterpret_cast<uint4*>(&sm.xb[warp].pair.wfrag[0][0][0])[lane] = make_uint4(0u, 0u, 0u, 0u);
-            __syncwarp();
             const int r4_hi = L - w;
             for (int j = k; j < a1; j += 2) {
                 const bool two = j + 1 < a1;
@@ -958,14 +990,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             __syncwarp();
         } else {
             // ---- protected unit of (b, h), owned by this span
-            ProtState<G> st;
+            ProtState st;
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                st.M[g] = -INFINITY;
-                st.l[g] = 0.f;
+            for (int mm = 0; mm < 8; ++mm)
 #pragma unroll
-                for (int d = 0; d < 4; ++d) st.o[g][d] = 0.f;
-            }
+                for (int r = 0; r < 4; ++r) st.o[mm][r] = 0.f;
+            st.M = -INFINITY;
+            st.l = 0.f;
+            const float cq0 = hs < G ? -wq.corr8[hs][0] : 0.f;
+            const float cq1 = (hs ^ 1) < G ? -wq.corr8[hs ^ 1][1] : 0.f;
             const bool slot_ok = slot >= 0 && slot < a.max_slots;
             const int Lp = slot_ok ? L : 0;
             if (lane == 0) {
@@ -977,8 +1010,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     const int s0 = cst, s1 = next_stage(cst);
                     wait_stage(s0);
                     wait_stage(s1);
-                    prot_group<G, DEBUG>(a, sm, st, sm.stage[warp][s0], sm.stage[warp][s1], grp, Lp, b,
-                                         h, warp, lane);
+                    prot_group<G, DEBUG>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
+                                         sm.stage[warp][s1], grp, Lp, b, h, warp, lane);
                     cons += 2;
                     cst = next_stage(s1);
                     produce();
@@ -989,16 +1022,22 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                 cst = next_stage(cst);
                 produce();
             }
+#pragma unroll
+            for (int msk = 4; msk < 32; msk <<= 1) st.l += __shfl_xor_sync(kFull, st.l, msk);
             float* po = a.part_o + ((int64_t)(b * H + h) * G) * kHeadDim;
+            if (tq < 2) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float l = st.l[g];
+                for (int j = 0; j < 2; ++j) {
+                    const int hd = 2 * tq + j;
+                    if (hd >= G) continue;
 #pragma unroll
-                for (int msk = 16; msk > 0; msk >>= 1) l += __shfl_xor_sync(kFull, l, msk);
-                *reinterpret_cast<float4*>(po + g * kHeadDim + 4 * lane) =
-                    make_float4(st.o[g][0], st.o[g][1], st.o[g][2], st.o[g][3]);
-                if (lane == 0) a.part_ml[(int64_t)(b * H + h) * G + g] = make_float2(st.M[g], l);
+                    for (int mm = 0; mm < 8; ++mm) {
+                        po[hd * kHeadDim + 16 * mm + gq] = st.o[mm][j];
+                        po[hd * kHeadDim + 16 * mm + gq + 8] = st.o[mm][2 + j];
+                    }
+                }
             }
+            if (gq == 0 && hs < G) a.part_ml[(int64_t)(b * H + h) * G + hs] = make_float2(st.M, st.l);
             Walk C = walk_load(Csm);
             walk_next_bh(C, a, cp);
             __syncwarp();

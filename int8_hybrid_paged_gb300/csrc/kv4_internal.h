@@ -18,12 +18,16 @@ constexpr int kVCodeOff = 1024;          // [64 dim pairs][16 tok], fragment ord
 constexpr int kMetaOff = 2048;           // [8][K t, K t+8, V t, V t+8] {fp16 delta, fp16 min}
 constexpr int kMaxProtected = 256;       // s + w limit
 // Side buffer of one (slot, KV head): ceil((s+w)/16) groups of 16 rows, each two
-// page-sized blocks: [K codes 16x128 | K meta 16x4 | V meta 16x4] [V codes 16x128 | pad]
+// page-sized blocks laid out for the tensor-core fragments of the protected path:
+//   K block: codes in two 1024-byte planes [16 rows][4 lanes][4 words], K meta
+//            [8][row r, row r+8] at 2048
+//   V block: codes [4][32 lanes][4 words] (PV A fragments), V meta [4][rows
+//            t, t+8, t+4, t+12] at 2048
 constexpr int kSideGroupBytes = 2 * kPageBlock;
 constexpr int kSideKCodeOff = 0;
 constexpr int kSideKMetaOff = 2048;
-constexpr int kSideVMetaOff = 2112;
 constexpr int kSideVCodeOff = kPageBlock;
+constexpr int kSideVMetaOff = kPageBlock + 2048;
 constexpr int kDecodeThreads = 128;      // 4 warps per decode CTA
 constexpr int kStages = 5;               // page stages per warp
 
@@ -35,7 +39,8 @@ struct PlanHeader {
     int32_t pad;
 };
 
-constexpr int kQInfoBytes = 144;   // per q head: 128 INT8 query bytes + {s_q, Σq8, offsets x2}
+constexpr int kQInfoBytes = 160;   // per q head: 128 INT8 query bytes, {s_q, Σq8, INT4 offsets x2},
+                                   // {INT8 offsets x2, 0, 0}
 
 // Pointers into a decode workspace (cache-owned or the static no-allocation array).
 struct DecodeWorkspace {

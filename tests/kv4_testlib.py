@@ -37,17 +37,42 @@ def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
     return k, v, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
 
 
+def side_k_offset(r, d):
+    """Byte of (side row r, dim d) in a group's K block, as declared in include/kv4.h."""
+    u = d % 32
+    e = (u % 8 // 2) % 2
+    byte = 2 * (u % 2) + (u % 8) // 4
+    word = 2 * (u // 8) + e
+    return 1024 * (word // 4) + 64 * r + 16 * (d // 32) + 4 * (word % 4) + byte
+
+
+def side_v_byte(r):
+    return (r // 8) % 2 + 2 * ((r // 4) % 2)
+
+
+def side_v_offset(r, d):
+    """Byte of (side row r, dim d) in a group's V block, as declared in include/kv4.h."""
+    n = 4 * (d % 8) + r % 4
+    word = 2 * (d // 16) + (d // 8) % 2
+    return 16 * (32 * (word // 4) + n) + 4 * (word % 4) + side_v_byte(r)
+
+
 def unpack_side(side, side_block, H, S, slot, h):
-    """INT8 side rows 0..S-1 of (slot, head h): 16-row groups of two 2176-byte blocks
-    ([K codes | K meta | V meta] [V codes | pad]), as declared in include/kv4.h."""
+    """INT8 side rows 0..S-1 of (slot, head h): 16-row groups of a K block and a V block
+    in tensor-core fragment order, as declared in include/kv4.h."""
     blk = side[(slot * H + h) * side_block:(slot * H + h + 1) * side_block]
     r = np.arange(S)
     g = (r // 16) * 4352
     rr = r % 16
-    k8 = blk[(g + rr * 128)[:, None] + np.arange(128)[None, :]]
-    v8 = blk[(g + 2176 + rr * 128)[:, None] + np.arange(128)[None, :]]
-    km = blk[(g + 2048 + rr * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
-    vm = blk[(g + 2112 + rr * 4)[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    d = np.arange(128)
+    koff = np.array([[side_k_offset(x, y) for y in d] for x in range(16)])
+    voff = np.array([[side_v_offset(x, y) for y in d] for x in range(16)])
+    k8 = blk[g[:, None] + koff[rr]]
+    v8 = blk[g[:, None] + 2176 + voff[rr]]
+    kmo = g + 2048 + 8 * (rr % 8) + 4 * (rr // 8)
+    vmo = g + 2176 + 2048 + 16 * (rr % 4) + 4 * np.array([side_v_byte(x) for x in rr], dtype=np.int64)
+    km = blk[kmo[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    vm = blk[vmo[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
     return k8, v8, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
 
 
