@@ -1047,6 +1047,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
     }
 }
 
+// ---------------------------------------------------------------- merge
+// Exact log-sum-exp merge, one warp per q head: the protected unit's partial and
+// those of the INT4 run pieces of its (b, h). Lane k loads the (max, normalizer)
+// of item k; every lane then loads its four dims of eight items at once, so the
+// merge costs a few load round trips whatever the number of pieces.
 template <int G>
 __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 {
@@ -1060,30 +1065,47 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
     const int cbh = n + cp, csb = a.cost_start[b];
     int first = a.seg_start[b];
     for (int hh = 0; hh < h; ++hh) first += n_pieces(csb + hh * cbh, n, span);
-    const int cnt = n_pieces(csb + h * cbh, n, span);
+    const int nit = n_pieces(csb + h * cbh, n, span) + 1;       // item 0: protected partial
     auto item = [&](int k) { return k == 0 ? b * H + h : first + k - 1; };
     float Mx = -INFINITY;
-    for (int k = lane; k <= cnt; k += 32) Mx = fmaxf(Mx, a.part_ml[(int64_t)item(k) * G + g].x);
+    for (int c0 = 0; c0 < nit; c0 += 32)
+        if (c0 + lane < nit) Mx = fmaxf(Mx, __ldg(&a.part_ml[(int64_t)item(c0 + lane) * G + g].x));
     Mx = warp_max(Mx);
     float den = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     if (Mx != -INFINITY) {
-        for (int k = 0; k <= cnt; ++k) {
-            const int it = item(k);
-            const float2 ml = a.part_ml[(int64_t)it * G + g];
-            if (ml.x == -INFINITY) continue;
-            const float f = exp2f(ml.x - Mx);
-            den = fmaf(f, ml.y, den);
-            const float4 v = *reinterpret_cast<const float4*>(
-                &a.part_o[((int64_t)it * G + g) * kHeadDim + 4 * lane]);
-            o.x = fmaf(f, v.x, o.x);
-            o.y = fmaf(f, v.y, o.y);
-            o.z = fmaf(f, v.z, o.z);
-            o.w = fmaf(f, v.w, o.w);
+        for (int c0 = 0; c0 < nit; c0 += 8) {
+            float f = 0.f;
+            if (lane < 8 && c0 + lane < nit) {
+                const float2 ml = __ldg(&a.part_ml[(int64_t)item(c0 + lane) * G + g]);
+                if (ml.x != -INFINITY) {
+                    f = exp2f(ml.x - Mx);
+                    den = fmaf(f, ml.y, den);
+                }
+            }
+            float4 v[8];
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int it = item(min(c0 + kk, nit - 1));      // weight 0 past the last item
+                v[kk] = __ldg(reinterpret_cast<const float4*>(
+                    &a.part_o[((int64_t)it * G + g) * kHeadDim + 4 * lane]));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const float fk = __shfl_sync(kFull, f, kk);
+                o.x = fmaf(fk, v[kk].x, o.x);
+                o.y = fmaf(fk, v[kk].y, o.y);
+                o.z = fmaf(fk, v[kk].z, o.z);
+                o.w = fmaf(fk, v[kk].w, o.w);
+            }
         }
+        den = warp_sum(den);
     }
     float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (den > 0.f) res = make_float4(o.x / den, o.y / den, o.z / den, o.w / den);
+    if (den > 0.f) {
+        const float r = 1.f / den;
+        res = make_float4(o.x * r, o.y * r, o.z * r, o.w * r);
+    }
     *reinterpret_cast<float4*>(&a.out[((int64_t)b * a.num_q_heads + hq) * kHeadDim + 4 * lane]) = res;
     if (a.lse && lane == 0)
         a.lse[(int64_t)b * a.num_q_heads + hq] =

@@ -57,6 +57,12 @@ __device__ __forceinline__ float warp_min(float v)
     for (int m = 16; m > 0; m >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, m));
     return v;
 }
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(kFull, v, m);
+    return v;
+}
 __device__ __forceinline__ int warp_sum_int(int v)
 {
 #pragma unroll
