@@ -746,14 +746,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
         __syncwarp();
     }
     const int p_first = s / kPage;
-    uint32_t phase = 0;                     // bit k: parity awaited next on stage k
     int prod = 0, cons = 0;                 // items issued / consumed
     int pst = 0, cst = 0;                   // stage of the next item to issue / consume
+    uint32_t cph = 0;                       // parity awaited on stage cst (flips as cst wraps)
     bool aborted = false;
+    const uint32_t stage0 = smem_u32(&sm.stage[warp][0][0]);
+    const uint32_t bar0 = smem_u32(&sm.bar[warp][0]);
+    const uint32_t is_l0 = lane == 0;
 
     // Producer: walks the span run by run; within a run the items are consecutive
     // pages (block-table window of 32 entries, one load per lane) or consecutive
-    // side blocks. All lanes track it; lane 0 issues.
+    // side blocks. All lanes track it; lane 0 issues (predicated, no branch).
     int r_kind = -1;                        // 0 INT4 pages, 1 side blocks, 2 empty item; -1 none
     int r_i = 0, r_end = 0, win_lo = 0, win = 0, r_b = 0;
     const uint8_t* r_src = nullptr;
@@ -788,19 +791,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
         return more;
     };
     auto produce = [&]() {
-        bool fenced = false;
         while (prod < cons + kStages) {
-            if (r_kind < 0 || r_i >= r_end) {
+            if (r_i >= r_end) {
                 if (!next_run()) break;
             }
-            if (!fenced) {
-                if (lane == 0) fence_proxy_async();
-                fenced = true;
-            }
-            uint64_t* bar = &sm.bar[warp][pst];
+            const uint32_t bar = bar0 + 8u * pst;
+            const uint32_t dst = stage0 + (uint32_t)(kPageBlock * pst);
             if (r_kind == 0) {
                 const int lp = p_first + r_i;
-                if (lp - win_lo >= 32 || lp < win_lo) {
+                if ((unsigned)(lp - win_lo) >= 32u) {
                     win_lo = lp;
                     const int e = lp + lane;
                     int pg = -1;
@@ -813,32 +812,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     win = pg;
                 }
                 const int page = __shfl_sync(kFull, win, lp - win_lo);
-                if (lane == 0) {
-                    mbar_expect_tx(bar, kPageBlock);
-                    bulk_g2s(sm.stage[warp][pst], r_src + (int64_t)page * H * kPageBlock, kPageBlock, bar);
-                }
+                issue_bulk(dst, r_src + (int64_t)page * H * kPageBlock, kPageBlock, bar, is_l0);
             } else if (r_kind == 1) {
-                if (lane == 0) {
-                    mbar_expect_tx(bar, kPageBlock);
-                    bulk_g2s(sm.stage[warp][pst], r_src + (int64_t)r_i * kPageBlock, kPageBlock, bar);
-                }
-            } else if (lane == 0) {
-                mbar_arrive(bar);           // empty protected item: no side buffer
+                issue_bulk(dst, r_src + (int64_t)r_i * kPageBlock, kPageBlock, bar, is_l0);
+            } else {
+                arrive_pred(bar, is_l0);    // empty protected item: no side buffer
             }
             ++r_i;
             ++prod;
-            if (++pst == kStages) pst = 0;
+            pst = (pst + 1 == kStages) ? 0 : pst + 1;
         }
     };
-    auto wait_stage = [&](int stg) {
-        const bool okw = aborted || mbar_wait_bounded(&sm.bar[warp][stg], (phase >> stg) & 1u);
-        phase ^= 1u << stg;
-        if (!okw) {
-            if (lane == 0) report_error(a.err, KV4_DEVERR_WAIT_TIMEOUT);
-            aborted = true;
+    // consume the next item: wait for its stage, advance the consumer position
+    auto wait_next = [&]() -> int {
+        const int stg = cst;
+        if (!aborted) {
+            const uint32_t bar = bar0 + 8u * stg;
+            if (!mbar_try_wait_at(bar, cph) && !mbar_wait_slow(bar, cph)) {
+                if (lane == 0) report_error(a.err, KV4_DEVERR_WAIT_TIMEOUT);
+                aborted = true;
+            }
         }
+        if (++cst == kStages) {
+            cst = 0;
+            cph ^= 1u;
+        }
+        ++cons;
+        return stg;
     };
-    auto next_stage = [](int x) { return x + 1 == kStages ? 0 : x + 1; };
 
     produce();
     int q_b = -1, q_h = -1;
@@ -924,12 +925,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             const int r4_hi = L - w;
             for (int j = k; j < a1; j += 2) {
                 const bool two = j + 1 < a1;
-                const int s0 = cst, s1 = next_stage(cst);
-                wait_stage(s0);
-                if (two) wait_stage(s1);
+                const int s0 = wait_next();
+                const int s1 = two ? wait_next() : s0;
                 const int lp0 = p_first + j;
                 const uint8_t* pg0 = sm.stage[warp][s0];
-                const uint8_t* pg1 = two ? sm.stage[warp][s1] : pg0;
+                const uint8_t* pg1 = sm.stage[warp][s1];
                 // interior pairs: both pages whole and inside [s, L - w)
                 if (two && lp0 * kPage >= s && (lp0 + 2) * kPage <= r4_hi)
                     int4_pair<G, DEBUG, false>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, true,
@@ -937,8 +937,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                 else
                     int4_pair<G, DEBUG, true>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, two,
                                               lp0, r4_hi, b, h, warp, lane);
-                cons += two ? 2 : 1;
-                cst = two ? next_stage(s1) : s1;
                 produce();
             }
             // ---- partial of this piece: normalizer, offset terms and weight sums over the
@@ -1007,19 +1005,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             }
             if (S > 0) {
                 for (int grp = 0; grp < nb; ++grp) {
-                    const int s0 = cst, s1 = next_stage(cst);
-                    wait_stage(s0);
-                    wait_stage(s1);
+                    const int s0 = wait_next();
+                    const int s1 = wait_next();
                     prot_group<G, DEBUG>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
                                          sm.stage[warp][s1], grp, Lp, b, h, warp, lane);
-                    cons += 2;
-                    cst = next_stage(s1);
                     produce();
                 }
             } else {
-                wait_stage(cst);
-                cons += 1;
-                cst = next_stage(cst);
+                wait_next();
                 produce();
             }
 #pragma unroll

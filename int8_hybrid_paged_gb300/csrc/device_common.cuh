@@ -263,6 +263,53 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Lane-predicated (pred != 0) arm of `bar` for `bytes` and 1-D bulk copy global ->
+// shared completing on it: one asm block, no branch around it.
+__device__ __forceinline__ void issue_bulk(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                           uint32_t pred)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %2;\n\t"
+        "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "r"(pred)
+        : "memory");
+}
+
+// Lane-predicated plain arrive on `bar` (an item with nothing to copy).
+__device__ __forceinline__ void arrive_pred(uint32_t bar, uint32_t pred)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar), "r"(pred)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_at(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(20000u)
+        : "memory");
+    return ok != 0;
+}
+
+// Slow path of a wait whose first try failed: retry, giving up after ~2 s.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_at(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > 2000000000ull) return false;
+    }
+}
+
 // Wait for phase `parity` of `bar`, giving up after ~2 s. Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity)
 {
