@@ -790,7 +790,26 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
         __syncwarp();
         return more;
     };
+    const int64_t page_stride = (int64_t)H * kPageBlock;
     auto produce = [&]() {
+        // common case: two more pages of the current INT4 run, both inside the
+        // block-table window, and two free stages
+        if (r_kind == 0 && prod + 2 <= cons + kStages && r_i + 2 <= r_end) {
+            const int o0 = p_first + r_i - win_lo;
+            if ((unsigned)o0 < 31u) {
+                const int pg0 = __shfl_sync(kFull, win, o0);
+                const int pg1 = __shfl_sync(kFull, win, o0 + 1);
+                const int p1 = (pst + 1 == kStages) ? 0 : pst + 1;
+                issue_bulk(stage0 + (uint32_t)(kPageBlock * pst), r_src + (int64_t)pg0 * page_stride,
+                           kPageBlock, bar0 + 8u * pst, is_l0);
+                issue_bulk(stage0 + (uint32_t)(kPageBlock * p1), r_src + (int64_t)pg1 * page_stride,
+                           kPageBlock, bar0 + 8u * p1, is_l0);
+                r_i += 2;
+                prod += 2;
+                pst = (p1 + 1 == kStages) ? 0 : p1 + 1;
+                return;
+            }
+        }
         while (prod < cons + kStages) {
             if (r_i >= r_end) {
                 if (!next_run()) break;
@@ -812,7 +831,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
                     win = pg;
                 }
                 const int page = __shfl_sync(kFull, win, lp - win_lo);
-                issue_bulk(dst, r_src + (int64_t)page * H * kPageBlock, kPageBlock, bar, is_l0);
+                issue_bulk(dst, r_src + (int64_t)page * page_stride, kPageBlock, bar, is_l0);
             } else if (r_kind == 1) {
                 issue_bulk(dst, r_src + (int64_t)r_i * kPageBlock, kPageBlock, bar, is_l0);
             } else {
