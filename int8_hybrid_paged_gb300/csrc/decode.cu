@@ -240,6 +240,8 @@ __device__ __forceinline__ uint32_t wide_lo(uint32_t w)
     return and_or(w, 0x000F000Fu, 0x64006400u);
 }
 // nibbles 1 and 5 of w as fp16 (1024 + 16 n1, 1024 + 16 n5)
+// bytes 0 and 2 whole (two nibbles) as fp16 1024 + byte
+__device__ __forceinline__ uint32_t wide_byte(uint32_t w) { return and_or(w, 0x00ff00ffu, 0x64006400u); }
 __device__ __forceinline__ uint32_t wide_hi(uint32_t w)
 {
     return and_or(w, 0x00F000F0u, 0x64006400u);
@@ -519,10 +521,13 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
         float c[4];
-        const uint32_t sa = vA[m] >> 8, sb = vB[m] >> 8;
-        mma_f16(c, wide_lo(vA[m]), wide_hi(vA[m]), wide_lo(sa), wide_hi(sa), bw0.x, bw0.y, 0.f, 0.f,
+        // rows g' (dim 2j) take the whole byte, 1024 + lo + 16 hi; rows g' + 8 (dim 2j+1)
+        // take 1024 + 16 hi; the flush removes 16 x the second from the first
+        const uint32_t xa = prmt(vA[m], 0x64646464u, 0x4341u);
+        const uint32_t xb = prmt(vB[m], 0x64646464u, 0x4341u);
+        mma_f16(c, wide_byte(vA[m]), wide_hi(vA[m]), xa, xa & 0xfff0fff0u, bw0.x, bw0.y, 0.f, 0.f,
                 0.f, 0.f);
-        mma_f16(c, wide_lo(vB[m]), wide_hi(vB[m]), wide_lo(sb), wide_hi(sb), bw1.x, bw1.y, c[0], c[1],
+        mma_f16(c, wide_byte(vB[m]), wide_hi(vB[m]), xb, xb & 0xfff0fff0u, bw1.x, bw1.y, c[0], c[1],
                 c[2], c[3]);
         st.o[m][0][0] = fmaf(kA, c[0], st.o[m][0][0]);
         st.o[m][0][1] = fmaf(kB, c[1], st.o[m][0][1]);
@@ -972,16 +977,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(Dec
             const float biasB = __shfl_sync(kFull, st.bias, srcA | 2);
             const float waccA = __shfl_sync(kFull, st.wacc, srcA);
             const float waccB = __shfl_sync(kFull, st.wacc, srcA | 2);
-            // rows r = 0 carry low-nibble dims (code + 1024), rows r = 1 high-nibble dims
-            // ((16 code + 1024) / 16): remove 1024 resp. 64 times the scaled weight sums
-            const float offA0 = biasA - 1024.f * waccA, offA1 = biasA - 64.f * waccA;
-            const float offB0 = biasB - 1024.f * waccB, offB1 = biasB - 64.f * waccB;
+            // rows r = 1 (dim 2j+1) carry (1024 + 16 code)/16: remove 64 x the scaled weight
+            // sums; rows r = 0 (dim 2j) carry 1024 + code(2j) + 16 code(2j+1): remove 16 x
+            // the raw r = 1 value, which takes the offset and the other nibble with it
+            const float offA1 = biasA - 64.f * waccA, offB1 = biasB - 64.f * waccB;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
-                st.o[m][0][0] += __shfl_xor_sync(kFull, st.o[m][0][0], 2) + offA0;
-                st.o[m][0][1] += __shfl_xor_sync(kFull, st.o[m][0][1], 2) + offB0;
-                st.o[m][1][0] += __shfl_xor_sync(kFull, st.o[m][1][0], 2) + offA1;
-                st.o[m][1][1] += __shfl_xor_sync(kFull, st.o[m][1][1], 2) + offB1;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float lo = st.o[m][0][c] + __shfl_xor_sync(kFull, st.o[m][0][c], 2);
+                    const float hi = st.o[m][1][c] + __shfl_xor_sync(kFull, st.o[m][1][c], 2);
+                    st.o[m][0][c] = fmaf(-16.f, hi, lo) + (c ? biasB : biasA);
+                    st.o[m][1][c] = hi + (c ? offB1 : offA1);
+                }
             }
             Walk C = walk_load(Csm);
             const int base = C.csb + h * C.cbh;
