@@ -87,6 +87,10 @@ __device__ __forceinline__ int int4_pages(int L, int s, int w)
 // or one empty item when there is no side buffer (so every (b, h) has a unit).
 __device__ __forceinline__ int prot_items(int S) { return S > 0 ? 2 * ((S + 15) >> 4) : 1; }
 
+// Cost-line length of a (b, h) unit: its n INT4 pages, its cp protected items and the
+// positions that stand for its setup and flush.
+__device__ __forceinline__ int unit_cost(int n, int cp) { return n + cp + kUnitOverhead; }
+
 // Number of warp-span pieces of the INT4 pages [base, base + n) of the cost line.
 __device__ __forceinline__ int n_pieces(int base, int n, int span)
 {
@@ -135,7 +139,7 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
         const int per = (B + 1023) / 1024;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int cost = 0;
-        for (int b = b0; b < b1; ++b) cost += H * (int4_pages(max(0, a.context_lens[b]), s, w) + cp);
+        for (int b = b0; b < b1; ++b) cost += H * unit_cost(int4_pages(max(0, a.context_lens[b]), s, w), cp);
         int total = 0;
         int off = block_scan(cost, s_scan, total);
         const int span = max(1, (total + a.num_warps - 1) / a.num_warps);
@@ -143,8 +147,8 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
         for (int b = b0; b < b1; ++b) {
             a.cost_start[b] = off;
             const int n = int4_pages(max(0, a.context_lens[b]), s, w);
-            for (int h = 0; h < H; ++h) segs += n_pieces(off + h * (n + cp), n, span);
-            off += H * (n + cp);
+            for (int h = 0; h < H; ++h) segs += n_pieces(off + h * unit_cost(n, cp), n, span);
+            off += H * unit_cost(n, cp);
         }
         int nseg = 0;
         int soff = block_scan(segs, s_scan, nseg);
@@ -153,7 +157,7 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
             a.seg_start[b] = base + soff;
             const int n = int4_pages(max(0, a.context_lens[b]), s, w);
             const int cs = a.cost_start[b];
-            for (int h = 0; h < H; ++h) soff += n_pieces(cs + h * (n + cp), n, span);
+            for (int h = 0; h < H; ++h) soff += n_pieces(cs + h * unit_cost(n, cp), n, span);
         }
         if (tid == 1023) {
             a.cost_start[B] = total;
@@ -268,7 +272,7 @@ __device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b,
     W.b = b;
     W.L = max(0, __ldg(&a.context_lens[b]));
     W.n = int4_pages(W.L, a.sink, a.window);
-    W.cbh = W.n + cp;
+    W.cbh = unit_cost(W.n, cp);
     W.csb = __ldg(&a.cost_start[b]);
     W.slot = __ldg(&a.slot_ids[b]);
 }
@@ -721,7 +725,7 @@ __device__ __forceinline__ void walk_store(volatile Walk& d, const Walk& w)
 }
 
 template <int G, bool DEBUG>
-__global__ void __launch_bounds__(kDecodeThreads, 4) kv4_decode_split_kernel(DecodeArgs a)
+__global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
@@ -1082,7 +1086,7 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
     const int h = hq / G, g = hq - h * G;
     const int H = a.num_heads, cp = prot_items(a.sink + a.window), span = a.plan->span;
     const int n = int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
-    const int cbh = n + cp, csb = a.cost_start[b];
+    const int cbh = unit_cost(n, cp), csb = a.cost_start[b];
     int first = a.seg_start[b];
     for (int hh = 0; hh < h; ++hh) first += n_pieces(csb + hh * cbh, n, span);
     const int nit = n_pieces(csb + h * cbh, n, span) + 1;       // item 0: protected partial

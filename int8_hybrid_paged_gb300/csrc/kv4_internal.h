@@ -28,8 +28,11 @@ constexpr int kSideKCodeOff = 0;
 constexpr int kSideKMetaOff = 2048;
 constexpr int kSideVCodeOff = kPageBlock;
 constexpr int kSideVMetaOff = kPageBlock + 2048;
-constexpr int kDecodeThreads = 128;      // 4 warps per decode CTA
+constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per SM
 constexpr int kStages = 5;               // page stages per warp
+// Cost-line positions charged to every (sequence, KV head) unit beyond its stage
+// items: the run setup and flush it costs its warps (no items sit there).
+constexpr int kUnitOverhead = 12;
 
 // Device-resident decode plan, written by the prep kernel, read by split and merge.
 struct PlanHeader {
