@@ -32,7 +32,7 @@ constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per
 constexpr int kStages = 5;               // page stages per warp
 // Cost-line positions charged to every (sequence, KV head) unit beyond its stage
 // items: the run setup and flush it costs its warps (no items sit there).
-constexpr int kUnitOverhead = 12;
+constexpr int kUnitOverhead = 8;
 
 // Device-resident decode plan, written by the prep kernel, read by split and merge.
 struct PlanHeader {
