@@ -46,9 +46,10 @@
  *   R6 Scores are log2-domain: σ = fl(fl(u · s_q) · C), u = fmaf(Δ, dot, fl(m · Σq8)),
  *      C = fl(sm_scale · log2 e).
  *   R7 Protected PV ("BF16 PV, FP32 accumulation"): the side rows are taken in
- *      groups of 16 in side-row order (sink rows, then ring slots) under a running
- *      max M; p = exp2(σ − M) with the exp2 below; the product uses p and
- *      v = bf16(fmaf(Δ8, c, m8)) both rounded to BF16 and sums in FP32; the
+ *      groups of 16 in side-row order (sink rows, then ring slots); in each group
+ *      p = exp2(σ − M_group) with the exp2 below and the group's own max; the
+ *      product uses p and v = bf16(fmaf(Δ8, c, m8)) both rounded to BF16 and sums
+ *      in FP32; groups are combined by 2^(M_group − M) like INT4 pages; the
  *      normaliser sums the unrounded p. Float mode keeps p unrounded.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
@@ -475,9 +476,9 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
     }
 
     /* ---- protected region (R7): INT8 side keys and BF16 values, side rows in
-       groups of 16 in side-row order under a running max; the product takes p
-       rounded to BF16 (integer mode) or unrounded (float mode); the normaliser
-       sums the unrounded p ---- */
+       groups of 16 in side-row order, p against each group's own max; the
+       product takes p rounded to BF16 (integer mode) or unrounded (float mode);
+       the normaliser sums the unrounded p ---- */
     float Mr = -INFINITY;
     double lp_ = 0.0;
     double opr[ORC_D];
@@ -499,14 +500,15 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
             if (sg[i] > Mg) Mg = sg[i];
         }
         if (Mg == -INFINITY) continue;               /* no protected row in this group */
-        const float Mn = (Mg > Mr) ? Mg : Mr;
-        const double a = (Mr == -INFINITY) ? 0.0 : exp2((double)Mr - (double)Mn);
-        for (int j = 0; j < ORC_D; j++) opr[j] *= a;
-        lp_ *= a;
+        /* the group's output relative to its own max, then folded into the region
+           total relative to the running max */
+        double og[ORC_D];
+        double lg = 0.0;
+        for (int j = 0; j < ORC_D; j++) og[j] = 0.0;
         for (int i = 0; i < n; i++) {
             if (pos[i] < 0) continue;
             size_t si = idx_side(c, slot, g0 + i, head);
-            const float p = orc_exp2f(sg[i] - Mn);
+            const float p = orc_exp2f(sg[i] - Mg);
             const double pw = (pv_mode == ORC_PV_FLOAT)
                                   ? (double)p
                                   : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
@@ -515,10 +517,15 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
             const uint8_t *vc = c->v8_code + si * ORC_D;
             for (int j = 0; j < ORC_D; j++) {
                 float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
-                opr[j] += pw * (double)v;
+                og[j] += pw * (double)v;
             }
-            lp_ += (double)p;
+            lg += (double)p;
         }
+        const float Mn = (Mg > Mr) ? Mg : Mr;
+        const double a = (Mr == -INFINITY) ? 0.0 : exp2((double)Mr - (double)Mn);
+        const double bsc = exp2((double)Mg - (double)Mn);
+        for (int j = 0; j < ORC_D; j++) opr[j] = opr[j] * a + og[j] * bsc;
+        lp_ = lp_ * a + lg * bsc;
         Mr = Mn;
     }
     const double Mp_ = (double)Mr;
