@@ -206,15 +206,15 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
  *   other arguments : as kv4_decode_attention
  * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 160 bytes
- * per q head plus G * 520 bytes for each of 2 * batch * H_kv + (persistent warps: 16 per SM)
- * partials (on a 152-SM GB300 with H_q = 32, H_kv = 8 that is batch <= 305); larger
- * calls return KV4_ERR_OUT_OF_RANGE before anything is enqueued. The first call on each device looks up the scratch
- * array's device address with that device current; make that first call before
- * any stream capture. Every call on a device shares the one array and leaves
- * its contents behind (each call rewrites what it reads, including the work
- * counter that must start at zero), so calls whose kernels overlap on the GPU
- * race: issue them on one stream. Device-side index errors are skipped without
- * a report (there is no cache error word here).
+ * per q head, 4 bytes per (sequence, KV head) and G * 520 bytes for each of
+ * 2 * batch * H_kv + (persistent warps: 16 per SM) partials (on a 152-SM GB300 with
+ * H_q = 32, H_kv = 8 that is batch <= 304); larger calls return KV4_ERR_OUT_OF_RANGE
+ * before anything is enqueued. The first call on each device looks up the scratch
+ * array's device address with that device current; make that first call before any
+ * stream capture. Every call on a device shares the one array and leaves its contents
+ * behind (each call writes everything it reads there before reading it), so calls
+ * whose kernels overlap on the GPU race: issue them on one stream. Device-side index
+ * errors are skipped without a report (there is no cache error word here).
  */
 kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
                                         const void *page_pool_dev, const void *side_pool_dev,

@@ -244,7 +244,7 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     kv4::decode_workspace_bytes(batch, num_q_heads, H, G, c->grid[G], &ws, c->ws);
     a.plan = ws.plan;
     a.cost_start = ws.cost_start;
-    a.seg_start = ws.seg_start;
+    a.unit_seg = ws.unit_seg;
     a.qinfo = ws.qinfo;
     a.part_o = ws.part_o;
     a.part_ml = ws.part_ml;

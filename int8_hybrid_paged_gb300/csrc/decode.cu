@@ -55,7 +55,7 @@ struct Walk {
     int L, n, cbh, csb, slot;   // of the current b
     int k;                      // current item of (b, h): k < n INT4 page, else protected item
     int a1;                     // end of the span's INT4 pages of (b, h)
-    int own;                    // this span owns (b, h)'s protected unit
+    int g0, g1;                 // the span's protected groups of (b, h): first items in [lo, hi)
     int done;
 };
 
@@ -91,12 +91,31 @@ __device__ __forceinline__ int prot_items(int S) { return S > 0 ? 2 * ((S + 15) 
 // positions that stand for its setup and flush.
 __device__ __forceinline__ int unit_cost(int n, int cp) { return n + cp + kUnitOverhead; }
 
+// Protected groups of a unit: ceil(S/16) groups of two stage items (a side K block and
+// a side V block), or one empty item when there is no side buffer.
+__device__ __forceinline__ int group_items(int cp) { return cp > 1 ? 2 : 1; }
+__device__ __forceinline__ int prot_groups(int cp) { return cp > 1 ? cp >> 1 : 1; }
+// Cost-line extent from the first to the last group's first item (inclusive).
+__device__ __forceinline__ int prot_span_len(int cp) { return group_items(cp) * (prot_groups(cp) - 1) + 1; }
+// Groups of a unit whose first item lies before cost position pstart + x.
+__device__ __forceinline__ int groups_before(int x, int cp)
+{
+    const int gi = group_items(cp);
+    return x <= 0 ? 0 : min(prot_groups(cp), (x + gi - 1) / gi);
+}
+
 // Number of warp-span pieces of the INT4 pages [base, base + n) of the cost line.
 __device__ __forceinline__ int n_pieces(int base, int n, int span)
 {
     return n > 0 ? (base + n - 1) / span - base / span + 1 : 0;
 }
 
+// First partial of unit (b, h), laid out by the plan: per unit its INT4 pieces, then
+// its protected pieces (spans holding the first item of one of its groups).
+__device__ __forceinline__ int unit_first_partial(const DecodeArgs& a, int b, int h)
+{
+    return __ldg(&a.unit_seg[b * a.num_heads + h]);
+}
 // Block-wide exclusive scan over 1024 threads; returns the thread's offset and the total.
 __device__ __forceinline__ int block_scan(int v, int* s_scan, int& total)
 {
@@ -142,29 +161,34 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
         for (int b = b0; b < b1; ++b) cost += H * unit_cost(int4_pages(max(0, a.context_lens[b]), s, w), cp);
         int total = 0;
         int off = block_scan(cost, s_scan, total);
-        const int span = max(1, (total + a.num_warps - 1) / a.num_warps);
+        const int span = max(2, (total + a.num_warps - 1) / a.num_warps);
         int segs = 0;
         for (int b = b0; b < b1; ++b) {
             a.cost_start[b] = off;
             const int n = int4_pages(max(0, a.context_lens[b]), s, w);
-            for (int h = 0; h < H; ++h) segs += n_pieces(off + h * unit_cost(n, cp), n, span);
+            for (int h = 0; h < H; ++h) {
+                const int base = off + h * unit_cost(n, cp);
+                segs += n_pieces(base, n, span) + n_pieces(base + n, prot_span_len(cp), span);
+            }
             off += H * unit_cost(n, cp);
         }
         int nseg = 0;
         int soff = block_scan(segs, s_scan, nseg);
-        const int base = B * H;                        // protected partials come first
         for (int b = b0; b < b1; ++b) {
-            a.seg_start[b] = base + soff;
             const int n = int4_pages(max(0, a.context_lens[b]), s, w);
             const int cs = a.cost_start[b];
-            for (int h = 0; h < H; ++h) soff += n_pieces(cs + h * unit_cost(n, cp), n, span);
+            for (int h = 0; h < H; ++h) {
+                a.unit_seg[b * H + h] = soff;
+                const int base = cs + h * unit_cost(n, cp);
+                soff += n_pieces(base, n, span) + n_pieces(base + n, prot_span_len(cp), span);
+            }
         }
         if (tid == 1023) {
             a.cost_start[B] = total;
-            a.seg_start[B] = base + nseg;
+            a.unit_seg[B * H] = nseg;
             a.plan->total_cost = total;
             a.plan->span = span;
-            a.plan->total_items = base + nseg;
+            a.plan->total_items = nseg;
         }
         return;
     }
@@ -278,15 +302,16 @@ __device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b,
 }
 
 // Position the walker at the first item of (b, h) inside the span; false if none.
-__device__ __forceinline__ bool walk_enter(Walk& W)
+__device__ __forceinline__ bool walk_enter(Walk& W, int cp)
 {
     const int base = W.csb + W.h * W.cbh;
     const int a0 = max(W.lo, base) - base;
     W.a1 = min(W.hi, base + W.n) - base;
     const int pstart = base + W.n;
-    W.own = pstart >= W.lo && pstart < W.hi;
+    W.g0 = groups_before(W.lo - pstart, cp);
+    W.g1 = groups_before(W.hi - pstart, cp);
     if (a0 < W.a1) { W.k = a0; return true; }
-    if (W.own) { W.k = W.n; return true; }
+    if (W.g0 < W.g1) { W.k = W.n + group_items(cp) * W.g0; return true; }
     return false;
 }
 
@@ -299,7 +324,7 @@ __device__ __forceinline__ void walk_next_bh(Walk& W, const DecodeArgs& a, int c
             W.h = 0;
         }
         if (W.csb + W.h * W.cbh >= W.hi) { W.done = true; return; }
-        if (walk_enter(W)) return;
+        if (walk_enter(W, cp)) return;
     }
 }
 
@@ -316,21 +341,9 @@ __device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, 
     }
     walk_load_b(W, a, l, cp);
     W.h = min(a.num_heads - 1, (lo - W.csb) / W.cbh);
-    if (!walk_enter(W)) walk_next_bh(W, a, cp);
+    if (!walk_enter(W, cp)) walk_next_bh(W, a, cp);
 }
 
-// one item forward
-__device__ __forceinline__ void walk_step(Walk& W, const DecodeArgs& a, int cp)
-{
-    if (W.k < W.n) {
-        if (++W.k < W.a1) return;
-        if (W.own) { W.k = W.n; return; }
-        walk_next_bh(W, a, cp);
-        return;
-    }
-    if (++W.k < W.n + cp) return;
-    walk_next_bh(W, a, cp);
-}
 
 // ---------------------------------------------------------------- INT4 page pair
 // Lane (g', t') = (lane >> 2, lane & 3) scores tokens g' and g' + 8 of each page for
@@ -546,9 +559,9 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
 // QK: an INT8 code widens to 1024 + c in a low slot and to 16384 + 16c in a high
 // slot (whose query entry is q/16), one byte permute per two codes, so the query
 // B fragments of the INT4 path serve unchanged and every slot carries 1024 q.
-// PV: values dequantized to BF16 (A; rows = dims), weights p rounded to BF16 (B;
-// columns = heads, k order t, t+8, t+4, t+12 so a scoring lane's pair of rows is
-// one B word), FP32 accumulation straight into the running output.
+// PV: values dequantized to BF16 (A; rows = dims), weights p against the group's max
+// rounded to BF16 (B; columns = heads, k order t, t+8, t+4, t+12 so a scoring lane's
+// pair of rows is one B word), FP32 accumulation, folded into the running output.
 struct ProtState {
     float o[8][4];     // lanes t' < 2: dims 16m + g' (+8) of heads 2t', 2t' + 1
     float M, l;        // running max and normalizer share of head hs
@@ -655,15 +668,20 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     float m = fmaxf(sig.x, sig.y);
 #pragma unroll
     for (int msk = 4; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
+    // weights against the group's own max (so their BF16 rounding does not depend on
+    // which groups share a piece), folded in by 2^(group max - running max)
     const float Mn = fmaxf(st.M, m);
-    const float alpha = (Mn == -INFINITY) ? 1.f : exp2_fast(st.M - Mn);
+    const bool none = (Mn == -INFINITY);
+    const float alpha = none ? 1.f : exp2_fast(st.M - Mn);
+    const float beta = none ? 0.f : exp2_fast(m - Mn);
     st.M = Mn;
-    // masked rows give -inf - Mn (NaN while nothing is valid yet): exp2_poly2 returns 0
-    const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(-Mn, -Mn)));
-    st.l = fmaf(st.l, alpha, pp.x + pp.y);
+    // masked rows give -inf - m (NaN for an empty group): exp2_poly2 returns 0
+    const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(-m, -m)));
+    st.l = fmaf(st.l, alpha, beta * (pp.x + pp.y));
     ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
+    const int srcA = (lane & ~3) | (tq & 1);
+    const float bA = __shfl_sync(kFull, beta, srcA), bB = __shfl_sync(kFull, beta, srcA | 2);
     if (__any_sync(kFull, alpha != 1.f)) {
-        const int srcA = (lane & ~3) | (tq & 1);
         const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
 #pragma unroll
         for (int mm = 0; mm < 8; ++mm) {
@@ -695,8 +713,12 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
         uint32_t a0, a1, a2, a3;
         dequant_word(w0, dA, mA, dB, mB, a0, a2);
         dequant_word(w1, dA, mA, dB, mB, a1, a3);
-        mma_bf16(st.o[mm], a0, a1, a2, a3, bw.x, bw.y, st.o[mm][0], st.o[mm][1], st.o[mm][2],
-                 st.o[mm][3]);
+        float c[4];
+        mma_bf16(c, a0, a1, a2, a3, bw.x, bw.y, 0.f, 0.f, 0.f, 0.f);
+        st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
+        st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
+        st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
+        st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
     }
     __syncwarp();
 }
@@ -714,14 +736,14 @@ __device__ __forceinline__ Walk walk_load(const volatile Walk& s)
 {
     Walk w;
     w.lo = s.lo; w.hi = s.hi; w.b = s.b; w.h = s.h; w.L = s.L; w.n = s.n; w.cbh = s.cbh;
-    w.csb = s.csb; w.slot = s.slot; w.k = s.k; w.a1 = s.a1; w.own = s.own; w.done = s.done;
+    w.csb = s.csb; w.slot = s.slot; w.k = s.k; w.a1 = s.a1; w.g0 = s.g0; w.g1 = s.g1; w.done = s.done;
     return w;
 }
 
 __device__ __forceinline__ void walk_store(volatile Walk& d, const Walk& w)
 {
     d.lo = w.lo; d.hi = w.hi; d.b = w.b; d.h = w.h; d.L = w.L; d.n = w.n; d.cbh = w.cbh;
-    d.csb = w.csb; d.slot = w.slot; d.k = w.k; d.a1 = w.a1; d.own = w.own; d.done = w.done;
+    d.csb = w.csb; d.slot = w.slot; d.k = w.k; d.a1 = w.a1; d.g0 = w.g0; d.g1 = w.g1; d.done = w.done;
 }
 
 template <int G, bool DEBUG>
@@ -738,7 +760,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     __syncthreads();
 
     const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
-    const int cp = prot_items(S), nb = (S + 15) >> 4;
+    const int cp = prot_items(S);
     const int span = a.plan->span;
     const int wg = blockIdx.x * kWarps + warp;
     volatile Walk& Psm = sm.walk[warp][0];
@@ -772,7 +794,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     auto next_run = [&]() -> bool {
         Walk P = walk_load(Psm);
         if (r_kind >= 0) {                  // leave the run that just ended
-            if (r_kind == 0 && P.own) P.k = P.n;
+            if (r_kind == 0 && P.g0 < P.g1) P.k = P.n + group_items(cp) * P.g0;
             else walk_next_bh(P, a, cp);
         }
         bool more = !P.done;
@@ -786,8 +808,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 win_lo = -64;               // force a window load
             } else {
                 r_kind = S > 0 ? 1 : 2;
-                r_i = 0;
-                r_end = cp;
+                r_i = P.k - P.n;
+                r_end = group_items(cp) * P.g1;
                 const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
                 r_src = a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes;
             }
@@ -819,6 +841,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 return;
             }
         }
+#pragma unroll 1
         while (prod < cons + kStages) {
             if (r_i >= r_end) {
                 if (!next_run()) break;
@@ -873,11 +896,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     int q_b = -1, q_h = -1;
     const int gq = lane >> 2, tq = lane & 3, half = tq >> 1;
     while (!aborted) {
-        int b, h, k, n, a1, L, slot;
+        int b, h, k, n, a1, L, slot, g0, g1;
         {
             const Walk C = walk_load(Csm);
             if (C.done) break;
-            b = C.b; h = C.h; k = C.k; n = C.n; a1 = C.a1; L = C.L; slot = C.slot;
+            b = C.b; h = C.h; k = C.k; n = C.n; a1 = C.a1; L = C.L; slot = C.slot; g0 = C.g0; g1 = C.g1;
         }
         // ---- query state of (b, h) into this warp's shared memory
         if (b != q_b || h != q_h) {
@@ -951,6 +974,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             st.bias = 0.f;
             st.wacc = 0.f;
             const int r4_hi = L - w;
+#pragma unroll 1
             for (int j = k; j < a1; j += 2) {
                 const bool two = j + 1 < a1;
                 const int s0 = wait_next();
@@ -997,8 +1021,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             }
             Walk C = walk_load(Csm);
             const int base = C.csb + h * C.cbh;
-            int idx = __ldg(&a.seg_start[b]) + (wg - base / span);
-            for (int hh = 0; hh < h; ++hh) idx += n_pieces(C.csb + hh * C.cbh, C.n, span);
+            const int idx = unit_first_partial(a, b, h) + (wg - base / span);
             if (tq < 2) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -1012,7 +1035,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 }
             }
             if (gq == 0 && hs < G) a.part_ml[(int64_t)idx * G + hs] = make_float2(st.M, st.l);
-            if (C.own) C.k = C.n;
+            if (C.g0 < C.g1) C.k = C.n + group_items(cp) * C.g0;
             else walk_next_bh(C, a, cp);
             __syncwarp();
             if (lane == 0) walk_store(Csm, C);
@@ -1035,7 +1058,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 else if (L != __ldg(&a.seq_len[slot])) report_error(a.err, KV4_DEVERR_LEN_MISMATCH);
             }
             if (S > 0) {
-                for (int grp = 0; grp < nb; ++grp) {
+#pragma unroll 1
+                for (int grp = g0; grp < g1; ++grp) {
                     const int s0 = wait_next();
                     const int s1 = wait_next();
                     prot_group<G, DEBUG>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
@@ -1048,7 +1072,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             }
 #pragma unroll
             for (int msk = 4; msk < 32; msk <<= 1) st.l += __shfl_xor_sync(kFull, st.l, msk);
-            float* po = a.part_o + ((int64_t)(b * H + h) * G) * kHeadDim;
+            int pidx;
+            {
+                const Walk C = walk_load(Csm);
+                const int base = C.csb + h * C.cbh;
+                pidx = unit_first_partial(a, b, h) +
+                       n_pieces(base, C.n, span) + (wg - (base + C.n) / span);
+            }
+            float* po = a.part_o + ((int64_t)pidx * G) * kHeadDim;
             if (tq < 2) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -1061,7 +1092,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                     }
                 }
             }
-            if (gq == 0 && hs < G) a.part_ml[(int64_t)(b * H + h) * G + hs] = make_float2(st.M, st.l);
+            if (gq == 0 && hs < G) a.part_ml[(int64_t)pidx * G + hs] = make_float2(st.M, st.l);
             Walk C = walk_load(Csm);
             walk_next_bh(C, a, cp);
             __syncwarp();
@@ -1084,13 +1115,13 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
     if (gw >= a.batch * a.num_q_heads) return;
     const int b = gw / a.num_q_heads, hq = gw - b * a.num_q_heads;
     const int h = hq / G, g = hq - h * G;
-    const int H = a.num_heads, cp = prot_items(a.sink + a.window), span = a.plan->span;
+    const int cp = prot_items(a.sink + a.window), span = a.plan->span;
     const int n = int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
     const int cbh = unit_cost(n, cp), csb = a.cost_start[b];
-    int first = a.seg_start[b];
-    for (int hh = 0; hh < h; ++hh) first += n_pieces(csb + hh * cbh, n, span);
-    const int nit = n_pieces(csb + h * cbh, n, span) + 1;       // item 0: protected partial
-    auto item = [&](int k) { return k == 0 ? b * H + h : first + k - 1; };
+    const int first = unit_first_partial(a, b, h);
+    const int base = csb + h * cbh;
+    const int nit = n_pieces(base, n, span) + n_pieces(base + n, prot_span_len(cp), span);
+    auto item = [&](int k) { return first + k; };
     float Mx = -INFINITY;
     for (int c0 = 0; c0 < nit; c0 += 32)
         if (c0 + lane < nit) Mx = fmaxf(Mx, __ldg(&a.part_ml[(int64_t)item(c0 + lane) * G + g].x));
@@ -1192,20 +1223,20 @@ cudaError_t decode_ctas_per_sm(int group, int* ctas)
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int group, int grid,
                               DecodeWorkspace* ws, unsigned char* base)
 {
-    // plan header | cost_start[B+1] | seg_start[B+1] | query records | partial (M, l) | partial o
+    // plan header | cost_start[B+1] | unit_seg[B*H+1] | query records | partial (M, l) | partial o
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t items = (size_t)2 * batch * num_kv_heads + (size_t)grid * kWarps;
     size_t off = 0;
     const size_t o_plan = off;  off = up(off + sizeof(PlanHeader));
     const size_t o_cost = off;  off = up(off + sizeof(int32_t) * (batch + 1));
-    const size_t o_seg = off;   off = up(off + sizeof(int32_t) * (batch + 1));
+    const size_t o_seg = off;   off = up(off + sizeof(int32_t) * ((size_t)batch * num_kv_heads + 1));
     const size_t o_q = off;     off = up(off + (size_t)kQInfoBytes * batch * num_q_heads);
     const size_t o_ml = off;    off = up(off + sizeof(float2) * items * group);
     const size_t o_o = off;     off = up(off + sizeof(float) * items * group * kHeadDim);
     if (ws && base) {
         ws->plan = reinterpret_cast<PlanHeader*>(base + o_plan);
         ws->cost_start = reinterpret_cast<int32_t*>(base + o_cost);
-        ws->seg_start = reinterpret_cast<int32_t*>(base + o_seg);
+        ws->unit_seg = reinterpret_cast<int32_t*>(base + o_seg);
         ws->qinfo = base + o_q;
         ws->part_ml = reinterpret_cast<float2*>(base + o_ml);
         ws->part_o = reinterpret_cast<float*>(base + o_o);
@@ -1331,7 +1362,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.err = nullptr;                      // no error word: device index errors are skipped silently
     a.plan = ws.plan;
     a.cost_start = ws.cost_start;
-    a.seg_start = ws.seg_start;
+    a.unit_seg = ws.unit_seg;
     a.qinfo = ws.qinfo;
     a.part_o = ws.part_o;
     a.part_ml = ws.part_ml;

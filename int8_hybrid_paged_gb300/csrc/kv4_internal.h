@@ -49,7 +49,7 @@ constexpr int kQInfoBytes = 160;   // per q head: 128 INT8 query bytes, {s_q, Σ
 struct DecodeWorkspace {
     PlanHeader* plan;
     int32_t* cost_start;   // [B+1]
-    int32_t* seg_start;    // [B+1]
+    int32_t* unit_seg;     // [B*H+1] first partial of each (b, h) unit, then the total
     uint8_t* qinfo;        // [B*Hq][144]
     float2* part_ml;       // [items][G] {max (log2), normalizer}
     float* part_o;         // [items][G][128]
@@ -98,7 +98,7 @@ struct DecodeArgs {
     // workspace
     PlanHeader* plan;
     int32_t* cost_start;
-    int32_t* seg_start;
+    int32_t* unit_seg;
     uint8_t* qinfo;
     float* part_o;
     float2* part_ml;
