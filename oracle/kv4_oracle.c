@@ -29,7 +29,7 @@
  *   an exact softmax (log-sum-exp) merge
  *       [ko] 전제와 한계; [zh] 核心方法 (third difference).
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open:
  *   R1 V is not rotated; only K (post-RoPE) and q are.
  *   R2 Δ and m use directed rounding: m = fp16_down(min x) (a zero minimum as +0),
  *      Δ = fp16_up(up((max x − m) / n)), so m ≤ min x and m + nΔ ≥ max x.
