@@ -50,8 +50,12 @@ def parse():
     ap.add_argument("--workload", default="qwen3-8b", choices=["qwen3-8b", "qwen3-4b", "long-tail"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work of the oracle baseline sample")
+    ap.add_argument("--sink", type=int, default=None,
+                    help="override the sink size s (with --window 0 and --sink 0: unprotected KV4)")
+    ap.add_argument("--window", type=int, default=None, help="override the recent window w")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
     return ap.parse_args()
 
 
@@ -176,6 +180,18 @@ def split_kernel_traffic():
 
 # --------------------------------------------------------------------------- workload
 
+def workload_from_args(args):
+    """The named workload, with the protected region overridden if asked."""
+    import dataclasses
+    wl = inputs.workload(args.workload)
+    if args.sink is not None or args.window is not None:
+        s = wl.sink if args.sink is None else args.sink
+        w = wl.window if args.window is None else args.window
+        wl = dataclasses.replace(wl, sink=s, window=w,
+                                 name=wl.name + f" (protected region overridden: s={s}, w={w})")
+    return wl
+
+
 def build_workload(wl, seed, device, sample_seqs=0):
     """Fill a cache with the workload's sequences (one prefill append). Host copies
     (bf16 bits) of the first `sample_seqs` sequences' K/V are kept for the CPU
@@ -249,7 +265,7 @@ def run_kv4(args, rank, world, local):
     kbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = inputs.workload(args.workload)
+    wl = workload_from_args(args)
     seed = wl.seed + rank
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     st = build_workload(wl, seed, dev, sample_seqs=8 if want_cpu else 0)
@@ -329,6 +345,10 @@ def run_kv4(args, rank, world, local):
         "clocks": clk,
     }
 
+    # ---- append stress (the quantize + pack + side-write path), only on rank 0 at N = 1
+    if world == 1 and not args.no_append:
+        res["append_stress"] = run_append_stress(dev, peak)
+
     # ---- end to end through the public API from pinned host buffers
     if not args.no_e2e:
         res["e2e"] = run_e2e(st, wl, args, dev, world)
@@ -339,6 +359,50 @@ def run_kv4(args, rank, world, local):
     cache.close()
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def run_append_stress(dev, peak):
+    """kv4_append on the append-stress shapes: (a) one new token for 512 sequences at
+    position 2000, (b) a 16384-token re-prefill chunk for 8 sequences from position 0;
+    8 KV heads, seeded bf16 K/V with outlier channels. CUDA-event time per call, after
+    warm-up; GB/s counts bf16 K/V read, INT4 pages and INT8 side rows written."""
+    from int8_hybrid_paged_gb300.kv4 import KV4Cache
+    H, s, w = 8, 16, 128
+    out = {}
+    for tag, B, T, start_pos, reps in (("b", 8, 16384, 0, 20), ("a", 512, 1, 2000, 200)):
+        stride = (start_pos + T + 15) // 16 + 1
+        num_pages = B * stride + 8
+        bt = torch.from_numpy(inputs.block_tables([stride * 16] * B, 16, num_pages, 1)).to(dev)
+        k, v = inputs.kv_tokens(B * T, H, 23, device=dev)
+        cu = torch.arange(0, B * T + 1, T, dtype=torch.int32, device=dev)
+        slots = torch.arange(B, dtype=torch.int32, device=dev)
+        start = torch.full((B,), start_pos, dtype=torch.int32, device=dev)
+        cache = KV4Cache(H, num_pages, max_slots=B, max_batch=B, max_q_heads=4 * H, sink=s, window=w)
+        try:
+            for _ in range(3):
+                cache.append(k, v, cu, slots, start, bt)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                cache.append(k, v, cu, slots, start, bt)
+            e1.record()
+            torch.cuda.synchronize()
+            if cache.device_error():
+                raise RuntimeError("device error during the append stress")
+            ms = e0.elapsed_time(e1) / reps
+            side = B * (min(T, s + w) if start_pos == 0 else 1 + (1 if start_pos < s else 0))
+            nbytes = bytes_model.append_call_bytes(B * T, H, side * H)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            out[tag] = {"case": f"{B} sequences x {T} token(s) from position {start_pos}, {H} KV heads",
+                        "us_per_call": ms * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+                        "frac_of_hbm_peak": gbs / peak}
+        finally:
+            cache.close()
+            del k, v
+            torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(st, wl, args, dev, world):
@@ -393,7 +457,7 @@ def run_reference(args, rank, world):
     import oracle
 
     oracle.load()
-    wl = inputs.workload(args.workload)
+    wl = workload_from_args(args)
     lens = list(wl.context_lens)
     H, G, Hq = wl.num_kv_heads, wl.group, wl.num_q_heads
     threads = host_cores()
