@@ -7,10 +7,10 @@
 //        前置知识 › 分组仿射 KV 量化
 //   [ko] "INT4 KV 캐시로 비동기 RLVR 롤아웃을 1.8배 가속한다" — 전제와 한계
 //
-// One warp per (token, KV head): lane l holds dims 4l..4l+3 of K and V (one
-// 8-byte load each, 256 contiguous bytes per warp), the rotation and both
-// min/max reductions run in registers and shuffles, and the warp writes the
-// token's 64-byte K code row in one coalesced store.
+// One warp per token, looping over its KV heads: lane l holds dims 4l..4l+3 of K
+// and V of a head (one 8-byte load each, 256 contiguous bytes per warp), the
+// rotation and both min/max reductions run in registers and shuffles, and the warp
+// writes the token's 64-byte K code row in one coalesced store.
 #include "device_common.cuh"
 #include "kv4_internal.h"
 
@@ -48,13 +48,72 @@ __device__ __forceinline__ int side_v_offset(int r, int d)
     return 16 * (32 * (word >> 2) + n) + 4 * (word & 3) + side_v_byte(r);
 }
 
-__global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
+// Quantize and store one token-head: K (rotated) and V to 4-bit codes in the page
+// block, and the 8-bit side copies when the position is protected.
+__device__ __forceinline__ void append_head(const AppendArgs& a, float (&kx)[4], float (&vx)[4],
+                                            uint8_t* blk, int ts, uint8_t* sb, bool to_sink,
+                                            bool to_ring, int pos, int lane)
+{
+    warp_fwht128(kx, lane);                 // keys are stored in the rotated basis; V is not rotated
+    uint32_t kc[4], vc[4];
+    __half kd, km, vd, vm;
+    warp_quant<15>(kx, kc, kd, km);
+    warp_quant<15>(vx, vc, vd, vm);
+    // K row ts: byte j = c[2j] | c[2j+1] << 4; this lane owns bytes 2l and 2l+1
+    const uint16_t kb = (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
+    *reinterpret_cast<uint16_t*>(blk + kKCodeOff + ts * 64 + 2 * lane) = kb;
+    // V dim pairs 2l and 2l+1 of token ts, at their places in the tile-interleaved layout
+    blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
+    if (lane == 0) {
+        // metadata row ts % 8: [K ts, K ts+8, V ts, V ts+8] for ts < 8, the same row for ts >= 8
+        uint8_t* mrow = blk + kMetaOff + 16 * (ts & 7) + 4 * (ts >> 3);
+        *reinterpret_cast<__half2*>(mrow) = __halves2half2(kd, km);
+        *reinterpret_cast<__half2*>(mrow + 8) = __halves2half2(vd, vm);
+    }
+
+    // INT8 side copies: sink row pos (pos < s), ring row s + pos mod w for the last
+    // w positions of this append. Earlier positions of a long chunk would map to the
+    // same ring rows and be overwritten anyway; skipping them avoids the race.
+    if (to_sink || to_ring) {
+        const int s = a.sink, w = a.window;
+        uint32_t k8[4], v8[4];
+        __half k8d, k8m, v8d, v8m;
+        warp_quant<255>(kx, k8, k8d, k8m);
+        warp_quant<255>(vx, v8, v8d, v8m);
+        int idx[2];
+        int n = 0;
+        if (to_sink) idx[n++] = pos;
+        if (to_ring) idx[n++] = s + pos % w;
+        for (int k = 0; k < n; ++k) {
+            uint8_t* g = sb + (idx[k] >> 4) * kSideGroupBytes;
+            const int rr = idx[k] & 15;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                g[kSideKCodeOff + side_k_offset(rr, 4 * lane + i)] = (uint8_t)k8[i];
+                g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
+            }
+            if (lane == 0) {
+                *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
+                    __halves2half2(k8d, k8m);
+                *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
+                    __halves2half2(v8d, v8m);
+            }
+        }
+    }
+}
+
+// One warp per (token, group of hpw KV heads): the sequence lookup, validation and
+// page lookup happen once per warp, then the warp quantizes its heads two at a time
+// (both heads' loads and arithmetic in flight together).
+__global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (gw >= (int64_t)a.total_tokens * a.num_heads) return;   // whole warp leaves together
-    const int tok = (int)(gw / a.num_heads);
-    const int h = (int)(gw - (int64_t)tok * a.num_heads);
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int groups = (a.num_heads + hpw - 1) / hpw;   // head groups per token
+    const int tok = gw / groups;
+    if (tok >= a.total_tokens) return;      // whole warp leaves together
+    const int h_lo = (gw - tok * groups) * hpw, h_hi = min(a.num_heads, h_lo + hpw);
 
     // sequence i of this token: the largest i with cu[i] <= tok (cu[n] = total > tok)
     int lo = 0, hi = a.n_seqs;
@@ -87,73 +146,44 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a)
         return;
     }
 
-    float kx[4], vx[4];
-    const int64_t row = ((int64_t)tok * a.num_heads + h) * kHeadDim + 4 * lane;
-    load_bf16x4(a.k + row, kx);
-    load_bf16x4(a.v + row, vx);
-    warp_fwht128(kx, lane);                 // keys are stored in the rotated basis; V is not rotated
-
-    uint32_t kc[4], vc[4];
-    __half kd, km, vd, vm;
-    warp_quant<15>(kx, kc, kd, km);
-    warp_quant<15>(vx, vc, vd, vm);
-
-    uint8_t* blk = a.pages + ((int64_t)page * a.num_heads + h) * kPageBlock;
-    const int ts = pos % kPage;
-    // K row ts: byte j = c[2j] | c[2j+1] << 4; this lane owns bytes 2l and 2l+1
-    const uint16_t kb = (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
-    *reinterpret_cast<uint16_t*>(blk + kKCodeOff + ts * 64 + 2 * lane) = kb;
-    // V dim pairs 2l and 2l+1 of token ts, at their places in the tile-interleaved layout
-    blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
-    blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
-    if (lane == 0) {
-        // metadata row ts % 8: [K ts, K ts+8, V ts, V ts+8] for ts < 8, the same row for ts >= 8
-        uint8_t* mrow = blk + kMetaOff + 16 * (ts & 7) + 4 * (ts >> 3);
-        *reinterpret_cast<__half2*>(mrow) = __halves2half2(kd, km);
-        *reinterpret_cast<__half2*>(mrow + 8) = __halves2half2(vd, vm);
+    const int H = a.num_heads, ts = pos % kPage;
+    const bool to_sink = pos < a.sink;
+    const bool to_ring = (a.window > 0) && (pos >= new_len - a.window);
+    const uint16_t* krow = a.k + (int64_t)tok * H * kHeadDim + 4 * lane;
+    const uint16_t* vrow = a.v + (int64_t)tok * H * kHeadDim + 4 * lane;
+    uint8_t* blk0 = a.pages + (int64_t)page * H * kPageBlock;
+    uint8_t* sb0 = a.side + (int64_t)slot * H * a.side_block_bytes;
+    int h = h_lo;
+    for (; h + 1 < h_hi; h += 2) {
+        float kx0[4], vx0[4], kx1[4], vx1[4];
+        load_bf16x4(krow + h * kHeadDim, kx0);
+        load_bf16x4(vrow + h * kHeadDim, vx0);
+        load_bf16x4(krow + (h + 1) * kHeadDim, kx1);
+        load_bf16x4(vrow + (h + 1) * kHeadDim, vx1);
+        append_head(a, kx0, vx0, blk0 + h * kPageBlock, ts, sb0 + h * a.side_block_bytes, to_sink,
+                    to_ring, pos, lane);
+        append_head(a, kx1, vx1, blk0 + (h + 1) * kPageBlock, ts, sb0 + (h + 1) * a.side_block_bytes,
+                    to_sink, to_ring, pos, lane);
     }
-
-    // INT8 side copies: sink row pos (pos < s), ring row s + pos mod w for the last
-    // w positions of this append. Earlier positions of a long chunk would map to the
-    // same ring rows and be overwritten anyway; skipping them avoids the race.
-    const int s = a.sink, w = a.window;
-    const bool to_sink = pos < s;
-    const bool to_ring = (w > 0) && (pos >= new_len - w);
-    if (to_sink || to_ring) {
-        uint32_t k8[4], v8[4];
-        __half k8d, k8m, v8d, v8m;
-        warp_quant<255>(kx, k8, k8d, k8m);
-        warp_quant<255>(vx, v8, v8d, v8m);
-        uint8_t* sb = a.side + ((int64_t)slot * a.num_heads + h) * a.side_block_bytes;
-        int idx[2];
-        int n = 0;
-        if (to_sink) idx[n++] = pos;
-        if (to_ring) idx[n++] = s + pos % w;
-        for (int k = 0; k < n; ++k) {
-            uint8_t* g = sb + (idx[k] >> 4) * kSideGroupBytes;
-            const int rr = idx[k] & 15;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                g[kSideKCodeOff + side_k_offset(rr, 4 * lane + i)] = (uint8_t)k8[i];
-                g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
-            }
-            if (lane == 0) {
-                *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
-                    __halves2half2(k8d, k8m);
-                *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
-                    __halves2half2(v8d, v8m);
-            }
-        }
+    if (h < h_hi) {
+        float kx[4], vx[4];
+        load_bf16x4(krow + h * kHeadDim, kx);
+        load_bf16x4(vrow + h * kHeadDim, vx);
+        append_head(a, kx, vx, blk0 + h * kPageBlock, ts, sb0 + h * a.side_block_bytes, to_sink,
+                    to_ring, pos, lane);
     }
-    if (lane == 0 && h == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
+    if (lane == 0 && h_lo == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream)
 {
-    const int64_t warps = (int64_t)a.total_tokens * a.num_heads;
-    if (warps == 0) return cudaSuccess;
+    if (a.total_tokens == 0) return cudaSuccess;
+    // all heads of a token in one warp when there are enough tokens to fill the GPU
+    // (the per-token lookup is paid once); one head per warp for small appends
+    const int hpw = (int64_t)a.total_tokens >= 16384 ? a.num_heads : 1;
+    const int64_t warps = (int64_t)a.total_tokens * ((a.num_heads + hpw - 1) / hpw);
     const int64_t blocks = (warps + 7) / 8;
-    kv4_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a);
+    kv4_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a, hpw);
     return cudaGetLastError();
 }
 
