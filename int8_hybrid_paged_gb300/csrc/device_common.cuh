@@ -105,6 +105,24 @@ __device__ __forceinline__ void warp_fwht128(float (&x)[4], int lane)
 // Δ = fp16 rounded up from (max x − m)/LEVELS, itself rounded up in float,
 // c = clamp(rint((x − m) · fl(1/Δ)), 0, LEVELS); Δ = 0 gives c = 0.
 // [zh] 前置知识 › 分组仿射 KV 量化; 方法步骤详情 step 2 (fp16 Δ, m computed online).
+// The smallest fp16 value >= r / n for r >= 0, i.e. the quotient rounded up to fp16
+// (rounding up to fp32 first and then to fp16 gives the same value). An fp32 estimate
+// r * fl(1/n), within a few fp32 ulps, is rounded up to fp16 and then moved by at most
+// one fp16 step, decided by exact comparisons: c * n is exact for an 11-bit c and an
+// integer n below 2^13.
+__device__ __forceinline__ __half half_div_up(float r, float n, float inv_n)
+{
+    const __half c = __float2half_ru(__fmul_rn(r, inv_n));
+    unsigned short cb = __half_as_ushort(c);
+    if (__fmul_rn(__half2float(c), n) < r) {
+        ++cb;                                           // estimate below the quotient
+    } else if (cb != 0) {
+        const unsigned short pb = (unsigned short)(cb - 1);
+        if (__fmul_rn(__half2float(__ushort_as_half(pb)), n) >= r) cb = pb;   // one step too high
+    }
+    return __ushort_as_half(cb);
+}
+
 template <int LEVELS>
 __device__ __forceinline__ void warp_quant(const float (&x)[4], uint32_t (&c)[4],
                                            __half& delta_h, __half& min_h)
@@ -115,15 +133,14 @@ __device__ __forceinline__ void warp_quant(const float (&x)[4], uint32_t (&c)[4]
     min_h = __float2half_rd(lo);
     const float m = __half2float(min_h);
     const float r = __fadd_ru(hi, -m);
-    const float d = __fdiv_ru(r, (float)LEVELS);
-    delta_h = __float2half_ru(d);
+    delta_h = half_div_up(r, (float)LEVELS, 1.0f / (float)LEVELS);
     const float delta = __half2float(delta_h);
     if (delta == 0.0f) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[i] = 0;
         return;
     }
-    const float inv = __fdiv_rn(1.0f, delta);
+    const float inv = __frcp_rn(delta);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         int v = __float2int_rn(__fmul_rn(__fsub_rn(x[i], m), inv));
