@@ -110,15 +110,38 @@ __device__ __forceinline__ int n_pieces(int base, int n, int span)
     return n > 0 ? (base + n - 1) / span - base / span + 1 : 0;
 }
 
+// Division of non-negative 32-bit values by one divisor d >= 2 with a multiply-high:
+// m = floor(2^32 (2^s - d) / d) + 1 with s = ceil(log2 d), q = (t + ((x - t) >> 1)) >> (s - 1)
+// where t = mulhi(x, m) (exact for every x < 2^32).
+struct SpanDiv {
+    uint32_t m, s;
+    __device__ explicit SpanDiv(uint32_t d)
+    {
+        s = 32u - (uint32_t)__clz(d - 1u);
+        m = (uint32_t)((((1ull << 32) * ((1ull << s) - d)) / d) + 1ull);
+    }
+    __device__ __forceinline__ int operator()(int x) const
+    {
+        const uint32_t t = __umulhi((uint32_t)x, m);
+        return (int)((t + (((uint32_t)x - t) >> 1)) >> (s - 1u));
+    }
+    // pieces of [base, base + n) as n_pieces
+    __device__ __forceinline__ int pieces(int base, int n) const
+    {
+        return n > 0 ? (*this)(base + n - 1) - (*this)(base) + 1 : 0;
+    }
+};
+
 // First partial of unit (b, h), laid out by the plan: per unit its INT4 pieces, then
 // its protected pieces (spans holding the first item of one of its groups).
 __device__ __forceinline__ int unit_first_partial(const DecodeArgs& a, int b, int h)
 {
     return __ldg(&a.unit_seg[b * a.num_heads + h]);
 }
-// Block-wide exclusive scan over 1024 threads; returns the thread's offset and the total.
+// Block-wide exclusive scan (up to 1024 threads); returns the thread's offset and the total.
 __device__ __forceinline__ int block_scan(int v, int* s_scan, int& total)
 {
+    const int nwarps = blockDim.x >> 5;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
 #pragma unroll
@@ -129,7 +152,7 @@ __device__ __forceinline__ int block_scan(int v, int* s_scan, int& total)
     if (lane == 31) s_scan[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        const int x0 = s_scan[lane];
+        const int x0 = lane < nwarps ? s_scan[lane] : 0;
         int x = x0;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
@@ -147,7 +170,9 @@ __device__ __forceinline__ int block_scan(int v, int* s_scan, int& total)
 }
 
 // ---------------------------------------------------------------- prep
-__global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
+constexpr int kPrepThreads = 256;
+
+__global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArgs a)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == 0) {
@@ -155,20 +180,22 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
         __shared__ int s_scan[33];
         const int B = a.batch, H = a.num_heads, s = a.sink, w = a.window;
         const int cp = prot_items(s + w);
-        const int per = (B + 1023) / 1024;
+        const int per = (B + kPrepThreads - 1) / kPrepThreads;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int cost = 0;
         for (int b = b0; b < b1; ++b) cost += H * unit_cost(int4_pages(max(0, a.context_lens[b]), s, w), cp);
         int total = 0;
         int off = block_scan(cost, s_scan, total);
         const int span = max(2, (total + a.num_warps - 1) / a.num_warps);
+        const SpanDiv sd((uint32_t)span);
+        const int plen = prot_span_len(cp);
         int segs = 0;
         for (int b = b0; b < b1; ++b) {
             a.cost_start[b] = off;
             const int n = int4_pages(max(0, a.context_lens[b]), s, w);
             for (int h = 0; h < H; ++h) {
                 const int base = off + h * unit_cost(n, cp);
-                segs += n_pieces(base, n, span) + n_pieces(base + n, prot_span_len(cp), span);
+                segs += sd.pieces(base, n) + sd.pieces(base + n, plen);
             }
             off += H * unit_cost(n, cp);
         }
@@ -180,10 +207,10 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
             for (int h = 0; h < H; ++h) {
                 a.unit_seg[b * H + h] = soff;
                 const int base = cs + h * unit_cost(n, cp);
-                soff += n_pieces(base, n, span) + n_pieces(base + n, prot_span_len(cp), span);
+                soff += sd.pieces(base, n) + sd.pieces(base + n, plen);
             }
         }
-        if (tid == 1023) {
+        if (tid == kPrepThreads - 1) {
             a.cost_start[B] = total;
             a.unit_seg[B * H] = nseg;
             a.plan->total_cost = total;
@@ -193,7 +220,7 @@ __global__ void __launch_bounds__(1024) kv4_decode_prep_kernel(DecodeArgs a)
         return;
     }
     // ---- query: rotate and quantize one q head per warp
-    const int gw = (blockIdx.x - 1) * 32 + warp;
+    const int gw = (blockIdx.x - 1) * (kPrepThreads / 32) + warp;
     if (gw >= a.batch * a.num_q_heads) return;
     float x[4];
     load_bf16x4(a.q + (int64_t)gw * kHeadDim + 4 * lane, x);
@@ -1103,10 +1130,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 }
 
 // ---------------------------------------------------------------- merge
-// Exact log-sum-exp merge, one warp per q head: the protected unit's partial and
-// those of the INT4 run pieces of its (b, h). Lane k loads the (max, normalizer)
-// of item k; every lane then loads its four dims of eight items at once, so the
-// merge costs a few load round trips whatever the number of pieces.
+// Exact log-sum-exp merge, one warp per q head, over the partials (INT4 pieces and
+// protected pieces) of its (b, h). Lane k loads the (max, normalizer) of item k;
+// every lane then loads its four dims of four items at once, so the merge costs a
+// few load round trips whatever the number of pieces.
 template <int G>
 __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 {
@@ -1115,13 +1142,53 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
     if (gw >= a.batch * a.num_q_heads) return;
     const int b = gw / a.num_q_heads, hq = gw - b * a.num_q_heads;
     const int h = hq / G, g = hq - h * G;
-    const int cp = prot_items(a.sink + a.window), span = a.plan->span;
-    const int n = int4_pages(max(0, a.context_lens[b]), a.sink, a.window);
-    const int cbh = unit_cost(n, cp), csb = a.cost_start[b];
-    const int first = unit_first_partial(a, b, h);
-    const int base = csb + h * cbh;
-    const int nit = n_pieces(base, n, span) + n_pieces(base + n, prot_span_len(cp), span);
+    // a unit's partials are consecutive: its count is the next unit's first minus its own
+    const int u = b * a.num_heads + h;
+    const int first = __ldg(&a.unit_seg[u]);
+    const int nit = __ldg(&a.unit_seg[u + 1]) - first;
     auto item = [&](int k) { return first + k; };
+    auto pout = [&](int it) {
+        return __ldg(reinterpret_cast<const float4*>(&a.part_o[((int64_t)it * G + g) * kHeadDim + 4 * lane]));
+    };
+    if (nit <= 32) {
+        // one round for the (max, normalizer) of every item and the first four outputs
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (lane < nit) ml = __ldg(&a.part_ml[(int64_t)item(lane) * G + g]);
+        float4 v[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) v[kk] = pout(item(min(kk, nit - 1)));   // weight 0 past the last
+        const float Mx = warp_max(ml.x);
+        float den = 0.f;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Mx != -INFINITY) {
+            const float f = (ml.x != -INFINITY) ? exp2f(ml.x - Mx) : 0.f;
+            den = warp_sum(f * ml.y);
+            for (int c0 = 0; c0 < nit; c0 += 4) {
+                if (c0 > 0) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) v[kk] = pout(item(min(c0 + kk, nit - 1)));
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float fk = __shfl_sync(kFull, f, (c0 + kk) & 31);
+                    o.x = fmaf(fk, v[kk].x, o.x);
+                    o.y = fmaf(fk, v[kk].y, o.y);
+                    o.z = fmaf(fk, v[kk].z, o.z);
+                    o.w = fmaf(fk, v[kk].w, o.w);
+                }
+            }
+        }
+        float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (den > 0.f) {
+            const float r = 1.f / den;
+            res = make_float4(o.x * r, o.y * r, o.z * r, o.w * r);
+        }
+        *reinterpret_cast<float4*>(&a.out[((int64_t)b * a.num_q_heads + hq) * kHeadDim + 4 * lane]) = res;
+        if (a.lse && lane == 0)
+            a.lse[(int64_t)b * a.num_q_heads + hq] =
+                (den > 0.f) ? (Mx + log2f(den)) * 0.69314718055994531f : -INFINITY;
+        return;
+    }
     float Mx = -INFINITY;
     for (int c0 = 0; c0 < nit; c0 += 32)
         if (c0 + lane < nit) Mx = fmaxf(Mx, __ldg(&a.part_ml[(int64_t)item(c0 + lane) * G + g].x));
@@ -1129,24 +1196,24 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
     float den = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     if (Mx != -INFINITY) {
-        for (int c0 = 0; c0 < nit; c0 += 8) {
+        for (int c0 = 0; c0 < nit; c0 += 4) {
             float f = 0.f;
-            if (lane < 8 && c0 + lane < nit) {
+            if (lane < 4 && c0 + lane < nit) {
                 const float2 ml = __ldg(&a.part_ml[(int64_t)item(c0 + lane) * G + g]);
                 if (ml.x != -INFINITY) {
                     f = exp2f(ml.x - Mx);
                     den = fmaf(f, ml.y, den);
                 }
             }
-            float4 v[8];
+            float4 v[4];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < 4; ++kk) {
                 const int it = item(min(c0 + kk, nit - 1));      // weight 0 past the last item
                 v[kk] = __ldg(reinterpret_cast<const float4*>(
                     &a.part_o[((int64_t)it * G + g) * kHeadDim + 4 * lane]));
             }
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < 4; ++kk) {
                 const float fk = __shfl_sync(kFull, f, kk);
                 o.x = fmaf(fk, v[kk].x, o.x);
                 o.y = fmaf(fk, v[kk].y, o.y);
@@ -1172,8 +1239,8 @@ template <int G, bool DEBUG>
 static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     if (ev) cudaEventRecord(ev[0], stream);
-    const int prep_blocks = 1 + (a.batch * a.num_q_heads + 31) / 32;
-    kv4_decode_prep_kernel<<<prep_blocks, 1024, 0, stream>>>(a);
+    const int prep_blocks = 1 + (a.batch * a.num_q_heads + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+    kv4_decode_prep_kernel<<<prep_blocks, kPrepThreads, 0, stream>>>(a);
     if (ev) cudaEventRecord(ev[1], stream);
     kv4_decode_split_kernel<G, DEBUG><<<grid, kDecodeThreads, sizeof(SplitSmem), stream>>>(a);
     if (ev) cudaEventRecord(ev[2], stream);
