@@ -76,7 +76,10 @@ typedef struct {
  * INT4 page pool: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES = 2176 bytes;
  * the block of (page p, KV head h) starts at (p * H_kv + h) * 2176. Inside it,
  * for the 16 token slots t of the page:
- *   [0,    1024)  K codes, row t = 64 bytes; byte j = c[2j] | c[2j+1] << 4 (rotated K)
+ *   [0,    1024)  K codes (rotated K): tokens t and t+8 (t < 8) share bytes, token t in
+ *                 the low nibble. Code d of token t sits in the byte at
+ *                 512*(i/4) + 16*(4*(t%8) + d/32) + 4*(i%4) + {0, 2, 1, 3}[d%4] with
+ *                 i = (d%32)/4 (two planes of eight 16-byte slots per token pair)
  *   [1024, 2048)  V codes: one byte per (dim pair j, token t) = c_t[2j] | c_t[2j+1] << 4, at
  *                 offset 4*(8*(4*(j%8) + t%4) + j/8) + t/4 (32 groups of eight 32-bit
  *                 words; each word holds one dim pair of tokens u, u+4, u+8, u+12 with
@@ -88,9 +91,8 @@ typedef struct {
  * block (slot, h) at (slot * H_kv + h) * side_block_bytes. Side row i (i = p for a
  * sink position p < s, i = s + p mod w for a ring position) is row r = i%16 of group
  * i/16; group g starts at g * 4352 and holds two 2176-byte blocks. For dim d write
- * u = d%32, e = (u%8/2)%2, b = 2*(u%2) + (u%8)/4 and word W = 2*(u/8) + e; a code
- * byte (u8, INT8 grid) sits at:
- *   K block [0, 2176):    1024*(W/4) + 64*r + 16*(d/32) + 4*(W%4) + b   (rotated K)
+ * W = (d%32)/4; a code byte (u8, INT8 grid) sits at:
+ *   K block [0, 2176):    1024*(W/4) + 64*r + 16*(d/32) + 4*(W%4) + d%4   (rotated K)
  *                         K metadata {fp16 delta, fp16 min} of row r at 2048 + 8*(r%8) + 4*(r/8)
  *   V block [2176, 4352): with n = 4*(d%8) + r%4, W' = 2*(d/16) + (d/8)%2 and
  *                         b' = (r/8)%2 + 2*((r/4)%2): 2176 + 16*(32*(W'/4) + n) + 4*(W'%4) + b'

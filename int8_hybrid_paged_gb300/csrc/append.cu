@@ -26,14 +26,12 @@ __device__ __forceinline__ int v_byte_offset(int j, int t)
 }
 
 // Side K code byte of (row r, dim d): the QK A fragments of the protected path take,
-// per 32-dim chunk t = d / 32, eight words [u, u+4, u+1, u+5] (u = 8 i + 2 e) in two
-// planes, so one byte permute widens two codes of one fragment register.
+// per 32-dim chunk c = d / 32, eight words of four consecutive dims in two planes, so
+// one byte permute widens two codes of one fragment register.
 __device__ __forceinline__ int side_k_offset(int r, int d)
 {
-    const int u = d & 31, r8 = u & 7;
-    const int word = 2 * (u >> 3) + ((r8 >> 1) & 1);
-    const int byte = ((r8 & 1) << 1) | (r8 >> 2);
-    return 1024 * (word >> 2) + 64 * r + 16 * (d >> 5) + 4 * (word & 3) + byte;
+    const int word = (d & 31) >> 2;
+    return 1024 * (word >> 2) + 64 * r + 16 * (d >> 5) + 4 * (word & 3) + (d & 3);
 }
 
 // Byte of side row r inside a V fragment word (rows t, t+8, t+4, t+12 with t = r % 4).
@@ -48,20 +46,29 @@ __device__ __forceinline__ int side_v_offset(int r, int d)
     return 16 * (32 * (word >> 2) + n) + 4 * (word & 3) + side_v_byte(r);
 }
 
-// Quantize and store one token-head: K (rotated) and V to 4-bit codes in the page
-// block, and the 8-bit side copies when the position is protected.
-__device__ __forceinline__ void append_head(const AppendArgs& a, float (&kx)[4], float (&vx)[4],
-                                            uint8_t* blk, int ts, uint8_t* sb, bool to_sink,
-                                            bool to_ring, int pos, int lane)
+// Page K codes: tokens t and t+8 share bytes (t in the low nibble). Lane l of a warp
+// holding dims 4l..4l+3 owns one 32-bit word per token pair: dims 4i, 4i+2, 4i+1,
+// 4i+3 of chunk c (i = l % 8, c = l / 8) in bytes 0..3, at plane i / 4 (512 bytes),
+// slot 4t + c (16 bytes), word i % 4 -- the QK fragment of lane (t, c) of the MMAs.
+__device__ __forceinline__ int k_word_offset(int t, int lane)
+{
+    const int i = lane & 7, c = lane >> 3;
+    return (i >> 2) * 512 + (4 * t + c) * 16 + (i & 3) * 4;
+}
+
+// Quantize and store one token-head: V to 4-bit codes in the page block, the metadata,
+// and the 8-bit side copies when the position is protected. Returns the lane's K codes
+// as a nibble word (bytes: dims 4i, 4i+2, 4i+1, 4i+3, low nibbles); the caller stores K.
+__device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)[4], float (&vx)[4],
+                                                uint8_t* blk, int ts, uint8_t* sb, bool to_sink,
+                                                bool to_ring, int pos, int lane)
 {
     warp_fwht128(kx, lane);                 // keys are stored in the rotated basis; V is not rotated
     uint32_t kc[4], vc[4];
     __half kd, km, vd, vm;
     warp_quant<15>(kx, kc, kd, km);
     warp_quant<15>(vx, vc, vd, vm);
-    // K row ts: byte j = c[2j] | c[2j+1] << 4; this lane owns bytes 2l and 2l+1
-    const uint16_t kb = (uint16_t)(kc[0] | (kc[1] << 4) | (kc[2] << 8) | (kc[3] << 12));
-    *reinterpret_cast<uint16_t*>(blk + kKCodeOff + ts * 64 + 2 * lane) = kb;
+    const uint32_t kn = kc[0] | (kc[2] << 8) | (kc[1] << 16) | (kc[3] << 24);
     // V dim pairs 2l and 2l+1 of token ts, at their places in the tile-interleaved layout
     blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
     blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
@@ -101,11 +108,12 @@ __device__ __forceinline__ void append_head(const AppendArgs& a, float (&kx)[4],
             }
         }
     }
+    return kn;
 }
 
 // One warp per (token, group of hpw KV heads): the sequence lookup, validation and
-// page lookup happen once per warp, then the warp quantizes its heads two at a time
-// (both heads' loads and arithmetic in flight together).
+// page lookup happen once per warp, then the warp quantizes its heads one by one (for
+// a token pair t, t + 8 both tokens' loads and arithmetic are in flight together).
 __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
 {
     const int lane = threadIdx.x & 31;
@@ -147,32 +155,57 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
     }
 
     const int H = a.num_heads, ts = pos % kPage;
-    const bool to_sink = pos < a.sink;
-    const bool to_ring = (a.window > 0) && (pos >= new_len - a.window);
-    const uint16_t* krow = a.k + (int64_t)tok * H * kHeadDim + 4 * lane;
-    const uint16_t* vrow = a.v + (int64_t)tok * H * kHeadDim + 4 * lane;
+    // tokens t and t+8 of a page share their K bytes. When both are in this append,
+    // their 2 x groups warps split the heads of both tokens and each writes whole
+    // words; a token without its partner merges its nibbles into the word (the partner
+    // was written by an earlier append or is not written yet)
+    const bool lower = ts < 8;
+    const bool pair = lower ? (pos + 8 < new_len) : (pos - 8 >= start);
+    const int posA = pair && !lower ? pos - 8 : pos;       // first token of the work
+    const int tokA = tok - (pos - posA);
+    const int posB = posA + 8;
+    int hb = h_lo, he = h_hi;
+    if (pair) {
+        const int k = (lower ? 0 : groups) + h_lo / hpw;     // warp of the pair, 0 .. 2 groups
+        hb = k * H / (2 * groups);
+        he = (k + 1) * H / (2 * groups);
+    }
+    const bool sinkA = posA < a.sink, ringA = (a.window > 0) && (posA >= new_len - a.window);
+    const bool sinkB = posB < a.sink, ringB = (a.window > 0) && (posB >= new_len - a.window);
+    const uint16_t* krow = a.k + (int64_t)tokA * H * kHeadDim + 4 * lane;
+    const uint16_t* vrow = a.v + (int64_t)tokA * H * kHeadDim + 4 * lane;
+    const int64_t rowB = (int64_t)8 * H * kHeadDim;        // token tokA + 8
     uint8_t* blk0 = a.pages + (int64_t)page * H * kPageBlock;
     uint8_t* sb0 = a.side + (int64_t)slot * H * a.side_block_bytes;
-    int h = h_lo;
-    for (; h + 1 < h_hi; h += 2) {
-        float kx0[4], vx0[4], kx1[4], vx1[4];
-        load_bf16x4(krow + h * kHeadDim, kx0);
-        load_bf16x4(vrow + h * kHeadDim, vx0);
-        load_bf16x4(krow + (h + 1) * kHeadDim, kx1);
-        load_bf16x4(vrow + (h + 1) * kHeadDim, vx1);
-        append_head(a, kx0, vx0, blk0 + h * kPageBlock, ts, sb0 + h * a.side_block_bytes, to_sink,
-                    to_ring, pos, lane);
-        append_head(a, kx1, vx1, blk0 + (h + 1) * kPageBlock, ts, sb0 + (h + 1) * a.side_block_bytes,
-                    to_sink, to_ring, pos, lane);
+    const int tsA = posA % kPage;
+    const int kw = kKCodeOff + k_word_offset(tsA & 7, lane);
+    if (pair) {
+        for (int h = hb; h < he; ++h) {
+            uint8_t* blk = blk0 + h * kPageBlock;
+            uint8_t* sb = sb0 + h * a.side_block_bytes;
+            float kxA[4], vxA[4], kxB[4], vxB[4];
+            load_bf16x4(krow + h * kHeadDim, kxA);
+            load_bf16x4(vrow + h * kHeadDim, vxA);
+            load_bf16x4(krow + rowB + h * kHeadDim, kxB);
+            load_bf16x4(vrow + rowB + h * kHeadDim, vxB);
+            const uint32_t knA = append_head(a, kxA, vxA, blk, tsA, sb, sinkA, ringA, posA, lane);
+            const uint32_t knB = append_head(a, kxB, vxB, blk, tsA + 8, sb, sinkB, ringB, posB, lane);
+            *reinterpret_cast<uint32_t*>(blk + kw) = knA | (knB << 4);
+        }
+    } else {
+        for (int h = hb; h < he; ++h) {
+            uint8_t* blk = blk0 + h * kPageBlock;
+            uint32_t* kp = reinterpret_cast<uint32_t*>(blk + kw);
+            const uint32_t old = *kp;                       // issued before the arithmetic
+            float kx[4], vx[4];
+            load_bf16x4(krow + h * kHeadDim, kx);
+            load_bf16x4(vrow + h * kHeadDim, vx);
+            const uint32_t kn = append_head(a, kx, vx, blk, tsA, sb0 + h * a.side_block_bytes,
+                                            sinkA, ringA, posA, lane);
+            *kp = lower ? ((old & 0xf0f0f0f0u) | kn) : ((old & 0x0f0f0f0fu) | (kn << 4));
+        }
     }
-    if (h < h_hi) {
-        float kx[4], vx[4];
-        load_bf16x4(krow + h * kHeadDim, kx);
-        load_bf16x4(vrow + h * kHeadDim, vx);
-        append_head(a, kx, vx, blk0 + h * kPageBlock, ts, sb0 + h * a.side_block_bytes, to_sink,
-                    to_ring, pos, lane);
-    }
-    if (lane == 0 && h_lo == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
+    if (lane == 0 && hb == 0 && he > 0 && (pair ? tokA + 8 : tok) == c1 - 1) a.seq_len[slot] = new_len;
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream)

@@ -43,8 +43,7 @@ struct __align__(16) WarpQ {
     int8_t q8[kMaxG][kHeadDim];
     float scale[kMaxG];
     float qsum[kMaxG];
-    float corr[kMaxG][2];     // INT4 widening offsets per dim half
-    float corr8[kMaxG][2];    // INT8 (side) widening offsets per dim half
+    float corr[kMaxG][2];     // QK widening offsets per dim half
 };
 
 // Span walker state (one per producer and consumer of a warp): the current (b, h) of
@@ -235,38 +234,32 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
         for (int i = 0; i < 4; ++i) q[i] = __float2int_rn(__fmul_rn(x[i], inv));
         sq = __fdiv_rn(amax, 127.0f);
     }
-    const int qsum = warp_sum_int(q[0] + q[1] + q[2] + q[3]);
-    // widening offsets of each dim half for the tensor-core QK: 1024·Σ q_even + 64·Σ q_odd
-    int se = q[0] + q[2], so = q[1] + q[3];
+    // QK widening offsets: every code slot carries 1024 q, so each dim half is offset by
+    // 1024 times its query sum
+    int hsum = q[0] + q[1] + q[2] + q[3];
 #pragma unroll
-    for (int m = 1; m < 16; m <<= 1) {
-        se += __shfl_xor_sync(kFull, se, m);
-        so += __shfl_xor_sync(kFull, so, m);
-    }
-    const float corr = 1024.f * (float)se + 64.f * (float)so;
+    for (int m = 1; m < 16; m <<= 1) hsum += __shfl_xor_sync(kFull, hsum, m);
+    const int qsum = hsum + __shfl_xor_sync(kFull, hsum, 16);
+    const float corr = 1024.f * (float)hsum;
     const float corr_hi = __shfl_sync(kFull, corr, 16);
-    // INT8 side codes widen to 1024 + c in either slot: 1024·Σ q per dim half
-    const float corr8 = 1024.f * (float)(se + so);
-    const float corr8_hi = __shfl_sync(kFull, corr8, 16);
     const uint32_t packed = (uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
                             ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24);
     uint8_t* rec = a.qinfo + (int64_t)gw * kQInfoBytes;
     *reinterpret_cast<uint32_t*>(rec + 4 * lane) = packed;
-    if (lane == 0) {
+    if (lane == 0)
         *reinterpret_cast<float4*>(rec + kHeadDim) = make_float4(sq, (float)qsum, corr, corr_hi);
-        *reinterpret_cast<float4*>(rec + kHeadDim + 16) = make_float4(corr8, corr8_hi, 0.f, 0.f);
-    }
     if (a.dbg_q8) *reinterpret_cast<uint32_t*>(a.dbg_q8 + (int64_t)gw * kHeadDim + 4 * lane) = packed;
     if (a.dbg_qscale && lane == 0) a.dbg_qscale[gw] = sq;
 }
 
 // ---------------------------------------------------------------- tensor-core integer dots
-// A 4-bit code c is widened to the fp16 value 1024 + c (low nibble) or 1024 + 16c
-// (high nibble) by one AND/OR of its 32-bit word; the INT8 query enters as fp16 q
-// (even dims, low nibbles) or q/16 (odd dims), all exactly representable. Every
-// product is exact, every partial sum an integer below 2^23, and the accumulator
-// is seeded with minus the widening offset (1024·Σq_even + 64·Σq_odd for QK,
-// 1024·Σŵ for PV), so the fp32 result is the exact integer dot.
+// Integer codes enter the fp16 MMA as exact fp16 values 1024 + x, where x is a whole
+// byte (a code pair or an INT8 code) or 16 times a high nibble, cut from the 32-bit
+// word by one LOP3 or byte permute; the INT8 query enters as fp16 q. Every product is
+// exact, every partial sum an integer below 2^24, and the accumulator is seeded with
+// minus the widening offset (1024·Σq per dim half for QK, 1024·Σŵ for PV), so the
+// fp32 result is the exact integer dot; row or slot differences then separate the
+// two nibbles of a byte.
 // QK: m16n8k16, rows = the 16 tokens of a page, 8 columns = 4 heads x 2 halves of
 // the 128 dims. PV: rows = 16 dims, k = the 16 tokens of one page, 8 columns =
 // 2 pages x 4 heads (pages are taken in pairs). No column is padding.
@@ -289,14 +282,9 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
-// nibbles 0 and 4 of w as fp16 (1024 + n0, 1024 + n4)
-__device__ __forceinline__ uint32_t wide_lo(uint32_t w)
-{
-    return and_or(w, 0x000F000Fu, 0x64006400u);
-}
-// nibbles 1 and 5 of w as fp16 (1024 + 16 n1, 1024 + 16 n5)
 // bytes 0 and 2 whole (two nibbles) as fp16 1024 + byte
 __device__ __forceinline__ uint32_t wide_byte(uint32_t w) { return and_or(w, 0x00ff00ffu, 0x64006400u); }
+// nibbles 1 and 5 of w as fp16 (1024 + 16 n1, 1024 + 16 n5)
 __device__ __forceinline__ uint32_t wide_hi(uint32_t w)
 {
     return and_or(w, 0x00F000F0u, 0x64006400u);
@@ -411,12 +399,14 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     const uint8_t* pgs[2] = {pg0, pg1};
     PairSmem& ps = sm.xb[warp].pair;
 
-    // ---- integer QK of both pages (two independent MMA chains)
-    uint4 kr0[2], kr1[2], mt[2];
+    // ---- integer QK of both pages (two independent MMA chains). A page word holds one
+    // dim of tokens gq (low nibble) and gq + 8 (high nibble): rows gq take the whole byte
+    // (1024 + c + 16 c'), rows gq + 8 take 1024 + 16 c'; row differences recover both dots
+    uint4 kp0[2], kp1[2], mt[2];
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        kr0[p] = lds128(pgs[p] + kKCodeOff + gq * 64 + 16 * tq);
-        kr1[p] = lds128(pgs[p] + kKCodeOff + (gq + 8) * 64 + 16 * tq);
+        kp0[p] = lds128(pgs[p] + kKCodeOff + 16 * lane);
+        kp1[p] = lds128(pgs[p] + kKCodeOff + 512 + 16 * lane);
         mt[p] = lds128(pgs[p] + kMetaOff + 16 * gq);
     }
     float d[2][4];
@@ -429,16 +419,18 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     }
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii) {
-        const uint4 qv = qf[32 * ii];                // B fragments of k steps 2ii, 2ii + 1
+        const uint4 qv = qf[32 * ii];                // B fragments of MMAs 2ii, 2ii + 1
 #pragma unroll
         for (int p = 0; p < 2; ++p) {
-            const uint32_t w0 = ii == 0 ? kr0[p].x : ii == 1 ? kr0[p].y : ii == 2 ? kr0[p].z : kr0[p].w;
-            const uint32_t w1 = ii == 0 ? kr1[p].x : ii == 1 ? kr1[p].y : ii == 2 ? kr1[p].z : kr1[p].w;
-            mma_f16(d[p], wide_lo(w0), wide_lo(w1), wide_hi(w0), wide_hi(w1), qv.x, qv.y, d[p][0],
-                    d[p][1], d[p][2], d[p][3]);
-            const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
-            mma_f16(d[p], wide_lo(s0), wide_lo(s1), wide_hi(s0), wide_hi(s1), qv.z, qv.w, d[p][0],
-                    d[p][1], d[p][2], d[p][3]);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int i = 2 * ii + e;                // MMA (word) index
+                const uint4& kq = i < 4 ? kp0[p] : kp1[p];
+                const uint32_t wd = (i & 3) == 0 ? kq.x : (i & 3) == 1 ? kq.y : (i & 3) == 2 ? kq.z : kq.w;
+                const uint32_t x = prmt(wd, 0x64646464u, 0x4341u);
+                mma_f16(d[p], wide_byte(wd), wide_hi(wd), x, x & 0xfff0fff0u, e ? qv.z : qv.x,
+                        e ? qv.w : qv.y, d[p][0], d[p][1], d[p][2], d[p][3]);
+            }
         }
     }
 
@@ -448,9 +440,12 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     float Mp[2];
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
-        const float r0 = __shfl_xor_sync(kFull, d[p][1], 2);
+        // column sums: rows gq hold dot(gq) + 16 dot(gq+8), rows gq + 8 hold 16 dot(gq+8)
+        const float2 own = __fadd2_rn(make_float2(d[p][0], d[p][1]), make_float2(-d[p][2], -d[p][3]));
+        const float r0 = __shfl_xor_sync(kFull, own.y, 2);
         const float r1 = __shfl_xor_sync(kFull, d[p][3], 2);
-        const float2 dot = __fadd2_rn(make_float2(d[p][0], d[p][2]), make_float2(r0, r1));
+        const float2 dot = __fmul2_rn(__fadd2_rn(make_float2(own.x, d[p][2]), make_float2(r0, r1)),
+                                      make_float2(1.f, 0.0625f));
         const __half2 km0 = u32_half2(mt[p].x), km1 = u32_half2(mt[p].y);
         const __half2 vm0 = u32_half2(mt[p].z), vm1 = u32_half2(mt[p].w);
         vdl[p] = make_float2(__low2float(vm0), __low2float(vm1));
@@ -583,9 +578,8 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
 
 // ---------------------------------------------------------------- protected group
 // One 16-row side group on the tensor cores, lane roles as on an INT4 page.
-// QK: an INT8 code widens to 1024 + c in a low slot and to 16384 + 16c in a high
-// slot (whose query entry is q/16), one byte permute per two codes, so the query
-// B fragments of the INT4 path serve unchanged and every slot carries 1024 q.
+// QK: an INT8 code widens to 1024 + c, one byte permute per two codes, so the query
+// B fragments and accumulator seeds of the INT4 path serve unchanged.
 // PV: values dequantized to BF16 (A; rows = dims), weights p against the group's max
 // rounded to BF16 (B; columns = heads, k order t, t+8, t+4, t+12 so a scoring lane's
 // pair of rows is one B word), FP32 accumulation, folded into the running output.
@@ -605,9 +599,9 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
 
-// INT8 codes of bytes 0, 1 as fp16 1024 + c; of bytes 2, 3 as fp16 16384 + 16c
+// INT8 codes of bytes 0, 1 (resp. 2, 3) as fp16 1024 + c
 __device__ __forceinline__ uint32_t w8_lo(uint32_t w) { return prmt(w, 0x64646464u, 0x4140u); }
-__device__ __forceinline__ uint32_t w8_hi(uint32_t w) { return prmt(w, 0x74747474u, 0x4342u); }
+__device__ __forceinline__ uint32_t w8_hi(uint32_t w) { return prmt(w, 0x64646464u, 0x4342u); }
 
 __device__ __forceinline__ uint32_t bf16x2_u32(float lo, float hi)
 {
@@ -940,21 +934,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             }
             if (lane < G) {
                 const float4 f = __ldg(reinterpret_cast<const float4*>(rec + lane * kQInfoBytes + kHeadDim));
-                const float4 f8 =
-                    __ldg(reinterpret_cast<const float4*>(rec + lane * kQInfoBytes + kHeadDim + 16));
                 sm.wq[warp].scale[lane] = f.x;
                 sm.wq[warp].qsum[lane] = f.y;
                 sm.wq[warp].corr[lane][0] = f.z;
                 sm.wq[warp].corr[lane][1] = f.w;
-                sm.wq[warp].corr8[lane][0] = f8.x;
-                sm.wq[warp].corr8[lane][1] = f8.y;
             }
             __syncwarp();
             {
                 // QK B fragments. Column g' = head(g') over dim half g' & 1 with
                 // head(n) = n < 4 ? n : n ^ 5; k rows 2t', 2t'+1, 2t'+8, 2t'+9 come from code
                 // lane t', whose dims lie in half t' >> 1. Lane (g', t') keeps its column's
-                // fragments; the high slots hold q/16.
+                // fragments.
                 const int bh = gq < 4 ? gq : (gq ^ 5);
                 const bool bok = (half == (gq & 1)) && (bh < G);
                 const int8_t* qq = sm.wq[warp].q8[bok ? bh : 0];
@@ -963,11 +953,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                     uint32_t f[4];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int base = 32 * tq + 8 * ii + 2 * e;
-                        f[2 * e] = bok ? half2_bits(__int2half_rn(qq[base]), __int2half_rn(qq[base + 4])) : 0u;
-                        f[2 * e + 1] = bok ? half2_bits(__float2half_rn(0.0625f * (float)qq[base + 1]),
-                                                        __float2half_rn(0.0625f * (float)qq[base + 5]))
-                                           : 0u;
+                        // MMA i = 2ii + e: k rows 2t', 2t'+1 are dims 4i, 4i+1 of chunk t',
+                        // k rows 2t'+8, 2t'+9 are dims 4i+2, 4i+3
+                        const int base = 32 * tq + 4 * (2 * ii + e);
+                        f[2 * e] = bok ? half2_bits(__int2half_rn(qq[base]), __int2half_rn(qq[base + 1])) : 0u;
+                        f[2 * e + 1] = bok ? half2_bits(__int2half_rn(qq[base + 2]), __int2half_rn(qq[base + 3])) : 0u;
                     }
                     sm.qfrag[warp][ii][lane] = make_uint4(f[0], f[1], f[2], f[3]);
                 }
@@ -1076,8 +1066,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 for (int r = 0; r < 4; ++r) st.o[mm][r] = 0.f;
             st.M = -INFINITY;
             st.l = 0.f;
-            const float cq0 = hs < G ? -wq.corr8[hs][0] : 0.f;
-            const float cq1 = (hs ^ 1) < G ? -wq.corr8[hs ^ 1][1] : 0.f;
+            const float cq0 = hs < G ? -wq.corr[hs][0] : 0.f;
+            const float cq1 = (hs ^ 1) < G ? -wq.corr[hs ^ 1][1] : 0.f;
             const bool slot_ok = slot >= 0 && slot < a.max_slots;
             const int Lp = slot_ok ? L : 0;
             if (lane == 0) {

@@ -42,8 +42,7 @@ struct PlanHeader {
     int32_t pad;
 };
 
-constexpr int kQInfoBytes = 160;   // per q head: 128 INT8 query bytes, {s_q, Σq8, INT4 offsets x2},
-                                   // {INT8 offsets x2, 0, 0}
+constexpr int kQInfoBytes = 144;   // per q head: 128 INT8 query bytes, {s_q, Σq8, QK offsets x2}
 
 // Pointers into a decode workspace (cache-owned or the static no-allocation array).
 struct DecodeWorkspace {

@@ -20,10 +20,13 @@ def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
     n = len(page_ids)
     base = (np.asarray(page_ids, np.int64) * H + h) * BLOCK
     ts = np.asarray(slots_in_page, np.int64)
-    krow = pages[(base + ts * 64)[:, None] + np.arange(64)[None, :]]
-    k = np.empty((n, D), np.uint8)
-    k[:, 0::2] = krow & 15
-    k[:, 1::2] = krow >> 4
+    dd = np.arange(D)
+    lane = dd // 4
+    i, c = lane % 8, lane // 8
+    kbyte = (i // 4) * 512 + (4 * (ts[:, None] % 8) + c[None, :]) * 16 + (i % 4 * 4)[None, :] \
+        + np.array([0, 2, 1, 3])[dd % 4][None, :]
+    kb = pages[base[:, None] + kbyte]
+    k = np.where((ts[:, None] // 8) == 0, kb & 15, kb >> 4).astype(np.uint8)
     j = np.arange(64)[None, :]
     t = ts[:, None]
     voff = 4 * (8 * (4 * (j % 8) + t % 4) + j // 8) + t // 4
@@ -39,11 +42,8 @@ def unpack_page_tokens(pages, H, page_ids, slots_in_page, h):
 
 def side_k_offset(r, d):
     """Byte of (side row r, dim d) in a group's K block, as declared in include/kv4.h."""
-    u = d % 32
-    e = (u % 8 // 2) % 2
-    byte = 2 * (u % 2) + (u % 8) // 4
-    word = 2 * (u // 8) + e
-    return 1024 * (word // 4) + 64 * r + 16 * (d // 32) + 4 * (word % 4) + byte
+    word = d % 32 // 4
+    return 1024 * (word // 4) + 64 * r + 16 * (d // 32) + 4 * (word % 4) + d % 4
 
 
 def side_v_byte(r):
