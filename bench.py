@@ -38,7 +38,8 @@ UNIT = "context tokens/s"
 DTYPE = "s8 x u4/u8 -> s32 dots, fp32 softmax/accumulate"
 L2_BYTES = 129 * 2 ** 20
 SPLIT_SOURCES = ["int8_hybrid_paged_gb300/csrc/decode.cu",
-                 "int8_hybrid_paged_gb300/csrc/device_common.cuh"]
+                 "int8_hybrid_paged_gb300/csrc/device_common.cuh",
+                 "int8_hybrid_paged_gb300/csrc/kv4_internal.h"]
 
 
 def parse():
