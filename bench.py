@@ -313,7 +313,9 @@ def run_kv4(args, rank, world, local):
     value = tok_sum / (t_max * 1e-3)
 
     call_bytes = bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
-    split_bytes = call_bytes - B * Hq * (128 * 4 + 4)        # outputs are written by the merge
+    # the split kernel reads 144-byte query records (written by the prep kernel) instead
+    # of the bf16 queries; the outputs are written by the merge
+    split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
     split_ms = prof["split_ms"] / max(1, prof["calls"])
     peak, peak_src = measured_peaks()
     achieved = split_bytes / (split_ms * 1e-3) / 1e9
