@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the unprotected KV4 (s = w = 0) measurement")
     return ap.parse_args()
 
 
@@ -352,6 +354,10 @@ def run_kv4(args, rank, world, local):
     if world == 1 and not args.no_append:
         res["append_stress"] = run_append_stress(dev, peak)
 
+    # ---- the same workload without the protected region (pure KV4), rank 0 at N = 1
+    if world == 1 and not args.no_variants and (wl.sink > 0 or wl.window > 0):
+        res["kv4_unprotected"] = run_unprotected(wl, seed, dev, peak, value, min(args.steps, 500))
+
     # ---- end to end through the public API from pinned host buffers
     if not args.no_e2e:
         res["e2e"] = run_e2e(st, wl, args, dev, world)
@@ -362,6 +368,56 @@ def run_kv4(args, rank, world, local):
     cache.close()
     if rank == 0:
         print(json.dumps(res), flush=True)
+
+
+def run_unprotected(wl, seed, dev, peak, protected_value, steps):
+    """The same sequences, KV and queries with s = w = 0 (every position in the INT4
+    pages, no side cache): context tokens/s of the whole decode call, the split
+    kernel's HBM rate, and the share of it the protected configuration keeps."""
+    import dataclasses
+    from int8_hybrid_paged_gb300 import kv4
+
+    wl0 = dataclasses.replace(wl, sink=0, window=0)
+    st = build_workload(wl0, seed, dev)
+    cache = st["cache"]
+    B, Hq = wl0.batch, wl0.num_q_heads
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        def step():
+            for _ in range(wl0.layers):
+                kv4.kv4_decode_attention(cache.handle, st["q"], st["slots"], st["cl"],
+                                         st["bt_dev"], out, lse, stream=stream)
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+        kv4.kv4_profile_start(cache.handle, steps * wl0.layers)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        prof = kv4.kv4_profile_stop(cache.handle)
+        if cache.device_error():
+            raise RuntimeError("device error in the unprotected decode")
+        ms = e0.elapsed_time(e1) / steps
+        value = float(sum(st["lens"])) * wl0.layers / (ms * 1e-3)
+        call_bytes = bytes_model.decode_call_bytes(st["lens"], Hq, wl0.num_kv_heads, 0, 0,
+                                                   with_lse=True)
+        split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
+        split_ms = prof["split_ms"] / max(1, prof["calls"])
+        gbs = split_bytes / (split_ms * 1e-3) / 1e9
+        return {"case": "the same workload with s = w = 0 (no INT8 side cache)",
+                "value": value, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+                "split_us": split_ms * 1e3, "split_algorithmic_bytes": split_bytes,
+                "split_achieved_gbs": gbs, "split_frac_of_hbm_peak": gbs / peak,
+                "protected_retains": protected_value / value}
+    finally:
+        cache.close()
+        torch.cuda.empty_cache()
 
 
 def run_append_stress(dev, peak):

@@ -207,10 +207,10 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  *   config          : the cache geometry the pools were built with
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
  *   other arguments : as kv4_decode_attention
- * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 160 bytes
+ * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 144 bytes
  * per q head, 4 bytes per (sequence, KV head) and G * 520 bytes for each of
  * 2 * batch * H_kv + (persistent warps: 16 per SM) partials (on a 152-SM GB300 with
- * H_q = 32, H_kv = 8 that is batch <= 304); larger calls return KV4_ERR_OUT_OF_RANGE
+ * H_q = 32, H_kv = 8 that is batch <= 308); larger calls return KV4_ERR_OUT_OF_RANGE
  * before anything is enqueued. The first call on each device looks up the scratch
  * array's device address with that device current; make that first call before any
  * stream capture. Every call on a device shares the one array and leaves its contents
