@@ -51,6 +51,12 @@
  *      product uses p and v = bf16(fmaf(Δ8, c, m8)) both rounded to BF16 and sums
  *      in FP32; groups are combined by 2^(M_group − M) like INT4 pages; the
  *      normaliser sums the unrounded p. Float mode keeps p unrounded.
+ *   R10 KV8, the 8-bit whole-cache configuration the pages compare KV4 against
+ *      ([zh] 核心发现 (2), (3); 实验结果, decode-forward replay): every position holds
+ *      the 8-bit affine codes of the side cache (rotated K, unrotated V, the R2
+ *      quantizer with n = 255), and decode applies the protected path of R6 and R7
+ *      to every position, in groups of 16 consecutive positions (one page) in
+ *      position order.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -306,8 +312,10 @@ static void append_one(orc_cache *c, int slot, int pos, int head,
                        const float *k_rot, const float *v)
 {
     size_t mi = idx_main(c, slot, pos, head);
-    orc_quant_affine(k_rot, ORC_D, 15, c->k4_code + mi * ORC_D, c->k4_delta + mi, c->k4_min + mi);
-    orc_quant_affine(v, ORC_D, 15, c->v4_code + mi * ORC_D, c->v4_delta + mi, c->v4_min + mi);
+    const int levels = c->kv8 ? 255 : 15;          /* R10: KV8 keeps 8-bit codes everywhere */
+    orc_quant_affine(k_rot, ORC_D, levels, c->k4_code + mi * ORC_D, c->k4_delta + mi, c->k4_min + mi);
+    orc_quant_affine(v, ORC_D, levels, c->v4_code + mi * ORC_D, c->v4_delta + mi, c->v4_min + mi);
+    if (c->kv8) return;
 
     /* Side buffer: an INT8 copy of a sink position and of the position in the
        recent ring. [ko] 전제와 한계; [zh] 方法步骤详情 step 3. */
@@ -329,6 +337,7 @@ int orc_append(orc_cache *c, int slot, int start, int T,
 {
     if (slot < 0 || slot >= c->num_slots || start < 0 || T < 0 || start + T > c->max_len)
         return -1;
+    if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
     float kx[ORC_D], kr[ORC_D], vx[ORC_D];
     for (int t = 0; t < T; t++) {
         for (int h = 0; h < c->num_heads; h++) {
@@ -391,9 +400,9 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                         int32_t *dbg_qk, float *dbg_sigma, uint8_t *dbg_w)
 {
     const int s = c->sink, w = c->window, P = 16;
-    /* Regions, reading R4. */
+    /* Regions, reading R4 (R10: no INT4 region in KV8). */
     int r4_lo = s, r4_hi = L - w;
-    if (r4_hi < r4_lo) r4_hi = r4_lo;                 /* empty */
+    if (r4_hi < r4_lo || c->kv8) r4_hi = r4_lo;      /* empty */
 
     /* ---- INT4 region: integer QK, page-local integer PV (reading R5) ---- */
     double M4 = -INFINITY, l4 = 0.0;
@@ -478,23 +487,32 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
     /* ---- protected region (R7): INT8 side keys and BF16 values, side rows in
        groups of 16 in side-row order, p against each group's own max; the
        product takes p rounded to BF16 (integer mode) or unrounded (float mode);
-       the normaliser sums the unrounded p ---- */
+       the normaliser sums the unrounded p. KV8 (R10): the same over every
+       position, groups of 16 consecutive positions, codes from the main arrays. ---- */
+    const uint8_t *k8c = c->kv8 ? c->k4_code : c->k8_code;
+    const uint8_t *v8c = c->kv8 ? c->v4_code : c->v8_code;
+    const uint16_t *k8d = c->kv8 ? c->k4_delta : c->k8_delta;
+    const uint16_t *k8m = c->kv8 ? c->k4_min : c->k8_min;
+    const uint16_t *v8d = c->kv8 ? c->v4_delta : c->v8_delta;
+    const uint16_t *v8m = c->kv8 ? c->v4_min : c->v8_min;
     float Mr = -INFINITY;
     double lp_ = 0.0;
     double opr[ORC_D];
     for (int j = 0; j < ORC_D; j++) opr[j] = 0.0;
-    const int S = s + w;
+    const int S = c->kv8 ? L : s + w;               /* rows: side rows, or positions in KV8 */
     for (int g0 = 0; g0 < S; g0 += 16) {
         const int n = (S - g0 < 16) ? S - g0 : 16;
         int pos[16];
+        size_t rix[16];
         float sg[16];
         float Mg = -INFINITY;
         for (int i = 0; i < n; i++) {
-            pos[i] = side_row_position(g0 + i, s, w, L);
+            pos[i] = c->kv8 ? g0 + i : side_row_position(g0 + i, s, w, L);
             if (pos[i] < 0) continue;
-            size_t si = idx_side(c, slot, g0 + i, head);
-            int32_t dot = dot_s8_u8(q8, c->k8_code + si * ORC_D);
-            sg[i] = score_from_dot(dot, c->k8_delta[si], c->k8_min[si], q_scale, q_sum, C);
+            const size_t si = c->kv8 ? idx_main(c, slot, g0 + i, head) : idx_side(c, slot, g0 + i, head);
+            rix[i] = si;
+            int32_t dot = dot_s8_u8(q8, k8c + si * ORC_D);
+            sg[i] = score_from_dot(dot, k8d[si], k8m[si], q_scale, q_sum, C);
             if (dbg_qk) dbg_qk[pos[i]] = dot;
             if (dbg_sigma) dbg_sigma[pos[i]] = sg[i];
             if (sg[i] > Mg) Mg = sg[i];
@@ -507,14 +525,14 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         for (int j = 0; j < ORC_D; j++) og[j] = 0.0;
         for (int i = 0; i < n; i++) {
             if (pos[i] < 0) continue;
-            size_t si = idx_side(c, slot, g0 + i, head);
+            const size_t si = rix[i];
             const float p = orc_exp2f(sg[i] - Mg);
             const double pw = (pv_mode == ORC_PV_FLOAT)
                                   ? (double)p
                                   : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
-            float dv = (float)orc_f16_to_f64(c->v8_delta[si]);
-            float mv = (float)orc_f16_to_f64(c->v8_min[si]);
-            const uint8_t *vc = c->v8_code + si * ORC_D;
+            float dv = (float)orc_f16_to_f64(v8d[si]);
+            float mv = (float)orc_f16_to_f64(v8m[si]);
+            const uint8_t *vc = v8c + si * ORC_D;
             for (int j = 0; j < ORC_D; j++) {
                 float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
                 og[j] += pw * (double)v;
@@ -550,6 +568,7 @@ int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf1
     if (slot < 0 || slot >= c->num_slots || L < 0 || L > c->max_len || G <= 0)
         return -1;
     if (c->sink + c->window > 256) return -1;
+    if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
     const float C = log2e_scale(sm_scale);
     const int HG = c->num_heads * G;
     for (int hq = 0; hq < HG; hq++) {
@@ -600,6 +619,7 @@ int orc_decode_batch(const orc_cache *c, int B, const int32_t *slots, const int3
         if (slots[b] < 0 || slots[b] >= c->num_slots || lens[b] < 0 || lens[b] > c->max_len)
             return -1;
     if (G <= 0 || c->sink + c->window > 256) return -1;
+    if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
     const long n = (long)B * HG;
 #ifdef _OPENMP
     if (num_threads > 0) omp_set_num_threads(num_threads);

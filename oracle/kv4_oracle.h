@@ -35,7 +35,10 @@ typedef struct {
     int32_t window;      /* w */
     int32_t max_len;     /* positions per slot */
     int32_t num_slots;
-    /* INT4 main cache: codes [slot][pos][head][128] in 0..15, meta [slot][pos][head] fp16 bits */
+    int32_t kv8;         /* 0: INT4 main cache + INT8 side buffer; 1: whole-cache INT8 (KV8),
+                            where the main arrays hold 8-bit codes and sink = window = 0 */
+    /* INT4 main cache: codes [slot][pos][head][128] in 0..15 (0..255 in KV8), meta
+       [slot][pos][head] fp16 bits */
     uint8_t  *k4_code, *v4_code;
     uint16_t *k4_delta, *k4_min, *v4_delta, *v4_min;
     /* INT8 side cache: codes [slot][s+w][head][128] in 0..255, meta [slot][s+w][head] fp16 bits.

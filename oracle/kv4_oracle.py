@@ -134,7 +134,7 @@ _STATE_ARRAYS = ("k4_code", "v4_code", "k4_delta", "k4_min", "v4_delta", "v4_min
 
 class _State(C.Structure):
     _fields_ = [("num_heads", C.c_int32), ("sink", C.c_int32), ("window", C.c_int32),
-                ("max_len", C.c_int32), ("num_slots", C.c_int32)] + \
+                ("max_len", C.c_int32), ("num_slots", C.c_int32), ("kv8", C.c_int32)] + \
                [(n, C.c_void_p) for n in _STATE_ARRAYS]
 
 
@@ -144,10 +144,15 @@ class _Debug(C.Structure):
 
 class OracleCache:
     """Logical KV4 cache state: INT4 main cache for every position plus the
-    bounded INT8 side buffer (s sink + w recent positions) per slot."""
+    bounded INT8 side buffer (s sink + w recent positions) per slot. With
+    kv8=True, the whole-cache 8-bit configuration (reading R10): 8-bit codes for
+    every position, no side buffer (sink = window = 0)."""
 
-    def __init__(self, num_heads, sink, window, max_len, num_slots=1):
+    def __init__(self, num_heads, sink, window, max_len, num_slots=1, kv8=False):
+        if kv8 and (sink or window):
+            raise ValueError("the KV8 configuration has no protected region")
         H, S = num_heads, sink + window
+        self.kv8 = bool(kv8)
         self.H, self.s, self.w, self.max_len, self.num_slots = H, sink, window, max_len, num_slots
         z = np.zeros
         self.k4_code = z((num_slots, max_len, H, D), np.uint8)
@@ -163,7 +168,7 @@ class OracleCache:
         self.v8_delta = z((num_slots, S, H), np.uint16)
         self.v8_min = z((num_slots, S, H), np.uint16)
         self.length = z((num_slots,), np.int32)
-        st = _State(H, sink, window, max_len, num_slots)
+        st = _State(H, sink, window, max_len, num_slots, int(self.kv8))
         for n in _STATE_ARRAYS:
             setattr(st, n, getattr(self, n).ctypes.data)
         self._st = st
