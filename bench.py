@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the unprotected KV4 (s = w = 0) measurement")
+                    help="skip the unprotected KV4 (s = w = 0) and whole-cache 8-bit measurements")
     return ap.parse_args()
 
 
@@ -195,7 +195,7 @@ def workload_from_args(args):
     return wl
 
 
-def build_workload(wl, seed, device, sample_seqs=0):
+def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
     """Fill a cache with the workload's sequences (one prefill append). Host copies
     (bf16 bits) of the first `sample_seqs` sequences' K/V are kept for the CPU
     baseline; the device K/V are freed once appended."""
@@ -207,7 +207,7 @@ def build_workload(wl, seed, device, sample_seqs=0):
     num_pages = need + max(64, need // 100)
     bt = inputs.block_tables(lens, 16, num_pages, seed)
     cache = KV4Cache(H, num_pages, max_slots=B, max_batch=B, max_q_heads=Hq, sink=wl.sink,
-                     window=wl.window)
+                     window=wl.window, fmt=fmt)
     total = sum(lens)
     k, v = inputs.kv_tokens(total, H, seed * 1_000_003 + 17, device=device)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
@@ -357,6 +357,8 @@ def run_kv4(args, rank, world, local):
     # ---- the same workload without the protected region (pure KV4), rank 0 at N = 1
     if world == 1 and not args.no_variants and (wl.sink > 0 or wl.window > 0):
         res["kv4_unprotected"] = run_unprotected(wl, seed, dev, peak, value, min(args.steps, 500))
+    if world == 1 and not args.no_variants:
+        res["kv8"] = run_kv8(wl, seed, dev, peak, value, min(args.steps, 500))
 
     # ---- end to end through the public API from pinned host buffers
     if not args.no_e2e:
@@ -415,6 +417,56 @@ def run_unprotected(wl, seed, dev, peak, protected_value, steps):
                 "split_us": split_ms * 1e3, "split_algorithmic_bytes": split_bytes,
                 "split_achieved_gbs": gbs, "split_frac_of_hbm_peak": gbs / peak,
                 "protected_retains": protected_value / value}
+    finally:
+        cache.close()
+        torch.cuda.empty_cache()
+
+
+def run_kv8(wl, seed, dev, peak, kv4_value, steps):
+    """The same sequences, KV and queries in the whole-cache 8-bit format (every
+    position's 8-bit codes in its page, the protected path's arithmetic): context
+    tokens/s of the whole decode call and the split kernel's HBM rate."""
+    import dataclasses
+    from int8_hybrid_paged_gb300 import kv4
+
+    wl8 = dataclasses.replace(wl, sink=0, window=0)
+    st = build_workload(wl8, seed, dev, fmt=kv4.FORMAT_INT8)
+    cache = st["cache"]
+    B, Hq = wl8.batch, wl8.num_q_heads
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    try:
+        def step():
+            for _ in range(wl8.layers):
+                kv4.kv4_decode_attention(cache.handle, st["q"], st["slots"], st["cl"],
+                                         st["bt_dev"], out, lse, stream=stream)
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+        kv4.kv4_profile_start(cache.handle, steps * wl8.layers)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        prof = kv4.kv4_profile_stop(cache.handle)
+        if cache.device_error():
+            raise RuntimeError("device error in the 8-bit decode")
+        ms = e0.elapsed_time(e1) / steps
+        value = float(sum(st["lens"])) * wl8.layers / (ms * 1e-3)
+        call_bytes = bytes_model.decode_call_bytes_kv8(st["lens"], Hq, wl8.num_kv_heads,
+                                                       with_lse=True)
+        split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
+        split_ms = prof["split_ms"] / max(1, prof["calls"])
+        gbs = split_bytes / (split_ms * 1e-3) / 1e9
+        return {"case": "the same workload, whole-cache 8-bit format (KV8: 264 B per token-head)",
+                "value": value, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+                "split_us": split_ms * 1e3, "split_algorithmic_bytes": split_bytes,
+                "split_achieved_gbs": gbs, "split_frac_of_hbm_peak": gbs / peak,
+                "kv4_speedup_over_kv8": kv4_value / value}
     finally:
         cache.close()
         torch.cuda.empty_cache()

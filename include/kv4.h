@@ -56,6 +56,16 @@ typedef enum {
     KV4_DEVERR_BAD_TOKENS = 6      /* cu_tokens not non-decreasing or not ending at total_tokens */
 } kv4_device_error;
 
+/* Cache formats. KV4_FORMAT_INT4_HYBRID is the method: INT4 pages for every
+ * position plus the bounded INT8 side buffer of sink and recent positions.
+ * KV4_FORMAT_INT8 is the whole-cache 8-bit configuration the pages compare it
+ * against (KV8, [zh] 核心发现 (2)): the same 8-bit group-affine codes as the side
+ * buffer for every position, in pages, and no side buffer (sink = window = 0). */
+typedef enum {
+    KV4_FORMAT_INT4_HYBRID = 0,
+    KV4_FORMAT_INT8 = 1
+} kv4_format;
+
 typedef struct {
     int32_t num_kv_heads;    /* H_kv >= 1 */
     int32_t head_dim;        /* must be 128 (one quantization group per token-head, [zh] 分组仿射 KV 量化) */
@@ -68,6 +78,7 @@ typedef struct {
     int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
     int32_t max_work_items;  /* ignored (kept for layout stability): the decode workspace is sized
                                 from max_batch, max_q_heads and the device's SM count */
+    int32_t format;          /* kv4_format; KV4_FORMAT_INT8 requires sink = window = 0 */
 } kv4_cache_config;
 
 /*
@@ -98,11 +109,15 @@ typedef struct {
  *                         b' = (r/8)%2 + 2*((r/4)%2): 2176 + 16*(32*(W'/4) + n) + 4*(W'%4) + b'
  *                         V metadata of row r at 2176 + 2048 + 16*(r%4) + 4*b'
  * so each lane of a warp reads its tensor-core fragments with 16-byte loads.
+ * KV4_FORMAT_INT8 pages: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES_INT8 = 4352
+ * bytes, block (p, h) at (p * H_kv + h) * 4352, each laid out as one side group
+ * above with row r = t, the page's token slot t; there is no side pool.
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128
 #define KV4_PAGE_SIZE 16
 #define KV4_PAGE_BLOCK_BYTES 2176
+#define KV4_PAGE_BLOCK_BYTES_INT8 4352
 
 typedef struct {
     void   *page_pool_dev;   size_t page_pool_bytes;
@@ -134,6 +149,8 @@ kv4_status kv4_cache_get_info(const kv4_cache *cache, kv4_cache_info *info);
  * slot pos%16. A position p < s also gets an 8-bit copy in sink row p; a
  * position p >= L_new - w (L_new = start_pos[i] + its token count) gets an
  * 8-bit copy in ring row s + p mod w. The slot's length becomes L_new.
+ * KV4_FORMAT_INT8 caches store the 8-bit codes (n = 255, same rounding) of
+ * rotated K and V for every position in row pos%16 of the page's block instead.
  *   k_bf16_dev, v_bf16_dev : [total_tokens][H_kv][128] bf16, tokens of sequence i
  *                            at rows cu_tokens[i] .. cu_tokens[i+1]-1
  *   cu_tokens_dev          : [n_seqs+1] int32, non-decreasing, cu[0] = 0, cu[n] = total_tokens
@@ -160,6 +177,8 @@ kv4_status kv4_append(kv4_cache *cache, const void *k_bf16_dev, const void *v_bf
  *     side keys; side values dequantized to bf16; PV accumulated in FP32.
  *   The regions' outputs and log-normalizers are merged exactly (log-sum-exp),
  *   split-K partials over pages likewise.
+ *   KV4_FORMAT_INT8 caches: every position takes the protected region's arithmetic
+ *   (INT8 keys, bf16 values, FP32 PV) from its page, 16 positions per group.
  *   q_bf16_dev       : [batch][num_q_heads][128] bf16 (post-RoPE, unrotated)
  *   slot_ids_dev     : [batch] int32
  *   context_lens_dev : [batch] int32 L_b, including the token appended this step;
@@ -182,7 +201,8 @@ kv4_status kv4_decode_attention(kv4_cache *cache, const void *q_bf16_dev, int nu
  *   q8_dev     : [batch][num_q_heads][128] int8 quantized rotated query
  *   q_scale_dev: [batch][num_q_heads] fp32 s_q
  *   qk_dev     : [batch][num_q_heads][debug_stride] int32 QK accumulator per position
- *                (INT4 codes in the INT4 region, INT8 side codes in the protected region)
+ *                (INT4 codes in the INT4 region, INT8 side codes in the protected region,
+ *                INT8 page codes in KV4_FORMAT_INT8)
  *   w_hat_dev  : [batch][num_q_heads][debug_stride] u8 PV weight per INT4-region position
  * Positions >= debug_stride are not written. For tests; slower than the plain call.
  */
@@ -206,6 +226,7 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *   config          : the cache geometry the pools were built with
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
+ *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8 configuration)
  *   other arguments : as kv4_decode_attention
  * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 144 bytes
  * per q head, 4 bytes per (sequence, KV head) and G * 520 bytes for each of

@@ -59,6 +59,23 @@ def decode_call_bytes(context_lens, num_q_heads: int, num_kv_heads: int, sink: i
     return total
 
 
+def decode_call_bytes_kv8(context_lens, num_q_heads: int, num_kv_heads: int,
+                          page_size: int = 16, with_lse: bool = False) -> int:
+    """Algorithmic HBM bytes of one decode-attention call on the whole-cache 8-bit
+    format: 8-bit codes + metadata of every position (264 B per position-head), bf16
+    queries, fp32 outputs, context lengths and slot ids, and the block-table entries
+    of the pages read."""
+    total = 0
+    for L in context_lens:
+        L = int(L)
+        total += num_kv_heads * L * SIDE_POSITION_HEAD_BYTES + 4 * ((L + page_size - 1) // page_size) + 8
+    B = len(context_lens)
+    total += B * num_q_heads * HEAD_DIM * (2 + 4)
+    if with_lse:
+        total += B * num_q_heads * 4
+    return total
+
+
 def append_call_bytes(num_tokens: int, num_kv_heads: int, side_writes: int) -> int:
     """Algorithmic bytes of one append: bf16 K and V read, INT4 codes and metadata
     written, and ``side_writes`` INT8 side position-heads written."""

@@ -99,6 +99,9 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
         return KV4_ERR_INVALID_ARG;
     if (cfg->head_dim != KV4_HEAD_DIM || cfg->page_size != KV4_PAGE_SIZE) return KV4_ERR_UNSUPPORTED;
     if (cfg->sink + cfg->window > kv4::kMaxProtected) return KV4_ERR_UNSUPPORTED;
+    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8) return KV4_ERR_INVALID_ARG;
+    const bool kv8 = cfg->format == KV4_FORMAT_INT8;
+    if (kv8 && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
     if (cfg->max_q_heads % cfg->num_kv_heads != 0) return KV4_ERR_INVALID_ARG;
     const int gmax = cfg->max_q_heads / cfg->num_kv_heads;
     if (gmax > 4) return KV4_ERR_UNSUPPORTED;
@@ -122,7 +125,7 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
     const int H = cfg->num_kv_heads;
     const int S = cfg->sink + cfg->window;
     c->side_block = (size_t)((S + 15) / 16) * kv4::kSideGroupBytes;
-    c->pages_bytes = (size_t)cfg->num_pages * H * kv4::kPageBlock;
+    c->pages_bytes = (size_t)cfg->num_pages * H * (kv8 ? kv4::kPageBlock8 : kv4::kPageBlock);
     c->side_bytes = (size_t)cfg->max_slots * H * c->side_block;
     int grid_max = 0;
     for (int g = 1; g <= 4; g <<= 1) grid_max = std::max(grid_max, c->grid[g]);
@@ -199,6 +202,7 @@ kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t*
     a.side_block_bytes = (int64_t)c->side_block;
     a.seq_len = c->seq_len;
     a.err = c->err;
+    a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
     return check_launch(kv4::launch_append(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -256,6 +260,7 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.dbg_qk = dqk;
     a.dbg_w = dw;
     a.dbg_stride = dbg_stride;
+    a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
     cudaEvent_t* ev = nullptr;
     if (c->profiling && c->prof_calls < c->prof_capacity) ev = &c->events[4 * c->prof_calls++];
     return check_launch(kv4::launch_decode(a, c->grid[G], static_cast<cudaStream_t>(stream), ev));

@@ -46,6 +46,26 @@ __device__ __forceinline__ int side_v_offset(int r, int d)
     return 16 * (32 * (word >> 2) + n) + 4 * (word & 3) + side_v_byte(r);
 }
 
+// One row rr of a 16-row INT8 group (a side group, or a page of the 8-bit format):
+// this lane's four K and V codes (dims 4 lane .. 4 lane + 3) and, from lane 0, the
+// row's metadata.
+__device__ __forceinline__ void store_int8_row(uint8_t* g, int rr, const uint32_t (&k8)[4],
+                                               const uint32_t (&v8)[4], __half k8d, __half k8m,
+                                               __half v8d, __half v8m, int lane)
+{
+    // the K codes of four consecutive dims are one word in natural order
+    *reinterpret_cast<uint32_t*>(g + kSideKCodeOff + side_k_offset(rr, 4 * lane)) =
+        k8[0] | (k8[1] << 8) | (k8[2] << 16) | (k8[3] << 24);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
+    if (lane == 0) {
+        *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
+            __halves2half2(k8d, k8m);
+        *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
+            __halves2half2(v8d, v8m);
+    }
+}
+
 // Page K codes: tokens t and t+8 share bytes (t in the low nibble). Lane l of a warp
 // holding dims 4l..4l+3 owns one 32-bit word per token pair: dims 4i, 4i+2, 4i+1,
 // 4i+3 of chunk c (i = l % 8, c = l / 8) in bytes 0..3, at plane i / 4 (512 bytes),
@@ -92,21 +112,9 @@ __device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)
         int n = 0;
         if (to_sink) idx[n++] = pos;
         if (to_ring) idx[n++] = s + pos % w;
-        for (int k = 0; k < n; ++k) {
-            uint8_t* g = sb + (idx[k] >> 4) * kSideGroupBytes;
-            const int rr = idx[k] & 15;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                g[kSideKCodeOff + side_k_offset(rr, 4 * lane + i)] = (uint8_t)k8[i];
-                g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
-            }
-            if (lane == 0) {
-                *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
-                    __halves2half2(k8d, k8m);
-                *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
-                    __halves2half2(v8d, v8m);
-            }
-        }
+        for (int k = 0; k < n; ++k)
+            store_int8_row(sb + (idx[k] >> 4) * kSideGroupBytes, idx[k] & 15, k8, v8, k8d, k8m, v8d,
+                           v8m, lane);
     }
     return kn;
 }
@@ -155,6 +163,25 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
     }
 
     const int H = a.num_heads, ts = pos % kPage;
+    if (a.kv8) {
+        // whole-cache 8-bit format: row ts of the page's group, every head of the warp
+        uint8_t* blk8 = a.pages + (int64_t)page * H * kPageBlock8;
+        const uint16_t* krow = a.k + (int64_t)tok * H * kHeadDim + 4 * lane;
+        const uint16_t* vrow = a.v + (int64_t)tok * H * kHeadDim + 4 * lane;
+        for (int h = h_lo; h < h_hi; ++h) {
+            float kx[4], vx[4];
+            load_bf16x4(krow + h * kHeadDim, kx);
+            load_bf16x4(vrow + h * kHeadDim, vx);
+            warp_fwht128(kx, lane);
+            uint32_t k8[4], v8[4];
+            __half k8d, k8m, v8d, v8m;
+            warp_quant<255>(kx, k8, k8d, k8m);
+            warp_quant<255>(vx, v8, v8d, v8m);
+            store_int8_row(blk8 + h * kPageBlock8, ts, k8, v8, k8d, k8m, v8d, v8m, lane);
+        }
+        if (lane == 0 && h_lo == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
+        return;
+    }
     // tokens t and t+8 of a page share their K bytes. When both are in this append,
     // their 2 x groups warps split the heads of both tokens and each writes whole
     // words; a token without its partner merges its nibbles into the word (the partner

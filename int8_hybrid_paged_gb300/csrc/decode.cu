@@ -28,6 +28,7 @@
 #include <float.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "kv4_internal.h"
@@ -51,7 +52,7 @@ struct __align__(16) WarpQ {
 struct Walk {
     int lo, hi;
     int b, h;
-    int L, n, cbh, csb, slot;   // of the current b
+    int L, n, cp, cbh, csb, slot;   // of the current b (cp: protected stage items per unit)
     int k;                      // current item of (b, h): k < n INT4 page, else protected item
     int a1;                     // end of the span's INT4 pages of (b, h)
     int g0, g1;                 // the span's protected groups of (b, h): first items in [lo, hi)
@@ -178,20 +179,27 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
         // ---- plan: cost line, spans, piece counts
         __shared__ int s_scan[33];
         const int B = a.batch, H = a.num_heads, s = a.sink, w = a.window;
-        const int cp = prot_items(s + w);
+        const bool kv8 = a.kv8 != 0;
+        // INT4 pages and protected stage items of sequence b's units (KV8: all of its
+        // positions are protected rows of its pages)
+        auto n_of = [&](int L) { return kv8 ? 0 : int4_pages(L, s, w); };
+        auto cp_of = [&](int L) { return prot_items(kv8 ? L : s + w); };
         const int per = (B + kPrepThreads - 1) / kPrepThreads;
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         int cost = 0;
-        for (int b = b0; b < b1; ++b) cost += H * unit_cost(int4_pages(max(0, a.context_lens[b]), s, w), cp);
+        for (int b = b0; b < b1; ++b) {
+            const int L = max(0, a.context_lens[b]);
+            cost += H * unit_cost(n_of(L), cp_of(L));
+        }
         int total = 0;
         int off = block_scan(cost, s_scan, total);
         const int span = max(2, (total + a.num_warps - 1) / a.num_warps);
         const SpanDiv sd((uint32_t)span);
-        const int plen = prot_span_len(cp);
         int segs = 0;
         for (int b = b0; b < b1; ++b) {
             a.cost_start[b] = off;
-            const int n = int4_pages(max(0, a.context_lens[b]), s, w);
+            const int L = max(0, a.context_lens[b]);
+            const int n = n_of(L), cp = cp_of(L), plen = prot_span_len(cp);
             for (int h = 0; h < H; ++h) {
                 const int base = off + h * unit_cost(n, cp);
                 segs += sd.pieces(base, n) + sd.pieces(base + n, plen);
@@ -201,7 +209,8 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
         int nseg = 0;
         int soff = block_scan(segs, s_scan, nseg);
         for (int b = b0; b < b1; ++b) {
-            const int n = int4_pages(max(0, a.context_lens[b]), s, w);
+            const int L = max(0, a.context_lens[b]);
+            const int n = n_of(L), cp = cp_of(L), plen = prot_span_len(cp);
             const int cs = a.cost_start[b];
             for (int h = 0; h < H; ++h) {
                 a.unit_seg[b * H + h] = soff;
@@ -306,19 +315,24 @@ __device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_c
 // (b, h) touched, the INT4 pages of the span's overlap, then the protected unit
 // if its first item lies in the span (its owner takes all of it).
 
+// KV8: no INT4 pages; every position is a protected row of its page, so the
+// protected items of a unit follow its length.
+template <bool KV8>
 __device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b, int cp)
 {
     W.b = b;
     W.L = max(0, __ldg(&a.context_lens[b]));
-    W.n = int4_pages(W.L, a.sink, a.window);
-    W.cbh = unit_cost(W.n, cp);
+    W.n = KV8 ? 0 : int4_pages(W.L, a.sink, a.window);
+    W.cp = KV8 ? prot_items(W.L) : cp;
+    W.cbh = unit_cost(W.n, W.cp);
     W.csb = __ldg(&a.cost_start[b]);
     W.slot = __ldg(&a.slot_ids[b]);
 }
 
 // Position the walker at the first item of (b, h) inside the span; false if none.
-__device__ __forceinline__ bool walk_enter(Walk& W, int cp)
+__device__ __forceinline__ bool walk_enter(Walk& W)
 {
+    const int cp = W.cp;
     const int base = W.csb + W.h * W.cbh;
     const int a0 = max(W.lo, base) - base;
     W.a1 = min(W.hi, base + W.n) - base;
@@ -330,19 +344,21 @@ __device__ __forceinline__ bool walk_enter(Walk& W, int cp)
     return false;
 }
 
+template <bool KV8>
 __device__ __forceinline__ void walk_next_bh(Walk& W, const DecodeArgs& a, int cp)
 {
     for (;;) {
         if (++W.h == a.num_heads) {
             if (W.b + 1 >= a.batch) { W.done = true; return; }
-            walk_load_b(W, a, W.b + 1, cp);
+            walk_load_b<KV8>(W, a, W.b + 1, cp);
             W.h = 0;
         }
         if (W.csb + W.h * W.cbh >= W.hi) { W.done = true; return; }
-        if (walk_enter(W, cp)) return;
+        if (walk_enter(W)) return;
     }
 }
 
+template <bool KV8>
 __device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, int hi, int cp)
 {
     W.lo = lo;
@@ -354,9 +370,9 @@ __device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, 
         const int m = (l + r) >> 1;
         if (__ldg(&a.cost_start[m]) <= lo) l = m; else r = m;
     }
-    walk_load_b(W, a, l, cp);
+    walk_load_b<KV8>(W, a, l, cp);
     W.h = min(a.num_heads - 1, (lo - W.csb) / W.cbh);
-    if (!walk_enter(W, cp)) walk_next_bh(W, a, cp);
+    if (!walk_enter(W)) walk_next_bh<KV8>(W, a, cp);
 }
 
 
@@ -639,7 +655,7 @@ __device__ __forceinline__ int side_row_position(int rr, int s, int w, int L)
     return p >= s ? p : -1;
 }
 
-template <int G, bool DEBUG>
+template <int G, bool DEBUG, bool KV8>
 __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, ProtState& st,
                                            const uint4* __restrict__ qf, float cq0, float cq1,
                                            float sqh, float qsh, const uint8_t* pk,
@@ -676,8 +692,12 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     const float2 u = __ffma2_rn(kd, dot, __fmul2_rn(kmin, make_float2(qsh, qsh)));
     const float2 sg =
         __fmul2_rn(__fmul2_rn(u, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
-    const int pos0 = side_row_position(16 * grp + gq, a.sink, a.window, L);
-    const int pos1 = side_row_position(16 * grp + gq + 8, a.sink, a.window, L);
+    // rows of a side group hold the positions of the ring/sink rule; rows of a KV8
+    // page hold its 16 consecutive positions
+    const int pos0 = KV8 ? (16 * grp + gq < L ? 16 * grp + gq : -1)
+                         : side_row_position(16 * grp + gq, a.sink, a.window, L);
+    const int pos1 = KV8 ? (16 * grp + gq + 8 < L ? 16 * grp + gq + 8 : -1)
+                         : side_row_position(16 * grp + gq + 8, a.sink, a.window, L);
     const float2 sig = make_float2(pos0 >= 0 ? sg.x : -INFINITY, pos1 >= 0 ? sg.y : -INFINITY);
     if (DEBUG && a.dbg_qk && hs < G) {
         const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
@@ -756,18 +776,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 __device__ __forceinline__ Walk walk_load(const volatile Walk& s)
 {
     Walk w;
-    w.lo = s.lo; w.hi = s.hi; w.b = s.b; w.h = s.h; w.L = s.L; w.n = s.n; w.cbh = s.cbh;
+    w.lo = s.lo; w.hi = s.hi; w.b = s.b; w.h = s.h; w.L = s.L; w.n = s.n; w.cp = s.cp; w.cbh = s.cbh;
     w.csb = s.csb; w.slot = s.slot; w.k = s.k; w.a1 = s.a1; w.g0 = s.g0; w.g1 = s.g1; w.done = s.done;
     return w;
 }
 
 __device__ __forceinline__ void walk_store(volatile Walk& d, const Walk& w)
 {
-    d.lo = w.lo; d.hi = w.hi; d.b = w.b; d.h = w.h; d.L = w.L; d.n = w.n; d.cbh = w.cbh;
+    d.lo = w.lo; d.hi = w.hi; d.b = w.b; d.h = w.h; d.L = w.L; d.n = w.n; d.cp = w.cp; d.cbh = w.cbh;
     d.csb = w.csb; d.slot = w.slot; d.k = w.k; d.a1 = w.a1; d.g0 = w.g0; d.g1 = w.g1; d.done = w.done;
 }
 
-template <int G, bool DEBUG>
+template <int G, bool DEBUG, bool KV8>
 __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -790,7 +810,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
         const int total = a.plan->total_cost;
         const int lo = min(total, wg * span), hi = min(total, lo + span);
         Walk W;
-        walk_init(W, a, lo, hi, cp);
+        walk_init<KV8>(W, a, lo, hi, cp);
         if (lane == 0) {
             walk_store(Psm, W);
             walk_store(Csm, W);
@@ -815,8 +835,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     auto next_run = [&]() -> bool {
         Walk P = walk_load(Psm);
         if (r_kind >= 0) {                  // leave the run that just ended
-            if (r_kind == 0 && P.g0 < P.g1) P.k = P.n + group_items(cp) * P.g0;
-            else walk_next_bh(P, a, cp);
+            if (r_kind == 0 && P.g0 < P.g1) P.k = P.n + group_items(P.cp) * P.g0;
+            else walk_next_bh<KV8>(P, a, cp);
         }
         bool more = !P.done;
         if (more) {
@@ -827,10 +847,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 r_b = P.b;
                 r_src = a.pages + (int64_t)P.h * kPageBlock;
                 win_lo = -64;               // force a window load
+            } else if (KV8) {
+                // the unit's pages, two stage items (K block, V block) each
+                r_kind = P.L > 0 ? 3 : 2;
+                r_i = P.k;
+                r_end = group_items(P.cp) * P.g1;
+                r_b = P.b;
+                r_src = a.pages + (int64_t)P.h * kPageBlock8;
+                win_lo = -64;               // force a window load
             } else {
                 r_kind = S > 0 ? 1 : 2;
                 r_i = P.k - P.n;
-                r_end = group_items(cp) * P.g1;
+                r_end = group_items(P.cp) * P.g1;
                 const int slot = (P.slot >= 0 && P.slot < a.max_slots) ? P.slot : 0;
                 r_src = a.side + ((int64_t)slot * H + P.h) * a.side_block_bytes;
             }
@@ -843,6 +871,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
         return more;
     };
     const int64_t page_stride = (int64_t)H * kPageBlock;
+    const int64_t page_stride8 = (int64_t)H * kPageBlock8;
     auto produce = [&]() {
         // common case: two more pages of the current INT4 run, both inside the
         // block-table window, and two free stages
@@ -887,6 +916,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 issue_bulk(dst, r_src + (int64_t)page * page_stride, kPageBlock, bar, is_l0);
             } else if (r_kind == 1) {
                 issue_bulk(dst, r_src + (int64_t)r_i * kPageBlock, kPageBlock, bar, is_l0);
+            } else if (KV8 && r_kind == 3) {
+                const int lp = r_i >> 1;
+                if ((unsigned)(lp - win_lo) >= 32u) {
+                    win_lo = lp;
+                    const int e = lp + lane;
+                    int pg = -1;
+                    if (e < a.stride) pg = __ldg(&a.block_table[(int64_t)r_b * a.stride + e]);
+                    // entries past the unit's pages are never issued; report the rest
+                    if (e < (r_end >> 1) && (e >= a.stride || pg < 0 || (int64_t)pg >= a.num_pages)) {
+                        report_error(a.err, e >= a.stride ? KV4_DEVERR_BAD_POSITION : KV4_DEVERR_BAD_PAGE);
+                        pg = 0;
+                    }
+                    win = pg;
+                }
+                const int page = __shfl_sync(kFull, win, lp - win_lo);
+                issue_bulk(dst, r_src + (int64_t)page * page_stride8 + (r_i & 1) * kPageBlock, kPageBlock,
+                           bar, is_l0);
             } else {
                 arrive_pred(bar, is_l0);    // empty protected item: no side buffer
             }
@@ -975,7 +1021,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
         reinterpret_cast<uint4*>(&sm.xb[warp].pair.wfrag[0][0][0])[lane] = make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
 
-        if (k < n) {
+        if (!KV8 && k < n) {
             // ---- INT4 run: pages k .. a1-1 of (b, h)
             // accumulator seeds: minus the widening offsets of (head hs, half 0) and
             // (head hs ^ 1, half 1), the two columns this lane's C fragment covers
@@ -1052,8 +1098,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 }
             }
             if (gq == 0 && hs < G) a.part_ml[(int64_t)idx * G + hs] = make_float2(st.M, st.l);
-            if (C.g0 < C.g1) C.k = C.n + group_items(cp) * C.g0;
-            else walk_next_bh(C, a, cp);
+            if (C.g0 < C.g1) C.k = C.n + group_items(C.cp) * C.g0;
+            else walk_next_bh<KV8>(C, a, cp);
             __syncwarp();
             if (lane == 0) walk_store(Csm, C);
             __syncwarp();
@@ -1074,12 +1120,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 if (!slot_ok) report_error(a.err, KV4_DEVERR_BAD_SLOT);
                 else if (L != __ldg(&a.seq_len[slot])) report_error(a.err, KV4_DEVERR_LEN_MISMATCH);
             }
-            if (S > 0) {
+            if (KV8 ? L > 0 : S > 0) {
 #pragma unroll 1
                 for (int grp = g0; grp < g1; ++grp) {
                     const int s0 = wait_next();
                     const int s1 = wait_next();
-                    prot_group<G, DEBUG>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
+                    prot_group<G, DEBUG, KV8>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
                                          sm.stage[warp][s1], grp, Lp, b, h, warp, lane);
                     produce();
                 }
@@ -1111,7 +1157,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             }
             if (gq == 0 && hs < G) a.part_ml[(int64_t)pidx * G + hs] = make_float2(st.M, st.l);
             Walk C = walk_load(Csm);
-            walk_next_bh(C, a, cp);
+            walk_next_bh<KV8>(C, a, cp);
             __syncwarp();
             if (lane == 0) walk_store(Csm, C);
             __syncwarp();
@@ -1225,14 +1271,14 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 }
 
 // ---------------------------------------------------------------- launchers
-template <int G, bool DEBUG>
+template <int G, bool DEBUG, bool KV8>
 static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     if (ev) cudaEventRecord(ev[0], stream);
     const int prep_blocks = 1 + (a.batch * a.num_q_heads + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
     kv4_decode_prep_kernel<<<prep_blocks, kPrepThreads, 0, stream>>>(a);
     if (ev) cudaEventRecord(ev[1], stream);
-    kv4_decode_split_kernel<G, DEBUG><<<grid, kDecodeThreads, sizeof(SplitSmem), stream>>>(a);
+    kv4_decode_split_kernel<G, DEBUG, KV8><<<grid, kDecodeThreads, sizeof(SplitSmem), stream>>>(a);
     if (ev) cudaEventRecord(ev[2], stream);
     const int warps = a.batch * a.num_q_heads;
     kv4_decode_merge_kernel<G><<<(warps + 3) / 4, 128, 0, stream>>>(a);
@@ -1243,10 +1289,20 @@ static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     const bool dbg = a.dbg_q8 || a.dbg_qscale || a.dbg_qk || a.dbg_w;
+    const int sel = (dbg ? 1 : 0) + (a.kv8 ? 2 : 0);
+    auto go = [&](auto g) -> cudaError_t {
+        constexpr int Gc = decltype(g)::value;
+        switch (sel) {
+        case 0: return launch_g<Gc, false, false>(a, grid, stream, ev);
+        case 1: return launch_g<Gc, true, false>(a, grid, stream, ev);
+        case 2: return launch_g<Gc, false, true>(a, grid, stream, ev);
+        default: return launch_g<Gc, true, true>(a, grid, stream, ev);
+        }
+    };
     switch (a.group) {
-    case 1: return dbg ? launch_g<1, true>(a, grid, stream, ev) : launch_g<1, false>(a, grid, stream, ev);
-    case 2: return dbg ? launch_g<2, true>(a, grid, stream, ev) : launch_g<2, false>(a, grid, stream, ev);
-    case 4: return dbg ? launch_g<4, true>(a, grid, stream, ev) : launch_g<4, false>(a, grid, stream, ev);
+    case 1: return go(std::integral_constant<int, 1>{});
+    case 2: return go(std::integral_constant<int, 2>{});
+    case 4: return go(std::integral_constant<int, 4>{});
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1257,13 +1313,12 @@ template <int G>
 static cudaError_t split_setup(int* ctas)
 {
     const int smem = (int)sizeof(SplitSmem);
-    cudaError_t e = cudaFuncSetAttribute(kv4_decode_split_kernel<G, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kv4_decode_split_kernel<G, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaSuccess;
+    for (auto k : {kv4_decode_split_kernel<G, false, false>, kv4_decode_split_kernel<G, true, false>,
+                   kv4_decode_split_kernel<G, false, true>, kv4_decode_split_kernel<G, true, true>})
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false, false>,
                                                          kDecodeThreads, smem);
 }
 
@@ -1371,8 +1426,11 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
         cfg->max_slots < 1)
         return KV4_ERR_INVALID_ARG;
     if (cfg->sink + cfg->window > kMaxProtected || cfg->num_pages > INT32_MAX) return KV4_ERR_UNSUPPORTED;
+    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8) return KV4_ERR_INVALID_ARG;
+    const bool kv8 = cfg->format == KV4_FORMAT_INT8;
+    if (kv8 && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
     if (batch == 0) return KV4_OK;
-    if (!page_pool_dev || !side_pool_dev || !seq_len_dev || !q_bf16_dev || !slot_ids_dev ||
+    if (!page_pool_dev || (!side_pool_dev && !kv8) || !seq_len_dev || !q_bf16_dev || !slot_ids_dev ||
         !context_lens_dev || !block_table_dev || !out_dev || block_table_stride < 1)
         return KV4_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale) || sm_scale == INFINITY || sm_scale == -INFINITY) return KV4_ERR_INVALID_ARG;
@@ -1426,6 +1484,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.num_warps = d->grid[G] * (kDecodeThreads / 32);
     a.out = out_dev;
     a.lse = lse_dev;
+    a.kv8 = kv8;
     const cudaError_t e = launch_decode(a, d->grid[G], static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
 }

@@ -28,6 +28,8 @@ constexpr int kSideKCodeOff = 0;
 constexpr int kSideKMetaOff = 2048;
 constexpr int kSideVCodeOff = kPageBlock;
 constexpr int kSideVMetaOff = kPageBlock + 2048;
+// A page block of the whole-cache 8-bit format: one side group, row r = token slot r.
+constexpr int kPageBlock8 = kSideGroupBytes;
 constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per SM
 constexpr int kStages = 5;               // page stages per warp
 // Cost-line positions charged to every (sequence, KV head) unit beyond its stage
@@ -73,6 +75,7 @@ struct AppendArgs {
     int64_t side_block_bytes;
     int32_t* seq_len;
     int32_t* err;
+    int32_t kv8;                  // KV4_FORMAT_INT8: 8-bit codes in pages of kPageBlock8 bytes
 };
 
 struct DecodeArgs {
@@ -111,6 +114,7 @@ struct DecodeArgs {
     int32_t* dbg_qk;
     uint8_t* dbg_w;
     int32_t dbg_stride;
+    int32_t kv8;                  // KV4_FORMAT_INT8: every position a protected row of its page
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);

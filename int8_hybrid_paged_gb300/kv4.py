@@ -41,7 +41,11 @@ class kv4_cache_config(C.Structure):
     _fields_ = [("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("page_size", C.c_int32),
                 ("sink", C.c_int32), ("window", C.c_int32), ("num_pages", C.c_int64),
                 ("max_slots", C.c_int32), ("max_batch", C.c_int32), ("max_q_heads", C.c_int32),
-                ("max_work_items", C.c_int32)]
+                ("max_work_items", C.c_int32), ("format", C.c_int32)]
+
+
+FORMAT_INT4_HYBRID = 0     # INT4 pages + bounded INT8 side buffer (the method)
+FORMAT_INT8 = 1            # whole-cache 8-bit codes in pages, no side buffer (KV8)
 
 
 class kv4_cache_info(C.Structure):
@@ -127,9 +131,10 @@ def kv4_status_string(status: int) -> str:
 
 
 def kv4_cache_create(num_kv_heads, num_pages, max_slots, max_batch, max_q_heads, sink=16,
-                     window=128, head_dim=HEAD_DIM, page_size=PAGE_SIZE, max_work_items=0):
+                     window=128, head_dim=HEAD_DIM, page_size=PAGE_SIZE, max_work_items=0,
+                     fmt=FORMAT_INT4_HYBRID):
     cfg = kv4_cache_config(num_kv_heads, head_dim, page_size, sink, window, num_pages, max_slots,
-                           max_batch, max_q_heads, max_work_items)
+                           max_batch, max_q_heads, max_work_items, fmt)
     h = C.c_void_p()
     _check(load().kv4_cache_create(C.byref(cfg), C.byref(h)), "kv4_cache_create")
     return h
@@ -228,11 +233,11 @@ class KV4Cache:
     """Owning wrapper: creates the cache on construction, frees it on close()."""
 
     def __init__(self, num_kv_heads, num_pages, max_slots, max_batch, max_q_heads, sink=16,
-                 window=128, max_work_items=0):
+                 window=128, max_work_items=0, fmt=FORMAT_INT4_HYBRID):
         self.num_kv_heads, self.sink, self.window = num_kv_heads, sink, window
-        self.num_pages, self.max_slots = num_pages, max_slots
+        self.num_pages, self.max_slots, self.fmt = num_pages, max_slots, fmt
         self.handle = kv4_cache_create(num_kv_heads, num_pages, max_slots, max_batch, max_q_heads,
-                                       sink, window, max_work_items=max_work_items)
+                                       sink, window, max_work_items=max_work_items, fmt=fmt)
 
     def close(self):
         if self.handle is not None:

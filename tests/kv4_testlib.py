@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from int8_hybrid_paged_gb300 import inputs
-from int8_hybrid_paged_gb300.kv4 import KV4Cache
+from int8_hybrid_paged_gb300.kv4 import FORMAT_INT4_HYBRID, FORMAT_INT8, KV4Cache
 
 D = 128
 P = 16
@@ -57,6 +57,28 @@ def side_v_offset(r, d):
     return 16 * (32 * (word // 4) + n) + 4 * (word % 4) + side_v_byte(r)
 
 
+def unpack_int8_rows(blk, gbase, rr):
+    """8-bit codes and metadata of rows rr of the 16-row groups starting at byte
+    offsets gbase of blk (side groups, or pages of the 8-bit format)."""
+    d = np.arange(128)
+    koff = np.array([[side_k_offset(x, y) for y in d] for x in range(16)])
+    voff = np.array([[side_v_offset(x, y) for y in d] for x in range(16)])
+    k8 = blk[gbase[:, None] + koff[rr]]
+    v8 = blk[gbase[:, None] + 2176 + voff[rr]]
+    kmo = gbase + 2048 + 8 * (rr % 8) + 4 * (rr // 8)
+    vmo = gbase + 2176 + 2048 + 16 * (rr % 4) + 4 * np.array([side_v_byte(x) for x in rr], dtype=np.int64)
+    km = blk[kmo[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    vm = blk[vmo[:, None] + np.arange(4)[None, :]].copy().view(np.uint16)
+    return k8, v8, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
+
+
+def unpack_kv8_pages(pages, H, page_ids, slots_in_page, h):
+    """8-bit codes and metadata of positions (page_ids[i], slots_in_page[i]) of head h in
+    a KV4_FORMAT_INT8 page pool: one 4352-byte group per (page, head), row = slot."""
+    base = (np.asarray(page_ids, np.int64) * H + h) * 4352
+    return unpack_int8_rows(pages, base, np.asarray(slots_in_page, np.int64))
+
+
 def unpack_side(side, side_block, H, S, slot, h):
     """INT8 side rows 0..S-1 of (slot, head h): 16-row groups of a K block and a V block
     in tensor-core fragment order, as declared in include/kv4.h."""
@@ -80,8 +102,8 @@ class Setup:
     """A GPU cache and (for the sampled sequences) oracle caches over the same inputs."""
 
     def __init__(self, H, G, s, w, lens, seed=0, spare_pages=7, kv_device="cpu",
-                 chunks=None, max_work_items=0):
-        self.H, self.G, self.s, self.w = H, G, s, w
+                 chunks=None, max_work_items=0, kv8=False):
+        self.H, self.G, self.s, self.w, self.kv8 = H, G, s, w, kv8
         self.lens = [int(L) for L in lens]
         self.B = len(lens)
         self.seed = seed
@@ -89,7 +111,8 @@ class Setup:
         self.num_pages = need + spare_pages
         self.bt = inputs.block_tables(self.lens, P, self.num_pages, seed)
         self.cache = KV4Cache(H, self.num_pages, max_slots=self.B + 1, max_batch=self.B,
-                              max_q_heads=H * G, sink=s, window=w, max_work_items=max_work_items)
+                              max_q_heads=H * G, sink=s, window=w, max_work_items=max_work_items,
+                              fmt=FORMAT_INT8 if kv8 else FORMAT_INT4_HYBRID)
         self.kv = []
         for b, L in enumerate(self.lens):
             k, v = inputs.sequence_kv(b, L, H, seed, device=kv_device)
@@ -122,7 +145,7 @@ class Setup:
                               self.bt_dev[rows].contiguous())
 
     def oracle_for(self, b):
-        oc = oracle.OracleCache(self.H, self.s, self.w, self.lens[b], num_slots=1)
+        oc = oracle.OracleCache(self.H, self.s, self.w, self.lens[b], num_slots=1, kv8=self.kv8)
         k, v = self.kv[b]
         oc.append(0, 0, inputs.bf16_bits(k), inputs.bf16_bits(v))
         return oc

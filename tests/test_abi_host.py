@@ -41,7 +41,7 @@ def test_status_strings(lib):
 
 def _cfg(**kw):
     base = dict(num_kv_heads=8, head_dim=128, page_size=16, sink=16, window=128, num_pages=64,
-                max_slots=4, max_batch=4, max_q_heads=32, max_work_items=0)
+                max_slots=4, max_batch=4, max_q_heads=32, max_work_items=0, format=0)
     base.update(kw)
     return kv4.kv4_cache_config(*[base[f] for f, _ in kv4.kv4_cache_config._fields_])
 
@@ -55,6 +55,9 @@ def _cfg(**kw):
     (dict(num_kv_heads=0), -1),
     (dict(num_pages=0), -1),
     (dict(sink=-1), -1),
+    (dict(format=2), -1),                # unknown cache format
+    (dict(format=1), -1),                # the 8-bit format has no protected region
+    (dict(format=1, sink=0, window=4), -1),
 ])
 def test_create_rejects_bad_configs_before_the_device(lib, kw, status):
     h = C.c_void_p()

@@ -37,3 +37,14 @@ def test_regions_and_decode_bytes():
     pages = (1000 - 128 - 1) // 16 - 16 // 16 + 1
     expect = n4 * 136 + npr * 264 + 4 * pages + 8 + 128 * 6
     assert bm.decode_call_bytes([1000], 1, 1, s, w) == expect
+
+
+def test_kv8_decode_bytes():
+    """Every position at 264 B per head (8-bit codes of K and V plus two FP16 pairs):
+    a length-1000 context over 8 heads reads 2,112,000 KV bytes, 63 block-table
+    entries, and the query/output bytes of 32 q heads."""
+    got = bm.decode_call_bytes_kv8([1000], 32, 8)
+    assert got == 8 * 1000 * 264 + 4 * 63 + 8 + 32 * 128 * 6
+    assert bm.decode_call_bytes_kv8([0], 4, 1) == 8 + 4 * 128 * 6
+    # KV8 reads 264 / 136 of the INT4 bytes per token-head
+    assert bm.SIDE_POSITION_HEAD_BYTES / bm.INT4_TOKEN_HEAD_BYTES == 264 / 136
