@@ -295,7 +295,6 @@ def run_kv4(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
-    kv4.kv4_profile_start(cache.handle, args.steps * layers)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -303,12 +302,20 @@ def run_kv4(args, rank, world, local):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    prof = kv4.kv4_profile_stop(cache.handle)
     clk = clocks.stop()
     barrier(world)
     ms = e0.elapsed_time(e1)
     if cache.device_error():
         raise RuntimeError("device error during the timed region")
+
+    # per-kernel times: a separate pass with the library's events between the three
+    # launches (each kernel then runs alone, so the events time it)
+    prof_steps = min(args.steps, 500)
+    kv4.kv4_profile_start(cache.handle, prof_steps * layers)
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize()
+    prof = kv4.kv4_profile_stop(cache.handle)
 
     tokens_step = float(sum(lens)) * layers
     t_max, tok_sum = reduce_max_sum(world, ms, tokens_step * args.steps, dev)
@@ -345,7 +352,9 @@ def run_kv4(args, rank, world, local):
                      "avg_launch_ms": split_ms,
                      "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
                      "plan_ms": prof["plan_ms"] / max(1, prof["calls"]),
-                     "merge_ms": prof["merge_ms"] / max(1, prof["calls"])},
+                     "merge_ms": prof["merge_ms"] / max(1, prof["calls"]),
+                     "kernel_timing": f"separate {prof_steps}-step pass with CUDA events "
+                                      "between the three launches of each call"},
         "gpu_launches": 3 * args.steps * layers,
         "clocks": clk,
     }
@@ -372,6 +381,31 @@ def run_kv4(args, rank, world, local):
         print(json.dumps(res), flush=True)
 
 
+def time_calls(step, cache, steps, layers):
+    """Mean ms per step over `steps` timed steps (CUDA events on the stream, no
+    per-kernel events inside), then the per-kernel times from a second pass with the
+    library's events between the launches."""
+    from int8_hybrid_paged_gb300 import kv4
+
+    stream = torch.cuda.current_stream()
+    for _ in range(20):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    kv4.kv4_profile_start(cache.handle, steps * layers)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    return ms, kv4.kv4_profile_stop(cache.handle)
+
+
 def run_unprotected(wl, seed, dev, peak, protected_value, steps):
     """The same sequences, KV and queries with s = w = 0 (every position in the INT4
     pages, no side cache): context tokens/s of the whole decode call, the split
@@ -391,21 +425,9 @@ def run_unprotected(wl, seed, dev, peak, protected_value, steps):
             for _ in range(wl0.layers):
                 kv4.kv4_decode_attention(cache.handle, st["q"], st["slots"], st["cl"],
                                          st["bt_dev"], out, lse, stream=stream)
-        for _ in range(20):
-            step()
-        torch.cuda.synchronize()
-        kv4.kv4_profile_start(cache.handle, steps * wl0.layers)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        prof = kv4.kv4_profile_stop(cache.handle)
+        ms, prof = time_calls(step, cache, steps, wl0.layers)
         if cache.device_error():
             raise RuntimeError("device error in the unprotected decode")
-        ms = e0.elapsed_time(e1) / steps
         value = float(sum(st["lens"])) * wl0.layers / (ms * 1e-3)
         call_bytes = bytes_model.decode_call_bytes(st["lens"], Hq, wl0.num_kv_heads, 0, 0,
                                                    with_lse=True)
@@ -441,21 +463,9 @@ def run_kv8(wl, seed, dev, peak, kv4_value, steps):
             for _ in range(wl8.layers):
                 kv4.kv4_decode_attention(cache.handle, st["q"], st["slots"], st["cl"],
                                          st["bt_dev"], out, lse, stream=stream)
-        for _ in range(20):
-            step()
-        torch.cuda.synchronize()
-        kv4.kv4_profile_start(cache.handle, steps * wl8.layers)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        prof = kv4.kv4_profile_stop(cache.handle)
+        ms, prof = time_calls(step, cache, steps, wl8.layers)
         if cache.device_error():
             raise RuntimeError("device error in the 8-bit decode")
-        ms = e0.elapsed_time(e1) / steps
         value = float(sum(st["lens"])) * wl8.layers / (ms * 1e-3)
         call_bytes = bytes_model.decode_call_bytes_kv8(st["lens"], Hq, wl8.num_kv_heads,
                                                        with_lse=True)

@@ -174,6 +174,8 @@ constexpr int kPrepThreads = 256;
 
 __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArgs a)
 {
+    // the split kernel may be scheduled now; it waits for this grid's writes itself
+    grid_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (blockIdx.x == 0) {
         // ---- plan: cost line, spans, piece counts
@@ -799,6 +801,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
         fence_mbar_init();
     }
     __syncthreads();
+    // launched as a programmatic dependent of the prep kernel: everything above ran
+    // alongside its tail; the plan and query records are read only past this wait
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
     const int cp = prot_items(S);
@@ -1173,6 +1179,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 template <int G>
 __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 {
+    grid_dependency_wait();                 // the split kernel's partials are complete past here
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (gw >= a.batch * a.num_q_heads) return;
@@ -1271,19 +1278,43 @@ __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 }
 
 // ---------------------------------------------------------------- launchers
+// Launch k(a) on the stream; dependent = programmatic dependent launch (the kernel
+// may start while the previous one drains and waits for its writes on the device).
+static cudaError_t launch_k(void (*k)(DecodeArgs), int grid, int block, size_t smem,
+                            cudaStream_t stream, const DecodeArgs& a, bool dependent)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
 template <int G, bool DEBUG, bool KV8>
 static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
+    // with profiling events between the kernels each one runs alone, so the events
+    // time it; otherwise split and merge are programmatic dependents of their predecessor
+    const bool dep = ev == nullptr;
     if (ev) cudaEventRecord(ev[0], stream);
     const int prep_blocks = 1 + (a.batch * a.num_q_heads + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
-    kv4_decode_prep_kernel<<<prep_blocks, kPrepThreads, 0, stream>>>(a);
+    cudaError_t e = launch_k(kv4_decode_prep_kernel, prep_blocks, kPrepThreads, 0, stream, a, false);
     if (ev) cudaEventRecord(ev[1], stream);
-    kv4_decode_split_kernel<G, DEBUG, KV8><<<grid, kDecodeThreads, sizeof(SplitSmem), stream>>>(a);
+    if (e == cudaSuccess)
+        e = launch_k(kv4_decode_split_kernel<G, DEBUG, KV8>, grid, kDecodeThreads, sizeof(SplitSmem),
+                     stream, a, dep);
     if (ev) cudaEventRecord(ev[2], stream);
     const int warps = a.batch * a.num_q_heads;
-    kv4_decode_merge_kernel<G><<<(warps + 3) / 4, 128, 0, stream>>>(a);
+    if (e == cudaSuccess)
+        e = launch_k(kv4_decode_merge_kernel<G>, (warps + 3) / 4, 128, 0, stream, a, dep);
     if (ev) cudaEventRecord(ev[3], stream);
-    return cudaGetLastError();
+    return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
