@@ -118,6 +118,16 @@ def queries(batch: int, num_q_heads: int, seed: int, device="cpu"):
     return q.to(torch.bfloat16)
 
 
+def rope_table(max_pos: int, base: float = 1_000_000.0) -> np.ndarray:
+    """The model's RoPE constants as a float32 table [max_pos][128]: for position p and
+    pair i < 64 (dims i and i + 64), cos(p·base^(−i/64)) at [p][i] and its sin at
+    [p][64 + i], evaluated in float64 and rounded once. base = 1e6 is Qwen3's."""
+    p = np.arange(max_pos, dtype=np.float64)[:, None]
+    inv_freq = base ** (-np.arange(HEAD_DIM // 2, dtype=np.float64) / (HEAD_DIM // 2))
+    ang = p * inv_freq[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
 def block_tables(context_lens, page_size: int, num_pages: int, seed: int,
                  stride: int | None = None) -> np.ndarray:
     """int32 [B][stride] block tables: a seeded random choice of distinct physical

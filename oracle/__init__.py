@@ -21,4 +21,5 @@ from .kv4_oracle import (  # noqa: F401
     num_threads,
     quant_affine,
     quant_query,
+    rope128,
 )

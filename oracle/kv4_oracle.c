@@ -57,6 +57,12 @@
  *      quantizer with n = 255), and decode applies the protected path of R6 and R7
  *      to every position, in groups of 16 consecutive positions (one page) in
  *      position order.
+ *   R11 RoPE, when the caller supplies its table: keys are rotated by RoPE at their
+ *      position and then by the Hadamard transform, queries the same at position
+ *      L − 1 ([zh] 核心方法: the Hadamard rotation follows RoPE; 方法步骤详情 step 2:
+ *      the query takes the same rotations). Pairing (i, i + 64) ("rotate half"), with
+ *      a = x_i, b = x_{i+64}: x'_i = fmaf(a, cos, −fl(b·sin)),
+ *      x'_{i+64} = fmaf(b, cos, fl(a·sin)); cos and sin are the caller's FP32 table.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -228,6 +234,18 @@ void orc_fwht128(const float *in, float *out)
     for (int i = 0; i < ORC_D; i++) out[i] = x[i] * scale;
 }
 
+/* RoPE of one 128-dim vector with one row of the caller's table (reading R11): dims i
+   and i + 64 rotate together by the angle whose cos and sin are row[i] and row[64 + i]. */
+void orc_rope128(const float *in, const float *cs, float *out)
+{
+    for (int i = 0; i < ORC_D / 2; i++) {
+        const float a = in[i], b = in[i + ORC_D / 2];
+        const float c = cs[i], s = cs[ORC_D / 2 + i];
+        out[i] = fmaf(a, c, -(b * s));
+        out[i + ORC_D / 2] = fmaf(b, c, a * s);
+    }
+}
+
 /* Group-affine quantizer x^ = Δc + m over one group of n values, levels = 2^b − 1.
    [zh] 分组仿射 KV 量化; 方法步骤详情 step 2 (FP16 Δ and m computed online).
    Rounding directions: reading R2 in the file header. */
@@ -338,12 +356,17 @@ int orc_append(orc_cache *c, int slot, int start, int T,
     if (slot < 0 || slot >= c->num_slots || start < 0 || T < 0 || start + T > c->max_len)
         return -1;
     if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
-    float kx[ORC_D], kr[ORC_D], vx[ORC_D];
+    if (c->rope && start + T > c->rope_max_pos) return -1;
+    float kx[ORC_D], kp[ORC_D], kr[ORC_D], vx[ORC_D];
     for (int t = 0; t < T; t++) {
         for (int h = 0; h < c->num_heads; h++) {
             size_t off = ((size_t)t * c->num_heads + h) * ORC_D;
             load_bf16_row(k_bf16 + off, kx);
             load_bf16_row(v_bf16 + off, vx);
+            if (c->rope) {                          /* R11: RoPE, then the Hadamard rotation */
+                orc_rope128(kx, c->rope + (size_t)(start + t) * ORC_D, kp);
+                memcpy(kx, kp, sizeof kx);
+            }
             orc_fwht128(kx, kr);
             append_one(c, slot, start + t, h, kr, vx);
         }
@@ -562,6 +585,15 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
     *lse = (Ms + log2(den)) * 0.69314718055994530942;
 }
 
+/* R11: the query of a decode step sits at position L − 1 */
+static void query_rope(const orc_cache *c, int L, float *qx)
+{
+    if (!c->rope || L <= 0) return;
+    float qp[ORC_D];
+    orc_rope128(qx, c->rope + (size_t)(L - 1) * ORC_D, qp);
+    memcpy(qx, qp, sizeof qp);
+}
+
 int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf16,
                float sm_scale, int pv_mode, double *out, double *lse, orc_debug *dbg)
 {
@@ -569,6 +601,7 @@ int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf1
         return -1;
     if (c->sink + c->window > 256) return -1;
     if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
+    if (c->rope && L > c->rope_max_pos) return -1;
     const float C = log2e_scale(sm_scale);
     const int HG = c->num_heads * G;
     for (int hq = 0; hq < HG; hq++) {
@@ -577,6 +610,7 @@ int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf1
         float q_scale;
         int32_t q_sum;
         load_bf16_row(q_bf16 + (size_t)hq * ORC_D, qx);
+        query_rope(c, L, qx);
         orc_fwht128(qx, qr);
         orc_quant_query(qr, q8, &q_scale, &q_sum);
         if (dbg) {
@@ -602,6 +636,7 @@ static int decode_one_head(const orc_cache *c, int slot, int L, int G, int hq,
     float q_scale;
     int32_t q_sum;
     load_bf16_row(q_row, qx);
+    query_rope(c, L, qx);
     orc_fwht128(qx, qr);
     orc_quant_query(qr, q8, &q_scale, &q_sum);
     decode_head(c, slot, L, hq / G, q8, q_scale, q_sum, C, pv_mode, out, lse, NULL, NULL, NULL);
@@ -616,7 +651,8 @@ int orc_decode_batch(const orc_cache *c, int B, const int32_t *slots, const int3
     const int HG = c->num_heads * G;
     const float C = log2e_scale(sm_scale);
     for (int b = 0; b < B; b++)
-        if (slots[b] < 0 || slots[b] >= c->num_slots || lens[b] < 0 || lens[b] > c->max_len)
+        if (slots[b] < 0 || slots[b] >= c->num_slots || lens[b] < 0 || lens[b] > c->max_len ||
+            (c->rope && lens[b] > c->rope_max_pos))
             return -1;
     if (G <= 0 || c->sink + c->window > 256) return -1;
     if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;

@@ -46,6 +46,11 @@ typedef struct {
     uint8_t  *k8_code, *v8_code;
     uint16_t *k8_delta, *k8_min, *v8_delta, *v8_min;
     int32_t  *length;    /* [slot] positions appended so far */
+    /* RoPE (reading R11), or NULL: keys given to orc_append and queries given to decode
+       are then pre-RoPE. Table [rope_max_pos][128]: cos of the angle of pair i at [p][i],
+       its sin at [p][64 + i] (i < 64). */
+    const float *rope;
+    int32_t  rope_max_pos;
 } orc_cache;
 
 /* Optional per-call debug record of orc_decode (any pointer may be NULL).
@@ -68,6 +73,7 @@ float    orc_exp2f(float x);
 
 /* steps */
 void orc_fwht128(const float *in, float *out);
+void orc_rope128(const float *in, const float *cos_sin_row, float *out);
 void orc_quant_affine(const float *x, int n, int levels,
                       uint8_t *code, uint16_t *delta_h, uint16_t *min_h);
 void orc_quant_query(const float *q_rot, int8_t *q8, float *q_scale, int32_t *q_sum);

@@ -31,6 +31,7 @@ def load():
         lib.orc_exp2f.argtypes = [C.c_float]
         lib.orc_exp2f.restype = C.c_float
         lib.orc_fwht128.argtypes = [P, P]
+        lib.orc_rope128.argtypes = [P, P, P]
         lib.orc_quant_affine.argtypes = [P, C.c_int, C.c_int, P, P, P]
         lib.orc_quant_query.argtypes = [P, P, P, P]
         lib.orc_append.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
@@ -102,6 +103,16 @@ def fwht128(x):
     return out
 
 
+def rope128(x, cos_sin_row):
+    """RoPE of one 128-dim vector with one table row (cos at [i], sin at [64+i])."""
+    x = _c(x, np.float32)
+    row = _c(cos_sin_row, np.float32)
+    assert x.shape == (D,) and row.shape == (D,)
+    out = np.empty(D, np.float32)
+    load().orc_rope128(_p(x), _p(row), _p(out))
+    return out
+
+
 def quant_affine(x, levels):
     """Returns (codes uint8[n], delta fp16 bits, min fp16 bits)."""
     x = _c(x, np.float32)
@@ -135,7 +146,8 @@ _STATE_ARRAYS = ("k4_code", "v4_code", "k4_delta", "k4_min", "v4_delta", "v4_min
 class _State(C.Structure):
     _fields_ = [("num_heads", C.c_int32), ("sink", C.c_int32), ("window", C.c_int32),
                 ("max_len", C.c_int32), ("num_slots", C.c_int32), ("kv8", C.c_int32)] + \
-               [(n, C.c_void_p) for n in _STATE_ARRAYS]
+               [(n, C.c_void_p) for n in _STATE_ARRAYS] + \
+               [("rope", C.c_void_p), ("rope_max_pos", C.c_int32)]
 
 
 class _Debug(C.Structure):
@@ -148,7 +160,7 @@ class OracleCache:
     kv8=True, the whole-cache 8-bit configuration (reading R10): 8-bit codes for
     every position, no side buffer (sink = window = 0)."""
 
-    def __init__(self, num_heads, sink, window, max_len, num_slots=1, kv8=False):
+    def __init__(self, num_heads, sink, window, max_len, num_slots=1, kv8=False, rope=None):
         if kv8 and (sink or window):
             raise ValueError("the KV8 configuration has no protected region")
         H, S = num_heads, sink + window
@@ -171,6 +183,13 @@ class OracleCache:
         st = _State(H, sink, window, max_len, num_slots, int(self.kv8))
         for n in _STATE_ARRAYS:
             setattr(st, n, getattr(self, n).ctypes.data)
+        # reading R11: with a RoPE table [max_pos][128] (cos at [p][i], sin at [p][64+i]),
+        # appended keys and decode queries are pre-RoPE
+        self.rope = None if rope is None else _c(rope, np.float32)
+        if self.rope is not None:
+            assert self.rope.ndim == 2 and self.rope.shape[1] == D
+            st.rope = self.rope.ctypes.data
+            st.rope_max_pos = self.rope.shape[0]
         self._st = st
 
     def append(self, slot, start, k_bits, v_bits):
