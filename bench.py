@@ -485,12 +485,15 @@ def run_kv8(wl, seed, dev, peak, kv4_value, steps):
 def run_append_stress(dev, peak):
     """kv4_append on the append-stress shapes: (a) one new token for 512 sequences at
     position 2000, (b) a 16384-token re-prefill chunk for 8 sequences from position 0;
-    8 KV heads, seeded bf16 K/V with outlier channels. CUDA-event time per call, after
-    warm-up; GB/s counts bf16 K/V read, INT4 pages and INT8 side rows written."""
+    8 KV heads, seeded bf16 K/V with outlier channels; each also with pre-RoPE keys and
+    RoPE fused into the append (the table's reads are not counted). CUDA-event time per
+    call, after warm-up; GB/s counts bf16 K/V read, INT4 pages and INT8 side rows written."""
     from int8_hybrid_paged_gb300.kv4 import KV4Cache
     H, s, w = 8, 16, 128
     out = {}
-    for tag, B, T, start_pos, reps in (("b", 8, 16384, 0, 20), ("a", 512, 1, 2000, 200)):
+    cases = (("b", 8, 16384, 0, 20, False), ("a", 512, 1, 2000, 200, False),
+             ("b_rope", 8, 16384, 0, 20, True), ("a_rope", 512, 1, 2000, 200, True))
+    for tag, B, T, start_pos, reps, rope in cases:
         stride = (start_pos + T + 15) // 16 + 1
         num_pages = B * stride + 8
         bt = torch.from_numpy(inputs.block_tables([stride * 16] * B, 16, num_pages, 1)).to(dev)
@@ -499,6 +502,8 @@ def run_append_stress(dev, peak):
         slots = torch.arange(B, dtype=torch.int32, device=dev)
         start = torch.full((B,), start_pos, dtype=torch.int32, device=dev)
         cache = KV4Cache(H, num_pages, max_slots=B, max_batch=B, max_q_heads=4 * H, sink=s, window=w)
+        if rope:                             # pre-RoPE keys: RoPE fused ahead of the Hadamard
+            cache.set_rope(torch.from_numpy(inputs.rope_table(start_pos + T)).to(dev))
         try:
             for _ in range(3):
                 cache.append(k, v, cu, slots, start, bt)
@@ -516,7 +521,8 @@ def run_append_stress(dev, peak):
             side = B * (min(T, s + w) if start_pos == 0 else 1 + (1 if start_pos < s else 0))
             nbytes = bytes_model.append_call_bytes(B * T, H, side * H)
             gbs = nbytes / (ms * 1e-3) / 1e9
-            out[tag] = {"case": f"{B} sequences x {T} token(s) from position {start_pos}, {H} KV heads",
+            out[tag] = {"case": f"{B} sequences x {T} token(s) from position {start_pos}, {H} KV heads"
+                                + (", RoPE fused" if rope else ""),
                         "us_per_call": ms * 1e3, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
                         "frac_of_hbm_peak": gbs / peak}
         finally:

@@ -140,6 +140,25 @@ kv4_status kv4_cache_free(kv4_cache *cache);
 kv4_status kv4_cache_get_info(const kv4_cache *cache, kv4_cache_info *info);
 
 /*
+ * kv4_cache_set_rope — fuse RoPE into the cache's appends and decodes.
+ * [zh] 核心方法 (keys take the Hadamard rotation after RoPE), 方法步骤详情 step 2
+ * (the query takes the same rotations before attention).
+ * With a table set, kv4_append takes PRE-RoPE keys and rotates each key by RoPE at
+ * its position before the Hadamard transform, and kv4_decode_attention(_debug)
+ * takes PRE-RoPE queries and rotates the query of sequence b at position L_b - 1.
+ * Pairs are (i, i + 64) ("rotate half"): with a = x_i, b = x_{i+64},
+ * x_i' = fmaf(a, cos, -(b*sin)) and x_{i+64}' = fmaf(b, cos, a*sin) in FP32.
+ *   cos_sin_dev : [max_pos][128] fp32 device table, 16-byte aligned, owned by the caller
+ *                 and valid while set: cos of pair i at position p at [p][i], its sin
+ *                 at [p][64 + i]; NULL clears the setting (inputs are post-RoPE again)
+ *   max_pos     : rows of the table (>= 1 when cos_sin_dev is set)
+ * A position at or beyond max_pos is a device-side error (KV4_DEVERR_BAD_POSITION):
+ * an append skips the sequence, a decode uses the unrotated query. Errors:
+ * KV4_ERR_INVALID_ARG. kv4_decode_attention_noalloc never applies RoPE.
+ */
+kv4_status kv4_cache_set_rope(kv4_cache *cache, const float *cos_sin_dev, int max_pos);
+
+/*
  * kv4_append — quantize and store new tokens of n_seqs sequences.
  * [zh] 方法步骤详情 steps 2-3, 前置知识 › 分组仿射 KV 量化; [ko] 전제와 한계.
  * For each token-head: rotate K (post-RoPE, supplied by the caller) with the

@@ -26,6 +26,8 @@ struct kv4_cache {
     unsigned char* ws = nullptr;           // decode workspace (layout: decode_workspace_bytes)
     size_t ws_bytes = 0;
     int32_t max_group = 0;
+    const float* rope = nullptr;           // RoPE table (kv4_cache_set_rope), or null
+    int32_t rope_max_pos = 0;
     // profiling: 4 events per recorded decode call
     std::vector<cudaEvent_t> events;
     int prof_capacity = 0;
@@ -172,6 +174,20 @@ kv4_status kv4_cache_get_info(const kv4_cache* c, kv4_cache_info* info)
     return KV4_OK;
 }
 
+kv4_status kv4_cache_set_rope(kv4_cache* c, const float* cos_sin, int max_pos)
+{
+    if (!c) return KV4_ERR_INVALID_ARG;
+    if (!cos_sin) {
+        c->rope = nullptr;
+        c->rope_max_pos = 0;
+        return KV4_OK;
+    }
+    if (max_pos < 1 || (reinterpret_cast<uintptr_t>(cos_sin) & 15)) return KV4_ERR_INVALID_ARG;
+    c->rope = cos_sin;
+    c->rope_max_pos = max_pos;
+    return KV4_OK;
+}
+
 kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t* cu_tokens,
                       const int32_t* slot_ids, const int32_t* start_pos, const int32_t* block_table,
                       int stride, int n_seqs, int total_tokens, void* stream)
@@ -203,6 +219,8 @@ kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t*
     a.seq_len = c->seq_len;
     a.err = c->err;
     a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
+    a.rope = c->rope;
+    a.rope_max_pos = c->rope_max_pos;
     return check_launch(kv4::launch_append(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -261,6 +279,8 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.dbg_w = dw;
     a.dbg_stride = dbg_stride;
     a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
+    a.rope = c->rope;
+    a.rope_max_pos = c->rope_max_pos;
     cudaEvent_t* ev = nullptr;
     if (c->profiling && c->prof_calls < c->prof_capacity) ev = &c->events[4 * c->prof_calls++];
     return check_launch(kv4::launch_decode(a, c->grid[G], static_cast<cudaStream_t>(stream), ev));

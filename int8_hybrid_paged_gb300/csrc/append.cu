@@ -122,6 +122,7 @@ __device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)
 // One warp per (token, group of hpw KV heads): the sequence lookup, validation and
 // page lookup happen once per warp, then the warp quantizes its heads one by one (for
 // a token pair t, t + 8 both tokens' loads and arithmetic are in flight together).
+template <bool ROPE>
 __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
 {
     const int lane = threadIdx.x & 31;
@@ -156,6 +157,10 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
         if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_POSITION);
         return;
     }
+    if (ROPE && new_len > a.rope_max_pos) {           // positions beyond the RoPE table
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_POSITION);
+        return;
+    }
     const int page = __ldg(&a.block_table[(int64_t)i * a.stride + pos / kPage]);
     if (page < 0 || (int64_t)page >= a.num_pages) {
         if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_PAGE);
@@ -172,6 +177,7 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
             float kx[4], vx[4];
             load_bf16x4(krow + h * kHeadDim, kx);
             load_bf16x4(vrow + h * kHeadDim, vx);
+            if (ROPE) warp_rope128(kx, a.rope + (int64_t)pos * kHeadDim, lane);
             warp_fwht128(kx, lane);
             uint32_t k8[4], v8[4];
             __half k8d, k8m, v8d, v8m;
@@ -215,6 +221,10 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
             load_bf16x4(vrow + h * kHeadDim, vxA);
             load_bf16x4(krow + rowB + h * kHeadDim, kxB);
             load_bf16x4(vrow + rowB + h * kHeadDim, vxB);
+            if (ROPE) {
+                warp_rope128(kxA, a.rope + (int64_t)posA * kHeadDim, lane);
+                warp_rope128(kxB, a.rope + (int64_t)posB * kHeadDim, lane);
+            }
             const uint32_t knA = append_head(a, kxA, vxA, blk, tsA, sb, sinkA, ringA, posA, lane);
             const uint32_t knB = append_head(a, kxB, vxB, blk, tsA + 8, sb, sinkB, ringB, posB, lane);
             *reinterpret_cast<uint32_t*>(blk + kw) = knA | (knB << 4);
@@ -227,6 +237,7 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
             float kx[4], vx[4];
             load_bf16x4(krow + h * kHeadDim, kx);
             load_bf16x4(vrow + h * kHeadDim, vx);
+            if (ROPE) warp_rope128(kx, a.rope + (int64_t)posA * kHeadDim, lane);
             const uint32_t kn = append_head(a, kx, vx, blk, tsA, sb0 + h * a.side_block_bytes,
                                             sinkA, ringA, posA, lane);
             *kp = lower ? ((old & 0xf0f0f0f0u) | kn) : ((old & 0x0f0f0f0fu) | (kn << 4));
@@ -243,7 +254,8 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream)
     const int hpw = (int64_t)a.total_tokens >= 16384 ? a.num_heads : 1;
     const int64_t warps = (int64_t)a.total_tokens * ((a.num_heads + hpw - 1) / hpw);
     const int64_t blocks = (warps + 7) / 8;
-    kv4_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a, hpw);
+    if (a.rope) kv4_append_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(a, hpw);
+    else kv4_append_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(a, hpw);
     return cudaGetLastError();
 }
 

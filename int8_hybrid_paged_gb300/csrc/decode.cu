@@ -234,6 +234,15 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
     if (gw >= a.batch * a.num_q_heads) return;
     float x[4];
     load_bf16x4(a.q + (int64_t)gw * kHeadDim + 4 * lane, x);
+    if (a.rope) {
+        // the query of this step sits at position L - 1 of its sequence
+        const int L = __ldg(&a.context_lens[gw / a.num_q_heads]);
+        if (L > a.rope_max_pos) {
+            if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_POSITION);
+        } else if (L > 0) {
+            warp_rope128(x, a.rope + (int64_t)(L - 1) * kHeadDim, lane);
+        }
+    }
     warp_fwht128(x, lane);
     const float amax =
         warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));

@@ -241,6 +241,25 @@ __device__ __forceinline__ void fence_mbar_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// RoPE of one 128-dim vector held 4 dims per lane (lane l: dims 4l .. 4l+3) with one
+// row of the caller's table (cos of pair i at row[i], sin at row[64 + i]): dims i and
+// i + 64 (lanes l and l ^ 16) rotate together, x_i' = fma(x_i, cos, -(x_{i+64} sin)),
+// x_{i+64}' = fma(x_{i+64}, cos, x_i sin), each product and fma rounded once.
+__device__ __forceinline__ void warp_rope128(float (&x)[4], const float* __restrict__ row, int lane)
+{
+    const int i0 = 4 * (lane & 15);
+    const float4 c = __ldg(reinterpret_cast<const float4*>(row + i0));
+    const float4 s = __ldg(reinterpret_cast<const float4*>(row + 64 + i0));
+    const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+    const bool lo = lane < 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float y = __shfl_xor_sync(0xffffffffu, x[j], 16);       // the paired dim
+        x[j] = lo ? __fmaf_rn(x[j], cc[j], -__fmul_rn(y, ss[j]))
+                  : __fmaf_rn(x[j], cc[j], __fmul_rn(y, ss[j]));
+    }
+}
+
 // Programmatic dependent launch: wait until the grid this one depends on has completed
 // and its memory is visible (returns at once for an ordinary launch), and allow the
 // next grid on the stream to be scheduled.

@@ -76,6 +76,8 @@ struct AppendArgs {
     int32_t* seq_len;
     int32_t* err;
     int32_t kv8;                  // KV4_FORMAT_INT8: 8-bit codes in pages of kPageBlock8 bytes
+    const float* rope;            // [rope_max_pos][128] cos | sin, or null (keys are post-RoPE)
+    int32_t rope_max_pos;
 };
 
 struct DecodeArgs {
@@ -115,6 +117,8 @@ struct DecodeArgs {
     uint8_t* dbg_w;
     int32_t dbg_stride;
     int32_t kv8;                  // KV4_FORMAT_INT8: every position a protected row of its page
+    const float* rope;            // [rope_max_pos][128] cos | sin, or null (queries are post-RoPE)
+    int32_t rope_max_pos;
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);

@@ -28,7 +28,7 @@ PAGE_SIZE = 16
 EXPORTED = ("kv4_cache_create", "kv4_cache_free", "kv4_cache_get_info", "kv4_append",
             "kv4_decode_attention", "kv4_decode_attention_debug", "kv4_get_device_error",
             "kv4_status_string", "kv4_profile_start", "kv4_profile_stop",
-            "kv4_decode_attention_noalloc")
+            "kv4_decode_attention_noalloc", "kv4_cache_set_rope")
 
 
 class KV4Error(RuntimeError):
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
     lib.kv4_decode_attention_noalloc.argtypes = [C.POINTER(kv4_cache_config), P, P, P, P, I, P,
                                                  P, P, I, I, F, P, P, P]
     lib.kv4_profile_stop.argtypes = [P, C.POINTER(kv4_profile)]
+    lib.kv4_cache_set_rope.argtypes = [P, P, I]
     for name in EXPORTED:
         getattr(lib, name).restype = C.c_int if name != "kv4_status_string" else C.c_char_p
     _lib = lib
@@ -138,6 +139,18 @@ def kv4_cache_create(num_kv_heads, num_pages, max_slots, max_batch, max_q_heads,
     h = C.c_void_p()
     _check(load().kv4_cache_create(C.byref(cfg), C.byref(h)), "kv4_cache_create")
     return h
+
+
+def kv4_cache_set_rope(handle, cos_sin=None):
+    """RoPE table for the cache's appends and decodes: a float32 CUDA tensor
+    [max_pos][128] (cos of pair i at [p][i], sin at [p][64+i]), or None to clear.
+    The tensor must outlive the setting."""
+    if cos_sin is None:
+        _check(load().kv4_cache_set_rope(handle, None, 0), "kv4_cache_set_rope")
+        return
+    assert cos_sin.dim() == 2 and cos_sin.shape[1] == HEAD_DIM
+    _check(load().kv4_cache_set_rope(handle, _ptr(cos_sin, torch.float32, "cos_sin"),
+                                     int(cos_sin.shape[0])), "kv4_cache_set_rope")
 
 
 def kv4_cache_free(handle):
@@ -258,6 +271,11 @@ class KV4Cache:
 
     def info(self):
         return kv4_cache_get_info(self.handle)
+
+    def set_rope(self, cos_sin=None):
+        """Fuse RoPE into appends and decodes (pre-RoPE K and q from now on); None clears."""
+        self._rope = cos_sin                 # keep the table alive while it is set
+        kv4_cache_set_rope(self.handle, cos_sin)
 
     def append(self, k, v, cu_tokens, slot_ids, start_pos, block_table, stream=None):
         kv4_append(self.handle, k, v, cu_tokens, slot_ids, start_pos, block_table, stream)

@@ -102,8 +102,9 @@ class Setup:
     """A GPU cache and (for the sampled sequences) oracle caches over the same inputs."""
 
     def __init__(self, H, G, s, w, lens, seed=0, spare_pages=7, kv_device="cpu",
-                 chunks=None, max_work_items=0, kv8=False):
+                 chunks=None, max_work_items=0, kv8=False, rope=None):
         self.H, self.G, self.s, self.w, self.kv8 = H, G, s, w, kv8
+        self.rope = rope                     # float32 numpy table [max_pos][128] or None
         self.lens = [int(L) for L in lens]
         self.B = len(lens)
         self.seed = seed
@@ -118,6 +119,8 @@ class Setup:
             k, v = inputs.sequence_kv(b, L, H, seed, device=kv_device)
             self.kv.append((k, v))
         self.bt_dev = torch.from_numpy(self.bt).cuda()
+        if rope is not None:
+            self.cache.set_rope(torch.from_numpy(rope).cuda())
         self._append(chunks)
 
     def _append(self, chunks):
@@ -145,7 +148,8 @@ class Setup:
                               self.bt_dev[rows].contiguous())
 
     def oracle_for(self, b):
-        oc = oracle.OracleCache(self.H, self.s, self.w, self.lens[b], num_slots=1, kv8=self.kv8)
+        oc = oracle.OracleCache(self.H, self.s, self.w, self.lens[b], num_slots=1, kv8=self.kv8,
+                                rope=self.rope)
         k, v = self.kv[b]
         oc.append(0, 0, inputs.bf16_bits(k), inputs.bf16_bits(v))
         return oc
