@@ -486,8 +486,9 @@ def run_append_stress(dev, peak):
     """kv4_append on the append-stress shapes: (a) one new token for 512 sequences at
     position 2000, (b) a 16384-token re-prefill chunk for 8 sequences from position 0;
     8 KV heads, seeded bf16 K/V with outlier channels; each also with pre-RoPE keys and
-    RoPE fused into the append (the table's reads are not counted). CUDA-event time per
-    call, after warm-up; GB/s counts bf16 K/V read, INT4 pages and INT8 side rows written."""
+    RoPE fused into the append (the table's reads are not counted). Device time per call:
+    CUDA events around one replay of a CUDA graph of the repeated calls, after warm-up;
+    GB/s counts bf16 K/V read, INT4 pages and INT8 side rows written."""
     from int8_hybrid_paged_gb300.kv4 import KV4Cache
     H, s, w = 8, 16, 128
     out = {}
@@ -508,13 +509,21 @@ def run_append_stress(dev, peak):
             for _ in range(3):
                 cache.append(k, v, cu, slots, start, bt)
             torch.cuda.synchronize()
+            # the calls are captured in a CUDA graph so the device time is measured, not
+            # the host's launch rate (a one-token append is shorter than a Python call)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for _ in range(reps):
+                    cache.append(k, v, cu, slots, start, bt)
+            graph.replay()
+            torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record()
-            for _ in range(reps):
-                cache.append(k, v, cu, slots, start, bt)
+            graph.replay()
             e1.record()
             torch.cuda.synchronize()
+            del graph
             if cache.device_error():
                 raise RuntimeError("device error during the append stress")
             ms = e0.elapsed_time(e1) / reps

@@ -132,21 +132,38 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
     if (tok >= a.total_tokens) return;      // whole warp leaves together
     const int h_lo = (gw - tok * groups) * hpw, h_hi = min(a.num_heads, h_lo + hpw);
 
-    // sequence i of this token: the largest i with cu[i] <= tok (cu[n] = total > tok)
-    int lo = 0, hi = a.n_seqs;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(&a.cu_tokens[mid]) <= tok) lo = mid; else hi = mid;
+    // this token's K/V rows do not depend on the lookup below: start them towards L2
+    if (lane < 2 * (h_hi - h_lo)) {
+        const uint16_t* src = (lane & 1 ? a.v : a.k) + ((int64_t)tok * a.num_heads + h_lo + (lane >> 1)) * kHeadDim;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src + 64));
     }
-    const int i = lo;
-    const int c0 = __ldg(&a.cu_tokens[i]);
-    const int c1 = __ldg(&a.cu_tokens[i + 1]);
+
+    // sequence i of this token: the largest i with cu[i] <= tok (cu[n] = total > tok).
+    // First guess in proportion (exact when the sequences append equal counts, e.g.
+    // one token each; its slot and start are loaded alongside), then a binary search
+    // if the guess misses.
+    int i = (int)(((int64_t)tok * a.n_seqs) / a.total_tokens);
+    int c0 = __ldg(&a.cu_tokens[i]);
+    int c1 = __ldg(&a.cu_tokens[i + 1]);
+    int slot = __ldg(&a.slot_ids[i]);
+    int start = __ldg(&a.start_pos[i]);
+    if (!(c0 <= tok && tok < c1)) {
+        int lo = 0, hi = a.n_seqs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(&a.cu_tokens[mid]) <= tok) lo = mid; else hi = mid;
+        }
+        i = lo;
+        c0 = __ldg(&a.cu_tokens[i]);
+        c1 = __ldg(&a.cu_tokens[i + 1]);
+        slot = __ldg(&a.slot_ids[i]);
+        start = __ldg(&a.start_pos[i]);
+    }
     if (tok < c0 || tok >= c1) {
         if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_TOKENS);
         return;
     }
-    const int slot = __ldg(&a.slot_ids[i]);
-    const int start = __ldg(&a.start_pos[i]);
     const int pos = start + (tok - c0);
     const int new_len = start + (c1 - c0);
     if (slot < 0 || slot >= a.max_slots) {
