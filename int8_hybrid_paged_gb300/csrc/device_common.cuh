@@ -87,11 +87,13 @@ __device__ __forceinline__ void warp_fwht128(float (&x)[4], int lane)
     x[3] = __fsub_rn(a1, a3);
 #pragma unroll
     for (int m = 1; m < 32; m <<= 1) {
-        const bool upper = (lane & m) != 0;
+        // lower lane: x + y; upper lane: y - x (its partner's value minus its own),
+        // one fma with an exact ±1 product, so each rounds once as an add/sub would
+        const float sg = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            float y = __shfl_xor_sync(kFull, x[i], m);
-            x[i] = upper ? __fsub_rn(y, x[i]) : __fadd_rn(x[i], y);
+            const float y = __shfl_xor_sync(kFull, x[i], m);
+            x[i] = __fmaf_rn(x[i], sg, y);
         }
     }
     const float inv_sqrt128 = 0x1.6a09e6p-4f;   // nearest float to 1/√128
@@ -123,12 +125,25 @@ __device__ __forceinline__ __half half_div_up(float r, float n, float inv_n)
     return __ushort_as_half(cb);
 }
 
+// Order-preserving map of a float to uint32 (and back), for the warp's integer
+// min/max reductions: the bits with the sign flipped for x >= 0, all bits flipped
+// for x < 0 (so -0 sorts just below +0; either is a zero minimum).
+__device__ __forceinline__ uint32_t f2key(float f)
+{
+    const uint32_t b = __float_as_uint(f);
+    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k)
+{
+    return __uint_as_float(k ^ (((k >> 31) - 1u) | 0x80000000u));
+}
+
 template <int LEVELS>
 __device__ __forceinline__ void warp_quant(const float (&x)[4], uint32_t (&c)[4],
                                            __half& delta_h, __half& min_h)
 {
-    float lo = warp_min(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
-    float hi = warp_max(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
+    float lo = key2f(__reduce_min_sync(kFull, f2key(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])))));
+    const float hi = key2f(__reduce_max_sync(kFull, f2key(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])))));
     lo = __fadd_rn(lo, 0.0f);
     min_h = __float2half_rd(lo);
     const float m = __half2float(min_h);
