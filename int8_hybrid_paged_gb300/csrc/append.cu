@@ -190,11 +190,13 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
         uint8_t* blk8 = a.pages + (int64_t)page * H * kPageBlock8;
         const uint16_t* krow = a.k + (int64_t)tok * H * kHeadDim + 4 * lane;
         const uint16_t* vrow = a.v + (int64_t)tok * H * kHeadDim + 4 * lane;
+        RopeRow rr{};
+        if (ROPE) rr = rope_row(a.rope + (int64_t)pos * kHeadDim, lane);   // one row for all heads
         for (int h = h_lo; h < h_hi; ++h) {
             float kx[4], vx[4];
             load_bf16x4(krow + h * kHeadDim, kx);
             load_bf16x4(vrow + h * kHeadDim, vx);
-            if (ROPE) warp_rope128(kx, a.rope + (int64_t)pos * kHeadDim, lane);
+            if (ROPE) warp_rope128(kx, rr, lane);
             warp_fwht128(kx, lane);
             uint32_t k8[4], v8[4];
             __half k8d, k8m, v8d, v8m;
@@ -229,6 +231,11 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
     uint8_t* sb0 = a.side + (int64_t)slot * H * a.side_block_bytes;
     const int tsA = posA % kPage;
     const int kw = kKCodeOff + k_word_offset(tsA & 7, lane);
+    RopeRow rA{}, rB{};                     // the tokens' RoPE rows, shared by all heads
+    if (ROPE) {
+        rA = rope_row(a.rope + (int64_t)posA * kHeadDim, lane);
+        if (pair) rB = rope_row(a.rope + (int64_t)posB * kHeadDim, lane);
+    }
     if (pair) {
         for (int h = hb; h < he; ++h) {
             uint8_t* blk = blk0 + h * kPageBlock;
@@ -239,8 +246,8 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
             load_bf16x4(krow + rowB + h * kHeadDim, kxB);
             load_bf16x4(vrow + rowB + h * kHeadDim, vxB);
             if (ROPE) {
-                warp_rope128(kxA, a.rope + (int64_t)posA * kHeadDim, lane);
-                warp_rope128(kxB, a.rope + (int64_t)posB * kHeadDim, lane);
+                warp_rope128(kxA, rA, lane);
+                warp_rope128(kxB, rB, lane);
             }
             const uint32_t knA = append_head(a, kxA, vxA, blk, tsA, sb, sinkA, ringA, posA, lane);
             const uint32_t knB = append_head(a, kxB, vxB, blk, tsA + 8, sb, sinkB, ringB, posB, lane);
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
             float kx[4], vx[4];
             load_bf16x4(krow + h * kHeadDim, kx);
             load_bf16x4(vrow + h * kHeadDim, vx);
-            if (ROPE) warp_rope128(kx, a.rope + (int64_t)posA * kHeadDim, lane);
+            if (ROPE) warp_rope128(kx, rA, lane);
             const uint32_t kn = append_head(a, kx, vx, blk, tsA, sb0 + h * a.side_block_bytes,
                                             sinkA, ringA, posA, lane);
             *kp = lower ? ((old & 0xf0f0f0f0u) | kn) : ((old & 0x0f0f0f0fu) | (kn << 4));

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
         if (L > a.rope_max_pos) {
             if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_POSITION);
         } else if (L > 0) {
-            warp_rope128(x, a.rope + (int64_t)(L - 1) * kHeadDim, lane);
+            warp_rope128(x, rope_row(a.rope + (int64_t)(L - 1) * kHeadDim, lane), lane);
         }
     }
     warp_fwht128(x, lane);

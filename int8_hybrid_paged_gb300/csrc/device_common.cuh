@@ -260,12 +260,18 @@ __device__ __forceinline__ void fence_mbar_init()
 // row of the caller's table (cos of pair i at row[i], sin at row[64 + i]): dims i and
 // i + 64 (lanes l and l ^ 16) rotate together, x_i' = fma(x_i, cos, -(x_{i+64} sin)),
 // x_{i+64}' = fma(x_{i+64}, cos, x_i sin), each product and fma rounded once.
-__device__ __forceinline__ void warp_rope128(float (&x)[4], const float* __restrict__ row, int lane)
+struct RopeRow {
+    float4 c, s;                 // this lane's cos and sin (pairs 4 (l mod 16) .. +3)
+};
+__device__ __forceinline__ RopeRow rope_row(const float* __restrict__ row, int lane)
 {
     const int i0 = 4 * (lane & 15);
-    const float4 c = __ldg(reinterpret_cast<const float4*>(row + i0));
-    const float4 s = __ldg(reinterpret_cast<const float4*>(row + 64 + i0));
-    const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+    return {__ldg(reinterpret_cast<const float4*>(row + i0)),
+            __ldg(reinterpret_cast<const float4*>(row + 64 + i0))};
+}
+__device__ __forceinline__ void warp_rope128(float (&x)[4], const RopeRow& r, int lane)
+{
+    const float cc[4] = {r.c.x, r.c.y, r.c.z, r.c.w}, ss[4] = {r.s.x, r.s.y, r.s.z, r.s.w};
     const bool lo = lane < 16;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
