@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
+    ap.add_argument("--format", choices=["int4-hybrid", "int8"], default="int4-hybrid",
+                    help="cache format of the main measurement: the method (INT4 pages + INT8 "
+                         "side buffer) or the whole-cache 8-bit format (KV8, s = w = 0)")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the unprotected KV4 (s = w = 0) and whole-cache 8-bit measurements")
     return ap.parse_args()
@@ -184,9 +187,13 @@ def split_kernel_traffic():
 # --------------------------------------------------------------------------- workload
 
 def workload_from_args(args):
-    """The named workload, with the protected region overridden if asked."""
+    """The named workload, with the protected region overridden if asked (the 8-bit
+    format has none)."""
     import dataclasses
     wl = inputs.workload(args.workload)
+    if getattr(args, "format", "int4-hybrid") == "int8":
+        return dataclasses.replace(wl, sink=0, window=0,
+                                   name=wl.name + " (whole-cache 8-bit format)")
     if args.sink is not None or args.window is not None:
         s = wl.sink if args.sink is None else args.sink
         w = wl.window if args.window is None else args.window
@@ -229,7 +236,7 @@ def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
                 slots=slots, lens=lens, num_pages=num_pages)
 
 
-def oracle_sample(wl, st, cpu_seconds, threads):
+def oracle_sample(wl, st, cpu_seconds, threads, kv8=False):
     """Time the CPU oracle's decode over a bounded sample of the workload's sequences
     (the same inputs as the GPU run). Returns the cpu_baseline dict."""
     import oracle
@@ -238,7 +245,7 @@ def oracle_sample(wl, st, cpu_seconds, threads):
     pick = list(range(len(st["host_kv"])))
     H, G = wl.num_kv_heads, wl.group
     maxL = max(lens[b] for b in pick)
-    oc = oracle.OracleCache(H, wl.sink, wl.window, maxL, num_slots=len(pick))
+    oc = oracle.OracleCache(H, wl.sink, wl.window, maxL, num_slots=len(pick), kv8=kv8)
     for i, b in enumerate(pick):
         oc.append(i, 0, st["host_kv"][b][0], st["host_kv"][b][1])
     qb = inputs.bf16_bits(st["q"][pick])
@@ -269,9 +276,11 @@ def run_kv4(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workload_from_args(args)
+    kv8 = args.format == "int8"
     seed = wl.seed + rank
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    st = build_workload(wl, seed, dev, sample_seqs=8 if want_cpu else 0)
+    st = build_workload(wl, seed, dev, sample_seqs=8 if want_cpu else 0,
+                        fmt=kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_INT4_HYBRID)
     cache = st["cache"]
     B, Hq, H = wl.batch, wl.num_q_heads, wl.num_kv_heads
     lens = st["lens"]
@@ -321,14 +330,17 @@ def run_kv4(args, rank, world, local):
     t_max, tok_sum = reduce_max_sum(world, ms, tokens_step * args.steps, dev)
     value = tok_sum / (t_max * 1e-3)
 
-    call_bytes = bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
+    if kv8:
+        call_bytes = bytes_model.decode_call_bytes_kv8(lens, Hq, H, with_lse=True)
+    else:
+        call_bytes = bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
     # the split kernel reads 144-byte query records (written by the prep kernel) instead
     # of the bf16 queries; the outputs are written by the merge
     split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
     split_ms = prof["split_ms"] / max(1, prof["calls"])
     peak, peak_src = measured_peaks()
     achieved = split_bytes / (split_ms * 1e-3) / 1e9
-    traffic = split_kernel_traffic()
+    traffic = None if kv8 else split_kernel_traffic()
     step_gbs = call_bytes * layers / (ms / args.steps * 1e-3) / 1e9
 
     res = {
@@ -364,9 +376,9 @@ def run_kv4(args, rank, world, local):
         res["append_stress"] = run_append_stress(dev, peak)
 
     # ---- the same workload without the protected region (pure KV4), rank 0 at N = 1
-    if world == 1 and not args.no_variants and (wl.sink > 0 or wl.window > 0):
+    if world == 1 and not args.no_variants and not kv8 and (wl.sink > 0 or wl.window > 0):
         res["kv4_unprotected"] = run_unprotected(wl, seed, dev, peak, value, min(args.steps, 500))
-    if world == 1 and not args.no_variants:
+    if world == 1 and not args.no_variants and not kv8:
         res["kv8"] = run_kv8(wl, seed, dev, peak, value, min(args.steps, 500))
 
     # ---- end to end through the public API from pinned host buffers
@@ -375,7 +387,7 @@ def run_kv4(args, rank, world, local):
 
     # ---- CPU oracle baseline (rank 0, one GPU)
     if want_cpu:
-        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores())
+        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores(), kv8)
     cache.close()
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -611,7 +623,8 @@ def run_reference(args, rank, world):
     qb = inputs.bf16_bits(inputs.queries(wl.batch, Hq, wl.seed))
 
     def make(nseq):
-        oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq)
+        oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq,
+                                kv8=args.format == "int8")
         for i in range(nseq):
             oc.append(i, 0, *seq(i))
         return oc
