@@ -267,6 +267,21 @@ kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
                                         int batch, float sm_scale, float *out_dev, float *lse_dev,
                                         void *stream);
 
+/*
+ * kv4_linear_bf16 — Y = X · Wᵀ on the tcgen05 tensor cores (the QKV projection ahead
+ * of the cache): BF16 inputs, FP32 accumulation in tensor memory, BF16 output
+ * (round to nearest). Tiles of 128 × 128 outputs, TMA loads with a 128-byte swizzle.
+ *   x_dev   : [M][K] bf16, K contiguous, 16-byte aligned
+ *   w_dev   : [N][K] bf16, K contiguous (the nn.Linear weight layout), 16-byte aligned
+ *   y_dev   : [M][N] bf16, 16-byte aligned
+ *   M >= 1; N a multiple of 128; K a multiple of 64
+ *   err_dev : device int32 error word (KV4_DEVERR_WAIT_TIMEOUT if a staging wait gave
+ *             up, leaving the output incomplete), or NULL
+ * Errors: KV4_ERR_INVALID_ARG (sizes, alignment), KV4_ERR_CUDA.
+ */
+kv4_status kv4_linear_bf16(const void *x_dev, const void *w_dev, void *y_dev, int M, int N, int K,
+                           int32_t *err_dev, void *stream);
+
 /* Per-kernel device time of decode calls, from CUDA events recorded around each
  * of the three decode launches on the caller's stream while profiling is on. */
 typedef struct {

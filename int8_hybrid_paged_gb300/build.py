@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkv4.so")
 
-SOURCES = ["api.cpp", "append.cu", "decode.cu"]
+SOURCES = ["api.cpp", "append.cu", "decode.cu", "qkv.cu"]
 HEADERS = ["kv4_internal.h", "device_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

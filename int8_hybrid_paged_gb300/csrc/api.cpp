@@ -343,6 +343,16 @@ kv4_status kv4_profile_stop(kv4_cache* c, kv4_profile* out)
     return st;
 }
 
+kv4_status kv4_linear_bf16(const void* x, const void* w, void* y, int M, int N, int K, int32_t* err,
+                           void* stream)
+{
+    if (!x || !w || !y || M < 1 || N < 128 || K < 64 || N % 128 != 0 || K % 64 != 0)
+        return KV4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(y)) & 15)
+        return KV4_ERR_INVALID_ARG;
+    return check_launch(kv4::launch_linear_bf16(x, w, y, M, N, K, err, static_cast<cudaStream_t>(stream)));
+}
+
 kv4_status kv4_get_device_error(kv4_cache* c, int32_t* code, int clear)
 {
     if (!c || !code) return KV4_ERR_INVALID_ARG;

@@ -122,6 +122,9 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+// Y = X · Wᵀ (BF16 in and out, FP32 accumulation) on the tcgen05 tensor cores.
+cudaError_t launch_linear_bf16(const void* x, const void* w, void* y, int M, int N, int K, int32_t* err,
+                               cudaStream_t stream);
 // ev: null, or 4 events recorded before plan, between plan/split, split/merge, after merge.
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev);
 // Persistent decode CTAs that fit on one SM (occupancy of the split kernel); also

@@ -1,0 +1,279 @@
+// qkv.cu — the projection ahead of the cache on the 5th-generation tensor cores:
+// Y = X · Wᵀ with X [M][K] and W [N][K] in BF16 (both K-contiguous, the nn.Linear
+// layout), FP32 accumulation in tensor memory.
+//
+// One CTA computes a 128 × 128 tile of Y: one thread streams 128 × 64 tiles of X and W
+// into a ring of shared-memory stages with TMA (128-byte swizzle); one thread issues
+// tcgen05.mma (M = 128, N = 128, K = 16 per instruction) into a TMEM accumulator and
+// frees each stage with tcgen05.commit; then the four warps read their 32 TMEM lanes
+// (rows) back with tcgen05.ld and write the tile. Every wait is bounded: a wait that
+// gives up records an error and the CTA still releases its tensor memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "kv4_internal.h"
+
+namespace kv4 {
+
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64;      // tile; kBK * 2 bytes = one 128-byte swizzle row
+constexpr int kGemmStages = 4;
+constexpr int kTileBytes = kBM * kBK * 2;           // 16 KB per operand tile
+constexpr int kGemmThreads = 128;
+constexpr uint32_t kTmemCols = 128;                 // FP32 accumulator columns (= kBN)
+
+struct __align__(1024) GemmSmem {
+    uint8_t a[kGemmStages][kTileBytes];             // 1024-byte aligned: swizzle atoms
+    uint8_t b[kGemmStages][kTileBytes];
+    uint64_t full[kGemmStages], empty[kGemmStages], accum;
+    uint32_t tmem_base;
+    int32_t abort;
+};
+
+// ---- TMA, tcgen05 (inline PTX)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzle
+// layout: start address, leading offset (unused for this layout, 16 bytes), stride
+// between 8-row groups 1024 bytes, descriptor version 1, swizzle mode 2 (128 bytes).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(16u >> 4) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both K-major,
+// N = kBN, M = kBM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive FP32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Bounded wait on an mbarrier phase (about 2 s), false when it gave up.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
+{
+    if (mbar_try_wait_at(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                       uint16_t* __restrict__ y, int M, int N, int K, int32_t* err)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+    const int nk = K / kBK;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGemmStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        mbar_init(&sm.accum, 1);
+        sm.abort = 0;
+        fence_mbar_init();
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+    }
+    if (warp == 0) {
+        // the accumulator: kTmemCols columns x 128 lanes of tensor memory
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(&sm.tmem_base)), "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (tid == 0) {
+        // ---- producer: TMA of the X and W tiles of every k block
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kGemmStages, r = kb / kGemmStages;
+            if (r > 0 && !wait_phase(smem_u32(&sm.empty[s]), (r - 1) & 1)) {
+                report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
+                atomicExch(&sm.abort, 1);
+                break;
+            }
+            const uint32_t fb = smem_u32(&sm.full[s]);
+            arrive_expect_tx(fb, 2 * kTileBytes);
+            tma_load_2d(smem_u32(sm.a[s]), &map_x, kb * kBK, m0, fb);
+            tma_load_2d(smem_u32(sm.b[s]), &map_w, kb * kBK, n0, fb);
+        }
+    } else if (tid == 32) {
+        // ---- MMA issuer: four K = 16 steps per stage, accumulate after the first
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % kGemmStages, r = kb / kGemmStages;
+            if (!wait_phase(smem_u32(&sm.full[s]), r & 1)) {
+                report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
+                atomicExch(&sm.abort, 1);
+                ok = false;
+                break;
+            }
+            tmem_fence_after();
+            const uint64_t ad = smem_desc_sw128(smem_u32(sm.a[s]));
+            const uint64_t bd = smem_desc_sw128(smem_u32(sm.b[s]));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)              // +32 bytes along K = +2 in the address field
+                umma_bf16(tmem, ad + 2 * k, bd + 2 * k, (kb | k) != 0);
+            umma_commit(smem_u32(&sm.empty[s]));          // stage free once these MMAs have read it
+        }
+        if (ok) umma_commit(smem_u32(&sm.accum));
+        else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&sm.accum)) : "memory");
+    }
+
+    // ---- epilogue: every warp reads its 32 lanes (rows) of the accumulator
+    const bool got = wait_phase(smem_u32(&sm.accum), 0);
+    tmem_fence_after();
+    __syncwarp();
+    if (got && !sm.abort) {
+        const int row = m0 + 32 * warp + lane;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c), v);
+            if (row < M) {
+                uint4* dst = reinterpret_cast<uint4*>(y + (int64_t)row * N + n0 + 32 * c);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                        w[e] = *reinterpret_cast<const uint32_t*>(&h);
+                    }
+                    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+    } else if (!got && lane == 0) {
+        report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
+    }
+    tmem_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tmem_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---- host: tensor maps through the driver entry point
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// rows x K BF16, K contiguous; boxes of kBK x 128 rows, 128-byte swizzle; rows past
+// the end read as zero
+bool make_map(CUtensorMap* map, const void* base, int rows, int K)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_linear_bf16(const void* x, const void* w, void* y, int M, int N, int K, int32_t* err,
+                               cudaStream_t stream)
+{
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, M, K) || !make_map(&mw, w, N, K)) return cudaErrorInvalidValue;
+    const size_t smem = sizeof(GemmSmem) + 1024;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [smem]() {
+        attr = cudaFuncSetAttribute(kv4_linear_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+    });
+    if (attr != cudaSuccess) return attr;
+    const dim3 grid((unsigned)(N / kBN), (unsigned)((M + kBM - 1) / kBM));
+    kv4_linear_bf16_kernel<<<grid, kGemmThreads, smem, stream>>>(mx, mw, static_cast<uint16_t*>(y), M, N, K,
+                                                                  err);
+    return cudaGetLastError();
+}
+
+}  // namespace kv4

@@ -28,7 +28,7 @@ PAGE_SIZE = 16
 EXPORTED = ("kv4_cache_create", "kv4_cache_free", "kv4_cache_get_info", "kv4_append",
             "kv4_decode_attention", "kv4_decode_attention_debug", "kv4_get_device_error",
             "kv4_status_string", "kv4_profile_start", "kv4_profile_stop",
-            "kv4_decode_attention_noalloc", "kv4_cache_set_rope")
+            "kv4_decode_attention_noalloc", "kv4_cache_set_rope", "kv4_linear_bf16")
 
 
 class KV4Error(RuntimeError):
@@ -87,6 +87,7 @@ def load(path: str = LIB_PATH):
                                                  P, P, I, I, F, P, P, P]
     lib.kv4_profile_stop.argtypes = [P, C.POINTER(kv4_profile)]
     lib.kv4_cache_set_rope.argtypes = [P, P, I]
+    lib.kv4_linear_bf16.argtypes = [P, P, P, I, I, I, P, P]
     for name in EXPORTED:
         getattr(lib, name).restype = C.c_int if name != "kv4_status_string" else C.c_char_p
     _lib = lib
@@ -151,6 +152,21 @@ def kv4_cache_set_rope(handle, cos_sin=None):
     assert cos_sin.dim() == 2 and cos_sin.shape[1] == HEAD_DIM
     _check(load().kv4_cache_set_rope(handle, _ptr(cos_sin, torch.float32, "cos_sin"),
                                      int(cos_sin.shape[0])), "kv4_cache_set_rope")
+
+
+def kv4_linear_bf16(x, w, y=None, err=None, stream=None):
+    """y = x @ w.T on the tcgen05 tensor cores: x [M][K], w [N][K] bf16 CUDA tensors
+    (N % 128 == 0, K % 64 == 0); returns y [M][N] bf16. err: optional int32 device word."""
+    M, K = x.shape
+    N = w.shape[0]
+    assert w.shape[1] == K
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().kv4_linear_bf16(_ptr(x, torch.bfloat16, "x"), _ptr(w, torch.bfloat16, "w"),
+                                  _ptr(y, torch.bfloat16, "y"), M, N, K,
+                                  _ptr(err, torch.int32, "err"), _stream(stream)),
+           "kv4_linear_bf16")
+    return y
 
 
 def kv4_cache_free(handle):
