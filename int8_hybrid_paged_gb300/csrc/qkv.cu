@@ -2,9 +2,10 @@
 // Y = X · Wᵀ with X [M][K] and W [N][K] in BF16 (both K-contiguous, the nn.Linear
 // layout), FP32 accumulation in tensor memory.
 //
-// One CTA computes a 128 × 128 tile of Y: one thread streams 128 × 64 tiles of X and W
-// into a ring of shared-memory stages with TMA (128-byte swizzle); one thread issues
-// tcgen05.mma (M = 128, N = 128, K = 16 per instruction) into a TMEM accumulator and
+// One CTA computes a 128 × BN tile of Y (BN = 256, or 128 when that leaves SMs idle):
+// one thread streams 128 × 64 tiles of X and BN × 64 tiles of W into a ring of
+// shared-memory stages with TMA (128-byte swizzle); one thread issues tcgen05.mma
+// (M = 128, N = BN, K = 16 per instruction) into a TMEM accumulator and
 // frees each stage with tcgen05.commit; then the four warps read their 32 TMEM lanes
 // (rows) back with tcgen05.ld and write the tile. Every wait is bounded: a wait that
 // gives up records an error and the CTA still releases its tensor memory.
@@ -22,15 +23,16 @@ namespace kv4 {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;      // tile; kBK * 2 bytes = one 128-byte swizzle row
+constexpr int kBM = 128, kBK = 64;                 // kBK * 2 bytes = one 128-byte swizzle row
 constexpr int kGemmStages = 4;
-constexpr int kTileBytes = kBM * kBK * 2;           // 16 KB per operand tile
+constexpr int kTileBytes = kBM * kBK * 2;           // 16 KB: the X tile
 constexpr int kGemmThreads = 128;
-constexpr uint32_t kTmemCols = 128;                 // FP32 accumulator columns (= kBN)
 
+// BN = 128 or 256 output columns per tile (the W tile and the TMEM accumulator width)
+template <int BN>
 struct __align__(1024) GemmSmem {
     uint8_t a[kGemmStages][kTileBytes];             // 1024-byte aligned: swizzle atoms
-    uint8_t b[kGemmStages][kTileBytes];
+    uint8_t b[kGemmStages][BN * kBK * 2];
     uint64_t full[kGemmStages], empty[kGemmStages], accum;
     uint32_t tmem_base;
     int32_t abort;
@@ -67,17 +69,20 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr)
 }
 
 // Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both K-major,
-// N = kBN, M = kBM.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
+// N = BN, M = kBM.
+template <int BN>
+constexpr uint32_t idesc_bf16()
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
 
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate)
+                                          uint32_t idesc, uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -117,15 +122,18 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
     return mbar_wait_slow(bar, parity);
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                        uint16_t* __restrict__ y, int M, int N, int K, int32_t* err)
 {
+    constexpr uint32_t kTmemCols = BN;              // FP32 accumulator columns
+    constexpr int kWBytes = BN * kBK * 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    GemmSmem& sm = *reinterpret_cast<GemmSmem*>(
+    GemmSmem<BN>& sm = *reinterpret_cast<GemmSmem<BN>*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
     const int nk = K / kBK;
 
     if (tid == 0) {
@@ -161,9 +169,11 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
                 break;
             }
             const uint32_t fb = smem_u32(&sm.full[s]);
-            arrive_expect_tx(fb, 2 * kTileBytes);
+            arrive_expect_tx(fb, kTileBytes + kWBytes);
             tma_load_2d(smem_u32(sm.a[s]), &map_x, kb * kBK, m0, fb);
-            tma_load_2d(smem_u32(sm.b[s]), &map_w, kb * kBK, n0, fb);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)              // boxes of 128 W rows
+                tma_load_2d(smem_u32(sm.b[s]) + h * kTileBytes, &map_w, kb * kBK, n0 + 128 * h, fb);
         }
     } else if (tid == 32) {
         // ---- MMA issuer: four K = 16 steps per stage, accumulate after the first
@@ -181,7 +191,7 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
             const uint64_t bd = smem_desc_sw128(smem_u32(sm.b[s]));
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)              // +32 bytes along K = +2 in the address field
-                umma_bf16(tmem, ad + 2 * k, bd + 2 * k, (kb | k) != 0);
+                umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc_bf16<BN>(), (kb | k) != 0);
             umma_commit(smem_u32(&sm.empty[s]));          // stage free once these MMAs have read it
         }
         if (ok) umma_commit(smem_u32(&sm.accum));
@@ -195,7 +205,7 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
     if (got && !sm.abort) {
         const int row = m0 + 32 * warp + lane;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = 0; c < BN / 32; ++c) {
             float v[32];
             tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c), v);
             if (row < M) {
@@ -257,23 +267,38 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int K)
 
 }  // namespace
 
+template <int BN>
+static cudaError_t launch_bn(const CUtensorMap& mx, const CUtensorMap& mw, void* y, int M, int N, int K,
+                             int32_t* err, cudaStream_t stream)
+{
+    const size_t smem = sizeof(GemmSmem<BN>) + 1024;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [smem]() {
+        attr = cudaFuncSetAttribute(kv4_linear_bf16_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+    });
+    if (attr != cudaSuccess) return attr;
+    const dim3 grid((unsigned)(N / BN), (unsigned)((M + kBM - 1) / kBM));
+    kv4_linear_bf16_kernel<BN><<<grid, kGemmThreads, smem, stream>>>(mx, mw, static_cast<uint16_t*>(y), M, N,
+                                                                      K, err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_linear_bf16(const void* x, const void* w, void* y, int M, int N, int K, int32_t* err,
                                cudaStream_t stream)
 {
     CUtensorMap mx, mw;
     if (!make_map(&mx, x, M, K) || !make_map(&mw, w, N, K)) return cudaErrorInvalidValue;
-    const size_t smem = sizeof(GemmSmem) + 1024;
-    static std::once_flag once;
-    static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [smem]() {
-        attr = cudaFuncSetAttribute(kv4_linear_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem);
-    });
-    if (attr != cudaSuccess) return attr;
-    const dim3 grid((unsigned)(N / kBN), (unsigned)((M + kBM - 1) / kBM));
-    kv4_linear_bf16_kernel<<<grid, kGemmThreads, smem, stream>>>(mx, mw, static_cast<uint16_t*>(y), M, N, K,
-                                                                  err);
-    return cudaGetLastError();
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // 256-wide tiles halve the operand bytes per multiply-add; when they would leave SMs
+    // idle (few row tiles), 128-wide tiles double the CTAs
+    const int mt = (M + kBM - 1) / kBM;
+    if (N % 256 == 0 && (int64_t)mt * (N / 256) >= sms)
+        return launch_bn<256>(mx, mw, y, M, N, K, err, stream);
+    return launch_bn<128>(mx, mw, y, M, N, K, err, stream);
 }
 
 }  // namespace kv4
