@@ -282,6 +282,27 @@ kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
 kv4_status kv4_linear_bf16(const void *x_dev, const void *w_dev, void *y_dev, int M, int N, int K,
                            int32_t *err_dev, void *stream);
 
+/*
+ * kv4_qkv_append — the attention input projection with the append fused into its
+ * epilogue ([zh] 核心方法: keys take RoPE, then the Hadamard rotation, then the cache
+ * quantization): Y = X · W_qkvᵀ on the tcgen05 tensor cores (BF16 operands, FP32
+ * accumulation), Y rounded to BF16; the Q columns are written to q_out and the K and V
+ * columns of every token are appended to the cache exactly as kv4_append would append
+ * those BF16 rows (RoPE when a table is set, either cache format).
+ *   x_dev     : [total_tokens][d_model] bf16 hidden states, 16-byte aligned
+ *   w_qkv_dev : [(num_q_heads + 2 H_kv) * 128][d_model] bf16, rows in the order Q heads,
+ *               then K head 0, V head 0, K head 1, V head 1, ... (128 rows each)
+ *   q_out_dev : [total_tokens][num_q_heads][128] bf16 projected queries (pre-RoPE)
+ *   d_model   : a multiple of 64; num_q_heads * 128 a multiple of 256
+ *   other arguments: as kv4_append (the token order of x is the order of cu_tokens)
+ * Errors: as kv4_append, and KV4_ERR_INVALID_ARG for the sizes above.
+ */
+kv4_status kv4_qkv_append(kv4_cache *cache, const void *x_dev, const void *w_qkv_dev, int num_q_heads,
+                          int d_model, void *q_out_dev, const int32_t *cu_tokens_dev,
+                          const int32_t *slot_ids_dev, const int32_t *start_pos_dev,
+                          const int32_t *block_table_dev, int block_table_stride, int n_seqs,
+                          int total_tokens, void *stream);
+
 /* Per-kernel device time of decode calls, from CUDA events recorded around each
  * of the three decode launches on the caller's stream while profiling is on. */
 typedef struct {

@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkv4.so")
 
 SOURCES = ["api.cpp", "append.cu", "decode.cu", "qkv.cu"]
-HEADERS = ["kv4_internal.h", "device_common.cuh"]
+HEADERS = ["kv4_internal.h", "device_common.cuh", "append_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

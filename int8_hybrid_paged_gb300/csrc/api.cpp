@@ -343,6 +343,46 @@ kv4_status kv4_profile_stop(kv4_cache* c, kv4_profile* out)
     return st;
 }
 
+kv4_status kv4_qkv_append(kv4_cache* c, const void* x, const void* w, int num_q_heads, int d_model,
+                          void* q_out, const int32_t* cu_tokens, const int32_t* slot_ids,
+                          const int32_t* start_pos, const int32_t* block_table, int stride, int n_seqs,
+                          int total_tokens, void* stream)
+{
+    if (!c || n_seqs < 0 || total_tokens < 0 || stride < 0 || num_q_heads < 1 || d_model < 64)
+        return KV4_ERR_INVALID_ARG;
+    if (n_seqs == 0 || total_tokens == 0) return KV4_OK;
+    if (!x || !w || !q_out || !cu_tokens || !slot_ids || !start_pos || !block_table || stride < 1)
+        return KV4_ERR_INVALID_ARG;
+    if (d_model % 64 != 0 || (num_q_heads * KV4_HEAD_DIM) % 256 != 0) return KV4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(q_out)) &
+        15)
+        return KV4_ERR_INVALID_ARG;
+    if ((int64_t)total_tokens * c->cfg.num_kv_heads > (int64_t)INT32_MAX * 8) return KV4_ERR_OUT_OF_RANGE;
+    kv4::AppendArgs a{};
+    a.cu_tokens = cu_tokens;
+    a.slot_ids = slot_ids;
+    a.start_pos = start_pos;
+    a.block_table = block_table;
+    a.stride = stride;
+    a.n_seqs = n_seqs;
+    a.total_tokens = total_tokens;
+    a.num_heads = c->cfg.num_kv_heads;
+    a.sink = c->cfg.sink;
+    a.window = c->cfg.window;
+    a.max_slots = c->cfg.max_slots;
+    a.num_pages = c->cfg.num_pages;
+    a.pages = c->pages;
+    a.side = c->side;
+    a.side_block_bytes = (int64_t)c->side_block;
+    a.seq_len = c->seq_len;
+    a.err = c->err;
+    a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
+    a.rope = c->rope;
+    a.rope_max_pos = c->rope_max_pos;
+    return check_launch(
+        kv4::launch_qkv_append(a, x, w, q_out, num_q_heads, d_model, static_cast<cudaStream_t>(stream)));
+}
+
 kv4_status kv4_linear_bf16(const void* x, const void* w, void* y, int M, int N, int K, int32_t* err,
                            void* stream)
 {

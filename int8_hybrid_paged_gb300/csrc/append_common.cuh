@@ -1,0 +1,168 @@
+// append_common.cuh — the per-token work of an append, shared by the append kernel and
+// the fused projection epilogue: page and side-group byte layouts, the 8-bit row store,
+// and the rotation + quantization + packing of one token-head.
+//
+// Pages cited (title, then section):
+//   [zh] "KV4-RL:用 INT4 KV 缓存量化为 RLVR 异步 Rollout 提速" — 方法步骤详情 steps 2-3,
+//        前置知识 › 分组仿射 KV 量化
+//   [ko] "INT4 KV 캐시로 비동기 RLVR 롤아웃을 1.8배 가속한다" — 전제와 한계
+#pragma once
+
+#include "device_common.cuh"
+#include "kv4_internal.h"
+
+namespace kv4 {
+
+// Byte of (dim pair j, token t) inside a page's V code block. The block is 32 lanes x
+// 8 words: word (l, m) holds pair j = 8m + (l >> 2) for tokens u, u+4, u+8, u+12 with
+// u = l & 3 (bytes 0..3), so one lane's eight words are one tensor-core fragment per
+// 16-dim tile and sit in 32 contiguous bytes.
+__device__ __forceinline__ int v_byte_offset(int j, int t)
+{
+    return ((((j & 7) << 2) + (t & 3)) * 8 + (j >> 3)) * 4 + (t >> 2);
+}
+
+// Side K code byte of (row r, dim d): the QK A fragments of the protected path take,
+// per 32-dim chunk c = d / 32, eight words of four consecutive dims in two planes, so
+// one byte permute widens two codes of one fragment register.
+__device__ __forceinline__ int side_k_offset(int r, int d)
+{
+    const int word = (d & 31) >> 2;
+    return 1024 * (word >> 2) + 64 * r + 16 * (d >> 5) + 4 * (word & 3) + (d & 3);
+}
+
+// Byte of side row r inside a V fragment word (rows t, t+8, t+4, t+12 with t = r % 4).
+__device__ __forceinline__ int side_v_byte(int r) { return ((r >> 3) & 1) | (((r >> 2) & 1) << 1); }
+
+// Side V code byte of (row r, dim d): lane n = 4 (d % 8) + r % 4 of the PV A fragments,
+// word 2 (d / 16) + (d / 8) % 2 of its sixteen, stored as four 512-byte planes.
+__device__ __forceinline__ int side_v_offset(int r, int d)
+{
+    const int n = 4 * (d & 7) + (r & 3);
+    const int word = 2 * (d >> 4) + ((d >> 3) & 1);
+    return 16 * (32 * (word >> 2) + n) + 4 * (word & 3) + side_v_byte(r);
+}
+
+// One row rr of a 16-row INT8 group (a side group, or a page of the 8-bit format):
+// this lane's four K and V codes (dims 4 lane .. 4 lane + 3) and, from lane 0, the
+// row's metadata.
+__device__ __forceinline__ void store_int8_row(uint8_t* g, int rr, const uint32_t (&k8)[4],
+                                               const uint32_t (&v8)[4], __half k8d, __half k8m,
+                                               __half v8d, __half v8m, int lane)
+{
+    // the K codes of four consecutive dims are one word in natural order
+    *reinterpret_cast<uint32_t*>(g + kSideKCodeOff + side_k_offset(rr, 4 * lane)) =
+        k8[0] | (k8[1] << 8) | (k8[2] << 16) | (k8[3] << 24);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
+    if (lane == 0) {
+        *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
+            __halves2half2(k8d, k8m);
+        *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
+            __halves2half2(v8d, v8m);
+    }
+}
+
+// Page K codes: tokens t and t+8 share bytes (t in the low nibble). Lane l of a warp
+// holding dims 4l..4l+3 owns one 32-bit word per token pair: dims 4i, 4i+2, 4i+1,
+// 4i+3 of chunk c (i = l % 8, c = l / 8) in bytes 0..3, at plane i / 4 (512 bytes),
+// slot 4t + c (16 bytes), word i % 4 -- the QK fragment of lane (t, c) of the MMAs.
+__device__ __forceinline__ int k_word_offset(int t, int lane)
+{
+    const int i = lane & 7, c = lane >> 3;
+    return (i >> 2) * 512 + (4 * t + c) * 16 + (i & 3) * 4;
+}
+
+// Quantize and store one token-head: V to 4-bit codes in the page block, the metadata,
+// and the 8-bit side copies when the position is protected. Returns the lane's K codes
+// as a nibble word (bytes: dims 4i, 4i+2, 4i+1, 4i+3, low nibbles); the caller stores K.
+__device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)[4], float (&vx)[4],
+                                                uint8_t* blk, int ts, uint8_t* sb, bool to_sink,
+                                                bool to_ring, int pos, int lane)
+{
+    warp_fwht128(kx, lane);                 // keys are stored in the rotated basis; V is not rotated
+    uint32_t kc[4], vc[4];
+    __half kd, km, vd, vm;
+    warp_quant<15>(kx, kc, kd, km);
+    warp_quant<15>(vx, vc, vd, vm);
+    const uint32_t kn = kc[0] | (kc[2] << 8) | (kc[1] << 16) | (kc[3] << 24);
+    // V dim pairs 2l and 2l+1 of token ts, at their places in the tile-interleaved layout
+    blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
+    if (lane == 0) {
+        // metadata row ts % 8: [K ts, K ts+8, V ts, V ts+8] for ts < 8, the same row for ts >= 8
+        uint8_t* mrow = blk + kMetaOff + 16 * (ts & 7) + 4 * (ts >> 3);
+        *reinterpret_cast<__half2*>(mrow) = __halves2half2(kd, km);
+        *reinterpret_cast<__half2*>(mrow + 8) = __halves2half2(vd, vm);
+    }
+
+    // INT8 side copies: sink row pos (pos < s), ring row s + pos mod w for the last
+    // w positions of this append. Earlier positions of a long chunk would map to the
+    // same ring rows and be overwritten anyway; skipping them avoids the race.
+    if (to_sink || to_ring) {
+        const int s = a.sink, w = a.window;
+        uint32_t k8[4], v8[4];
+        __half k8d, k8m, v8d, v8m;
+        warp_quant<255>(kx, k8, k8d, k8m);
+        warp_quant<255>(vx, v8, v8d, v8m);
+        int idx[2];
+        int n = 0;
+        if (to_sink) idx[n++] = pos;
+        if (to_ring) idx[n++] = s + pos % w;
+        for (int k = 0; k < n; ++k)
+            store_int8_row(sb + (idx[k] >> 4) * kSideGroupBytes, idx[k] & 15, k8, v8, k8d, k8m, v8d,
+                           v8m, lane);
+    }
+    return kn;
+}
+
+// Where token tok of an append goes: its sequence entry i (cu_tokens[i] <= tok <
+// cu_tokens[i+1]), slot, position, the sequence's length after the append and the
+// page of the position. False, with the error reported, when an input is invalid.
+struct TokenLoc {
+    int i, c0, c1, slot, start, pos, new_len, page;
+};
+
+__device__ __forceinline__ bool locate_token(const AppendArgs& a, int tok, int lane, TokenLoc& L)
+{
+    int i = (int)(((int64_t)tok * a.n_seqs) / a.total_tokens);     // proportional guess
+    int c0 = __ldg(&a.cu_tokens[i]);
+    int c1 = __ldg(&a.cu_tokens[i + 1]);
+    if (!(c0 <= tok && tok < c1)) {
+        int lo = 0, hi = a.n_seqs;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(&a.cu_tokens[mid]) <= tok) lo = mid; else hi = mid;
+        }
+        i = lo;
+        c0 = __ldg(&a.cu_tokens[i]);
+        c1 = __ldg(&a.cu_tokens[i + 1]);
+    }
+    if (tok < c0 || tok >= c1) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_TOKENS);
+        return false;
+    }
+    L.i = i;
+    L.c0 = c0;
+    L.c1 = c1;
+    L.slot = __ldg(&a.slot_ids[i]);
+    L.start = __ldg(&a.start_pos[i]);
+    L.pos = L.start + (tok - c0);
+    L.new_len = L.start + (c1 - c0);
+    if (L.slot < 0 || L.slot >= a.max_slots) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_SLOT);
+        return false;
+    }
+    if (L.start < 0 || L.pos / kPage >= a.stride || (a.rope && L.new_len > a.rope_max_pos)) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_POSITION);
+        return false;
+    }
+    L.page = __ldg(&a.block_table[(int64_t)i * a.stride + L.pos / kPage]);
+    if (L.page < 0 || (int64_t)L.page >= a.num_pages) {
+        if (lane == 0) report_error(a.err, KV4_DEVERR_BAD_PAGE);
+        return false;
+    }
+    return true;
+}
+
+}  // namespace kv4

@@ -122,6 +122,10 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+// The projection X · W_qkvᵀ on the tcgen05 tensor cores with the append fused into its
+// epilogue: Q columns to q_out (bf16), K and V columns appended as ap describes.
+cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w, void* q_out, int num_q_heads,
+                              int d_model, cudaStream_t stream);
 // Y = X · Wᵀ (BF16 in and out, FP32 accumulation) on the tcgen05 tensor cores.
 cudaError_t launch_linear_bf16(const void* x, const void* w, void* y, int M, int N, int K, int32_t* err,
                                cudaStream_t stream);

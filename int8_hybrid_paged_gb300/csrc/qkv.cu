@@ -16,6 +16,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "append_common.cuh"
 #include "device_common.cuh"
 #include "kv4_internal.h"
 
@@ -122,20 +123,16 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
     return mbar_wait_slow(bar, parity);
 }
 
+// The tile's main loop: barrier and TMEM set-up, thread 0 streams the X and W tiles of
+// every k block, thread 32 issues the MMAs, and every thread then waits for the
+// accumulator. True when the accumulator holds the finished tile.
 template <int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
-                       uint16_t* __restrict__ y, int M, int N, int K, int32_t* err)
+__device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& map_x,
+                                          const CUtensorMap& map_w, int m0, int n0, int nk,
+                                          int32_t* err)
 {
-    constexpr uint32_t kTmemCols = BN;              // FP32 accumulator columns
     constexpr int kWBytes = BN * kBK * 2;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    GemmSmem<BN>& sm = *reinterpret_cast<GemmSmem<BN>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
-    const int nk = K / kBK;
-
+    const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
         for (int s = 0; s < kGemmStages; ++s) {
             mbar_init(&sm.full[s], 1);
@@ -148,9 +145,9 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
     }
     if (warp == 0) {
-        // the accumulator: kTmemCols columns x 128 lanes of tensor memory
+        // the accumulator: BN columns x 128 lanes of tensor memory
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(&sm.tmem_base)), "r"(kTmemCols)
+                     ::"r"(smem_u32(&sm.tmem_base)), "r"((uint32_t)BN)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -197,40 +194,170 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
         if (ok) umma_commit(smem_u32(&sm.accum));
         else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&sm.accum)) : "memory");
     }
-
-    // ---- epilogue: every warp reads its 32 lanes (rows) of the accumulator
     const bool got = wait_phase(smem_u32(&sm.accum), 0);
     tmem_fence_after();
-    __syncwarp();
-    if (got && !sm.abort) {
-        const int row = m0 + 32 * warp + lane;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            float v[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * c), v);
-            if (row < M) {
-                uint4* dst = reinterpret_cast<uint4*>(y + (int64_t)row * N + n0 + 32 * c);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
-                        w[e] = *reinterpret_cast<const uint32_t*>(&h);
-                    }
-                    dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-        }
-    } else if (!got && lane == 0) {
-        report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
-    }
+    if (!got && (tid & 31) == 0) report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
+    // one answer for the whole CTA: the warp-collective TMEM loads that follow must be
+    // executed by every lane of every warp or by none
+    return __syncthreads_and(got && !sm.abort) != 0;
+}
+
+// Release the tile's tensor memory (after every warp's last tcgen05.ld).
+template <int BN>
+__device__ __forceinline__ void gemm_release(GemmSmem<BN>& sm)
+{
     tmem_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if ((threadIdx.x >> 5) == 0) {
         tmem_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(sm.tmem_base), "r"((uint32_t)BN)
                      : "memory");
+    }
+}
+
+// Columns [0, 32 * nc) of this thread's accumulator row as BF16 (round to nearest)
+// into dst (16-byte aligned, 64 bytes per 32 columns) when write is set. The TMEM
+// loads are warp-collective (.sync.aligned): every lane of the warp must call this,
+// with write false for rows that are not stored.
+__device__ __forceinline__ void store_row_bf16(uint32_t taddr, int nc, uint16_t* dst, bool write)
+{
+#pragma unroll 1
+    for (int c = 0; c < nc; ++c) {
+        float v[32];
+        tmem_ld32(taddr + (uint32_t)(32 * c), v);
+        if (!write) continue;
+        uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                w[e] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            d4[q] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                       uint16_t* __restrict__ y, int M, int N, int K, int32_t* err)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    GemmSmem<BN>& sm = *reinterpret_cast<GemmSmem<BN>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
+    const bool ok = gemm_tile<BN>(sm, map_x, map_w, m0, n0, K / kBK, err);
+    const int row = m0 + 32 * warp + lane;
+    if (ok)                                  // CTA-uniform: every lane loads, rows < M store
+        store_row_bf16(sm.tmem_base + ((uint32_t)(32 * warp) << 16), BN / 32, y + (int64_t)row * N + n0,
+                       row < M);
+    gemm_release<BN>(sm);
+}
+
+// Fused projection + append. Output columns: [Q heads | K0 V0 | K1 V1 | ...], 128 each;
+// a 256-wide tile is two Q heads or the K and V heads of one KV head.
+struct QkvArgs {
+    AppendArgs ap;                // the cache append (ap.k, ap.v unused)
+    uint16_t* q_out;              // [T][Hq * 128] bf16
+    int32_t q_cols;               // Hq * 128
+};
+
+template <bool KV8>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                      const QkvArgs qa, int K)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    GemmSmem<256>& sm = *reinterpret_cast<GemmSmem<256>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const AppendArgs& a = qa.ap;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * 256;
+    const int T = a.total_tokens;
+    const bool ok = gemm_tile<256>(sm, map_x, map_w, m0, n0, K / kBK, a.err);
+    const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * warp) << 16);
+    const int r = 32 * warp + lane, row = m0 + r;
+    if (n0 < qa.q_cols) {
+        // ---- two Q heads: the projection itself
+        if (ok) store_row_bf16(trow, 8, qa.q_out + (int64_t)row * qa.q_cols + n0, row < T);
+        gemm_release<256>(sm);
+        return;
+    }
+    // ---- K and V of KV head h for tokens m0 .. m0+127: rounded to BF16 as the projection
+    // would be, staged in the (now idle) W stages, then appended token by token
+    const int h = (n0 - qa.q_cols) / 256;
+    uint16_t* kt = reinterpret_cast<uint16_t*>(sm.b[0]);              // [128][128] bf16
+    uint16_t* vt = kt + 128 * 128;
+    fence_proxy_async();                    // the MMAs' reads of the stages precede these writes
+    if (ok) {                                // CTA-uniform; rows past T are staged but never read
+        store_row_bf16(trow, 4, kt + 128 * r, true);
+        store_row_bf16(trow + 128u, 4, vt + 128 * r, true);
+    }
+    gemm_release<256>(sm);                                            // ends with a CTA barrier
+    if (!ok) return;
+    const int H = a.num_heads;
+#pragma unroll 1
+    for (int rr = warp; rr < kBM; rr += kGemmThreads / 32) {
+        const int tok = m0 + rr;
+        if (tok >= T) break;
+        TokenLoc L;
+        if (!locate_token(a, tok, lane, L)) continue;
+        const int ts = L.pos % kPage;
+        float kxA[4], vxA[4];
+        {
+            const uint2 kw2 = *reinterpret_cast<const uint2*>(kt + 128 * rr + 4 * lane);
+            const uint2 vw2 = *reinterpret_cast<const uint2*>(vt + 128 * rr + 4 * lane);
+            kxA[0] = bf16_lo(kw2.x); kxA[1] = bf16_hi(kw2.x); kxA[2] = bf16_lo(kw2.y); kxA[3] = bf16_hi(kw2.y);
+            vxA[0] = bf16_lo(vw2.x); vxA[1] = bf16_hi(vw2.x); vxA[2] = bf16_lo(vw2.y); vxA[3] = bf16_hi(vw2.y);
+        }
+        if (a.rope) warp_rope128(kxA, rope_row(a.rope + (int64_t)L.pos * kHeadDim, lane), lane);
+        if (KV8) {
+            warp_fwht128(kxA, lane);
+            uint32_t k8[4], v8[4];
+            __half k8d, k8m, v8d, v8m;
+            warp_quant<255>(kxA, k8, k8d, k8m);
+            warp_quant<255>(vxA, v8, v8d, v8m);
+            store_int8_row(a.pages + ((int64_t)L.page * H + h) * kPageBlock8, ts, k8, v8, k8d, k8m, v8d, v8m,
+                           lane);
+            if (lane == 0 && h == 0 && tok == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+            continue;
+        }
+        // tokens t and t + 8 of a page share K bytes: a pair inside this tile is written
+        // whole by the lower token's warp; a token whose partner is elsewhere (another
+        // tile of this call, or an earlier append) merges its nibbles atomically
+        const bool lower = ts < 8;
+        const bool pair = lower ? (L.pos + 8 < L.new_len && rr + 8 < kBM && tok + 8 < T)
+                                : (L.pos - 8 >= L.start && rr >= 8);
+        if (pair && !lower) continue;                      // written with its lower partner
+        uint8_t* blk = a.pages + ((int64_t)L.page * H + h) * kPageBlock;
+        uint8_t* sb = a.side + ((int64_t)L.slot * H + h) * a.side_block_bytes;
+        const int kwo = kKCodeOff + k_word_offset(ts & 7, lane);
+        const bool sinkA = L.pos < a.sink, ringA = (a.window > 0) && (L.pos >= L.new_len - a.window);
+        const uint32_t knA = append_head(a, kxA, vxA, blk, ts, sb, sinkA, ringA, L.pos, lane);
+        uint32_t* kp = reinterpret_cast<uint32_t*>(blk + kwo);
+        if (pair) {
+            const int rb = rr + 8, posB = L.pos + 8;
+            float kxB[4], vxB[4];
+            const uint2 kw2 = *reinterpret_cast<const uint2*>(kt + 128 * rb + 4 * lane);
+            const uint2 vw2 = *reinterpret_cast<const uint2*>(vt + 128 * rb + 4 * lane);
+            kxB[0] = bf16_lo(kw2.x); kxB[1] = bf16_hi(kw2.x); kxB[2] = bf16_lo(kw2.y); kxB[3] = bf16_hi(kw2.y);
+            vxB[0] = bf16_lo(vw2.x); vxB[1] = bf16_hi(vw2.x); vxB[2] = bf16_lo(vw2.y); vxB[3] = bf16_hi(vw2.y);
+            if (a.rope) warp_rope128(kxB, rope_row(a.rope + (int64_t)posB * kHeadDim, lane), lane);
+            const bool sinkB = posB < a.sink, ringB = (a.window > 0) && (posB >= L.new_len - a.window);
+            const uint32_t knB = append_head(a, kxB, vxB, blk, ts + 8, sb, sinkB, ringB, posB, lane);
+            *kp = knA | (knB << 4);
+        } else if (lower) {
+            atomicAnd(kp, 0xf0f0f0f0u);
+            atomicOr(kp, knA);
+        } else {
+            atomicAnd(kp, 0x0f0f0f0fu);
+            atomicOr(kp, knA << 4);
+        }
+        if (lane == 0 && h == 0 && (pair ? tok + 8 : tok) == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
     }
 }
 
@@ -282,6 +409,34 @@ static cudaError_t launch_bn(const CUtensorMap& mx, const CUtensorMap& mw, void*
     const dim3 grid((unsigned)(N / BN), (unsigned)((M + kBM - 1) / kBM));
     kv4_linear_bf16_kernel<BN><<<grid, kGemmThreads, smem, stream>>>(mx, mw, static_cast<uint16_t*>(y), M, N,
                                                                       K, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w, void* q_out, int num_q_heads,
+                              int d_model, cudaStream_t stream)
+{
+    const int T = ap.total_tokens;
+    const int N = (num_q_heads + 2 * ap.num_heads) * kHeadDim;
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, T, d_model) || !make_map(&mw, w, N, d_model)) return cudaErrorInvalidValue;
+    QkvArgs qa{};
+    qa.ap = ap;
+    qa.q_out = static_cast<uint16_t*>(q_out);
+    qa.q_cols = num_q_heads * kHeadDim;
+    const size_t smem = sizeof(GemmSmem<256>) + 1024;
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [smem]() {
+        attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)smem);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr != cudaSuccess) return attr;
+    const dim3 grid((unsigned)(N / 256), (unsigned)((T + kBM - 1) / kBM));
+    if (ap.kv8) kv4_qkv_append_kernel<true><<<grid, kGemmThreads, smem, stream>>>(mx, mw, qa, d_model);
+    else kv4_qkv_append_kernel<false><<<grid, kGemmThreads, smem, stream>>>(mx, mw, qa, d_model);
     return cudaGetLastError();
 }
 

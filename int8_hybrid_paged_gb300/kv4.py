@@ -28,7 +28,8 @@ PAGE_SIZE = 16
 EXPORTED = ("kv4_cache_create", "kv4_cache_free", "kv4_cache_get_info", "kv4_append",
             "kv4_decode_attention", "kv4_decode_attention_debug", "kv4_get_device_error",
             "kv4_status_string", "kv4_profile_start", "kv4_profile_stop",
-            "kv4_decode_attention_noalloc", "kv4_cache_set_rope", "kv4_linear_bf16")
+            "kv4_decode_attention_noalloc", "kv4_cache_set_rope", "kv4_linear_bf16",
+            "kv4_qkv_append")
 
 
 class KV4Error(RuntimeError):
@@ -88,6 +89,7 @@ def load(path: str = LIB_PATH):
     lib.kv4_profile_stop.argtypes = [P, C.POINTER(kv4_profile)]
     lib.kv4_cache_set_rope.argtypes = [P, P, I]
     lib.kv4_linear_bf16.argtypes = [P, P, P, I, I, I, P, P]
+    lib.kv4_qkv_append.argtypes = [P, P, P, I, I, P, P, P, P, P, I, I, I, P]
     for name in EXPORTED:
         getattr(lib, name).restype = C.c_int if name != "kv4_status_string" else C.c_char_p
     _lib = lib
@@ -167,6 +169,23 @@ def kv4_linear_bf16(x, w, y=None, err=None, stream=None):
                                   _ptr(err, torch.int32, "err"), _stream(stream)),
            "kv4_linear_bf16")
     return y
+
+
+def kv4_qkv_append(handle, x, w_qkv, num_q_heads, cu_tokens, slot_ids, start_pos, block_table,
+                   q_out=None, stream=None):
+    """Projection + fused append: x [T][d_model], w_qkv [(Hq + 2 H_kv) * 128][d_model] (rows:
+    Q heads, then K0, V0, K1, V1, ...) bf16 CUDA tensors; appends K/V to the cache and
+    returns q_out [T][Hq][128] bf16."""
+    T, d_model = x.shape
+    if q_out is None:
+        q_out = torch.empty((T, num_q_heads, HEAD_DIM), dtype=torch.bfloat16, device=x.device)
+    _check(load().kv4_qkv_append(
+        handle, _ptr(x, torch.bfloat16, "x"), _ptr(w_qkv, torch.bfloat16, "w_qkv"), num_q_heads, d_model,
+        _ptr(q_out, torch.bfloat16, "q_out"), _ptr(cu_tokens, torch.int32, "cu_tokens"),
+        _ptr(slot_ids, torch.int32, "slot_ids"), _ptr(start_pos, torch.int32, "start_pos"),
+        _ptr(block_table, torch.int32, "block_table"), block_table.shape[-1], slot_ids.shape[0], T,
+        _stream(stream)), "kv4_qkv_append")
+    return q_out
 
 
 def kv4_cache_free(handle):
@@ -287,6 +306,11 @@ class KV4Cache:
 
     def info(self):
         return kv4_cache_get_info(self.handle)
+
+    def qkv_append(self, x, w_qkv, num_q_heads, cu_tokens, slot_ids, start_pos, block_table,
+                   q_out=None, stream=None):
+        return kv4_qkv_append(self.handle, x, w_qkv, num_q_heads, cu_tokens, slot_ids, start_pos,
+                              block_table, q_out, stream)
 
     def set_rope(self, cos_sin=None):
         """Fuse RoPE into appends and decodes (pre-RoPE K and q from now on); None clears."""
