@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--format", choices=["int4-hybrid", "int8"], default="int4-hybrid",
                     help="cache format of the main measurement: the method (INT4 pages + INT8 "
                          "side buffer) or the whole-cache 8-bit format (KV8, s = w = 0)")
+    ap.add_argument("--no-qkv", action="store_true",
+                    help="skip the fused projection + append measurement")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the unprotected KV4 (s = w = 0) and whole-cache 8-bit measurements")
     return ap.parse_args()
@@ -375,6 +377,10 @@ def run_kv4(args, rank, world, local):
     if world == 1 and not args.no_append:
         res["append_stress"] = run_append_stress(dev, peak)
 
+    # ---- the attention input projection with the append fused into its epilogue
+    if world == 1 and not args.no_qkv and not kv8:
+        res["qkv_append"] = run_qkv_append(dev)
+
     # ---- the same workload without the protected region (pure KV4), rank 0 at N = 1
     if world == 1 and not args.no_variants and not kv8 and (wl.sink > 0 or wl.window > 0):
         res["kv4_unprotected"] = run_unprotected(wl, seed, dev, peak, value, min(args.steps, 500))
@@ -492,6 +498,86 @@ def run_kv8(wl, seed, dev, peak, kv4_value, steps):
     finally:
         cache.close()
         torch.cuda.empty_cache()
+
+
+def run_qkv_append(dev):
+    """kv4_qkv_append (the QKV projection on the tcgen05 tensor cores with RoPE, the
+    Hadamard rotation and the 4-bit append fused into its epilogue) against the same
+    work in two steps (kv4_linear_bf16, then kv4_append), on Qwen3-8B attention shapes
+    (d_model 4096, 32 q heads, 8 KV heads): a decode step of 256 single tokens and a
+    re-prefill chunk of 8 x 2048 tokens. The two-step path also gathers the K and V
+    columns into [T][H][128] tensors for the append. Device time per call from one
+    replay of a CUDA graph of repeated calls; seeded random bf16 weights and hidden
+    states."""
+    from int8_hybrid_paged_gb300 import kv4
+    from int8_hybrid_paged_gb300.kv4 import KV4Cache
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak_tf = float(peaks.get("bf16_tflops", 1900.0))
+    H, Hq, d = 8, 32, 4096
+    N = (Hq + 2 * H) * 128
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    w = (torch.randn((N, d), generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+    out = {}
+    for tag, B, T, start_pos, reps in (("decode", 256, 1, 600, 50), ("prefill", 8, 2048, 0, 10)):
+        stride = (start_pos + T + 15) // 16 + 1
+        num_pages = B * stride + 8
+        bt = torch.from_numpy(inputs.block_tables([stride * 16] * B, 16, num_pages, 3)).to(dev)
+        x = torch.randn((B * T, d), generator=g, device=dev).to(torch.bfloat16)
+        cu = torch.arange(0, B * T + 1, T, dtype=torch.int32, device=dev)
+        slots = torch.arange(B, dtype=torch.int32, device=dev)
+        start = torch.full((B,), start_pos, dtype=torch.int32, device=dev)
+        tab = torch.from_numpy(inputs.rope_table(start_pos + T + 16)).to(dev)
+        caches = [KV4Cache(H, num_pages, B + 1, B, Hq, 16, 128) for _ in range(2)]
+        y = torch.empty((B * T, N), dtype=torch.bfloat16, device=dev)
+        q = torch.empty((B * T, Hq, 128), dtype=torch.bfloat16, device=dev)
+        try:
+            for c in caches:
+                c.set_rope(tab)
+
+            def fused():
+                caches[0].qkv_append(x, w, Hq, cu, slots, start, bt, q_out=q)
+
+            def apart():
+                kv4.kv4_linear_bf16(x, w, y)
+                kvp = y[:, Hq * 128:].view(B * T, H, 2, 128)      # the append takes [T][H][128] rows
+                caches[1].append(kvp[:, :, 0].contiguous(), kvp[:, :, 1].contiguous(), cu, slots, start, bt)
+
+            res = {}
+            for name, fn in (("fused", fused), ("apart", apart)):
+                for _ in range(3):
+                    fn()
+                torch.cuda.synchronize()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for _ in range(reps):
+                        fn()
+                graph.replay()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                graph.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                del graph
+                res[name] = e0.elapsed_time(e1) / reps
+            if caches[0].device_error() or caches[1].device_error():
+                raise RuntimeError("device error in the projection + append measurement")
+            flops = 2.0 * B * T * N * d
+            out[tag] = {"case": f"{B} sequences x {T} token(s) from position {start_pos}: X [{B * T}][{d}] "
+                                f"x W_qkv [{N}][{d}], RoPE + Hadamard + 4-bit append of 8 KV heads",
+                        "fused_us": res["fused"] * 1e3, "apart_us": res["apart"] * 1e3,
+                        "fused_tflops": flops / (res["fused"] * 1e-3) / 1e12,
+                        "fused_frac_of_bf16_peak": flops / (res["fused"] * 1e-3) / 1e12 / peak_tf,
+                        "speedup_over_apart": res["apart"] / res["fused"]}
+        finally:
+            for c in caches:
+                c.close()
+            del x, y, q
+            torch.cuda.empty_cache()
+    return out
 
 
 def run_append_stress(dev, peak):

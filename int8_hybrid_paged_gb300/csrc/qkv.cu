@@ -266,8 +266,12 @@ struct QkvArgs {
     int32_t q_cols;               // Hq * 128
 };
 
+// 8 warps: warps w and w + 4 read the same TMEM lane quarter (rows 32 (w % 4) ..), the
+// first the low 128 columns and the second the high 128; all 8 share the append loop.
+constexpr int kQkvThreads = 256;
+
 template <bool KV8>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kQkvThreads, 1)
 kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                       const QkvArgs qa, int K)
 {
@@ -279,11 +283,12 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * 256;
     const int T = a.total_tokens;
     const bool ok = gemm_tile<256>(sm, map_x, map_w, m0, n0, K / kBK, a.err);
-    const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * warp) << 16);
-    const int r = 32 * warp + lane, row = m0 + r;
+    const int quarter = warp & 3, colh = warp >> 2;                 // TMEM lane quarter, column half
+    const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(128 * colh);
+    const int r = 32 * quarter + lane, row = m0 + r;
     if (n0 < qa.q_cols) {
         // ---- two Q heads: the projection itself
-        if (ok) store_row_bf16(trow, 8, qa.q_out + (int64_t)row * qa.q_cols + n0, row < T);
+        if (ok) store_row_bf16(trow, 4, qa.q_out + (int64_t)row * qa.q_cols + n0 + 128 * colh, row < T);
         gemm_release<256>(sm);
         return;
     }
@@ -293,15 +298,13 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     uint16_t* kt = reinterpret_cast<uint16_t*>(sm.b[0]);              // [128][128] bf16
     uint16_t* vt = kt + 128 * 128;
     fence_proxy_async();                    // the MMAs' reads of the stages precede these writes
-    if (ok) {                                // CTA-uniform; rows past T are staged but never read
-        store_row_bf16(trow, 4, kt + 128 * r, true);
-        store_row_bf16(trow + 128u, 4, vt + 128 * r, true);
-    }
+    if (ok)                                  // CTA-uniform; rows past T are staged but never read
+        store_row_bf16(trow, 4, (colh ? vt : kt) + 128 * r, true);
     gemm_release<256>(sm);                                            // ends with a CTA barrier
     if (!ok) return;
     const int H = a.num_heads;
 #pragma unroll 1
-    for (int rr = warp; rr < kBM; rr += kGemmThreads / 32) {
+    for (int rr = warp; rr < kBM; rr += kQkvThreads / 32) {
         const int tok = m0 + rr;
         if (tok >= T) break;
         TokenLoc L;
@@ -435,8 +438,8 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     });
     if (attr != cudaSuccess) return attr;
     const dim3 grid((unsigned)(N / 256), (unsigned)((T + kBM - 1) / kBM));
-    if (ap.kv8) kv4_qkv_append_kernel<true><<<grid, kGemmThreads, smem, stream>>>(mx, mw, qa, d_model);
-    else kv4_qkv_append_kernel<false><<<grid, kGemmThreads, smem, stream>>>(mx, mw, qa, d_model);
+    if (ap.kv8) kv4_qkv_append_kernel<true><<<grid, kQkvThreads, smem, stream>>>(mx, mw, qa, d_model);
+    else kv4_qkv_append_kernel<false><<<grid, kQkvThreads, smem, stream>>>(mx, mw, qa, d_model);
     return cudaGetLastError();
 }
 
