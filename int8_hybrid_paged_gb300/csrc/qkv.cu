@@ -266,9 +266,9 @@ struct QkvArgs {
     int32_t q_cols;               // Hq * 128
 };
 
-// 8 warps: warps w and w + 4 read the same TMEM lane quarter (rows 32 (w % 4) ..), the
-// first the low 128 columns and the second the high 128; all 8 share the append loop.
-constexpr int kQkvThreads = 256;
+// 16 warps: warps w, w + 4, w + 8, w + 12 read the same TMEM lane quarter (rows
+// 32 (w % 4) ..), each a quarter of the 256 columns; all 16 share the append loop.
+constexpr int kQkvThreads = 512;
 
 template <bool KV8>
 __global__ void __launch_bounds__(kQkvThreads, 1)
@@ -283,12 +283,12 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * 256;
     const int T = a.total_tokens;
     const bool ok = gemm_tile<256>(sm, map_x, map_w, m0, n0, K / kBK, a.err);
-    const int quarter = warp & 3, colh = warp >> 2;                 // TMEM lane quarter, column half
-    const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(128 * colh);
+    const int quarter = warp & 3, colq = warp >> 2;                 // TMEM lane quarter, column quarter
+    const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(64 * colq);
     const int r = 32 * quarter + lane, row = m0 + r;
     if (n0 < qa.q_cols) {
         // ---- two Q heads: the projection itself
-        if (ok) store_row_bf16(trow, 4, qa.q_out + (int64_t)row * qa.q_cols + n0 + 128 * colh, row < T);
+        if (ok) store_row_bf16(trow, 2, qa.q_out + (int64_t)row * qa.q_cols + n0 + 64 * colq, row < T);
         gemm_release<256>(sm);
         return;
     }
@@ -299,7 +299,7 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     uint16_t* vt = kt + 128 * 128;
     fence_proxy_async();                    // the MMAs' reads of the stages precede these writes
     if (ok)                                  // CTA-uniform; rows past T are staged but never read
-        store_row_bf16(trow, 4, (colh ? vt : kt) + 128 * r, true);
+        store_row_bf16(trow, 2, (colq >= 2 ? vt : kt) + 128 * r + 64 * (colq & 1), true);
     gemm_release<256>(sm);                                            // ends with a CTA barrier
     if (!ok) return;
     const int H = a.num_heads;
