@@ -46,21 +46,31 @@ __device__ __forceinline__ int side_v_offset(int r, int d)
 // One row rr of a 16-row INT8 group (a side group, or a page of the 8-bit format):
 // this lane's four K and V codes (dims 4 lane .. 4 lane + 3) and, from lane 0, the
 // row's metadata.
-__device__ __forceinline__ void store_int8_row(uint8_t* g, int rr, const uint32_t (&k8)[4],
-                                               const uint32_t (&v8)[4], __half k8d, __half k8m,
-                                               __half v8d, __half v8m, int lane)
+// ... its K half (codes and metadata) and its V half, for callers that hold one of them
+__device__ __forceinline__ void store_int8_k(uint8_t* g, int rr, const uint32_t (&k8)[4], __half k8d,
+                                             __half k8m, int lane)
 {
     // the K codes of four consecutive dims are one word in natural order
     *reinterpret_cast<uint32_t*>(g + kSideKCodeOff + side_k_offset(rr, 4 * lane)) =
         k8[0] | (k8[1] << 8) | (k8[2] << 16) | (k8[3] << 24);
+    if (lane == 0)
+        *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) = __halves2half2(k8d, k8m);
+}
+__device__ __forceinline__ void store_int8_v(uint8_t* g, int rr, const uint32_t (&v8)[4], __half v8d,
+                                             __half v8m, int lane)
+{
 #pragma unroll
     for (int i = 0; i < 4; ++i) g[kSideVCodeOff + side_v_offset(rr, 4 * lane + i)] = (uint8_t)v8[i];
-    if (lane == 0) {
-        *reinterpret_cast<__half2*>(g + kSideKMetaOff + 8 * (rr & 7) + 4 * (rr >> 3)) =
-            __halves2half2(k8d, k8m);
+    if (lane == 0)
         *reinterpret_cast<__half2*>(g + kSideVMetaOff + 16 * (rr & 3) + 4 * side_v_byte(rr)) =
             __halves2half2(v8d, v8m);
-    }
+}
+__device__ __forceinline__ void store_int8_row(uint8_t* g, int rr, const uint32_t (&k8)[4],
+                                               const uint32_t (&v8)[4], __half k8d, __half k8m,
+                                               __half v8d, __half v8m, int lane)
+{
+    store_int8_k(g, rr, k8, k8d, k8m, lane);
+    store_int8_v(g, rr, v8, v8d, v8m, lane);
 }
 
 // Page K codes: tokens t and t+8 share bytes (t in the low nibble). Lane l of a warp
@@ -114,6 +124,52 @@ __device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)
                            v8m, lane);
     }
     return kn;
+}
+
+// The K half and the V half of append_head, for callers that hold one of the two
+// tensors: the same bytes (K codes returned as the nibble word, K metadata and K side
+// rows; V codes, V metadata and V side rows).
+__device__ __forceinline__ uint32_t append_k(const AppendArgs& a, float (&kx)[4], uint8_t* blk, int ts,
+                                             uint8_t* sb, bool to_sink, bool to_ring, int pos, int lane)
+{
+    warp_fwht128(kx, lane);
+    uint32_t kc[4];
+    __half kd, km;
+    warp_quant<15>(kx, kc, kd, km);
+    if (lane == 0)
+        *reinterpret_cast<__half2*>(blk + kMetaOff + 16 * (ts & 7) + 4 * (ts >> 3)) = __halves2half2(kd, km);
+    if (to_sink || to_ring) {
+        uint32_t k8[4];
+        __half k8d, k8m;
+        warp_quant<255>(kx, k8, k8d, k8m);
+        if (to_sink) store_int8_k(sb + (pos >> 4) * kSideGroupBytes, pos & 15, k8, k8d, k8m, lane);
+        if (to_ring) {
+            const int i = a.sink + pos % a.window;
+            store_int8_k(sb + (i >> 4) * kSideGroupBytes, i & 15, k8, k8d, k8m, lane);
+        }
+    }
+    return kc[0] | (kc[2] << 8) | (kc[1] << 16) | (kc[3] << 24);
+}
+__device__ __forceinline__ void append_v(const AppendArgs& a, float (&vx)[4], uint8_t* blk, int ts,
+                                         uint8_t* sb, bool to_sink, bool to_ring, int pos, int lane)
+{
+    uint32_t vc[4];
+    __half vd, vm;
+    warp_quant<15>(vx, vc, vd, vm);
+    blk[kVCodeOff + v_byte_offset(2 * lane, ts)] = (uint8_t)(vc[0] | (vc[1] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane + 1, ts)] = (uint8_t)(vc[2] | (vc[3] << 4));
+    if (lane == 0)
+        *reinterpret_cast<__half2*>(blk + kMetaOff + 16 * (ts & 7) + 4 * (ts >> 3) + 8) = __halves2half2(vd, vm);
+    if (to_sink || to_ring) {
+        uint32_t v8[4];
+        __half v8d, v8m;
+        warp_quant<255>(vx, v8, v8d, v8m);
+        if (to_sink) store_int8_v(sb + (pos >> 4) * kSideGroupBytes, pos & 15, v8, v8d, v8m, lane);
+        if (to_ring) {
+            const int i = a.sink + pos % a.window;
+            store_int8_v(sb + (i >> 4) * kSideGroupBytes, i & 15, v8, v8d, v8m, lane);
+        }
+    }
 }
 
 // Where token tok of an append goes: its sequence entry i (cu_tokens[i] <= tok <

@@ -364,6 +364,100 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     }
 }
 
+// The same with 128-wide tiles, for calls with few tokens (twice the CTAs): a tile is one
+// Q head, or the K or the V head of one KV head, appended with the K or V half of the
+// per-token routine (the same bytes as the combined one).
+template <bool KV8>
+__global__ void __launch_bounds__(kQkvThreads, 1)
+kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                             const QkvArgs qa, int K)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    GemmSmem<128>& sm = *reinterpret_cast<GemmSmem<128>*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const AppendArgs& a = qa.ap;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * 128;
+    const int T = a.total_tokens;
+    const bool ok = gemm_tile<128>(sm, map_x, map_w, m0, n0, K / kBK, a.err);
+    const int quarter = warp & 3, colq = warp >> 2;                 // TMEM lane quarter, column quarter
+    const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * colq);
+    const int r = 32 * quarter + lane, row = m0 + r;
+    if (n0 < qa.q_cols) {
+        if (ok) store_row_bf16(trow, 1, qa.q_out + (int64_t)row * qa.q_cols + n0 + 32 * colq, row < T);
+        gemm_release<128>(sm);
+        return;
+    }
+    const int kvj = (n0 - qa.q_cols) / 128, h = kvj >> 1;
+    const bool is_v = (kvj & 1) != 0;
+    uint16_t* xt = reinterpret_cast<uint16_t*>(sm.b[0]);              // [128][128] bf16: K or V
+    fence_proxy_async();
+    if (ok) store_row_bf16(trow, 1, xt + 128 * r + 32 * colq, true);
+    gemm_release<128>(sm);
+    if (!ok) return;
+    const int H = a.num_heads;
+#pragma unroll 1
+    for (int rr = warp; rr < kBM; rr += kQkvThreads / 32) {
+        const int tok = m0 + rr;
+        if (tok >= T) break;
+        TokenLoc L;
+        if (!locate_token(a, tok, lane, L)) continue;
+        const int ts = L.pos % kPage;
+        float xA[4];
+        {
+            const uint2 w2 = *reinterpret_cast<const uint2*>(xt + 128 * rr + 4 * lane);
+            xA[0] = bf16_lo(w2.x); xA[1] = bf16_hi(w2.x); xA[2] = bf16_lo(w2.y); xA[3] = bf16_hi(w2.y);
+        }
+        if (!is_v && a.rope) warp_rope128(xA, rope_row(a.rope + (int64_t)L.pos * kHeadDim, lane), lane);
+        if (KV8) {
+            uint8_t* g = a.pages + ((int64_t)L.page * H + h) * kPageBlock8;
+            uint32_t c8[4];
+            __half d8, m8;
+            if (!is_v) {
+                warp_fwht128(xA, lane);
+                warp_quant<255>(xA, c8, d8, m8);
+                store_int8_k(g, ts, c8, d8, m8, lane);
+                if (lane == 0 && h == 0 && tok == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+            } else {
+                warp_quant<255>(xA, c8, d8, m8);
+                store_int8_v(g, ts, c8, d8, m8, lane);
+            }
+            continue;
+        }
+        uint8_t* blk = a.pages + ((int64_t)L.page * H + h) * kPageBlock;
+        uint8_t* sb = a.side + ((int64_t)L.slot * H + h) * a.side_block_bytes;
+        const bool sinkA = L.pos < a.sink, ringA = (a.window > 0) && (L.pos >= L.new_len - a.window);
+        if (is_v) {
+            append_v(a, xA, blk, ts, sb, sinkA, ringA, L.pos, lane);
+            continue;
+        }
+        // K: tokens t and t + 8 of a page inside the tile are written together, others merge
+        const bool lower = ts < 8;
+        const bool pair = lower ? (L.pos + 8 < L.new_len && rr + 8 < kBM && tok + 8 < T)
+                                : (L.pos - 8 >= L.start && rr >= 8);
+        if (pair && !lower) continue;
+        const uint32_t knA = append_k(a, xA, blk, ts, sb, sinkA, ringA, L.pos, lane);
+        uint32_t* kp = reinterpret_cast<uint32_t*>(blk + kKCodeOff + k_word_offset(ts & 7, lane));
+        if (pair) {
+            const int rb = rr + 8, posB = L.pos + 8;
+            float xB[4];
+            const uint2 w2 = *reinterpret_cast<const uint2*>(xt + 128 * rb + 4 * lane);
+            xB[0] = bf16_lo(w2.x); xB[1] = bf16_hi(w2.x); xB[2] = bf16_lo(w2.y); xB[3] = bf16_hi(w2.y);
+            if (a.rope) warp_rope128(xB, rope_row(a.rope + (int64_t)posB * kHeadDim, lane), lane);
+            const bool sinkB = posB < a.sink, ringB = (a.window > 0) && (posB >= L.new_len - a.window);
+            const uint32_t knB = append_k(a, xB, blk, ts + 8, sb, sinkB, ringB, posB, lane);
+            *kp = knA | (knB << 4);
+        } else if (lower) {
+            atomicAnd(kp, 0xf0f0f0f0u);
+            atomicOr(kp, knA);
+        } else {
+            atomicAnd(kp, 0x0f0f0f0fu);
+            atomicOr(kp, knA << 4);
+        }
+        if (lane == 0 && h == 0 && (pair ? tok + 8 : tok) == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+    }
+}
+
 // ---- host: tensor maps through the driver entry point
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -426,20 +520,36 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     qa.ap = ap;
     qa.q_out = static_cast<uint16_t*>(q_out);
     qa.q_cols = num_q_heads * kHeadDim;
-    const size_t smem = sizeof(GemmSmem<256>) + 1024;
+    const size_t smem_w = sizeof(GemmSmem<256>) + 1024, smem_n = sizeof(GemmSmem<128>) + 1024;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
-    std::call_once(once, [smem]() {
-        attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)smem);
+    std::call_once(once, [smem_w, smem_n]() {
+        const int sw = (int)smem_w, sn = (int)smem_n;
+        attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sw);
         if (attr == cudaSuccess)
-            attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sw);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(kv4_qkv_append_narrow_kernel<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
+        if (attr == cudaSuccess)
+            attr = cudaFuncSetAttribute(kv4_qkv_append_narrow_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
     });
     if (attr != cudaSuccess) return attr;
-    const dim3 grid((unsigned)(N / 256), (unsigned)((T + kBM - 1) / kBM));
-    if (ap.kv8) kv4_qkv_append_kernel<true><<<grid, kQkvThreads, smem, stream>>>(mx, mw, qa, d_model);
-    else kv4_qkv_append_kernel<false><<<grid, kQkvThreads, smem, stream>>>(mx, mw, qa, d_model);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int mt = (T + kBM - 1) / kBM;
+    if ((int64_t)mt * (N / 256) >= sms) {
+        const dim3 grid((unsigned)(N / 256), (unsigned)mt);
+        if (ap.kv8) kv4_qkv_append_kernel<true><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+        else kv4_qkv_append_kernel<false><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+    } else {
+        // few tokens: 128-wide tiles double the CTAs
+        const dim3 grid((unsigned)(N / 128), (unsigned)mt);
+        if (ap.kv8) kv4_qkv_append_narrow_kernel<true><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+        else kv4_qkv_append_narrow_kernel<false><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+    }
     return cudaGetLastError();
 }
 

@@ -94,6 +94,13 @@ def test_fused_chunked_appends(fmt, s, w):
     _case(2, 8, 256, LENS, cuts, fmt, s, w, True, seed=12)
 
 
+@pytest.mark.parametrize("fmt,s,w", [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0)])
+def test_fused_wide_tiles(fmt, s, w):
+    """Enough tokens for 256-wide tiles (K and V of a head in one tile); the cases above
+    take 128-wide tiles (K or V alone)."""
+    _case(2, 8, 256, [1500, 2000, 333], [700], fmt, s, w, True, seed=14)
+
+
 def test_fused_qwen3_8b_shapes():
     """Qwen3-8B attention shapes (32 q heads, 8 KV heads, d_model 4096): a decode step of
     256 single tokens after a 600-token prefill."""
