@@ -22,4 +22,9 @@ from .kv4_oracle import (  # noqa: F401
     quant_affine,
     quant_query,
     rope128,
+    e4m3_rn,
+    e4m3_value,
+    e2m1_rn,
+    e2m1_value,
+    quant_nvfp4,
 )

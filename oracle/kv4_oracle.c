@@ -63,6 +63,16 @@
  *      the query takes the same rotations). Pairing (i, i + 64) ("rotate half"), with
  *      a = x_i, b = x_{i+64}: x'_i = fmaf(a, cos, −fl(b·sin)),
  *      x'_{i+64} = fmaf(b, cos, fl(a·sin)); cos and sin are the caller's FP32 table.
+ *   R12 NVFP4, the 4-bit floating-point KV format the pages compare against ([zh]
+ *      技术新颖性: an appendix compares NVFP4/MXFP4; 未来方向: a KV4 variant on native
+ *      FP4 hardware): the public NVFP4 layout with the method's online per-vector
+ *      scaling. Each 128-value token-head vector (rotated K, unrotated V) has an FP32
+ *      scale g = amax / (6·448) and, per block of 16, an E4M3 scale
+ *      s_b = e4m3(amax_b / fl(6g)); each value is e2m1(x · fl(1/fl(s_b g))), nearest
+ *      with ties to even. The whole cache is NVFP4 (no protected region). Decode keeps the
+ *      INT8 query: the score is ((Σ_b fma-chained s_b·dot_b)·g·s_q)·C with each block dot
+ *      exact; values enter PV as bf16(e2m1·fl(s_b g)) with R7's BF16 weights, in groups of
+ *      16 consecutive positions.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -306,6 +316,98 @@ void orc_quant_query(const float *q_rot, int8_t *q8, float *q_scale, int32_t *q_
     *q_sum = sum;
 }
 
+/* ---- NVFP4 (reading R12): E2M1 elements, E4M3 block scales, an FP32 vector scale ---- */
+
+/* E4M3 (bias 7, no infinities, largest finite 448): t >= 0 rounded to the nearest
+   representable value, ties to even mantissa, values above 448 held at 448. The
+   subnormal quantum is 2^-9; normal values of exponent e have quantum 2^(e-3). */
+uint8_t orc_e4m3_rn(float t)
+{
+    if (!(t > 0.0f)) return 0;
+    if (t >= 448.0f) return 0x7E;
+    int e;
+    frexpf(t, &e);                                /* t = f 2^e, f in [0.5, 1) */
+    e -= 1;                                       /* floor(log2 t) */
+    if (e < -6) e = -6;                           /* subnormal range shares the 2^-9 quantum */
+    const float q = ldexpf(1.0f, e - 3);
+    float m = rintf(t / q);                       /* exact division by a power of two; rint: ties even */
+    float v = m * q;
+    if (v >= 448.0f) return 0x7E;
+    if (v == 0.0f) return 0;
+    if (v < 0x1p-6f) return (uint8_t)(v / 0x1p-9f);            /* subnormal: mantissa only */
+    frexpf(v, &e);
+    e -= 1;
+    const int mant = (int)(v / ldexpf(1.0f, e - 3)) - 8;        /* 0..7 */
+    return (uint8_t)(((e + 7) << 3) | mant);
+}
+
+float orc_e4m3_value(uint8_t bits)
+{
+    const int E = (bits >> 3) & 15, m = bits & 7;
+    const float mag = E == 0 ? ldexpf((float)m, -9) : ldexpf(1.0f + (float)m / 8.0f, E - 7);
+    return (bits & 0x80) ? -mag : mag;
+}
+
+/* E2M1 magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 (codes 0..7), sign in bit 3. v rounded to the
+   nearest, ties to the even code, held at 6; a zero magnitude is code 0. */
+static const float kE2M1[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+uint8_t orc_e2m1_rn(float v)
+{
+    const float a = fabsf(v);
+    int best = 7;
+    if (a < 6.0f) {
+        for (int k = 0; k < 7; k++) {
+            const float mid = 0.5f * (kE2M1[k] + kE2M1[k + 1]);        /* exact */
+            if (a < mid || (a == mid && (k & 1) == 0)) { best = k; break; }
+        }
+    }
+    if (best == 0) return 0;
+    return (uint8_t)(best | (v < 0.0f ? 8 : 0));
+}
+
+float orc_e2m1_value(uint8_t code)
+{
+    const float mag = kE2M1[code & 7];
+    return (code & 8) ? -mag : mag;
+}
+
+/* One 128-value vector to NVFP4: g = amax / (6 * 448); block b of 16 values takes the
+   E4M3 scale s_b = e4m3(amax_b / fl(6 g)); each value x becomes e2m1(x * fl(1 / fl(s_b g))).
+   A zero vector (or block) has zero scales and zero codes. */
+void orc_quant_nvfp4(const float *x, uint8_t *codes, uint8_t *bscale, float *gscale)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < ORC_D; i++) amax = fmaxf(amax, fabsf(x[i]));
+    const float g = amax / 2688.0f;
+    *gscale = g;
+    const float d = g * 6.0f;
+    for (int b = 0; b < ORC_D / 16; b++) {
+        float ab = 0.0f;
+        for (int i = 0; i < 16; i++) ab = fmaxf(ab, fabsf(x[16 * b + i]));
+        const uint8_t sb = d > 0.0f ? orc_e4m3_rn(ab / d) : 0;
+        bscale[b] = sb;
+        const float scale = orc_e4m3_value(sb) * g;
+        const float inv = scale > 0.0f ? 1.0f / scale : 0.0f;
+        for (int i = 0; i < 16; i++)
+            codes[16 * b + i] = scale > 0.0f ? orc_e2m1_rn(x[16 * b + i] * inv) : 0;
+    }
+}
+
+/* R12 score of an NVFP4 key: the exact dot of each block with the INT8 query, scaled by
+   the block's E4M3 scale in an fma chain over the blocks in order, then by g, s_q and C. */
+static float score_nvfp4(const uint8_t *codes, const uint8_t *bscale, float g, const int8_t *q8,
+                         float q_scale, float C)
+{
+    float acc = 0.0f;
+    for (int b = 0; b < ORC_D / 16; b++) {
+        double db = 0.0;
+        for (int i = 0; i < 16; i++) db += (double)orc_e2m1_value(codes[16 * b + i]) * (double)q8[16 * b + i];
+        acc = fmaf(orc_e4m3_value(bscale[b]), (float)db, acc);
+    }
+    return ((acc * g) * q_scale) * C;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Cache state                                                               */
 /* ------------------------------------------------------------------------ */
@@ -330,10 +432,15 @@ static void append_one(orc_cache *c, int slot, int pos, int head,
                        const float *k_rot, const float *v)
 {
     size_t mi = idx_main(c, slot, pos, head);
-    const int levels = c->kv8 ? 255 : 15;          /* R10: KV8 keeps 8-bit codes everywhere */
+    if (c->format == ORC_FMT_NVFP4) {               /* R12: NVFP4 codes and scales */
+        orc_quant_nvfp4(k_rot, c->k4_code + mi * ORC_D, c->k_bscale + mi * 8, c->k_gscale + mi);
+        orc_quant_nvfp4(v, c->v4_code + mi * ORC_D, c->v_bscale + mi * 8, c->v_gscale + mi);
+        return;
+    }
+    const int levels = c->format == ORC_FMT_KV8 ? 255 : 15;   /* R10: KV8 keeps 8-bit codes */
     orc_quant_affine(k_rot, ORC_D, levels, c->k4_code + mi * ORC_D, c->k4_delta + mi, c->k4_min + mi);
     orc_quant_affine(v, ORC_D, levels, c->v4_code + mi * ORC_D, c->v4_delta + mi, c->v4_min + mi);
-    if (c->kv8) return;
+    if (c->format == ORC_FMT_KV8) return;
 
     /* Side buffer: an INT8 copy of a sink position and of the position in the
        recent ring. [ko] 전제와 한계; [zh] 方法步骤详情 step 3. */
@@ -355,7 +462,7 @@ int orc_append(orc_cache *c, int slot, int start, int T,
 {
     if (slot < 0 || slot >= c->num_slots || start < 0 || T < 0 || start + T > c->max_len)
         return -1;
-    if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
+    if (c->format != ORC_FMT_HYBRID && (c->sink != 0 || c->window != 0)) return -1;
     if (c->rope && start + T > c->rope_max_pos) return -1;
     float kx[ORC_D], kp[ORC_D], kr[ORC_D], vx[ORC_D];
     for (int t = 0; t < T; t++) {
@@ -425,7 +532,7 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
     const int s = c->sink, w = c->window, P = 16;
     /* Regions, reading R4 (R10: no INT4 region in KV8). */
     int r4_lo = s, r4_hi = L - w;
-    if (r4_hi < r4_lo || c->kv8) r4_hi = r4_lo;      /* empty */
+    if (r4_hi < r4_lo || c->format != ORC_FMT_HYBRID) r4_hi = r4_lo;   /* empty */
 
     /* ---- INT4 region: integer QK, page-local integer PV (reading R5) ---- */
     double M4 = -INFINITY, l4 = 0.0;
@@ -512,17 +619,19 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
        product takes p rounded to BF16 (integer mode) or unrounded (float mode);
        the normaliser sums the unrounded p. KV8 (R10): the same over every
        position, groups of 16 consecutive positions, codes from the main arrays. ---- */
-    const uint8_t *k8c = c->kv8 ? c->k4_code : c->k8_code;
-    const uint8_t *v8c = c->kv8 ? c->v4_code : c->v8_code;
-    const uint16_t *k8d = c->kv8 ? c->k4_delta : c->k8_delta;
-    const uint16_t *k8m = c->kv8 ? c->k4_min : c->k8_min;
-    const uint16_t *v8d = c->kv8 ? c->v4_delta : c->v8_delta;
-    const uint16_t *v8m = c->kv8 ? c->v4_min : c->v8_min;
+    const int is8 = c->format != ORC_FMT_HYBRID;     /* KV8 and NVFP4: every position, in pages */
+    const int isf4 = c->format == ORC_FMT_NVFP4;
+    const uint8_t *k8c = is8 ? c->k4_code : c->k8_code;
+    const uint8_t *v8c = is8 ? c->v4_code : c->v8_code;
+    const uint16_t *k8d = is8 ? c->k4_delta : c->k8_delta;
+    const uint16_t *k8m = is8 ? c->k4_min : c->k8_min;
+    const uint16_t *v8d = is8 ? c->v4_delta : c->v8_delta;
+    const uint16_t *v8m = is8 ? c->v4_min : c->v8_min;
     float Mr = -INFINITY;
     double lp_ = 0.0;
     double opr[ORC_D];
     for (int j = 0; j < ORC_D; j++) opr[j] = 0.0;
-    const int S = c->kv8 ? L : s + w;               /* rows: side rows, or positions in KV8 */
+    const int S = is8 ? L : s + w;               /* rows: side rows, or positions in KV8 */
     for (int g0 = 0; g0 < S; g0 += 16) {
         const int n = (S - g0 < 16) ? S - g0 : 16;
         int pos[16];
@@ -530,10 +639,17 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         float sg[16];
         float Mg = -INFINITY;
         for (int i = 0; i < n; i++) {
-            pos[i] = c->kv8 ? g0 + i : side_row_position(g0 + i, s, w, L);
+            pos[i] = is8 ? g0 + i : side_row_position(g0 + i, s, w, L);
             if (pos[i] < 0) continue;
-            const size_t si = c->kv8 ? idx_main(c, slot, g0 + i, head) : idx_side(c, slot, g0 + i, head);
+            const size_t si = is8 ? idx_main(c, slot, g0 + i, head) : idx_side(c, slot, g0 + i, head);
             rix[i] = si;
+            if (isf4) {                              /* R12 */
+                sg[i] = score_nvfp4(k8c + si * ORC_D, c->k_bscale + si * 8, c->k_gscale[si], q8,
+                                    q_scale, C);
+                if (dbg_sigma) dbg_sigma[pos[i]] = sg[i];
+                if (sg[i] > Mg) Mg = sg[i];
+                continue;
+            }
             int32_t dot = dot_s8_u8(q8, k8c + si * ORC_D);
             sg[i] = score_from_dot(dot, k8d[si], k8m[si], q_scale, q_sum, C);
             if (dbg_qk) dbg_qk[pos[i]] = dot;
@@ -553,12 +669,20 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
             const double pw = (pv_mode == ORC_PV_FLOAT)
                                   ? (double)p
                                   : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
-            float dv = (float)orc_f16_to_f64(v8d[si]);
-            float mv = (float)orc_f16_to_f64(v8m[si]);
             const uint8_t *vc = v8c + si * ORC_D;
-            for (int j = 0; j < ORC_D; j++) {
-                float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
-                og[j] += pw * (double)v;
+            if (isf4) {                              /* R12: v = bf16(e2m1(c) * fl(s_b g)) */
+                for (int j = 0; j < ORC_D; j++) {
+                    const float scale = orc_e4m3_value(c->v_bscale[si * 8 + j / 16]) * c->v_gscale[si];
+                    const float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(orc_e2m1_value(vc[j]) * scale));
+                    og[j] += pw * (double)v;
+                }
+            } else {
+                float dv = (float)orc_f16_to_f64(v8d[si]);
+                float mv = (float)orc_f16_to_f64(v8m[si]);
+                for (int j = 0; j < ORC_D; j++) {
+                    float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(fmaf(dv, (float)vc[j], mv)));
+                    og[j] += pw * (double)v;
+                }
             }
             lg += (double)p;
         }
@@ -600,7 +724,7 @@ int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf1
     if (slot < 0 || slot >= c->num_slots || L < 0 || L > c->max_len || G <= 0)
         return -1;
     if (c->sink + c->window > 256) return -1;
-    if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
+    if (c->format != ORC_FMT_HYBRID && (c->sink != 0 || c->window != 0)) return -1;
     if (c->rope && L > c->rope_max_pos) return -1;
     const float C = log2e_scale(sm_scale);
     const int HG = c->num_heads * G;
@@ -655,7 +779,7 @@ int orc_decode_batch(const orc_cache *c, int B, const int32_t *slots, const int3
             (c->rope && lens[b] > c->rope_max_pos))
             return -1;
     if (G <= 0 || c->sink + c->window > 256) return -1;
-    if (c->kv8 && (c->sink != 0 || c->window != 0)) return -1;
+    if (c->format != ORC_FMT_HYBRID && (c->sink != 0 || c->window != 0)) return -1;
     const long n = (long)B * HG;
 #ifdef _OPENMP
     if (num_threads > 0) omp_set_num_threads(num_threads);

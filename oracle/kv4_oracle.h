@@ -26,6 +26,8 @@ extern "C" {
 
 /* FP16 rounding modes for orc_f32_to_f16. */
 enum { ORC_RN = 0, ORC_RD = 1, ORC_RU = 2 };
+/* Cache formats. */
+enum { ORC_FMT_HYBRID = 0, ORC_FMT_KV8 = 1, ORC_FMT_NVFP4 = 2 };
 /* PV modes for the INT4 region of orc_decode. */
 enum { ORC_PV_INTEGER = 0, ORC_PV_FLOAT = 1 };
 
@@ -35,8 +37,10 @@ typedef struct {
     int32_t window;      /* w */
     int32_t max_len;     /* positions per slot */
     int32_t num_slots;
-    int32_t kv8;         /* 0: INT4 main cache + INT8 side buffer; 1: whole-cache INT8 (KV8),
-                            where the main arrays hold 8-bit codes and sink = window = 0 */
+    int32_t format;      /* ORC_FMT_HYBRID: INT4 main cache + INT8 side buffer; ORC_FMT_KV8:
+                            whole-cache INT8 (the main arrays hold 8-bit codes); ORC_FMT_NVFP4:
+                            whole-cache NVFP4 (E2M1 codes in the main arrays, block and vector
+                            scales below); the last two have sink = window = 0 */
     /* INT4 main cache: codes [slot][pos][head][128] in 0..15 (0..255 in KV8), meta
        [slot][pos][head] fp16 bits */
     uint8_t  *k4_code, *v4_code;
@@ -51,6 +55,10 @@ typedef struct {
        its sin at [p][64 + i] (i < 64). */
     const float *rope;
     int32_t  rope_max_pos;
+    /* NVFP4 scales (reading R12): E4M3 bits of the 8 block scales [slot][pos][head][8] and
+       the FP32 vector scale [slot][pos][head], for K and V */
+    uint8_t  *k_bscale, *v_bscale;
+    float    *k_gscale, *v_gscale;
 } orc_cache;
 
 /* Optional per-call debug record of orc_decode (any pointer may be NULL).
@@ -77,6 +85,11 @@ void orc_rope128(const float *in, const float *cos_sin_row, float *out);
 void orc_quant_affine(const float *x, int n, int levels,
                       uint8_t *code, uint16_t *delta_h, uint16_t *min_h);
 void orc_quant_query(const float *q_rot, int8_t *q8, float *q_scale, int32_t *q_sum);
+uint8_t orc_e4m3_rn(float t);               /* t >= 0, round to nearest even, saturating at 448 */
+float   orc_e4m3_value(uint8_t bits);
+uint8_t orc_e2m1_rn(float v);               /* sign | magnitude code, nearest even, saturating at 6 */
+float   orc_e2m1_value(uint8_t code);
+void    orc_quant_nvfp4(const float *x, uint8_t *codes, uint8_t *bscale, float *gscale);
 
 /* whole path */
 int orc_append(orc_cache *c, int slot, int start, int T,

@@ -32,6 +32,15 @@ def load():
         lib.orc_exp2f.restype = C.c_float
         lib.orc_fwht128.argtypes = [P, P]
         lib.orc_rope128.argtypes = [P, P, P]
+        lib.orc_e4m3_rn.argtypes = [C.c_float]
+        lib.orc_e4m3_rn.restype = C.c_uint8
+        lib.orc_e4m3_value.argtypes = [C.c_uint8]
+        lib.orc_e4m3_value.restype = C.c_float
+        lib.orc_e2m1_rn.argtypes = [C.c_float]
+        lib.orc_e2m1_rn.restype = C.c_uint8
+        lib.orc_e2m1_value.argtypes = [C.c_uint8]
+        lib.orc_e2m1_value.restype = C.c_float
+        lib.orc_quant_nvfp4.argtypes = [P, P, P, P]
         lib.orc_quant_affine.argtypes = [P, C.c_int, C.c_int, P, P, P]
         lib.orc_quant_query.argtypes = [P, P, P, P]
         lib.orc_append.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
@@ -113,6 +122,35 @@ def rope128(x, cos_sin_row):
     return out
 
 
+def e4m3_rn(t):
+    """E4M3 bits of t >= 0 (nearest, ties even, held at 448)."""
+    return int(load().orc_e4m3_rn(C.c_float(t)))
+
+
+def e4m3_value(bits):
+    return float(load().orc_e4m3_value(C.c_uint8(bits)))
+
+
+def e2m1_rn(v):
+    """E2M1 code (sign in bit 3) of v (nearest, ties to the even code, held at 6)."""
+    return int(load().orc_e2m1_rn(C.c_float(v)))
+
+
+def e2m1_value(code):
+    return float(load().orc_e2m1_value(C.c_uint8(code)))
+
+
+def quant_nvfp4(x):
+    """(codes uint8[128], block scales uint8[8] E4M3 bits, vector scale float32)."""
+    x = _c(x, np.float32)
+    assert x.shape == (D,)
+    codes = np.empty(D, np.uint8)
+    bs = np.empty(8, np.uint8)
+    g = np.zeros(1, np.float32)
+    load().orc_quant_nvfp4(_p(x), _p(codes), _p(bs), _p(g))
+    return codes, bs, np.float32(g[0])
+
+
 def quant_affine(x, levels):
     """Returns (codes uint8[n], delta fp16 bits, min fp16 bits)."""
     x = _c(x, np.float32)
@@ -145,9 +183,10 @@ _STATE_ARRAYS = ("k4_code", "v4_code", "k4_delta", "k4_min", "v4_delta", "v4_min
 
 class _State(C.Structure):
     _fields_ = [("num_heads", C.c_int32), ("sink", C.c_int32), ("window", C.c_int32),
-                ("max_len", C.c_int32), ("num_slots", C.c_int32), ("kv8", C.c_int32)] + \
+                ("max_len", C.c_int32), ("num_slots", C.c_int32), ("format", C.c_int32)] + \
                [(n, C.c_void_p) for n in _STATE_ARRAYS] + \
-               [("rope", C.c_void_p), ("rope_max_pos", C.c_int32)]
+               [("rope", C.c_void_p), ("rope_max_pos", C.c_int32)] + \
+               [(n, C.c_void_p) for n in ("k_bscale", "v_bscale", "k_gscale", "v_gscale")]
 
 
 class _Debug(C.Structure):
@@ -160,11 +199,14 @@ class OracleCache:
     kv8=True, the whole-cache 8-bit configuration (reading R10): 8-bit codes for
     every position, no side buffer (sink = window = 0)."""
 
-    def __init__(self, num_heads, sink, window, max_len, num_slots=1, kv8=False, rope=None):
-        if kv8 and (sink or window):
-            raise ValueError("the KV8 configuration has no protected region")
+    def __init__(self, num_heads, sink, window, max_len, num_slots=1, kv8=False, rope=None,
+                 nvfp4=False):
+        if (kv8 or nvfp4) and (sink or window):
+            raise ValueError("the KV8 and NVFP4 configurations have no protected region")
         H, S = num_heads, sink + window
         self.kv8 = bool(kv8)
+        self.nvfp4 = bool(nvfp4)
+        self.format = 2 if nvfp4 else (1 if kv8 else 0)
         self.H, self.s, self.w, self.max_len, self.num_slots = H, sink, window, max_len, num_slots
         z = np.zeros
         self.k4_code = z((num_slots, max_len, H, D), np.uint8)
@@ -180,7 +222,14 @@ class OracleCache:
         self.v8_delta = z((num_slots, S, H), np.uint16)
         self.v8_min = z((num_slots, S, H), np.uint16)
         self.length = z((num_slots,), np.int32)
-        st = _State(H, sink, window, max_len, num_slots, int(self.kv8))
+        # reading R12 (NVFP4): E4M3 block scales and the FP32 vector scale per token-head
+        self.k_bscale = z((num_slots, max_len, H, 8), np.uint8)
+        self.v_bscale = z((num_slots, max_len, H, 8), np.uint8)
+        self.k_gscale = z((num_slots, max_len, H), np.float32)
+        self.v_gscale = z((num_slots, max_len, H), np.float32)
+        st = _State(H, sink, window, max_len, num_slots, self.format)
+        for n in ("k_bscale", "v_bscale", "k_gscale", "v_gscale"):
+            setattr(st, n, getattr(self, n).ctypes.data)
         for n in _STATE_ARRAYS:
             setattr(st, n, getattr(self, n).ctypes.data)
         # reading R11: with a RoPE table [max_pos][128] (cos at [p][i], sin at [p][64+i]),
