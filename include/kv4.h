@@ -63,7 +63,9 @@ typedef enum {
  * buffer for every position, in pages, and no side buffer (sink = window = 0). */
 typedef enum {
     KV4_FORMAT_INT4_HYBRID = 0,
-    KV4_FORMAT_INT8 = 1
+    KV4_FORMAT_INT8 = 1,
+    KV4_FORMAT_NVFP4 = 2      /* NVFP4 for every position (E2M1 values, E4M3 scales per 16
+                                 dims, an FP32 scale per token-head vector), no side buffer */
 } kv4_format;
 
 typedef struct {
@@ -78,7 +80,8 @@ typedef struct {
     int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
     int32_t max_work_items;  /* ignored (kept for layout stability): the decode workspace is sized
                                 from max_batch, max_q_heads and the device's SM count */
-    int32_t format;          /* kv4_format; KV4_FORMAT_INT8 requires sink = window = 0 */
+    int32_t format;          /* kv4_format; KV4_FORMAT_INT8 and KV4_FORMAT_NVFP4 require
+                                sink = window = 0 */
 } kv4_cache_config;
 
 /*
@@ -112,12 +115,23 @@ typedef struct {
  * KV4_FORMAT_INT8 pages: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES_INT8 = 4352
  * bytes, block (p, h) at (p * H_kv + h) * 4352, each laid out as one side group
  * above with row r = t, the page's token slot t; there is no side pool.
+ * KV4_FORMAT_NVFP4 pages: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES_NVFP4 = 2432 bytes,
+ * block (p, h) at (p * H_kv + h) * 2432: a K half at 0 and a V half at 1216, each with
+ *   [0, 1024)    E2M1 codes (sign in bit 3; dim d in the low nibble of its byte when d is
+ *                the lower dim of the byte's pair), one byte per (token, dim pair):
+ *                K: dims (2j, 2j+1) of token t, j = 8b + jj (block b, jj < 8), at
+ *                   16*(32*(b/4) + 4*(t%8) + jj%4) + 4*(b%4) + t/8 + 2*(jj/4)
+ *                V: dims (d, d+8) of token t, d = 16m + g (g < 8), at
+ *                   16*(32*(m/4) + 4*g + t%4) + 4*(m%4) + {0,2,1,3}[t/4]
+ *   [1024, 1152) E4M3 block scales, byte 8*t + b (block b = dims 16b .. 16b+15)
+ *   [1152, 1216) FP32 vector scales, float t
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128
 #define KV4_PAGE_SIZE 16
 #define KV4_PAGE_BLOCK_BYTES 2176
 #define KV4_PAGE_BLOCK_BYTES_INT8 4352
+#define KV4_PAGE_BLOCK_BYTES_NVFP4 2432
 
 typedef struct {
     void   *page_pool_dev;   size_t page_pool_bytes;
@@ -169,7 +183,10 @@ kv4_status kv4_cache_set_rope(kv4_cache *cache, const float *cos_sin_dev, int ma
  * position p >= L_new - w (L_new = start_pos[i] + its token count) gets an
  * 8-bit copy in ring row s + p mod w. The slot's length becomes L_new.
  * KV4_FORMAT_INT8 caches store the 8-bit codes (n = 255, same rounding) of
- * rotated K and V for every position in row pos%16 of the page's block instead.
+ * rotated K and V for every position in row pos%16 of the page's block instead;
+ * KV4_FORMAT_NVFP4 caches store the NVFP4 codes and scales of rotated K and V:
+ * g = amax / 2688, s_b = e4m3(amax_b / fl(6 g)), code = e2m1(x * fl(1 / fl(s_b g)))
+ * (nearest, ties to even, saturating).
  *   k_bf16_dev, v_bf16_dev : [total_tokens][H_kv][128] bf16, tokens of sequence i
  *                            at rows cu_tokens[i] .. cu_tokens[i+1]-1
  *   cu_tokens_dev          : [n_seqs+1] int32, non-decreasing, cu[0] = 0, cu[n] = total_tokens
@@ -198,6 +215,9 @@ kv4_status kv4_append(kv4_cache *cache, const void *k_bf16_dev, const void *v_bf
  *   split-K partials over pages likewise.
  *   KV4_FORMAT_INT8 caches: every position takes the protected region's arithmetic
  *   (INT8 keys, bf16 values, FP32 PV) from its page, 16 positions per group.
+ *   KV4_FORMAT_NVFP4 caches: the same q8 against the E2M1 keys, block dots exact and
+ *   scaled after the dot (fma chain over the blocks), values bf16(e2m1 * fl(s_b g)),
+ *   bf16 weights, FP32 PV, 16 positions per group.
  *   q_bf16_dev       : [batch][num_q_heads][128] bf16 (post-RoPE, unrotated)
  *   slot_ids_dev     : [batch] int32
  *   context_lens_dev : [batch] int32 L_b, including the token appended this step;
@@ -295,7 +315,8 @@ kv4_status kv4_linear_bf16(const void *x_dev, const void *w_dev, void *y_dev, in
  *   q_out_dev : [total_tokens][num_q_heads][128] bf16 projected queries (pre-RoPE)
  *   d_model   : a multiple of 64; num_q_heads * 128 a multiple of 256
  *   other arguments: as kv4_append (the token order of x is the order of cu_tokens)
- * Errors: as kv4_append, and KV4_ERR_INVALID_ARG for the sizes above.
+ * Errors: as kv4_append, KV4_ERR_INVALID_ARG for the sizes above, KV4_ERR_UNSUPPORTED for a
+ * KV4_FORMAT_NVFP4 cache (append the projection's rows with kv4_append there).
  */
 kv4_status kv4_qkv_append(kv4_cache *cache, const void *x_dev, const void *w_qkv_dev, int num_q_heads,
                           int d_model, void *q_out_dev, const int32_t *cu_tokens_dev,

@@ -101,9 +101,10 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
         return KV4_ERR_INVALID_ARG;
     if (cfg->head_dim != KV4_HEAD_DIM || cfg->page_size != KV4_PAGE_SIZE) return KV4_ERR_UNSUPPORTED;
     if (cfg->sink + cfg->window > kv4::kMaxProtected) return KV4_ERR_UNSUPPORTED;
-    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8) return KV4_ERR_INVALID_ARG;
-    const bool kv8 = cfg->format == KV4_FORMAT_INT8;
-    if (kv8 && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
+    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8 && cfg->format != KV4_FORMAT_NVFP4)
+        return KV4_ERR_INVALID_ARG;
+    const bool kv8 = cfg->format == KV4_FORMAT_INT8, fp4 = cfg->format == KV4_FORMAT_NVFP4;
+    if ((kv8 || fp4) && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
     if (cfg->max_q_heads % cfg->num_kv_heads != 0) return KV4_ERR_INVALID_ARG;
     const int gmax = cfg->max_q_heads / cfg->num_kv_heads;
     if (gmax > 4) return KV4_ERR_UNSUPPORTED;
@@ -127,7 +128,8 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
     const int H = cfg->num_kv_heads;
     const int S = cfg->sink + cfg->window;
     c->side_block = (size_t)((S + 15) / 16) * kv4::kSideGroupBytes;
-    c->pages_bytes = (size_t)cfg->num_pages * H * (kv8 ? kv4::kPageBlock8 : kv4::kPageBlock);
+    c->pages_bytes = (size_t)cfg->num_pages * H *
+                     (fp4 ? kv4::kPageBlock4f : kv8 ? kv4::kPageBlock8 : kv4::kPageBlock);
     c->side_bytes = (size_t)cfg->max_slots * H * c->side_block;
     int grid_max = 0;
     for (int g = 1; g <= 4; g <<= 1) grid_max = std::max(grid_max, c->grid[g]);
@@ -218,7 +220,8 @@ kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t*
     a.side_block_bytes = (int64_t)c->side_block;
     a.seq_len = c->seq_len;
     a.err = c->err;
-    a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
+    a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
+    a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
     a.rope = c->rope;
     a.rope_max_pos = c->rope_max_pos;
     return check_launch(kv4::launch_append(a, static_cast<cudaStream_t>(stream)));
@@ -242,6 +245,7 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     if (!group_supported(G)) return KV4_ERR_UNSUPPORTED;
     if (batch > c->cfg.max_batch || num_q_heads > c->cfg.max_q_heads) return KV4_ERR_OUT_OF_RANGE;
     if ((dqk || dw) && dbg_stride < 1) return KV4_ERR_INVALID_ARG;
+    if (c->cfg.format == KV4_FORMAT_NVFP4) return KV4_ERR_UNSUPPORTED;
     kv4::DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.slot_ids = slot_ids;
@@ -278,7 +282,8 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.dbg_qk = dqk;
     a.dbg_w = dw;
     a.dbg_stride = dbg_stride;
-    a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
+    a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
+    a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
     a.rope = c->rope;
     a.rope_max_pos = c->rope_max_pos;
     cudaEvent_t* ev = nullptr;
@@ -354,6 +359,7 @@ kv4_status kv4_qkv_append(kv4_cache* c, const void* x, const void* w, int num_q_
     if (!x || !w || !q_out || !cu_tokens || !slot_ids || !start_pos || !block_table || stride < 1)
         return KV4_ERR_INVALID_ARG;
     if (d_model % 64 != 0 || (num_q_heads * KV4_HEAD_DIM) % 256 != 0) return KV4_ERR_INVALID_ARG;
+    if (c->cfg.format == KV4_FORMAT_NVFP4) return KV4_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(q_out)) &
         15)
         return KV4_ERR_INVALID_ARG;
@@ -376,7 +382,8 @@ kv4_status kv4_qkv_append(kv4_cache* c, const void* x, const void* w, int num_q_
     a.side_block_bytes = (int64_t)c->side_block;
     a.seq_len = c->seq_len;
     a.err = c->err;
-    a.kv8 = c->cfg.format == KV4_FORMAT_INT8;
+    a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
+    a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
     a.rope = c->rope;
     a.rope_max_pos = c->rope_max_pos;
     return check_launch(

@@ -172,6 +172,96 @@ __device__ __forceinline__ void append_v(const AppendArgs& a, float (&vx)[4], ui
     }
 }
 
+// ---- NVFP4 (E2M1 values, an E4M3 scale per 16 dims, an FP32 scale per vector)
+// E4M3 bits of t >= 0: nearest value, ties to the even mantissa, held at 448 (0x7E).
+// Quantum 2^(e-3) for exponent e = floor(log2 t) >= -6, 2^-9 below (subnormals).
+__device__ __forceinline__ uint32_t e4m3_rn(float t)
+{
+    if (!(t > 0.0f)) return 0u;
+    if (t >= 448.0f) return 0x7Eu;
+    const int e = max(-6, (int)((__float_as_uint(t) >> 23) & 0xffu) - 127);
+    const float m = rintf(__fmul_rn(t, __uint_as_float((uint32_t)(127 + 3 - e) << 23)));   // t / 2^(e-3)
+    const float v = __fmul_rn(m, __uint_as_float((uint32_t)(127 - 3 + e) << 23));
+    if (v >= 448.0f) return 0x7Eu;
+    if (v == 0.0f) return 0u;
+    if (v < 0x1p-6f) return (uint32_t)__float2int_rn(__fmul_rn(v, 512.0f));             // E = 0
+    const int ev = (int)((__float_as_uint(v) >> 23) & 0xffu) - 127;
+    const int mant = __float2int_rn(__fmul_rn(v, __uint_as_float((uint32_t)(127 + 3 - ev) << 23))) - 8;
+    return (uint32_t)(((ev + 7) << 3) | mant);
+}
+__device__ __forceinline__ float e4m3_value(uint32_t bits)
+{
+    const int E = (bits >> 3) & 15, m = bits & 7;
+    return E == 0 ? __fmul_rn((float)m, 0x1p-9f)
+                  : __fmul_rn((float)(8 + m), __uint_as_float((uint32_t)(127 - 10 + E) << 23));
+}
+// E2M1 code of v: magnitude code (0, 0.5, 1, 1.5, 2, 3, 4, 6) nearest with ties to the
+// even code, held at 6, sign in bit 3; a zero magnitude is code 0.
+__device__ __forceinline__ uint32_t e2m1_rn(float v)
+{
+    const float a = fabsf(v);
+    uint32_t k;
+    if (a <= 0.25f) k = 0;
+    else if (a < 0.75f) k = 1;
+    else if (a <= 1.25f) k = 2;
+    else if (a < 1.75f) k = 3;
+    else if (a <= 2.5f) k = 4;
+    else if (a < 3.5f) k = 5;
+    else if (a <= 5.0f) k = 6;
+    else k = 7;
+    return k == 0 ? 0u : (k | (v < 0.0f ? 8u : 0u));
+}
+// The warp's 128 values (4 per lane: dims 4l .. 4l+3) to NVFP4: the lane's codes, its
+// block's E4M3 scale bits (lanes 4b .. 4b+3 hold block b) and the vector scale g.
+__device__ __forceinline__ void warp_quant_nvfp4(const float (&x)[4], uint32_t (&c)[4], uint32_t& sb,
+                                                 float& g)
+{
+    float la = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    const float amax = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(la)));
+    g = __fdiv_rn(amax, 2688.0f);
+    const float d = __fmul_rn(g, 6.0f);
+    la = fmaxf(la, __shfl_xor_sync(kFull, la, 1));
+    la = fmaxf(la, __shfl_xor_sync(kFull, la, 2));              // the block's max |x|
+    sb = d > 0.0f ? e4m3_rn(__fdiv_rn(la, d)) : 0u;
+    const float scale = __fmul_rn(e4m3_value(sb), g);
+    const float inv = scale > 0.0f ? __frcp_rn(scale) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = scale > 0.0f ? e2m1_rn(__fmul_rn(x[i], inv)) : 0u;
+}
+// One token-head in an NVFP4 page block: the K half (codes in the QK fragment order) or
+// the V half (codes in the PV fragment order), its block scales and vector scale.
+__device__ __forceinline__ void store_nvfp4_k(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t sb, float g,
+                                              int lane)
+{
+    const int b = lane >> 2;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {                                // dim pairs j = 2l + e
+        const int jj = 2 * (lane & 3) + e;                       // pair within the block
+        half[16 * (32 * (b >> 2) + 4 * (ts & 7) + (jj & 3)) + 4 * (b & 3) + (ts >> 3) + 2 * (jj >> 2)] =
+            (uint8_t)(c[2 * e] | (c[2 * e + 1] << 4));
+    }
+    if ((lane & 3) == 0) half[kFp4ScaleOff + 8 * ts + b] = (uint8_t)sb;
+    if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 4 * ts) = g;
+}
+__device__ __forceinline__ void store_nvfp4_v(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t sb, float g,
+                                              int lane)
+{
+    const int m = lane >> 2;
+    uint32_t hi[4];                                              // dims + 8, from lane l ^ 2
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hi[i] = __shfl_xor_sync(kFull, c[i], 2);
+    const int q4 = ts >> 2, kb = ((q4 & 1) << 1) | (q4 >> 1);     // tokens t, t+8, t+4, t+12 -> bytes 0..3
+    if ((lane & 2) == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gq = 4 * (lane & 3) + i;                   // dim 16m + gq, gq < 8
+            half[16 * (32 * (m >> 2) + 4 * gq + (ts & 3)) + 4 * (m & 3) + kb] = (uint8_t)(c[i] | (hi[i] << 4));
+        }
+    }
+    if ((lane & 3) == 0) half[kFp4ScaleOff + 8 * ts + m] = (uint8_t)sb;
+    if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 4 * ts) = g;
+}
+
 // Where token tok of an append goes: its sequence entry i (cu_tokens[i] <= tok <
 // cu_tokens[i+1]), slot, position, the sequence's length after the append and the
 // page of the position. False, with the error reported, when an input is invalid.

@@ -1466,8 +1466,9 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
         cfg->max_slots < 1)
         return KV4_ERR_INVALID_ARG;
     if (cfg->sink + cfg->window > kMaxProtected || cfg->num_pages > INT32_MAX) return KV4_ERR_UNSUPPORTED;
-    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8) return KV4_ERR_INVALID_ARG;
-    const bool kv8 = cfg->format == KV4_FORMAT_INT8;
+    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8 && cfg->format != KV4_FORMAT_NVFP4)
+        return KV4_ERR_INVALID_ARG;
+    const bool kv8 = cfg->format != KV4_FORMAT_INT4_HYBRID;
     if (kv8 && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
     if (batch == 0) return KV4_OK;
     if (!page_pool_dev || (!side_pool_dev && !kv8) || !seq_len_dev || !q_bf16_dev || !slot_ids_dev ||
@@ -1525,6 +1526,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.out = out_dev;
     a.lse = lse_dev;
     a.kv8 = kv8;
+    a.fp4 = cfg->format == KV4_FORMAT_NVFP4;
     const cudaError_t e = launch_decode(a, d->grid[G], static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
 }

@@ -30,6 +30,12 @@ constexpr int kSideVCodeOff = kPageBlock;
 constexpr int kSideVMetaOff = kPageBlock + 2048;
 // A page block of the whole-cache 8-bit format: one side group, row r = token slot r.
 constexpr int kPageBlock8 = kSideGroupBytes;
+// A page block of the NVFP4 format: a K half and a V half of kFp4Half bytes each (codes
+// in MMA-fragment order, E4M3 block scales, FP32 vector scales).
+constexpr int kFp4Half = 1216;
+constexpr int kPageBlock4f = 2 * kFp4Half;
+constexpr int kFp4ScaleOff = 1024;
+constexpr int kFp4GlobalOff = 1152;
 constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per SM
 constexpr int kStages = 5;               // page stages per warp
 // Cost-line positions charged to every (sequence, KV head) unit beyond its stage
@@ -75,7 +81,8 @@ struct AppendArgs {
     int64_t side_block_bytes;
     int32_t* seq_len;
     int32_t* err;
-    int32_t kv8;                  // KV4_FORMAT_INT8: 8-bit codes in pages of kPageBlock8 bytes
+    int32_t kv8;                  // KV4_FORMAT_INT8 or NVFP4: the whole cache in pages, no side buffer
+    int32_t fp4;                  // KV4_FORMAT_NVFP4: pages of kPageBlock4f bytes
     const float* rope;            // [rope_max_pos][128] cos | sin, or null (keys are post-RoPE)
     int32_t rope_max_pos;
 };
@@ -116,7 +123,8 @@ struct DecodeArgs {
     int32_t* dbg_qk;
     uint8_t* dbg_w;
     int32_t dbg_stride;
-    int32_t kv8;                  // KV4_FORMAT_INT8: every position a protected row of its page
+    int32_t kv8;                  // KV4_FORMAT_INT8 or NVFP4: every position a row of a page group
+    int32_t fp4;                  // KV4_FORMAT_NVFP4
     const float* rope;            // [rope_max_pos][128] cos | sin, or null (queries are post-RoPE)
     int32_t rope_max_pos;
 };
