@@ -57,13 +57,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
-    ap.add_argument("--format", choices=["int4-hybrid", "int8"], default="int4-hybrid",
+    ap.add_argument("--format", choices=["int4-hybrid", "int8", "nvfp4"], default="int4-hybrid",
                     help="cache format of the main measurement: the method (INT4 pages + INT8 "
-                         "side buffer) or the whole-cache 8-bit format (KV8, s = w = 0)")
+                         "side buffer), the whole-cache 8-bit format (KV8, s = w = 0) or the "
+                         "whole-cache NVFP4 format (s = w = 0)")
     ap.add_argument("--no-qkv", action="store_true",
                     help="skip the fused projection + append measurement")
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the unprotected KV4 (s = w = 0) and whole-cache 8-bit measurements")
+                    help="skip the unprotected KV4 (s = w = 0), whole-cache 8-bit and NVFP4 measurements")
     return ap.parse_args()
 
 
@@ -193,9 +194,11 @@ def workload_from_args(args):
     format has none)."""
     import dataclasses
     wl = inputs.workload(args.workload)
-    if getattr(args, "format", "int4-hybrid") == "int8":
+    fmt = getattr(args, "format", "int4-hybrid")
+    if fmt in ("int8", "nvfp4"):
+        what = "8-bit" if fmt == "int8" else "NVFP4"
         return dataclasses.replace(wl, sink=0, window=0,
-                                   name=wl.name + " (whole-cache 8-bit format)")
+                                   name=wl.name + f" (whole-cache {what} format)")
     if args.sink is not None or args.window is not None:
         s = wl.sink if args.sink is None else args.sink
         w = wl.window if args.window is None else args.window
@@ -238,7 +241,7 @@ def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
                 slots=slots, lens=lens, num_pages=num_pages)
 
 
-def oracle_sample(wl, st, cpu_seconds, threads, kv8=False):
+def oracle_sample(wl, st, cpu_seconds, threads, kv8=False, nvfp4=False):
     """Time the CPU oracle's decode over a bounded sample of the workload's sequences
     (the same inputs as the GPU run). Returns the cpu_baseline dict."""
     import oracle
@@ -247,7 +250,8 @@ def oracle_sample(wl, st, cpu_seconds, threads, kv8=False):
     pick = list(range(len(st["host_kv"])))
     H, G = wl.num_kv_heads, wl.group
     maxL = max(lens[b] for b in pick)
-    oc = oracle.OracleCache(H, wl.sink, wl.window, maxL, num_slots=len(pick), kv8=kv8)
+    oc = oracle.OracleCache(H, wl.sink, wl.window, maxL, num_slots=len(pick), kv8=kv8,
+                            nvfp4=nvfp4)
     for i, b in enumerate(pick):
         oc.append(i, 0, st["host_kv"][b][0], st["host_kv"][b][1])
     qb = inputs.bf16_bits(st["q"][pick])
@@ -278,11 +282,12 @@ def run_kv4(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workload_from_args(args)
-    kv8 = args.format == "int8"
+    kv8, fp4 = args.format == "int8", args.format == "nvfp4"
     seed = wl.seed + rank
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     st = build_workload(wl, seed, dev, sample_seqs=8 if want_cpu else 0,
-                        fmt=kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_INT4_HYBRID)
+                        fmt=(kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_NVFP4 if fp4
+                             else kv4.FORMAT_INT4_HYBRID))
     cache = st["cache"]
     B, Hq, H = wl.batch, wl.num_q_heads, wl.num_kv_heads
     lens = st["lens"]
@@ -334,6 +339,8 @@ def run_kv4(args, rank, world, local):
 
     if kv8:
         call_bytes = bytes_model.decode_call_bytes_kv8(lens, Hq, H, with_lse=True)
+    elif fp4:
+        call_bytes = bytes_model.decode_call_bytes_nvfp4(lens, Hq, H, with_lse=True)
     else:
         call_bytes = bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
     # the split kernel reads 144-byte query records (written by the prep kernel) instead
@@ -342,7 +349,7 @@ def run_kv4(args, rank, world, local):
     split_ms = prof["split_ms"] / max(1, prof["calls"])
     peak, peak_src = measured_peaks()
     achieved = split_bytes / (split_ms * 1e-3) / 1e9
-    traffic = None if kv8 else split_kernel_traffic()
+    traffic = None if (kv8 or fp4) else split_kernel_traffic()
     step_gbs = call_bytes * layers / (ms / args.steps * 1e-3) / 1e9
 
     res = {
@@ -378,14 +385,16 @@ def run_kv4(args, rank, world, local):
         res["append_stress"] = run_append_stress(dev, peak)
 
     # ---- the attention input projection with the append fused into its epilogue
-    if world == 1 and not args.no_qkv and not kv8:
+    hybrid = not (kv8 or fp4)
+    if world == 1 and not args.no_qkv and hybrid:
         res["qkv_append"] = run_qkv_append(dev)
 
     # ---- the same workload without the protected region (pure KV4), rank 0 at N = 1
-    if world == 1 and not args.no_variants and not kv8 and (wl.sink > 0 or wl.window > 0):
+    if world == 1 and not args.no_variants and hybrid and (wl.sink > 0 or wl.window > 0):
         res["kv4_unprotected"] = run_unprotected(wl, seed, dev, peak, value, min(args.steps, 500))
-    if world == 1 and not args.no_variants and not kv8:
-        res["kv8"] = run_kv8(wl, seed, dev, peak, value, min(args.steps, 500))
+    if world == 1 and not args.no_variants and hybrid:
+        res["kv8"] = run_whole_cache(wl, seed, dev, peak, value, min(args.steps, 500), "int8")
+        res["nvfp4"] = run_whole_cache(wl, seed, dev, peak, value, min(args.steps, 500), "nvfp4")
 
     # ---- end to end through the public API from pinned host buffers
     if not args.no_e2e:
@@ -393,7 +402,7 @@ def run_kv4(args, rank, world, local):
 
     # ---- CPU oracle baseline (rank 0, one GPU)
     if want_cpu:
-        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores(), kv8)
+        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores(), kv8, fp4)
     cache.close()
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -462,39 +471,43 @@ def run_unprotected(wl, seed, dev, peak, protected_value, steps):
         torch.cuda.empty_cache()
 
 
-def run_kv8(wl, seed, dev, peak, kv4_value, steps):
-    """The same sequences, KV and queries in the whole-cache 8-bit format (every
-    position's 8-bit codes in its page, the protected path's arithmetic): context
-    tokens/s of the whole decode call and the split kernel's HBM rate."""
+def run_whole_cache(wl, seed, dev, peak, kv4_value, steps, fmt_name):
+    """The same sequences, KV and queries in a whole-cache format with no protected
+    region: the 8-bit format (every position's 8-bit codes in its page, the protected
+    path's arithmetic) or NVFP4 (E2M1 codes, E4M3 block scales). Context tokens/s of the
+    whole decode call and the split kernel's HBM rate."""
     import dataclasses
     from int8_hybrid_paged_gb300 import kv4
 
-    wl8 = dataclasses.replace(wl, sink=0, window=0)
-    st = build_workload(wl8, seed, dev, fmt=kv4.FORMAT_INT8)
+    kv8 = fmt_name == "int8"
+    wlw = dataclasses.replace(wl, sink=0, window=0)
+    st = build_workload(wlw, seed, dev, fmt=kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_NVFP4)
     cache = st["cache"]
-    B, Hq = wl8.batch, wl8.num_q_heads
+    B, Hq = wlw.batch, wlw.num_q_heads
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     try:
         def step():
-            for _ in range(wl8.layers):
+            for _ in range(wlw.layers):
                 kv4.kv4_decode_attention(cache.handle, st["q"], st["slots"], st["cl"],
                                          st["bt_dev"], out, lse, stream=stream)
-        ms, prof = time_calls(step, cache, steps, wl8.layers)
+        ms, prof = time_calls(step, cache, steps, wlw.layers)
         if cache.device_error():
-            raise RuntimeError("device error in the 8-bit decode")
-        value = float(sum(st["lens"])) * wl8.layers / (ms * 1e-3)
-        call_bytes = bytes_model.decode_call_bytes_kv8(st["lens"], Hq, wl8.num_kv_heads,
-                                                       with_lse=True)
+            raise RuntimeError(f"device error in the {fmt_name} decode")
+        value = float(sum(st["lens"])) * wlw.layers / (ms * 1e-3)
+        bytes_fn = bytes_model.decode_call_bytes_kv8 if kv8 else bytes_model.decode_call_bytes_nvfp4
+        call_bytes = bytes_fn(st["lens"], Hq, wlw.num_kv_heads, with_lse=True)
         split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
         split_ms = prof["split_ms"] / max(1, prof["calls"])
         gbs = split_bytes / (split_ms * 1e-3) / 1e9
-        return {"case": "the same workload, whole-cache 8-bit format (KV8: 264 B per token-head)",
+        what = ("whole-cache 8-bit format (KV8: 264 B per token-head)" if kv8 else
+                "whole-cache NVFP4 format (E2M1 + E4M3 block scales: 152 B per token-head)")
+        return {"case": "the same workload, " + what,
                 "value": value, "unit": UNIT, "ms_per_step": ms, "steps": steps,
                 "split_us": split_ms * 1e3, "split_algorithmic_bytes": split_bytes,
                 "split_achieved_gbs": gbs, "split_frac_of_hbm_peak": gbs / peak,
-                "kv4_speedup_over_kv8": kv4_value / value}
+                "kv4_speedup": kv4_value / value}
     finally:
         cache.close()
         torch.cuda.empty_cache()
@@ -752,7 +765,7 @@ def run_reference(args, rank, world):
 
     def make(nseq):
         oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq,
-                                kv8=args.format == "int8")
+                                kv8=args.format == "int8", nvfp4=args.format == "nvfp4")
         for i in range(nseq):
             oc.append(i, 0, *seq(i))
         return oc

@@ -241,7 +241,9 @@ kv4_status kv4_decode_attention(kv4_cache *cache, const void *q_bf16_dev, int nu
  *   q_scale_dev: [batch][num_q_heads] fp32 s_q
  *   qk_dev     : [batch][num_q_heads][debug_stride] int32 QK accumulator per position
  *                (INT4 codes in the INT4 region, INT8 side codes in the protected region,
- *                INT8 page codes in KV4_FORMAT_INT8)
+ *                INT8 page codes in KV4_FORMAT_INT8); KV4_FORMAT_NVFP4 has no single
+ *                integer dot, and the record holds the bits of the FP32 score sigma
+ *                (log2 domain: the block-scaled dot times g, s_q and sm_scale * log2 e)
  *   w_hat_dev  : [batch][num_q_heads][debug_stride] u8 PV weight per INT4-region position
  * Positions >= debug_stride are not written. For tests; slower than the plain call.
  */
@@ -265,7 +267,8 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
  *   config          : the cache geometry the pools were built with
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
- *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8 configuration)
+ *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8 or
+ *                     KV4_FORMAT_NVFP4 configuration)
  *   other arguments : as kv4_decode_attention
  * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 144 bytes
  * per q head, 4 bytes per (sequence, KV head) and G * 520 bytes for each of

@@ -245,7 +245,6 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     if (!group_supported(G)) return KV4_ERR_UNSUPPORTED;
     if (batch > c->cfg.max_batch || num_q_heads > c->cfg.max_q_heads) return KV4_ERR_OUT_OF_RANGE;
     if ((dqk || dw) && dbg_stride < 1) return KV4_ERR_INVALID_ARG;
-    if (c->cfg.format == KV4_FORMAT_NVFP4) return KV4_ERR_UNSUPPORTED;
     kv4::DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.slot_ids = slot_ids;

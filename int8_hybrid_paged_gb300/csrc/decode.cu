@@ -666,6 +666,45 @@ __device__ __forceinline__ int side_row_position(int rr, int s, int w, int L)
     return p >= s ? p : -1;
 }
 
+// Running-max step of a 16-row group: lane (g', t') holds the scores of rows g', g' + 8
+// for head hs. The weights p = 2^(score - group max) go, rounded to BF16, to the PV B tile
+// (column hs, k order t, t+8, t+4, t+12); the running output and normalizer are rescaled
+// to the new running max. Returns the group's fold factors 2^(group max - running max)
+// of the two heads whose output this lane accumulates.
+__device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, float2 sig, int lane)
+{
+    const int gq = lane >> 2, tq = lane & 3;
+    const int hs = 2 * (tq & 1) + (tq >> 1);
+    float m = fmaxf(sig.x, sig.y);
+#pragma unroll
+    for (int msk = 4; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
+    // weights against the group's own max (so their BF16 rounding does not depend on
+    // which groups share a piece), folded in by 2^(group max - running max)
+    const float Mn = fmaxf(st.M, m);
+    const bool none = (Mn == -INFINITY);
+    const float alpha = none ? 1.f : exp2_fast(st.M - Mn);
+    const float beta = none ? 0.f : exp2_fast(m - Mn);
+    st.M = Mn;
+    // masked rows give -inf - m (NaN for an empty group): exp2_poly2 returns 0
+    const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(-m, -m)));
+    st.l = fmaf(st.l, alpha, beta * (pp.x + pp.y));
+    ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
+    const int srcA = (lane & ~3) | (tq & 1);
+    const float bA = __shfl_sync(kFull, beta, srcA), bB = __shfl_sync(kFull, beta, srcA | 2);
+    if (__any_sync(kFull, alpha != 1.f)) {
+        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            st.o[mm][0] *= aA;
+            st.o[mm][1] *= aB;
+            st.o[mm][2] *= aA;
+            st.o[mm][3] *= aB;
+        }
+    }
+    __syncwarp();
+    return make_float2(bA, bB);
+}
+
 template <int G, bool DEBUG, bool KV8>
 __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, ProtState& st,
                                            const uint4* __restrict__ qf, float cq0, float cq1,
@@ -717,33 +756,8 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     }
 
     // ---- running max of head hs; weights relative to it, rounded to BF16 for PV
-    float m = fmaxf(sig.x, sig.y);
-#pragma unroll
-    for (int msk = 4; msk < 32; msk <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, msk));
-    // weights against the group's own max (so their BF16 rounding does not depend on
-    // which groups share a piece), folded in by 2^(group max - running max)
-    const float Mn = fmaxf(st.M, m);
-    const bool none = (Mn == -INFINITY);
-    const float alpha = none ? 1.f : exp2_fast(st.M - Mn);
-    const float beta = none ? 0.f : exp2_fast(m - Mn);
-    st.M = Mn;
-    // masked rows give -inf - m (NaN for an empty group): exp2_poly2 returns 0
-    const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(-m, -m)));
-    st.l = fmaf(st.l, alpha, beta * (pp.x + pp.y));
-    ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
-    const int srcA = (lane & ~3) | (tq & 1);
-    const float bA = __shfl_sync(kFull, beta, srcA), bB = __shfl_sync(kFull, beta, srcA | 2);
-    if (__any_sync(kFull, alpha != 1.f)) {
-        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm) {
-            st.o[mm][0] *= aA;
-            st.o[mm][1] *= aB;
-            st.o[mm][2] *= aA;
-            st.o[mm][3] *= aB;
-        }
-    }
-    __syncwarp();
+    const float2 bAB = group_weights(st, ps, sig, lane);
+    const float bA = bAB.x, bB = bAB.y;
 
     // ---- BF16 PV, FP32 accumulation into the running output
     const uint2 bw = lds64(&ps.wfrag[0][gq][2 * tq]);
@@ -775,6 +789,149 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     __syncwarp();
 }
 
+// ---------------------------------------------------------------- NVFP4 page
+// One page of the NVFP4 format (16 positions of one KV head), lane roles as in a
+// protected group. The K and V halves arrive in two stage slots; each slot's bytes past
+// the half serve as scratch for its block scales widened to FP32.
+// QK: per 16-dim block one fp16 MMA of the E2M1 codes (A: rows = positions) with the
+// INT8 query (B: even columns 2t' hold head [0, 2, 1, 3][t'], odd columns are zero), so
+// lane t' finds its head's block dots of rows g', g' + 8 in c0, c2. The dots are exact
+// (halves times integers, sums below 2^14); they enter an FP32 fma chain over the
+// blocks with the E4M3 block scales, then the vector scale g, s_q and C.
+// PV: values bf16(e2m1 · fl(s_b g)) in the A order of the protected path (bytes of a
+// V word: tokens t, t+8, t+4, t+12; nibbles: dims d, d + 8), weights as there.
+__device__ __forceinline__ void e2m1x4_f16x2(uint32_t w, uint32_t (&o)[4])
+{
+    // byte k of w holds two E2M1 codes; its low nibble becomes the low half of o[k]
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\tmov.b32 {c0, c1, c2, c3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, c0;\n\tcvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\tcvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+// four E4M3 bytes (non-negative scales) to FP32, byte k to o[k]; every E4M3 value is
+// exact in fp16
+__device__ __forceinline__ void e4m3x4_f32(uint32_t w, float (&o)[4])
+{
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 p0, p1;\n\tmov.b32 {p0, p1}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, p0;\n\tcvt.rn.f16x2.e4m3x2 %1, p1;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
+    const float2 a = __half22float2(u32_half2(lo)), b = __half22float2(u32_half2(hi));
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+}
+
+// Scratch of a K slot: s_b of position t at [t & 7][16-byte chunk (b >> 1) ^ ((t >> 1) & 3)]
+// [b & 1][t >> 3], so a lane reads (s_b of t, of t + 8) pairs with four conflict-free loads.
+__device__ __forceinline__ int fp4_kscale_off(int t, int bb)
+{
+    const int g = t & 7;
+    return 64 * g + 16 * ((bb >> 1) ^ ((g >> 1) & 3)) + 8 * (bb & 1) + 4 * (t >> 3);
+}
+// Scratch of a V slot: fl(s_b g) of position t at [t & 3][16-byte chunk b ^ 2(t & 3)]
+// [order of t among t & 3 + {0, 8, 4, 12}], so a lane reads its four positions of block b
+// with one conflict-free load.
+__device__ __forceinline__ int fp4_vscale_off(int t, int bb)
+{
+    const int c = t & 3, q4 = t >> 2;
+    return 128 * c + 16 * (bb ^ (2 * c)) + 4 * (((q4 & 1) << 1) | (q4 >> 1));
+}
+
+template <int G, bool DEBUG>
+__device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, ProtState& st,
+                                          const uint4* __restrict__ qf, float sqh, uint8_t* pk,
+                                          uint8_t* pv, int grp, int L, int b, int h, int warp,
+                                          int lane)
+{
+    const int gq = lane >> 2, tq = lane & 3;
+    const int hs = 2 * (tq & 1) + (tq >> 1);
+    PairSmem& ps = sm.xb[warp].pair;
+    uint8_t* ksc = pk + kFp4Half;
+    uint8_t* vsc = pv + kFp4Half;
+
+    // ---- block scales to FP32: lane l takes blocks 4(l & 1) .. +3 of position l >> 1
+    {
+        const int t = lane >> 1, j = lane & 1;
+        float ks[4], vs[4];
+        e4m3x4_f32(lds32(pk + kFp4ScaleOff + 8 * t + 4 * j), ks);
+        e4m3x4_f32(lds32(pv + kFp4ScaleOff + 8 * t + 4 * j), vs);
+        const float gv = *reinterpret_cast<const float*>(pv + kFp4GlobalOff + 4 * t);
+        const float2 v01 = __fmul2_rn(make_float2(vs[0], vs[1]), make_float2(gv, gv));
+        const float2 v23 = __fmul2_rn(make_float2(vs[2], vs[3]), make_float2(gv, gv));
+        const float vv[4] = {v01.x, v01.y, v23.x, v23.y};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            *reinterpret_cast<float*>(ksc + fp4_kscale_off(t, 4 * j + i)) = ks[i];
+            *reinterpret_cast<float*>(vsc + fp4_vscale_off(t, 4 * j + i)) = vv[i];
+        }
+    }
+    __syncwarp();
+
+    // ---- QK: block dots of rows gq, gq + 8 and the fma chain over the blocks
+    const uint4 kc0 = lds128(pk + 16 * lane);            // blocks 0..3
+    const uint4 kc1 = lds128(pk + 512 + 16 * lane);      // blocks 4..7
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // (s_b of rows gq, gq + 8) for blocks 2i, 2i + 1
+        const float4 sp = *reinterpret_cast<const float4*>(ksc + 64 * gq + 16 * (i ^ ((gq >> 1) & 3)));
+        const uint4 qv = qf[32 * i];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int bb = 2 * i + e;
+            const uint4 kc = bb < 4 ? kc0 : kc1;
+            const uint32_t wd = (bb & 3) == 0 ? kc.x : (bb & 3) == 1 ? kc.y : (bb & 3) == 2 ? kc.z : kc.w;
+            uint32_t A[4];
+            e2m1x4_f16x2(wd, A);
+            float d[4];
+            mma_f16(d, A[0], A[1], A[2], A[3], e ? qv.z : qv.x, e ? qv.w : qv.y, 0.f, 0.f, 0.f, 0.f);
+            acc = __ffma2_rn(e ? make_float2(sp.z, sp.w) : make_float2(sp.x, sp.y), make_float2(d[0], d[2]), acc);
+        }
+    }
+    const float2 kg = make_float2(*reinterpret_cast<const float*>(pk + kFp4GlobalOff + 4 * gq),
+                                  *reinterpret_cast<const float*>(pk + kFp4GlobalOff + 4 * (gq + 8)));
+    const float2 sg = __fmul2_rn(__fmul2_rn(__fmul2_rn(acc, kg), make_float2(sqh, sqh)),
+                                 make_float2(a.log2_scale, a.log2_scale));
+    const int pos0 = 16 * grp + gq < L ? 16 * grp + gq : -1;
+    const int pos1 = 16 * grp + gq + 8 < L ? 16 * grp + gq + 8 : -1;
+    const float2 sig = make_float2(pos0 >= 0 ? sg.x : -INFINITY, pos1 >= 0 ? sg.y : -INFINITY);
+    if (DEBUG && a.dbg_qk && hs < G) {
+        // no single integer dot here: the record holds the score's FP32 bits
+        const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
+        if (pos0 >= 0 && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = __float_as_int(sg.x);
+        if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_qk[row + pos1] = __float_as_int(sg.y);
+    }
+
+    const float2 bAB = group_weights(st, ps, sig, lane);
+    const float bA = bAB.x, bB = bAB.y;
+
+    // ---- BF16 PV, FP32 accumulation into the running output
+    const uint2 bw = lds64(&ps.wfrag[0][gq][2 * tq]);
+    const uint4 vc0 = lds128(pv + 16 * lane);            // blocks 0..3
+    const uint4 vc1 = lds128(pv + 512 + 16 * lane);      // blocks 4..7
+#pragma unroll
+    for (int mm = 0; mm < 8; ++mm) {
+        const uint4 vc = mm < 4 ? vc0 : vc1;
+        const uint32_t wd = (mm & 3) == 0 ? vc.x : (mm & 3) == 1 ? vc.y : (mm & 3) == 2 ? vc.z : vc.w;
+        uint32_t hv[4];                                  // (dim d, d + 8) of tokens t, t+8, t+4, t+12
+        e2m1x4_f16x2(wd, hv);
+        const float4 sc = *reinterpret_cast<const float4*>(vsc + 128 * tq + 16 * (mm ^ (2 * tq)));
+        const float2 v0 = __fmul2_rn(__half22float2(u32_half2(hv[0])), make_float2(sc.x, sc.x));
+        const float2 v1 = __fmul2_rn(__half22float2(u32_half2(hv[1])), make_float2(sc.y, sc.y));
+        const float2 v2 = __fmul2_rn(__half22float2(u32_half2(hv[2])), make_float2(sc.z, sc.z));
+        const float2 v3 = __fmul2_rn(__half22float2(u32_half2(hv[3])), make_float2(sc.w, sc.w));
+        float c[4];
+        mma_bf16(c, bf16x2_u32(v0.x, v1.x), bf16x2_u32(v0.y, v1.y), bf16x2_u32(v2.x, v3.x),
+                 bf16x2_u32(v2.y, v3.y), bw.x, bw.y, 0.f, 0.f, 0.f, 0.f);
+        st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
+        st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
+        st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
+        st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+    }
+    __syncwarp();
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -798,7 +955,7 @@ __device__ __forceinline__ void walk_store(volatile Walk& d, const Walk& w)
     d.csb = w.csb; d.slot = w.slot; d.k = w.k; d.a1 = w.a1; d.g0 = w.g0; d.g1 = w.g1; d.done = w.done;
 }
 
-template <int G, bool DEBUG, bool KV8>
+template <int G, bool DEBUG, bool KV8, bool FP4>
 __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(DecodeArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -818,6 +975,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
     const int cp = prot_items(S);
     const int span = a.plan->span;
+    // whole-cache formats: a page block and each of its two stage items (K half, V half)
+    constexpr int kBlock8 = FP4 ? kPageBlock4f : kPageBlock8;
+    constexpr int kItem8 = FP4 ? kFp4Half : kPageBlock;
     const int wg = blockIdx.x * kWarps + warp;
     volatile Walk& Psm = sm.walk[warp][0];
     volatile Walk& Csm = sm.walk[warp][1];
@@ -868,7 +1028,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 r_i = P.k;
                 r_end = group_items(P.cp) * P.g1;
                 r_b = P.b;
-                r_src = a.pages + (int64_t)P.h * kPageBlock8;
+                r_src = a.pages + (int64_t)P.h * kBlock8;
                 win_lo = -64;               // force a window load
             } else {
                 r_kind = S > 0 ? 1 : 2;
@@ -886,7 +1046,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
         return more;
     };
     const int64_t page_stride = (int64_t)H * kPageBlock;
-    const int64_t page_stride8 = (int64_t)H * kPageBlock8;
+    const int64_t page_stride8 = (int64_t)H * kBlock8;
     auto produce = [&]() {
         // common case: two more pages of the current INT4 run, both inside the
         // block-table window, and two free stages
@@ -946,8 +1106,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                     win = pg;
                 }
                 const int page = __shfl_sync(kFull, win, lp - win_lo);
-                issue_bulk(dst, r_src + (int64_t)page * page_stride8 + (r_i & 1) * kPageBlock, kPageBlock,
-                           bar, is_l0);
+                issue_bulk(dst, r_src + (int64_t)page * page_stride8 + (r_i & 1) * kItem8, kItem8, bar,
+                           is_l0);
             } else {
                 arrive_pred(bar, is_l0);    // empty protected item: no side buffer
             }
@@ -1001,7 +1161,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 sm.wq[warp].corr[lane][1] = f.w;
             }
             __syncwarp();
-            {
+            if (FP4) {
+                // NVFP4 QK B fragments: even column g' is head [0, 2, 1, 3][g' / 2], odd
+                // columns are zero; block bb takes k rows 2t', 2t'+1, 2t'+8, 2t'+9 as dims
+                // 16bb + 2t' + {0, 1, 8, 9}. Slot ii holds blocks 2ii, 2ii + 1.
+                const int bh = 2 * ((gq >> 1) & 1) + (gq >> 2);
+                const bool bok = !(gq & 1) && bh < G;
+                const int8_t* qq = sm.wq[warp].q8[bok ? bh : 0];
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    uint32_t f[4];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int base = 16 * (2 * ii + e) + 2 * tq;
+                        f[2 * e] = bok ? half2_bits(__int2half_rn(qq[base]), __int2half_rn(qq[base + 1])) : 0u;
+                        f[2 * e + 1] = bok ? half2_bits(__int2half_rn(qq[base + 8]), __int2half_rn(qq[base + 9])) : 0u;
+                    }
+                    sm.qfrag[warp][ii][lane] = make_uint4(f[0], f[1], f[2], f[3]);
+                }
+            } else {
                 // QK B fragments. Column g' = head(g') over dim half g' & 1 with
                 // head(n) = n < 4 ? n : n ^ 5; k rows 2t', 2t'+1, 2t'+8, 2t'+9 come from code
                 // lane t', whose dims lie in half t' >> 1. Lane (g', t') keeps its column's
@@ -1140,8 +1318,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 for (int grp = g0; grp < g1; ++grp) {
                     const int s0 = wait_next();
                     const int s1 = wait_next();
-                    prot_group<G, DEBUG, KV8>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
-                                         sm.stage[warp][s1], grp, Lp, b, h, warp, lane);
+                    if (FP4)
+                        fp4_group<G, DEBUG>(a, sm, st, qf, sqh, sm.stage[warp][s0], sm.stage[warp][s1],
+                                            grp, Lp, b, h, warp, lane);
+                    else
+                        prot_group<G, DEBUG, KV8>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
+                                                  sm.stage[warp][s1], grp, Lp, b, h, warp, lane);
                     produce();
                 }
             } else {
@@ -1305,7 +1487,7 @@ static cudaError_t launch_k(void (*k)(DecodeArgs), int grid, int block, size_t s
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-template <int G, bool DEBUG, bool KV8>
+template <int G, bool DEBUG, bool KV8, bool FP4>
 static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     // with profiling events between the kernels each one runs alone, so the events
@@ -1316,7 +1498,7 @@ static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, 
     cudaError_t e = launch_k(kv4_decode_prep_kernel, prep_blocks, kPrepThreads, 0, stream, a, false);
     if (ev) cudaEventRecord(ev[1], stream);
     if (e == cudaSuccess)
-        e = launch_k(kv4_decode_split_kernel<G, DEBUG, KV8>, grid, kDecodeThreads, sizeof(SplitSmem),
+        e = launch_k(kv4_decode_split_kernel<G, DEBUG, KV8, FP4>, grid, kDecodeThreads, sizeof(SplitSmem),
                      stream, a, dep);
     if (ev) cudaEventRecord(ev[2], stream);
     const int warps = a.batch * a.num_q_heads;
@@ -1329,14 +1511,16 @@ static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     const bool dbg = a.dbg_q8 || a.dbg_qscale || a.dbg_qk || a.dbg_w;
-    const int sel = (dbg ? 1 : 0) + (a.kv8 ? 2 : 0);
+    const int sel = (dbg ? 1 : 0) + (a.fp4 ? 4 : a.kv8 ? 2 : 0);
     auto go = [&](auto g) -> cudaError_t {
         constexpr int Gc = decltype(g)::value;
         switch (sel) {
-        case 0: return launch_g<Gc, false, false>(a, grid, stream, ev);
-        case 1: return launch_g<Gc, true, false>(a, grid, stream, ev);
-        case 2: return launch_g<Gc, false, true>(a, grid, stream, ev);
-        default: return launch_g<Gc, true, true>(a, grid, stream, ev);
+        case 0: return launch_g<Gc, false, false, false>(a, grid, stream, ev);
+        case 1: return launch_g<Gc, true, false, false>(a, grid, stream, ev);
+        case 2: return launch_g<Gc, false, true, false>(a, grid, stream, ev);
+        case 3: return launch_g<Gc, true, true, false>(a, grid, stream, ev);
+        case 4: return launch_g<Gc, false, true, true>(a, grid, stream, ev);
+        default: return launch_g<Gc, true, true, true>(a, grid, stream, ev);
         }
     };
     switch (a.group) {
@@ -1354,11 +1538,12 @@ static cudaError_t split_setup(int* ctas)
 {
     const int smem = (int)sizeof(SplitSmem);
     cudaError_t e = cudaSuccess;
-    for (auto k : {kv4_decode_split_kernel<G, false, false>, kv4_decode_split_kernel<G, true, false>,
-                   kv4_decode_split_kernel<G, false, true>, kv4_decode_split_kernel<G, true, true>})
+    for (auto k : {kv4_decode_split_kernel<G, false, false, false>, kv4_decode_split_kernel<G, true, false, false>,
+                   kv4_decode_split_kernel<G, false, true, false>, kv4_decode_split_kernel<G, true, true, false>,
+                   kv4_decode_split_kernel<G, false, true, true>, kv4_decode_split_kernel<G, true, true, true>})
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false, false>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false, false, false>,
                                                          kDecodeThreads, smem);
 }
 

@@ -48,3 +48,14 @@ def test_kv8_decode_bytes():
     assert bm.decode_call_bytes_kv8([0], 4, 1) == 8 + 4 * 128 * 6
     # KV8 reads 264 / 136 of the INT4 bytes per token-head
     assert bm.SIDE_POSITION_HEAD_BYTES / bm.INT4_TOKEN_HEAD_BYTES == 264 / 136
+
+
+def test_nvfp4_decode_bytes():
+    """NVFP4 holds 4.75 bits per element (4-bit codes, an 8-bit scale per 16 values, a
+    32-bit scale per 128): 152 B per position-head for K and V, the page block size of
+    include/kv4.h over 16 positions."""
+    assert bm.NVFP4_POSITION_HEAD_BYTES == 152
+    assert bm.NVFP4_POSITION_HEAD_BYTES * 8 / (2 * 128) == 4.75
+    assert 16 * bm.NVFP4_POSITION_HEAD_BYTES == 2432
+    got = bm.decode_call_bytes_nvfp4([1000], 32, 8)
+    assert got == 8 * 1000 * 152 + 4 * 63 + 8 + 32 * 128 * 6
