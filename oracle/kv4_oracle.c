@@ -71,8 +71,12 @@
  *      s_b = e4m3(amax_b / fl(6g)); each value is e2m1(x · fl(1/fl(s_b g))), nearest
  *      with ties to even. The whole cache is NVFP4 (no protected region). Decode keeps the
  *      INT8 query: the score is ((Σ_b fma-chained s_b·dot_b)·g·s_q)·C with each block dot
- *      exact; values enter PV as bf16(e2m1·fl(s_b g)) with R7's BF16 weights, in groups of
- *      16 consecutive positions.
+ *      exact. PV runs in groups of 16 consecutive positions with the group's own max as in
+ *      R7, but the value scales move to the weights: the E2M1 values enter exactly, and
+ *      position i of head h weighs w_ib = fp16(fp16(fl(p_i·g_i)·2^-k)·s_ib) in block b,
+ *      where 2^k is the power of two just above the head's largest fl(p·g) in the group
+ *      (that largest weight lands in [0.5, 1); 2^k is taken as 2^-126 below the normal
+ *      range) and the group's sum is scaled by 2^k. The normaliser sums the plain p.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -662,6 +666,21 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         double og[ORC_D];
         double lg = 0.0;
         for (int j = 0; j < ORC_D; j++) og[j] = 0.0;
+        /* R12: the power of two 2^k just above the largest fl(p·g) of the group */
+        int f4k = -126;
+        if (isf4) {
+            float mx = 0.0f;
+            for (int i = 0; i < n; i++) {
+                if (pos[i] < 0) continue;
+                const float pg = orc_exp2f(sg[i] - Mg) * c->v_gscale[rix[i]];
+                if (pg > mx) mx = pg;
+            }
+            if (mx >= FLT_MIN) {
+                int k;
+                frexpf(mx, &k);                      /* mx in [2^(k-1), 2^k) */
+                f4k = k;
+            }
+        }
         for (int i = 0; i < n; i++) {
             if (pos[i] < 0) continue;
             const size_t si = rix[i];
@@ -670,11 +689,21 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                                   ? (double)p
                                   : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
             const uint8_t *vc = v8c + si * ORC_D;
-            if (isf4) {                              /* R12: v = bf16(e2m1(c) * fl(s_b g)) */
-                for (int j = 0; j < ORC_D; j++) {
-                    const float scale = orc_e4m3_value(c->v_bscale[si * 8 + j / 16]) * c->v_gscale[si];
-                    const float v = orc_bf16_to_f32(orc_f32_to_bf16_rn(orc_e2m1_value(vc[j]) * scale));
-                    og[j] += pw * (double)v;
+            if (isf4) {                              /* R12 */
+                const float gi = c->v_gscale[si];
+                if (pv_mode == ORC_PV_FLOAT) {       /* exact values, unrounded p */
+                    for (int j = 0; j < ORC_D; j++)
+                        og[j] += (double)p * (double)orc_e2m1_value(vc[j]) *
+                                 (double)orc_e4m3_value(c->v_bscale[si * 8 + j / 16]) * (double)gi;
+                } else {                             /* fp16 weights carrying the value scales */
+                    const float wn = ldexpf(p * gi, -f4k);
+                    const float w1 = (float)orc_f16_to_f64(orc_f32_to_f16(wn, ORC_RN));
+                    for (int bb = 0; bb < ORC_D / 16; bb++) {
+                        const float sb = orc_e4m3_value(c->v_bscale[si * 8 + bb]);
+                        const double wb = orc_f16_to_f64(orc_f32_to_f16(w1 * sb, ORC_RN));
+                        for (int j = 16 * bb; j < 16 * bb + 16; j++)
+                            og[j] += wb * (double)orc_e2m1_value(vc[j]);
+                    }
                 }
             } else {
                 float dv = (float)orc_f16_to_f64(v8d[si]);
@@ -686,6 +715,8 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
             }
             lg += (double)p;
         }
+        if (isf4 && pv_mode != ORC_PV_FLOAT)
+            for (int j = 0; j < ORC_D; j++) og[j] = ldexp(og[j], f4k);
         const float Mn = (Mg > Mr) ? Mg : Mr;
         const double a = (Mr == -INFINITY) ? 0.0 : exp2((double)Mr - (double)Mn);
         const double bsc = exp2((double)Mg - (double)Mn);
