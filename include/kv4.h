@@ -123,8 +123,10 @@ typedef struct {
  *                   16*(32*(b/4) + 4*(t%8) + jj%4) + 4*(b%4) + t/8 + 2*(jj/4)
  *                V: dims (d, d+8) of token t, d = 16m + g (g < 8), at
  *                   16*(32*(m/4) + 4*g + t%4) + 4*(m%4) + {0,2,1,3}[t/4]
- *   [1024, 1152) E4M3 block scales, byte 8*t + b (block b = dims 16b .. 16b+15)
- *   [1152, 1216) FP32 vector scales, float t
+ *   [1024, 1152) E4M3 block scales (block b = dims 16b .. 16b+15) of token t:
+ *                K: byte 16*(t%8) + 2*b + t/8      (tokens t, t+8 of a block paired)
+ *                V: byte 32*(t%4) + 4*b + {0,2,1,3}[t/4]  (tokens t, t+8, t+4, t+12)
+ *   [1152, 1216) FP32 vector scales, float of token t at byte 8*(t%8) + 4*(t/8)
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128

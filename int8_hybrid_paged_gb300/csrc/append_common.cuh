@@ -229,7 +229,10 @@ __device__ __forceinline__ void warp_quant_nvfp4(const float (&x)[4], uint32_t (
     for (int i = 0; i < 4; ++i) c[i] = scale > 0.0f ? e2m1_rn(__fmul_rn(x[i], inv)) : 0u;
 }
 // One token-head in an NVFP4 page block: the K half (codes in the QK fragment order) or
-// the V half (codes in the PV fragment order), its block scales and vector scale.
+// the V half (codes in the PV fragment order), its block scales and vector scale. The K
+// scales of tokens t, t + 8 sit side by side per block, the V scales of tokens t, t + 8,
+// t + 4, t + 12 per block, and the vector scales of t, t + 8 side by side, each in the
+// order a decode lane reads them.
 __device__ __forceinline__ void store_nvfp4_k(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t sb, float g,
                                               int lane)
 {
@@ -240,8 +243,8 @@ __device__ __forceinline__ void store_nvfp4_k(uint8_t* half, int ts, const uint3
         half[16 * (32 * (b >> 2) + 4 * (ts & 7) + (jj & 3)) + 4 * (b & 3) + (ts >> 3) + 2 * (jj >> 2)] =
             (uint8_t)(c[2 * e] | (c[2 * e + 1] << 4));
     }
-    if ((lane & 3) == 0) half[kFp4ScaleOff + 8 * ts + b] = (uint8_t)sb;
-    if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 4 * ts) = g;
+    if ((lane & 3) == 0) half[kFp4ScaleOff + 16 * (ts & 7) + 2 * b + (ts >> 3)] = (uint8_t)sb;
+    if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 8 * (ts & 7) + 4 * (ts >> 3)) = g;
 }
 __device__ __forceinline__ void store_nvfp4_v(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t sb, float g,
                                               int lane)
@@ -258,8 +261,8 @@ __device__ __forceinline__ void store_nvfp4_v(uint8_t* half, int ts, const uint3
             half[16 * (32 * (m >> 2) + 4 * gq + (ts & 3)) + 4 * (m & 3) + kb] = (uint8_t)(c[i] | (hi[i] << 4));
         }
     }
-    if ((lane & 3) == 0) half[kFp4ScaleOff + 8 * ts + m] = (uint8_t)sb;
-    if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 4 * ts) = g;
+    if ((lane & 3) == 0) half[kFp4ScaleOff + 32 * (ts & 3) + 4 * m + kb] = (uint8_t)sb;
+    if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 8 * (ts & 7) + 4 * (ts >> 3)) = g;
 }
 
 // Where token tok of an append goes: its sequence entry i (cu_tokens[i] <= tok <

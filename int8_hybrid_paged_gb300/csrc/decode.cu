@@ -671,7 +671,13 @@ __device__ __forceinline__ int side_row_position(int rr, int s, int w, int L)
 // (column hs, k order t, t+8, t+4, t+12); the running output and normalizer are rescaled
 // to the new running max. Returns the group's fold factors 2^(group max - running max)
 // of the two heads whose output this lane accumulates.
-__device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, float2 sig, int lane)
+// F16W (NVFP4): the weights carry their row's value scale, p·wsc·inv with inv = 2^-k
+// for the power of two 2^k just above the group's largest value scale, and go in fp16;
+// the fold factors carry up = 2^k. No weight exceeds 1; the normalizer still sums the
+// plain p.
+template <bool F16W>
+__device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, float2 sig, int lane,
+                                                float2 wsc, float inv, float up)
 {
     const int gq = lane >> 2, tq = lane & 3;
     const int hs = 2 * (tq & 1) + (tq >> 1);
@@ -688,9 +694,16 @@ __device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, flo
     // masked rows give -inf - m (NaN for an empty group): exp2_poly2 returns 0
     const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(-m, -m)));
     st.l = fmaf(st.l, alpha, beta * (pp.x + pp.y));
-    ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
+    float fold = beta;
+    if (F16W) {
+        const float2 wn = __fmul2_rn(__fmul2_rn(pp, wsc), make_float2(inv, inv));
+        ps.wfrag[0][hs][wfrag_pos(gq)] = half2_u32(__floats2half2_rn(wn.x, wn.y));
+        fold = beta * up;
+    } else {
+        ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
+    }
     const int srcA = (lane & ~3) | (tq & 1);
-    const float bA = __shfl_sync(kFull, beta, srcA), bB = __shfl_sync(kFull, beta, srcA | 2);
+    const float bA = __shfl_sync(kFull, fold, srcA), bB = __shfl_sync(kFull, fold, srcA | 2);
     if (__any_sync(kFull, alpha != 1.f)) {
         const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
 #pragma unroll
@@ -756,7 +769,7 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
     }
 
     // ---- running max of head hs; weights relative to it, rounded to BF16 for PV
-    const float2 bAB = group_weights(st, ps, sig, lane);
+    const float2 bAB = group_weights<false>(st, ps, sig, lane, make_float2(0.f, 0.f), 0.f, 0.f);
     const float bA = bAB.x, bB = bAB.y;
 
     // ---- BF16 PV, FP32 accumulation into the running output
@@ -791,15 +804,18 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
 
 // ---------------------------------------------------------------- NVFP4 page
 // One page of the NVFP4 format (16 positions of one KV head), lane roles as in a
-// protected group. The K and V halves arrive in two stage slots; each slot's bytes past
-// the half serve as scratch for its block scales widened to FP32.
+// protected group; the K and V halves arrive in two stage slots.
 // QK: per 16-dim block one fp16 MMA of the E2M1 codes (A: rows = positions) with the
 // INT8 query (B: even columns 2t' hold head [0, 2, 1, 3][t'], odd columns are zero), so
 // lane t' finds its head's block dots of rows g', g' + 8 in c0, c2. The dots are exact
 // (halves times integers, sums below 2^14); they enter an FP32 fma chain over the
-// blocks with the E4M3 block scales, then the vector scale g, s_q and C.
-// PV: values bf16(e2m1 · fl(s_b g)) in the A order of the protected path (bytes of a
-// V word: tokens t, t+8, t+4, t+12; nibbles: dims d, d + 8), weights as there.
+// blocks with the E4M3 block scales, then the vector scale g, s_q and C. The block
+// scales are widened to FP32 once per page into scratch space past the K half in its
+// stage slot (the bulk copy never writes there).
+// PV: fp16 MMA of the E2M1 values (A: rows = dims, exact) with weights that carry the
+// value scales, p·g / 2^k (from group_weights; 2^k just above the page's largest g)
+// times the E4M3 scale of the block: the B tile of block m is one packed multiply per
+// register. The FP32 results fold into the running output with 2^k.
 __device__ __forceinline__ void e2m1x4_f16x2(uint32_t w, uint32_t (&o)[4])
 {
     // byte k of w holds two E2M1 codes; its low nibble becomes the low half of o[k]
@@ -809,62 +825,51 @@ __device__ __forceinline__ void e2m1x4_f16x2(uint32_t w, uint32_t (&o)[4])
         : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
         : "r"(w));
 }
-// four E4M3 bytes (non-negative scales) to FP32, byte k to o[k]; every E4M3 value is
+// four E4M3 bytes to two fp16 pairs (bytes 0, 1 -> lo; 2, 3 -> hi); every E4M3 value is
 // exact in fp16
-__device__ __forceinline__ void e4m3x4_f32(uint32_t w, float (&o)[4])
+__device__ __forceinline__ void e4m3x4_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi)
 {
-    uint32_t lo, hi;
     asm("{\n\t.reg .b16 p0, p1;\n\tmov.b32 {p0, p1}, %2;\n\t"
         "cvt.rn.f16x2.e4m3x2 %0, p0;\n\tcvt.rn.f16x2.e4m3x2 %1, p1;\n\t}"
         : "=r"(lo), "=r"(hi)
         : "r"(w));
-    const float2 a = __half22float2(u32_half2(lo)), b = __half22float2(u32_half2(hi));
-    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
 }
-
-// Scratch of a K slot: s_b of position t at [t & 7][16-byte chunk (b >> 1) ^ ((t >> 1) & 3)]
-// [b & 1][t >> 3], so a lane reads (s_b of t, of t + 8) pairs with four conflict-free loads.
-__device__ __forceinline__ int fp4_kscale_off(int t, int bb)
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
 {
-    const int g = t & 7;
-    return 64 * g + 16 * ((bb >> 1) ^ ((g >> 1) & 3)) + 8 * (bb & 1) + 4 * (t >> 3);
-}
-// Scratch of a V slot: fl(s_b g) of position t at [t & 3][16-byte chunk b ^ 2(t & 3)]
-// [order of t among t & 3 + {0, 8, 4, 12}], so a lane reads its four positions of block b
-// with one conflict-free load.
-__device__ __forceinline__ int fp4_vscale_off(int t, int bb)
-{
-    const int c = t & 3, q4 = t >> 2;
-    return 128 * c + 16 * (bb ^ (2 * c)) + 4 * (((q4 & 1) << 1) | (q4 >> 1));
+    return half2_u32(__hmul2(u32_half2(a), u32_half2(b)));
 }
 
 template <int G, bool DEBUG>
 __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, ProtState& st,
                                           const uint4* __restrict__ qf, float sqh, uint8_t* pk,
-                                          uint8_t* pv, int grp, int L, int b, int h, int warp,
+                                          const uint8_t* pv, int grp, int L, int b, int h, int warp,
                                           int lane)
 {
     const int gq = lane >> 2, tq = lane & 3;
     const int hs = 2 * (tq & 1) + (tq >> 1);
     PairSmem& ps = sm.xb[warp].pair;
     uint8_t* ksc = pk + kFp4Half;
-    uint8_t* vsc = pv + kFp4Half;
+    const int pos0 = 16 * grp + gq < L ? 16 * grp + gq : -1;
+    const int pos1 = 16 * grp + gq + 8 < L ? 16 * grp + gq + 8 : -1;
 
-    // ---- block scales to FP32: lane l takes blocks 4(l & 1) .. +3 of position l >> 1
+    // ---- the PV weights' power of two 2^k, just above the largest V vector scale of the
+    // page's positions: g >= 0 orders as its bits; the biased exponent e gives
+    // g in [2^(e-127), 2^(e-126)), so k = e - 126 (e <= 243: g <= FLT_MAX / 2688)
+    const float2 vg = *reinterpret_cast<const float2*>(pv + kFp4GlobalOff + 8 * gq);
+    const uint32_t gb = __reduce_max_sync(
+        kFull, max(pos0 >= 0 ? __float_as_uint(vg.x) : 0u, pos1 >= 0 ? __float_as_uint(vg.y) : 0u));
+    const uint32_t ge = (gb >> 23) & 255u;
+    const float pinv = __uint_as_float((253u - ge) << 23), pup = __uint_as_float((ge + 1u) << 23);
+
+    // ---- K block scales to FP32: lane l widens blocks 2c, 2c + 1 (c = l >> 3) of positions
+    // t, t + 8 (t = l & 7), stored as (s of t, of t + 8) pairs in 16-byte chunk c ^ ((t >> 1) & 3)
+    // of row t, so that every load and store below is conflict-free
     {
-        const int t = lane >> 1, j = lane & 1;
-        float ks[4], vs[4];
-        e4m3x4_f32(lds32(pk + kFp4ScaleOff + 8 * t + 4 * j), ks);
-        e4m3x4_f32(lds32(pv + kFp4ScaleOff + 8 * t + 4 * j), vs);
-        const float gv = *reinterpret_cast<const float*>(pv + kFp4GlobalOff + 4 * t);
-        const float2 v01 = __fmul2_rn(make_float2(vs[0], vs[1]), make_float2(gv, gv));
-        const float2 v23 = __fmul2_rn(make_float2(vs[2], vs[3]), make_float2(gv, gv));
-        const float vv[4] = {v01.x, v01.y, v23.x, v23.y};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            *reinterpret_cast<float*>(ksc + fp4_kscale_off(t, 4 * j + i)) = ks[i];
-            *reinterpret_cast<float*>(vsc + fp4_vscale_off(t, 4 * j + i)) = vv[i];
-        }
+        const int t = lane & 7, c = lane >> 3;
+        uint32_t lo, hi;
+        e4m3x4_f16x2(lds32(pk + kFp4ScaleOff + 16 * t + 4 * c), lo, hi);
+        const float2 f0 = __half22float2(u32_half2(lo)), f1 = __half22float2(u32_half2(hi));
+        *reinterpret_cast<float4*>(ksc + 64 * t + 16 * (c ^ ((t >> 1) & 3))) = make_float4(f0.x, f0.y, f1.x, f1.y);
     }
     __syncwarp();
 
@@ -889,12 +894,9 @@ __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, Pr
             acc = __ffma2_rn(e ? make_float2(sp.z, sp.w) : make_float2(sp.x, sp.y), make_float2(d[0], d[2]), acc);
         }
     }
-    const float2 kg = make_float2(*reinterpret_cast<const float*>(pk + kFp4GlobalOff + 4 * gq),
-                                  *reinterpret_cast<const float*>(pk + kFp4GlobalOff + 4 * (gq + 8)));
+    const float2 kg = *reinterpret_cast<const float2*>(pk + kFp4GlobalOff + 8 * gq);
     const float2 sg = __fmul2_rn(__fmul2_rn(__fmul2_rn(acc, kg), make_float2(sqh, sqh)),
                                  make_float2(a.log2_scale, a.log2_scale));
-    const int pos0 = 16 * grp + gq < L ? 16 * grp + gq : -1;
-    const int pos1 = 16 * grp + gq + 8 < L ? 16 * grp + gq + 8 : -1;
     const float2 sig = make_float2(pos0 >= 0 ? sg.x : -INFINITY, pos1 >= 0 ? sg.y : -INFINITY);
     if (DEBUG && a.dbg_qk && hs < G) {
         // no single integer dot here: the record holds the score's FP32 bits
@@ -903,27 +905,28 @@ __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, Pr
         if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_qk[row + pos1] = __float_as_int(sg.y);
     }
 
-    const float2 bAB = group_weights(st, ps, sig, lane);
+    const float2 bAB = group_weights<true>(st, ps, sig, lane, vg, pinv, pup);
     const float bA = bAB.x, bB = bAB.y;
 
-    // ---- BF16 PV, FP32 accumulation into the running output
-    const uint2 bw = lds64(&ps.wfrag[0][gq][2 * tq]);
+    // ---- fp16 PV, FP32 accumulation into the running output
+    const uint2 pw = lds64(&ps.wfrag[0][gq][2 * tq]);    // weights of tokens (tq, tq+8), (tq+4, tq+12)
     const uint4 vc0 = lds128(pv + 16 * lane);            // blocks 0..3
     const uint4 vc1 = lds128(pv + 512 + 16 * lane);      // blocks 4..7
+    const uint4 vs0 = lds128(pv + kFp4ScaleOff + 32 * tq);        // E4M3 scales, blocks 0..3
+    const uint4 vs1 = lds128(pv + kFp4ScaleOff + 32 * tq + 16);   // blocks 4..7
 #pragma unroll
     for (int mm = 0; mm < 8; ++mm) {
         const uint4 vc = mm < 4 ? vc0 : vc1;
+        const uint4 vs = mm < 4 ? vs0 : vs1;
         const uint32_t wd = (mm & 3) == 0 ? vc.x : (mm & 3) == 1 ? vc.y : (mm & 3) == 2 ? vc.z : vc.w;
+        const uint32_t sw = (mm & 3) == 0 ? vs.x : (mm & 3) == 1 ? vs.y : (mm & 3) == 2 ? vs.z : vs.w;
         uint32_t hv[4];                                  // (dim d, d + 8) of tokens t, t+8, t+4, t+12
         e2m1x4_f16x2(wd, hv);
-        const float4 sc = *reinterpret_cast<const float4*>(vsc + 128 * tq + 16 * (mm ^ (2 * tq)));
-        const float2 v0 = __fmul2_rn(__half22float2(u32_half2(hv[0])), make_float2(sc.x, sc.x));
-        const float2 v1 = __fmul2_rn(__half22float2(u32_half2(hv[1])), make_float2(sc.y, sc.y));
-        const float2 v2 = __fmul2_rn(__half22float2(u32_half2(hv[2])), make_float2(sc.z, sc.z));
-        const float2 v3 = __fmul2_rn(__half22float2(u32_half2(hv[3])), make_float2(sc.w, sc.w));
+        uint32_t s01, s23;                               // block scales of tokens (t, t+8), (t+4, t+12)
+        e4m3x4_f16x2(sw, s01, s23);
         float c[4];
-        mma_bf16(c, bf16x2_u32(v0.x, v1.x), bf16x2_u32(v0.y, v1.y), bf16x2_u32(v2.x, v3.x),
-                 bf16x2_u32(v2.y, v3.y), bw.x, bw.y, 0.f, 0.f, 0.f, 0.f);
+        mma_f16(c, prmt(hv[0], hv[1], 0x5410u), prmt(hv[0], hv[1], 0x7632u), prmt(hv[2], hv[3], 0x5410u),
+                prmt(hv[2], hv[3], 0x7632u), hmul2_u32(pw.x, s01), hmul2_u32(pw.y, s23), 0.f, 0.f, 0.f, 0.f);
         st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
         st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
         st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
@@ -1060,6 +1063,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                            kPageBlock, bar0 + 8u * pst, is_l0);
                 issue_bulk(stage0 + (uint32_t)(kPageBlock * p1), r_src + (int64_t)pg1 * page_stride,
                            kPageBlock, bar0 + 8u * p1, is_l0);
+                r_i += 2;
+                prod += 2;
+                pst = (p1 + 1 == kStages) ? 0 : p1 + 1;
+                return;
+            }
+        }
+        // whole-cache formats: the next two items of the run (page halves), their pages'
+        // entries inside the block-table window, two free stages
+        if (KV8 && r_kind == 3 && prod + 2 <= cons + kStages && r_i + 2 <= r_end) {
+            const int o0 = (r_i >> 1) - win_lo, o1 = ((r_i + 1) >> 1) - win_lo;
+            if ((unsigned)o0 < 32u && (unsigned)o1 < 32u) {
+                const int h0 = (r_i & 1) * kItem8, h1 = kItem8 - h0;
+                const uint8_t* src0 = r_src + (int64_t)__shfl_sync(kFull, win, o0) * page_stride8 + h0;
+                const uint8_t* src1 = r_src + (int64_t)__shfl_sync(kFull, win, o1) * page_stride8 + h1;
+                const int p1 = (pst + 1 == kStages) ? 0 : pst + 1;
+                issue_bulk(stage0 + (uint32_t)(kPageBlock * pst), src0, kItem8, bar0 + 8u * pst, is_l0);
+                issue_bulk(stage0 + (uint32_t)(kPageBlock * p1), src1, kItem8, bar0 + 8u * p1, is_l0);
                 r_i += 2;
                 prod += 2;
                 pst = (p1 + 1 == kStages) ? 0 : p1 + 1;

@@ -74,9 +74,10 @@
  *      exact. PV runs in groups of 16 consecutive positions with the group's own max as in
  *      R7, but the value scales move to the weights: the E2M1 values enter exactly, and
  *      position i of head h weighs w_ib = fp16(fp16(fl(p_i·g_i)·2^-k)·s_ib) in block b,
- *      where 2^k is the power of two just above the head's largest fl(p·g) in the group
- *      (that largest weight lands in [0.5, 1); 2^k is taken as 2^-126 below the normal
- *      range) and the group's sum is scaled by 2^k. The normaliser sums the plain p.
+ *      where 2^k is the power of two just above the largest V vector scale g of the
+ *      group's positions (2^-126 below the normal range), so no fp16 weight before the
+ *      block scale exceeds 1, and the group's sum is scaled by 2^k. The normaliser sums
+ *      the plain p.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -666,14 +667,13 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         double og[ORC_D];
         double lg = 0.0;
         for (int j = 0; j < ORC_D; j++) og[j] = 0.0;
-        /* R12: the power of two 2^k just above the largest fl(p·g) of the group */
+        /* R12: the power of two 2^k just above the largest V vector scale of the group */
         int f4k = -126;
         if (isf4) {
             float mx = 0.0f;
             for (int i = 0; i < n; i++) {
                 if (pos[i] < 0) continue;
-                const float pg = orc_exp2f(sg[i] - Mg) * c->v_gscale[rix[i]];
-                if (pg > mx) mx = pg;
+                if (c->v_gscale[rix[i]] > mx) mx = c->v_gscale[rix[i]];
             }
             if (mx >= FLT_MIN) {
                 int k;

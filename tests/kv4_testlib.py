@@ -100,10 +100,13 @@ def unpack_nvfp4_pages(pages, H, page_ids, slots_in_page, h):
     vbyte = pages[base[:, None] + 1216 + voff]
     vc = np.where(r < 8, vbyte & 15, vbyte >> 4).astype(np.uint8)
     ts = np.asarray(slots_in_page, np.int64)
-    kbs = pages[(base + 1024 + 8 * ts)[:, None] + np.arange(8)[None, :]]
-    vbs = pages[(base + 1216 + 1024 + 8 * ts)[:, None] + np.arange(8)[None, :]]
-    kg = pages[(base + 1152 + 4 * ts)[:, None] + np.arange(4)[None, :]].copy().view(np.float32)[:, 0]
-    vg = pages[(base + 1216 + 1152 + 4 * ts)[:, None] + np.arange(4)[None, :]].copy().view(np.float32)[:, 0]
+    bb = np.arange(8)[None, :]
+    tt = ts[:, None]
+    kbs = pages[base[:, None] + 1024 + 16 * (tt % 8) + 2 * bb + tt // 8]
+    vbs = pages[base[:, None] + 1216 + 1024 + 32 * (tt % 4) + 4 * bb + np.array([0, 2, 1, 3])[tt // 4]]
+    goff = 1152 + 8 * (ts % 8) + 4 * (ts // 8)
+    kg = pages[(base + goff)[:, None] + np.arange(4)[None, :]].copy().view(np.float32)[:, 0]
+    vg = pages[(base + 1216 + goff)[:, None] + np.arange(4)[None, :]].copy().view(np.float32)[:, 0]
     return kc, kbs, kg, vc, vbs, vg
 
 

@@ -185,7 +185,8 @@ def test_fp16_weights_within_rounding_bound():
                 idx = np.arange(g0, min(L, g0 + 16))
                 Mg = sig[idx].max()
                 pg = np.exp2(sig[idx] - Mg) * c.v_gscale[b, idx, 0]
-                k = math.frexp(pg.max())[1] if pg.max() >= 2.0 ** -126 else -126
+                gm = c.v_gscale[b, idx, 0].max()
+                k = math.frexp(gm)[1] if gm >= 2.0 ** -126 else -126
                 for n, t in enumerate(idx):
                     sb = np.repeat([oracle.e4m3_value(int(x)) for x in c.v_bscale[b, t, 0]], 16)
                     e = np.abs([oracle.e2m1_value(int(x)) for x in c.v4_code[b, t, 0]])
