@@ -320,8 +320,7 @@ kv4_status kv4_linear_bf16(const void *x_dev, const void *w_dev, void *y_dev, in
  *   q_out_dev : [total_tokens][num_q_heads][128] bf16 projected queries (pre-RoPE)
  *   d_model   : a multiple of 64; num_q_heads * 128 a multiple of 256
  *   other arguments: as kv4_append (the token order of x is the order of cu_tokens)
- * Errors: as kv4_append, KV4_ERR_INVALID_ARG for the sizes above, KV4_ERR_UNSUPPORTED for a
- * KV4_FORMAT_NVFP4 cache (append the projection's rows with kv4_append there).
+ * Errors: as kv4_append, KV4_ERR_INVALID_ARG for the sizes above.
  */
 kv4_status kv4_qkv_append(kv4_cache *cache, const void *x_dev, const void *w_qkv_dev, int num_q_heads,
                           int d_model, void *q_out_dev, const int32_t *cu_tokens_dev,

@@ -358,7 +358,6 @@ kv4_status kv4_qkv_append(kv4_cache* c, const void* x, const void* w, int num_q_
     if (!x || !w || !q_out || !cu_tokens || !slot_ids || !start_pos || !block_table || stride < 1)
         return KV4_ERR_INVALID_ARG;
     if (d_model % 64 != 0 || (num_q_heads * KV4_HEAD_DIM) % 256 != 0) return KV4_ERR_INVALID_ARG;
-    if (c->cfg.format == KV4_FORMAT_NVFP4) return KV4_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(q_out)) &
         15)
         return KV4_ERR_INVALID_ARG;

@@ -270,7 +270,8 @@ struct QkvArgs {
 // 32 (w % 4) ..), each a quarter of the 256 columns; all 16 share the append loop.
 constexpr int kQkvThreads = 512;
 
-template <bool KV8>
+// FMT: 0 the method's format (INT4 pages + side buffer), 1 the 8-bit format, 2 NVFP4
+template <int FMT>
 __global__ void __launch_bounds__(kQkvThreads, 1)
 kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                       const QkvArgs qa, int K)
@@ -318,7 +319,19 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
             vxA[0] = bf16_lo(vw2.x); vxA[1] = bf16_hi(vw2.x); vxA[2] = bf16_lo(vw2.y); vxA[3] = bf16_hi(vw2.y);
         }
         if (a.rope) warp_rope128(kxA, rope_row(a.rope + (int64_t)L.pos * kHeadDim, lane), lane);
-        if (KV8) {
+        if (FMT == 2) {
+            warp_fwht128(kxA, lane);
+            uint32_t kc[4], vc[4], ksb, vsb;
+            float kg, vg;
+            warp_quant_nvfp4(kxA, kc, ksb, kg);
+            warp_quant_nvfp4(vxA, vc, vsb, vg);
+            uint8_t* b = a.pages + ((int64_t)L.page * H + h) * kPageBlock4f;
+            store_nvfp4_k(b, ts, kc, ksb, kg, lane);
+            store_nvfp4_v(b + kFp4Half, ts, vc, vsb, vg, lane);
+            if (lane == 0 && h == 0 && tok == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+            continue;
+        }
+        if (FMT == 1) {
             warp_fwht128(kxA, lane);
             uint32_t k8[4], v8[4];
             __half k8d, k8m, v8d, v8m;
@@ -367,7 +380,7 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
 // The same with 128-wide tiles, for calls with few tokens (twice the CTAs): a tile is one
 // Q head, or the K or the V head of one KV head, appended with the K or V half of the
 // per-token routine (the same bytes as the combined one).
-template <bool KV8>
+template <int FMT>
 __global__ void __launch_bounds__(kQkvThreads, 1)
 kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                              const QkvArgs qa, int K)
@@ -409,7 +422,22 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
             xA[0] = bf16_lo(w2.x); xA[1] = bf16_hi(w2.x); xA[2] = bf16_lo(w2.y); xA[3] = bf16_hi(w2.y);
         }
         if (!is_v && a.rope) warp_rope128(xA, rope_row(a.rope + (int64_t)L.pos * kHeadDim, lane), lane);
-        if (KV8) {
+        if (FMT == 2) {
+            uint8_t* b = a.pages + ((int64_t)L.page * H + h) * kPageBlock4f;
+            uint32_t c4[4], sb4;
+            float g4;
+            if (!is_v) {
+                warp_fwht128(xA, lane);
+                warp_quant_nvfp4(xA, c4, sb4, g4);
+                store_nvfp4_k(b, ts, c4, sb4, g4, lane);
+                if (lane == 0 && h == 0 && tok == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+            } else {
+                warp_quant_nvfp4(xA, c4, sb4, g4);
+                store_nvfp4_v(b + kFp4Half, ts, c4, sb4, g4, lane);
+            }
+            continue;
+        }
+        if (FMT == 1) {
             uint8_t* g = a.pages + ((int64_t)L.page * H + h) * kPageBlock8;
             uint32_t c8[4];
             __half d8, m8;
@@ -525,15 +553,11 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [smem_w, smem_n]() {
         const int sw = (int)smem_w, sn = (int)smem_n;
-        attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, sw);
-        if (attr == cudaSuccess)
-            attr = cudaFuncSetAttribute(kv4_qkv_append_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, sw);
-        if (attr == cudaSuccess)
-            attr = cudaFuncSetAttribute(kv4_qkv_append_narrow_kernel<false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
-        if (attr == cudaSuccess)
-            attr = cudaFuncSetAttribute(kv4_qkv_append_narrow_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
+        for (auto k : {kv4_qkv_append_kernel<0>, kv4_qkv_append_kernel<1>, kv4_qkv_append_kernel<2>})
+            if (attr == cudaSuccess) attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sw);
+        for (auto k : {kv4_qkv_append_narrow_kernel<0>, kv4_qkv_append_narrow_kernel<1>,
+                       kv4_qkv_append_narrow_kernel<2>})
+            if (attr == cudaSuccess) attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
     });
     if (attr != cudaSuccess) return attr;
     int dev = 0, sms = 0;
@@ -542,13 +566,15 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     const int mt = (T + kBM - 1) / kBM;
     if ((int64_t)mt * (N / 256) >= sms) {
         const dim3 grid((unsigned)(N / 256), (unsigned)mt);
-        if (ap.kv8) kv4_qkv_append_kernel<true><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
-        else kv4_qkv_append_kernel<false><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+        if (ap.fp4) kv4_qkv_append_kernel<2><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+        else if (ap.kv8) kv4_qkv_append_kernel<1><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+        else kv4_qkv_append_kernel<0><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
     } else {
         // few tokens: 128-wide tiles double the CTAs
         const dim3 grid((unsigned)(N / 128), (unsigned)mt);
-        if (ap.kv8) kv4_qkv_append_narrow_kernel<true><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
-        else kv4_qkv_append_narrow_kernel<false><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+        if (ap.fp4) kv4_qkv_append_narrow_kernel<2><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+        else if (ap.kv8) kv4_qkv_append_narrow_kernel<1><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+        else kv4_qkv_append_narrow_kernel<0><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
     }
     return cudaGetLastError();
 }

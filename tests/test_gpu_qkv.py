@@ -1,7 +1,7 @@
 """The fused projection + append (kv4_qkv_append) against the same two steps done
 apart: kv4_linear_bf16 (pinned against a float32 matmul) followed by kv4_append
 (pinned against the oracle). Pages, side buffers, slot lengths and the projected
-queries must agree byte for byte, for both cache formats, with and without RoPE,
+queries must agree byte for byte, for all three cache formats, with and without RoPE,
 over chunked appends that start at unaligned positions."""
 import numpy as np
 import pytest
@@ -80,21 +80,22 @@ def _case(H, Hq, d_model, lens, cuts, fmt, s, w, rope, seed):
 
 
 LENS = [300, 1000, 129, 5, 17]
+FORMATS = [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0), (kv4.FORMAT_NVFP4, 0, 0)]
 
 
-@pytest.mark.parametrize("fmt,s,w", [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0)])
+@pytest.mark.parametrize("fmt,s,w", FORMATS)
 @pytest.mark.parametrize("rope", [False, True])
 def test_fused_equals_projection_then_append(fmt, s, w, rope):
     _case(2, 8, 256, LENS, [], fmt, s, w, rope, seed=11)
 
 
-@pytest.mark.parametrize("fmt,s,w", [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0)])
+@pytest.mark.parametrize("fmt,s,w", FORMATS)
 def test_fused_chunked_appends(fmt, s, w):
     cuts = [1, 3, 17, 100, 250, 600] + [L - 1 for L in LENS]
     _case(2, 8, 256, LENS, cuts, fmt, s, w, True, seed=12)
 
 
-@pytest.mark.parametrize("fmt,s,w", [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0)])
+@pytest.mark.parametrize("fmt,s,w", FORMATS)
 def test_fused_wide_tiles(fmt, s, w):
     """Enough tokens for 256-wide tiles (K and V of a head in one tile); the cases above
     take 128-wide tiles (K or V alone)."""
