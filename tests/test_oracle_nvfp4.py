@@ -20,11 +20,6 @@ D = 128
 GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
 
 
-def bf16_round(x32):
-    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16) \
-        .to(torch.float32).numpy().astype(np.float64)
-
-
 def nearest_e2m1(v):
     """Brute force: the grid point nearest |v| (ties: the even code), clamped to 6."""
     a = min(abs(float(v)), 6.0)
