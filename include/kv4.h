@@ -267,6 +267,9 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  * split-K scratch in a 16 MiB array that libkv4 reserves statically on every
  * GPU that loads it, until the process exits. The call itself allocates
  * nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * A page is read whole, including its slots past a sequence's length, whose
+ * scores are masked: those slots must hold finite metadata and scales, as a
+ * zeroed pool (what kv4_cache_create makes) or earlier appends leave them.
  *   config          : the cache geometry the pools were built with
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
  *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8 or
