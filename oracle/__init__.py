@@ -27,4 +27,5 @@ from .kv4_oracle import (  # noqa: F401
     e2m1_rn,
     e2m1_value,
     quant_nvfp4,
+    quant_mxfp4,
 )

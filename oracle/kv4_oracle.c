@@ -78,6 +78,16 @@
  *      group's positions (2^-126 below the normal range), so no fp16 weight before the
  *      block scale exceeds 1, and the group's sum is scaled by 2^k. The normaliser sums
  *      the plain p.
+ *   R13 MXFP4, the other 4-bit floating-point format the pages name beside NVFP4
+ *      ([zh] 技术新颖性, 未来方向), as the public OCP microscaling format defines it:
+ *      per block of 32 values one shared E8M0 scale X = 2^s with
+ *      s = floor(log2 max|x|) − 2 (2 being the largest E2M1 exponent), held in
+ *      [−127, 127], and each value e2m1(x / X), nearest with ties to even, held at ±6;
+ *      an all-zero block takes s = −127 and zero codes. No per-vector scale. Decode
+ *      keeps the INT8 query: the score is fl(fl(acc·s_q)·C) with acc the fma chain
+ *      fmaf(2^s_b, dot_b, acc) over the four blocks of exact block dots; PV as R12, with
+ *      weights w_ib = fp16(fp16(p_i)·2^(s_ib − k)), 2^k the largest block scale of the
+ *      group's positions, exact E2M1 values and the group's sum scaled by 2^k.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -413,6 +423,45 @@ static float score_nvfp4(const uint8_t *codes, const uint8_t *bscale, float g, c
     return ((acc * g) * q_scale) * C;
 }
 
+/* ---- MXFP4 (reading R13): E2M1 elements, one E8M0 scale per 32 values ---- */
+
+/* One 128-value vector to MXFP4: per block b of 32 values the shared exponent
+   s = floor(log2 amax_b) − 2, held in [−127, 127] (stored biased, s + 127), and the codes
+   e2m1(x · 2^−s); an all-zero block stores s = −127 and zero codes. */
+void orc_quant_mxfp4(const float *x, uint8_t *codes, uint8_t *escale)
+{
+    for (int b = 0; b < ORC_D / 32; b++) {
+        float amax = 0.0f;
+        for (int i = 0; i < 32; i++) amax = fmaxf(amax, fabsf(x[32 * b + i]));
+        int sx = -127;
+        if (amax > 0.0f) {
+            int k;
+            frexpf(amax, &k);                   /* amax in [2^(k-1), 2^k): floor(log2) = k - 1 */
+            sx = k - 1 - 2;
+            if (sx < -127) sx = -127;
+            if (sx > 127) sx = 127;
+        }
+        escale[b] = (uint8_t)(sx + 127);
+        for (int i = 0; i < 32; i++)
+            codes[32 * b + i] = amax > 0.0f ? orc_e2m1_rn(ldexpf(x[32 * b + i], -sx)) : 0;
+    }
+}
+
+/* R13 score of an MXFP4 key: the exact dot of each 32-value block with the INT8 query,
+   scaled by the block's power of two in an fma chain over the blocks in order, then by
+   s_q and C. */
+static float score_mxfp4(const uint8_t *codes, const uint8_t *escale, const int8_t *q8,
+                         float q_scale, float C)
+{
+    float acc = 0.0f;
+    for (int b = 0; b < ORC_D / 32; b++) {
+        double db = 0.0;
+        for (int i = 0; i < 32; i++) db += (double)orc_e2m1_value(codes[32 * b + i]) * (double)q8[32 * b + i];
+        acc = fmaf(ldexpf(1.0f, (int)escale[b] - 127), (float)db, acc);
+    }
+    return (acc * q_scale) * C;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Cache state                                                               */
 /* ------------------------------------------------------------------------ */
@@ -437,6 +486,11 @@ static void append_one(orc_cache *c, int slot, int pos, int head,
                        const float *k_rot, const float *v)
 {
     size_t mi = idx_main(c, slot, pos, head);
+    if (c->format == ORC_FMT_MXFP4) {               /* R13: MXFP4 codes and scales */
+        orc_quant_mxfp4(k_rot, c->k4_code + mi * ORC_D, c->k_bscale + mi * 8);
+        orc_quant_mxfp4(v, c->v4_code + mi * ORC_D, c->v_bscale + mi * 8);
+        return;
+    }
     if (c->format == ORC_FMT_NVFP4) {               /* R12: NVFP4 codes and scales */
         orc_quant_nvfp4(k_rot, c->k4_code + mi * ORC_D, c->k_bscale + mi * 8, c->k_gscale + mi);
         orc_quant_nvfp4(v, c->v4_code + mi * ORC_D, c->v_bscale + mi * 8, c->v_gscale + mi);
@@ -626,6 +680,7 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
        position, groups of 16 consecutive positions, codes from the main arrays. ---- */
     const int is8 = c->format != ORC_FMT_HYBRID;     /* KV8 and NVFP4: every position, in pages */
     const int isf4 = c->format == ORC_FMT_NVFP4;
+    const int ismx = c->format == ORC_FMT_MXFP4;
     const uint8_t *k8c = is8 ? c->k4_code : c->k8_code;
     const uint8_t *v8c = is8 ? c->v4_code : c->v8_code;
     const uint16_t *k8d = is8 ? c->k4_delta : c->k8_delta;
@@ -648,6 +703,12 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
             if (pos[i] < 0) continue;
             const size_t si = is8 ? idx_main(c, slot, g0 + i, head) : idx_side(c, slot, g0 + i, head);
             rix[i] = si;
+            if (ismx) {                              /* R13 */
+                sg[i] = score_mxfp4(k8c + si * ORC_D, c->k_bscale + si * 8, q8, q_scale, C);
+                if (dbg_sigma) dbg_sigma[pos[i]] = sg[i];
+                if (sg[i] > Mg) Mg = sg[i];
+                continue;
+            }
             if (isf4) {                              /* R12 */
                 sg[i] = score_nvfp4(k8c + si * ORC_D, c->k_bscale + si * 8, c->k_gscale[si], q8,
                                     q_scale, C);
@@ -667,6 +728,15 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         double og[ORC_D];
         double lg = 0.0;
         for (int j = 0; j < ORC_D; j++) og[j] = 0.0;
+        /* R13: 2^mxk, the largest block scale of the group's positions */
+        int mxk = -127;
+        if (ismx) {
+            for (int i = 0; i < n; i++) {
+                if (pos[i] < 0) continue;
+                for (int bb = 0; bb < ORC_D / 32; bb++)
+                    if ((int)c->v_bscale[rix[i] * 8 + bb] - 127 > mxk) mxk = (int)c->v_bscale[rix[i] * 8 + bb] - 127;
+            }
+        }
         /* R12: the power of two 2^k just above the largest V vector scale of the group */
         int f4k = -126;
         if (isf4) {
@@ -689,7 +759,17 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                                   ? (double)p
                                   : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
             const uint8_t *vc = v8c + si * ORC_D;
-            if (isf4) {                              /* R12 */
+            if (ismx) {                              /* R13 */
+                const float p16 = (float)orc_f16_to_f64(orc_f32_to_f16(p, ORC_RN));
+                for (int bb = 0; bb < ORC_D / 32; bb++) {
+                    const int sb = (int)c->v_bscale[si * 8 + bb] - 127;
+                    const double wb = (pv_mode == ORC_PV_FLOAT)
+                                          ? ldexp((double)p, sb)
+                                          : orc_f16_to_f64(orc_f32_to_f16(ldexpf(p16, sb - mxk), ORC_RN));
+                    for (int j = 32 * bb; j < 32 * bb + 32; j++)
+                        og[j] += wb * (double)orc_e2m1_value(vc[j]);
+                }
+            } else if (isf4) {                       /* R12 */
                 const float gi = c->v_gscale[si];
                 if (pv_mode == ORC_PV_FLOAT) {       /* exact values, unrounded p */
                     for (int j = 0; j < ORC_D; j++)
@@ -717,6 +797,8 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         }
         if (isf4 && pv_mode != ORC_PV_FLOAT)
             for (int j = 0; j < ORC_D; j++) og[j] = ldexp(og[j], f4k);
+        if (ismx && pv_mode != ORC_PV_FLOAT)
+            for (int j = 0; j < ORC_D; j++) og[j] = ldexp(og[j], mxk);
         const float Mn = (Mg > Mr) ? Mg : Mr;
         const double a = (Mr == -INFINITY) ? 0.0 : exp2((double)Mr - (double)Mn);
         const double bsc = exp2((double)Mg - (double)Mn);

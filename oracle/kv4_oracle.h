@@ -27,7 +27,7 @@ extern "C" {
 /* FP16 rounding modes for orc_f32_to_f16. */
 enum { ORC_RN = 0, ORC_RD = 1, ORC_RU = 2 };
 /* Cache formats. */
-enum { ORC_FMT_HYBRID = 0, ORC_FMT_KV8 = 1, ORC_FMT_NVFP4 = 2 };
+enum { ORC_FMT_HYBRID = 0, ORC_FMT_KV8 = 1, ORC_FMT_NVFP4 = 2, ORC_FMT_MXFP4 = 3 };
 /* PV modes for the INT4 region of orc_decode. */
 enum { ORC_PV_INTEGER = 0, ORC_PV_FLOAT = 1 };
 
@@ -40,7 +40,9 @@ typedef struct {
     int32_t format;      /* ORC_FMT_HYBRID: INT4 main cache + INT8 side buffer; ORC_FMT_KV8:
                             whole-cache INT8 (the main arrays hold 8-bit codes); ORC_FMT_NVFP4:
                             whole-cache NVFP4 (E2M1 codes in the main arrays, block and vector
-                            scales below); the last two have sink = window = 0 */
+                            scales below); ORC_FMT_MXFP4: whole-cache MXFP4 (E2M1 codes in the
+                            main arrays, E8M0 scales of the four 32-value blocks in the first
+                            four block-scale bytes); the last three have sink = window = 0 */
     /* INT4 main cache: codes [slot][pos][head][128] in 0..15 (0..255 in KV8), meta
        [slot][pos][head] fp16 bits */
     uint8_t  *k4_code, *v4_code;
@@ -90,6 +92,7 @@ float   orc_e4m3_value(uint8_t bits);
 uint8_t orc_e2m1_rn(float v);               /* sign | magnitude code, nearest even, saturating at 6 */
 float   orc_e2m1_value(uint8_t code);
 void    orc_quant_nvfp4(const float *x, uint8_t *codes, uint8_t *bscale, float *gscale);
+void    orc_quant_mxfp4(const float *x, uint8_t *codes, uint8_t *escale);
 
 /* whole path */
 int orc_append(orc_cache *c, int slot, int start, int T,

@@ -41,6 +41,7 @@ def load():
         lib.orc_e2m1_value.argtypes = [C.c_uint8]
         lib.orc_e2m1_value.restype = C.c_float
         lib.orc_quant_nvfp4.argtypes = [P, P, P, P]
+        lib.orc_quant_mxfp4.argtypes = [P, P, P]
         lib.orc_quant_affine.argtypes = [P, C.c_int, C.c_int, P, P, P]
         lib.orc_quant_query.argtypes = [P, P, P, P]
         lib.orc_append.argtypes = [P, C.c_int, C.c_int, C.c_int, P, P]
@@ -151,6 +152,16 @@ def quant_nvfp4(x):
     return codes, bs, np.float32(g[0])
 
 
+def quant_mxfp4(x):
+    """(codes uint8[128], E8M0 scale bytes uint8[4] = shared exponent + 127), reading R13."""
+    x = _c(x, np.float32)
+    assert x.shape == (D,)
+    codes = np.empty(D, np.uint8)
+    es = np.empty(4, np.uint8)
+    load().orc_quant_mxfp4(_p(x), _p(codes), _p(es))
+    return codes, es
+
+
 def quant_affine(x, levels):
     """Returns (codes uint8[n], delta fp16 bits, min fp16 bits)."""
     x = _c(x, np.float32)
@@ -197,16 +208,20 @@ class OracleCache:
     """Logical KV4 cache state: INT4 main cache for every position plus the
     bounded INT8 side buffer (s sink + w recent positions) per slot. With
     kv8=True, the whole-cache 8-bit configuration (reading R10): 8-bit codes for
-    every position, no side buffer (sink = window = 0)."""
+    every position, no side buffer (sink = window = 0). With nvfp4=True or mxfp4=True,
+    the whole-cache 4-bit floating-point configurations of readings R12 and R13."""
 
     def __init__(self, num_heads, sink, window, max_len, num_slots=1, kv8=False, rope=None,
-                 nvfp4=False):
-        if (kv8 or nvfp4) and (sink or window):
-            raise ValueError("the KV8 and NVFP4 configurations have no protected region")
+                 nvfp4=False, mxfp4=False):
+        if (kv8 or nvfp4 or mxfp4) and (sink or window):
+            raise ValueError("the KV8, NVFP4 and MXFP4 configurations have no protected region")
+        if int(bool(kv8)) + int(bool(nvfp4)) + int(bool(mxfp4)) > 1:
+            raise ValueError("one cache format at a time")
         H, S = num_heads, sink + window
         self.kv8 = bool(kv8)
         self.nvfp4 = bool(nvfp4)
-        self.format = 2 if nvfp4 else (1 if kv8 else 0)
+        self.mxfp4 = bool(mxfp4)
+        self.format = 3 if mxfp4 else (2 if nvfp4 else (1 if kv8 else 0))
         self.H, self.s, self.w, self.max_len, self.num_slots = H, sink, window, max_len, num_slots
         z = np.zeros
         self.k4_code = z((num_slots, max_len, H, D), np.uint8)
@@ -222,7 +237,8 @@ class OracleCache:
         self.v8_delta = z((num_slots, S, H), np.uint16)
         self.v8_min = z((num_slots, S, H), np.uint16)
         self.length = z((num_slots,), np.int32)
-        # reading R12 (NVFP4): E4M3 block scales and the FP32 vector scale per token-head
+        # reading R12 (NVFP4): E4M3 block scales and the FP32 vector scale per token-head;
+        # reading R13 (MXFP4): E8M0 scales of the four 32-value blocks in bytes 0..3
         self.k_bscale = z((num_slots, max_len, H, 8), np.uint8)
         self.v_bscale = z((num_slots, max_len, H, 8), np.uint8)
         self.k_gscale = z((num_slots, max_len, H), np.float32)
