@@ -189,8 +189,9 @@ kv4_status kv4_cache_set_rope(kv4_cache *cache, const float *cos_sin_dev, int ma
  * KV4_FORMAT_NVFP4 caches store the NVFP4 codes and scales of rotated K and V:
  * g = amax / 2688, s_b = e4m3(amax_b / fl(6 g)), code = e2m1(x * fl(1 / fl(s_b g)))
  * (nearest, ties to even, saturating).
- *   k_bf16_dev, v_bf16_dev : [total_tokens][H_kv][128] bf16, tokens of sequence i
- *                            at rows cu_tokens[i] .. cu_tokens[i+1]-1
+ *   k_bf16_dev, v_bf16_dev : [total_tokens][H_kv][128] bf16, finite, tokens of sequence
+ *                            i at rows cu_tokens[i] .. cu_tokens[i+1]-1 (an infinite or
+ *                            NaN value makes its token-head's codes and scales undefined)
  *   cu_tokens_dev          : [n_seqs+1] int32, non-decreasing, cu[0] = 0, cu[n] = total_tokens
  *   slot_ids_dev           : [n_seqs] int32 side-buffer slot of each sequence (distinct)
  *   start_pos_dev          : [n_seqs] int32 position of each sequence's first new token
