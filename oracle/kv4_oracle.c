@@ -45,12 +45,15 @@
  *      2^-64 keeps only its offsets (ŵ = 0).
  *   R6 Scores are log2-domain: σ = fl(fl(u · s_q) · C), u = fmaf(Δ, dot, fl(m · Σq8)),
  *      C = fl(sm_scale · log2 e).
- *   R7 Protected PV ("BF16 PV, FP32 accumulation"): the side rows are taken in
- *      groups of 16 in side-row order (sink rows, then ring slots); in each group
- *      p = exp2(σ − M_group) with the exp2 below and the group's own max; the
- *      product uses p and v = bf16(fmaf(Δ8, c, m8)) both rounded to BF16 and sums
- *      in FP32; groups are combined by 2^(M_group − M) like INT4 pages; the
- *      normaliser sums the unrounded p. Float mode keeps p unrounded.
+ *   R7 Protected PV ("BF16 PV, FP32 accumulation"): the protected positions are
+ *      taken in position order, grouped by their 16-position page of the paged
+ *      cache (the unit R5 uses for the INT4 weights; a page may hold both sink and
+ *      window positions, or only part of either). In each page
+ *      p = exp2(σ − M_page) with the exp2 below and the max over the page's
+ *      protected positions; the product uses p and v = bf16(fmaf(Δ8, c, m8)) both
+ *      rounded to BF16 and sums in FP32; pages are combined by 2^(M_page − M) like
+ *      INT4 pages; the normaliser sums the unrounded p. Float mode keeps p
+ *      unrounded. Where a side row sits in the side buffer plays no part.
  *   R10 KV8, the 8-bit whole-cache configuration the pages compare KV4 against
  *      ([zh] 核心发现 (2), (3); 实验结果, decode-forward replay): every position holds
  *      the 8-bit affine codes of the side cache (rotated K, unrotated V, the R2
@@ -71,13 +74,15 @@
  *      s_b = e4m3(amax_b / fl(6g)); each value is e2m1(x · fl(1/fl(s_b g))), nearest
  *      with ties to even. The whole cache is NVFP4 (no protected region). Decode keeps the
  *      INT8 query: the score is ((Σ_b fma-chained s_b·dot_b)·g·s_q)·C with each block dot
- *      exact. PV runs in groups of 16 consecutive positions with the group's own max as in
+ *      exact. PV runs per page (16 consecutive positions) with the page's own max as in
  *      R7, but the value scales move to the weights: the E2M1 values enter exactly, and
  *      position i of head h weighs w_ib = fp16(fp16(fl(p_i·g_i)·2^-k)·s_ib) in block b,
  *      where 2^k is the power of two just above the largest V vector scale g of the
- *      group's positions (2^-126 below the normal range), so no fp16 weight before the
- *      block scale exceeds 1, and the group's sum is scaled by 2^k. The normaliser sums
- *      the plain p.
+ *      page's positions (2^-126 below the normal range), and the page's sum is scaled
+ *      by 2^k. 2^k is a property of the stored values alone, like the block scales:
+ *      p ≤ 1 and g < 2^k put every fp16 weight before the block scale at or below 1,
+ *      so it neither overflows nor loses the largest value's precision to a scale
+ *      that depends on the softmax. The normaliser sums the plain p.
  *   R13 MXFP4, the other 4-bit floating-point format the pages name beside NVFP4
  *      ([zh] 技术新颖性, 未来方向), as the public OCP microscaling format defines it:
  *      per block of 32 values one shared E8M0 scale X = 2^s with
@@ -87,7 +92,7 @@
  *      keeps the INT8 query: the score is fl(fl(acc·s_q)·C) with acc the fma chain
  *      fmaf(2^s_b, dot_b, acc) over the four blocks of exact block dots; PV as R12, with
  *      weights w_ib = fp16(fp16(p_i)·2^(s_ib − k)), 2^k the largest block scale of the
- *      group's positions, exact E2M1 values and the group's sum scaled by 2^k.
+ *      page's positions, exact E2M1 values and the page's sum scaled by 2^k.
  * Everything after the integer decisions (page outputs, region merges,
  * the protected path, the final normalisation) is carried in double here.
  */
@@ -568,25 +573,19 @@ static int32_t dot_s8_u8(const int8_t *a, const uint8_t *b)
     return s;
 }
 
-/* Position held by side row i (R4, R7): sink row i < s holds position i when
-   i < L; ring row s + k holds the latest position p < L with p mod w == k, which
-   is protected when p >= max(s, L - w). -1 when the row holds no protected
-   position. */
-static int side_row_position(int i, int s, int w, int L)
+/* Side row that holds protected position t (R4): sink row t for t < s, ring row
+   s + t mod w otherwise (a ring row keeps the latest position with its residue,
+   which for a protected t >= max(s, L - w) is t itself). */
+static int side_row_of(int t, int s, int w)
 {
-    if (i < s) return (i < L) ? i : -1;
-    const int k = i - s;
-    if (L - 1 < k) return -1;
-    const int p = k + w * ((L - 1 - k) / w);
-    const int lo = (L - w > s) ? L - w : s;
-    return (p >= lo) ? p : -1;
+    return (t < s) ? t : s + t % w;
 }
 
 /* One q head against one sequence. Returns output (normalised) and lse (natural log). */
 static void decode_head(const orc_cache *c, int slot, int L, int head,
                         const int8_t *q8, float q_scale, int32_t q_sum, float C,
                         int pv_mode, double *out, double *lse,
-                        int32_t *dbg_qk, float *dbg_sigma, uint8_t *dbg_w)
+                        int32_t *dbg_qk, float *dbg_sigma, uint8_t *dbg_w, uint16_t *dbg_p)
 {
     const int s = c->sink, w = c->window, P = 16;
     /* Regions, reading R4 (R10: no INT4 region in KV8). */
@@ -673,11 +672,13 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
         }
     }
 
-    /* ---- protected region (R7): INT8 side keys and BF16 values, side rows in
-       groups of 16 in side-row order, p against each group's own max; the
-       product takes p rounded to BF16 (integer mode) or unrounded (float mode);
-       the normaliser sums the unrounded p. KV8 (R10): the same over every
-       position, groups of 16 consecutive positions, codes from the main arrays. ---- */
+    /* ---- protected region (R7): the protected positions in position order, taken
+       by their 16-position page of the paged cache (the unit of R5's INT4 weights);
+       INT8 side keys and BF16 values, p against the page's own max over its
+       protected positions; the product takes p rounded to BF16 (integer mode) or
+       unrounded (float mode); the normaliser sums the unrounded p. KV8, NVFP4 and
+       MXFP4 (R10, R12, R13): every position is protected, codes from the main
+       arrays, so a group is a whole page. ---- */
     const int is8 = c->format != ORC_FMT_HYBRID;     /* KV8 and NVFP4: every position, in pages */
     const int isf4 = c->format == ORC_FMT_NVFP4;
     const int ismx = c->format == ORC_FMT_MXFP4;
@@ -691,17 +692,19 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
     double lp_ = 0.0;
     double opr[ORC_D];
     for (int j = 0; j < ORC_D; j++) opr[j] = 0.0;
-    const int S = is8 ? L : s + w;               /* rows: side rows, or positions in KV8 */
-    for (int g0 = 0; g0 < S; g0 += 16) {
-        const int n = (S - g0 < 16) ? S - g0 : 16;
+    /* R4: protected = [0, min(s, L)) ∪ [max(s, L − w), L); whole-cache formats: [0, L) */
+    const int win_lo = is8 ? 0 : ((L - w > s) ? L - w : s);
+    for (int g0 = 0; g0 < L; g0 += P) {
+        const int n = (L - g0 < P) ? L - g0 : P;
         int pos[16];
         size_t rix[16];
         float sg[16];
         float Mg = -INFINITY;
         for (int i = 0; i < n; i++) {
-            pos[i] = is8 ? g0 + i : side_row_position(g0 + i, s, w, L);
+            const int t = g0 + i;
+            pos[i] = (is8 || t < s || t >= win_lo) ? t : -1;
             if (pos[i] < 0) continue;
-            const size_t si = is8 ? idx_main(c, slot, g0 + i, head) : idx_side(c, slot, g0 + i, head);
+            const size_t si = is8 ? idx_main(c, slot, t, head) : idx_side(c, slot, side_row_of(t, s, w), head);
             rix[i] = si;
             if (ismx) {                              /* R13 */
                 sg[i] = score_mxfp4(k8c + si * ORC_D, c->k_bscale + si * 8, q8, q_scale, C);
@@ -722,13 +725,13 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
             if (dbg_sigma) dbg_sigma[pos[i]] = sg[i];
             if (sg[i] > Mg) Mg = sg[i];
         }
-        if (Mg == -INFINITY) continue;               /* no protected row in this group */
-        /* the group's output relative to its own max, then folded into the region
+        if (Mg == -INFINITY) continue;               /* no protected position in this page */
+        /* the page's output relative to its own max, then folded into the region
            total relative to the running max */
         double og[ORC_D];
         double lg = 0.0;
         for (int j = 0; j < ORC_D; j++) og[j] = 0.0;
-        /* R13: 2^mxk, the largest block scale of the group's positions */
+        /* R13: 2^mxk, the largest block scale of the page's positions */
         int mxk = -127;
         if (ismx) {
             for (int i = 0; i < n; i++) {
@@ -737,7 +740,7 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                     if ((int)c->v_bscale[rix[i] * 8 + bb] - 127 > mxk) mxk = (int)c->v_bscale[rix[i] * 8 + bb] - 127;
             }
         }
-        /* R12: the power of two 2^k just above the largest V vector scale of the group */
+        /* R12: the power of two 2^k just above the largest V vector scale of the page */
         int f4k = -126;
         if (isf4) {
             float mx = 0.0f;
@@ -759,8 +762,10 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                                   ? (double)p
                                   : (double)orc_bf16_to_f32(orc_f32_to_bf16_rn(p));
             const uint8_t *vc = v8c + si * ORC_D;
+            if (dbg_p) dbg_p[pos[i]] = orc_f32_to_bf16_rn(p);
             if (ismx) {                              /* R13 */
                 const float p16 = (float)orc_f16_to_f64(orc_f32_to_f16(p, ORC_RN));
+                if (dbg_p) dbg_p[pos[i]] = orc_f32_to_f16(p, ORC_RN);
                 for (int bb = 0; bb < ORC_D / 32; bb++) {
                     const int sb = (int)c->v_bscale[si * 8 + bb] - 127;
                     const double wb = (pv_mode == ORC_PV_FLOAT)
@@ -778,6 +783,7 @@ static void decode_head(const orc_cache *c, int slot, int L, int head,
                 } else {                             /* fp16 weights carrying the value scales */
                     const float wn = ldexpf(p * gi, -f4k);
                     const float w1 = (float)orc_f16_to_f64(orc_f32_to_f16(wn, ORC_RN));
+                    if (dbg_p) dbg_p[pos[i]] = orc_f32_to_f16(wn, ORC_RN);
                     for (int bb = 0; bb < ORC_D / 16; bb++) {
                         const float sb = orc_e4m3_value(c->v_bscale[si * 8 + bb]);
                         const double wb = orc_f16_to_f64(orc_f32_to_f16(w1 * sb, ORC_RN));
@@ -859,7 +865,8 @@ int orc_decode(const orc_cache *c, int slot, int L, int G, const uint16_t *q_bf1
                     out + (size_t)hq * ORC_D, lse + hq,
                     dbg && dbg->qk ? dbg->qk + (size_t)hq * L : NULL,
                     dbg && dbg->sigma ? dbg->sigma + (size_t)hq * L : NULL,
-                    dbg && dbg->w_hat ? dbg->w_hat + (size_t)hq * L : NULL);
+                    dbg && dbg->w_hat ? dbg->w_hat + (size_t)hq * L : NULL,
+                    dbg && dbg->p_bits ? dbg->p_bits + (size_t)hq * L : NULL);
     }
     return 0;
 }
@@ -876,7 +883,7 @@ static int decode_one_head(const orc_cache *c, int slot, int L, int G, int hq,
     query_rope(c, L, qx);
     orc_fwht128(qx, qr);
     orc_quant_query(qr, q8, &q_scale, &q_sum);
-    decode_head(c, slot, L, hq / G, q8, q_scale, q_sum, C, pv_mode, out, lse, NULL, NULL, NULL);
+    decode_head(c, slot, L, hq / G, q8, q_scale, q_sum, C, pv_mode, out, lse, NULL, NULL, NULL, NULL);
     return 0;
 }
 

@@ -72,6 +72,10 @@ typedef struct {
     int32_t *qk;        /* [HG][L] integer QK accumulator of the region that owns the position */
     float   *sigma;     /* [HG][L] log2-domain score */
     uint8_t *w_hat;     /* [HG][L] u8 PV weight (INT4 region only; 0 elsewhere) */
+    uint16_t *p_bits;   /* [HG][L] bits of each protected position's PV weight as the
+                           product takes it: BF16 p (hybrid protected region, KV8), fp16
+                           fl(p·g)·2^-k (NVFP4, before the block scale), fp16 p (MXFP4);
+                           0 in the INT4 region */
 } orc_debug;
 
 /* number formats */

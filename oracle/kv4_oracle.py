@@ -201,7 +201,7 @@ class _State(C.Structure):
 
 
 class _Debug(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in ("q8", "q_scale", "q_sum", "qk", "sigma", "w_hat")]
+    _fields_ = [(n, C.c_void_p) for n in ("q8", "q_scale", "q_sum", "qk", "sigma", "w_hat", "p_bits")]
 
 
 class OracleCache:
@@ -282,9 +282,9 @@ class OracleCache:
             dbg = dict(q8=np.zeros((HG, D), np.int8), q_scale=np.zeros(HG, np.float32),
                        q_sum=np.zeros(HG, np.int32), qk=np.zeros((HG, n), np.int32),
                        sigma=np.full((HG, n), np.nan, np.float32),
-                       w_hat=np.zeros((HG, n), np.uint8))
+                       w_hat=np.zeros((HG, n), np.uint8), p_bits=np.zeros((HG, n), np.uint16))
             dptr = _Debug(*[dbg[k].ctypes.data for k in ("q8", "q_scale", "q_sum", "qk",
-                                                         "sigma", "w_hat")])
+                                                         "sigma", "w_hat", "p_bits")])
         rc = load().orc_decode(C.byref(self._st), slot, L, G, _p(q), C.c_float(sm_scale),
                                pv_mode, _p(out), _p(lse),
                                C.byref(dptr) if dptr is not None else None)
