@@ -22,6 +22,9 @@
  *     records the first such error in a device error word, read with
  *     kv4_get_device_error(). No call traps, aborts or throws across the ABI.
  *   - head_dim is 128 and page_size is 16; other values return KV4_ERR_UNSUPPORTED.
+ *   - A call that takes a cache runs on the device the cache was created on: it makes
+ *     that device current for the call and restores the caller's device before it
+ *     returns. The stream passed must belong to that device.
  */
 #ifndef KV4_H
 #define KV4_H
@@ -38,7 +41,8 @@ typedef struct kv4_cache kv4_cache;
 typedef enum {
     KV4_OK = 0,
     KV4_ERR_INVALID_ARG = -1,   /* null pointer, negative size, inconsistent sizes */
-    KV4_ERR_UNSUPPORTED = -2,   /* head_dim != 128, page_size != 16, s + w > 256, group size */
+    KV4_ERR_UNSUPPORTED = -2,   /* head_dim != 128, page_size != 16, s + w > 256, s or w not a
+                                   multiple of 16, group size */
     KV4_ERR_OUT_OF_MEMORY = -3, /* a pool or workspace allocation failed at create */
     KV4_ERR_CUDA = -4,          /* a CUDA runtime call failed; the cache stays usable if it can */
     KV4_ERR_OUT_OF_RANGE = -5,  /* batch, q heads or tokens above the cache's configured limits */
@@ -73,13 +77,15 @@ typedef struct {
     int32_t head_dim;        /* must be 128 (one quantization group per token-head, [zh] 分组仿射 KV 量化) */
     int32_t page_size;       /* must be 16 */
     int32_t sink;            /* s >= 0: INT8-protected sink positions (16 in [zh] 核心方法) */
-    int32_t window;          /* w >= 0: INT8-protected recent positions (128 in [zh] 核心方法); s + w <= 256 */
+    int32_t window;          /* w >= 0: INT8-protected recent positions (128 in [zh] 核心方法); s + w <= 256;
+                                s and w multiples of 16 (the protected weights are formed per page,
+                                and this keeps each page's protected rows in one side group) */
     int64_t num_pages;       /* physical pages in the INT4 pool (each holds 16 positions of every KV head) */
     int32_t max_slots;       /* sequences that own a side buffer (slot ids are 0 .. max_slots-1) */
     int32_t max_batch;       /* largest batch of one decode call */
     int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
-    int32_t max_work_items;  /* ignored (kept for layout stability): the decode workspace is sized
-                                from max_batch, max_q_heads and the device's SM count */
+    int32_t max_work_items;  /* reserved: must be >= 0 and is otherwise ignored (the decode
+                                workspace is sized from max_batch, max_q_heads and the SM count) */
     int32_t format;          /* kv4_format; KV4_FORMAT_INT8 and KV4_FORMAT_NVFP4 require
                                 sink = window = 0 */
 } kv4_cache_config;
@@ -210,17 +216,23 @@ kv4_status kv4_append(kv4_cache *cache, const void *k_bf16_dev, const void *v_bf
  * Per q head (q head hq uses KV head hq / G, G = num_q_heads / H_kv):
  *   q' = Hadamard(q); q8 = rint(q' * 127/max|q'|) with s_q = max|q'|/127.
  *   INT4 region [s, L-w): integer dot q8 . c, score scale/offset applied after
- *     the dot; per page, u8 weights w^ = rint(255 * p'Delta_V / max) from
- *     p' = 2^(sigma - page max), integer PV sum w^ * c_V, rescaled in FP32.
+ *     the dot; per page, p' = 2^(sigma - page max) and w = p' * Delta_V, quantized to
+ *     u8 with one power-of-two scale per page: e = floor(log2 max w),
+ *     w^ = min(rint(w * 2^(7-e)), 255); integer PV sum w^ * c_V, page output
+ *     2^(e-7) * sum + sum p' * m_V, pages rescaled in FP32.
  *   Protected region [0, min(s,L)) U [max(s, L-w), L): the same q8 against INT8
- *     side keys; side values dequantized to bf16; PV accumulated in FP32.
+ *     side keys; per 16-position page of the protected positions, p = 2^(sigma -
+ *     that page's max) rounded to bf16, side values dequantized to bf16, PV
+ *     accumulated in FP32.
  *   The regions' outputs and log-normalizers are merged exactly (log-sum-exp),
  *   split-K partials over pages likewise.
  *   KV4_FORMAT_INT8 caches: every position takes the protected region's arithmetic
- *   (INT8 keys, bf16 values, FP32 PV) from its page, 16 positions per group.
+ *   (INT8 keys, bf16 weights and values, FP32 PV) from its page.
  *   KV4_FORMAT_NVFP4 caches: the same q8 against the E2M1 keys, block dots exact and
- *   scaled after the dot (fma chain over the blocks), values bf16(e2m1 * fl(s_b g)),
- *   bf16 weights, FP32 PV, 16 positions per group.
+ *   scaled after the dot (fma chain over the blocks, then g, s_q); per page, the exact
+ *   E2M1 values times fp16 weights that carry the value scales,
+ *   fp16(fp16(p * g * 2^-k) * s_b) with 2^k the power of two just above the page's
+ *   largest V vector scale, FP32 PV scaled by 2^k.
  *   q_bf16_dev       : [batch][num_q_heads][128] bf16 (post-RoPE, unrotated)
  *   slot_ids_dev     : [batch] int32
  *   context_lens_dev : [batch] int32 L_b, including the token appended this step;
@@ -248,6 +260,9 @@ kv4_status kv4_decode_attention(kv4_cache *cache, const void *q_bf16_dev, int nu
  *                integer dot, and the record holds the bits of the FP32 score sigma
  *                (log2 domain: the block-scaled dot times g, s_q and sm_scale * log2 e)
  *   w_hat_dev  : [batch][num_q_heads][debug_stride] u8 PV weight per INT4-region position
+ *   p_bits_dev : [batch][num_q_heads][debug_stride] uint16 bits of the PV weight of each
+ *                protected position as the product takes it: BF16 p (hybrid protected
+ *                region, KV4_FORMAT_INT8), fp16 p·g·2^-k before the block scale (NVFP4)
  * Positions >= debug_stride are not written. For tests; slower than the plain call.
  */
 kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, int num_q_heads,
@@ -255,7 +270,8 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
                                       const int32_t *block_table_dev, int block_table_stride,
                                       int batch, float sm_scale, float *out_dev, float *lse_dev,
                                       int8_t *q8_dev, float *q_scale_dev, int32_t *qk_dev,
-                                      uint8_t *w_hat_dev, int debug_stride, void *stream);
+                                      uint8_t *w_hat_dev, uint16_t *p_bits_dev, int debug_stride,
+                                      void *stream);
 
 /*
  * kv4_decode_attention_noalloc — the same decode attention for callers that
@@ -276,16 +292,23 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8 or
  *                     KV4_FORMAT_NVFP4 configuration)
  *   other arguments : as kv4_decode_attention
- * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB: 144 bytes
- * per q head, 4 bytes per (sequence, KV head) and G * 520 bytes for each of
- * 2 * batch * H_kv + (persistent warps: 16 per SM) partials (on a 152-SM GB300 with
- * H_q = 32, H_kv = 8 that is batch <= 308); larger calls return KV4_ERR_OUT_OF_RANGE
- * before anything is enqueued. The first call on each device looks up the scratch
- * array's device address with that device current; make that first call before any
- * stream capture. Every call on a device shares the one array and leaves its contents
- * behind (each call writes everything it reads there before reading it), so calls
- * whose kernels overlap on the GPU race: issue them on one stream. Device-side index
- * errors are skipped without a report (there is no cache error word here).
+ * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB. The
+ * workspace is six sections, each rounded up to a multiple of 256 bytes: a 16-byte
+ * plan header; 4 * (batch + 1) bytes of cost starts; 4 * (batch * H_kv + 1) bytes of
+ * unit offsets; 144 bytes per q head (batch * H_q); and 8 * G and 512 * G bytes for
+ * each of 2 * batch * H_kv + W partials, W being the persistent warps of the decode
+ * grid (16 per resident CTA, one CTA per SM on a GB300). On a 152-SM GB300 with
+ * H_q = 32, H_kv = 8 that admits batch <= 308. The limit depends on the SM count and
+ * the occupancy; KV4_ERR_OUT_OF_RANGE, returned before anything is enqueued, is the
+ * authoritative check. The first call on each device looks up the device addresses of
+ * the scratch array and of an error word with that device current; make that first
+ * call before any stream capture. Every call on a device shares the one array and
+ * leaves its contents behind (each call writes everything it reads there before
+ * reading it), so calls whose kernels overlap on the GPU race: issue them on one
+ * stream. Device-side errors (index errors, which are skipped, and staging waits that
+ * gave up, which leave out and lse of that call incomplete) go to that error word,
+ * first error wins: read it with kv4_get_device_error(NULL, ...) with the device
+ * current.
  */
 kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
                                         const void *page_pool_dev, const void *side_pool_dev,
@@ -299,7 +322,8 @@ kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
 /*
  * kv4_linear_bf16 — Y = X · Wᵀ on the tcgen05 tensor cores (the QKV projection ahead
  * of the cache): BF16 inputs, FP32 accumulation in tensor memory, BF16 output
- * (round to nearest). Tiles of 128 × 128 outputs, TMA loads with a 128-byte swizzle.
+ * (round to nearest). Tiles of 128 × 256 outputs (128 × 128 when 256-wide tiles would
+ * leave SMs idle), TMA loads with a 128-byte swizzle.
  *   x_dev   : [M][K] bf16, K contiguous, 16-byte aligned
  *   w_dev   : [N][K] bf16, K contiguous (the nn.Linear weight layout), 16-byte aligned
  *   y_dev   : [M][N] bf16, 16-byte aligned
@@ -349,7 +373,9 @@ kv4_status kv4_profile_start(kv4_cache *cache, int max_calls);
 kv4_status kv4_profile_stop(kv4_cache *cache, kv4_profile *out);
 
 /* Read (synchronously: waits for the device) and optionally clear the device
- * error word. *code receives a kv4_device_error value. Returns KV4_OK. */
+ * error word of a cache, or, with cache = NULL, the error word that
+ * kv4_decode_attention_noalloc reports to on the current device. *code receives a
+ * kv4_device_error value. Errors: KV4_ERR_INVALID_ARG (code NULL), KV4_ERR_CUDA. */
 kv4_status kv4_get_device_error(kv4_cache *cache, int32_t *code, int clear);
 
 /* Static description of a status code. */

@@ -74,6 +74,30 @@ kv4_status check_launch(cudaError_t e)
     return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
 }
 
+// Makes a cache's device current for one call and restores the caller's device after,
+// so a call made with another device current still runs where the cache lives.
+class DeviceScope {
+  public:
+    explicit DeviceScope(int dev)
+    {
+        ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+        if (ok_ && prev_ != dev) {
+            ok_ = cudaSetDevice(dev) == cudaSuccess;
+            switched_ = ok_;
+        }
+    }
+    ~DeviceScope()
+    {
+        if (switched_) cudaSetDevice(prev_);
+    }
+    bool ok() const { return ok_; }
+
+  private:
+    int prev_ = 0;
+    bool ok_ = false;
+    bool switched_ = false;
+};
+
 }  // namespace
 
 extern "C" {
@@ -105,6 +129,9 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
         return KV4_ERR_INVALID_ARG;
     const bool kv8 = cfg->format == KV4_FORMAT_INT8, fp4 = cfg->format == KV4_FORMAT_NVFP4;
     if ((kv8 || fp4) && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
+    // the protected weights are formed per page: a page's protected positions must sit in
+    // one side-buffer group of 16 rows, which s and w multiples of 16 guarantee
+    if (cfg->sink % KV4_PAGE_SIZE != 0 || cfg->window % KV4_PAGE_SIZE != 0) return KV4_ERR_UNSUPPORTED;
     if (cfg->max_q_heads % cfg->num_kv_heads != 0) return KV4_ERR_INVALID_ARG;
     const int gmax = cfg->max_q_heads / cfg->num_kv_heads;
     if (gmax > 4) return KV4_ERR_UNSUPPORTED;
@@ -200,6 +227,8 @@ kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t*
         return KV4_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 7) return KV4_ERR_INVALID_ARG;
     if ((int64_t)total_tokens * c->cfg.num_kv_heads > (int64_t)INT32_MAX * 8) return KV4_ERR_OUT_OF_RANGE;
+    DeviceScope dev(c->device);
+    if (!dev.ok()) return KV4_ERR_CUDA;
     kv4::AppendArgs a{};
     a.k = static_cast<const uint16_t*>(k);
     a.v = static_cast<const uint16_t*>(v);
@@ -231,7 +260,7 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
                                 const int32_t* slot_ids, const int32_t* context_lens,
                                 const int32_t* block_table, int stride, int batch, float sm_scale,
                                 float* out, float* lse, int8_t* dq8, float* dqs, int32_t* dqk,
-                                uint8_t* dw, int dbg_stride, void* stream)
+                                uint8_t* dw, uint16_t* dp, int dbg_stride, void* stream)
 {
     if (!c || batch < 0 || num_q_heads < 1 || stride < 0) return KV4_ERR_INVALID_ARG;
     if (batch == 0) return KV4_OK;
@@ -244,7 +273,9 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     const int G = num_q_heads / H;
     if (!group_supported(G)) return KV4_ERR_UNSUPPORTED;
     if (batch > c->cfg.max_batch || num_q_heads > c->cfg.max_q_heads) return KV4_ERR_OUT_OF_RANGE;
-    if ((dqk || dw) && dbg_stride < 1) return KV4_ERR_INVALID_ARG;
+    if ((dqk || dw || dp) && dbg_stride < 1) return KV4_ERR_INVALID_ARG;
+    DeviceScope dev(c->device);
+    if (!dev.ok()) return KV4_ERR_CUDA;
     kv4::DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.slot_ids = slot_ids;
@@ -280,6 +311,7 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.dbg_qscale = dqs;
     a.dbg_qk = dqk;
     a.dbg_w = dw;
+    a.dbg_p = dp;
     a.dbg_stride = dbg_stride;
     a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
     a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
@@ -295,23 +327,25 @@ kv4_status kv4_decode_attention(kv4_cache* c, const void* q, int num_q_heads, co
                                 int batch, float sm_scale, float* out, float* lse, void* stream)
 {
     return decode_common(c, q, num_q_heads, slot_ids, context_lens, block_table, stride, batch,
-                         sm_scale, out, lse, nullptr, nullptr, nullptr, nullptr, 0, stream);
+                         sm_scale, out, lse, nullptr, nullptr, nullptr, nullptr, nullptr, 0, stream);
 }
 
 kv4_status kv4_decode_attention_debug(kv4_cache* c, const void* q, int num_q_heads,
                                       const int32_t* slot_ids, const int32_t* context_lens,
                                       const int32_t* block_table, int stride, int batch,
                                       float sm_scale, float* out, float* lse, int8_t* q8,
-                                      float* q_scale, int32_t* qk, uint8_t* w_hat, int debug_stride,
-                                      void* stream)
+                                      float* q_scale, int32_t* qk, uint8_t* w_hat, uint16_t* p_bits,
+                                      int debug_stride, void* stream)
 {
     return decode_common(c, q, num_q_heads, slot_ids, context_lens, block_table, stride, batch,
-                         sm_scale, out, lse, q8, q_scale, qk, w_hat, debug_stride, stream);
+                         sm_scale, out, lse, q8, q_scale, qk, w_hat, p_bits, debug_stride, stream);
 }
 
 kv4_status kv4_profile_start(kv4_cache* c, int max_calls)
 {
     if (!c || max_calls < 1) return KV4_ERR_INVALID_ARG;
+    DeviceScope dev(c->device);
+    if (!dev.ok()) return KV4_ERR_CUDA;
     drop_events(c);
     c->events.resize((size_t)4 * max_calls, nullptr);
     for (auto& e : c->events)
@@ -331,6 +365,8 @@ kv4_status kv4_profile_stop(kv4_cache* c, kv4_profile* out)
     if (!c || !out) return KV4_ERR_INVALID_ARG;
     *out = kv4_profile{0, 0.f, 0.f, 0.f};
     if (!c->profiling) return KV4_OK;
+    DeviceScope dev(c->device);
+    if (!dev.ok()) return KV4_ERR_CUDA;
     kv4_status st = KV4_OK;
     for (int i = 0; i < c->prof_calls; ++i) {
         cudaEvent_t* e = &c->events[4 * i];
@@ -362,6 +398,8 @@ kv4_status kv4_qkv_append(kv4_cache* c, const void* x, const void* w, int num_q_
         15)
         return KV4_ERR_INVALID_ARG;
     if ((int64_t)total_tokens * c->cfg.num_kv_heads > (int64_t)INT32_MAX * 8) return KV4_ERR_OUT_OF_RANGE;
+    DeviceScope dev(c->device);
+    if (!dev.ok()) return KV4_ERR_CUDA;
     kv4::AppendArgs a{};
     a.cu_tokens = cu_tokens;
     a.slot_ids = slot_ids;
@@ -400,7 +438,10 @@ kv4_status kv4_linear_bf16(const void* x, const void* w, void* y, int M, int N, 
 
 kv4_status kv4_get_device_error(kv4_cache* c, int32_t* code, int clear)
 {
-    if (!c || !code) return KV4_ERR_INVALID_ARG;
+    if (!code) return KV4_ERR_INVALID_ARG;
+    if (!c) return kv4::noalloc_device_error(code, clear != 0) == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
+    DeviceScope dev(c->device);
+    if (!dev.ok()) return KV4_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return KV4_ERR_CUDA;
     if (cudaMemcpy(code, c->err, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
         return KV4_ERR_CUDA;

@@ -677,7 +677,7 @@ __device__ __forceinline__ int side_row_position(int rr, int s, int w, int L)
 // plain p.
 template <bool F16W>
 __device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, float2 sig, int lane,
-                                                float2 wsc, float inv, float up)
+                                                float2 wsc, float inv, float up, uint32_t& wbits)
 {
     const int gq = lane >> 2, tq = lane & 3;
     const int hs = 2 * (tq & 1) + (tq >> 1);
@@ -697,11 +697,12 @@ __device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, flo
     float fold = beta;
     if (F16W) {
         const float2 wn = __fmul2_rn(__fmul2_rn(pp, wsc), make_float2(inv, inv));
-        ps.wfrag[0][hs][wfrag_pos(gq)] = half2_u32(__floats2half2_rn(wn.x, wn.y));
+        wbits = half2_u32(__floats2half2_rn(wn.x, wn.y));
         fold = beta * up;
     } else {
-        ps.wfrag[0][hs][wfrag_pos(gq)] = bf16x2_u32(pp.x, pp.y);
+        wbits = bf16x2_u32(pp.x, pp.y);
     }
+    ps.wfrag[0][hs][wfrag_pos(gq)] = wbits;
     const int srcA = (lane & ~3) | (tq & 1);
     const float bA = __shfl_sync(kFull, fold, srcA), bB = __shfl_sync(kFull, fold, srcA | 2);
     if (__any_sync(kFull, alpha != 1.f)) {
@@ -716,6 +717,109 @@ __device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, flo
     }
     __syncwarp();
     return make_float2(bA, bB);
+}
+
+// Running-max step of a side group of the hybrid cache. A ring group whose residues the
+// window start cuts holds positions of two pages, the window's oldest and its newest;
+// each page's weights are formed against that page's own max. inA/inB say which of the
+// two column sets each of the lane's rows gq, gq + 8 belongs to (neither: a masked row);
+// each set holds the rows of one page. Set A's weights go to columns hs of the PV B
+// tile, set B's to columns 4 + hs (zero when the group holds one page). Lanes t' < 2
+// then accumulate set A's product and lanes t' >= 2 set B's, each with its page's fold
+// factors 2^(page max - running max), returned here; the two halves are added at the
+// end of the piece. wA, wB: the BF16 weight pairs written.
+__device__ __forceinline__ float2 group_weights_pages(ProtState& st, PairSmem& ps, float2 sig, bool inA0,
+                                                      bool inA1, bool inB0, bool inB1, int lane,
+                                                      uint32_t& wA, uint32_t& wB)
+{
+    const int gq = lane >> 2, tq = lane & 3;
+    const int hs = 2 * (tq & 1) + (tq >> 1);
+    // both pages' maxima in one reduction chain
+    float mA = fmaxf(inA0 ? sig.x : -INFINITY, inA1 ? sig.y : -INFINITY);
+    float mB = fmaxf(inB0 ? sig.x : -INFINITY, inB1 ? sig.y : -INFINITY);
+#pragma unroll
+    for (int msk = 4; msk < 32; msk <<= 1) {
+        mA = fmaxf(mA, __shfl_xor_sync(kFull, mA, msk));
+        mB = fmaxf(mB, __shfl_xor_sync(kFull, mB, msk));
+    }
+    const float Mn = fmaxf(st.M, fmaxf(mA, mB));
+    const bool none = (Mn == -INFINITY);
+    const float alpha = none ? 1.f : exp2_fast(st.M - Mn);
+    const float betaA = none ? 0.f : exp2_fast(mA - Mn);     // exp2(-inf) = 0 for a missing page
+    const float betaB = none ? 0.f : exp2_fast(mB - Mn);
+    st.M = Mn;
+    // each row against its own page's max; rows of neither page (masked, -inf) give 0
+    const float2 pp = exp2_poly2(__fadd2_rn(sig, make_float2(inA0 ? -mA : -mB, inA1 ? -mA : -mB)));
+    st.l = fmaf(st.l, alpha, fmaf(inA0 ? betaA : betaB, pp.x, (inA1 ? betaA : betaB) * pp.y));
+    wA = bf16x2_u32(inA0 ? pp.x : 0.f, inA1 ? pp.y : 0.f);
+    wB = bf16x2_u32(inB0 ? pp.x : 0.f, inB1 ? pp.y : 0.f);
+    ps.wfrag[0][hs][wfrag_pos(gq)] = wA;
+    ps.wfrag[0][4 + hs][wfrag_pos(gq)] = wB;
+    // fold factors: every lane of a scoring column holds its head's betaA and betaB after
+    // the reduction, so even rows publish betaA and odd rows betaB; lanes t' < 2 (set A)
+    // read an even row, lanes t' >= 2 (set B) an odd one
+    const float pub = (gq & 1) ? betaB : betaA;
+    const int src = ((lane & ~7) | ((tq >> 1) << 2)) | (tq & 1);
+    const float f0 = __shfl_sync(kFull, pub, src), f1 = __shfl_sync(kFull, pub, src | 2);
+    if (__any_sync(kFull, alpha != 1.f)) {
+        const int srcA = (lane & ~3) | (tq & 1);
+        const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            st.o[mm][0] *= aA;
+            st.o[mm][1] *= aB;
+            st.o[mm][2] *= aA;
+            st.o[mm][3] *= aB;
+        }
+    }
+    __syncwarp();
+    return make_float2(f0, f1);
+}
+
+// BF16 PV of one side group (values dequantized with each row's metadata, weights
+// from the B tile in shared memory), FP32 accumulation into the running output with
+// this lane's fold factors.
+__device__ __forceinline__ void prot_pv(ProtState& st, const PairSmem& ps, const uint8_t* pv, float2 fold,
+                                        int lane)
+{
+    const int gq = lane >> 2, tq = lane & 3;
+    const float bA = fold.x, bB = fold.y;
+    const uint2 bw = lds64(&ps.wfrag[0][gq][2 * tq]);
+    const uint4 vmw = lds128(pv + (kSideVMetaOff - kPageBlock) + 16 * tq);
+    const __half2 vt0 = u32_half2(vmw.x), vt8 = u32_half2(vmw.y);
+    const __half2 vt4 = u32_half2(vmw.z), vt12 = u32_half2(vmw.w);
+    const float2 dA = make_float2(__low2float(vt0), __low2float(vt8));
+    const float2 mA = make_float2(__high2float(vt0), __high2float(vt8));
+    const float2 dB = make_float2(__low2float(vt4), __low2float(vt12));
+    const float2 mB = make_float2(__high2float(vt4), __high2float(vt12));
+    uint4 vq[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vq[i] = lds128(pv + (kSideVCodeOff - kPageBlock) + 16 * (32 * i + lane));
+#pragma unroll
+    for (int mm = 0; mm < 8; ++mm) {
+        const uint4 q4 = vq[mm >> 1];
+        const uint32_t w0 = (mm & 1) ? q4.z : q4.x;      // dim 16 mm + gq
+        const uint32_t w1 = (mm & 1) ? q4.w : q4.y;      // dim 16 mm + gq + 8
+        uint32_t a0, a1, a2, a3;
+        dequant_word(w0, dA, mA, dB, mB, a0, a2);
+        dequant_word(w1, dA, mA, dB, mB, a1, a3);
+        float c[4];
+        mma_bf16(c, a0, a1, a2, a3, bw.x, bw.y, 0.f, 0.f, 0.f, 0.f);
+        st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
+        st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
+        st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
+        st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+    }
+    __syncwarp();
+}
+
+// Debug record of a lane's two rows: the bits of each row's weight (one half of wbits).
+__device__ __forceinline__ void record_weights(const DecodeArgs& a, int b, int hq, int pos0, int pos1,
+                                               uint32_t w0bits, uint32_t w1bits)
+{
+    const int64_t row = ((int64_t)b * a.num_q_heads + hq) * a.dbg_stride;
+    if (pos0 >= 0 && pos0 < a.dbg_stride) a.dbg_p[row + pos0] = (uint16_t)(w0bits & 0xffffu);
+    if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_p[row + pos1] = (uint16_t)(w1bits >> 16);
 }
 
 template <int G, bool DEBUG, bool KV8>
@@ -768,38 +872,30 @@ __device__ __forceinline__ void prot_group(const DecodeArgs& a, SplitSmem& sm, P
         if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_qk[row + pos1] = (int)dot.y;
     }
 
-    // ---- running max of head hs; weights relative to it, rounded to BF16 for PV
-    const float2 bAB = group_weights<false>(st, ps, sig, lane, make_float2(0.f, 0.f), 0.f, 0.f);
-    const float bA = bAB.x, bB = bAB.y;
-
-    // ---- BF16 PV, FP32 accumulation into the running output
-    const uint2 bw = lds64(&ps.wfrag[0][gq][2 * tq]);
-    const uint4 vmw = lds128(pv + (kSideVMetaOff - kPageBlock) + 16 * tq);
-    const __half2 vt0 = u32_half2(vmw.x), vt8 = u32_half2(vmw.y);
-    const __half2 vt4 = u32_half2(vmw.z), vt12 = u32_half2(vmw.w);
-    const float2 dA = make_float2(__low2float(vt0), __low2float(vt8));
-    const float2 mA = make_float2(__high2float(vt0), __high2float(vt8));
-    const float2 dB = make_float2(__low2float(vt4), __low2float(vt12));
-    const float2 mB = make_float2(__high2float(vt4), __high2float(vt12));
-    uint4 vq[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vq[i] = lds128(pv + (kSideVCodeOff - kPageBlock) + 16 * (32 * i + lane));
-#pragma unroll
-    for (int mm = 0; mm < 8; ++mm) {
-        const uint4 q4 = vq[mm >> 1];
-        const uint32_t w0 = (mm & 1) ? q4.z : q4.x;      // dim 16 mm + gq
-        const uint32_t w1 = (mm & 1) ? q4.w : q4.y;      // dim 16 mm + gq + 8
-        uint32_t a0, a1, a2, a3;
-        dequant_word(w0, dA, mA, dB, mB, a0, a2);
-        dequant_word(w1, dA, mA, dB, mB, a1, a3);
-        float c[4];
-        mma_bf16(c, a0, a1, a2, a3, bw.x, bw.y, 0.f, 0.f, 0.f, 0.f);
-        st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
-        st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
-        st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
-        st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+    if (KV8) {
+        // ---- a KV8 group is one page: weights against its max, BF16 PV
+        uint32_t wbits;
+        const float2 fold = group_weights<false>(st, ps, sig, lane, make_float2(0.f, 0.f), 0.f, 0.f, wbits);
+        if (DEBUG && a.dbg_p && hs < G) record_weights(a, b, h * G + hs, pos0, pos1, wbits, wbits);
+        prot_pv(st, ps, pv, fold, lane);
+        return;
     }
-    __syncwarp();
+    // ---- hybrid side group: weights per page of the positions its rows hold, against
+    // each page's own max. With s and w multiples of the page size (the host enforces it)
+    // all protected positions of a page sit in one side group, and a group holds at most
+    // two pages: a sink page, a whole window page, or the window's oldest and newest
+    // partial pages when the window start cuts a page (ring rows share residues mod w).
+    // Rows of the newest page (positions from ns = 16 floor((L - 1) / 16)) go to the
+    // second column set, every other row to the first, which separates the two pages of
+    // any group. (Taking the two-set step for every group measured faster than branching
+    // to the one-page step for groups that hold one page.)
+    const int ns = (L - 1) & ~(kPage - 1);
+    uint32_t wA, wB;
+    const float2 fold = group_weights_pages(st, ps, sig, pos0 >= 0 && pos0 < ns, pos1 >= 0 && pos1 < ns,
+                                            pos0 >= ns, pos1 >= ns, lane, wA, wB);
+    if (DEBUG && a.dbg_p && hs < G)
+        record_weights(a, b, h * G + hs, pos0, pos1, pos0 < ns ? wA : wB, pos1 < ns ? wA : wB);
+    prot_pv(st, ps, pv, fold, lane);
 }
 
 // ---------------------------------------------------------------- NVFP4 page
@@ -905,7 +1001,9 @@ __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, Pr
         if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_qk[row + pos1] = __float_as_int(sg.y);
     }
 
-    const float2 bAB = group_weights<true>(st, ps, sig, lane, vg, pinv, pup);
+    uint32_t wbits;
+    const float2 bAB = group_weights<true>(st, ps, sig, lane, vg, pinv, pup, wbits);
+    if (DEBUG && a.dbg_p && hs < G) record_weights(a, b, h * G + hs, pos0, pos1, wbits, wbits);
     const float bA = bAB.x, bB = bAB.y;
 
     // ---- fp16 PV, FP32 accumulation into the running output
@@ -1352,6 +1450,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             }
 #pragma unroll
             for (int msk = 4; msk < 32; msk <<= 1) st.l += __shfl_xor_sync(kFull, st.l, msk);
+            if (!KV8) {
+                // lanes t' >= 2 hold the products of the second column set: add them in
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) st.o[mm][r] += __shfl_xor_sync(kFull, st.o[mm][r], 2);
+            }
             int pidx;
             {
                 const Walk C = walk_load(Csm);
@@ -1530,7 +1635,7 @@ static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, 
 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
-    const bool dbg = a.dbg_q8 || a.dbg_qscale || a.dbg_qk || a.dbg_w;
+    const bool dbg = a.dbg_q8 || a.dbg_qscale || a.dbg_qk || a.dbg_w || a.dbg_p;
     const int sel = (dbg ? 1 : 0) + (a.fp4 ? 4 : a.kv8 ? 2 : 0);
     auto go = [&](auto g) -> cudaError_t {
         constexpr int Gc = decltype(g)::value;
@@ -1617,6 +1722,10 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;   // 16 MiB
 constexpr int kNoAllocMaxBatch = 4096;
 
 static __device__ __align__(256) unsigned char g_kv4_noalloc_scratch[kNoAllocScratchBytes];
+// Device error word of the allocation-free decode (first error wins, 0 = none), the
+// counterpart of a cache's error word: index errors and staging-wait timeouts of its
+// kernels land here.
+static __device__ int32_t g_kv4_noalloc_err;
 
 }  // namespace kv4
 
@@ -1627,6 +1736,7 @@ constexpr int kNoAllocMaxDevices = 64;
 struct NoAllocDevice {
     std::once_flag once;
     unsigned char* scratch = nullptr;   // device address of g_kv4_noalloc_scratch
+    int32_t* err = nullptr;             // device address of g_kv4_noalloc_err
     cudaError_t status = cudaSuccess;
     int grid[5] = {0, 0, 0, 0, 0};
 };
@@ -1644,6 +1754,9 @@ NoAllocDevice* noalloc_device(int dev)
         d->status = cudaGetSymbolAddress(&p, kv4::g_kv4_noalloc_scratch);
         if (d->status != cudaSuccess) return;
         d->scratch = static_cast<unsigned char*>(p);
+        d->status = cudaGetSymbolAddress(&p, kv4::g_kv4_noalloc_err);
+        if (d->status != cudaSuccess) return;
+        d->err = static_cast<int32_t*>(p);
         int sms = 0;
         d->status = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (d->status != cudaSuccess) return;
@@ -1675,6 +1788,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
         return KV4_ERR_INVALID_ARG;
     const bool kv8 = cfg->format != KV4_FORMAT_INT4_HYBRID;
     if (kv8 && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
+    if (cfg->sink % KV4_PAGE_SIZE != 0 || cfg->window % KV4_PAGE_SIZE != 0) return KV4_ERR_UNSUPPORTED;
     if (batch == 0) return KV4_OK;
     if (!page_pool_dev || (!side_pool_dev && !kv8) || !seq_len_dev || !q_bf16_dev || !slot_ids_dev ||
         !context_lens_dev || !block_table_dev || !out_dev || block_table_stride < 1)
@@ -1693,7 +1807,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     if (cudaGetDevice(&dev) != cudaSuccess) return KV4_ERR_CUDA;
     NoAllocDevice* d = noalloc_device(dev);
     if (!d) return KV4_ERR_UNSUPPORTED;
-    if (d->status != cudaSuccess || !d->scratch) return KV4_ERR_CUDA;
+    if (d->status != cudaSuccess || !d->scratch || !d->err) return KV4_ERR_CUDA;
     // a call whose workspace would not fit in the array is refused before anything runs
     if (decode_workspace_bytes(batch, num_q_heads, H, G, d->grid[G], nullptr, nullptr) >
         kNoAllocScratchBytes)
@@ -1720,7 +1834,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.side = static_cast<const uint8_t*>(side_pool_dev);
     a.side_block_bytes = (int64_t)((cfg->sink + cfg->window + 15) / 16) * kSideGroupBytes;
     a.seq_len = seq_len_dev;
-    a.err = nullptr;                      // no error word: device index errors are skipped silently
+    a.err = d->err;
     a.plan = ws.plan;
     a.cost_start = ws.cost_start;
     a.unit_seg = ws.unit_seg;
@@ -1735,3 +1849,20 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     const cudaError_t e = launch_decode(a, d->grid[G], static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
 }
+
+namespace kv4 {
+
+// Read (and optionally clear) the allocation-free decode's error word on the current
+// device. Synchronous; allocates nothing.
+cudaError_t noalloc_device_error(int32_t* code, bool clear)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(code, g_kv4_noalloc_err, sizeof(int32_t));
+    if (e == cudaSuccess && clear) {
+        const int32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_kv4_noalloc_err, &zero, sizeof(int32_t));
+    }
+    return e;
+}
+
+}  // namespace kv4

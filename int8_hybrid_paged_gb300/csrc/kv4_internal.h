@@ -122,6 +122,7 @@ struct DecodeArgs {
     float* dbg_qscale;
     int32_t* dbg_qk;
     uint8_t* dbg_w;
+    uint16_t* dbg_p;              // bits of each protected position's PV weight
     int32_t dbg_stride;
     int32_t kv8;                  // KV4_FORMAT_INT8 or NVFP4: every position a row of a page group
     int32_t fp4;                  // KV4_FORMAT_NVFP4
@@ -142,6 +143,9 @@ cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cu
 // Persistent decode CTAs that fit on one SM (occupancy of the split kernel); also
 // opts the kernel in to its shared memory on the current device.
 cudaError_t decode_ctas_per_sm(int group, int* ctas);
+// Read (synchronously) and optionally clear the error word of the allocation-free decode
+// on the current device.
+cudaError_t noalloc_device_error(int32_t* code, bool clear);
 // Bytes of a decode workspace for these sizes; with ws and base, also lays it out at base.
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int group, int grid,
                               DecodeWorkspace* ws, unsigned char* base);

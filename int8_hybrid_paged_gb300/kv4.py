@@ -82,7 +82,7 @@ def load(path: str = LIB_PATH):
     lib.kv4_cache_get_info.argtypes = [P, C.POINTER(kv4_cache_info)]
     lib.kv4_append.argtypes = [P, P, P, P, P, P, P, I, I, I, P]
     lib.kv4_decode_attention.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P]
-    lib.kv4_decode_attention_debug.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P, P, P, P, I, P]
+    lib.kv4_decode_attention_debug.argtypes = [P, P, I, P, P, P, I, I, F, P, P, P, P, P, P, P, I, P]
     lib.kv4_get_device_error.argtypes = [P, C.POINTER(C.c_int32), I]
     lib.kv4_profile_start.argtypes = [P, I]
     lib.kv4_decode_attention_noalloc.argtypes = [C.POINTER(kv4_cache_config), P, P, P, P, I, P,
@@ -227,18 +227,19 @@ def kv4_decode_attention(handle, q, slot_ids, context_lens, block_table, out, ls
 
 
 def kv4_decode_attention_debug(handle, q, slot_ids, context_lens, block_table, out, lse=None,
-                               q8=None, q_scale=None, qk=None, w_hat=None, sm_scale=None,
-                               stream=None):
+                               q8=None, q_scale=None, qk=None, w_hat=None, p_bits=None,
+                               sm_scale=None, stream=None):
     B, Hq = q.shape[0], q.shape[1]
     scale = float(HEAD_DIM ** -0.5 if sm_scale is None else sm_scale)
-    dstride = qk.shape[-1] if qk is not None else (w_hat.shape[-1] if w_hat is not None else 0)
+    dstride = next((t.shape[-1] for t in (qk, w_hat, p_bits) if t is not None), 0)
     _check(load().kv4_decode_attention_debug(
         handle, _ptr(q, torch.bfloat16, "q"), Hq, _ptr(slot_ids, torch.int32, "slot_ids"),
         _ptr(context_lens, torch.int32, "context_lens"),
         _ptr(block_table, torch.int32, "block_table"), block_table.shape[-1], B, scale,
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(q8, torch.int8, "q8"), _ptr(q_scale, torch.float32, "q_scale"),
-        _ptr(qk, torch.int32, "qk"), _ptr(w_hat, torch.uint8, "w_hat"), dstride,
+        _ptr(qk, torch.int32, "qk"), _ptr(w_hat, torch.uint8, "w_hat"),
+        _ptr(p_bits, torch.int16, "p_bits"), dstride,
         _stream(stream)), "kv4_decode_attention_debug")
 
 
@@ -263,6 +264,15 @@ def kv4_decode_attention_noalloc(config, page_pool_dev, side_pool_dev, seq_len_d
         _ptr(block_table, torch.int32, "block_table"), block_table.shape[-1], B, scale,
         _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _stream(stream)),
         "kv4_decode_attention_noalloc")
+
+
+def kv4_noalloc_device_error(clear=True) -> int:
+    """Error word of kv4_decode_attention_noalloc on the current device (kv4_device_error
+    code, 0 = none); waits for the device."""
+    code = C.c_int32(0)
+    _check(load().kv4_get_device_error(None, C.byref(code), 1 if clear else 0),
+           "kv4_get_device_error")
+    return int(code.value)
 
 
 def kv4_profile_start(handle, max_calls):

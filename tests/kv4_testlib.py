@@ -129,6 +129,30 @@ def unpack_side(side, side_block, H, S, slot, h):
     return k8, v8, km[:, 0], km[:, 1], vm[:, 0], vm[:, 1]
 
 
+class Guarded:
+    """A device tensor between two 256-byte guard bands of a known byte pattern; the
+    tensor starts 256 bytes into its allocation, so its alignment is kept."""
+    CANARY = 0xA5
+    GUARD = 256
+
+    def __init__(self, shape, dtype, fill=None):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((n + 2 * self.GUARD,), self.CANARY, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[self.GUARD:self.GUARD + n].view(dtype).view(shape)
+        if fill is not None:
+            self.t.fill_(fill)
+
+    @classmethod
+    def of(cls, src):
+        g = cls(tuple(src.shape), src.dtype)
+        g.t.copy_(src)
+        return g
+
+    def intact(self):
+        raw = self.raw.cpu().numpy()
+        return bool(np.all(raw[:self.GUARD] == self.CANARY) and np.all(raw[-self.GUARD:] == self.CANARY))
+
+
 class Setup:
     """A GPU cache and (for the sampled sequences) oracle caches over the same inputs."""
 
@@ -186,26 +210,90 @@ class Setup:
         return oc
 
     def decode(self, q, debug_stride=0, lens=None):
+        """One decode call: through the debug entry point when debug_stride > 0 (also
+        returning its records), else through plain kv4_decode_attention, the kernels
+        bench.py times. Every input and output sits between guard bands of a known byte
+        pattern that must come back intact, and the outputs start as NaN, so a stray
+        write or a missed one fails the test."""
         lens = self.lens if lens is None else lens
         B, Hq = q.shape[0], q.shape[1]
-        out = torch.empty((B, Hq, D), dtype=torch.float32, device="cuda")
-        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
-        slots = torch.arange(B, dtype=torch.int32, device="cuda")
-        cl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        bufs = {
+            "q": Guarded.of(q), "slots": Guarded.of(torch.arange(B, dtype=torch.int32, device="cuda")),
+            "lens": Guarded.of(torch.tensor(lens, dtype=torch.int32, device="cuda")),
+            "block_table": Guarded.of(self.bt_dev),
+            "out": Guarded((B, Hq, D), torch.float32, float("nan")),
+            "lse": Guarded((B, Hq), torch.float32, float("nan")),
+        }
+        args = (bufs["q"].t, bufs["slots"].t, bufs["lens"].t, bufs["block_table"].t,
+                bufs["out"].t, bufs["lse"].t)
+        dbg = None
         if debug_stride:
             from int8_hybrid_paged_gb300.kv4 import kv4_decode_attention_debug
-            q8 = torch.zeros((B, Hq, D), dtype=torch.int8, device="cuda")
-            qs = torch.zeros((B, Hq), dtype=torch.float32, device="cuda")
-            qk = torch.full((B, Hq, debug_stride), -(2 ** 31), dtype=torch.int32, device="cuda")
-            wh = torch.zeros((B, Hq, debug_stride), dtype=torch.uint8, device="cuda")
-            kv4_decode_attention_debug(self.cache.handle, q, slots, cl, self.bt_dev, out, lse,
-                                       q8, qs, qk, wh, sm_scale=1 / math.sqrt(D))
-            torch.cuda.synchronize()
-            return out, lse, dict(q8=q8.cpu().numpy(), q_scale=qs.cpu().numpy(),
-                                  qk=qk.cpu().numpy(), w_hat=wh.cpu().numpy())
-        self.cache.decode(q, slots, cl, self.bt_dev, out, lse, sm_scale=1 / math.sqrt(D))
+            bufs.update(q8=Guarded((B, Hq, D), torch.int8, 0), q_scale=Guarded((B, Hq), torch.float32, 0),
+                        qk=Guarded((B, Hq, debug_stride), torch.int32, -(2 ** 31)),
+                        w_hat=Guarded((B, Hq, debug_stride), torch.uint8, 0),
+                        p_bits=Guarded((B, Hq, debug_stride), torch.int16, 0))
+            kv4_decode_attention_debug(self.cache.handle, *args[:4], args[4], args[5],
+                                       bufs["q8"].t, bufs["q_scale"].t, bufs["qk"].t, bufs["w_hat"].t,
+                                       bufs["p_bits"].t, sm_scale=1 / math.sqrt(D))
+        else:
+            self.cache.decode(*args[:4], args[4], args[5], sm_scale=1 / math.sqrt(D))
         torch.cuda.synchronize()
-        return out, lse, None
+        for name, g in bufs.items():
+            assert g.intact(), f"decode wrote outside its {name} buffer"
+        if debug_stride:
+            dbg = {k: bufs[k].t.cpu().numpy() for k in ("q8", "q_scale", "qk", "w_hat")}
+            dbg["p_bits"] = bufs["p_bits"].t.cpu().numpy().view(np.uint16)
+        return bufs["out"].t, bufs["lse"].t, dbg
 
     def close(self):
         self.cache.close()
+
+
+ATOL, RTOL = 2e-3, 1e-2
+
+
+def protected_positions(L, s, w, whole_cache):
+    """Positions whose PV weight the protected arithmetic forms: every position in the
+    whole-cache formats, else [0, min(s, L)) ∪ [max(s, L − w), L)."""
+    if whole_cache:
+        return np.arange(L)
+    return np.array([t for t in range(L) if t < s or t >= max(s, L - w)], dtype=np.int64)
+
+
+def check_decode(st, q, bs, lens=None):
+    """Decode the whole batch through the debug entry point and through plain
+    kv4_decode_attention (the kernels bench.py times) and compare sequences bs with the
+    oracle: q8 and s_q, the QK record (integer dots, or the FP32 score bits of NVFP4),
+    the u8 INT4 weights and every protected weight bit for bit; outputs and
+    log-normalizers of both calls within 2e-3 abs / 1e-2 rel. Returns the worst output
+    difference."""
+    lens = st.lens if lens is None else lens
+    whole = st.kv8 or st.nvfp4
+    out, lse, dbg = st.decode(q, debug_stride=max(max(lens), 1), lens=lens)
+    pout, plse, _ = st.decode(q, lens=lens)
+    outs = [(out.cpu().numpy(), lse.cpu().numpy()), (pout.cpu().numpy(), plse.cpu().numpy())]
+    qb = inputs.bf16_bits(q)
+    worst = 0.0
+    for b in bs:
+        L = lens[b]
+        o_ref, lse_ref, d = st.oracle_for(b).decode(0, L, st.G, qb[b], 1 / math.sqrt(D), debug=True)
+        np.testing.assert_array_equal(dbg["q8"][b], d["q8"])
+        np.testing.assert_array_equal(dbg["q_scale"][b].view(np.uint32), d["q_scale"].view(np.uint32))
+        if L:
+            if st.nvfp4:
+                np.testing.assert_array_equal(dbg["qk"][b][:, :L], d["sigma"][:, :L].view(np.int32))
+            else:
+                np.testing.assert_array_equal(dbg["qk"][b][:, :L], d["qk"][:, :L])
+            r4 = np.setdiff1d(np.arange(L), protected_positions(L, st.s, st.w, whole))
+            np.testing.assert_array_equal(dbg["w_hat"][b][:, r4], d["w_hat"][:, r4])
+            prot = protected_positions(L, st.s, st.w, whole)
+            np.testing.assert_array_equal(dbg["p_bits"][b][:, prot], d["p_bits"][:, prot])
+        for o, l in outs:
+            np.testing.assert_allclose(o[b], o_ref, atol=ATOL, rtol=RTOL)
+            if L:
+                np.testing.assert_allclose(l[b], lse_ref, atol=ATOL, rtol=RTOL)
+                worst = max(worst, float(np.max(np.abs(o[b] - o_ref))))
+            else:
+                assert np.all(o[b] == 0) and np.all(np.isneginf(l[b]))
+    return worst

@@ -50,6 +50,8 @@ def _cfg(**kw):
     (dict(head_dim=64), -2),
     (dict(page_size=32), -2),
     (dict(sink=200, window=100), -2),
+    (dict(sink=5, window=128), -2),      # protected weights per page: s, w multiples of 16
+    (dict(sink=16, window=40), -2),
     (dict(max_q_heads=36), -1),          # not a multiple of H_kv
     (dict(max_q_heads=64), -2),          # group of 8
     (dict(num_kv_heads=0), -1),
@@ -74,5 +76,4 @@ def test_null_handles_are_rejected(lib):
     assert lib.kv4_append(None, None, None, None, None, None, None, 1, 1, 1, None) == -1
     assert lib.kv4_decode_attention(None, None, 32, None, None, None, 1, 1, 0.1, None, None,
                                     None) == -1
-    code = C.c_int32(0)
-    assert lib.kv4_get_device_error(None, C.byref(code), 0) == -1
+    assert lib.kv4_get_device_error(None, None, 0) == -1

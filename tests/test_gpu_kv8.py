@@ -4,7 +4,6 @@ KV8 configuration, through the C ABI, on the same seeded inputs.
 Bit-exact: 8-bit codes, fp16 Δ/m, slot lengths, INT8 query and its scale, integer QK
 accumulators. Floating point: outputs and log-normalizers within abs 2e-3 / rel 1e-2.
 """
-import math
 
 import numpy as np
 import pytest
@@ -12,11 +11,10 @@ import torch
 
 from int8_hybrid_paged_gb300 import build as kbuild
 from int8_hybrid_paged_gb300 import inputs, kv4
-from kv4_testlib import Setup, unpack_kv8_pages
+from kv4_testlib import Setup, check_decode, unpack_kv8_pages
 
 pytestmark = pytest.mark.gpu
 D = 128
-ATOL, RTOL = 2e-3, 1e-2
 EDGE_LENS = [1, 15, 16, 17, 143, 144, 145, 160, 161, 300, 1000, 2049]
 
 
@@ -44,27 +42,6 @@ def check_state(st, bs):
             np.testing.assert_array_equal(vd, oc.v4_delta[0, :L, h])
             np.testing.assert_array_equal(vm, oc.v4_min[0, :L, h])
         assert lens[b] == L
-
-
-def check_decode(st, q, bs, lens=None):
-    lens = st.lens if lens is None else lens
-    out, lse, dbg = st.decode(q, debug_stride=max(max(lens), 1), lens=lens)
-    out, lse = out.cpu().numpy(), lse.cpu().numpy()
-    qb = inputs.bf16_bits(q)
-    worst = 0.0
-    for b in bs:
-        L = lens[b]
-        o_ref, lse_ref, d = st.oracle_for(b).decode(0, L, st.G, qb[b], 1 / math.sqrt(D), debug=True)
-        np.testing.assert_array_equal(dbg["q8"][b], d["q8"])
-        if L:
-            np.testing.assert_array_equal(dbg["qk"][b][:, :L], d["qk"][:, :L])
-            assert np.all(dbg["w_hat"][b][:, :L] == 0)
-            np.testing.assert_allclose(lse[b], lse_ref, atol=ATOL, rtol=RTOL)
-        else:
-            assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b]))
-        np.testing.assert_allclose(out[b], o_ref, atol=ATOL, rtol=RTOL)
-        worst = max(worst, float(np.max(np.abs(out[b] - o_ref))) if L else 0.0)
-    return worst
 
 
 @pytest.mark.parametrize("H,G", [(2, 4), (1, 1), (3, 2)])

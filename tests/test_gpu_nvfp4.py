@@ -6,7 +6,6 @@ over the block scales, times g, s_q and C). Floating point: outputs and log-norm
 within abs 2e-3 / rel 1e-2 (the PV weights are formed identically on both sides, so the
 observed worst case is asserted below 1e-4).
 """
-import math
 
 import numpy as np
 import pytest
@@ -14,11 +13,10 @@ import torch
 
 from int8_hybrid_paged_gb300 import build as kbuild
 from int8_hybrid_paged_gb300 import inputs, kv4
-from kv4_testlib import Setup, unpack_nvfp4_pages
+from kv4_testlib import Setup, check_decode, unpack_nvfp4_pages
 
 pytestmark = pytest.mark.gpu
 D = 128
-ATOL, RTOL = 2e-3, 1e-2
 EDGE_LENS = [1, 15, 16, 17, 143, 144, 145, 300, 1000]
 DECODE_LENS = [1, 15, 16, 17, 143, 144, 145, 160, 161, 300, 1000, 2049]
 
@@ -67,29 +65,6 @@ def test_large_append_all_heads_per_warp():
         assert st.cache.device_error() == 0
     finally:
         st.close()
-
-
-def check_decode(st, q, bs, lens=None):
-    lens = st.lens if lens is None else lens
-    out, lse, dbg = st.decode(q, debug_stride=max(max(lens), 1), lens=lens)
-    out, lse = out.cpu().numpy(), lse.cpu().numpy()
-    qb = inputs.bf16_bits(q)
-    worst = 0.0
-    for b in bs:
-        L = lens[b]
-        o_ref, lse_ref, d = st.oracle_for(b).decode(0, L, st.G, qb[b], 1 / math.sqrt(D), debug=True)
-        np.testing.assert_array_equal(dbg["q8"][b], d["q8"])
-        np.testing.assert_array_equal(dbg["q_scale"][b].view(np.uint32), d["q_scale"].view(np.uint32))
-        if L:
-            # the QK record of this format holds each score's FP32 bits
-            np.testing.assert_array_equal(dbg["qk"][b][:, :L], d["sigma"][:, :L].view(np.int32))
-            assert np.all(dbg["w_hat"][b][:, :L] == 0)
-            np.testing.assert_allclose(lse[b], lse_ref, atol=ATOL, rtol=RTOL)
-        else:
-            assert np.all(out[b] == 0) and np.all(np.isneginf(lse[b]))
-        np.testing.assert_allclose(out[b], o_ref, atol=ATOL, rtol=RTOL)
-        worst = max(worst, float(np.max(np.abs(out[b] - o_ref))) if L else 0.0)
-    return worst
 
 
 @pytest.mark.parametrize("H,G", [(2, 4), (1, 1), (3, 2)])

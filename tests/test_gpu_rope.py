@@ -26,7 +26,7 @@ def _lib():
     kv4.load()
 
 
-@pytest.mark.parametrize("H,G,s,w", [(2, 4, 16, 128), (1, 2, 0, 0), (3, 1, 5, 40)])
+@pytest.mark.parametrize("H,G,s,w", [(2, 4, 16, 128), (1, 2, 0, 0), (3, 1, 32, 32)])
 def test_hybrid_with_rope_matches_oracle(H, G, s, w):
     st = Setup(H, G, s, w, EDGE_LENS, seed=31 + H, rope=inputs.rope_table(2100))
     try:
