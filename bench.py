@@ -37,6 +37,8 @@ METRIC = "decode-attn context tokens/s and achieved HBM GB/s (% GB300 peak), 1 G
 UNIT = "context tokens/s"
 DTYPE = "s8 x u4/u8 -> s32 dots, fp32 softmax/accumulate"
 L2_BYTES = 129 * 2 ** 20
+LONG_TAIL_POOL_BYTES = 120 * 10 ** 9     # page budget of the 36-layer long-tail stack
+ORACLE_SAMPLE_SEQS = 16                  # sequences of the CPU oracle's timed sample
 SPLIT_SOURCES = ["int8_hybrid_paged_gb300/csrc/decode.cu",
                  "int8_hybrid_paged_gb300/csrc/device_common.cuh",
                  "int8_hybrid_paged_gb300/csrc/kv4_internal.h"]
@@ -207,6 +209,17 @@ def workload_from_args(args):
     return wl
 
 
+def pool_pages_for(wl):
+    """Physical pages of a workload's pool: its sequences' pages plus 1 % spare, or, for
+    the long-tail stack, the share of a 120 GB page budget that one of its layers gets
+    (pages scattered over the whole budget)."""
+    need = sum((L + 15) // 16 for L in wl.context_lens)
+    if wl.layers > 1:
+        budget = LONG_TAIL_POOL_BYTES // wl.layers
+        return max(need + 64, budget // (wl.num_kv_heads * 2176))
+    return need + max(64, need // 100)
+
+
 def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
     """Fill a cache with the workload's sequences (one prefill append). Host copies
     (bf16 bits) of the first `sample_seqs` sequences' K/V are kept for the CPU
@@ -215,8 +228,7 @@ def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
 
     lens = list(wl.context_lens)
     B, H, Hq = wl.batch, wl.num_kv_heads, wl.num_q_heads
-    need = sum((L + 15) // 16 for L in lens)
-    num_pages = need + max(64, need // 100)
+    num_pages = pool_pages_for(wl)
     bt = inputs.block_tables(lens, 16, num_pages, seed)
     cache = KV4Cache(H, num_pages, max_slots=B, max_batch=B, max_q_heads=Hq, sink=wl.sink,
                      window=wl.window, fmt=fmt)
@@ -242,8 +254,9 @@ def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
 
 
 def oracle_sample(wl, st, cpu_seconds, threads, kv8=False, nvfp4=False):
-    """Time the CPU oracle's decode over a bounded sample of the workload's sequences
-    (the same inputs as the GPU run). Returns the cpu_baseline dict."""
+    """Time the CPU oracle's decode over a bounded sample of the workload (its first
+    sequences, the same inputs as the GPU run): with OpenMP over (sequence, q head) on
+    the host cores, and with one thread. Returns the cpu_baseline dict."""
     import oracle
 
     lens = st["lens"]
@@ -258,18 +271,51 @@ def oracle_sample(wl, st, cpu_seconds, threads, kv8=False, nvfp4=False):
     slots = np.arange(len(pick), dtype=np.int32)
     sl = np.array([lens[b] for b in pick], np.int32)
     used = min(threads, len(pick) * wl.num_q_heads)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        oc.decode_batch(slots, sl, G, qb, 1 / math.sqrt(128), threads=used)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= cpu_seconds:
-            break
-    return {"value": float(sl.sum()) * reps / el, "unit": UNIT, "cores": used,
-            "kind": "oracle",
+
+    def timed(nthreads, seconds):
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oc.decode_batch(slots, sl, G, qb, 1 / math.sqrt(128), threads=nthreads)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return float(sl.sum()) * reps / el, reps, el
+
+    v_all, reps, el = timed(used, cpu_seconds)
+    v_one, reps1, el1 = timed(1, cpu_seconds / 2)
+    return {"value": v_all, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": f"first {len(pick)} of {len(lens)} sequences ({int(sl.sum())} context "
                       f"tokens, {wl.num_q_heads} q heads) x {reps} repetitions in {el:.1f} s, "
-                      f"OpenMP over (sequence, q head); host CPU: {cpu_model()}"}
+                      f"OpenMP over (sequence, q head); host CPU: {cpu_model()}",
+            "one_thread": {"value": v_one, "unit": UNIT, "cores": 1,
+                           "sample": f"the same sample x {reps1} repetitions in {el1:.1f} s"}}
+
+
+def call_bytes_for(wl, fmt):
+    """Algorithmic bytes of one decode call over the workload's batch (with the LSE)."""
+    lens, Hq, H = list(wl.context_lens), wl.num_q_heads, wl.num_kv_heads
+    if fmt == "int8":
+        return bytes_model.decode_call_bytes_kv8(lens, Hq, H, with_lse=True)
+    if fmt == "nvfp4":
+        return bytes_model.decode_call_bytes_nvfp4(lens, Hq, H, with_lse=True)
+    return bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
+
+
+def workload_config(wl, world, call_bytes, pool_pages, copies=1):
+    """The config object of a bench line (both arms print the same one)."""
+    per_cycle = call_bytes * copies * wl.layers
+    if copies > 1:
+        l2 = (f"{copies} distinct cache copies cycled: {per_cycle / 1e9:.2f} GB read per cycle vs "
+              f"{L2_BYTES / 2**20:.0f} MiB L2, no flush")
+    else:
+        l2 = (f"inputs larger than L2: {call_bytes / 1e9:.2f} GB read per call vs "
+              f"{L2_BYTES / 2**20:.0f} MiB L2, no flush")
+    return {"workload": wl.name, "batch": wl.batch, "q_heads": wl.num_q_heads,
+            "kv_heads": wl.num_kv_heads, "head_dim": 128, "page_size": 16, "sink": wl.sink,
+            "window": wl.window, "layers": wl.layers,
+            "context_tokens_per_step": int(sum(wl.context_lens)) * wl.layers * copies,
+            "max_context": max(wl.context_lens), "pool_pages": pool_pages, "l2": l2,
+            "parallelism": f"replicas x{world} (independent batches)"}
 
 
 # --------------------------------------------------------------------------- arms
@@ -285,7 +331,7 @@ def run_kv4(args, rank, world, local):
     kv8, fp4 = args.format == "int8", args.format == "nvfp4"
     seed = wl.seed + rank
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    st = build_workload(wl, seed, dev, sample_seqs=8 if want_cpu else 0,
+    st = build_workload(wl, seed, dev, sample_seqs=ORACLE_SAMPLE_SEQS if want_cpu else 0,
                         fmt=(kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_NVFP4 if fp4
                              else kv4.FORMAT_INT4_HYBRID))
     cache = st["cache"]
@@ -337,12 +383,7 @@ def run_kv4(args, rank, world, local):
     t_max, tok_sum = reduce_max_sum(world, ms, tokens_step * args.steps, dev)
     value = tok_sum / (t_max * 1e-3)
 
-    if kv8:
-        call_bytes = bytes_model.decode_call_bytes_kv8(lens, Hq, H, with_lse=True)
-    elif fp4:
-        call_bytes = bytes_model.decode_call_bytes_nvfp4(lens, Hq, H, with_lse=True)
-    else:
-        call_bytes = bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
+    call_bytes = call_bytes_for(wl, args.format)
     # the split kernel reads 144-byte query records (written by the prep kernel) instead
     # of the bf16 queries; the outputs are written by the merge
     split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
@@ -357,13 +398,7 @@ def run_kv4(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded bf16 N(0,1) K/V/q, 4 K outlier channels x20, lognormal lengths)",
-        "config": {"workload": wl.name, "batch": B, "q_heads": Hq, "kv_heads": H,
-                   "head_dim": 128, "page_size": 16, "sink": wl.sink, "window": wl.window,
-                   "layers": layers, "context_tokens_per_step": int(tokens_step),
-                   "max_context": max(lens), "pool_pages": st["num_pages"],
-                   "l2": f"inputs larger than L2: {call_bytes / 1e9:.2f} GB read per call "
-                         f"vs {L2_BYTES / 2**20:.0f} MiB L2, no flush",
-                   "parallelism": f"replicas x{world} (independent batches)"},
+        "config": workload_config(wl, world, call_bytes, st["num_pages"]),
         "achieved_hbm_gbs": step_gbs,
         "pct_hbm_peak": 100.0 * step_gbs / peak,
         "roofline": {"bound": "hbm", "kernel": "kv4_decode_split_kernel", "achieved": achieved,
@@ -388,6 +423,11 @@ def run_kv4(args, rank, world, local):
     hybrid = not (kv8 or fp4)
     if world == 1 and not args.no_qkv and hybrid:
         res["qkv_append"] = run_qkv_append(dev)
+
+    # ---- the other workloads of the method's configuration, rank 0 at N = 1
+    if world == 1 and not args.no_variants and hybrid and args.workload == "qwen3-8b":
+        res["qwen3_4b"] = run_cache_set("qwen3-4b", dev, peak, min(args.steps, 200))
+        res["long_tail"] = run_cache_set("long-tail", dev, peak, min(args.steps, 50))
 
     # ---- the same workload without the protected region (pure KV4), rank 0 at N = 1
     if world == 1 and not args.no_variants and hybrid and (wl.sink > 0 or wl.window > 0):
@@ -431,6 +471,80 @@ def time_calls(step, cache, steps, layers):
         step()
     torch.cuda.synchronize()
     return ms, kv4.kv4_profile_stop(cache.handle)
+
+
+def run_cache_set(name, dev, peak, steps):
+    """A workload over several caches at once, each step one decode call per cache:
+    the Qwen3-4B-shaped layer in 4 distinct copies cycled (one copy, about 0.13 GB per
+    call, is about the L2's size), or the long-tail stack of 36 layers (each its own
+    cache, pages scattered over a 120 GB page budget) with the 36 calls of a step
+    captured in one CUDA graph. Context tokens/s over the whole step, and the split
+    kernel's HBM rate from a second pass with events between the launches."""
+    from int8_hybrid_paged_gb300 import kv4
+
+    base = inputs.workload(name)
+    copies = 4 if base.layers == 1 else base.layers
+    B, Hq = base.batch, base.num_q_heads
+    sts = []
+    try:
+        for i in range(copies):
+            sts.append(build_workload(base, base.seed + 101 * (i + 1), dev))
+        out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+
+        def step():
+            stream = torch.cuda.current_stream(dev)     # the capture stream inside the graph
+            for st in sts:
+                kv4.kv4_decode_attention(st["cache"].handle, st["q"], st["slots"], st["cl"],
+                                         st["bt_dev"], out, lse, stream=stream)
+
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        del graph
+        ms = e0.elapsed_time(e1) / steps
+        # per-kernel times: eager calls with the library's events between the launches
+        for st in sts:
+            kv4.kv4_profile_start(st["cache"].handle, steps)
+        for _ in range(steps):
+            step()
+        torch.cuda.synchronize()
+        profs = [kv4.kv4_profile_stop(st["cache"].handle) for st in sts]
+        if any(st["cache"].device_error() for st in sts):
+            raise RuntimeError(f"device error in the {name} measurement")
+        call_bytes = call_bytes_for(base, "int4-hybrid")
+        split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
+        split_ms = sum(p["split_ms"] for p in profs) / max(1, sum(p["calls"] for p in profs))
+        gbs = split_bytes / (split_ms * 1e-3) / 1e9
+        tokens = float(sum(base.context_lens)) * copies
+        return {"case": base.name + (f", {copies} distinct cache copies cycled" if base.layers == 1 else
+                                     f", {copies} layer caches, one CUDA graph of {3 * copies} launches"
+                                     " per step"),
+                "value": tokens / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+                "config": workload_config(base, 1, call_bytes, sts[0]["num_pages"],
+                                          copies=copies if base.layers == 1 else 1),
+                "step_gbs": call_bytes * copies / (ms * 1e-3) / 1e9,
+                "step_frac_of_hbm_peak": call_bytes * copies / (ms * 1e-3) / 1e9 / peak,
+                "split_us": split_ms * 1e3, "split_algorithmic_bytes": split_bytes,
+                "split_achieved_gbs": gbs, "split_frac_of_hbm_peak": gbs / peak}
+    finally:
+        for st in sts:
+            st["cache"].close()
+        sts.clear()
+        torch.cuda.empty_cache()
 
 
 def run_unprotected(wl, seed, dev, peak, protected_value, steps):
@@ -527,6 +641,7 @@ def run_qkv_append(dev):
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak_tf = float(peaks.get("bf16_tflops", 1900.0))
+    peak_hbm = float(peaks.get("hbm_gbs", 6800.0))
     H, Hq, d = 8, 32, 4096
     N = (Hq + 2 * H) * 128
     g = torch.Generator(device=dev)
@@ -579,11 +694,19 @@ def run_qkv_append(dev):
             if caches[0].device_error() or caches[1].device_error():
                 raise RuntimeError("device error in the projection + append measurement")
             flops = 2.0 * B * T * N * d
+            # bytes the fused call must move: W_qkv and X read, Q written in bf16, the INT4
+            # pages and INT8 side rows of the new tokens written
+            side_rows = B * T if start_pos == 0 else B
+            nbytes = (N * d + B * T * d + B * T * Hq * 128) * 2 + \
+                bytes_model.append_call_bytes(B * T, H, min(side_rows, B * 144) * H) - B * T * H * 512
+            tfl = flops / (res["fused"] * 1e-3) / 1e12
+            gbs = nbytes / (res["fused"] * 1e-3) / 1e9
             out[tag] = {"case": f"{B} sequences x {T} token(s) from position {start_pos}: X [{B * T}][{d}] "
                                 f"x W_qkv [{N}][{d}], RoPE + Hadamard + 4-bit append of 8 KV heads",
                         "fused_us": res["fused"] * 1e3, "apart_us": res["apart"] * 1e3,
-                        "fused_tflops": flops / (res["fused"] * 1e-3) / 1e12,
-                        "fused_frac_of_bf16_peak": flops / (res["fused"] * 1e-3) / 1e12 / peak_tf,
+                        "bound": "tensor" if flops / nbytes > peak_tf * 1e12 / (peak_hbm * 1e9) else "hbm",
+                        "fused_tflops": tfl, "fused_frac_of_bf16_peak": tfl / peak_tf,
+                        "algorithmic_bytes": nbytes, "fused_gbs": gbs, "fused_frac_of_hbm_peak": gbs / peak_hbm,
                         "speedup_over_apart": res["apart"] / res["fused"]}
         finally:
             for c in caches:
@@ -740,7 +863,9 @@ def run_e2e(st, wl, args, dev, world):
 
 
 def run_reference(args, rank, world):
-    """The CPU oracle on the host cores, each step a bounded sample of the workload."""
+    """The CPU oracle on the host cores: every step decodes the same bounded sample as
+    the main line's cpu_baseline (the workload's first sequences, drawn with the same
+    recipe on the host), with OpenMP over (sequence, q head)."""
     if rank != 0:
         return
     import oracle
@@ -750,38 +875,22 @@ def run_reference(args, rank, world):
     lens = list(wl.context_lens)
     H, G, Hq = wl.num_kv_heads, wl.group, wl.num_q_heads
     threads = host_cores()
-    # budget per step so that warm-up + steps stay near two minutes
-    per_step_s = min(2.0, 120.0 / max(1, args.steps + args.warmup))
-    # calibrate on the first sequence, then size the per-step sample
-    kv = {}
-
-    def seq(b):
-        if b not in kv:
-            k, v = inputs.sequence_kv(b, lens[b], H, wl.seed)
-            kv[b] = (inputs.bf16_bits(k), inputs.bf16_bits(v))
-        return kv[b]
-
-    qb = inputs.bf16_bits(inputs.queries(wl.batch, Hq, wl.seed))
-
-    def make(nseq):
-        oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq,
-                                kv8=args.format == "int8", nvfp4=args.format == "nvfp4")
-        for i in range(nseq):
-            oc.append(i, 0, *seq(i))
-        return oc
-
-    oc = make(1)
-    t0 = time.perf_counter()
-    oc.decode_batch(np.zeros(1, np.int32), np.array(lens[:1], np.int32), G, qb[:1],
-                    1 / math.sqrt(128), threads=threads)
-    t1 = max(1e-4, time.perf_counter() - t0)
-    nseq = int(max(1, min(wl.batch, 64, per_step_s / t1)))
-    oc = make(nseq)
+    nseq = min(ORACLE_SAMPLE_SEQS, wl.batch)
+    seed = wl.seed
+    cu = np.concatenate([[0], np.cumsum(lens[:nseq])]).astype(np.int64)
+    k, v = inputs.kv_tokens(int(cu[-1]), H, seed * 1_000_003 + 17)
+    kb, vb = inputs.bf16_bits(k), inputs.bf16_bits(v)
+    qb = inputs.bf16_bits(inputs.queries(wl.batch, Hq, seed))[:nseq]
+    oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq,
+                            kv8=args.format == "int8", nvfp4=args.format == "nvfp4")
+    for i in range(nseq):
+        oc.append(i, 0, kb[cu[i]:cu[i + 1]], vb[cu[i]:cu[i + 1]])
     slots = np.arange(nseq, dtype=np.int32)
     sl = np.array(lens[:nseq], np.int32)
+    used = min(threads, nseq * Hq)
 
     def step():
-        oc.decode_batch(slots, sl, G, qb[:nseq], 1 / math.sqrt(128), threads=threads)
+        oc.decode_batch(slots, sl, G, qb, 1 / math.sqrt(128), threads=used)
 
     for _ in range(args.warmup):
         step()
@@ -790,14 +899,15 @@ def run_reference(args, rank, world):
         step()
     el = time.perf_counter() - t0
     value = float(sl.sum()) * args.steps / el
-    sample = (f"{nseq} of {len(lens)} sequences per step ({int(sl.sum())} context tokens, "
-              f"{Hq} q heads), OpenMP over sequences, host CPU: {cpu_model()}")
+    sample = (f"first {nseq} of {len(lens)} sequences per step ({int(sl.sum())} context tokens, "
+              f"{Hq} q heads; the main line's cpu_baseline sample, values drawn on the host), "
+              f"OpenMP over (sequence, q head); host CPU: {cpu_model()}")
     res = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "fp32/fp64 (CPU oracle)", "data": "synthetic",
-           "config": {"workload": wl.name, "batch": wl.batch, "q_heads": Hq, "kv_heads": H},
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "config": workload_config(wl, world, call_bytes_for(wl, args.format), pool_pages_for(wl)),
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
