@@ -64,8 +64,10 @@ typedef enum {
 typedef enum {
     KV4_FORMAT_INT4_HYBRID = 0,
     KV4_FORMAT_INT8 = 1,
-    KV4_FORMAT_NVFP4 = 2      /* NVFP4 for every position (E2M1 values, E4M3 scales per 16
+    KV4_FORMAT_NVFP4 = 2,     /* NVFP4 for every position (E2M1 values, E4M3 scales per 16
                                  dims, an FP32 scale per token-head vector), no side buffer */
+    KV4_FORMAT_MXFP4 = 3      /* MXFP4 for every position (E2M1 values, an E8M0 power-of-two
+                                 scale per 32 dims), no side buffer */
 } kv4_format;
 
 typedef struct {
@@ -80,8 +82,8 @@ typedef struct {
     int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
     int32_t max_work_items;  /* ignored (kept for layout stability): the decode workspace is sized
                                 from max_batch, max_q_heads and the device's SM count */
-    int32_t format;          /* kv4_format; KV4_FORMAT_INT8 and KV4_FORMAT_NVFP4 require
-                                sink = window = 0 */
+    int32_t format;          /* kv4_format; KV4_FORMAT_INT8, KV4_FORMAT_NVFP4 and
+                                KV4_FORMAT_MXFP4 require sink = window = 0 */
 } kv4_cache_config;
 
 /*
@@ -127,6 +129,12 @@ typedef struct {
  *                K: byte 16*(t%8) + 2*b + t/8      (tokens t, t+8 of a block paired)
  *                V: byte 32*(t%4) + 4*b + {0,2,1,3}[t/4]  (tokens t, t+8, t+4, t+12)
  *   [1152, 1216) FP32 vector scales, float of token t at byte 8*(t%8) + 4*(t/8)
+ * KV4_FORMAT_MXFP4 pages: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES_MXFP4 = 2176 bytes,
+ * block (p, h) at (p * H_kv + h) * 2176: a K half at 0 and a V half at 1088, each with
+ *   [0, 1024)    E2M1 codes, bytes as in KV4_FORMAT_NVFP4
+ *   [1024, 1088) E8M0 scales (biased exponents s + 127) of block b = dims 32b .. 32b+31
+ *                of token t: K: byte 8*(t%8) + 2*b + t/8; V: byte 16*(t%4) + 4*b +
+ *                {0,2,1,3}[t/4]
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128
@@ -134,6 +142,7 @@ typedef struct {
 #define KV4_PAGE_BLOCK_BYTES 2176
 #define KV4_PAGE_BLOCK_BYTES_INT8 4352
 #define KV4_PAGE_BLOCK_BYTES_NVFP4 2432
+#define KV4_PAGE_BLOCK_BYTES_MXFP4 2176
 
 typedef struct {
     void   *page_pool_dev;   size_t page_pool_bytes;
