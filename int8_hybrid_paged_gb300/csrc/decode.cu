@@ -1178,6 +1178,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 return;
             }
         }
+        // side-buffer runs: the next two side blocks (consecutive in the slot's block), two
+        // free stages
+        if (!KV8 && r_kind == 1 && prod + 2 <= cons + kStages && r_i + 2 <= r_end) {
+            const int p1 = (pst + 1 == kStages) ? 0 : pst + 1;
+            const uint8_t* src = r_src + (int64_t)r_i * kPageBlock;
+            issue_bulk(stage0 + (uint32_t)(kPageBlock * pst), src, kPageBlock, bar0 + 8u * pst, is_l0);
+            issue_bulk(stage0 + (uint32_t)(kPageBlock * p1), src + kPageBlock, kPageBlock, bar0 + 8u * p1, is_l0);
+            r_i += 2;
+            prod += 2;
+            pst = (p1 + 1 == kStages) ? 0 : p1 + 1;
+            return;
+        }
         // whole-cache formats: the next two items of the run (page halves), their pages'
         // entries inside the block-table window, two free stages
         if (KV8 && r_kind == 3 && prod + 2 <= cons + kStages && r_i + 2 <= r_end) {
