@@ -59,10 +59,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
-    ap.add_argument("--format", choices=["int4-hybrid", "int8", "nvfp4"], default="int4-hybrid",
+    ap.add_argument("--format", choices=["int4-hybrid", "int8", "nvfp4", "mxfp4"], default="int4-hybrid",
                     help="cache format of the main measurement: the method (INT4 pages + INT8 "
                          "side buffer), the whole-cache 8-bit format (KV8, s = w = 0) or the "
-                         "whole-cache NVFP4 format (s = w = 0)")
+                         "whole-cache NVFP4 / MXFP4 formats (s = w = 0)")
     ap.add_argument("--no-qkv", action="store_true",
                     help="skip the fused projection + append measurement")
     ap.add_argument("--no-variants", action="store_true",
@@ -197,8 +197,8 @@ def workload_from_args(args):
     import dataclasses
     wl = inputs.workload(args.workload)
     fmt = getattr(args, "format", "int4-hybrid")
-    if fmt in ("int8", "nvfp4"):
-        what = "8-bit" if fmt == "int8" else "NVFP4"
+    if fmt in ("int8", "nvfp4", "mxfp4"):
+        what = {"int8": "8-bit", "nvfp4": "NVFP4", "mxfp4": "MXFP4"}[fmt]
         return dataclasses.replace(wl, sink=0, window=0,
                                    name=wl.name + f" (whole-cache {what} format)")
     if args.sink is not None or args.window is not None:
@@ -253,7 +253,7 @@ def build_workload(wl, seed, device, sample_seqs=0, fmt=0):
                 slots=slots, lens=lens, num_pages=num_pages)
 
 
-def oracle_sample(wl, st, cpu_seconds, threads, kv8=False, nvfp4=False):
+def oracle_sample(wl, st, cpu_seconds, threads, kv8=False, nvfp4=False, mxfp4=False):
     """Time the CPU oracle's decode over a bounded sample of the workload (its first
     sequences, the same inputs as the GPU run): with OpenMP over (sequence, q head) on
     the host cores, and with one thread. Returns the cpu_baseline dict."""
@@ -264,7 +264,7 @@ def oracle_sample(wl, st, cpu_seconds, threads, kv8=False, nvfp4=False):
     H, G = wl.num_kv_heads, wl.group
     maxL = max(lens[b] for b in pick)
     oc = oracle.OracleCache(H, wl.sink, wl.window, maxL, num_slots=len(pick), kv8=kv8,
-                            nvfp4=nvfp4)
+                            nvfp4=nvfp4, mxfp4=mxfp4)
     for i, b in enumerate(pick):
         oc.append(i, 0, st["host_kv"][b][0], st["host_kv"][b][1])
     qb = inputs.bf16_bits(st["q"][pick])
@@ -298,6 +298,9 @@ def call_bytes_for(wl, fmt):
         return bytes_model.decode_call_bytes_kv8(lens, Hq, H, with_lse=True)
     if fmt == "nvfp4":
         return bytes_model.decode_call_bytes_nvfp4(lens, Hq, H, with_lse=True)
+    if fmt == "mxfp4":
+        return bytes_model.decode_call_bytes_nvfp4(lens, Hq, H, with_lse=True,
+                                                   per_position=bytes_model.MXFP4_POSITION_HEAD_BYTES)
     return bytes_model.decode_call_bytes(lens, Hq, H, wl.sink, wl.window, with_lse=True)
 
 
@@ -328,12 +331,12 @@ def run_kv4(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = workload_from_args(args)
-    kv8, fp4 = args.format == "int8", args.format == "nvfp4"
+    kv8, fp4, mx = args.format == "int8", args.format == "nvfp4", args.format == "mxfp4"
     seed = wl.seed + rank
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
     st = build_workload(wl, seed, dev, sample_seqs=ORACLE_SAMPLE_SEQS if want_cpu else 0,
                         fmt=(kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_NVFP4 if fp4
-                             else kv4.FORMAT_INT4_HYBRID))
+                             else kv4.FORMAT_MXFP4 if mx else kv4.FORMAT_INT4_HYBRID))
     cache = st["cache"]
     B, Hq, H = wl.batch, wl.num_q_heads, wl.num_kv_heads
     lens = st["lens"]
@@ -390,7 +393,7 @@ def run_kv4(args, rank, world, local):
     split_ms = prof["split_ms"] / max(1, prof["calls"])
     peak, peak_src = measured_peaks()
     achieved = split_bytes / (split_ms * 1e-3) / 1e9
-    traffic = None if (kv8 or fp4) else split_kernel_traffic()
+    traffic = None if (kv8 or fp4 or mx) else split_kernel_traffic()
     step_gbs = call_bytes * layers / (ms / args.steps * 1e-3) / 1e9
 
     res = {
@@ -420,7 +423,7 @@ def run_kv4(args, rank, world, local):
         res["append_stress"] = run_append_stress(dev, peak)
 
     # ---- the attention input projection with the append fused into its epilogue
-    hybrid = not (kv8 or fp4)
+    hybrid = not (kv8 or fp4 or mx)
     if world == 1 and not args.no_qkv and hybrid:
         res["qkv_append"] = run_qkv_append(dev)
 
@@ -435,6 +438,7 @@ def run_kv4(args, rank, world, local):
     if world == 1 and not args.no_variants and hybrid:
         res["kv8"] = run_whole_cache(wl, seed, dev, peak, value, min(args.steps, 500), "int8")
         res["nvfp4"] = run_whole_cache(wl, seed, dev, peak, value, min(args.steps, 500), "nvfp4")
+        res["mxfp4"] = run_whole_cache(wl, seed, dev, peak, value, min(args.steps, 500), "mxfp4")
 
     # ---- end to end through the public API from pinned host buffers
     if not args.no_e2e:
@@ -442,7 +446,7 @@ def run_kv4(args, rank, world, local):
 
     # ---- CPU oracle baseline (rank 0, one GPU)
     if want_cpu:
-        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores(), kv8, fp4)
+        res["cpu_baseline"] = oracle_sample(wl, st, args.cpu_seconds, host_cores(), kv8, fp4, mx)
     cache.close()
     if rank == 0:
         print(json.dumps(res), flush=True)
@@ -593,9 +597,10 @@ def run_whole_cache(wl, seed, dev, peak, kv4_value, steps, fmt_name):
     import dataclasses
     from int8_hybrid_paged_gb300 import kv4
 
-    kv8 = fmt_name == "int8"
+    kv8, mx = fmt_name == "int8", fmt_name == "mxfp4"
     wlw = dataclasses.replace(wl, sink=0, window=0)
-    st = build_workload(wlw, seed, dev, fmt=kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_NVFP4)
+    st = build_workload(wlw, seed, dev, fmt=(kv4.FORMAT_INT8 if kv8 else kv4.FORMAT_MXFP4 if mx
+                                             else kv4.FORMAT_NVFP4))
     cache = st["cache"]
     B, Hq = wlw.batch, wlw.num_q_heads
     out = torch.empty((B, Hq, 128), dtype=torch.float32, device=dev)
@@ -610,12 +615,18 @@ def run_whole_cache(wl, seed, dev, peak, kv4_value, steps, fmt_name):
         if cache.device_error():
             raise RuntimeError(f"device error in the {fmt_name} decode")
         value = float(sum(st["lens"])) * wlw.layers / (ms * 1e-3)
-        bytes_fn = bytes_model.decode_call_bytes_kv8 if kv8 else bytes_model.decode_call_bytes_nvfp4
-        call_bytes = bytes_fn(st["lens"], Hq, wlw.num_kv_heads, with_lse=True)
+        if kv8:
+            call_bytes = bytes_model.decode_call_bytes_kv8(st["lens"], Hq, wlw.num_kv_heads, with_lse=True)
+        else:
+            call_bytes = bytes_model.decode_call_bytes_nvfp4(
+                st["lens"], Hq, wlw.num_kv_heads, with_lse=True,
+                per_position=(bytes_model.MXFP4_POSITION_HEAD_BYTES if mx
+                              else bytes_model.NVFP4_POSITION_HEAD_BYTES))
         split_bytes = call_bytes - B * Hq * (128 * 4 + 4) - B * Hq * (128 * 2 - 144)
         split_ms = prof["split_ms"] / max(1, prof["calls"])
         gbs = split_bytes / (split_ms * 1e-3) / 1e9
         what = ("whole-cache 8-bit format (KV8: 264 B per token-head)" if kv8 else
+                "whole-cache MXFP4 format (E2M1 + E8M0 scales per 32: 136 B per token-head)" if mx else
                 "whole-cache NVFP4 format (E2M1 + E4M3 block scales: 152 B per token-head)")
         return {"case": "the same workload, " + what,
                 "value": value, "unit": UNIT, "ms_per_step": ms, "steps": steps,
@@ -882,7 +893,8 @@ def run_reference(args, rank, world):
     kb, vb = inputs.bf16_bits(k), inputs.bf16_bits(v)
     qb = inputs.bf16_bits(inputs.queries(wl.batch, Hq, seed))[:nseq]
     oc = oracle.OracleCache(H, wl.sink, wl.window, max(lens[:nseq]), num_slots=nseq,
-                            kv8=args.format == "int8", nvfp4=args.format == "nvfp4")
+                            kv8=args.format == "int8", nvfp4=args.format == "nvfp4",
+                            mxfp4=args.format == "mxfp4")
     for i in range(nseq):
         oc.append(i, 0, kb[cu[i]:cu[i + 1]], vb[cu[i]:cu[i + 1]])
     slots = np.arange(nseq, dtype=np.int32)

@@ -68,8 +68,10 @@ typedef enum {
 typedef enum {
     KV4_FORMAT_INT4_HYBRID = 0,
     KV4_FORMAT_INT8 = 1,
-    KV4_FORMAT_NVFP4 = 2      /* NVFP4 for every position (E2M1 values, E4M3 scales per 16
+    KV4_FORMAT_NVFP4 = 2,     /* NVFP4 for every position (E2M1 values, E4M3 scales per 16
                                  dims, an FP32 scale per token-head vector), no side buffer */
+    KV4_FORMAT_MXFP4 = 3      /* MXFP4 for every position (E2M1 values, an E8M0 power-of-two
+                                 scale per 32 dims), no side buffer */
 } kv4_format;
 
 typedef struct {
@@ -86,8 +88,8 @@ typedef struct {
     int32_t max_q_heads;     /* largest H_q of one decode call (H_q = G * H_kv, G in {1, 2, 4}) */
     int32_t max_work_items;  /* reserved: must be >= 0 and is otherwise ignored (the decode
                                 workspace is sized from max_batch, max_q_heads and the SM count) */
-    int32_t format;          /* kv4_format; KV4_FORMAT_INT8 and KV4_FORMAT_NVFP4 require
-                                sink = window = 0 */
+    int32_t format;          /* kv4_format; KV4_FORMAT_INT8, KV4_FORMAT_NVFP4 and
+                                KV4_FORMAT_MXFP4 require sink = window = 0 */
 } kv4_cache_config;
 
 /*
@@ -133,6 +135,12 @@ typedef struct {
  *                K: byte 16*(t%8) + 2*b + t/8      (tokens t, t+8 of a block paired)
  *                V: byte 32*(t%4) + 4*b + {0,2,1,3}[t/4]  (tokens t, t+8, t+4, t+12)
  *   [1152, 1216) FP32 vector scales, float of token t at byte 8*(t%8) + 4*(t/8)
+ * KV4_FORMAT_MXFP4 pages: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES_MXFP4 = 2176 bytes,
+ * block (p, h) at (p * H_kv + h) * 2176: a K half at 0 and a V half at 1088, each with
+ *   [0, 1024)    E2M1 codes, bytes as in KV4_FORMAT_NVFP4
+ *   [1024, 1088) E8M0 scales (biased exponents s + 127) of block b = dims 32b .. 32b+31
+ *                of token t: K: byte 8*(t%8) + 2*b + t/8; V: byte 16*(t%4) + 4*b +
+ *                {0,2,1,3}[t/4]
  * Lengths: int32 per slot, the slot's length after its last append.
  */
 #define KV4_HEAD_DIM 128
@@ -140,6 +148,7 @@ typedef struct {
 #define KV4_PAGE_BLOCK_BYTES 2176
 #define KV4_PAGE_BLOCK_BYTES_INT8 4352
 #define KV4_PAGE_BLOCK_BYTES_NVFP4 2432
+#define KV4_PAGE_BLOCK_BYTES_MXFP4 2176
 
 typedef struct {
     void   *page_pool_dev;   size_t page_pool_bytes;
@@ -262,7 +271,8 @@ kv4_status kv4_decode_attention(kv4_cache *cache, const void *q_bf16_dev, int nu
  *   w_hat_dev  : [batch][num_q_heads][debug_stride] u8 PV weight per INT4-region position
  *   p_bits_dev : [batch][num_q_heads][debug_stride] uint16 bits of the PV weight of each
  *                protected position as the product takes it: BF16 p (hybrid protected
- *                region, KV4_FORMAT_INT8), fp16 p·g·2^-k before the block scale (NVFP4)
+ *                region, KV4_FORMAT_INT8), fp16 p·g·2^-k before the block scale (NVFP4),
+ *                fp16 p before the block powers of two (MXFP4)
  * Positions >= debug_stride are not written. For tests; slower than the plain call.
  */
 kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, int num_q_heads,
@@ -289,7 +299,7 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  * zeroed pool (what kv4_cache_create makes) or earlier appends leave them.
  *   config          : the cache geometry the pools were built with
  *   page_pool_dev, side_pool_dev, seq_len_dev : the pools (16-byte aligned) and slot lengths
- *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8 or
+ *                     (side_pool_dev may be NULL for a KV4_FORMAT_INT8, KV4_FORMAT_MXFP4 or
  *                     KV4_FORMAT_NVFP4 configuration)
  *   other arguments : as kv4_decode_attention
  * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB. The

@@ -17,6 +17,8 @@ SIDE_POSITION_HEAD_BYTES = 2 * (INT8_CODE_BYTES + META_BYTES)  # K + V: 264 B
 BF16_TOKEN_HEAD_BYTES = 2 * HEAD_DIM * 2                     # K + V: 512 B
 # NVFP4: E2M1 codes (64 B), one E4M3 scale per 16 dims (8 B) and an FP32 vector scale
 NVFP4_POSITION_HEAD_BYTES = 2 * (HEAD_DIM // 2 + HEAD_DIM // 16 + 4)   # K + V: 152 B
+# MXFP4: E2M1 codes (64 B) and one E8M0 scale per 32 dims (4 B)
+MXFP4_POSITION_HEAD_BYTES = 2 * (HEAD_DIM // 2 + HEAD_DIM // 32)        # K + V: 136 B
 
 
 def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, bytes_per_elem: float,
@@ -79,14 +81,16 @@ def decode_call_bytes_kv8(context_lens, num_q_heads: int, num_kv_heads: int,
 
 
 def decode_call_bytes_nvfp4(context_lens, num_q_heads: int, num_kv_heads: int,
-                            page_size: int = 16, with_lse: bool = False) -> int:
-    """Algorithmic HBM bytes of one decode-attention call on the NVFP4 format: codes and
-    scales of every position (152 B per position-head), bf16 queries, fp32 outputs,
-    context lengths and slot ids, and the block-table entries of the pages read."""
+                            page_size: int = 16, with_lse: bool = False,
+                            per_position: int = NVFP4_POSITION_HEAD_BYTES) -> int:
+    """Algorithmic HBM bytes of one decode-attention call on the NVFP4 format (or, with
+    per_position = MXFP4_POSITION_HEAD_BYTES, MXFP4): codes and scales of every position
+    (152 B, or 136 B, per position-head), bf16 queries, fp32 outputs, context lengths and
+    slot ids, and the block-table entries of the pages read."""
     total = 0
     for L in context_lens:
         L = int(L)
-        total += num_kv_heads * L * NVFP4_POSITION_HEAD_BYTES + 4 * ((L + page_size - 1) // page_size) + 8
+        total += num_kv_heads * L * per_position + 4 * ((L + page_size - 1) // page_size) + 8
     B = len(context_lens)
     total += B * num_q_heads * HEAD_DIM * (2 + 4)
     if with_lse:

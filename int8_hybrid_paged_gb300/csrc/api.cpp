@@ -125,10 +125,10 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
         return KV4_ERR_INVALID_ARG;
     if (cfg->head_dim != KV4_HEAD_DIM || cfg->page_size != KV4_PAGE_SIZE) return KV4_ERR_UNSUPPORTED;
     if (cfg->sink + cfg->window > kv4::kMaxProtected) return KV4_ERR_UNSUPPORTED;
-    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8 && cfg->format != KV4_FORMAT_NVFP4)
-        return KV4_ERR_INVALID_ARG;
+    if (cfg->format < KV4_FORMAT_INT4_HYBRID || cfg->format > KV4_FORMAT_MXFP4) return KV4_ERR_INVALID_ARG;
     const bool kv8 = cfg->format == KV4_FORMAT_INT8, fp4 = cfg->format == KV4_FORMAT_NVFP4;
-    if ((kv8 || fp4) && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
+    const bool mx = cfg->format == KV4_FORMAT_MXFP4;
+    if ((kv8 || fp4 || mx) && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
     // the protected weights are formed per page: a page's protected positions must sit in
     // one side-buffer group of 16 rows, which s and w multiples of 16 guarantee
     if (cfg->sink % KV4_PAGE_SIZE != 0 || cfg->window % KV4_PAGE_SIZE != 0) return KV4_ERR_UNSUPPORTED;
@@ -156,7 +156,7 @@ kv4_status kv4_cache_create(const kv4_cache_config* cfg, kv4_cache** out)
     const int S = cfg->sink + cfg->window;
     c->side_block = (size_t)((S + 15) / 16) * kv4::kSideGroupBytes;
     c->pages_bytes = (size_t)cfg->num_pages * H *
-                     (fp4 ? kv4::kPageBlock4f : kv8 ? kv4::kPageBlock8 : kv4::kPageBlock);
+                     (fp4 ? kv4::kPageBlock4f : kv8 ? kv4::kPageBlock8 : mx ? kv4::kPageBlockMx : kv4::kPageBlock);
     c->side_bytes = (size_t)cfg->max_slots * H * c->side_block;
     int grid_max = 0;
     for (int g = 1; g <= 4; g <<= 1) grid_max = std::max(grid_max, c->grid[g]);
@@ -251,6 +251,7 @@ kv4_status kv4_append(kv4_cache* c, const void* k, const void* v, const int32_t*
     a.err = c->err;
     a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
     a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
+    a.mx = c->cfg.format == KV4_FORMAT_MXFP4;
     a.rope = c->rope;
     a.rope_max_pos = c->rope_max_pos;
     return check_launch(kv4::launch_append(a, static_cast<cudaStream_t>(stream)));
@@ -315,6 +316,7 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.dbg_stride = dbg_stride;
     a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
     a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
+    a.mx = c->cfg.format == KV4_FORMAT_MXFP4;
     a.rope = c->rope;
     a.rope_max_pos = c->rope_max_pos;
     cudaEvent_t* ev = nullptr;
@@ -420,6 +422,7 @@ kv4_status kv4_qkv_append(kv4_cache* c, const void* x, const void* w, int num_q_
     a.err = c->err;
     a.kv8 = c->cfg.format != KV4_FORMAT_INT4_HYBRID;
     a.fp4 = c->cfg.format == KV4_FORMAT_NVFP4;
+    a.mx = c->cfg.format == KV4_FORMAT_MXFP4;
     a.rope = c->rope;
     a.rope_max_pos = c->rope_max_pos;
     return check_launch(

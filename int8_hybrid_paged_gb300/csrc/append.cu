@@ -107,6 +107,29 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
         if (lane == 0 && h_lo == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
         return;
     }
+    if (a.mx) {
+        // MXFP4 format: the K and V halves of the page's block, every head of the warp
+        uint8_t* blkm = a.pages + (int64_t)page * H * kPageBlockMx;
+        const uint16_t* krow = a.k + (int64_t)tok * H * kHeadDim + 4 * lane;
+        const uint16_t* vrow = a.v + (int64_t)tok * H * kHeadDim + 4 * lane;
+        RopeRow rr{};
+        if (ROPE) rr = rope_row(a.rope + (int64_t)pos * kHeadDim, lane);
+        for (int h = h_lo; h < h_hi; ++h) {
+            float kx[4], vx[4];
+            load_bf16x4(krow + h * kHeadDim, kx);
+            load_bf16x4(vrow + h * kHeadDim, vx);
+            if (ROPE) warp_rope128(kx, rr, lane);
+            warp_fwht128(kx, lane);
+            uint32_t kc[4], vc[4], ke, ve;
+            warp_quant_mxfp4(kx, kc, ke);
+            warp_quant_mxfp4(vx, vc, ve);
+            uint8_t* b = blkm + h * kPageBlockMx;
+            store_mxfp4_k(b, ts, kc, ke, lane);
+            store_mxfp4_v(b + kMxHalf, ts, vc, ve, lane);
+        }
+        if (lane == 0 && h_lo == 0 && tok == c1 - 1) a.seq_len[slot] = new_len;
+        return;
+    }
     if (a.kv8) {
         // whole-cache 8-bit format: row ts of the page's group, every head of the warp
         uint8_t* blk8 = a.pages + (int64_t)page * H * kPageBlock8;

@@ -265,6 +265,68 @@ __device__ __forceinline__ void store_nvfp4_v(uint8_t* half, int ts, const uint3
     if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 8 * (ts & 7) + 4 * (ts >> 3)) = g;
 }
 
+// ---- MXFP4 (E2M1 values, one E8M0 power-of-two scale per 32 values)
+// The warp's 128 values (4 per lane: dims 4l .. 4l+3) to MXFP4: the lane's codes and its
+// block's biased exponent e = s + 127 (lanes 8b .. 8b+7 hold block b), where
+// s = floor(log2 amax_b) - 2 held in [-127, 127]; an all-zero block takes s = -127.
+__device__ __forceinline__ void warp_quant_mxfp4(const float (&x)[4], uint32_t (&c)[4], uint32_t& e)
+{
+    float la = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+    la = fmaxf(la, __shfl_xor_sync(kFull, la, 1));
+    la = fmaxf(la, __shfl_xor_sync(kFull, la, 2));
+    la = fmaxf(la, __shfl_xor_sync(kFull, la, 4));              // the block's max |x|
+    // floor(log2 amax) is the biased exponent field minus 127 for a normal amax; a
+    // subnormal or zero amax lands below -127 and is held there
+    const int ef = (int)((__float_as_uint(la) >> 23) & 0xffu);
+    const int sx = min(127, max(-127, ef - 127 - 2));
+    e = (uint32_t)(sx + 127);
+    // 2^-s as a normal float (s <= 125 for finite inputs); the products are exact unless
+    // they fall below the normal range, where they round to nearest like any product
+    const float inv = __uint_as_float((uint32_t)(127 - sx) << 23);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = la > 0.0f ? e2m1_rn(__fmul_rn(x[i], inv)) : 0u;
+}
+// Codes of one token-head in a K or V half, in the NVFP4 byte order.
+__device__ __forceinline__ void store_e2m1_k(uint8_t* half, int ts, const uint32_t (&c)[4], int lane)
+{
+    const int b = lane >> 2;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int jj = 2 * (lane & 3) + e;
+        half[16 * (32 * (b >> 2) + 4 * (ts & 7) + (jj & 3)) + 4 * (b & 3) + (ts >> 3) + 2 * (jj >> 2)] =
+            (uint8_t)(c[2 * e] | (c[2 * e + 1] << 4));
+    }
+}
+__device__ __forceinline__ void store_e2m1_v(uint8_t* half, int ts, const uint32_t (&c)[4], int lane)
+{
+    const int m = lane >> 2;
+    uint32_t hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hi[i] = __shfl_xor_sync(kFull, c[i], 2);
+    const int q4 = ts >> 2, kb = ((q4 & 1) << 1) | (q4 >> 1);
+    if ((lane & 2) == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gq = 4 * (lane & 3) + i;
+            half[16 * (32 * (m >> 2) + 4 * gq + (ts & 3)) + 4 * (m & 3) + kb] = (uint8_t)(c[i] | (hi[i] << 4));
+        }
+    }
+}
+// One token-head in an MXFP4 page block: codes as NVFP4, E8M0 scales of tokens t, t + 8
+// side by side per block (K) or of tokens t, t + 8, t + 4, t + 12 per block (V).
+__device__ __forceinline__ void store_mxfp4_k(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t e, int lane)
+{
+    store_e2m1_k(half, ts, c, lane);
+    const int b = lane >> 3;
+    if ((lane & 7) == 0) half[kMxScaleOff + 8 * (ts & 7) + 2 * b + (ts >> 3)] = (uint8_t)e;
+}
+__device__ __forceinline__ void store_mxfp4_v(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t e, int lane)
+{
+    store_e2m1_v(half, ts, c, lane);
+    const int b = lane >> 3, q4 = ts >> 2, kb = ((q4 & 1) << 1) | (q4 >> 1);
+    if ((lane & 7) == 0) half[kMxScaleOff + 16 * (ts & 3) + 4 * b + kb] = (uint8_t)e;
+}
+
 // Where token tok of an append goes: its sequence entry i (cu_tokens[i] <= tok <
 // cu_tokens[i+1]), slot, position, the sequence's length after the append and the
 // page of the position. False, with the error reported, when an input is invalid.

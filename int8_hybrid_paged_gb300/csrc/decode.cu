@@ -1033,6 +1033,114 @@ __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, Pr
     __syncwarp();
 }
 
+// ---------------------------------------------------------------- MXFP4 page
+// One page of the MXFP4 format, lane roles and fragment orders as in an NVFP4 page. QK:
+// the two fp16 MMAs of a 32-value block chain their accumulators (the block dot stays
+// exact, below 2^24) and the fma chain runs over the four blocks with their powers of two.
+// PV: the weights are fp16(p) from group_weights, times 2^(s_b - k) per block and token
+// (one packed fp16 multiply per register), 2^k the page's largest block scale; the fold
+// factor carries 2^k.
+__device__ __forceinline__ float e8m0_f32(uint32_t e)
+{
+    return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);     // 2^(e - 127)
+}
+// 2^(e - emax) for a biased exponent e <= emax, as a float that rounds to fp16 (0 below
+// 2^-24 after rounding: 2^-25 is a tie to the even 0). A masked position's stale scale may
+// exceed emax; it gets 0, like its weight.
+__device__ __forceinline__ float pow2_rel(uint32_t e, uint32_t emax)
+{
+    const int j = (int)e - (int)emax;
+    return (j <= 0 && j >= -126) ? __uint_as_float((uint32_t)(j + 127) << 23) : 0.f;
+}
+__device__ __forceinline__ uint32_t pow2_pair_f16(uint32_t e0, uint32_t e1, uint32_t emax)
+{
+    return half2_u32(__floats2half2_rn(pow2_rel(e0, emax), pow2_rel(e1, emax)));
+}
+
+template <int G, bool DEBUG>
+__device__ __forceinline__ void mx_group(const DecodeArgs& a, SplitSmem& sm, ProtState& st,
+                                         const uint4* __restrict__ qf, float sqh, const uint8_t* pk,
+                                         const uint8_t* pv, int grp, int L, int b, int h, int warp,
+                                         int lane)
+{
+    const int gq = lane >> 2, tq = lane & 3;
+    const int hs = 2 * (tq & 1) + (tq >> 1);
+    PairSmem& ps = sm.xb[warp].pair;
+    const int pos0 = 16 * grp + gq < L ? 16 * grp + gq : -1;
+    const int pos1 = 16 * grp + gq + 8 < L ? 16 * grp + gq + 8 : -1;
+
+    // ---- V block scales of tokens tq, tq+8, tq+4, tq+12 (bytes 0..3 of word b) and the
+    // page's largest one over its valid positions
+    const uint4 vs = lds128(pv + kMxScaleOff + 16 * tq);
+    const int p0 = 16 * grp + tq;
+    const uint32_t vmask = (p0 < L ? 0xffu : 0u) | (p0 + 8 < L ? 0xff00u : 0u) |
+                           (p0 + 4 < L ? 0xff0000u : 0u) | (p0 + 12 < L ? 0xff000000u : 0u);
+    uint32_t m4 = __vmaxu4(__vmaxu4(vs.x & vmask, vs.y & vmask), __vmaxu4(vs.z & vmask, vs.w & vmask));
+    m4 = max(max(m4 & 0xffu, (m4 >> 8) & 0xffu), max((m4 >> 16) & 0xffu, m4 >> 24));
+    const uint32_t emax = __reduce_max_sync(kFull, m4);
+
+    // ---- QK: the four 32-value block dots of rows gq, gq + 8 and the fma chain
+    const uint2 ks = lds64(pk + kMxScaleOff + 8 * gq);   // (t, t+8) of blocks 0, 1 | 2, 3
+    const uint4 kc0 = lds128(pk + 16 * lane);            // 16-value blocks 0..3
+    const uint4 kc1 = lds128(pk + 512 + 16 * lane);      // 16-value blocks 4..7
+    float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {                        // 32-value block i = 16-value blocks 2i, 2i+1
+        const uint4 qv = qf[32 * i];
+        const uint4 kc = i < 2 ? kc0 : kc1;
+        const uint32_t w0 = (i & 1) ? kc.z : kc.x, w1 = (i & 1) ? kc.w : kc.y;
+        uint32_t A0[4], A1[4];
+        e2m1x4_f16x2(w0, A0);
+        e2m1x4_f16x2(w1, A1);
+        float d[4];
+        mma_f16(d, A0[0], A0[1], A0[2], A0[3], qv.x, qv.y, 0.f, 0.f, 0.f, 0.f);
+        mma_f16(d, A1[0], A1[1], A1[2], A1[3], qv.z, qv.w, d[0], d[1], d[2], d[3]);
+        const uint32_t sw = (i < 2) ? ks.x : ks.y;
+        const uint32_t e0 = (sw >> (16 * (i & 1))) & 0xffu, e1 = (sw >> (16 * (i & 1) + 8)) & 0xffu;
+        acc = __ffma2_rn(make_float2(e8m0_f32(e0), e8m0_f32(e1)), make_float2(d[0], d[2]), acc);
+    }
+    const float2 sg = __fmul2_rn(__fmul2_rn(acc, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
+    const float2 sig = make_float2(pos0 >= 0 ? sg.x : -INFINITY, pos1 >= 0 ? sg.y : -INFINITY);
+    if (DEBUG && a.dbg_qk && hs < G) {
+        // no single integer dot here: the record holds the score's FP32 bits
+        const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
+        if (pos0 >= 0 && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = __float_as_int(sg.x);
+        if (pos1 >= 0 && pos1 < a.dbg_stride) a.dbg_qk[row + pos1] = __float_as_int(sg.y);
+    }
+
+    uint32_t wbits;
+    const float2 bAB = group_weights<true>(st, ps, sig, lane, make_float2(1.f, 1.f), 1.f, e8m0_f32(emax), wbits);
+    if (DEBUG && a.dbg_p && hs < G) record_weights(a, b, h * G + hs, pos0, pos1, wbits, wbits);
+    const float bA = bAB.x, bB = bAB.y;
+
+    // ---- fp16 PV, FP32 accumulation into the running output
+    const uint2 pw = lds64(&ps.wfrag[0][gq][2 * tq]);    // fp16(p) of tokens (tq, tq+8), (tq+4, tq+12)
+    const uint4 vc0 = lds128(pv + 16 * lane);
+    const uint4 vc1 = lds128(pv + 512 + 16 * lane);
+#pragma unroll
+    for (int bb = 0; bb < 4; ++bb) {
+        const uint32_t sw = bb == 0 ? vs.x : bb == 1 ? vs.y : bb == 2 ? vs.z : vs.w;
+        const uint32_t b0 = hmul2_u32(pw.x, pow2_pair_f16(sw & 0xffu, (sw >> 8) & 0xffu, emax));
+        const uint32_t b1 = hmul2_u32(pw.y, pow2_pair_f16((sw >> 16) & 0xffu, sw >> 24, emax));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int mm = 2 * bb + e;
+            const uint4 vc = mm < 4 ? vc0 : vc1;
+            const uint32_t wd = (mm & 3) == 0 ? vc.x : (mm & 3) == 1 ? vc.y : (mm & 3) == 2 ? vc.z : vc.w;
+            uint32_t hv[4];
+            e2m1x4_f16x2(wd, hv);
+            float c[4];
+            mma_f16(c, prmt(hv[0], hv[1], 0x5410u), prmt(hv[0], hv[1], 0x7632u), prmt(hv[2], hv[3], 0x5410u),
+                    prmt(hv[2], hv[3], 0x7632u), b0, b1, 0.f, 0.f, 0.f, 0.f);
+            st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
+            st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
+            st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
+            st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+        }
+    }
+    __syncwarp();
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -1056,9 +1164,12 @@ __device__ __forceinline__ void walk_store(volatile Walk& d, const Walk& w)
     d.csb = w.csb; d.slot = w.slot; d.k = w.k; d.a1 = w.a1; d.g0 = w.g0; d.g1 = w.g1; d.done = w.done;
 }
 
-template <int G, bool DEBUG, bool KV8, bool FP4>
+// FMT: 0 the method's format (INT4 pages + side groups), 1 the 8-bit format, 2 NVFP4,
+// 3 MXFP4; the last three walk every page as one group.
+template <int G, bool DEBUG, int FMT>
 __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(DecodeArgs a)
 {
+    constexpr bool KV8 = FMT != 0, FP4 = FMT == 2, MX = FMT == 3;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1077,8 +1188,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     const int cp = prot_items(S);
     const int span = a.plan->span;
     // whole-cache formats: a page block and each of its two stage items (K half, V half)
-    constexpr int kBlock8 = FP4 ? kPageBlock4f : kPageBlock8;
-    constexpr int kItem8 = FP4 ? kFp4Half : kPageBlock;
+    constexpr int kBlock8 = FP4 ? kPageBlock4f : MX ? kPageBlockMx : kPageBlock8;
+    constexpr int kItem8 = FP4 ? kFp4Half : MX ? kMxHalf : kPageBlock;
     const int wg = blockIdx.x * kWarps + warp;
     volatile Walk& Psm = sm.walk[warp][0];
     volatile Walk& Csm = sm.walk[warp][1];
@@ -1279,8 +1390,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 sm.wq[warp].corr[lane][1] = f.w;
             }
             __syncwarp();
-            if (FP4) {
-                // NVFP4 QK B fragments: even column g' is head [0, 2, 1, 3][g' / 2], odd
+            if (FP4 || MX) {
+                // NVFP4 / MXFP4 QK B fragments: even column g' is head [0, 2, 1, 3][g' / 2], odd
                 // columns are zero; block bb takes k rows 2t', 2t'+1, 2t'+8, 2t'+9 as dims
                 // 16bb + 2t' + {0, 1, 8, 9}. Slot ii holds blocks 2ii, 2ii + 1.
                 const int bh = 2 * ((gq >> 1) & 1) + (gq >> 2);
@@ -1439,6 +1550,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                     if (FP4)
                         fp4_group<G, DEBUG>(a, sm, st, qf, sqh, sm.stage[warp][s0], sm.stage[warp][s1],
                                             grp, Lp, b, h, warp, lane);
+                    else if (MX)
+                        mx_group<G, DEBUG>(a, sm, st, qf, sqh, sm.stage[warp][s0], sm.stage[warp][s1],
+                                           grp, Lp, b, h, warp, lane);
                     else
                         prot_group<G, DEBUG, KV8>(a, sm, st, qf, cq0, cq1, sqh, qsh, sm.stage[warp][s0],
                                                   sm.stage[warp][s1], grp, Lp, b, h, warp, lane);
@@ -1612,7 +1726,7 @@ static cudaError_t launch_k(void (*k)(DecodeArgs), int grid, int block, size_t s
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-template <int G, bool DEBUG, bool KV8, bool FP4>
+template <int G, bool DEBUG, int FMT>
 static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     // with profiling events between the kernels each one runs alone, so the events
@@ -1623,7 +1737,7 @@ static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, 
     cudaError_t e = launch_k(kv4_decode_prep_kernel, prep_blocks, kPrepThreads, 0, stream, a, false);
     if (ev) cudaEventRecord(ev[1], stream);
     if (e == cudaSuccess)
-        e = launch_k(kv4_decode_split_kernel<G, DEBUG, KV8, FP4>, grid, kDecodeThreads, sizeof(SplitSmem),
+        e = launch_k(kv4_decode_split_kernel<G, DEBUG, FMT>, grid, kDecodeThreads, sizeof(SplitSmem),
                      stream, a, dep);
     if (ev) cudaEventRecord(ev[2], stream);
     const int warps = a.batch * a.num_q_heads;
@@ -1636,16 +1750,19 @@ static cudaError_t launch_g(const DecodeArgs& a, int grid, cudaStream_t stream, 
 cudaError_t launch_decode(const DecodeArgs& a, int grid, cudaStream_t stream, cudaEvent_t* ev)
 {
     const bool dbg = a.dbg_q8 || a.dbg_qscale || a.dbg_qk || a.dbg_w || a.dbg_p;
-    const int sel = (dbg ? 1 : 0) + (a.fp4 ? 4 : a.kv8 ? 2 : 0);
+    const int fmt = a.mx ? 3 : a.fp4 ? 2 : a.kv8 ? 1 : 0;
+    const int sel = 2 * fmt + (dbg ? 1 : 0);
     auto go = [&](auto g) -> cudaError_t {
         constexpr int Gc = decltype(g)::value;
         switch (sel) {
-        case 0: return launch_g<Gc, false, false, false>(a, grid, stream, ev);
-        case 1: return launch_g<Gc, true, false, false>(a, grid, stream, ev);
-        case 2: return launch_g<Gc, false, true, false>(a, grid, stream, ev);
-        case 3: return launch_g<Gc, true, true, false>(a, grid, stream, ev);
-        case 4: return launch_g<Gc, false, true, true>(a, grid, stream, ev);
-        default: return launch_g<Gc, true, true, true>(a, grid, stream, ev);
+        case 0: return launch_g<Gc, false, 0>(a, grid, stream, ev);
+        case 1: return launch_g<Gc, true, 0>(a, grid, stream, ev);
+        case 2: return launch_g<Gc, false, 1>(a, grid, stream, ev);
+        case 3: return launch_g<Gc, true, 1>(a, grid, stream, ev);
+        case 4: return launch_g<Gc, false, 2>(a, grid, stream, ev);
+        case 5: return launch_g<Gc, true, 2>(a, grid, stream, ev);
+        case 6: return launch_g<Gc, false, 3>(a, grid, stream, ev);
+        default: return launch_g<Gc, true, 3>(a, grid, stream, ev);
         }
     };
     switch (a.group) {
@@ -1663,12 +1780,13 @@ static cudaError_t split_setup(int* ctas)
 {
     const int smem = (int)sizeof(SplitSmem);
     cudaError_t e = cudaSuccess;
-    for (auto k : {kv4_decode_split_kernel<G, false, false, false>, kv4_decode_split_kernel<G, true, false, false>,
-                   kv4_decode_split_kernel<G, false, true, false>, kv4_decode_split_kernel<G, true, true, false>,
-                   kv4_decode_split_kernel<G, false, true, true>, kv4_decode_split_kernel<G, true, true, true>})
+    for (auto k : {kv4_decode_split_kernel<G, false, 0>, kv4_decode_split_kernel<G, true, 0>,
+                   kv4_decode_split_kernel<G, false, 1>, kv4_decode_split_kernel<G, true, 1>,
+                   kv4_decode_split_kernel<G, false, 2>, kv4_decode_split_kernel<G, true, 2>,
+                   kv4_decode_split_kernel<G, false, 3>, kv4_decode_split_kernel<G, true, 3>})
         if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false, false, false>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kv4_decode_split_kernel<G, false, 0>,
                                                          kDecodeThreads, smem);
 }
 
@@ -1784,7 +1902,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
         cfg->max_slots < 1)
         return KV4_ERR_INVALID_ARG;
     if (cfg->sink + cfg->window > kMaxProtected || cfg->num_pages > INT32_MAX) return KV4_ERR_UNSUPPORTED;
-    if (cfg->format != KV4_FORMAT_INT4_HYBRID && cfg->format != KV4_FORMAT_INT8 && cfg->format != KV4_FORMAT_NVFP4)
+    if (cfg->format < KV4_FORMAT_INT4_HYBRID || cfg->format > KV4_FORMAT_MXFP4)
         return KV4_ERR_INVALID_ARG;
     const bool kv8 = cfg->format != KV4_FORMAT_INT4_HYBRID;
     if (kv8 && (cfg->sink != 0 || cfg->window != 0)) return KV4_ERR_INVALID_ARG;
@@ -1846,6 +1964,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.lse = lse_dev;
     a.kv8 = kv8;
     a.fp4 = cfg->format == KV4_FORMAT_NVFP4;
+    a.mx = cfg->format == KV4_FORMAT_MXFP4;
     const cudaError_t e = launch_decode(a, d->grid[G], static_cast<cudaStream_t>(stream), nullptr);
     return e == cudaSuccess ? KV4_OK : KV4_ERR_CUDA;
 }

@@ -36,6 +36,11 @@ constexpr int kFp4Half = 1216;
 constexpr int kPageBlock4f = 2 * kFp4Half;
 constexpr int kFp4ScaleOff = 1024;
 constexpr int kFp4GlobalOff = 1152;
+// A page block of the MXFP4 format: a K half and a V half of kMxHalf bytes each (codes
+// in the NVFP4 order, then the E8M0 scales of the four 32-value blocks of 16 tokens).
+constexpr int kMxHalf = 1088;
+constexpr int kPageBlockMx = 2 * kMxHalf;
+constexpr int kMxScaleOff = 1024;
 constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per SM
 constexpr int kStages = 5;               // page stages per warp
 // Cost-line positions charged to every (sequence, KV head) unit beyond its stage
@@ -83,6 +88,7 @@ struct AppendArgs {
     int32_t* err;
     int32_t kv8;                  // KV4_FORMAT_INT8 or NVFP4: the whole cache in pages, no side buffer
     int32_t fp4;                  // KV4_FORMAT_NVFP4: pages of kPageBlock4f bytes
+    int32_t mx;                   // KV4_FORMAT_MXFP4: pages of kPageBlockMx bytes
     const float* rope;            // [rope_max_pos][128] cos | sin, or null (keys are post-RoPE)
     int32_t rope_max_pos;
 };
@@ -126,6 +132,7 @@ struct DecodeArgs {
     int32_t dbg_stride;
     int32_t kv8;                  // KV4_FORMAT_INT8 or NVFP4: every position a row of a page group
     int32_t fp4;                  // KV4_FORMAT_NVFP4
+    int32_t mx;                   // KV4_FORMAT_MXFP4
     const float* rope;            // [rope_max_pos][128] cos | sin, or null (queries are post-RoPE)
     int32_t rope_max_pos;
 };

@@ -270,7 +270,8 @@ struct QkvArgs {
 // 32 (w % 4) ..), each a quarter of the 256 columns; all 16 share the append loop.
 constexpr int kQkvThreads = 512;
 
-// FMT: 0 the method's format (INT4 pages + side buffer), 1 the 8-bit format, 2 NVFP4
+// FMT: 0 the method's format (INT4 pages + side buffer), 1 the 8-bit format, 2 NVFP4,
+// 3 MXFP4
 template <int FMT>
 __global__ void __launch_bounds__(kQkvThreads, 1)
 kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
@@ -319,6 +320,17 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
             vxA[0] = bf16_lo(vw2.x); vxA[1] = bf16_hi(vw2.x); vxA[2] = bf16_lo(vw2.y); vxA[3] = bf16_hi(vw2.y);
         }
         if (a.rope) warp_rope128(kxA, rope_row(a.rope + (int64_t)L.pos * kHeadDim, lane), lane);
+        if (FMT == 3) {
+            warp_fwht128(kxA, lane);
+            uint32_t kc[4], vc[4], ke, ve;
+            warp_quant_mxfp4(kxA, kc, ke);
+            warp_quant_mxfp4(vxA, vc, ve);
+            uint8_t* b = a.pages + ((int64_t)L.page * H + h) * kPageBlockMx;
+            store_mxfp4_k(b, ts, kc, ke, lane);
+            store_mxfp4_v(b + kMxHalf, ts, vc, ve, lane);
+            if (lane == 0 && h == 0 && tok == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+            continue;
+        }
         if (FMT == 2) {
             warp_fwht128(kxA, lane);
             uint32_t kc[4], vc[4], ksb, vsb;
@@ -422,6 +434,20 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
             xA[0] = bf16_lo(w2.x); xA[1] = bf16_hi(w2.x); xA[2] = bf16_lo(w2.y); xA[3] = bf16_hi(w2.y);
         }
         if (!is_v && a.rope) warp_rope128(xA, rope_row(a.rope + (int64_t)L.pos * kHeadDim, lane), lane);
+        if (FMT == 3) {
+            uint8_t* b = a.pages + ((int64_t)L.page * H + h) * kPageBlockMx;
+            uint32_t c4[4], e4;
+            if (!is_v) {
+                warp_fwht128(xA, lane);
+                warp_quant_mxfp4(xA, c4, e4);
+                store_mxfp4_k(b, ts, c4, e4, lane);
+                if (lane == 0 && h == 0 && tok == L.c1 - 1) a.seq_len[L.slot] = L.new_len;
+            } else {
+                warp_quant_mxfp4(xA, c4, e4);
+                store_mxfp4_v(b + kMxHalf, ts, c4, e4, lane);
+            }
+            continue;
+        }
         if (FMT == 2) {
             uint8_t* b = a.pages + ((int64_t)L.page * H + h) * kPageBlock4f;
             uint32_t c4[4], sb4;
@@ -553,10 +579,11 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [smem_w, smem_n]() {
         const int sw = (int)smem_w, sn = (int)smem_n;
-        for (auto k : {kv4_qkv_append_kernel<0>, kv4_qkv_append_kernel<1>, kv4_qkv_append_kernel<2>})
+        for (auto k : {kv4_qkv_append_kernel<0>, kv4_qkv_append_kernel<1>, kv4_qkv_append_kernel<2>,
+                       kv4_qkv_append_kernel<3>})
             if (attr == cudaSuccess) attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sw);
         for (auto k : {kv4_qkv_append_narrow_kernel<0>, kv4_qkv_append_narrow_kernel<1>,
-                       kv4_qkv_append_narrow_kernel<2>})
+                       kv4_qkv_append_narrow_kernel<2>, kv4_qkv_append_narrow_kernel<3>})
             if (attr == cudaSuccess) attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sn);
     });
     if (attr != cudaSuccess) return attr;
@@ -566,13 +593,15 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     const int mt = (T + kBM - 1) / kBM;
     if ((int64_t)mt * (N / 256) >= sms) {
         const dim3 grid((unsigned)(N / 256), (unsigned)mt);
-        if (ap.fp4) kv4_qkv_append_kernel<2><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+        if (ap.mx) kv4_qkv_append_kernel<3><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
+        else if (ap.fp4) kv4_qkv_append_kernel<2><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
         else if (ap.kv8) kv4_qkv_append_kernel<1><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
         else kv4_qkv_append_kernel<0><<<grid, kQkvThreads, smem_w, stream>>>(mx, mw, qa, d_model);
     } else {
         // few tokens: 128-wide tiles double the CTAs
         const dim3 grid((unsigned)(N / 128), (unsigned)mt);
-        if (ap.fp4) kv4_qkv_append_narrow_kernel<2><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+        if (ap.mx) kv4_qkv_append_narrow_kernel<3><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
+        else if (ap.fp4) kv4_qkv_append_narrow_kernel<2><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
         else if (ap.kv8) kv4_qkv_append_narrow_kernel<1><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
         else kv4_qkv_append_narrow_kernel<0><<<grid, kQkvThreads, smem_n, stream>>>(mx, mw, qa, d_model);
     }

@@ -48,6 +48,7 @@ class kv4_cache_config(C.Structure):
 FORMAT_INT4_HYBRID = 0     # INT4 pages + bounded INT8 side buffer (the method)
 FORMAT_INT8 = 1            # whole-cache 8-bit codes in pages, no side buffer (KV8)
 FORMAT_NVFP4 = 2           # whole-cache NVFP4 (E2M1, E4M3 block scales, FP32 vector scales)
+FORMAT_MXFP4 = 3           # whole-cache MXFP4 (E2M1, E8M0 scale per 32 values)
 
 
 class kv4_cache_info(C.Structure):

@@ -7,7 +7,8 @@ import torch
 
 import oracle
 from int8_hybrid_paged_gb300 import inputs
-from int8_hybrid_paged_gb300.kv4 import FORMAT_INT4_HYBRID, FORMAT_INT8, FORMAT_NVFP4, KV4Cache
+from int8_hybrid_paged_gb300.kv4 import (FORMAT_INT4_HYBRID, FORMAT_INT8, FORMAT_MXFP4, FORMAT_NVFP4,
+                                          KV4Cache)
 
 D = 128
 P = 16
@@ -110,6 +111,30 @@ def unpack_nvfp4_pages(pages, H, page_ids, slots_in_page, h):
     return kc, kbs, kg, vc, vbs, vg
 
 
+def unpack_mxfp4_pages(pages, H, page_ids, slots_in_page, h):
+    """E2M1 codes [n][128] and E8M0 scale bytes [n][4] of K and of V at positions
+    (page_ids[i], slots_in_page[i]) of head h in a KV4_FORMAT_MXFP4 pool (2176-byte blocks,
+    halves of 1088 bytes), following the layout declared in include/kv4.h."""
+    base = (np.asarray(page_ids, np.int64) * H + h) * 2176
+    t = np.asarray(slots_in_page, np.int64)[:, None]
+    d = np.arange(128)[None, :]
+    j = d // 2
+    b, jj = j // 8, j % 8
+    koff = 16 * (32 * (b // 4) + 4 * (t % 8) + jj % 4) + 4 * (b % 4) + t // 8 + 2 * (jj // 4)
+    kbyte = pages[base[:, None] + koff]
+    kc = np.where(d % 2 == 0, kbyte & 15, kbyte >> 4).astype(np.uint8)
+    m, r = d // 16, d % 16
+    g = r % 8
+    kb = np.array([0, 2, 1, 3])[t // 4]
+    voff = 16 * (32 * (m // 4) + 4 * g + t % 4) + 4 * (m % 4) + kb
+    vbyte = pages[base[:, None] + 1088 + voff]
+    vc = np.where(r < 8, vbyte & 15, vbyte >> 4).astype(np.uint8)
+    bb = np.arange(4)[None, :]
+    ke = pages[base[:, None] + 1024 + 8 * (t % 8) + 2 * bb + t // 8]
+    ve = pages[base[:, None] + 1088 + 1024 + 16 * (t % 4) + 4 * bb + kb]
+    return kc, ke, vc, ve
+
+
 def unpack_side(side, side_block, H, S, slot, h):
     """INT8 side rows 0..S-1 of (slot, head h): 16-row groups of a K block and a V block
     in tensor-core fragment order, as declared in include/kv4.h."""
@@ -157,8 +182,9 @@ class Setup:
     """A GPU cache and (for the sampled sequences) oracle caches over the same inputs."""
 
     def __init__(self, H, G, s, w, lens, seed=0, spare_pages=7, kv_device="cpu",
-                 chunks=None, max_work_items=0, kv8=False, rope=None, nvfp4=False):
+                 chunks=None, max_work_items=0, kv8=False, rope=None, nvfp4=False, mxfp4=False):
         self.H, self.G, self.s, self.w, self.kv8, self.nvfp4 = H, G, s, w, kv8, nvfp4
+        self.mxfp4 = mxfp4
         self.rope = rope                     # float32 numpy table [max_pos][128] or None
         self.lens = [int(L) for L in lens]
         self.B = len(lens)
@@ -168,7 +194,8 @@ class Setup:
         self.bt = inputs.block_tables(self.lens, P, self.num_pages, seed)
         self.cache = KV4Cache(H, self.num_pages, max_slots=self.B + 1, max_batch=self.B,
                               max_q_heads=H * G, sink=s, window=w, max_work_items=max_work_items,
-                              fmt=FORMAT_NVFP4 if nvfp4 else (FORMAT_INT8 if kv8 else FORMAT_INT4_HYBRID))
+                              fmt=(FORMAT_MXFP4 if mxfp4 else FORMAT_NVFP4 if nvfp4 else
+                                   (FORMAT_INT8 if kv8 else FORMAT_INT4_HYBRID)))
         self.kv = []
         for b, L in enumerate(self.lens):
             k, v = inputs.sequence_kv(b, L, H, seed, device=kv_device)
@@ -204,7 +231,7 @@ class Setup:
 
     def oracle_for(self, b):
         oc = oracle.OracleCache(self.H, self.s, self.w, self.lens[b], num_slots=1, kv8=self.kv8,
-                                rope=self.rope, nvfp4=self.nvfp4)
+                                rope=self.rope, nvfp4=self.nvfp4, mxfp4=self.mxfp4)
         k, v = self.kv[b]
         oc.append(0, 0, inputs.bf16_bits(k), inputs.bf16_bits(v))
         return oc
@@ -269,7 +296,7 @@ def check_decode(st, q, bs, lens=None):
     log-normalizers of both calls within 2e-3 abs / 1e-2 rel. Returns the worst output
     difference."""
     lens = st.lens if lens is None else lens
-    whole = st.kv8 or st.nvfp4
+    whole = st.kv8 or st.nvfp4 or st.mxfp4
     out, lse, dbg = st.decode(q, debug_stride=max(max(lens), 1), lens=lens)
     pout, plse, _ = st.decode(q, lens=lens)
     outs = [(out.cpu().numpy(), lse.cpu().numpy()), (pout.cpu().numpy(), plse.cpu().numpy())]
@@ -281,7 +308,7 @@ def check_decode(st, q, bs, lens=None):
         np.testing.assert_array_equal(dbg["q8"][b], d["q8"])
         np.testing.assert_array_equal(dbg["q_scale"][b].view(np.uint32), d["q_scale"].view(np.uint32))
         if L:
-            if st.nvfp4:
+            if st.nvfp4 or st.mxfp4:     # no single integer dot: the record holds the score's bits
                 np.testing.assert_array_equal(dbg["qk"][b][:, :L], d["sigma"][:, :L].view(np.int32))
             else:
                 np.testing.assert_array_equal(dbg["qk"][b][:, :L], d["qk"][:, :L])

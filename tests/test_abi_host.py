@@ -57,9 +57,10 @@ def _cfg(**kw):
     (dict(num_kv_heads=0), -1),
     (dict(num_pages=0), -1),
     (dict(sink=-1), -1),
-    (dict(format=3), -1),                # unknown cache format
+    (dict(format=4), -1),                # unknown cache format
     (dict(format=-1), -1),               # unknown cache format
     (dict(format=2), -1),                # NVFP4 has no protected region
+    (dict(format=3), -1),                # MXFP4 has no protected region
     (dict(format=1), -1),                # the 8-bit format has no protected region
     (dict(format=1, sink=0, window=4), -1),
 ])

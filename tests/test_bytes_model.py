@@ -59,3 +59,13 @@ def test_nvfp4_decode_bytes():
     assert 16 * bm.NVFP4_POSITION_HEAD_BYTES == 2432
     got = bm.decode_call_bytes_nvfp4([1000], 32, 8)
     assert got == 8 * 1000 * 152 + 4 * 63 + 8 + 32 * 128 * 6
+
+
+def test_mxfp4_decode_bytes():
+    """MXFP4 holds 4.25 bits per element (4-bit codes and an 8-bit scale per 32 values), the
+    storage of the method's INT4 codes with their fp16 (delta, min) per 128: 136 B per
+    position-head, and a 2176-byte page block of 16 positions."""
+    assert bm.MXFP4_POSITION_HEAD_BYTES == bm.INT4_TOKEN_HEAD_BYTES == 136
+    assert 16 * bm.MXFP4_POSITION_HEAD_BYTES == 2176
+    got = bm.decode_call_bytes_nvfp4([1000], 32, 8, per_position=bm.MXFP4_POSITION_HEAD_BYTES)
+    assert got == 8 * 1000 * 136 + 4 * 63 + 8 + 32 * 128 * 6

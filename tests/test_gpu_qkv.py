@@ -1,7 +1,7 @@
 """The fused projection + append (kv4_qkv_append) against the same two steps done
 apart: kv4_linear_bf16 (pinned against a float32 matmul) followed by kv4_append
 (pinned against the oracle). Pages, side buffers, slot lengths and the projected
-queries must agree byte for byte, for all three cache formats, with and without RoPE,
+queries must agree byte for byte, for all four cache formats, with and without RoPE,
 over chunked appends that start at unaligned positions."""
 import numpy as np
 import pytest
@@ -80,7 +80,8 @@ def _case(H, Hq, d_model, lens, cuts, fmt, s, w, rope, seed):
 
 
 LENS = [300, 1000, 129, 5, 17]
-FORMATS = [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0), (kv4.FORMAT_NVFP4, 0, 0)]
+FORMATS = [(kv4.FORMAT_INT4_HYBRID, 16, 128), (kv4.FORMAT_INT8, 0, 0), (kv4.FORMAT_NVFP4, 0, 0),
+           (kv4.FORMAT_MXFP4, 0, 0)]
 
 
 @pytest.mark.parametrize("fmt,s,w", FORMATS)

@@ -40,6 +40,8 @@ def _lib():
 
 
 def _fmt(st):
+    if st.mxfp4:
+        return kv4.FORMAT_MXFP4
     return kv4.FORMAT_NVFP4 if st.nvfp4 else (kv4.FORMAT_INT8 if st.kv8 else kv4.FORMAT_INT4_HYBRID)
 
 
@@ -117,9 +119,10 @@ def test_noalloc_other_group_sizes(H, G):
         st.close()
 
 
-@pytest.mark.parametrize("fmt", ["kv8", "nvfp4"])
+@pytest.mark.parametrize("fmt", ["kv8", "nvfp4", "mxfp4"])
 def test_noalloc_whole_cache_formats_without_a_side_pool(fmt):
-    st = Setup(8, 4, 0, 0, LENS, seed=24, kv_device="cuda", kv8=fmt == "kv8", nvfp4=fmt == "nvfp4")
+    st = Setup(8, 4, 0, 0, LENS, seed=24, kv_device="cuda", kv8=fmt == "kv8", nvfp4=fmt == "nvfp4",
+               mxfp4=fmt == "mxfp4")
     try:
         _two_calls(st, LENS, side=False)
     finally:
