@@ -303,11 +303,12 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  *                     KV4_FORMAT_NVFP4 configuration)
  *   other arguments : as kv4_decode_attention
  * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB. The
- * workspace is six sections, each rounded up to a multiple of 256 bytes: a 16-byte
+ * workspace is seven sections, each rounded up to a multiple of 256 bytes: a 16-byte
  * plan header; 4 * (batch + 1) bytes of cost starts; 4 * (batch * H_kv + 1) bytes of
- * unit offsets; 144 bytes per q head (batch * H_q); and 8 * G and 512 * G bytes for
- * each of 2 * batch * H_kv + W partials, W being the persistent warps of the decode
- * grid (16 per resident CTA, one CTA per SM on a GB300). On a 152-SM GB300 with
+ * unit offsets; 4 * W bytes of warp starts; 144 bytes per q head (batch * H_q); and
+ * 8 * G and 512 * G bytes for each of 2 * batch * H_kv + W partials, W being the
+ * persistent warps of the decode grid (16 per resident CTA, one CTA per SM on a
+ * GB300). On a 152-SM GB300 with
  * H_q = 32, H_kv = 8 that admits batch <= 308. The limit depends on the SM count and
  * the occupancy; KV4_ERR_OUT_OF_RANGE, returned before anything is enqueued, is the
  * authoritative check. The first call on each device looks up the device addresses of

@@ -89,25 +89,35 @@ __device__ __forceinline__ int prot_items(int S) { return S > 0 ? 2 * ((S + 15) 
 
 // Cost-line length of a (b, h) unit: its n INT4 pages, its cp protected items and the
 // positions that stand for its setup and flush.
-__device__ __forceinline__ int unit_cost(int n, int cp) { return n + cp + kUnitOverhead; }
+__device__ __forceinline__ int unit_cost(int n, int cp) { return kPageCost * n + kProtCost * cp + kUnitOverhead; }
 
 // Protected groups of a unit: ceil(S/16) groups of two stage items (a side K block and
 // a side V block), or one empty item when there is no side buffer.
 __device__ __forceinline__ int group_items(int cp) { return cp > 1 ? 2 : 1; }
 __device__ __forceinline__ int prot_groups(int cp) { return cp > 1 ? cp >> 1 : 1; }
 // Cost-line extent from the first to the last group's first item (inclusive).
-__device__ __forceinline__ int prot_span_len(int cp) { return group_items(cp) * (prot_groups(cp) - 1) + 1; }
+__device__ __forceinline__ int prot_span_len(int cp)
+{
+    return kProtCost * group_items(cp) * (prot_groups(cp) - 1) + 1;
+}
 // Groups of a unit whose first item lies before cost position pstart + x.
 __device__ __forceinline__ int groups_before(int x, int cp)
 {
-    const int gi = group_items(cp);
-    return x <= 0 ? 0 : min(prot_groups(cp), (x + gi - 1) / gi);
+    const int gc = kProtCost * group_items(cp);
+    return x <= 0 ? 0 : min(prot_groups(cp), (x + gc - 1) / gc);
 }
+// INT4 pages of a unit (of n) whose cost position lies before base + x.
+__device__ __forceinline__ int pages_before(int x, int n)
+{
+    return x <= 0 ? 0 : min(n, (x + kPageCost - 1) / kPageCost);
+}
+// Cost-line extent from the first to the last INT4 page (inclusive), 0 for none.
+__device__ __forceinline__ int int4_span_len(int n) { return n > 0 ? kPageCost * (n - 1) + 1 : 0; }
 
-// Number of warp-span pieces of the INT4 pages [base, base + n) of the cost line.
+// Number of warp-span pieces of the INT4 pages of a unit starting at base.
 __device__ __forceinline__ int n_pieces(int base, int n, int span)
 {
-    return n > 0 ? (base + n - 1) / span - base / span + 1 : 0;
+    return n > 0 ? (base + kPageCost * (n - 1)) / span - base / span + 1 : 0;
 }
 
 // Division of non-negative 32-bit values by one divisor d >= 2 with a multiply-high:
@@ -195,7 +205,9 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
         }
         int total = 0;
         int off = block_scan(cost, s_scan, total);
-        const int span = max(2, (total + a.num_warps - 1) / a.num_warps);
+        // a span holds at least one item position of any unit it lies inside (pages are
+        // kPageCost apart, protected groups 2 kProtCost), so every piece index is written
+        const int span = max(2 * kProtCost, (total + a.num_warps - 1) / a.num_warps);
         const SpanDiv sd((uint32_t)span);
         int segs = 0;
         for (int b = b0; b < b1; ++b) {
@@ -204,9 +216,13 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
             const int n = n_of(L), cp = cp_of(L), plen = prot_span_len(cp);
             for (int h = 0; h < H; ++h) {
                 const int base = off + h * unit_cost(n, cp);
-                segs += sd.pieces(base, n) + sd.pieces(base + n, plen);
+                segs += sd.pieces(base, int4_span_len(n)) + sd.pieces(base + kPageCost * n, plen);
             }
-            off += H * unit_cost(n, cp);
+            // the warps whose span starts inside this sequence's units
+            const int end = off + H * unit_cost(n, cp);
+            for (int wgi = (off + span - 1) / span; wgi < min(a.num_warps, (end + span - 1) / span); ++wgi)
+                a.warp_b[wgi] = b;
+            off = end;
         }
         int nseg = 0;
         int soff = block_scan(segs, s_scan, nseg);
@@ -217,7 +233,7 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
             for (int h = 0; h < H; ++h) {
                 a.unit_seg[b * H + h] = soff;
                 const int base = cs + h * unit_cost(n, cp);
-                soff += sd.pieces(base, n) + sd.pieces(base + n, plen);
+                soff += sd.pieces(base, int4_span_len(n)) + sd.pieces(base + kPageCost * n, plen);
             }
         }
         if (tid == kPrepThreads - 1) {
@@ -345,9 +361,9 @@ __device__ __forceinline__ bool walk_enter(Walk& W)
 {
     const int cp = W.cp;
     const int base = W.csb + W.h * W.cbh;
-    const int a0 = max(W.lo, base) - base;
-    W.a1 = min(W.hi, base + W.n) - base;
-    const int pstart = base + W.n;
+    const int a0 = pages_before(W.lo - base, W.n);
+    W.a1 = pages_before(W.hi - base, W.n);
+    const int pstart = base + kPageCost * W.n;
     W.g0 = groups_before(W.lo - pstart, cp);
     W.g1 = groups_before(W.hi - pstart, cp);
     if (a0 < W.a1) { W.k = a0; return true; }
@@ -370,18 +386,13 @@ __device__ __forceinline__ void walk_next_bh(Walk& W, const DecodeArgs& a, int c
 }
 
 template <bool KV8>
-__device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, int hi, int cp)
+__device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, int hi, int cp, int wg)
 {
     W.lo = lo;
     W.hi = hi;
     W.done = lo >= hi;
     if (W.done) return;
-    int l = 0, r = a.batch;                          // largest b with cost_start[b] <= lo
-    while (r - l > 1) {
-        const int m = (l + r) >> 1;
-        if (__ldg(&a.cost_start[m]) <= lo) l = m; else r = m;
-    }
-    walk_load_b<KV8>(W, a, l, cp);
+    walk_load_b<KV8>(W, a, __ldg(&a.warp_b[wg]), cp);      // the plan's sequence of lo
     W.h = min(a.num_heads - 1, (lo - W.csb) / W.cbh);
     if (!walk_enter(W)) walk_next_bh<KV8>(W, a, cp);
 }
@@ -1197,7 +1208,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
         const int total = a.plan->total_cost;
         const int lo = min(total, wg * span), hi = min(total, lo + span);
         Walk W;
-        walk_init<KV8>(W, a, lo, hi, cp);
+        walk_init<KV8>(W, a, lo, hi, cp, wg);
         if (lane == 0) {
             walk_store(Psm, W);
             walk_store(Csm, W);
@@ -1576,7 +1587,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 const Walk C = walk_load(Csm);
                 const int base = C.csb + h * C.cbh;
                 pidx = unit_first_partial(a, b, h) +
-                       n_pieces(base, C.n, span) + (wg - (base + C.n) / span);
+                       n_pieces(base, C.n, span) + (wg - (base + kPageCost * C.n) / span);
             }
             float* po = a.part_o + ((int64_t)pidx * G) * kHeadDim;
             if (tq < 2) {
@@ -1803,13 +1814,15 @@ cudaError_t decode_ctas_per_sm(int group, int* ctas)
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int group, int grid,
                               DecodeWorkspace* ws, unsigned char* base)
 {
-    // plan header | cost_start[B+1] | unit_seg[B*H+1] | query records | partial (M, l) | partial o
+    // plan header | cost_start[B+1] | unit_seg[B*H+1] | warp_b[warps] | query records |
+    // partial (M, l) | partial o
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t items = (size_t)2 * batch * num_kv_heads + (size_t)grid * kWarps;
     size_t off = 0;
     const size_t o_plan = off;  off = up(off + sizeof(PlanHeader));
     const size_t o_cost = off;  off = up(off + sizeof(int32_t) * (batch + 1));
     const size_t o_seg = off;   off = up(off + sizeof(int32_t) * ((size_t)batch * num_kv_heads + 1));
+    const size_t o_wb = off;    off = up(off + sizeof(int32_t) * (size_t)grid * kWarps);
     const size_t o_q = off;     off = up(off + (size_t)kQInfoBytes * batch * num_q_heads);
     const size_t o_ml = off;    off = up(off + sizeof(float2) * items * group);
     const size_t o_o = off;     off = up(off + sizeof(float) * items * group * kHeadDim);
@@ -1817,6 +1830,7 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
         ws->plan = reinterpret_cast<PlanHeader*>(base + o_plan);
         ws->cost_start = reinterpret_cast<int32_t*>(base + o_cost);
         ws->unit_seg = reinterpret_cast<int32_t*>(base + o_seg);
+        ws->warp_b = reinterpret_cast<int32_t*>(base + o_wb);
         ws->qinfo = base + o_q;
         ws->part_ml = reinterpret_cast<float2*>(base + o_ml);
         ws->part_o = reinterpret_cast<float*>(base + o_o);
@@ -1956,6 +1970,7 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.plan = ws.plan;
     a.cost_start = ws.cost_start;
     a.unit_seg = ws.unit_seg;
+    a.warp_b = ws.warp_b;
     a.qinfo = ws.qinfo;
     a.part_o = ws.part_o;
     a.part_ml = ws.part_ml;

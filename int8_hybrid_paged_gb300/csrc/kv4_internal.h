@@ -43,9 +43,14 @@ constexpr int kPageBlockMx = 2 * kMxHalf;
 constexpr int kMxScaleOff = 1024;
 constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per SM
 constexpr int kStages = 5;               // page stages per warp
-// Cost-line positions charged to every (sequence, KV head) unit beyond its stage
-// items: the run setup and flush it costs its warps (no items sit there).
-constexpr int kUnitOverhead = 8;
+// The decode plan's cost line, in quarter-page units (fitted to measured per-warp times
+// on the 4B- and 8B-shaped and long-tail layers): an INT4 page costs 4, a protected stage
+// item (half a side group, or half a page of a whole-cache format) 5, and every
+// (sequence, KV head) unit is charged kUnitOverhead more for the setup and flush of its
+// runs (no items sit there).
+constexpr int kPageCost = 4;
+constexpr int kProtCost = 5;
+constexpr int kUnitOverhead = 36;
 
 // Device-resident decode plan, written by the prep kernel, read by split and merge.
 struct PlanHeader {
@@ -62,6 +67,7 @@ struct DecodeWorkspace {
     PlanHeader* plan;
     int32_t* cost_start;   // [B+1]
     int32_t* unit_seg;     // [B*H+1] first partial of each (b, h) unit, then the total
+    int32_t* warp_b;       // [warps] sequence holding the start of each warp's span
     uint8_t* qinfo;        // [B*Hq][144]
     float2* part_ml;       // [items][G] {max (log2), normalizer}
     float* part_o;         // [items][G][128]
@@ -116,6 +122,7 @@ struct DecodeArgs {
     PlanHeader* plan;
     int32_t* cost_start;
     int32_t* unit_seg;
+    int32_t* warp_b;
     uint8_t* qinfo;
     float* part_o;
     float2* part_ml;
