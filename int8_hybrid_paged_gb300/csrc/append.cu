@@ -21,7 +21,7 @@ namespace kv4 {
 // page lookup happen once per warp, then the warp quantizes its heads one by one (for
 // a token pair t, t + 8 both tokens' loads and arithmetic are in flight together).
 template <bool ROPE>
-__global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
+__global__ void __launch_bounds__(256, 3) kv4_append_kernel(AppendArgs a, int hpw)
 {
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -194,9 +194,8 @@ __global__ void __launch_bounds__(256) kv4_append_kernel(AppendArgs a, int hpw)
                 warp_rope128(kxA, rA, lane);
                 warp_rope128(kxB, rB, lane);
             }
-            const uint32_t knA = append_head(a, kxA, vxA, blk, tsA, sb, sinkA, ringA, posA, lane);
-            const uint32_t knB = append_head(a, kxB, vxB, blk, tsA + 8, sb, sinkB, ringB, posB, lane);
-            *reinterpret_cast<uint32_t*>(blk + kw) = knA | (knB << 4);
+            *reinterpret_cast<uint32_t*>(blk + kw) =
+                append_head_pair(a, kxA, vxA, kxB, vxB, blk, tsA, sb, sinkA, ringA, sinkB, ringB, posA, lane);
         }
     } else {
         for (int h = hb; h < he; ++h) {

@@ -126,6 +126,91 @@ __device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)
     return kn;
 }
 
+// Tokens A = t and B = t + 8 (t < 8) of one page and KV head together, the bytes of
+// append_head for each: K of both rotated with packed fp32x2 arithmetic; the four
+// 4-bit quantizers (K and V of A and B) reduce their min/max, and lanes 0..3 compute the
+// parameters of groups KA, KB, VA, VB (one pass for all four; lane g also stores group
+// g's metadata) before the codes come out pairwise. Writes the V
+// codes, the metadata and the side rows; returns the lane's K word with A in the low and
+// B in the high nibbles. kA and kB leave rotated.
+__device__ __forceinline__ uint32_t append_head_pair(const AppendArgs& a, float (&kA)[4], float (&vA)[4],
+                                                     float (&kB)[4], float (&vB)[4], uint8_t* blk, int tsA,
+                                                     uint8_t* sb, bool sinkA, bool ringA, bool sinkB,
+                                                     bool ringB, int posA, int lane)
+{
+    float2 k2[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) k2[i] = make_float2(kA[i], kB[i]);
+    warp_fwht128x2(k2, lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        kA[i] = k2[i].x;
+        kB[i] = k2[i].y;
+    }
+    // group extremes, each reduced over the warp
+    auto lmin = [](const float (&x)[4]) { return fminf(fminf(x[0], x[1]), fminf(x[2], x[3])); };
+    auto lmax = [](const float (&x)[4]) { return fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])); };
+    const float loKA = key2f(__reduce_min_sync(kFull, f2key(lmin(kA))));
+    const float hiKA = key2f(__reduce_max_sync(kFull, f2key(lmax(kA))));
+    const float loKB = key2f(__reduce_min_sync(kFull, f2key(lmin(kB))));
+    const float hiKB = key2f(__reduce_max_sync(kFull, f2key(lmax(kB))));
+    const float loVA = key2f(__reduce_min_sync(kFull, f2key(lmin(vA))));
+    const float hiVA = key2f(__reduce_max_sync(kFull, f2key(lmax(vA))));
+    const float loVB = key2f(__reduce_min_sync(kFull, f2key(lmin(vB))));
+    const float hiVB = key2f(__reduce_max_sync(kFull, f2key(lmax(vB))));
+    // lane g (mod 4) takes group g = KA, KB, VA, VB
+    const int g = lane & 3;
+    const float lo = g == 0 ? loKA : g == 1 ? loKB : g == 2 ? loVA : loVB;
+    const float hi = g == 0 ? hiKA : g == 1 ? hiKB : g == 2 ? hiVA : hiVB;
+    __half min_h, delta_h;
+    float m, inv;
+    quant_params<15>(lo, hi, min_h, delta_h, m, inv);
+    // metadata [K ts | K ts+8 | V ts | V ts+8] of row tsA: group g at 4 g
+    if (lane < 4)
+        *reinterpret_cast<__half2*>(blk + kMetaOff + 16 * tsA + 4 * g) = __halves2half2(delta_h, min_h);
+    const float2 mK = make_float2(__shfl_sync(kFull, m, 0), __shfl_sync(kFull, m, 1));
+    const float2 iK = make_float2(__shfl_sync(kFull, inv, 0), __shfl_sync(kFull, inv, 1));
+    const float2 mV = make_float2(__shfl_sync(kFull, m, 2), __shfl_sync(kFull, m, 3));
+    const float2 iV = make_float2(__shfl_sync(kFull, inv, 2), __shfl_sync(kFull, inv, 3));
+    uint32_t kb[4], vab[4], vbb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint2 ck = code_pair(k2[i], mK, iK);
+        const uint2 cv = code_pair(make_float2(vA[i], vB[i]), mV, iV);
+        kb[i] = ck.x | (ck.y << 4);                                                      // A | B << 4
+        vab[i] = cv.x;
+        vbb[i] = cv.y;
+    }
+    // V dim pairs 2l and 2l+1 of each token, at their places in the tile-interleaved layout
+    blk[kVCodeOff + v_byte_offset(2 * lane, tsA)] = (uint8_t)(vab[0] | (vab[1] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane + 1, tsA)] = (uint8_t)(vab[2] | (vab[3] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane, tsA + 8)] = (uint8_t)(vbb[0] | (vbb[1] << 4));
+    blk[kVCodeOff + v_byte_offset(2 * lane + 1, tsA + 8)] = (uint8_t)(vbb[2] | (vbb[3] << 4));
+
+    // INT8 side copies of protected positions (sink rows, the ring rows of the last w)
+    if (sinkA || ringA || sinkB || ringB) {
+        const int s = a.sink, w = a.window;
+#pragma unroll
+        for (int tk = 0; tk < 2; ++tk) {
+            const bool to_sink = tk ? sinkB : sinkA, to_ring = tk ? ringB : ringA;
+            if (!(to_sink || to_ring)) continue;
+            const int pos = posA + 8 * tk;
+            uint32_t k8[4], v8[4];
+            __half k8d, k8m, v8d, v8m;
+            warp_quant<255>(tk ? kB : kA, k8, k8d, k8m);
+            warp_quant<255>(tk ? vB : vA, v8, v8d, v8m);
+            if (to_sink)
+                store_int8_row(sb + (pos >> 4) * kSideGroupBytes, pos & 15, k8, v8, k8d, k8m, v8d, v8m, lane);
+            if (to_ring) {
+                const int i = s + pos % w;
+                store_int8_row(sb + (i >> 4) * kSideGroupBytes, i & 15, k8, v8, k8d, k8m, v8d, v8m, lane);
+            }
+        }
+    }
+    // bytes: dims 4i, 4i+2, 4i+1, 4i+3
+    return kb[0] | (kb[2] << 8) | (kb[1] << 16) | (kb[3] << 24);
+}
+
 // The K half and the V half of append_head, for callers that hold one of the two
 // tensors: the same bytes (K codes returned as the nibble word, K metadata and K side
 // rows; V codes, V metadata and V side rows).

@@ -101,6 +101,32 @@ __device__ __forceinline__ void warp_fwht128(float (&x)[4], int lane)
     for (int i = 0; i < 4; ++i) x[i] = __fmul_rn(x[i], inv_sqrt128);
 }
 
+// The same transform of two vectors at once (x[i] = (value of one, of the other)), with
+// packed fp32x2 arithmetic: every element rounds exactly as in warp_fwht128.
+__device__ __forceinline__ void warp_fwht128x2(float2 (&x)[4], int lane)
+{
+    const float2 a0 = __fadd2_rn(x[0], x[1]);
+    const float2 a1 = __fadd2_rn(x[0], make_float2(-x[1].x, -x[1].y));
+    const float2 a2 = __fadd2_rn(x[2], x[3]);
+    const float2 a3 = __fadd2_rn(x[2], make_float2(-x[3].x, -x[3].y));
+    x[0] = __fadd2_rn(a0, a2);
+    x[2] = __fadd2_rn(a0, make_float2(-a2.x, -a2.y));
+    x[1] = __fadd2_rn(a1, a3);
+    x[3] = __fadd2_rn(a1, make_float2(-a3.x, -a3.y));
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+        const float sg = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 y = make_float2(__shfl_xor_sync(kFull, x[i].x, m), __shfl_xor_sync(kFull, x[i].y, m));
+            x[i] = __ffma2_rn(x[i], make_float2(sg, sg), y);
+        }
+    }
+    const float inv_sqrt128 = 0x1.6a09e6p-4f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = __fmul2_rn(x[i], make_float2(inv_sqrt128, inv_sqrt128));
+}
+
 // ---------------------------------------------------------------- affine quantizer
 // One group = the warp's 128 values. x^ = Δc + m with fp16 Δ, m:
 // m = fp16 rounded down from min x (a zero minimum is taken as +0),
@@ -138,30 +164,46 @@ __device__ __forceinline__ float key2f(uint32_t k)
     return __uint_as_float(k ^ (((k >> 31) - 1u) | 0x80000000u));
 }
 
+// The quantizer's parameters of one group from its min lo and max hi: fp16 m rounded
+// down, fp16 Δ rounded up, their float values and inv = fl(1/Δ) (0 when Δ = 0, which
+// makes every code 0).
+template <int LEVELS>
+__device__ __forceinline__ void quant_params(float lo, float hi, __half& min_h, __half& delta_h, float& m,
+                                             float& inv)
+{
+    lo = __fadd_rn(lo, 0.0f);
+    min_h = __float2half_rd(lo);
+    m = __half2float(min_h);
+    const float r = __fadd_ru(hi, -m);
+    delta_h = half_div_up(r, (float)LEVELS, 1.0f / (float)LEVELS);
+    const float delta = __half2float(delta_h);
+    inv = delta == 0.0f ? 0.0f : __frcp_rn(delta);
+}
+
+// The codes of a pair of values, rint(fl(fl(x − m)·inv)) with ties to even. The clamp
+// to [0, LEVELS] of the definition never acts: m ≤ min x makes x − m ≥ 0, and
+// m + LEVELS·Δ ≥ max x with fl(1/Δ) and the two roundings keeps the product below
+// LEVELS + 1/2.
+__device__ __forceinline__ uint2 code_pair(float2 x, float2 m, float2 inv)
+{
+    const float2 v = __fmul2_rn(__fadd2_rn(x, make_float2(-m.x, -m.y)), inv);
+    return make_uint2((uint32_t)__float2int_rn(v.x), (uint32_t)__float2int_rn(v.y));
+}
+
 template <int LEVELS>
 __device__ __forceinline__ void warp_quant(const float (&x)[4], uint32_t (&c)[4],
                                            __half& delta_h, __half& min_h)
 {
-    float lo = key2f(__reduce_min_sync(kFull, f2key(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])))));
+    const float lo = key2f(__reduce_min_sync(kFull, f2key(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])))));
     const float hi = key2f(__reduce_max_sync(kFull, f2key(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])))));
-    lo = __fadd_rn(lo, 0.0f);
-    min_h = __float2half_rd(lo);
-    const float m = __half2float(min_h);
-    const float r = __fadd_ru(hi, -m);
-    delta_h = half_div_up(r, (float)LEVELS, 1.0f / (float)LEVELS);
-    const float delta = __half2float(delta_h);
-    if (delta == 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[i] = 0;
-        return;
-    }
-    const float inv = __frcp_rn(delta);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        int v = __float2int_rn(__fmul_rn(__fsub_rn(x[i], m), inv));
-        v = v < 0 ? 0 : (v > LEVELS ? LEVELS : v);
-        c[i] = (uint32_t)v;
-    }
+    float m, inv;
+    quant_params<LEVELS>(lo, hi, min_h, delta_h, m, inv);
+    const uint2 c01 = code_pair(make_float2(x[0], x[1]), make_float2(m, m), make_float2(inv, inv));
+    const uint2 c23 = code_pair(make_float2(x[2], x[3]), make_float2(m, m), make_float2(inv, inv));
+    c[0] = c01.x;
+    c[1] = c01.y;
+    c[2] = c23.x;
+    c[3] = c23.y;
 }
 
 // ---------------------------------------------------------------- exp2
