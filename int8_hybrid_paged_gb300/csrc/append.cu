@@ -21,7 +21,7 @@ namespace kv4 {
 // page lookup happen once per warp, then the warp quantizes its heads one by one (for
 // a token pair t, t + 8 both tokens' loads and arithmetic are in flight together).
 template <bool ROPE>
-__global__ void __launch_bounds__(256, 3) kv4_append_kernel(AppendArgs a, int hpw)
+__global__ void __launch_bounds__(256, 4) kv4_append_kernel(AppendArgs a, int hpw)
 {
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -182,20 +182,26 @@ __global__ void __launch_bounds__(256, 3) kv4_append_kernel(AppendArgs a, int hp
         if (pair) rB = rope_row(a.rope + (int64_t)posB * kHeadDim, lane);
     }
     if (pair) {
-        for (int h = hb; h < he; ++h) {
-            uint8_t* blk = blk0 + h * kPageBlock;
-            uint8_t* sb = sb0 + h * a.side_block_bytes;
+        // per-head pointers advance by one head; the offsets inside a block are fixed
+        const PairVOffsets vo(tsA, lane);
+        const int64_t sbb = a.side_block_bytes;
+        uint8_t* blk = blk0 + hb * kPageBlock;
+        uint8_t* sb = sb0 + hb * sbb;
+        const uint16_t* kr = krow + hb * kHeadDim;
+        const uint16_t* vr = vrow + hb * kHeadDim;
+#pragma unroll 1
+        for (int h = hb; h < he; ++h, blk += kPageBlock, sb += sbb, kr += kHeadDim, vr += kHeadDim) {
             float kxA[4], vxA[4], kxB[4], vxB[4];
-            load_bf16x4(krow + h * kHeadDim, kxA);
-            load_bf16x4(vrow + h * kHeadDim, vxA);
-            load_bf16x4(krow + rowB + h * kHeadDim, kxB);
-            load_bf16x4(vrow + rowB + h * kHeadDim, vxB);
+            load_bf16x4(kr, kxA);
+            load_bf16x4(vr, vxA);
+            load_bf16x4(kr + rowB, kxB);
+            load_bf16x4(vr + rowB, vxB);
             if (ROPE) {
                 warp_rope128(kxA, rA, lane);
                 warp_rope128(kxB, rB, lane);
             }
             *reinterpret_cast<uint32_t*>(blk + kw) =
-                append_head_pair(a, kxA, vxA, kxB, vxB, blk, tsA, sb, sinkA, ringA, sinkB, ringB, posA, lane);
+                append_head_pair(a, kxA, vxA, kxB, vxB, blk, tsA, vo, sb, sinkA, ringA, sinkB, ringB, posA, lane);
         }
     } else {
         for (int h = hb; h < he; ++h) {

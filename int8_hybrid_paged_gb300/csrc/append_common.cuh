@@ -133,10 +133,20 @@ __device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)
 // g's metadata) before the codes come out pairwise. Writes the V
 // codes, the metadata and the side rows; returns the lane's K word with A in the low and
 // B in the high nibbles. kA and kB leave rotated.
+// Byte offsets of a lane's four V bytes of tokens tsA and tsA + 8 in a page block.
+struct PairVOffsets {
+    int a0, a1, b0, b1;
+    __device__ __forceinline__ PairVOffsets(int tsA, int lane)
+        : a0(kVCodeOff + v_byte_offset(2 * lane, tsA)), a1(kVCodeOff + v_byte_offset(2 * lane + 1, tsA)),
+          b0(kVCodeOff + v_byte_offset(2 * lane, tsA + 8)), b1(kVCodeOff + v_byte_offset(2 * lane + 1, tsA + 8))
+    {
+    }
+};
+
 __device__ __forceinline__ uint32_t append_head_pair(const AppendArgs& a, float (&kA)[4], float (&vA)[4],
                                                      float (&kB)[4], float (&vB)[4], uint8_t* blk, int tsA,
-                                                     uint8_t* sb, bool sinkA, bool ringA, bool sinkB,
-                                                     bool ringB, int posA, int lane)
+                                                     const PairVOffsets& vo, uint8_t* sb, bool sinkA,
+                                                     bool ringA, bool sinkB, bool ringB, int posA, int lane)
 {
     float2 k2[4];
 #pragma unroll
@@ -182,10 +192,10 @@ __device__ __forceinline__ uint32_t append_head_pair(const AppendArgs& a, float 
         vbb[i] = cv.y;
     }
     // V dim pairs 2l and 2l+1 of each token, at their places in the tile-interleaved layout
-    blk[kVCodeOff + v_byte_offset(2 * lane, tsA)] = (uint8_t)(vab[0] | (vab[1] << 4));
-    blk[kVCodeOff + v_byte_offset(2 * lane + 1, tsA)] = (uint8_t)(vab[2] | (vab[3] << 4));
-    blk[kVCodeOff + v_byte_offset(2 * lane, tsA + 8)] = (uint8_t)(vbb[0] | (vbb[1] << 4));
-    blk[kVCodeOff + v_byte_offset(2 * lane + 1, tsA + 8)] = (uint8_t)(vbb[2] | (vbb[3] << 4));
+    blk[vo.a0] = (uint8_t)(vab[0] | (vab[1] << 4));
+    blk[vo.a1] = (uint8_t)(vab[2] | (vab[3] << 4));
+    blk[vo.b0] = (uint8_t)(vbb[0] | (vbb[1] << 4));
+    blk[vo.b1] = (uint8_t)(vbb[2] | (vbb[3] << 4));
 
     // INT8 side copies of protected positions (sink rows, the ring rows of the last w)
     if (sinkA || ringA || sinkB || ringB) {

@@ -141,14 +141,12 @@ __device__ __forceinline__ void warp_fwht128x2(float2 (&x)[4], int lane)
 __device__ __forceinline__ __half half_div_up(float r, float n, float inv_n)
 {
     const __half c = __float2half_ru(__fmul_rn(r, inv_n));
-    unsigned short cb = __half_as_ushort(c);
-    if (__fmul_rn(__half2float(c), n) < r) {
-        ++cb;                                           // estimate below the quotient
-    } else if (cb != 0) {
-        const unsigned short pb = (unsigned short)(cb - 1);
-        if (__fmul_rn(__half2float(__ushort_as_half(pb)), n) >= r) cb = pb;   // one step too high
-    }
-    return __ushort_as_half(cb);
+    const unsigned short cb = __half_as_ushort(c);
+    const unsigned short pb = (unsigned short)(cb - 1);
+    const bool below = __fmul_rn(__half2float(c), n) < r;                     // estimate below the quotient
+    const bool above = cb != 0 && __fmul_rn(__half2float(__ushort_as_half(pb)), n) >= r;   // one step too high
+    // selects, not branches: lanes that hold different groups take different cases
+    return __ushort_as_half(below ? (unsigned short)(cb + 1) : (above ? pb : cb));
 }
 
 // Order-preserving map of a float to uint32 (and back), for the warp's integer
