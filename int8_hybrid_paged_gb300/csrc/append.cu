@@ -176,11 +176,8 @@ __global__ void __launch_bounds__(256, 4) kv4_append_kernel(AppendArgs a, int hp
     uint8_t* sb0 = a.side + (int64_t)slot * H * a.side_block_bytes;
     const int tsA = posA % kPage;
     const int kw = kKCodeOff + k_word_offset(tsA & 7, lane);
-    RopeRow rA{}, rB{};                     // the tokens' RoPE rows, shared by all heads
-    if (ROPE) {
-        rA = rope_row(a.rope + (int64_t)posA * kHeadDim, lane);
-        if (pair) rB = rope_row(a.rope + (int64_t)posB * kHeadDim, lane);
-    }
+    RopeRow rA{};                           // a lone token's RoPE row, shared by all heads
+    if (ROPE && !pair) rA = rope_row(a.rope + (int64_t)posA * kHeadDim, lane);
     if (pair) {
         // per-head pointers advance by one head; the offsets inside a block are fixed
         const PairVOffsets vo(tsA, lane);
@@ -196,12 +193,16 @@ __global__ void __launch_bounds__(256, 4) kv4_append_kernel(AppendArgs a, int hp
             load_bf16x4(vr, vxA);
             load_bf16x4(kr + rowB, kxB);
             load_bf16x4(vr + rowB, vxB);
-            if (ROPE) {
-                warp_rope128(kxA, rA, lane);
-                warp_rope128(kxB, rB, lane);
-            }
+            float2 k2[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) k2[i] = make_float2(kxA[i], kxB[i]);
+            // the tokens' RoPE rows are read again for every head (from L1): holding them
+            // across the loop costs more registers than the loads cost
+            if (ROPE)
+                warp_rope128x2(k2, rope_row(a.rope + (int64_t)posA * kHeadDim, lane),
+                               rope_row(a.rope + (int64_t)posB * kHeadDim, lane), lane);
             *reinterpret_cast<uint32_t*>(blk + kw) =
-                append_head_pair(a, kxA, vxA, kxB, vxB, blk, tsA, vo, sb, sinkA, ringA, sinkB, ringB, posA, lane);
+                append_head_pair(a, k2, vxA, vxB, blk, tsA, vo, sb, sinkA, ringA, sinkB, ringB, posA, lane);
         }
     } else {
         for (int h = hb; h < he; ++h) {

@@ -127,12 +127,13 @@ __device__ __forceinline__ uint32_t append_head(const AppendArgs& a, float (&kx)
 }
 
 // Tokens A = t and B = t + 8 (t < 8) of one page and KV head together, the bytes of
-// append_head for each: K of both rotated with packed fp32x2 arithmetic; the four
+// append_head for each: K of both (k2[i] = (A, B), after RoPE when a table is set)
+// rotated with packed fp32x2 arithmetic; the four
 // 4-bit quantizers (K and V of A and B) reduce their min/max, and lanes 0..3 compute the
 // parameters of groups KA, KB, VA, VB (one pass for all four; lane g also stores group
 // g's metadata) before the codes come out pairwise. Writes the V
 // codes, the metadata and the side rows; returns the lane's K word with A in the low and
-// B in the high nibbles. kA and kB leave rotated.
+// B in the high nibbles.
 // Byte offsets of a lane's four V bytes of tokens tsA and tsA + 8 in a page block.
 struct PairVOffsets {
     int a0, a1, b0, b1;
@@ -143,15 +144,13 @@ struct PairVOffsets {
     }
 };
 
-__device__ __forceinline__ uint32_t append_head_pair(const AppendArgs& a, float (&kA)[4], float (&vA)[4],
-                                                     float (&kB)[4], float (&vB)[4], uint8_t* blk, int tsA,
+__device__ __forceinline__ uint32_t append_head_pair(const AppendArgs& a, float2 (&k2)[4], const float (&vA)[4],
+                                                     const float (&vB)[4], uint8_t* blk, int tsA,
                                                      const PairVOffsets& vo, uint8_t* sb, bool sinkA,
                                                      bool ringA, bool sinkB, bool ringB, int posA, int lane)
 {
-    float2 k2[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) k2[i] = make_float2(kA[i], kB[i]);
     warp_fwht128x2(k2, lane);
+    float kA[4], kB[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         kA[i] = k2[i].x;
@@ -160,14 +159,10 @@ __device__ __forceinline__ uint32_t append_head_pair(const AppendArgs& a, float 
     // group extremes, each reduced over the warp
     auto lmin = [](const float (&x)[4]) { return fminf(fminf(x[0], x[1]), fminf(x[2], x[3])); };
     auto lmax = [](const float (&x)[4]) { return fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])); };
-    const float loKA = key2f(__reduce_min_sync(kFull, f2key(lmin(kA))));
-    const float hiKA = key2f(__reduce_max_sync(kFull, f2key(lmax(kA))));
-    const float loKB = key2f(__reduce_min_sync(kFull, f2key(lmin(kB))));
-    const float hiKB = key2f(__reduce_max_sync(kFull, f2key(lmax(kB))));
-    const float loVA = key2f(__reduce_min_sync(kFull, f2key(lmin(vA))));
-    const float hiVA = key2f(__reduce_max_sync(kFull, f2key(lmax(vA))));
-    const float loVB = key2f(__reduce_min_sync(kFull, f2key(lmin(vB))));
-    const float hiVB = key2f(__reduce_max_sync(kFull, f2key(lmax(vB))));
+    const float loKA = warp_min_f32(lmin(kA)), hiKA = warp_max_f32(lmax(kA));
+    const float loKB = warp_min_f32(lmin(kB)), hiKB = warp_max_f32(lmax(kB));
+    const float loVA = warp_min_f32(lmin(vA)), hiVA = warp_max_f32(lmax(vA));
+    const float loVB = warp_min_f32(lmin(vB)), hiVB = warp_max_f32(lmax(vB));
     // lane g (mod 4) takes group g = KA, KB, VA, VB
     const int g = lane & 3;
     const float lo = g == 0 ? loKA : g == 1 ? loKB : g == 2 ? loVA : loVB;

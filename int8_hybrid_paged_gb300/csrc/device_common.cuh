@@ -149,19 +149,6 @@ __device__ __forceinline__ __half half_div_up(float r, float n, float inv_n)
     return __ushort_as_half(below ? (unsigned short)(cb + 1) : (above ? pb : cb));
 }
 
-// Order-preserving map of a float to uint32 (and back), for the warp's integer
-// min/max reductions: the bits with the sign flipped for x >= 0, all bits flipped
-// for x < 0 (so -0 sorts just below +0; either is a zero minimum).
-__device__ __forceinline__ uint32_t f2key(float f)
-{
-    const uint32_t b = __float_as_uint(f);
-    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);
-}
-__device__ __forceinline__ float key2f(uint32_t k)
-{
-    return __uint_as_float(k ^ (((k >> 31) - 1u) | 0x80000000u));
-}
-
 // The quantizer's parameters of one group from its min lo and max hi: fp16 m rounded
 // down, fp16 Δ rounded up, their float values and inv = fl(1/Δ) (0 when Δ = 0, which
 // makes every code 0).
@@ -188,12 +175,26 @@ __device__ __forceinline__ uint2 code_pair(float2 x, float2 m, float2 inv)
     return make_uint2((uint32_t)__float2int_rn(v.x), (uint32_t)__float2int_rn(v.y));
 }
 
+// Warp-wide min and max of a float (sm_100 redux on floats; -0 orders below +0).
+__device__ __forceinline__ float warp_min_f32(float v)
+{
+    float r;
+    asm volatile("redux.sync.min.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float warp_max_f32(float v)
+{
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 template <int LEVELS>
 __device__ __forceinline__ void warp_quant(const float (&x)[4], uint32_t (&c)[4],
                                            __half& delta_h, __half& min_h)
 {
-    const float lo = key2f(__reduce_min_sync(kFull, f2key(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])))));
-    const float hi = key2f(__reduce_max_sync(kFull, f2key(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])))));
+    const float lo = warp_min_f32(fminf(fminf(x[0], x[1]), fminf(x[2], x[3])));
+    const float hi = warp_max_f32(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])));
     float m, inv;
     quant_params<LEVELS>(lo, hi, min_h, delta_h, m, inv);
     const uint2 c01 = code_pair(make_float2(x[0], x[1]), make_float2(m, m), make_float2(inv, inv));
@@ -318,6 +319,22 @@ __device__ __forceinline__ void warp_rope128(float (&x)[4], const RopeRow& r, in
         const float y = __shfl_xor_sync(0xffffffffu, x[j], 16);       // the paired dim
         x[j] = lo ? __fmaf_rn(x[j], cc[j], -__fmul_rn(y, ss[j]))
                   : __fmaf_rn(x[j], cc[j], __fmul_rn(y, ss[j]));
+    }
+}
+
+// The same rotation of two vectors at once (x[j] = (value of one, of the other)), each
+// with its own table row; every element rounds exactly as in warp_rope128.
+__device__ __forceinline__ void warp_rope128x2(float2 (&x)[4], const RopeRow& ra, const RopeRow& rb, int lane)
+{
+    const float ca[4] = {ra.c.x, ra.c.y, ra.c.z, ra.c.w}, sa[4] = {ra.s.x, ra.s.y, ra.s.z, ra.s.w};
+    const float cb[4] = {rb.c.x, rb.c.y, rb.c.z, rb.c.w}, sb[4] = {rb.s.x, rb.s.y, rb.s.z, rb.s.w};
+    const float sg = lane < 16 ? -1.0f : 1.0f;        // lower half: x cos - y sin; upper: x cos + y sin
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 y = make_float2(__shfl_xor_sync(0xffffffffu, x[j].x, 16),
+                                     __shfl_xor_sync(0xffffffffu, x[j].y, 16));
+        const float2 t = __fmul2_rn(y, make_float2(sg * sa[j], sg * sb[j]));   // exact sign flip
+        x[j] = __ffma2_rn(x[j], make_float2(ca[j], cb[j]), t);
     }
 }
 
