@@ -411,8 +411,11 @@ __device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, 
 // PV columns: n = 4 page + head. The u8 weights go to shared memory as packed half2
 // words (token g', token g' + 8) in the B-fragment order of each page's MMA; the
 // columns of the other page stay zero, so each MMA takes its operand with one load.
+// Component c of a float2 (c a compile-time constant in the unrolled loops).
+__device__ __forceinline__ float& fc(float2& v, int c) { return c ? v.y : v.x; }
+
 struct Int4State {
-    float o[8][2][2];
+    float2 o[8][2];      // [m][r] = (column 0, column 1) of rows r of tile m: packed FFMA2 operands
     float M, l, bias;    // running max, normalizer and offset-term share of the scored head
     float wacc;          // Σ over pages of (page scale) x Σ u8 weights, for the widening offset
 };
@@ -577,8 +580,7 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
         for (int m = 0; m < 8; ++m)
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                st.o[m][r][0] *= aA;
-                st.o[m][r][1] *= aB;
+                st.o[m][r] = __fmul2_rn(st.o[m][r], make_float2(aA, aB));
             }
     }
     __syncwarp();
@@ -606,10 +608,8 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
                 0.f, 0.f);
         mma_f16(c, wide_byte(vB[m]), wide_hi(vB[m]), xb, xb & 0xfff0fff0u, bw1.x, bw1.y, c[0], c[1],
                 c[2], c[3]);
-        st.o[m][0][0] = fmaf(kA, c[0], st.o[m][0][0]);
-        st.o[m][0][1] = fmaf(kB, c[1], st.o[m][0][1]);
-        st.o[m][1][0] = fmaf(kAh, c[2], st.o[m][1][0]);
-        st.o[m][1][1] = fmaf(kBh, c[3], st.o[m][1][1]);
+        st.o[m][0] = __ffma2_rn(make_float2(kA, kB), make_float2(c[0], c[1]), st.o[m][0]);
+        st.o[m][1] = __ffma2_rn(make_float2(kAh, kBh), make_float2(c[2], c[3]), st.o[m][1]);
     }
     __syncwarp();
 }
@@ -622,7 +622,7 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
 // rounded to BF16 (B; columns = heads, k order t, t+8, t+4, t+12 so a scoring lane's
 // pair of rows is one B word), FP32 accumulation, folded into the running output.
 struct ProtState {
-    float o[8][4];     // lanes t' < 2: dims 16m + g' (+8) of heads 2t', 2t' + 1
+    float2 o[8][2];    // [m][0]: dim 16m + g', [m][1]: dim 16m + g' + 8, of the lane's two columns
     float M, l;        // running max and normalizer share of head hs
 };
 
@@ -720,10 +720,8 @@ __device__ __forceinline__ float2 group_weights(ProtState& st, PairSmem& ps, flo
         const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
 #pragma unroll
         for (int mm = 0; mm < 8; ++mm) {
-            st.o[mm][0] *= aA;
-            st.o[mm][1] *= aB;
-            st.o[mm][2] *= aA;
-            st.o[mm][3] *= aB;
+            st.o[mm][0] = __fmul2_rn(st.o[mm][0], make_float2(aA, aB));
+            st.o[mm][1] = __fmul2_rn(st.o[mm][1], make_float2(aA, aB));
         }
     }
     __syncwarp();
@@ -777,10 +775,8 @@ __device__ __forceinline__ float2 group_weights_pages(ProtState& st, PairSmem& p
         const float aA = __shfl_sync(kFull, alpha, srcA), aB = __shfl_sync(kFull, alpha, srcA | 2);
 #pragma unroll
         for (int mm = 0; mm < 8; ++mm) {
-            st.o[mm][0] *= aA;
-            st.o[mm][1] *= aB;
-            st.o[mm][2] *= aA;
-            st.o[mm][3] *= aB;
+            st.o[mm][0] = __fmul2_rn(st.o[mm][0], make_float2(aA, aB));
+            st.o[mm][1] = __fmul2_rn(st.o[mm][1], make_float2(aA, aB));
         }
     }
     __syncwarp();
@@ -816,10 +812,8 @@ __device__ __forceinline__ void prot_pv(ProtState& st, const PairSmem& ps, const
         dequant_word(w1, dA, mA, dB, mB, a1, a3);
         float c[4];
         mma_bf16(c, a0, a1, a2, a3, bw.x, bw.y, 0.f, 0.f, 0.f, 0.f);
-        st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
-        st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
-        st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
-        st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+        st.o[mm][0] = __ffma2_rn(make_float2(bA, bB), make_float2(c[0], c[1]), st.o[mm][0]);
+        st.o[mm][1] = __ffma2_rn(make_float2(bA, bB), make_float2(c[2], c[3]), st.o[mm][1]);
     }
     __syncwarp();
 }
@@ -1036,10 +1030,11 @@ __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, Pr
         float c[4];
         mma_f16(c, prmt(hv[0], hv[1], 0x5410u), prmt(hv[0], hv[1], 0x7632u), prmt(hv[2], hv[3], 0x5410u),
                 prmt(hv[2], hv[3], 0x7632u), hmul2_u32(pw.x, s01), hmul2_u32(pw.y, s23), 0.f, 0.f, 0.f, 0.f);
-        st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
-        st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
-        st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
-        st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+        // scalar fmas here: the packed form measured slower in this routine
+        fc(st.o[mm][0], 0) = fmaf(bA, c[0], fc(st.o[mm][0], 0));
+        fc(st.o[mm][0], 1) = fmaf(bB, c[1], fc(st.o[mm][0], 1));
+        fc(st.o[mm][1], 0) = fmaf(bA, c[2], fc(st.o[mm][1], 0));
+        fc(st.o[mm][1], 1) = fmaf(bB, c[3], fc(st.o[mm][1], 1));
     }
     __syncwarp();
 }
@@ -1143,10 +1138,11 @@ __device__ __forceinline__ void mx_group(const DecodeArgs& a, SplitSmem& sm, Pro
             float c[4];
             mma_f16(c, prmt(hv[0], hv[1], 0x5410u), prmt(hv[0], hv[1], 0x7632u), prmt(hv[2], hv[3], 0x5410u),
                     prmt(hv[2], hv[3], 0x7632u), b0, b1, 0.f, 0.f, 0.f, 0.f);
-            st.o[mm][0] = fmaf(bA, c[0], st.o[mm][0]);
-            st.o[mm][1] = fmaf(bB, c[1], st.o[mm][1]);
-            st.o[mm][2] = fmaf(bA, c[2], st.o[mm][2]);
-            st.o[mm][3] = fmaf(bB, c[3], st.o[mm][3]);
+            // scalar fmas here: the packed form measured slower in this routine
+            fc(st.o[mm][0], 0) = fmaf(bA, c[0], fc(st.o[mm][0], 0));
+            fc(st.o[mm][0], 1) = fmaf(bB, c[1], fc(st.o[mm][0], 1));
+            fc(st.o[mm][1], 0) = fmaf(bA, c[2], fc(st.o[mm][1], 0));
+            fc(st.o[mm][1], 1) = fmaf(bB, c[3], fc(st.o[mm][1], 1));
         }
     }
     __syncwarp();
@@ -1464,7 +1460,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 #pragma unroll
             for (int m = 0; m < 8; ++m)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) st.o[m][r][0] = st.o[m][r][1] = 0.f;
+                for (int r = 0; r < 2; ++r) st.o[m][r] = make_float2(0.f, 0.f);
             st.M = -INFINITY;
             st.l = 0.f;
             st.bias = 0.f;
@@ -1509,10 +1505,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             for (int m = 0; m < 8; ++m) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
-                    const float lo = st.o[m][0][c] + __shfl_xor_sync(kFull, st.o[m][0][c], 2);
-                    const float hi = st.o[m][1][c] + __shfl_xor_sync(kFull, st.o[m][1][c], 2);
-                    st.o[m][0][c] = fmaf(-16.f, hi, lo) + (c ? biasB : biasA);
-                    st.o[m][1][c] = hi + (c ? offB1 : offA1);
+                    const float lo = fc(st.o[m][0], c) + __shfl_xor_sync(kFull, fc(st.o[m][0], c), 2);
+                    const float hi = fc(st.o[m][1], c) + __shfl_xor_sync(kFull, fc(st.o[m][1], c), 2);
+                    fc(st.o[m][0], c) = fmaf(-16.f, hi, lo) + (c ? biasB : biasA);
+                    fc(st.o[m][1], c) = hi + (c ? offB1 : offA1);
                 }
             }
             Walk C = walk_load(Csm);
@@ -1527,7 +1523,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 #pragma unroll
                     for (int m = 0; m < 8; ++m)
                         *reinterpret_cast<float2*>(po + 16 * m + 2 * gq) =
-                            make_float2(st.o[m][0][j], st.o[m][1][j]);
+                            make_float2(fc(st.o[m][0], j), fc(st.o[m][1], j));
                 }
             }
             if (gq == 0 && hs < G) a.part_ml[(int64_t)idx * G + hs] = make_float2(st.M, st.l);
@@ -1542,7 +1538,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 #pragma unroll
             for (int mm = 0; mm < 8; ++mm)
 #pragma unroll
-                for (int r = 0; r < 4; ++r) st.o[mm][r] = 0.f;
+                for (int r = 0; r < 2; ++r) st.o[mm][r] = make_float2(0.f, 0.f);
             st.M = -INFINITY;
             st.l = 0.f;
             const float cq0 = hs < G ? -wq.corr[hs][0] : 0.f;
@@ -1580,7 +1576,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 #pragma unroll
                 for (int mm = 0; mm < 8; ++mm)
 #pragma unroll
-                    for (int r = 0; r < 4; ++r) st.o[mm][r] += __shfl_xor_sync(kFull, st.o[mm][r], 2);
+                    for (int r = 0; r < 2; ++r) {
+                        st.o[mm][r].x += __shfl_xor_sync(kFull, st.o[mm][r].x, 2);
+                        st.o[mm][r].y += __shfl_xor_sync(kFull, st.o[mm][r].y, 2);
+                    }
             }
             int pidx;
             {
@@ -1597,8 +1596,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                     if (hd >= G) continue;
 #pragma unroll
                     for (int mm = 0; mm < 8; ++mm) {
-                        po[hd * kHeadDim + 16 * mm + gq] = st.o[mm][j];
-                        po[hd * kHeadDim + 16 * mm + gq + 8] = st.o[mm][2 + j];
+                        po[hd * kHeadDim + 16 * mm + gq] = fc(st.o[mm][0], j);
+                        po[hd * kHeadDim + 16 * mm + gq + 8] = fc(st.o[mm][1], j);
                     }
                 }
             }
