@@ -124,12 +124,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
 }
 
 // The tile's main loop: barrier and TMEM set-up, thread 0 streams the X and W tiles of
-// every k block, thread 32 issues the MMAs, and every thread then waits for the
-// accumulator. True when the accumulator holds the finished tile.
-template <int BN>
+// every k block, thread 32 issues the MMAs, threads 64 and up run pre(tid - 64) (work
+// that does not need the tile: no warp-collective operations), and every thread then
+// waits for the accumulator. True when the accumulator holds the finished tile.
+template <int BN, class PreWait>
 __device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& map_x,
                                           const CUtensorMap& map_w, int m0, int n0, int nk,
-                                          int32_t* err)
+                                          int32_t* err, PreWait&& pre)
 {
     constexpr int kWBytes = BN * kBK * 2;
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -193,6 +194,8 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& m
         }
         if (ok) umma_commit(smem_u32(&sm.accum));
         else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&sm.accum)) : "memory");
+    } else if (tid >= 64) {
+        pre(tid - 64);
     }
     const bool got = wait_phase(smem_u32(&sm.accum), 0);
     tmem_fence_after();
@@ -250,7 +253,7 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
-    const bool ok = gemm_tile<BN>(sm, map_x, map_w, m0, n0, K / kBK, err);
+    const bool ok = gemm_tile<BN>(sm, map_x, map_w, m0, n0, K / kBK, err, [](int) {});
     const int row = m0 + 32 * warp + lane;
     if (ok)                                  // CTA-uniform: every lane loads, rows < M store
         store_row_bf16(sm.tmem_base + ((uint32_t)(32 * warp) << 16), BN / 32, y + (int64_t)row * N + n0,
@@ -270,6 +273,23 @@ struct QkvArgs {
 // 32 (w % 4) ..), each a quarter of the 256 columns; all 16 share the append loop.
 constexpr int kQkvThreads = 512;
 
+// Where each token of a K/V tile goes, found by the idle threads while the tile's MMAs
+// run (the lookups are dependent global loads: done in the append loop they would come
+// one token after another); kept in shared memory past the GEMM's stages.
+struct TokenLocS {
+    TokenLoc L;
+    int32_t ok;
+};
+__device__ __forceinline__ void locate_tile_tokens(const AppendArgs& a, TokenLocS* loc, int m0, int t)
+{
+    for (int rr = t; rr < kBM; rr += kQkvThreads - 64) {
+        const int tok = m0 + rr;
+        TokenLocS e{};
+        e.ok = tok < a.total_tokens && locate_token(a, tok, 0, e.L);
+        loc[rr] = e;
+    }
+}
+
 // FMT: 0 the method's format (INT4 pages + side buffer), 1 the 8-bit format, 2 NVFP4,
 // 3 MXFP4
 template <int FMT>
@@ -284,7 +304,11 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * 256;
     const int T = a.total_tokens;
-    const bool ok = gemm_tile<256>(sm, map_x, map_w, m0, n0, K / kBK, a.err);
+    TokenLocS* loc = reinterpret_cast<TokenLocS*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(GemmSmem<256>));
+    const bool kv_tile = n0 >= qa.q_cols;
+    const bool ok = gemm_tile<256>(sm, map_x, map_w, m0, n0, K / kBK, a.err, [&](int t) {
+        if (kv_tile) locate_tile_tokens(a, loc, m0, t);
+    });
     const int quarter = warp & 3, colq = warp >> 2;                 // TMEM lane quarter, column quarter
     const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(64 * colq);
     const int r = 32 * quarter + lane, row = m0 + r;
@@ -309,8 +333,8 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     for (int rr = warp; rr < kBM; rr += kQkvThreads / 32) {
         const int tok = m0 + rr;
         if (tok >= T) break;
-        TokenLoc L;
-        if (!locate_token(a, tok, lane, L)) continue;
+        if (!loc[rr].ok) continue;
+        const TokenLoc L = loc[rr].L;
         const int ts = L.pos % kPage;
         float kxA[4], vxA[4];
         {
@@ -404,7 +428,11 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * 128;
     const int T = a.total_tokens;
-    const bool ok = gemm_tile<128>(sm, map_x, map_w, m0, n0, K / kBK, a.err);
+    TokenLocS* loc = reinterpret_cast<TokenLocS*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(GemmSmem<128>));
+    const bool kv_tile = n0 >= qa.q_cols;
+    const bool ok = gemm_tile<128>(sm, map_x, map_w, m0, n0, K / kBK, a.err, [&](int t) {
+        if (kv_tile) locate_tile_tokens(a, loc, m0, t);
+    });
     const int quarter = warp & 3, colq = warp >> 2;                 // TMEM lane quarter, column quarter
     const uint32_t trow = sm.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * colq);
     const int r = 32 * quarter + lane, row = m0 + r;
@@ -425,8 +453,8 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
     for (int rr = warp; rr < kBM; rr += kQkvThreads / 32) {
         const int tok = m0 + rr;
         if (tok >= T) break;
-        TokenLoc L;
-        if (!locate_token(a, tok, lane, L)) continue;
+        if (!loc[rr].ok) continue;
+        const TokenLoc L = loc[rr].L;
         const int ts = L.pos % kPage;
         float xA[4];
         {
@@ -574,7 +602,8 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
     qa.ap = ap;
     qa.q_out = static_cast<uint16_t*>(q_out);
     qa.q_cols = num_q_heads * kHeadDim;
-    const size_t smem_w = sizeof(GemmSmem<256>) + 1024, smem_n = sizeof(GemmSmem<128>) + 1024;
+    const size_t smem_w = sizeof(GemmSmem<256>) + sizeof(TokenLocS) * kBM + 1024,
+                 smem_n = sizeof(GemmSmem<128>) + sizeof(TokenLocS) * kBM + 1024;
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [smem_w, smem_n]() {
