@@ -25,16 +25,20 @@ namespace kv4 {
 namespace {
 
 constexpr int kBM = 128, kBK = 64;                 // kBK * 2 bytes = one 128-byte swizzle row
-constexpr int kGemmStages = 4;
+// TMA ring depth: 4 stages of 48 KB for 256-wide tiles, 6 of 32 KB for 128-wide ones
+// (a deeper ring keeps more bytes in flight per SM when few tiles share the GPU)
+template <int BN>
+constexpr int gemm_stages() { return BN == 256 ? 4 : 6; }
 constexpr int kTileBytes = kBM * kBK * 2;           // 16 KB: the X tile
 constexpr int kGemmThreads = 128;
 
 // BN = 128 or 256 output columns per tile (the W tile and the TMEM accumulator width)
 template <int BN>
 struct __align__(1024) GemmSmem {
-    uint8_t a[kGemmStages][kTileBytes];             // 1024-byte aligned: swizzle atoms
-    uint8_t b[kGemmStages][BN * kBK * 2];
-    uint64_t full[kGemmStages], empty[kGemmStages], accum;
+    static constexpr int kStages = gemm_stages<BN>();
+    uint8_t a[kStages][kTileBytes];                 // 1024-byte aligned: swizzle atoms
+    uint8_t b[kStages][BN * kBK * 2];
+    uint64_t full[kStages], empty[kStages], accum;
     uint32_t tmem_base;
     int32_t abort;
 };
@@ -135,7 +139,7 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& m
     constexpr int kWBytes = BN * kBK * 2;
     const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
-        for (int s = 0; s < kGemmStages; ++s) {
+        for (int s = 0; s < GemmSmem<BN>::kStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
@@ -160,7 +164,7 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& m
     if (tid == 0) {
         // ---- producer: TMA of the X and W tiles of every k block
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kGemmStages, r = kb / kGemmStages;
+            const int s = kb % GemmSmem<BN>::kStages, r = kb / GemmSmem<BN>::kStages;
             if (r > 0 && !wait_phase(smem_u32(&sm.empty[s]), (r - 1) & 1)) {
                 report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
                 atomicExch(&sm.abort, 1);
@@ -177,7 +181,7 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& m
         // ---- MMA issuer: four K = 16 steps per stage, accumulate after the first
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % kGemmStages, r = kb / kGemmStages;
+            const int s = kb % GemmSmem<BN>::kStages, r = kb / GemmSmem<BN>::kStages;
             if (!wait_phase(smem_u32(&sm.full[s]), r & 1)) {
                 report_error(err, KV4_DEVERR_WAIT_TIMEOUT);
                 atomicExch(&sm.abort, 1);
