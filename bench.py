@@ -642,11 +642,11 @@ def run_qkv_append(dev):
     """kv4_qkv_append (the QKV projection on the tcgen05 tensor cores with RoPE, the
     Hadamard rotation and the 4-bit append fused into its epilogue) against the same
     work in two steps (kv4_linear_bf16, then kv4_append), on Qwen3-8B attention shapes
-    (d_model 4096, 32 q heads, 8 KV heads): a decode step of 256 single tokens and a
-    re-prefill chunk of 8 x 2048 tokens. The two-step path also gathers the K and V
+    (d_model 4096, 32 q heads, 8 KV heads): decode steps of 256 and of 128 single tokens
+    (the second on the split-K cluster path) and a re-prefill chunk of 8 x 2048 tokens. The two-step path also gathers the K and V
     columns into [T][H][128] tensors for the append. Device time per call from one
-    replay of a CUDA graph of repeated calls; seeded random bf16 weights and hidden
-    states."""
+    replay of a CUDA graph of repeated calls, each on the next of four weight copies;
+    seeded random bf16 weights and hidden states."""
     from int8_hybrid_paged_gb300 import kv4
     from int8_hybrid_paged_gb300.kv4 import KV4Cache
     peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
@@ -657,9 +657,12 @@ def run_qkv_append(dev):
     N = (Hq + 2 * H) * 128
     g = torch.Generator(device=dev)
     g.manual_seed(7)
-    w = (torch.randn((N, d), generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+    # four copies of W_qkv (4 x 50 MB, above the 129 MB L2), one per call in turn: no
+    # call finds its weights in L2
+    ws = [(torch.randn((N, d), generator=g, device=dev) / d ** 0.5).to(torch.bfloat16) for _ in range(4)]
     out = {}
-    for tag, B, T, start_pos, reps in (("decode", 256, 1, 600, 50), ("prefill", 8, 2048, 0, 10)):
+    for tag, B, T, start_pos, reps in (("decode", 256, 1, 600, 50), ("decode_b128", 128, 1, 600, 50),
+                                       ("prefill", 8, 2048, 0, 10)):
         stride = (start_pos + T + 15) // 16 + 1
         num_pages = B * stride + 8
         bt = torch.from_numpy(inputs.block_tables([stride * 16] * B, 16, num_pages, 3)).to(dev)
@@ -675,23 +678,23 @@ def run_qkv_append(dev):
             for c in caches:
                 c.set_rope(tab)
 
-            def fused():
+            def fused(w):
                 caches[0].qkv_append(x, w, Hq, cu, slots, start, bt, q_out=q)
 
-            def apart():
+            def apart(w):
                 kv4.kv4_linear_bf16(x, w, y)
                 kvp = y[:, Hq * 128:].view(B * T, H, 2, 128)      # the append takes [T][H][128] rows
                 caches[1].append(kvp[:, :, 0].contiguous(), kvp[:, :, 1].contiguous(), cu, slots, start, bt)
 
             res = {}
             for name, fn in (("fused", fused), ("apart", apart)):
-                for _ in range(3):
-                    fn()
+                for i in range(4):
+                    fn(ws[i])
                 torch.cuda.synchronize()
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph):
-                    for _ in range(reps):
-                        fn()
+                    for i in range(reps):
+                        fn(ws[i % len(ws)])
                 graph.replay()
                 torch.cuda.synchronize()
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -713,7 +716,8 @@ def run_qkv_append(dev):
             tfl = flops / (res["fused"] * 1e-3) / 1e12
             gbs = nbytes / (res["fused"] * 1e-3) / 1e9
             out[tag] = {"case": f"{B} sequences x {T} token(s) from position {start_pos}: X [{B * T}][{d}] "
-                                f"x W_qkv [{N}][{d}], RoPE + Hadamard + 4-bit append of 8 KV heads",
+                                f"x W_qkv [{N}][{d}], RoPE + Hadamard + 4-bit append of 8 KV heads; "
+                                f"{len(ws)} copies of W_qkv cycled (weights never in L2)",
                         "fused_us": res["fused"] * 1e3, "apart_us": res["apart"] * 1e3,
                         "bound": "tensor" if flops / nbytes > peak_tf * 1e12 / (peak_hbm * 1e9) else "hbm",
                         "fused_tflops": tfl, "fused_frac_of_bf16_peak": tfl / peak_tf,

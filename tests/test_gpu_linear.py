@@ -28,6 +28,7 @@ def _inputs(M, N, K, seed):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (300, 256, 128), (129, 384, 576),
+                                   (64, 1024, 512), (100, 384, 256), (128, 128, 128),   # split-K clusters
                                    (256, 6144, 4096), (2048, 1024, 4096),
                                    (1300, 6144, 320), (4096, 6144, 4096)])   # 256-wide tiles
 def test_linear_matches_float32_matmul(M, N, K):
