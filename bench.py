@@ -57,6 +57,8 @@ def parse():
                     help="override the sink size s (with --window 0 and --sink 0: unprotected KV4)")
     ap.add_argument("--window", type=int, default=None, help="override the recent window w")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="time the CPU oracle once over the whole workload (no GPU) and exit")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-append", action="store_true", help="skip the append-stress measurement")
     ap.add_argument("--format", choices=["int4-hybrid", "int8", "nvfp4", "mxfp4"], default="int4-hybrid",
@@ -929,8 +931,63 @@ def run_reference(args, rank, world):
     print(json.dumps(res), flush=True)
 
 
+def run_oracle_full(args):
+    """The CPU oracle over a whole workload once: every sequence of the batch (of the
+    long-tail stack, its first layer: the other 35 have the same shape), its caches built
+    and decoded in groups of 16 sequences. Only the decodes are timed, with OpenMP over
+    (sequence, q head) on the host cores and with one thread. The K/V and queries come
+    from the CPU generator (the same shapes and distributions as the GPU run, not the
+    same values: the GPU run draws them on the device). Prints one JSON line."""
+    import oracle
+
+    wl = inputs.workload(args.workload)
+    kv8, fp4, mx = args.format == "int8", args.format == "nvfp4", args.format == "mxfp4"
+    lens = list(wl.context_lens)
+    H, G, Hq = wl.num_kv_heads, wl.group, wl.num_q_heads
+    sink, window = (0, 0) if (kv8 or fp4 or mx) else (wl.sink, wl.window)
+    t_build = time.perf_counter()
+    k, v = inputs.kv_tokens(sum(lens), H, wl.seed * 1_000_003 + 17)
+    q = inputs.bf16_bits(inputs.queries(wl.batch, Hq, wl.seed))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    build = time.perf_counter() - t_build
+    threads = host_cores()
+    t_omp = t_one = 0.0
+    for g0 in range(0, wl.batch, 16):
+        pick = list(range(g0, min(wl.batch, g0 + 16)))
+        t0 = time.perf_counter()
+        oc = oracle.OracleCache(H, sink, window, max(lens[b] for b in pick), num_slots=len(pick), kv8=kv8,
+                                nvfp4=fp4, mxfp4=mx)
+        for i, b in enumerate(pick):
+            oc.append(i, 0, inputs.bf16_bits(k[cu[b]:cu[b + 1]]), inputs.bf16_bits(v[cu[b]:cu[b + 1]]))
+        build += time.perf_counter() - t0
+        slots = np.arange(len(pick), dtype=np.int32)
+        sl = np.array([lens[b] for b in pick], np.int32)
+        for nthreads in (threads, 1):
+            t0 = time.perf_counter()
+            oc.decode_batch(slots, sl, G, q[pick], 1 / math.sqrt(128), threads=nthreads)
+            el = time.perf_counter() - t0
+            if nthreads == 1:
+                t_one += el
+            else:
+                t_omp += el
+        del oc
+    tokens = float(sum(lens))
+    print(json.dumps({"impl": "oracle-full", "workload": wl.name, "format": args.format,
+                      "context_tokens": int(tokens), "q_heads": Hq,
+                      "decode_seconds": t_omp, "value": tokens / t_omp, "unit": UNIT, "cores": threads,
+                      "one_thread": {"decode_seconds": t_one, "value": tokens / t_one, "cores": 1},
+                      "cache_build_seconds_untimed": build,
+                      "layers_note": ("one layer of the stack; the step is 36 such layers"
+                                      if wl.layers > 1 else "the whole batch"),
+                      "host_cpu": cpu_model(),
+                      "inputs": "CPU generator stream: same shapes and distributions as the GPU run"}))
+
+
 def main():
     args = parse()
+    if args.oracle_full:
+        run_oracle_full(args)
+        return
     rank, world, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -303,12 +303,11 @@ kv4_status kv4_decode_attention_debug(kv4_cache *cache, const void *q_bf16_dev, 
  *                     KV4_FORMAT_NVFP4 configuration)
  *   other arguments : as kv4_decode_attention
  * Limits: batch <= 4096, and the call's workspace must fit in the 16 MiB. The
- * workspace is seven sections, each rounded up to a multiple of 256 bytes: a 16-byte
+ * workspace is six sections, each rounded up to a multiple of 256 bytes: a 16-byte
  * plan header; 4 * (batch + 1) bytes of cost starts; 4 * (batch * H_kv + 1) bytes of
- * unit offsets; 4 * W bytes of warp starts; 144 bytes per q head (batch * H_q); and
- * 8 * G and 512 * G bytes for each of 2 * batch * H_kv + W partials, W being the
- * persistent warps of the decode grid (16 per resident CTA, one CTA per SM on a
- * GB300). On a 152-SM GB300 with
+ * unit offsets; 144 bytes per q head (batch * H_q); and 8 * G and 512 * G bytes for
+ * each of 2 * batch * H_kv + W partials, W being the persistent warps of the decode
+ * grid (16 per resident CTA, one CTA per SM on a GB300). On a 152-SM GB300 with
  * H_q = 32, H_kv = 8 that admits batch <= 308. The limit depends on the SM count and
  * the occupancy; KV4_ERR_OUT_OF_RANGE, returned before anything is enqueued, is the
  * authoritative check. The first call on each device looks up the device addresses of
@@ -334,7 +333,12 @@ kv4_status kv4_decode_attention_noalloc(const kv4_cache_config *config,
  * kv4_linear_bf16 — Y = X · Wᵀ on the tcgen05 tensor cores (the QKV projection ahead
  * of the cache): BF16 inputs, FP32 accumulation in tensor memory, BF16 output
  * (round to nearest). Tiles of 128 × 256 outputs (128 × 128 when 256-wide tiles would
- * leave SMs idle), TMA loads with a 128-byte swizzle.
+ * leave SMs idle), TMA loads with a 128-byte swizzle. With M <= 128 the k range of each
+ * 128 × 128 tile is split over the CTAs of a thread-block cluster (up to 8, as many as
+ * fit on the GPU at once), whose FP32 partial sums are added in a fixed order through
+ * distributed shared memory: the result does not depend on scheduling. The same call
+ * shape always takes the same split, and kv4_qkv_append takes the same one, so the two
+ * produce the same sums.
  *   x_dev   : [M][K] bf16, K contiguous, 16-byte aligned
  *   w_dev   : [N][K] bf16, K contiguous (the nn.Linear weight layout), 16-byte aligned
  *   y_dev   : [M][N] bf16, 16-byte aligned

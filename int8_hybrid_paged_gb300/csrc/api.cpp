@@ -302,7 +302,6 @@ static kv4_status decode_common(kv4_cache* c, const void* q, int num_q_heads,
     a.plan = ws.plan;
     a.cost_start = ws.cost_start;
     a.unit_seg = ws.unit_seg;
-    a.warp_b = ws.warp_b;
     a.qinfo = ws.qinfo;
     a.part_o = ws.part_o;
     a.part_ml = ws.part_ml;

@@ -142,6 +142,15 @@ struct SpanDiv {
     }
 };
 
+// Span of each warp on a cost line of length total: a span holds at least one item
+// position of any unit it lies inside (pages are kPageCost apart, protected groups
+// 2 kProtCost), so every piece index is written. The plan kernel and the split kernel
+// both compute it, from the same inputs.
+__device__ __forceinline__ int plan_span(int total, int num_warps)
+{
+    return max(2 * kProtCost, (total + num_warps - 1) / num_warps);
+}
+
 // First partial of unit (b, h), laid out by the plan: per unit its INT4 pieces, then
 // its protected pieces (spans holding the first item of one of its groups).
 __device__ __forceinline__ int unit_first_partial(const DecodeArgs& a, int b, int h)
@@ -205,9 +214,7 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
         }
         int total = 0;
         int off = block_scan(cost, s_scan, total);
-        // a span holds at least one item position of any unit it lies inside (pages are
-        // kPageCost apart, protected groups 2 kProtCost), so every piece index is written
-        const int span = max(2 * kProtCost, (total + a.num_warps - 1) / a.num_warps);
+        const int span = plan_span(total, a.num_warps);
         const SpanDiv sd((uint32_t)span);
         int segs = 0;
         for (int b = b0; b < b1; ++b) {
@@ -218,11 +225,7 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
                 const int base = off + h * unit_cost(n, cp);
                 segs += sd.pieces(base, int4_span_len(n)) + sd.pieces(base + kPageCost * n, plen);
             }
-            // the warps whose span starts inside this sequence's units
-            const int end = off + H * unit_cost(n, cp);
-            for (int wgi = (off + span - 1) / span; wgi < min(a.num_warps, (end + span - 1) / span); ++wgi)
-                a.warp_b[wgi] = b;
-            off = end;
+            off += H * unit_cost(n, cp);
         }
         int nseg = 0;
         int soff = block_scan(segs, s_scan, nseg);
@@ -344,15 +347,16 @@ __device__ __forceinline__ uint32_t lds32(const void* p) { return *reinterpret_c
 
 // KV8: no INT4 pages; every position is a protected row of its page, so the
 // protected items of a unit follow its length.
+// csb: the cost position of b's first unit (the previous sequence's plus its H units)
 template <bool KV8>
-__device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b, int cp)
+__device__ __forceinline__ void walk_load_b(Walk& W, const DecodeArgs& a, int b, int cp, int csb)
 {
     W.b = b;
     W.L = max(0, __ldg(&a.context_lens[b]));
     W.n = KV8 ? 0 : int4_pages(W.L, a.sink, a.window);
     W.cp = KV8 ? prot_items(W.L) : cp;
     W.cbh = unit_cost(W.n, W.cp);
-    W.csb = __ldg(&a.cost_start[b]);
+    W.csb = csb;
     W.slot = __ldg(&a.slot_ids[b]);
 }
 
@@ -377,7 +381,7 @@ __device__ __forceinline__ void walk_next_bh(Walk& W, const DecodeArgs& a, int c
     for (;;) {
         if (++W.h == a.num_heads) {
             if (W.b + 1 >= a.batch) { W.done = true; return; }
-            walk_load_b<KV8>(W, a, W.b + 1, cp);
+            walk_load_b<KV8>(W, a, W.b + 1, cp, W.csb + a.num_heads * W.cbh);
             W.h = 0;
         }
         if (W.csb + W.h * W.cbh >= W.hi) { W.done = true; return; }
@@ -385,14 +389,15 @@ __device__ __forceinline__ void walk_next_bh(Walk& W, const DecodeArgs& a, int c
     }
 }
 
+// b, csb: the sequence whose units hold cost position lo, and its first unit's position
 template <bool KV8>
-__device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, int hi, int cp, int wg)
+__device__ __forceinline__ void walk_init(Walk& W, const DecodeArgs& a, int lo, int hi, int cp, int b, int csb)
 {
     W.lo = lo;
     W.hi = hi;
     W.done = lo >= hi;
     if (W.done) return;
-    walk_load_b<KV8>(W, a, __ldg(&a.warp_b[wg]), cp);      // the plan's sequence of lo
+    walk_load_b<KV8>(W, a, b, cp, csb);
     W.h = min(a.num_heads - 1, (lo - W.csb) / W.cbh);
     if (!walk_enter(W)) walk_next_bh<KV8>(W, a, cp);
 }
@@ -1185,26 +1190,49 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             for (int k = 0; k < kStages; ++k) mbar_init(&sm.bar[ww][k], 1);
         fence_mbar_init();
     }
-    __syncthreads();
-    // launched as a programmatic dependent of the prep kernel: everything above ran
-    // alongside its tail; the plan and query records are read only past this wait
-    grid_dependency_wait();
-    grid_launch_dependents();
 
     const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
     const int cp = prot_items(S);
-    const int span = a.plan->span;
     // whole-cache formats: a page block and each of its two stage items (K half, V half)
     constexpr int kBlock8 = FP4 ? kPageBlock4f : MX ? kPageBlockMx : kPageBlock8;
     constexpr int kItem8 = FP4 ? kFp4Half : MX ? kMxHalf : kPageBlock;
     const int wg = blockIdx.x * kWarps + warp;
     volatile Walk& Psm = sm.walk[warp][0];
     volatile Walk& Csm = sm.walk[warp][1];
+    // ---- this CTA's share of the plan, from the call's inputs alone, so that it and the
+    // first bulk copies run before the dependency wait, alongside the plan kernel: the
+    // cost line's length (one block-wide scan over the batch, the plan kernel's
+    // arithmetic) and, for each of the CTA's warps, the sequence whose units hold the
+    // start of its span (left in the warp's consumer walker slot)
+    int span, total;
     {
-        const int total = a.plan->total_cost;
+        int* s_scan = reinterpret_cast<int*>(&sm.wq[0]);    // free until the first query load
+        const int B = a.batch;
+        const int per = (B + kDecodeThreads - 1) / kDecodeThreads;
+        const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+        auto unit_of = [&](int L) {
+            return KV8 ? unit_cost(0, prot_items(L)) : unit_cost(int4_pages(L, s, w), cp);
+        };
+        int cost = 0;
+        for (int b = b0; b < b1; ++b) cost += H * unit_of(max(0, __ldg(&a.context_lens[b])));
+        int off = block_scan(cost, s_scan, total);
+        span = plan_span(total, a.num_warps);
+        const int wg0 = blockIdx.x * kWarps;
+        for (int b = b0; b < b1; ++b) {
+            const int end = off + H * unit_of(max(0, __ldg(&a.context_lens[b])));
+            const int first = max(wg0, (off + span - 1) / span), last = min(wg0 + kWarps, (end + span - 1) / span);
+            for (int wgi = first; wgi < last; ++wgi) {
+                sm.walk[wgi - wg0][1].b = b;
+                sm.walk[wgi - wg0][1].csb = off;
+            }
+            off = end;
+        }
+        __syncthreads();
         const int lo = min(total, wg * span), hi = min(total, lo + span);
+        const int b_lo = Csm.b, csb_lo = Csm.csb;
+        __syncwarp();
         Walk W;
-        walk_init<KV8>(W, a, lo, hi, cp, wg);
+        walk_init<KV8>(W, a, lo, hi, cp, b_lo, csb_lo);
         if (lane == 0) {
             walk_store(Psm, W);
             walk_store(Csm, W);
@@ -1371,6 +1399,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
     };
 
     produce();
+    // launched as a programmatic dependent of the prep kernel: everything above ran
+    // alongside its tail; the query records and the partials' layout are read only
+    // past this wait
+    grid_dependency_wait();
+    grid_launch_dependents();
     int q_b = -1, q_h = -1;
     const int gq = lane >> 2, tq = lane & 3, half = tq >> 1;
     while (!aborted) {
@@ -1813,15 +1846,14 @@ cudaError_t decode_ctas_per_sm(int group, int* ctas)
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int group, int grid,
                               DecodeWorkspace* ws, unsigned char* base)
 {
-    // plan header | cost_start[B+1] | unit_seg[B*H+1] | warp_b[warps] | query records |
-    // partial (M, l) | partial o
+    // plan header | cost_start[B+1] | unit_seg[B*H+1] | query records | partial (M, l) |
+    // partial o
     auto up = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t items = (size_t)2 * batch * num_kv_heads + (size_t)grid * kWarps;
     size_t off = 0;
     const size_t o_plan = off;  off = up(off + sizeof(PlanHeader));
     const size_t o_cost = off;  off = up(off + sizeof(int32_t) * (batch + 1));
     const size_t o_seg = off;   off = up(off + sizeof(int32_t) * ((size_t)batch * num_kv_heads + 1));
-    const size_t o_wb = off;    off = up(off + sizeof(int32_t) * (size_t)grid * kWarps);
     const size_t o_q = off;     off = up(off + (size_t)kQInfoBytes * batch * num_q_heads);
     const size_t o_ml = off;    off = up(off + sizeof(float2) * items * group);
     const size_t o_o = off;     off = up(off + sizeof(float) * items * group * kHeadDim);
@@ -1829,7 +1861,6 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
         ws->plan = reinterpret_cast<PlanHeader*>(base + o_plan);
         ws->cost_start = reinterpret_cast<int32_t*>(base + o_cost);
         ws->unit_seg = reinterpret_cast<int32_t*>(base + o_seg);
-        ws->warp_b = reinterpret_cast<int32_t*>(base + o_wb);
         ws->qinfo = base + o_q;
         ws->part_ml = reinterpret_cast<float2*>(base + o_ml);
         ws->part_o = reinterpret_cast<float*>(base + o_o);
@@ -1969,7 +2000,6 @@ extern "C" kv4_status kv4_decode_attention_noalloc(
     a.plan = ws.plan;
     a.cost_start = ws.cost_start;
     a.unit_seg = ws.unit_seg;
-    a.warp_b = ws.warp_b;
     a.qinfo = ws.qinfo;
     a.part_o = ws.part_o;
     a.part_ml = ws.part_ml;

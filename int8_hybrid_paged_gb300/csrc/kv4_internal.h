@@ -67,7 +67,6 @@ struct DecodeWorkspace {
     PlanHeader* plan;
     int32_t* cost_start;   // [B+1]
     int32_t* unit_seg;     // [B*H+1] first partial of each (b, h) unit, then the total
-    int32_t* warp_b;       // [warps] sequence holding the start of each warp's span
     uint8_t* qinfo;        // [B*Hq][144]
     float2* part_ml;       // [items][G] {max (log2), normalizer}
     float* part_o;         // [items][G][128]
@@ -122,7 +121,6 @@ struct DecodeArgs {
     PlanHeader* plan;
     int32_t* cost_start;
     int32_t* unit_seg;
-    int32_t* warp_b;
     uint8_t* qinfo;
     float* part_o;
     float2* part_ml;
