@@ -1190,6 +1190,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             for (int k = 0; k < kStages; ++k) mbar_init(&sm.bar[ww][k], 1);
         fence_mbar_init();
     }
+    __syncthreads();
 
     const int H = a.num_heads, s = a.sink, w = a.window, S = s + w;
     const int cp = prot_items(S);
