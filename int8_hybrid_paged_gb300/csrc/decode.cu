@@ -88,8 +88,14 @@ __device__ __forceinline__ int int4_pages(int L, int s, int w)
 __device__ __forceinline__ int prot_items(int S) { return S > 0 ? 2 * ((S + 15) >> 4) : 1; }
 
 // Cost-line length of a (b, h) unit: its n INT4 pages, its cp protected items and the
-// positions that stand for its setup and flush.
-__device__ __forceinline__ int unit_cost(int n, int cp) { return kPageCost * n + kProtCost * cp + kUnitOverhead; }
+// positions that stand for the setup of its two runs and its flush.
+__device__ __forceinline__ int unit_cost(int n, int cp)
+{
+    return kRunSetup + kPageCost * n + kProtSetup + kProtCost * cp + kUnitFlush;
+}
+// Cost positions of a unit starting at base: its first INT4 page, its first protected item.
+__device__ __forceinline__ int int4_start(int base) { return base + kRunSetup; }
+__device__ __forceinline__ int prot_start(int base, int n) { return base + kRunSetup + kPageCost * n + kProtSetup; }
 
 // Protected groups of a unit: ceil(S/16) groups of two stage items (a side K block and
 // a side V block), or one empty item when there is no side buffer.
@@ -106,7 +112,7 @@ __device__ __forceinline__ int groups_before(int x, int cp)
     const int gc = kProtCost * group_items(cp);
     return x <= 0 ? 0 : min(prot_groups(cp), (x + gc - 1) / gc);
 }
-// INT4 pages of a unit (of n) whose cost position lies before base + x.
+// INT4 pages of a unit (of n) whose cost position lies before int4_start(base) + x.
 __device__ __forceinline__ int pages_before(int x, int n)
 {
     return x <= 0 ? 0 : min(n, (x + kPageCost - 1) / kPageCost);
@@ -114,10 +120,10 @@ __device__ __forceinline__ int pages_before(int x, int n)
 // Cost-line extent from the first to the last INT4 page (inclusive), 0 for none.
 __device__ __forceinline__ int int4_span_len(int n) { return n > 0 ? kPageCost * (n - 1) + 1 : 0; }
 
-// Number of warp-span pieces of the INT4 pages of a unit starting at base.
-__device__ __forceinline__ int n_pieces(int base, int n, int span)
+// Number of warp-span pieces of n INT4 pages whose first sits at cost position first.
+__device__ __forceinline__ int n_pieces(int first, int n, int span)
 {
-    return n > 0 ? (base + kPageCost * (n - 1)) / span - base / span + 1 : 0;
+    return n > 0 ? (first + kPageCost * (n - 1)) / span - first / span + 1 : 0;
 }
 
 // Division of non-negative 32-bit values by one divisor d >= 2 with a multiply-high:
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
             const int n = n_of(L), cp = cp_of(L), plen = prot_span_len(cp);
             for (int h = 0; h < H; ++h) {
                 const int base = off + h * unit_cost(n, cp);
-                segs += sd.pieces(base, int4_span_len(n)) + sd.pieces(base + kPageCost * n, plen);
+                segs += sd.pieces(int4_start(base), int4_span_len(n)) + sd.pieces(prot_start(base, n), plen);
             }
             off += H * unit_cost(n, cp);
         }
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kPrepThreads) kv4_decode_prep_kernel(DecodeArg
             for (int h = 0; h < H; ++h) {
                 a.unit_seg[b * H + h] = soff;
                 const int base = cs + h * unit_cost(n, cp);
-                soff += sd.pieces(base, int4_span_len(n)) + sd.pieces(base + kPageCost * n, plen);
+                soff += sd.pieces(int4_start(base), int4_span_len(n)) + sd.pieces(prot_start(base, n), plen);
             }
         }
         if (tid == kPrepThreads - 1) {
@@ -365,9 +371,9 @@ __device__ __forceinline__ bool walk_enter(Walk& W)
 {
     const int cp = W.cp;
     const int base = W.csb + W.h * W.cbh;
-    const int a0 = pages_before(W.lo - base, W.n);
-    W.a1 = pages_before(W.hi - base, W.n);
-    const int pstart = base + kPageCost * W.n;
+    const int a0 = pages_before(W.lo - int4_start(base), W.n);
+    W.a1 = pages_before(W.hi - int4_start(base), W.n);
+    const int pstart = prot_start(base, W.n);
     W.g0 = groups_before(W.lo - pstart, cp);
     W.g1 = groups_before(W.hi - pstart, cp);
     if (a0 < W.a1) { W.k = a0; return true; }
@@ -1547,7 +1553,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
             }
             Walk C = walk_load(Csm);
             const int base = C.csb + h * C.cbh;
-            const int idx = unit_first_partial(a, b, h) + (wg - base / span);
+            const int idx = unit_first_partial(a, b, h) + (wg - int4_start(base) / span);
             if (tq < 2) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
@@ -1620,7 +1626,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 const Walk C = walk_load(Csm);
                 const int base = C.csb + h * C.cbh;
                 pidx = unit_first_partial(a, b, h) +
-                       n_pieces(base, C.n, span) + (wg - (base + kPageCost * C.n) / span);
+                       n_pieces(int4_start(base), C.n, span) + (wg - prot_start(base, C.n) / span);
             }
             float* po = a.part_o + ((int64_t)pidx * G) * kHeadDim;
             if (tq < 2) {

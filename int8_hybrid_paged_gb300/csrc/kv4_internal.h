@@ -44,13 +44,17 @@ constexpr int kMxScaleOff = 1024;
 constexpr int kDecodeThreads = 512;      // 16 warps per decode CTA, one CTA per SM
 constexpr int kStages = 5;               // page stages per warp
 // The decode plan's cost line, in quarter-page units (fitted to measured per-warp times
-// on the 4B- and 8B-shaped and long-tail layers): an INT4 page costs 4, a protected stage
-// item (half a side group, or half a page of a whole-cache format) 5, and every
-// (sequence, KV head) unit is charged kUnitOverhead more for the setup and flush of its
-// runs (no items sit there).
+// on the 8B-shaped and long-tail layers): an INT4 page costs 4, a protected stage item
+// (half a side group, or half a page of a whole-cache format) 5. A (sequence, KV head)
+// unit lays out as [kRunSetup][its INT4 pages][kProtSetup][its protected items]
+// [kUnitFlush]: the gaps hold no items and stand for the setup of the INT4 run and of the
+// protected run, and for the unit's flush, so that a span is charged for the runs it
+// starts.
 constexpr int kPageCost = 4;
 constexpr int kProtCost = 5;
-constexpr int kUnitOverhead = 36;
+constexpr int kRunSetup = 12;
+constexpr int kProtSetup = 16;
+constexpr int kUnitFlush = 0;
 
 // Device-resident decode plan, written by the prep kernel, read by split and merge.
 struct PlanHeader {
