@@ -9,22 +9,26 @@
 //        accumulation; disjoint regions merged by their log-normalizers)
 //
 // Three launches on the caller's stream:
-//   prep   block 0 plans the call: every (sequence b, KV head h) is a run of
-//          "stage items" — its INT4 pages (one 2176-byte block each) followed by
-//          its protected unit (the side-buffer groups, two page-sized blocks per 16
-//          rows) — and the runs are laid end to end in one cost line. Every warp of
-//          the split grid gets an equal span of that line. The other blocks rotate
-//          and quantize every q head once (INT8 query, its scale, sum and widening
-//          offsets).
-//   split  persistent; each warp walks its span alone: a producer (lane 0 issues,
-//          all lanes track) keeps a 6-deep ring of 1-D bulk copies (global ->
-//          shared, mbarrier-completed) running across run boundaries, and the
-//          consumer turns INT4 pages into integer QK / integer PV on the tensor
-//          cores and protected groups into INT8 QK / FP32 PV. Each run piece ends
-//          in one partial (output relative to its max, max, normalizer).
-//   merge  warp per q head: exact log-sum-exp merge of that head's partials.
-// No ticket, search or block-wide barrier sits on the data path, and the spans
-// are balanced to one run piece, whatever the length mix.
+//   prep   block 0 plans the call: every (sequence b, KV head h) is a unit of
+//          "stage items" — its INT4 pages (one 2176-byte block each) and its
+//          protected run (the side-buffer groups, two page-sized blocks per 16 rows),
+//          with positions for the setup of each run — and the units are laid end to
+//          end in one cost line, cut into equal spans, one per warp of the split grid;
+//          block 0 records where each unit's partials go. The other blocks rotate and
+//          quantize every q head once (INT8 query, its scale, sum and widening offsets).
+//   split  persistent, a programmatic dependent of prep; each CTA repeats the plan's
+//          arithmetic for its own warps (one block-wide scan over the batch) and
+//          issues its first copies before it waits for prep. Each warp walks its span
+//          alone: a producer (lane 0 issues, all lanes track) keeps a 5-deep ring of
+//          1-D bulk copies (global -> shared, mbarrier-completed) running across run
+//          boundaries, and the consumer turns INT4 pages into integer QK / integer PV
+//          on the tensor cores and protected groups into INT8 QK / BF16 PV with FP32
+//          accumulation. Each run piece ends in one partial (output relative to its
+//          max, max, normalizer).
+//   merge  a programmatic dependent of split; warp per q head: exact log-sum-exp
+//          merge of that head's partials.
+// No ticket or search sits on the data path, and the spans are balanced to one run
+// piece, whatever the length mix.
 #include <float.h>
 
 #include <mutex>
@@ -1659,16 +1663,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
 template <int G>
 __global__ void __launch_bounds__(128) kv4_decode_merge_kernel(DecodeArgs a)
 {
-    grid_dependency_wait();                 // the split kernel's partials are complete past here
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (gw >= a.batch * a.num_q_heads) return;
+    const bool live = gw < a.batch * a.num_q_heads;
     const int b = gw / a.num_q_heads, hq = gw - b * a.num_q_heads;
     const int h = hq / G, g = hq - h * G;
-    // a unit's partials are consecutive: its count is the next unit's first minus its own
+    // a unit's partials are consecutive: its count is the next unit's first minus its own.
+    // The plan kernel wrote these before the split kernel began, so they are read before
+    // the wait for the split kernel's partials.
     const int u = b * a.num_heads + h;
-    const int first = __ldg(&a.unit_seg[u]);
-    const int nit = __ldg(&a.unit_seg[u + 1]) - first;
+    const int first = live ? __ldg(&a.unit_seg[u]) : 0;
+    const int nit = live ? __ldg(&a.unit_seg[u + 1]) - first : 0;
+    grid_dependency_wait();                 // the split kernel's partials are complete past here
+    if (!live) return;
     auto item = [&](int k) { return first + k; };
     auto pout = [&](int it) {
         return __ldg(reinterpret_cast<const float4*>(&a.part_o[((int64_t)it * G + g) * kHeadDim + 4 * lane]));
