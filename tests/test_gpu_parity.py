@@ -204,6 +204,38 @@ def test_long_tail_layer_sampled():
         st.close()
 
 
+def test_large_batch_of_short_contexts():
+    """1300 sequences of 0..200 tokens: more sequences than threads in the plan kernel and
+    in the split kernel's own plan (several sequences per thread), 2600 units."""
+    rng = np.random.default_rng(31)
+    lens = [int(x) for x in rng.integers(1, 201, size=1300)]
+    lens[7] = 1
+    st = Setup(2, 4, 16, 128, lens, seed=31)
+    try:
+        q = inputs.queries(st.B, 8, seed=31).cuda()
+        bs = [0, 7, 511, 512, 513, 1023, 1024, 1299] + sorted(int(b) for b in np.argsort(lens)[-2:])
+        check_decode(st, q, bs)
+        zl = list(lens)
+        zl[3] = 0                                             # an empty context inside the batch
+        check_decode(st, q, [2, 3, 4], lens=zl)
+        st.cache.device_error()                               # slot 3 holds more than 0 positions
+    finally:
+        st.close()
+
+
+def test_one_very_long_context():
+    """One 120,000-token sequence among short ones: its units are cut into hundreds of
+    pieces, so the merge takes more than 32 partials per q head."""
+    lens = [120000, 5, 3000]
+    st = Setup(1, 4, 16, 128, lens, seed=32, kv_device="cuda", spare_pages=16)
+    try:
+        q = inputs.queries(st.B, 4, seed=32).cuda()
+        check_decode(st, q, [0, 1, 2])
+        assert st.cache.device_error() == 0
+    finally:
+        st.close()
+
+
 def test_append_stress_sampled():
     # (a) 512 sequences, one new token each after a short prefix
     lens = [33 + (i % 7) for i in range(512)]
