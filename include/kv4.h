@@ -125,12 +125,15 @@ typedef struct {
  * above with row r = t, the page's token slot t; there is no side pool.
  * KV4_FORMAT_NVFP4 pages: num_pages * H_kv blocks of KV4_PAGE_BLOCK_BYTES_NVFP4 = 2432 bytes,
  * block (p, h) at (p * H_kv + h) * 2432: a K half at 0 and a V half at 1216, each with
- *   [0, 1024)    E2M1 codes (sign in bit 3; dim d in the low nibble of its byte when d is
- *                the lower dim of the byte's pair), one byte per (token, dim pair):
- *                K: dims (2j, 2j+1) of token t, j = 8b + jj (block b, jj < 8), at
+ *   [0, 1024)    E2M1 codes (sign in bit 3), two per byte:
+ *                K: one byte per (token, dim pair): dims 2j (low nibble) and 2j+1 (high)
+ *                   of token t, j = 8b + jj (block b, jj < 8), at
  *                   16*(32*(b/4) + 4*(t%8) + jj%4) + 4*(b%4) + t/8 + 2*(jj/4)
- *                V: dims (d, d+8) of token t, d = 16m + g (g < 8), at
- *                   16*(32*(m/4) + 4*g + t%4) + 4*(m%4) + {0,2,1,3}[t/4]
+ *                V: one byte per (dim, token pair): dim d = 16m + r (r < 16) of tokens
+ *                   t (low nibble) and t+8 (high nibble), t%16 < 8, at
+ *                   16*(32*(m/4) + 4*(r%8) + t%4) + 4*(m%4) + 2*((t/4)%2) + r/8
+ *                   (an append writes a token's nibbles with atomic clear-and-set of
+ *                   their 32-bit word, which holds four tokens' nibbles)
  *   [1024, 1152) E4M3 block scales (block b = dims 16b .. 16b+15) of token t:
  *                K: byte 16*(t%8) + 2*b + t/8      (tokens t, t+8 of a block paired)
  *                V: byte 32*(t%4) + 4*b + {0,2,1,3}[t/4]  (tokens t, t+8, t+4, t+12)

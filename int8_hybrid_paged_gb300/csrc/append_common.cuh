@@ -318,6 +318,42 @@ __device__ __forceinline__ void warp_quant_nvfp4(const float (&x)[4], uint32_t (
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = scale > 0.0f ? e2m1_rn(__fmul_rn(x[i], inv)) : 0u;
 }
+// E2M1 codes of one token-head in a K or V half (NVFP4 and MXFP4). K: a byte holds
+// dims 2j, 2j + 1 of one token, in the QK fragment order.
+__device__ __forceinline__ void store_e2m1_k(uint8_t* half, int ts, const uint32_t (&c)[4], int lane)
+{
+    const int b = lane >> 2;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const int jj = 2 * (lane & 3) + e;
+        half[16 * (32 * (b >> 2) + 4 * (ts & 7) + (jj & 3)) + 4 * (b & 3) + (ts >> 3) + 2 * (jj >> 2)] =
+            (uint8_t)(c[2 * e] | (c[2 * e + 1] << 4));
+    }
+}
+// V codes: a byte holds one dim of tokens t (low nibble) and t + 8 (high nibble), the
+// pairs of a PV A fragment, so a reader widens it with one conversion per register; the
+// word of (dim group 16m + g, token t mod 4) holds dims g, g + 8 of tokens {t, t + 8} in
+// bytes 0, 1 and of tokens {t + 4, t + 12} in bytes 2, 3. A token owns one nibble of each
+// of two bytes of a word that three other tokens share: it clears and sets its nibbles
+// with atomics, whatever order the tokens of a page are written in.
+__device__ __forceinline__ void store_e2m1_v(uint8_t* half, int ts, const uint32_t (&c)[4], int lane)
+{
+    const int m = lane >> 2;
+    uint32_t hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) hi[i] = __shfl_xor_sync(kFull, c[i], 2);
+    const int sh = 16 * ((ts >> 2) & 1) + 4 * (ts >> 3);          // this token's nibble in byte 0 of its pair
+    const uint32_t mask = (0xfu << sh) | (0xfu << (sh + 8));
+    if ((lane & 2) == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int gq = 4 * (lane & 3) + i;
+            uint32_t* w = reinterpret_cast<uint32_t*>(half + 16 * (32 * (m >> 2) + 4 * gq + (ts & 3)) + 4 * (m & 3));
+            atomicAnd(w, ~mask);
+            atomicOr(w, (c[i] << sh) | (hi[i] << (sh + 8)));
+        }
+    }
+}
 // One token-head in an NVFP4 page block: the K half (codes in the QK fragment order) or
 // the V half (codes in the PV fragment order), its block scales and vector scale. The K
 // scales of tokens t, t + 8 sit side by side per block, the V scales of tokens t, t + 8,
@@ -326,31 +362,17 @@ __device__ __forceinline__ void warp_quant_nvfp4(const float (&x)[4], uint32_t (
 __device__ __forceinline__ void store_nvfp4_k(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t sb, float g,
                                               int lane)
 {
+    store_e2m1_k(half, ts, c, lane);
     const int b = lane >> 2;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {                                // dim pairs j = 2l + e
-        const int jj = 2 * (lane & 3) + e;                       // pair within the block
-        half[16 * (32 * (b >> 2) + 4 * (ts & 7) + (jj & 3)) + 4 * (b & 3) + (ts >> 3) + 2 * (jj >> 2)] =
-            (uint8_t)(c[2 * e] | (c[2 * e + 1] << 4));
-    }
     if ((lane & 3) == 0) half[kFp4ScaleOff + 16 * (ts & 7) + 2 * b + (ts >> 3)] = (uint8_t)sb;
     if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 8 * (ts & 7) + 4 * (ts >> 3)) = g;
 }
 __device__ __forceinline__ void store_nvfp4_v(uint8_t* half, int ts, const uint32_t (&c)[4], uint32_t sb, float g,
                                               int lane)
 {
+    store_e2m1_v(half, ts, c, lane);
     const int m = lane >> 2;
-    uint32_t hi[4];                                              // dims + 8, from lane l ^ 2
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hi[i] = __shfl_xor_sync(kFull, c[i], 2);
     const int q4 = ts >> 2, kb = ((q4 & 1) << 1) | (q4 >> 1);     // tokens t, t+8, t+4, t+12 -> bytes 0..3
-    if ((lane & 2) == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int gq = 4 * (lane & 3) + i;                   // dim 16m + gq, gq < 8
-            half[16 * (32 * (m >> 2) + 4 * gq + (ts & 3)) + 4 * (m & 3) + kb] = (uint8_t)(c[i] | (hi[i] << 4));
-        }
-    }
     if ((lane & 3) == 0) half[kFp4ScaleOff + 32 * (ts & 3) + 4 * m + kb] = (uint8_t)sb;
     if (lane == 0) *reinterpret_cast<float*>(half + kFp4GlobalOff + 8 * (ts & 7) + 4 * (ts >> 3)) = g;
 }
@@ -375,32 +397,6 @@ __device__ __forceinline__ void warp_quant_mxfp4(const float (&x)[4], uint32_t (
     const float inv = __uint_as_float((uint32_t)(127 - sx) << 23);
 #pragma unroll
     for (int i = 0; i < 4; ++i) c[i] = la > 0.0f ? e2m1_rn(__fmul_rn(x[i], inv)) : 0u;
-}
-// Codes of one token-head in a K or V half, in the NVFP4 byte order.
-__device__ __forceinline__ void store_e2m1_k(uint8_t* half, int ts, const uint32_t (&c)[4], int lane)
-{
-    const int b = lane >> 2;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-        const int jj = 2 * (lane & 3) + e;
-        half[16 * (32 * (b >> 2) + 4 * (ts & 7) + (jj & 3)) + 4 * (b & 3) + (ts >> 3) + 2 * (jj >> 2)] =
-            (uint8_t)(c[2 * e] | (c[2 * e + 1] << 4));
-    }
-}
-__device__ __forceinline__ void store_e2m1_v(uint8_t* half, int ts, const uint32_t (&c)[4], int lane)
-{
-    const int m = lane >> 2;
-    uint32_t hi[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hi[i] = __shfl_xor_sync(kFull, c[i], 2);
-    const int q4 = ts >> 2, kb = ((q4 & 1) << 1) | (q4 >> 1);
-    if ((lane & 2) == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int gq = 4 * (lane & 3) + i;
-            half[16 * (32 * (m >> 2) + 4 * gq + (ts & 3)) + 4 * (m & 3) + kb] = (uint8_t)(c[i] | (hi[i] << 4));
-        }
-    }
 }
 // One token-head in an MXFP4 page block: codes as NVFP4, E8M0 scales of tokens t, t + 8
 // side by side per block (K) or of tokens t, t + 8, t + 4, t + 12 per block (V).

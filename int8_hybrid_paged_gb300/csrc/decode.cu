@@ -1038,13 +1038,12 @@ __device__ __forceinline__ void fp4_group(const DecodeArgs& a, SplitSmem& sm, Pr
         const uint4 vs = mm < 4 ? vs0 : vs1;
         const uint32_t wd = (mm & 3) == 0 ? vc.x : (mm & 3) == 1 ? vc.y : (mm & 3) == 2 ? vc.z : vc.w;
         const uint32_t sw = (mm & 3) == 0 ? vs.x : (mm & 3) == 1 ? vs.y : (mm & 3) == 2 ? vs.z : vs.w;
-        uint32_t hv[4];                                  // (dim d, d + 8) of tokens t, t+8, t+4, t+12
-        e2m1x4_f16x2(wd, hv);
+        uint32_t hv[4];                                  // the A fragment: (dim d | d + 8) x tokens
+        e2m1x4_f16x2(wd, hv);                            // (t, t+8), (t+4, t+12)
         uint32_t s01, s23;                               // block scales of tokens (t, t+8), (t+4, t+12)
         e4m3x4_f16x2(sw, s01, s23);
         float c[4];
-        mma_f16(c, prmt(hv[0], hv[1], 0x5410u), prmt(hv[0], hv[1], 0x7632u), prmt(hv[2], hv[3], 0x5410u),
-                prmt(hv[2], hv[3], 0x7632u), hmul2_u32(pw.x, s01), hmul2_u32(pw.y, s23), 0.f, 0.f, 0.f, 0.f);
+        mma_f16(c, hv[0], hv[1], hv[2], hv[3], hmul2_u32(pw.x, s01), hmul2_u32(pw.y, s23), 0.f, 0.f, 0.f, 0.f);
         // scalar fmas here: the packed form measured slower in this routine
         fc(st.o[mm][0], 0) = fmaf(bA, c[0], fc(st.o[mm][0], 0));
         fc(st.o[mm][0], 1) = fmaf(bB, c[1], fc(st.o[mm][0], 1));
@@ -1149,10 +1148,9 @@ __device__ __forceinline__ void mx_group(const DecodeArgs& a, SplitSmem& sm, Pro
             const uint4 vc = mm < 4 ? vc0 : vc1;
             const uint32_t wd = (mm & 3) == 0 ? vc.x : (mm & 3) == 1 ? vc.y : (mm & 3) == 2 ? vc.z : vc.w;
             uint32_t hv[4];
-            e2m1x4_f16x2(wd, hv);
+            e2m1x4_f16x2(wd, hv);                        // the A fragment, as in an NVFP4 page
             float c[4];
-            mma_f16(c, prmt(hv[0], hv[1], 0x5410u), prmt(hv[0], hv[1], 0x7632u), prmt(hv[2], hv[3], 0x5410u),
-                    prmt(hv[2], hv[3], 0x7632u), b0, b1, 0.f, 0.f, 0.f, 0.f);
+            mma_f16(c, hv[0], hv[1], hv[2], hv[3], b0, b1, 0.f, 0.f, 0.f, 0.f);
             // scalar fmas here: the packed form measured slower in this routine
             fc(st.o[mm][0], 0) = fmaf(bA, c[0], fc(st.o[mm][0], 0));
             fc(st.o[mm][0], 1) = fmaf(bB, c[1], fc(st.o[mm][0], 1));

@@ -93,13 +93,14 @@ def unpack_nvfp4_pages(pages, H, page_ids, slots_in_page, h):
     koff = 16 * (32 * (b // 4) + 4 * (t % 8) + jj % 4) + 4 * (b % 4) + t // 8 + 2 * (jj // 4)
     kbyte = pages[base[:, None] + koff]
     kc = np.where(d % 2 == 0, kbyte & 15, kbyte >> 4).astype(np.uint8)
-    # V: dims (dd, dd+8), dd = 16m + g, g < 8
+    # V: a byte holds dim 16m + r of tokens t (low nibble) and t + 8 (high nibble);
+    # the word of (16m + r mod 8, t mod 4) has dims r < 8, r >= 8 of tokens {t, t+8} in
+    # bytes 0, 1 and of tokens {t+4, t+12} in bytes 2, 3
     m, r = d // 16, d % 16
     g = r % 8
-    kb = np.array([0, 2, 1, 3])[t // 4]
-    voff = 16 * (32 * (m // 4) + 4 * g + t % 4) + 4 * (m % 4) + kb
+    voff = 16 * (32 * (m // 4) + 4 * g + t % 4) + 4 * (m % 4) + 2 * ((t // 4) % 2) + (r >= 8)
     vbyte = pages[base[:, None] + 1216 + voff]
-    vc = np.where(r < 8, vbyte & 15, vbyte >> 4).astype(np.uint8)
+    vc = np.where(t < 8, vbyte & 15, vbyte >> 4).astype(np.uint8)
     ts = np.asarray(slots_in_page, np.int64)
     bb = np.arange(8)[None, :]
     tt = ts[:, None]
@@ -126,9 +127,9 @@ def unpack_mxfp4_pages(pages, H, page_ids, slots_in_page, h):
     m, r = d // 16, d % 16
     g = r % 8
     kb = np.array([0, 2, 1, 3])[t // 4]
-    voff = 16 * (32 * (m // 4) + 4 * g + t % 4) + 4 * (m % 4) + kb
+    voff = 16 * (32 * (m // 4) + 4 * g + t % 4) + 4 * (m % 4) + 2 * ((t // 4) % 2) + (r >= 8)
     vbyte = pages[base[:, None] + 1088 + voff]
-    vc = np.where(r < 8, vbyte & 15, vbyte >> 4).astype(np.uint8)
+    vc = np.where(t < 8, vbyte & 15, vbyte >> 4).astype(np.uint8)
     bb = np.arange(4)[None, :]
     ke = pages[base[:, None] + 1024 + 8 * (t % 8) + 2 * bb + t // 8]
     ve = pages[base[:, None] + 1088 + 1024 + 16 * (t % 4) + 4 * bb + kb]
