@@ -26,21 +26,18 @@ namespace kv4 {
 namespace {
 
 constexpr int kBM = 128, kBK = 64;                 // kBK * 2 bytes = one 128-byte swizzle row
-// TMA ring depth: 4 stages of 48 KB (256-wide tiles, or two row tiles of a 128-wide
-// one), 6 of 32 KB otherwise (a deeper ring keeps more bytes in flight per SM when
-// few tiles share the GPU)
-template <int BN, int MT>
-constexpr int gemm_stages() { return (BN == 256 || MT == 2) ? 4 : 6; }
+// TMA ring depth: 4 stages of 48 KB for 256-wide tiles, 6 of 32 KB for 128-wide ones
+// (a deeper ring keeps more bytes in flight per SM when few tiles share the GPU)
+template <int BN>
+constexpr int gemm_stages() { return BN == 256 ? 4 : 6; }
 constexpr int kTileBytes = kBM * kBK * 2;           // 16 KB: the X tile
 constexpr int kGemmThreads = 128;
 
-// BN = 128 or 256 output columns per tile (the W tile and the TMEM accumulator width);
-// MT = 1 or 2 row tiles of 128 tokens, each with its own accumulator (MT = 2 only with
-// BN = 128: the two accumulators fill 256 TMEM columns)
-template <int BN, int MT = 1>
+// BN = 128 or 256 output columns per tile (the W tile and the TMEM accumulator width)
+template <int BN>
 struct __align__(1024) GemmSmem {
-    static constexpr int kStages = gemm_stages<BN, MT>();
-    uint8_t a[kStages][MT][kTileBytes];             // 1024-byte aligned: swizzle atoms
+    static constexpr int kStages = gemm_stages<BN>();
+    uint8_t a[kStages][kTileBytes];                 // 1024-byte aligned: swizzle atoms
     uint8_t b[kStages][BN * kBK * 2];
     uint64_t full[kStages], empty[kStages], accum;
     uint32_t tmem_base;
@@ -132,18 +129,17 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity)
 }
 
 // The tile's main loop over k blocks [kb0, kb1): barrier and TMEM set-up, thread 0
-// streams the X and W tiles of every k block, thread 32 issues the MMAs (row tile t into
-// TMEM columns [t BN, (t + 1) BN)), threads 64 and up run pre(tid - 64) (work that does
-// not need the tile: no warp-collective operations), and every thread then waits for the
-// accumulator. True when the accumulator holds the finished tile.
-template <int BN, int MT, class PreWait>
-__device__ __forceinline__ bool gemm_tile(GemmSmem<BN, MT>& sm, const CUtensorMap& map_x,
+// streams the X and W tiles of every k block, thread 32 issues the MMAs, threads 64 and
+// up run pre(tid - 64) (work that does not need the tile: no warp-collective
+// operations), and every thread then waits for the accumulator. True when the
+// accumulator holds the finished tile.
+template <int BN, class PreWait>
+__device__ __forceinline__ bool gemm_tile(GemmSmem<BN>& sm, const CUtensorMap& map_x,
                                           const CUtensorMap& map_w, int m0, int n0, int kb0, int kb1,
                                           int32_t* err, PreWait&& pre)
 {
-    static_assert(MT == 1 || BN == 128, "two row tiles only with 128-wide tiles");
     constexpr int kWBytes = BN * kBK * 2;
-    constexpr int kS = GemmSmem<BN, MT>::kStages;
+    constexpr int kS = GemmSmem<BN>::kStages;
     const int tid = threadIdx.x, warp = tid >> 5;
     if (tid == 0) {
         for (int s = 0; s < kS; ++s) {
@@ -157,9 +153,9 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN, MT>& sm, const CUtensorMa
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
     }
     if (warp == 0) {
-        // the accumulators: MT x BN columns x 128 lanes of tensor memory
+        // the accumulator: BN columns x 128 lanes of tensor memory
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                     ::"r"(smem_u32(&sm.tmem_base)), "r"((uint32_t)(BN * MT))
+                     ::"r"(smem_u32(&sm.tmem_base)), "r"((uint32_t)BN)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -178,16 +174,14 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN, MT>& sm, const CUtensorMa
                 break;
             }
             const uint32_t fb = smem_u32(&sm.full[s]);
-            arrive_expect_tx(fb, MT * kTileBytes + kWBytes);
-#pragma unroll
-            for (int t = 0; t < MT; ++t)
-                tma_load_2d(smem_u32(sm.a[s][t]), &map_x, kb * kBK, m0 + kBM * t, fb);
+            arrive_expect_tx(fb, kTileBytes + kWBytes);
+            tma_load_2d(smem_u32(sm.a[s]), &map_x, kb * kBK, m0, fb);
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)              // boxes of 128 W rows
                 tma_load_2d(smem_u32(sm.b[s]) + h * kTileBytes, &map_w, kb * kBK, n0 + 128 * h, fb);
         }
     } else if (tid == 32) {
-        // ---- MMA issuer: four K = 16 steps per stage and row tile, accumulate after the first
+        // ---- MMA issuer: four K = 16 steps per stage, accumulate after the first
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
             const int i = kb - kb0, s = i % kS, r = i / kS;
@@ -198,15 +192,11 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN, MT>& sm, const CUtensorMa
                 break;
             }
             tmem_fence_after();
+            const uint64_t ad = smem_desc_sw128(smem_u32(sm.a[s]));
             const uint64_t bd = smem_desc_sw128(smem_u32(sm.b[s]));
 #pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                const uint64_t ad = smem_desc_sw128(smem_u32(sm.a[s][t]));
-#pragma unroll
-                for (int k = 0; k < kBK / 16; ++k)          // +32 bytes along K = +2 in the address field
-                    umma_bf16(tmem + (uint32_t)(BN * t), ad + 2 * k, bd + 2 * k, idesc_bf16<BN>(),
-                              (i | k) != 0);
-            }
+            for (int k = 0; k < kBK / 16; ++k)              // +32 bytes along K = +2 in the address field
+                umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc_bf16<BN>(), (i | k) != 0);
             umma_commit(smem_u32(&sm.empty[s]));          // stage free once these MMAs have read it
         }
         if (ok) umma_commit(smem_u32(&sm.accum));
@@ -223,15 +213,15 @@ __device__ __forceinline__ bool gemm_tile(GemmSmem<BN, MT>& sm, const CUtensorMa
 }
 
 // Release the tile's tensor memory (after every warp's last tcgen05.ld).
-template <int BN, int MT>
-__device__ __forceinline__ void gemm_release(GemmSmem<BN, MT>& sm)
+template <int BN>
+__device__ __forceinline__ void gemm_release(GemmSmem<BN>& sm)
 {
     tmem_fence_before();
     __syncthreads();
     if ((threadIdx.x >> 5) == 0) {
         tmem_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(sm.tmem_base),
-                     "r"((uint32_t)(BN * MT))
+                     "r"((uint32_t)BN)
                      : "memory");
     }
 }
@@ -271,12 +261,12 @@ kv4_linear_bf16_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_c
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
-    const bool ok = gemm_tile<BN, 1>(sm, map_x, map_w, m0, n0, 0, K / kBK, err, [](int) {});
+    const bool ok = gemm_tile<BN>(sm, map_x, map_w, m0, n0, 0, K / kBK, err, [](int) {});
     const int row = m0 + 32 * warp + lane;
     if (ok)                                  // CTA-uniform: every lane loads, rows < M store
         store_row_bf16(sm.tmem_base + ((uint32_t)(32 * warp) << 16), BN / 32, y + (int64_t)row * N + n0,
                        row < M);
-    gemm_release<BN, 1>(sm);
+    gemm_release<BN>(sm);
 }
 
 // Fused projection + append. Output columns: [Q heads | K0 V0 | K1 V1 | ...], 128 each;
@@ -410,7 +400,7 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     const int T = a.total_tokens;
     TokenLocS* loc = reinterpret_cast<TokenLocS*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(GemmSmem<256>));
     const bool kv_tile = n0 >= qa.q_cols;
-    const bool ok = gemm_tile<256, 1>(sm, map_x, map_w, m0, n0, 0, K / kBK, a.err, [&](int t) {
+    const bool ok = gemm_tile<256>(sm, map_x, map_w, m0, n0, 0, K / kBK, a.err, [&](int t) {
         if (kv_tile) locate_tile_tokens(a, loc, m0, t);
     });
     const int quarter = warp & 3, colq = warp >> 2;                 // TMEM lane quarter, column quarter
@@ -419,7 +409,7 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     if (n0 < qa.q_cols) {
         // ---- two Q heads: the projection itself
         if (ok) store_row_bf16(trow, 2, qa.q_out + (int64_t)row * qa.q_cols + n0 + 64 * colq, row < T);
-        gemm_release<256, 1>(sm);
+        gemm_release<256>(sm);
         return;
     }
     // ---- K and V of KV head h for tokens m0 .. m0+127: rounded to BF16 as the projection
@@ -430,7 +420,7 @@ kv4_qkv_append_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_co
     fence_proxy_async();                    // the MMAs' reads of the stages precede these writes
     if (ok)                                  // CTA-uniform; rows past T are staged but never read
         store_row_bf16(trow, 2, (colq >= 2 ? vt : kt) + 128 * r + 64 * (colq & 1), true);
-    gemm_release<256, 1>(sm);                                            // ends with a CTA barrier
+    gemm_release<256>(sm);                                            // ends with a CTA barrier
     if (!ok) return;
     append_kv_rows<FMT>(a, loc, m0, 0, kBM, h, warp, lane,
                         [&](int rr, float (&kx)[4], float (&vx)[4]) {
@@ -557,7 +547,7 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
     const int T = a.total_tokens;
     TokenLocS* loc = reinterpret_cast<TokenLocS*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(GemmSmem<128>));
     const bool kv_tile = n0 >= qa.q_cols;
-    const bool ok = gemm_tile<128, 1>(sm, map_x, map_w, m0, n0, 0, K / kBK, a.err, [&](int t) {
+    const bool ok = gemm_tile<128>(sm, map_x, map_w, m0, n0, 0, K / kBK, a.err, [&](int t) {
         if (kv_tile) locate_tile_tokens(a, loc, m0, t);
     });
     const int quarter = warp & 3, colq = warp >> 2;                 // TMEM lane quarter, column quarter
@@ -565,7 +555,7 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
     const int r = 32 * quarter + lane, row = m0 + r;
     if (n0 < qa.q_cols) {
         if (ok) store_row_bf16(trow, 1, qa.q_out + (int64_t)row * qa.q_cols + n0 + 32 * colq, row < T);
-        gemm_release<128, 1>(sm);
+        gemm_release<128>(sm);
         return;
     }
     const int kvj = (n0 - qa.q_cols) / 128, h = kvj >> 1;
@@ -573,7 +563,7 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
     uint16_t* xt = reinterpret_cast<uint16_t*>(sm.b[0]);              // [128][128] bf16: K or V
     fence_proxy_async();
     if (ok) store_row_bf16(trow, 1, xt + 128 * r + 32 * colq, true);
-    gemm_release<128, 1>(sm);
+    gemm_release<128>(sm);
     if (!ok) return;
     append_half_rows<FMT>(a, loc, m0, 0, kBM, h, is_v, warp, lane, [&](int rr, float (&x)[4]) {
         const uint2 w2 = *reinterpret_cast<const uint2*>(xt + 128 * rr + 4 * lane);
@@ -582,8 +572,7 @@ kv4_qkv_append_narrow_kernel(const __grid_constant__ CUtensorMap map_x, const __
 }
 
 // ---- split-K for few tokens (a small decode step): the S CTAs of a thread-block cluster
-// share one BN-column tile of MT row tiles (each row tile with its own TMEM accumulator;
-// the host plans MT = 1), CTA c taking k blocks [c nk / S, (c + 1) nk / S). Each CTA parks its partial sums in its own
+// share one 128 x 128 tile, CTA c taking k blocks [c nk / S, (c + 1) nk / S). Each CTA parks its partial sums in its own
 // shared memory; after a cluster barrier, CTA c adds the S partials (in rank order, the
 // same for every caller) of its share of the rows through distributed shared memory and
 // runs the tile's epilogue on them: BF16 rows for the plain projection and for Q, the
@@ -596,10 +585,9 @@ struct SplitKArgs {
     int32_t* err;                 // the plain projection's error word
 };
 
-template <int BN, int MT>
 struct SplitKSmem {
-    GemmSmem<BN, MT> g;           // its stages hold the parked partials after the main loop
-    TokenLocS loc[MT * kBM];
+    GemmSmem<128> g;              // its stages hold the parked partials after the main loop
+    TokenLocS loc[kBM];
     int32_t ok;
 };
 
@@ -648,54 +636,47 @@ __device__ __forceinline__ void round_bf16x4(float (&x)[4])
     for (int i = 0; i < 4; ++i) x[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
 }
 
-// Grid: (column tiles x S, row groups of MT x 128 tokens), clusters of S along x.
-// FMT: -1 the plain projection; 0..3 the fused call in the cache's format (as above),
-// whose 128-wide tiles are one Q head, or the K or the V head of one KV head.
-template <int BN, int MT, int FMT>
+// Grid: column tiles x S CTAs, clusters of S. FMT: -1 the plain projection; 0..3 the
+// fused call in the cache's format (as above), whose tiles are one Q head, or the K or
+// the V head of one KV head.
+template <int FMT>
 __global__ void __launch_bounds__(kQkvThreads, 1)
 kv4_gemm_splitk_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                        const SplitKArgs ka)
 {
-    // parked rows: BN + 4 floats, so that the 16-byte chunks written by 8 consecutive rows
+    // parked rows: 132 floats, so that the 16-byte chunks written by 8 consecutive rows
     // fall in distinct bank groups
-    constexpr int kPS = BN + 4;
+    constexpr int BN = 128, kPS = BN + 4;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    SplitKSmem<BN, MT>& sm = *reinterpret_cast<SplitKSmem<BN, MT>*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    static_assert(MT * kBM * kPS * 4 <= sizeof(sm.g.a) + sizeof(sm.g.b), "partials exceed the stages");
+    SplitKSmem& sm = *reinterpret_cast<SplitKSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    static_assert(kBM * kPS * 4 <= sizeof(sm.g.a) + sizeof(sm.g.b), "partials exceed the stages");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = (int)cluster_size(), c = (int)cluster_rank();
-    const int n0 = (int)(blockIdx.x / S) * BN, m0 = (int)blockIdx.y * (MT * kBM);
+    const int n0 = (int)(blockIdx.x / S) * BN, m0 = 0;
     const int kb0 = c * ka.nk / S, kb1 = (c + 1) * ka.nk / S;
-    constexpr int R = MT * kBM;
+    constexpr int R = kBM;
     const int share = ((R + S - 1) / S + 15) & ~15;                  // rows per CTA, whole 16-row groups
     const int r0 = min(R, c * share), r1 = min(R, r0 + share);
     const AppendArgs& a = ka.qa.ap;
     const bool kv_tile = FMT >= 0 && n0 >= ka.qa.q_cols;
     const int M = FMT >= 0 ? a.total_tokens : ka.M;
-    const bool ok = gemm_tile<BN, MT>(sm.g, map_x, map_w, m0, n0, kb0, kb1, FMT >= 0 ? a.err : ka.err,
+    const bool ok = gemm_tile<BN>(sm.g, map_x, map_w, m0, n0, kb0, kb1, FMT >= 0 ? a.err : ka.err,
                                       [&](int t) {
                                           if (kv_tile) locate_tile_tokens(a, sm.loc, m0, t, r0, r1);
                                       });
     // park this CTA's partial sums: TMEM -> shared memory rows; warp w reads TMEM lane
     // quarter w % 4, column quarter w / 4
-    float* P = reinterpret_cast<float*>(&sm.g.a[0][0][0]);
+    float* P = reinterpret_cast<float*>(&sm.g.a[0][0]);
     fence_proxy_async();                    // the stages were last written by TMA, read by the MMAs
     if (ok) {                               // CTA-uniform
-        const int quarter = warp & 3, colq = warp >> 2;
+        const int quarter = warp & 3, col = 32 * (warp >> 2);
+        float v[32];
+        tmem_ld32(sm.g.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col, v);
+        float4* d = reinterpret_cast<float4*>(P + (32 * quarter + lane) * kPS + col);
 #pragma unroll
-        for (int t = 0; t < MT; ++t)
-#pragma unroll
-            for (int j = 0; j < BN / 128; ++j) {
-                const int col = colq * (BN / 4) + 32 * j;
-                float v[32];
-                tmem_ld32(sm.g.tmem_base + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(BN * t + col), v);
-                float4* d = reinterpret_cast<float4*>(P + (kBM * t + 32 * quarter + lane) * kPS + col);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            }
+        for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
-    gemm_release<BN, MT>(sm.g);             // CTA barrier, TMEM freed
+    gemm_release<BN>(sm.g);                 // CTA barrier, TMEM freed
     if (threadIdx.x == 0) sm.ok = ok ? 1 : 0;
     cluster_sync_all();
     const uint32_t p_loc = smem_u32(P);
@@ -819,14 +800,14 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int K)
 
 }  // namespace
 
-template <int BN, int MT, int FMT>
+template <int FMT>
 static cudaError_t splitk_attr()
 {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, []() {
-        attr = cudaFuncSetAttribute(kv4_gemm_splitk_kernel<BN, MT, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)(sizeof(SplitKSmem<BN, MT>) + 1024));
+        attr = cudaFuncSetAttribute(kv4_gemm_splitk_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(sizeof(SplitKSmem) + 1024));
     });
     return attr;
 }
@@ -843,11 +824,11 @@ static int max_clusters(int S)
     std::lock_guard<std::mutex> g(mu);
     if (cache[dev][S] == 0) {
         int n = 0;
-        if (splitk_attr<128, 1, -1>() == cudaSuccess) {
+        if (splitk_attr<-1>() == cudaSuccess) {
             cudaLaunchConfig_t cfg{};
             cfg.gridDim = dim3((unsigned)S);
             cfg.blockDim = dim3(kQkvThreads);
-            cfg.dynamicSmemBytes = sizeof(SplitKSmem<128, 1>) + 1024;
+            cfg.dynamicSmemBytes = sizeof(SplitKSmem) + 1024;
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;
             at[0].val.clusterDim.x = (unsigned)S;
@@ -855,7 +836,7 @@ static int max_clusters(int S)
             at[0].val.clusterDim.z = 1;
             cfg.attrs = at;
             cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&n, kv4_gemm_splitk_kernel<128, 1, -1>, &cfg) != cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&n, kv4_gemm_splitk_kernel<-1>, &cfg) != cudaSuccess) {
                 cudaGetLastError();
                 n = 0;
             }
@@ -873,35 +854,31 @@ static int max_clusters(int S)
 // split. S = 1: no split. The plain and the fused projection take the same plan, so their
 // sums agree bit for bit.
 struct SplitKPlan {
-    int bn, mt, groups, S;        // tile width, row tiles per CTA, clusters, CTAs per cluster
+    int groups, S;                // 128-wide column tiles (one cluster each), CTAs per cluster
 };
 static SplitKPlan splitk_plan(int M, int N, int K, int sms)
 {
-    SplitKPlan p{0, 0, 0, 1};
+    SplitKPlan p{N / 128, 1};
     if (M > kBM) return p;
     const int nk = K / kBK;
-    p.bn = 128;
-    p.mt = 1;
-    p.groups = N / 128;
     for (int S = std::min(8, nk); S >= 2; --S)
         if ((int64_t)p.groups * S <= sms && p.groups <= max_clusters(S)) {
             p.S = S;
             return p;
         }
-    p.S = 1;
     return p;
 }
 
-template <int BN, int MT, int FMT>
+template <int FMT>
 static cudaError_t launch_splitk(const CUtensorMap& mx, const CUtensorMap& mw, const SplitKArgs& ka,
                                  const SplitKPlan& pl, cudaStream_t stream)
 {
-    const cudaError_t attr = splitk_attr<BN, MT, FMT>();
+    const cudaError_t attr = splitk_attr<FMT>();
     if (attr != cudaSuccess) return attr;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(ka.N / BN * pl.S), (unsigned)(pl.groups / (ka.N / BN)));
+    cfg.gridDim = dim3((unsigned)(pl.groups * pl.S));
     cfg.blockDim = dim3(kQkvThreads);
-    cfg.dynamicSmemBytes = sizeof(SplitKSmem<BN, MT>) + 1024;
+    cfg.dynamicSmemBytes = sizeof(SplitKSmem) + 1024;
     cfg.stream = stream;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -910,14 +887,7 @@ static cudaError_t launch_splitk(const CUtensorMap& mx, const CUtensorMap& mw, c
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kv4_gemm_splitk_kernel<BN, MT, FMT>, mx, mw, ka);
-}
-
-template <int FMT>
-static cudaError_t launch_splitk_fmt(const CUtensorMap& mx, const CUtensorMap& mw, const SplitKArgs& ka,
-                                     const SplitKPlan& pl, cudaStream_t stream)
-{
-    return launch_splitk<128, 1, FMT>(mx, mw, ka, pl, stream);
+    return cudaLaunchKernelEx(&cfg, kv4_gemm_splitk_kernel<FMT>, mx, mw, ka);
 }
 
 template <int BN>
@@ -973,10 +943,10 @@ cudaError_t launch_qkv_append(const AppendArgs& ap, const void* x, const void* w
         ka.M = T;
         ka.N = N;
         ka.nk = d_model / kBK;
-        if (ap.mx) return launch_splitk_fmt<3>(mx, mw, ka, pl, stream);
-        if (ap.fp4) return launch_splitk_fmt<2>(mx, mw, ka, pl, stream);
-        if (ap.kv8) return launch_splitk_fmt<1>(mx, mw, ka, pl, stream);
-        return launch_splitk_fmt<0>(mx, mw, ka, pl, stream);
+        if (ap.mx) return launch_splitk<3>(mx, mw, ka, pl, stream);
+        if (ap.fp4) return launch_splitk<2>(mx, mw, ka, pl, stream);
+        if (ap.kv8) return launch_splitk<1>(mx, mw, ka, pl, stream);
+        return launch_splitk<0>(mx, mw, ka, pl, stream);
     }
     const int mt = (T + kBM - 1) / kBM;
     if ((int64_t)mt * (N / 256) >= sms) {
@@ -1012,7 +982,7 @@ cudaError_t launch_linear_bf16(const void* x, const void* w, void* y, int M, int
         ka.N = N;
         ka.nk = K / kBK;
         ka.err = err;
-        return launch_splitk_fmt<-1>(mx, mw, ka, pl, stream);
+        return launch_splitk<-1>(mx, mw, ka, pl, stream);
     }
     // 256-wide tiles halve the operand bytes per multiply-add; when they would leave SMs
     // idle (few row tiles), 128-wide tiles double the CTAs
