@@ -22,7 +22,6 @@ HEADERS = ["kv4_internal.h", "device_common.cuh", "append_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]
-NO_CONTRACT = {}
 
 
 def _nvcc() -> str:
@@ -51,7 +50,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     def compile_one(src):
         obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
         lang = ["-x", "cu"] if src.endswith(".cu") else ["-x", "c++"]
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *NO_CONTRACT.get(src, []), *extra, "-I",
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-I",
                os.path.join(ROOT, "include"), *lang, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
