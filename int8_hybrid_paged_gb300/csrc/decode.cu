@@ -442,7 +442,7 @@ __device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cas
 // a lane reads words t' and t' + 4 with one 8-byte load
 __device__ __forceinline__ int wfrag_pos(int w) { return 2 * (w & 3) + (w >> 2); }
 
-template <int G, bool DEBUG, bool EDGE>
+template <int G, bool DEBUG>
 __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, Int4State& st,
                                           const uint4* __restrict__ qf, float cq0, float cq1,
                                           float sqh, float qsh, const uint8_t* pg0,
@@ -491,6 +491,7 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
     }
 
     // ---- scores of head hs, tokens gq and gq + 8 of each page
+    const int hi_eff = two ? r4_hi : min(r4_hi, (lp0 + 1) * kPage);
     float2 sig[2], vdl[2], vmn[2];
     bool v0[2], v1[2];
     float Mp[2];
@@ -511,16 +512,12 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
         const float2 u = __ffma2_rn(kd, dot, __fmul2_rn(kmin, make_float2(qsh, qsh)));
         const float2 sg =
             __fmul2_rn(__fmul2_rn(u, make_float2(sqh, sqh)), make_float2(a.log2_scale, a.log2_scale));
+        // INT4 pages start at s (a multiple of 16): a position is masked only past the
+        // region's end or, for a lone page, past that page
         const int pos0 = (lp0 + p) * kPage + gq;
-        if (EDGE) {
-            const bool live = p == 0 || two;
-            v0[p] = live && pos0 >= a.sink && pos0 < r4_hi;
-            v1[p] = live && pos0 + 8 >= a.sink && pos0 + 8 < r4_hi;
-            sig[p] = make_float2(v0[p] ? sg.x : -INFINITY, v1[p] ? sg.y : -INFINITY);
-        } else {
-            v0[p] = v1[p] = true;
-            sig[p] = sg;
-        }
+        v0[p] = pos0 < hi_eff;
+        v1[p] = pos0 + 8 < hi_eff;
+        sig[p] = make_float2(v0[p] ? sg.x : -INFINITY, v1[p] ? sg.y : -INFINITY);
         if (DEBUG && a.dbg_qk && hs < G) {
             const int64_t row = ((int64_t)b * a.num_q_heads + h * G + hs) * a.dbg_stride;
             if (v0[p] && pos0 < a.dbg_stride) a.dbg_qk[row + pos0] = (int)dot.x;
@@ -532,19 +529,11 @@ __device__ __forceinline__ void int4_pair(const DecodeArgs& a, SplitSmem& sm, In
         Mp[p] = m;
     }
 
-    // ---- running max of head hs and rescale factors
+    // ---- running max of head hs and rescale factors. The first page's first position
+    // lies inside the region, so Mn is finite; st.M or a masked page's -inf gives 0
     const float Mn = fmaxf(st.M, fmaxf(Mp[0], Mp[1]));
-    float alpha, beta[2];
-    if (EDGE) {
-        const bool none = (Mn == -INFINITY);
-        alpha = none ? 1.f : exp2_fast(st.M - Mn);
-        beta[0] = none ? 0.f : exp2_fast(Mp[0] - Mn);
-        beta[1] = none ? 0.f : exp2_fast(Mp[1] - Mn);
-    } else {
-        alpha = exp2_fast(st.M - Mn);              // st.M = -inf gives 0
-        beta[0] = exp2_fast(Mp[0] - Mn);
-        beta[1] = exp2_fast(Mp[1] - Mn);
-    }
+    const float alpha = exp2_fast(st.M - Mn);
+    const float beta[2] = {exp2_fast(Mp[0] - Mn), exp2_fast(Mp[1] - Mn)};
     st.M = Mn;
 
     // ---- page-local weights, u8 with one power-of-two scale per (page, head)
@@ -1516,13 +1505,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) kv4_decode_split_kernel(Dec
                 const int lp0 = p_first + j;
                 const uint8_t* pg0 = sm.stage[warp][s0];
                 const uint8_t* pg1 = sm.stage[warp][s1];
-                // interior pairs: both pages whole and inside [s, L - w)
-                if (two && lp0 * kPage >= s && (lp0 + 2) * kPage <= r4_hi)
-                    int4_pair<G, DEBUG, false>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, true,
-                                               lp0, r4_hi, b, h, warp, lane);
-                else
-                    int4_pair<G, DEBUG, true>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, two,
-                                              lp0, r4_hi, b, h, warp, lane);
+                int4_pair<G, DEBUG>(a, sm, st, qf, cq0, cq1, sqh, qsh, pg0, pg1, two, lp0, r4_hi, b, h,
+                                    warp, lane);
                 produce();
             }
             // ---- partial of this piece: normalizer, offset terms and weight sums over the
